@@ -1,0 +1,466 @@
+"""Benchmark of the paged-KV decode step on one GB300 (or N independent replicas).
+
+A step is one Qwen3-0.6B-shaped decode step at batch 16: for each of 28
+layers, append the new token's K/V rows (pkv_append) and run decode
+attention over the paged cache (pkv_decode_attn). Request lengths are
+U{300..3000} (short clips plus prompt), pages randomly placed, every layer has
+its own KV pool (about 3 GB in total, far larger than the 129 MB L2, so no L2
+flush is needed between steps). The 56 launches of a step are captured once in
+a CUDA graph and replayed.
+
+Printed: one JSON line (rank 0). `value` is decode steps/s over all ranks.
+`roofline` is for the decode kernel: algorithmic bytes per launch (every
+cached K/V row of the layer once, plus q, out, block table and lengths) over
+its mean duration, measured with CUDA events on the launch stream during a
+separate timed pass of the same launches. `e2e` runs the same step through the
+Python API with the step's inputs copied from pinned host memory and the
+attention output copied back, synchronising every step. `cpu_baseline` times
+the fp64 CPU oracle on a bounded sample of the same workload.
+
+`--impl reference` times the oracle alone (on the host cores) on samples of
+the same workload and prints the same line with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn KV GB/s & % HBM peak; decode steps/s at bs16 (1×GB300)"
+UNIT = "steps/s"
+WORKLOAD = "qwen3-0.6b decode step: 28 layers x bs16, 16q/8kv heads, d128, page 16, seq U{300..3000}"
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops", 1954.7)), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+# ------------------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi SM clock / throttle-reason samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self._t:
+            self._t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() in ("active", "1"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------ workload
+class DecodeStep:
+    """Device-resident 28-layer decode step (all layers share one block table)."""
+
+    def __init__(self, device, seq_lens, layers: int, seed: int):
+        import torch
+
+        import paged_kv_decode_gb300 as pkv
+        from paged_kv_decode_gb300 import workloads as W
+
+        self.torch, self.pkv = torch, pkv
+        case = W.decode_case(seed, seq_lens, layers=layers, device=device, pending_append=True, poison=True)
+        self.case = case
+        self.layers = layers
+        self.B = case.batch
+        self.scale = case.geom.scale
+        i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)
+        self.q, self.k_pages, self.v_pages = case.q, case.k_pages, case.v_pages
+        self.k_new, self.v_new = case.k_new, case.v_new
+        self.block_table = i32(case.block_table)
+        self.seq_lens = i32(case.seq_lens)
+        self.slot_mapping = i32(case.slot_mapping)
+        self.out = torch.empty_like(self.q)
+        nbytes = pkv.decode_workspace_bytes(self.B, case.max_pages, case.num_pages)
+        self.ws = pkv.Workspace(nbytes, device)
+        self.graph = None
+
+    # algorithmic bytes of one decode launch (one layer)
+    def decode_bytes(self) -> int:
+        c = self.case
+        kv = int(c.seq_lens.astype(np.int64).sum()) * c.geom.n_kv_heads * c.geom.head_dim * 2 * 2
+        qo = 2 * self.B * c.geom.n_q_heads * c.geom.head_dim * 2
+        meta = self.block_table.numel() * 4 + self.B * 4
+        return kv + qo + meta
+
+    def append_bytes(self) -> int:
+        c = self.case
+        return 2 * 2 * self.B * c.geom.n_kv_heads * c.geom.head_dim * 2 + self.B * 4
+
+    def layer(self, l):
+        pkv = self.pkv
+        pkv.append(self.k_new[l], self.v_new[l], self.slot_mapping, self.k_pages[l], self.v_pages[l], self.ws)
+        pkv.decode_attn(self.q[l], self.k_pages[l], self.v_pages[l], self.block_table, self.seq_lens, self.out[l],
+                        self.scale, self.ws)
+
+    def step_eager(self):
+        for l in range(self.layers):
+            self.layer(l)
+
+    def capture(self):
+        torch = self.torch
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            self.step_eager()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.step_eager()
+        torch.cuda.synchronize()
+        self.graph = g
+        return g
+
+
+def _barrier(dist_on):
+    if dist_on:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def _max_over_ranks(x: float, dist_on: bool) -> float:
+    if not dist_on:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def time_graph(step, steps, warmup, dist_on):
+    torch = step.torch
+    g = step.graph
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    _barrier(dist_on)
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(steps):
+        g.replay()
+    e1.record(st)
+    torch.cuda.synchronize()
+    _barrier(dist_on)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1)  # ms
+
+
+def time_decode_launches(step, reps):
+    """Mean duration (ms) of the decode kernel: per-launch CUDA events on the launch stream,
+    with the stream kept busy so that launch latency does not enter the intervals."""
+    torch, pkv = step.torch, step.pkv
+    st = torch.cuda.current_stream()
+    durs = []
+    n = step.layers
+    for _ in range(reps):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        torch.cuda._sleep(int(2e7))  # ~10 ms of GPU work queued ahead of the launches
+        for l in range(n):
+            evs[l][0].record(st)
+            pkv.decode_attn(step.q[l], step.k_pages[l], step.v_pages[l], step.block_table, step.seq_lens,
+                            step.out[l], step.scale, step.ws)
+            evs[l][1].record(st)
+        torch.cuda.synchronize()
+        durs += [a.elapsed_time(b) for a, b in evs]
+    return float(np.mean(durs)), len(durs)
+
+
+def time_e2e(step, steps, warmup, dist_on):
+    """Steps/s through the Python API with host buffers: H2D of q, k_new, v_new, slots, lengths and
+    block table from pinned memory, the graph-captured step, D2H of the attention output, sync."""
+    torch = step.torch
+    pin = lambda t: t.detach().to("cpu").pin_memory()
+    hq, hk, hv = pin(step.q), pin(step.k_new), pin(step.v_new)
+    hs, hl, hb = pin(step.slot_mapping), pin(step.seq_lens), pin(step.block_table)
+    hout = torch.empty(step.out.shape, dtype=step.out.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hs, hl, hb))
+    d2h = hout.numel() * hout.element_size()
+
+    def one():
+        step.q.copy_(hq, non_blocking=True)
+        step.k_new.copy_(hk, non_blocking=True)
+        step.v_new.copy_(hv, non_blocking=True)
+        step.slot_mapping.copy_(hs, non_blocking=True)
+        step.seq_lens.copy_(hl, non_blocking=True)
+        step.block_table.copy_(hb, non_blocking=True)
+        step.graph.replay()
+        hout.copy_(step.out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(warmup):
+        one()
+    _barrier(dist_on)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    dt = time.perf_counter() - t0
+    _barrier(dist_on)
+    return dt, h2d, d2h
+
+
+# ------------------------------------------------------------------------------ CPU oracle
+def _cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_sample_case(seed):
+    from paged_kv_decode_gb300 import workloads as W
+
+    return W.decode_case(seed, W.config_seq_lens(2, seed), layers=1, device="cpu", pending_append=False,
+                         poison=True)
+
+
+def time_oracle_requests(case, n_requests, threads, start=0):
+    """Time the oracle on n_requests single-request decode samples (cycling the batch)."""
+    import oracle
+
+    t = 0.0
+    B = case.batch
+    for i in range(n_requests):
+        b = (start + i) % B
+        q = case.q[0][b:b + 1]
+        bt = case.block_table[b:b + 1]
+        sl = case.seq_lens[b:b + 1]
+        t0 = time.perf_counter()
+        oracle.decode(q, case.k_pages[0], case.v_pages[0], bt, sl, case.geom.scale, n_threads=threads)
+        t += time.perf_counter() - t0
+    return t
+
+
+def cpu_baseline(seed, budget_s=10.0):
+    """Oracle on whole layers of the workload (all 16 requests), as many as fit the budget."""
+    import oracle
+
+    case = oracle_sample_case(seed)
+    cores = _cpu_cores()
+    layers = 0
+    t = 0.0
+    while layers < 1 or t < budget_s:
+        t0 = time.perf_counter()
+        oracle.decode(case.q[0], case.k_pages[0], case.v_pages[0], case.block_table, case.seq_lens, case.geom.scale,
+                      n_threads=cores)
+        t += time.perf_counter() - t0
+        layers += 1
+        if layers >= 200:
+            break
+    steps_per_s = layers / t / 28.0
+    return {"value": steps_per_s, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{layers} full layers (bs16, all heads) of the same workload, fp64 C oracle, "
+                      f"{t:.1f} s; steps/s = layers/s / 28"}
+
+
+# ------------------------------------------------------------------------------ main
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    case = oracle_sample_case(2)
+    cores = _cpu_cores()
+    for i in range(args.warmup):
+        time_oracle_requests(case, 1, cores, start=i)
+    t = time_oracle_requests(case, args.steps, cores, start=args.warmup)
+    # one step of the workload = 16 requests x 28 layers
+    steps_per_s = args.steps / t / (case.batch * 28)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": steps_per_s, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 / steps_per_s, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "global_batch": 16, "layers": 28, "seq_len": "U{300..3000}",
+                   "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": steps_per_s, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"each timed step = one request of one layer (16 q heads) of the workload; "
+                                   f"{args.steps} steps in {t:.2f} s, scaled by 16 requests x 28 layers"},
+        "e2e": {"value": steps_per_s, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--layers", type=int, default=28)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the 40k-context decode measurement")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import torch
+
+    from paged_kv_decode_gb300.build import build_library
+    from paged_kv_decode_gb300 import workloads as W
+
+    if rank == 0 or world == 1:
+        build_library()
+    dist_on = world > 1
+    if dist_on:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+        if rank != 0:
+            build_library()
+    device = torch.device("cuda", local_rank if dist_on else 0)
+    torch.cuda.set_device(device)
+
+    # each replica runs its own copy of the workload (replicas only: requests are independent)
+    step = DecodeStep(device, W.config_seq_lens(2), args.layers, seed=2 + rank)
+    step.capture()
+    launches_per_step = 2 * args.layers
+
+    clocks = ClockSampler(device.index)
+    clocks.start()
+    ms_total = time_graph(step, args.steps, args.warmup, dist_on)
+    dec_ms, dec_n = time_decode_launches(step, reps=max(3, min(20, args.steps // 50)))
+    clk = clocks.stop()
+
+    ms_total = _max_over_ranks(ms_total, dist_on)
+    ms_per_step = ms_total / args.steps
+    steps_per_s = world * 1e3 / ms_per_step
+
+    e2e_dt, h2d, d2h = time_e2e(step, max(10, args.steps // 10), args.warmup, dist_on)
+    e2e_dt = _max_over_ranks(e2e_dt, dist_on)
+    e2e_steps = max(10, args.steps // 10)
+    e2e_value = world * e2e_steps / e2e_dt
+
+    hbm, bf16, peak_kind = _peaks()
+    dec_bytes = step.decode_bytes()
+    achieved = dec_bytes / (dec_ms * 1e-3) / 1e9
+    step_bytes = args.layers * (dec_bytes + step.append_bytes())
+    pool_bytes = 2 * step.k_pages.numel() * step.k_pages.element_size()
+
+    extra = {}
+    if not args.no_extra:
+        long_step = None
+        del step
+        torch.cuda.empty_cache()
+        long_step = DecodeStep(device, W.config_seq_lens(3, context=40000), args.layers, seed=3 + rank)
+        long_step.capture()
+        lt = time_graph(long_step, max(20, args.steps // 4), args.warmup, dist_on) / max(20, args.steps // 4)
+        ld_ms, _ = time_decode_launches(long_step, reps=5)
+        lb = long_step.decode_bytes()
+        extra["long_context_40k"] = {
+            "workload": "long-audio decode: 28 layers x bs1, context 40000, same geometry",
+            "ms_per_step": lt, "steps_per_s": 1e3 / lt,
+            "decode_kernel_us": ld_ms * 1e3, "decode_gbps": lb / (ld_ms * 1e-3) / 1e9,
+            "frac_of_measured_hbm": lb / (ld_ms * 1e-3) / 1e9 / hbm,
+        }
+        del long_step
+        torch.cuda.empty_cache()
+
+    if rank != 0:
+        if dist_on:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+        return
+
+    line = {
+        "metric": METRIC, "value": steps_per_s, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "global_batch": 16 * world, "layers": args.layers,
+                   "seq_len": "U{300..3000}", "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "no flush: %d distinct layer pools of %.2f GB in total exceed the 129 MB L2" % (
+                       args.layers, pool_bytes / 1e9)},
+        "kv_gbps_step": step_bytes / (ms_per_step * 1e-3) / 1e9 * world,
+        "roofline": {"bound": "hbm", "kernel": "pkv::decode_kernel", "achieved": achieved, "peak": hbm,
+                     "unit": "GB/s", "frac": achieved / hbm, "traffic": None, "peak_kind": peak_kind,
+                     "algorithmic_bytes_per_launch": dec_bytes, "launch_us": dec_ms * 1e3,
+                     "launches_timed": dec_n, "frac_of_nominal_8tbs": achieved / 8000.0},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    if extra:
+        line["extra"] = extra
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(2)
+    print(json.dumps(line), flush=True)
+    if dist_on:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

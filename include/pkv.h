@@ -1,0 +1,198 @@
+/*
+ * pkv.h -- C ABI of libpkv, paged-KV attention for a GB300 (sm_103a).
+ *
+ * The library implements the data-parallel hot path of LLM decoding in an
+ * audio-LLM ASR server: appending new key/value rows to a paged KV cache,
+ * batched decode attention over that cache, and chunked-prefill attention.
+ *
+ * Sources of the operations (titles of the pages they come from):
+ *  - "FunASR vLLM Inference Engine Guide", section 2 "vLLM Engine Architecture"
+ *    and the table "Why vLLM?": the LLM engine runs PagedAttention over a KV
+ *    cache that is allocated on demand, with continuous batching and CUDA
+ *    graphs.
+ *  - "Fun-ASR-Nano Native Runtime Design", section "Decoder And Prompt": the
+ *    decoder is a Qwen3-0.6B with 28 layers and 16 query / 8 KV heads.
+ *  - "Optimizing ASR for 90-minute multi-speaker audio" (MOSS-TD in
+ *    SGLang-Omni): section "Time spent: profiling" (decode takes over 94% of
+ *    the time on long audio), section "Chunked prefill for long audio"
+ *    (4096-token prefill chunks interleaved with decode steps) and section
+ *    "Autoregressive decoding" (decode replayed as CUDA graphs over batches
+ *    padded to buckets 1, 2, 4, 8, ...).
+ *
+ * Data layout (a reading; no page gives one):
+ *  - k_pages, v_pages: bf16 [num_pages][num_kv_heads][page_size][head_dim],
+ *    K and V in separate pools. One (page, KV head) tile is contiguous.
+ *  - Logical position j of request b is page block_table[b][j / page_size],
+ *    slot j % page_size. A slot index s names page s / page_size, slot
+ *    s % page_size.
+ *  - Query head h reads KV head h / (num_q_heads / num_kv_heads).
+ *  - q and out: bf16, row-major [rows][num_q_heads][head_dim].
+ *  - block_table: int32 [rows][max_pages_per_seq]; entries past a request's
+ *    last page are never read.
+ *
+ * Supported geometry: num_q_heads = 16, num_kv_heads = 8, head_dim = 128,
+ * page_size = 16 (other values return PKV_ERR_UNSUPPORTED).
+ *
+ * Conventions for every entry point:
+ *  - Every pointer argument except `desc` is DEVICE memory owned by the
+ *    caller; `desc` is a host pointer read during the call only. The library
+ *    never allocates, frees or synchronises, and keeps no state between calls
+ *    apart from a per-device cache of the SM count.
+ *  - Work is enqueued on `stream` (NULL = the legacy default stream) and is
+ *    ordered with the caller's other work on that stream. No call reads
+ *    device memory from the host, so the calls can be captured in a CUDA graph.
+ *  - Return value: PKV_OK, or a negative PKV_ERR_* code when the arguments are
+ *    rejected on the host (nothing is launched) or the launch fails.
+ *  - Errors found on the device (a page id outside the pool, a length beyond
+ *    the block table, a wait that ran out of time) are written to the status
+ *    word at the start of the workspace; the first error wins. The kernel
+ *    skips the offending access and stays within the caller's buffers.
+ *    Read the word with pkv_read_status().
+ *  - A workspace must be zero-filled once before its first use
+ *    (pkv_workspace_init); the kernels leave it ready for the next call. Calls
+ *    that may run concurrently (different streams) need separate workspaces.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+struct CUstream_st;
+typedef struct CUstream_st* pkv_stream_t;
+
+typedef struct pkv_cache_desc {
+  int32_t num_q_heads;  /* query heads (16) */
+  int32_t num_kv_heads; /* KV heads (8) */
+  int32_t head_dim;     /* 128 */
+  int32_t page_size;    /* tokens per page (16) */
+  int32_t num_pages;    /* pages in each of k_pages / v_pages */
+} pkv_cache_desc;
+
+enum {
+  PKV_OK = 0,
+  PKV_ERR_NULL_ARG = -1,            /* a required pointer is NULL */
+  PKV_ERR_BAD_SHAPE = -2,           /* a size is negative, zero where it may not be, or inconsistent */
+  PKV_ERR_UNSUPPORTED = -3,         /* geometry other than 16/8/128/16, or no sm_103 device */
+  PKV_ERR_WORKSPACE_TOO_SMALL = -4, /* workspace_bytes below the matching *_workspace_bytes() */
+  PKV_ERR_CUDA = -5,                /* a CUDA runtime call or the launch failed */
+  PKV_ERR_DEVICE_TIMEOUT = -6,      /* device: a bounded wait for a copy ran out (status word only) */
+  PKV_ERR_OUT_OF_BOUNDS = -7,       /* device: page id, slot or length outside the pool/table (status word only) */
+  PKV_ERR_MISALIGNED = -8           /* a buffer is not 16-byte aligned */
+};
+
+/* Bytes of the status header at the start of every workspace. */
+#define PKV_STATUS_BYTES 256
+
+/* Zero a workspace (cudaMemsetAsync on `stream`). Call once after allocating it. */
+int pkv_workspace_init(void* workspace, size_t workspace_bytes, pkv_stream_t stream);
+
+/*
+ * Read the status word of a workspace: waits for `stream`, then copies the
+ * word to the host. For tests and debugging only (it synchronises).
+ * Returns the device status (PKV_OK or a PKV_ERR_* code), or PKV_ERR_CUDA.
+ */
+int pkv_read_status(const void* workspace, pkv_stream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char* pkv_status_string(int status);
+
+/*
+ * pkv_append -- write the key and value rows of new tokens into their slots.
+ *
+ * Source: the KV cache grows by one row per generated token and by a chunk of
+ * rows per prefill chunk ("FunASR vLLM Inference Engine Guide", section 2:
+ * PagedAttention with on-demand allocation; "Optimizing ASR for 90-minute
+ * multi-speaker audio", section "LLM prefill").
+ *
+ *  k_new, v_new:  bf16 [n_tokens][num_kv_heads][head_dim], 16-byte aligned.
+ *  slot_mapping:  int32 [n_tokens]; token t goes to slot slot_mapping[t];
+ *                 a negative slot skips the token; a slot >= num_pages *
+ *                 page_size sets PKV_ERR_OUT_OF_BOUNDS and is skipped.
+ *  n_tokens:      >= 0 (0 launches nothing).
+ *  k_pages, v_pages: the pools, updated in place. Bit-exact copy.
+ *  workspace:     may be NULL (device errors then go unreported); otherwise
+ *                 at least PKV_STATUS_BYTES.
+ */
+int pkv_append(const void* k_new, const void* v_new, const int32_t* slot_mapping, int32_t n_tokens,
+               void* k_pages, void* v_pages, const pkv_cache_desc* desc, pkv_stream_t stream,
+               void* workspace, size_t workspace_bytes);
+
+/*
+ * Workspace bytes pkv_decode_attn needs for `batch` requests on the current
+ * device (status header, one counter per (request, KV head), and the
+ * split-KV partial results). Returns 0 for unsupported arguments.
+ */
+size_t pkv_decode_workspace_bytes(const pkv_cache_desc* desc, int32_t batch, int32_t max_pages_per_seq);
+
+/*
+ * pkv_decode_attn -- decode attention over the paged KV cache.
+ *
+ * Source: PagedAttention decoding ("FunASR vLLM Inference Engine Guide",
+ * section 2); decode dominates long-audio serving ("Optimizing ASR for
+ * 90-minute multi-speaker audio", section "Time spent: profiling").
+ *
+ * For every request b and query head h:
+ *   out[b][h] = sum_j softmax_j(scale * <q[b][h], k_j>) v_j,  j < seq_lens[b],
+ * with k_j, v_j the rows of KV head h / (num_q_heads / num_kv_heads) at
+ * logical position j. seq_lens counts the token appended this step (append
+ * first). A request with seq_lens[b] == 0 (a padding row of a graph bucket)
+ * gets an all-zero output row. Inputs bf16, fp32 accumulation, bf16 output.
+ * The split of long contexts over CTAs and the merge of the partial results
+ * happen inside the call; the result does not depend on page placement.
+ *
+ *  q:            bf16 [batch][num_q_heads][head_dim]
+ *  k_pages, v_pages: bf16 pools (see layout above), 16-byte aligned
+ *  block_table:  int32 [batch][max_pages_per_seq]
+ *  seq_lens:     int32 [batch], 0 <= seq_lens[b] <= max_pages_per_seq * page_size
+ *                (larger values are clamped and set PKV_ERR_OUT_OF_BOUNDS)
+ *  out:          bf16 [batch][num_q_heads][head_dim]
+ *  scale:        softmax scale (1/sqrt(head_dim) for the Qwen3 decoder)
+ *  batch:        >= 0 (0 launches nothing), max_pages_per_seq >= 1
+ *  workspace:    >= pkv_decode_workspace_bytes(desc, batch, max_pages_per_seq)
+ */
+int pkv_decode_attn(const void* q, const void* k_pages, const void* v_pages, const int32_t* block_table,
+                    const int32_t* seq_lens, void* out, float scale, pkv_stream_t stream,
+                    const pkv_cache_desc* desc, int32_t batch, int32_t max_pages_per_seq, void* workspace,
+                    size_t workspace_bytes);
+
+/*
+ * Workspace bytes pkv_prefill_chunk_attn needs (status header only at present).
+ */
+size_t pkv_prefill_workspace_bytes(const pkv_cache_desc* desc, int32_t num_seqs, int32_t max_q_len);
+
+/*
+ * pkv_prefill_chunk_attn -- causal attention of prefill chunks over the cache.
+ *
+ * Source: "Optimizing ASR for 90-minute multi-speaker audio", section
+ * "Chunked prefill for long audio": a long prompt is prefilled in 4096-token
+ * chunks, one per scheduler step, between other requests' decode steps.
+ *
+ * Request n owns query rows cu_q_lens[n] .. cu_q_lens[n+1]-1 of q; its chunk
+ * follows prefix_lens[n] cached tokens, and row i of the chunk (absolute
+ * position prefix_lens[n] + i) attends keys 0 .. prefix_lens[n] + i of the
+ * request (bottom-right causal alignment). The chunk's own K/V rows must
+ * already be in the pool (pkv_append first).
+ *
+ *  q, out:       bf16 [total_q][num_q_heads][head_dim], total_q = cu_q_lens[num_seqs]
+ *  block_table:  int32 [num_seqs][max_pages_per_seq]
+ *  prefix_lens:  int32 [num_seqs]
+ *  cu_q_lens:    int32 [num_seqs + 1], cu_q_lens[0] = 0, non-decreasing
+ *  max_q_len:    host-side upper bound on any chunk length (sizes the grid)
+ *  workspace:    >= pkv_prefill_workspace_bytes(...)
+ */
+int pkv_prefill_chunk_attn(const void* q, const void* k_pages, const void* v_pages, const int32_t* block_table,
+                           const int32_t* prefix_lens, const int32_t* cu_q_lens, int32_t num_seqs, void* out,
+                           float scale, pkv_stream_t stream, const pkv_cache_desc* desc, int32_t max_pages_per_seq,
+                           int32_t max_q_len, void* workspace, size_t workspace_bytes);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

@@ -1,0 +1,198 @@
+"""paged_kv_decode_gb300 -- paged-KV attention for a GB300 (sm_103a), Python binding.
+
+Thin marshalling over the C ABI of libpkv (include/pkv.h): every step of the
+path (KV append, decode attention, chunked-prefill attention) runs in the
+library's CUDA kernels. torch tensors supply device memory and the current
+CUDA stream. There is no CPU fallback: without the compiled library every call
+raises.
+
+Layout (see include/pkv.h): pools bf16 [num_pages, 8, 16, 128]; q / out bf16
+[rows, 16, 128]; block tables int32 [rows, max_pages]; lengths int32.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+from . import _lib
+
+PKV_OK = 0
+PKV_STATUS_BYTES = 256
+ERRORS = {
+    -1: "PKV_ERR_NULL_ARG",
+    -2: "PKV_ERR_BAD_SHAPE",
+    -3: "PKV_ERR_UNSUPPORTED",
+    -4: "PKV_ERR_WORKSPACE_TOO_SMALL",
+    -5: "PKV_ERR_CUDA",
+    -6: "PKV_ERR_DEVICE_TIMEOUT",
+    -7: "PKV_ERR_OUT_OF_BOUNDS",
+    -8: "PKV_ERR_MISALIGNED",
+}
+
+__all__ = [
+    "PkvError", "desc", "Workspace", "append", "decode_attn", "prefill_chunk_attn",
+    "decode_workspace_bytes", "prefill_workspace_bytes", "workspace_init", "read_status", "status_string",
+]
+
+
+class PkvError(RuntimeError):
+    def __init__(self, code: int, what: str = ""):
+        self.code = code
+        super().__init__(f"{what}: {ERRORS.get(code, code)} ({status_string(code)})")
+
+
+def status_string(code: int) -> str:
+    return _lib.load().pkv_status_string(int(code)).decode()
+
+
+def _check(code: int, what: str):
+    if code != PKV_OK:
+        raise PkvError(code, what)
+
+
+def desc(num_pages: int, num_q_heads: int = 16, num_kv_heads: int = 8, head_dim: int = 128, page_size: int = 16):
+    return _lib.CacheDesc(num_q_heads, num_kv_heads, head_dim, page_size, int(num_pages))
+
+
+def _desc_of(k_pages) -> "_lib.CacheDesc":
+    if k_pages.dim() != 4:
+        raise ValueError("pools are [num_pages, num_kv_heads, page_size, head_dim]")
+    p, hkv, ps, d = k_pages.shape
+    return desc(p, 16, hkv, d, ps)
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    import torch
+
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t, dtype, name, device=None):
+    import torch
+
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    return t
+
+
+def workspace_init(ws, stream=None):
+    _check(_lib.load().pkv_workspace_init(ctypes.c_void_p(ws.data_ptr()), ws.numel() * ws.element_size(),
+                                          _stream(stream)), "pkv_workspace_init")
+
+
+def read_status(ws, stream=None) -> int:
+    """Status word of a workspace (synchronises the stream; tests and debugging only)."""
+    return int(_lib.load().pkv_read_status(ctypes.c_void_p(ws.data_ptr()), _stream(stream)))
+
+
+def decode_workspace_bytes(batch: int, max_pages: int, num_pages: int = 1) -> int:
+    d = desc(num_pages)
+    return int(_lib.load().pkv_decode_workspace_bytes(ctypes.byref(d), int(batch), int(max_pages)))
+
+
+def prefill_workspace_bytes(num_seqs: int, max_q_len: int, num_pages: int = 1) -> int:
+    d = desc(num_pages)
+    return int(_lib.load().pkv_prefill_workspace_bytes(ctypes.byref(d), int(num_seqs), int(max_q_len)))
+
+
+class Workspace:
+    """A zero-initialised device workspace (uint8 tensor) for one stream's calls."""
+
+    def __init__(self, nbytes: int, device=None):
+        import torch
+
+        nbytes = max(int(nbytes), PKV_STATUS_BYTES)
+        self.tensor = torch.empty(nbytes, dtype=torch.uint8, device=device or "cuda")
+        workspace_init(self.tensor)
+
+    @property
+    def nbytes(self) -> int:
+        return self.tensor.numel()
+
+    def status(self) -> int:
+        return read_status(self.tensor)
+
+    def ensure(self, nbytes: int):
+        if nbytes > self.nbytes:
+            self.__init__(nbytes, self.tensor.device)
+        return self
+
+
+def append(k_new, v_new, slot_mapping, k_pages, v_pages, workspace: Optional[Workspace] = None, stream=None):
+    """Write rows k_new / v_new [n, 8, 128] into the pools at slot_mapping [n] (int32)."""
+    import torch
+
+    _need(k_pages, torch.bfloat16, "k_pages")
+    dev = k_pages.device
+    _need(v_pages, torch.bfloat16, "v_pages", dev)
+    _need(k_new, torch.bfloat16, "k_new", dev)
+    _need(v_new, torch.bfloat16, "v_new", dev)
+    _need(slot_mapping, torch.int32, "slot_mapping", dev)
+    n = slot_mapping.numel()
+    if k_new.shape[0] != n or v_new.shape != k_new.shape or v_pages.shape != k_pages.shape:
+        raise ValueError("shape mismatch")
+    d = _desc_of(k_pages)
+    ws = workspace.tensor if workspace is not None else None
+    rc = _lib.load().pkv_append(_ptr(k_new), _ptr(v_new), _ptr(slot_mapping), n, _ptr(k_pages), _ptr(v_pages),
+                                ctypes.byref(d), _stream(stream), _ptr(ws), 0 if ws is None else ws.numel())
+    _check(rc, "pkv_append")
+
+
+def decode_attn(q, k_pages, v_pages, block_table, seq_lens, out, scale: float, workspace: Workspace, stream=None):
+    """Decode attention: out [B, 16, 128] from q [B, 16, 128] over the paged cache."""
+    import torch
+
+    _need(k_pages, torch.bfloat16, "k_pages")
+    dev = k_pages.device
+    _need(v_pages, torch.bfloat16, "v_pages", dev)
+    _need(q, torch.bfloat16, "q", dev)
+    _need(out, torch.bfloat16, "out", dev)
+    _need(block_table, torch.int32, "block_table", dev)
+    _need(seq_lens, torch.int32, "seq_lens", dev)
+    B = q.shape[0]
+    if out.shape != q.shape or block_table.dim() != 2 or block_table.shape[0] != B or seq_lens.numel() != B:
+        raise ValueError("shape mismatch")
+    d = _desc_of(k_pages)
+    ws = workspace.tensor
+    rc = _lib.load().pkv_decode_attn(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), _ptr(seq_lens),
+                                     _ptr(out), float(scale), _stream(stream), ctypes.byref(d), B,
+                                     block_table.shape[1], _ptr(ws), ws.numel())
+    _check(rc, "pkv_decode_attn")
+
+
+def prefill_chunk_attn(q, k_pages, v_pages, block_table, prefix_lens, cu_q_lens, out, scale: float, max_q_len: int,
+                       workspace: Workspace, stream=None):
+    """Causal chunk attention: out [total_q, 16, 128] for chunks packed by cu_q_lens."""
+    import torch
+
+    _need(k_pages, torch.bfloat16, "k_pages")
+    dev = k_pages.device
+    _need(v_pages, torch.bfloat16, "v_pages", dev)
+    _need(q, torch.bfloat16, "q", dev)
+    _need(out, torch.bfloat16, "out", dev)
+    _need(block_table, torch.int32, "block_table", dev)
+    _need(prefix_lens, torch.int32, "prefix_lens", dev)
+    _need(cu_q_lens, torch.int32, "cu_q_lens", dev)
+    S = prefix_lens.numel()
+    if cu_q_lens.numel() != S + 1 or block_table.shape[0] != S or out.shape != q.shape:
+        raise ValueError("shape mismatch")
+    d = _desc_of(k_pages)
+    ws = workspace.tensor
+    rc = _lib.load().pkv_prefill_chunk_attn(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
+                                            _ptr(prefix_lens), _ptr(cu_q_lens), S, _ptr(out), float(scale),
+                                            _stream(stream), ctypes.byref(d), block_table.shape[1], int(max_q_len),
+                                            _ptr(ws), ws.numel())
+    _check(rc, "pkv_prefill_chunk_attn")

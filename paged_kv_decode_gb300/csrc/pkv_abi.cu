@@ -1,0 +1,177 @@
+// pkv_abi.cu -- the extern "C" entry points of libpkv: argument checks on the
+// host, launch-configuration choice, and the status word helpers. All device
+// work is in append.cu, decode.cu and prefill.cu.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "pkv.h"
+#include "pkv_kernels.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool known = false;
+  bool supported = false;
+  int num_sms = 0;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+// SM count of the current device, and whether it is an sm_103 part (the only
+// architecture the kernels are compiled for).
+int current_device(int* num_sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return PKV_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.known) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return PKV_ERR_CUDA;
+    d.supported = (major == 10 && minor == 3);
+    d.num_sms = sms;
+    d.known = true;
+  }
+  if (!d.supported) return PKV_ERR_UNSUPPORTED;
+  *num_sms = d.num_sms;
+  return PKV_OK;
+}
+
+int check_desc(const pkv_cache_desc* d) {
+  if (d == nullptr) return PKV_ERR_NULL_ARG;
+  if (d->num_q_heads <= 0 || d->num_kv_heads <= 0 || d->head_dim <= 0 || d->page_size <= 0 || d->num_pages <= 0)
+    return PKV_ERR_BAD_SHAPE;
+  if (d->num_q_heads != 16 || d->num_kv_heads != 8 || d->head_dim != 128 || d->page_size != 16)
+    return PKV_ERR_UNSUPPORTED;
+  return PKV_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Largest block table the kernels index with 32-bit triple counts.
+bool table_fits(int32_t rows, int32_t max_pages) {
+  return static_cast<long long>(rows) * max_pages * 8 < (1LL << 31);
+}
+
+}  // namespace
+
+extern "C" {
+
+int pkv_workspace_init(void* workspace, size_t workspace_bytes, pkv_stream_t stream) {
+  if (workspace == nullptr) return PKV_ERR_NULL_ARG;
+  if (workspace_bytes < PKV_STATUS_BYTES) return PKV_ERR_WORKSPACE_TOO_SMALL;
+  return cudaMemsetAsync(workspace, 0, workspace_bytes, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PKV_OK
+             : PKV_ERR_CUDA;
+}
+
+int pkv_read_status(const void* workspace, pkv_stream_t stream) {
+  if (workspace == nullptr) return PKV_ERR_NULL_ARG;
+  int v = 0;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&v, workspace, sizeof v, cudaMemcpyDeviceToHost, s) != cudaSuccess) return PKV_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return PKV_ERR_CUDA;
+  return v;
+}
+
+const char* pkv_status_string(int status) {
+  switch (status) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_NULL_ARG: return "a required pointer is NULL";
+    case PKV_ERR_BAD_SHAPE: return "bad or inconsistent size";
+    case PKV_ERR_UNSUPPORTED: return "unsupported geometry or device (needs 16/8/128/16 on sm_103)";
+    case PKV_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case PKV_ERR_CUDA: return "CUDA runtime or launch error";
+    case PKV_ERR_DEVICE_TIMEOUT: return "a device-side wait ran out of time";
+    case PKV_ERR_OUT_OF_BOUNDS: return "page id, slot or length outside the pool or block table";
+    case PKV_ERR_MISALIGNED: return "buffer not 16-byte aligned";
+    default: return "unknown status";
+  }
+}
+
+int pkv_append(const void* k_new, const void* v_new, const int32_t* slot_mapping, int32_t n_tokens, void* k_pages,
+               void* v_pages, const pkv_cache_desc* desc, pkv_stream_t stream, void* workspace,
+               size_t workspace_bytes) {
+  int rc = check_desc(desc);
+  if (rc != PKV_OK) return rc;
+  if (n_tokens < 0) return PKV_ERR_BAD_SHAPE;
+  if (workspace != nullptr && workspace_bytes < PKV_STATUS_BYTES) return PKV_ERR_WORKSPACE_TOO_SMALL;
+  if (n_tokens == 0) return PKV_OK;
+  if (!k_new || !v_new || !slot_mapping || !k_pages || !v_pages) return PKV_ERR_NULL_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pages) || !aligned16(v_pages))
+    return PKV_ERR_MISALIGNED;
+  int sms = 0;
+  rc = current_device(&sms);
+  if (rc != PKV_OK) return rc;
+  return pkv::launch_append(k_new, v_new, slot_mapping, n_tokens, k_pages, v_pages, desc->num_pages,
+                            static_cast<int*>(workspace), sms, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t pkv_decode_workspace_bytes(const pkv_cache_desc* desc, int32_t batch, int32_t max_pages_per_seq) {
+  if (check_desc(desc) != PKV_OK || batch < 0 || max_pages_per_seq < 1) return 0;
+  if (batch > pkv::decode_max_batch() || !table_fits(batch, max_pages_per_seq)) return 0;
+  int sms = 0;
+  if (current_device(&sms) != PKV_OK) return 0;
+  return pkv::decode_workspace_bytes(batch, sms);
+}
+
+int pkv_decode_attn(const void* q, const void* k_pages, const void* v_pages, const int32_t* block_table,
+                    const int32_t* seq_lens, void* out, float scale, pkv_stream_t stream,
+                    const pkv_cache_desc* desc, int32_t batch, int32_t max_pages_per_seq, void* workspace,
+                    size_t workspace_bytes) {
+  int rc = check_desc(desc);
+  if (rc != PKV_OK) return rc;
+  if (batch < 0 || max_pages_per_seq < 1) return PKV_ERR_BAD_SHAPE;
+  if (batch > pkv::decode_max_batch()) return PKV_ERR_UNSUPPORTED;
+  if (!table_fits(batch, max_pages_per_seq)) return PKV_ERR_BAD_SHAPE;
+  if (workspace == nullptr) return PKV_ERR_NULL_ARG;
+  if (batch == 0) return PKV_OK;
+  if (!q || !k_pages || !v_pages || !block_table || !seq_lens || !out) return PKV_ERR_NULL_ARG;
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(out) || !aligned16(workspace))
+    return PKV_ERR_MISALIGNED;
+  int sms = 0;
+  rc = current_device(&sms);
+  if (rc != PKV_OK) return rc;
+  if (workspace_bytes < pkv::decode_workspace_bytes(batch, sms)) return PKV_ERR_WORKSPACE_TOO_SMALL;
+  return pkv::launch_decode(q, k_pages, v_pages, block_table, seq_lens, out, scale, batch, max_pages_per_seq,
+                            desc->num_pages, workspace, sms, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t pkv_prefill_workspace_bytes(const pkv_cache_desc* desc, int32_t num_seqs, int32_t max_q_len) {
+  if (check_desc(desc) != PKV_OK || num_seqs < 0 || max_q_len < 0) return 0;
+  int sms = 0;
+  if (current_device(&sms) != PKV_OK) return 0;
+  return pkv::prefill_workspace_bytes(num_seqs, max_q_len, sms);
+}
+
+int pkv_prefill_chunk_attn(const void* q, const void* k_pages, const void* v_pages, const int32_t* block_table,
+                           const int32_t* prefix_lens, const int32_t* cu_q_lens, int32_t num_seqs, void* out,
+                           float scale, pkv_stream_t stream, const pkv_cache_desc* desc, int32_t max_pages_per_seq,
+                           int32_t max_q_len, void* workspace, size_t workspace_bytes) {
+  int rc = check_desc(desc);
+  if (rc != PKV_OK) return rc;
+  if (num_seqs < 0 || max_q_len < 0 || max_pages_per_seq < 1) return PKV_ERR_BAD_SHAPE;
+  if (!table_fits(num_seqs, max_pages_per_seq)) return PKV_ERR_BAD_SHAPE;
+  if (workspace == nullptr) return PKV_ERR_NULL_ARG;
+  if (num_seqs == 0 || max_q_len == 0) return PKV_OK;
+  if (!q || !k_pages || !v_pages || !block_table || !prefix_lens || !cu_q_lens || !out) return PKV_ERR_NULL_ARG;
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(out) || !aligned16(workspace))
+    return PKV_ERR_MISALIGNED;
+  int sms = 0;
+  rc = current_device(&sms);
+  if (rc != PKV_OK) return rc;
+  if (workspace_bytes < pkv::prefill_workspace_bytes(num_seqs, max_q_len, sms)) return PKV_ERR_WORKSPACE_TOO_SMALL;
+  return pkv::launch_prefill(q, k_pages, v_pages, block_table, prefix_lens, cu_q_lens, num_seqs, out, scale,
+                             max_pages_per_seq, max_q_len, desc->num_pages, workspace, sms,
+                             reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

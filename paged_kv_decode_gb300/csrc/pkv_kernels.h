@@ -1,0 +1,26 @@
+// pkv_kernels.h -- internal launchers behind the C ABI (host side).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pkv {
+
+int launch_append(const void* k_new, const void* v_new, const int32_t* slot_mapping, int32_t n_tokens, void* k_pages,
+                  void* v_pages, int32_t num_pages, int* status, int num_sms, cudaStream_t stream);
+
+// Decode: workspace = [status header | counters (batch * kv heads) | partials].
+size_t decode_workspace_bytes(int32_t batch, int num_sms);
+int launch_decode(const void* q, const void* k_pages, const void* v_pages, const int32_t* block_table,
+                  const int32_t* seq_lens, void* out, float scale, int32_t batch, int32_t max_pages,
+                  int32_t num_pages, void* workspace, int num_sms, cudaStream_t stream);
+int decode_max_batch();
+
+size_t prefill_workspace_bytes(int32_t num_seqs, int32_t max_q_len, int num_sms);
+int launch_prefill(const void* q, const void* k_pages, const void* v_pages, const int32_t* block_table,
+                   const int32_t* prefix_lens, const int32_t* cu_q_lens, int32_t num_seqs, void* out, float scale,
+                   int32_t max_pages, int32_t max_q_len, int32_t num_pages, void* workspace, int num_sms,
+                   cudaStream_t stream);
+
+}  // namespace pkv

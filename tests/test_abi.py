@@ -1,0 +1,72 @@
+"""The C-ABI library: it builds, loads, exports every symbol include/pkv.h
+declares, and rejects bad arguments on the host before touching a device.
+CPU only: no call here launches or queries a GPU."""
+import ctypes
+
+import pytest
+
+from paged_kv_decode_gb300 import _lib
+from paged_kv_decode_gb300.build import build_library
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_library()
+    return _lib.load()
+
+
+def test_exports_every_declared_function(lib):
+    declared = _lib.header_functions()
+    assert len(declared) >= 8
+    assert set(declared) == set(_lib.PROTOTYPES), "binding prototypes out of sync with include/pkv.h"
+    for name in declared:
+        assert hasattr(lib, name), f"libpkv.so does not export {name}"
+
+
+def test_status_strings(lib):
+    for code in [0, -1, -2, -3, -4, -5, -6, -7, -8]:
+        s = lib.pkv_status_string(code).decode()
+        assert s and s != "unknown status"
+    assert lib.pkv_status_string(12345).decode() == "unknown status"
+
+
+def _desc(**kw):
+    d = dict(num_q_heads=16, num_kv_heads=8, head_dim=128, page_size=16, num_pages=4)
+    d.update(kw)
+    return _lib.CacheDesc(**d)
+
+
+def test_host_argument_checks(lib):
+    d = _desc()
+    # NULL descriptor
+    assert lib.pkv_append(None, None, None, 1, None, None, None, None, None, 0) == -1
+    # unsupported geometry
+    bad = _desc(head_dim=64)
+    assert lib.pkv_append(None, None, None, 1, None, None, ctypes.byref(bad), None, None, 0) == -3
+    bad = _desc(num_kv_heads=4)
+    assert lib.pkv_decode_attn(None, None, None, None, None, None, 1.0, None, ctypes.byref(bad), 1, 1, None, 0) == -3
+    # sizes
+    assert lib.pkv_append(None, None, None, -1, None, None, ctypes.byref(d), None, None, 0) == -2
+    assert lib.pkv_decode_attn(None, None, None, None, None, None, 1.0, None, ctypes.byref(d), -1, 1, None, 0) == -2
+    assert lib.pkv_decode_attn(None, None, None, None, None, None, 1.0, None, ctypes.byref(d), 1, 0, None, 0) == -2
+    zero_pages = _desc(num_pages=0)
+    assert lib.pkv_append(None, None, None, 1, None, None, ctypes.byref(zero_pages), None, None, 0) == -2
+    # nothing to do is fine, without any device
+    assert lib.pkv_append(None, None, None, 0, None, None, ctypes.byref(d), None, None, 0) == 0
+    # missing pointers
+    assert lib.pkv_append(None, None, None, 3, None, None, ctypes.byref(d), None, None, 0) == -1
+    assert lib.pkv_decode_attn(None, None, None, None, None, None, 1.0, None, ctypes.byref(d), 2, 4, None, 0) == -1
+    # a workspace smaller than the status header
+    ws = ctypes.create_string_buffer(64)
+    assert lib.pkv_append(None, None, None, 0, None, None, ctypes.byref(d), None, ws, 64) == -4
+    # workspace queries refuse bad arguments
+    assert lib.pkv_decode_workspace_bytes(None, 1, 1) == 0
+    assert lib.pkv_decode_workspace_bytes(ctypes.byref(d), -1, 1) == 0
+    assert lib.pkv_decode_workspace_bytes(ctypes.byref(d), 1, 0) == 0
+
+
+def test_no_cpu_fallback_without_the_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(_lib, "_lib", None)
+    monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        _lib.load()

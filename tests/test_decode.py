@@ -1,0 +1,207 @@
+"""Decode attention on the GPU against the fp64 oracle.
+
+Bar: max |diff| <= 1e-2, mean |diff| <= 1e-3 and relative L2 <= 1e-2 over
+every output element (tests/parity.py). Exact cases (one cached token, page
+placement, empty rows) are compared bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_decode_gb300 as pkv
+from gpu_util import DecodeOnDevice, bits, ensure_built, i32
+from parity import assert_close, bf16_to_f64
+from paged_kv_decode_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def _oracle_after_append(case, layer, dev_run):
+    kp, vp = dev_run.pools_cpu()  # pools after the GPU append (append itself is checked bit-exact elsewhere)
+    if case.k_new is not None:
+        want_k, want_v = oracle.append(case.k_new[layer], case.v_new[layer], case.slot_mapping,
+                                       case.k_pages[layer], case.v_pages[layer])
+        assert np.array_equal(bits(kp), want_k) and np.array_equal(bits(vp), want_v)
+        return want_k, want_v
+    return kp, vp
+
+
+def _check_case(case, dev, layers=(0,), what=""):
+    for layer in layers:
+        run = DecodeOnDevice(case, layer, dev)
+        out = run.step()
+        torch.cuda.synchronize()
+        kp, vp = _oracle_after_append(case, layer, run)
+        want = oracle.decode(case.q[layer], kp, vp, case.block_table, case.seq_lens, case.geom.scale)
+        assert_close(bf16_to_f64(out), want, f"{what} layer {layer}")
+        assert run.ws.status() == 0
+
+
+def test_tiny_config(cuda_device):
+    case = W.decode_case(1, W.config_seq_lens(1), pending_append=True, poison=False)
+    assert case.num_pages == 17  # 16 request pages + the unused last page
+    _check_case(case, cuda_device, what="tiny")
+
+
+def test_qwen3_bs16_two_layers(cuda_device):
+    case = W.decode_case(2, W.config_seq_lens(2), layers=2, pending_append=True, poison=True)
+    _check_case(case, cuda_device, layers=(0, 1), what="bs16")
+
+
+@pytest.mark.parametrize("context", [4096, 16384, 40000, 65536])
+def test_long_context(cuda_device, context):
+    case = W.decode_case(3, W.config_seq_lens(3, context=context), pending_append=True, poison=True)
+    _check_case(case, cuda_device, what=f"context {context}")
+
+
+def test_cfg_pairs(cuda_device):
+    case = W.decode_case(5, W.config_seq_lens(5), pending_append=True, poison=True)
+    _check_case(case, cuda_device, what="cfg")
+
+
+def test_mixed_step_decode_part(cuda_device):
+    case = W.decode_case(4, W.mixed_decode_lens(), pending_append=True, poison=True)
+    _check_case(case, cuda_device, what="mixed decode")
+
+
+@pytest.mark.parametrize("lens", [[1], [17], [15, 16, 17, 31, 32, 33], list(range(1, 65))])
+def test_ragged_lengths(cuda_device, lens):
+    case = W.decode_case(6, lens, pending_append=True, poison=True)
+    _check_case(case, cuda_device, what=f"ragged {lens[:4]}")
+
+
+def test_graph_bucket_padding_rows_are_zero(cuda_device):
+    lens = [700, 0, 33, 0, 0, 1, 2900, 0]
+    case = W.decode_case(7, lens, pending_append=True, poison=True)
+    run = DecodeOnDevice(case, 0, cuda_device)
+    run.out.fill_(7.0)
+    out = run.step()
+    torch.cuda.synchronize()
+    for b, n in enumerate(lens):
+        if n == 0:
+            assert torch.count_nonzero(out[b]).item() == 0
+    kp, vp = _oracle_after_append(case, 0, run)
+    want = oracle.decode(case.q[0], kp, vp, case.block_table, case.seq_lens, case.geom.scale)
+    assert_close(bf16_to_f64(out), want, "padded bucket")
+
+
+def test_all_rows_empty(cuda_device):
+    case = W.decode_case(8, [0, 0, 0, 0], pending_append=False, poison=True)
+    run = DecodeOnDevice(case, 0, cuda_device)
+    run.out.fill_(1.0)
+    out = run.step()
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(out).item() == 0
+    assert run.ws.status() == 0
+
+
+def test_single_cached_token_is_exact(cuda_device):
+    # softmax over one key is 1; 1 * v is exact in fp32 and rounds back to the same bf16
+    case = W.decode_case(9, [1] * 16, pending_append=False, poison=True)
+    run = DecodeOnDevice(case, 0, cuda_device)
+    out = run.step().cpu()
+    for b in range(16):
+        page = case.block_table[b, 0]
+        for h in range(16):
+            assert torch.equal(out[b, h].view(torch.int16), case.v_pages[0, page, h // 2, 0].view(torch.int16))
+
+
+def test_page_placement_gives_identical_bits(cuda_device):
+    case = W.decode_case(10, W.config_seq_lens(2), pending_append=False, poison=True)
+    out1 = DecodeOnDevice(case, 0, cuda_device).step().clone()
+    rng = np.random.default_rng(1234)
+    perm = rng.permutation(case.num_pages)
+    kp2 = torch.empty_like(case.k_pages)
+    vp2 = torch.empty_like(case.v_pages)
+    kp2[:, perm] = case.k_pages
+    vp2[:, perm] = case.v_pages
+    case.k_pages, case.v_pages = kp2, vp2
+    case.block_table = perm[case.block_table].astype(np.int32)
+    out2 = DecodeOnDevice(case, 0, cuda_device).step()
+    torch.cuda.synchronize()
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+
+
+def test_peaked_scores(cuda_device):
+    # one key per (request, KV head) made a large multiple of the query: the softmax is
+    # nearly one-hot, so a wrong page, slot or head shows up as an O(1) error
+    case = W.decode_case(11, [300, 1234, 2900, 45], pending_append=False, poison=True)
+    rng = np.random.default_rng(5)
+    for b, n in enumerate(case.seq_lens):
+        for g in range(8):
+            j = int(rng.integers(0, n))
+            page, slot = case.block_table[b, j // 16], j % 16
+            case.k_pages[0, page, g, slot] = (case.q[0, b, 2 * g].float() * 0.5).to(torch.bfloat16)
+    run = DecodeOnDevice(case, 0, cuda_device)
+    out = run.step()
+    torch.cuda.synchronize()
+    want = oracle.decode(case.q[0], case.k_pages[0], case.v_pages[0], case.block_table, case.seq_lens,
+                         case.geom.scale)
+    assert_close(bf16_to_f64(out), want, "peaked")
+
+
+def test_cuda_graph_replay_matches_eager(cuda_device):
+    case = W.decode_case(12, W.config_seq_lens(2), layers=2, pending_append=False, poison=True)
+    runs = [DecodeOnDevice(case, layer, cuda_device) for layer in range(2)]
+    eager = [r.step().clone() for r in runs]
+    for r in runs:
+        r.out.zero_()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for r in runs:  # warm-up on the capture stream
+            r.step()
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for r in runs:
+            r.step()
+    for r in runs:
+        r.out.zero_()
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    for r, e in zip(runs, eager):
+        assert torch.equal(r.out.view(torch.int16), e.view(torch.int16))
+        assert r.ws.status() == 0
+
+
+def test_repeated_calls_reuse_the_workspace(cuda_device):
+    # the split-KV counters return to zero, so a second call on the same workspace is identical
+    case = W.decode_case(13, [40000], pending_append=False, poison=True)
+    run = DecodeOnDevice(case, 0, cuda_device)
+    a = run.step().clone()
+    b = run.step().clone()
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    cnt = run.ws.tensor[256:256 + 4 * 8].view(torch.int32)
+    assert torch.count_nonzero(cnt).item() == 0
+
+
+def test_page_id_outside_pool_is_reported_not_read(cuda_device):
+    case = W.decode_case(14, [100, 200], pending_append=False, poison=True)
+    case.block_table[1, 3] = case.num_pages + 1000
+    run = DecodeOnDevice(case, 0, cuda_device)
+    run.step()
+    torch.cuda.synchronize()
+    assert run.ws.status() == -7
+
+
+def test_length_beyond_table_is_clamped_and_reported(cuda_device):
+    case = W.decode_case(15, [100, 200], pending_append=False, poison=False)
+    ensure_built()
+    run = DecodeOnDevice(case, 0, cuda_device)
+    run.seq_lens = i32([100, case.max_pages * 16 + 50], cuda_device)
+    run.step()
+    torch.cuda.synchronize()
+    assert run.ws.status() == -7
+
+
+def test_workspace_too_small_is_rejected(cuda_device):
+    case = W.decode_case(16, [100, 200], pending_append=False)
+    run = DecodeOnDevice(case, 0, cuda_device)
+    run.ws = pkv.Workspace(512, cuda_device)
+    with pytest.raises(pkv.PkvError) as e:
+        run.step()
+    assert e.value.code == -4
