@@ -184,8 +184,12 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
     }
   }
 
+  // Only min(gridDim.x, T) CTAs take a share, so that every share is non-empty
+  // and the CTAs between the first and last holder of a (request, KV head) all
+  // hold a piece of it.
   const long long T = pref[batch];
-  const int G = gridDim.x;
+  const int G = static_cast<int>(T < gridDim.x ? T : gridDim.x);
+  if (static_cast<int>(blockIdx.x) >= G) return;
   const long long lo = share_lo(blockIdx.x, T, G);
   const long long hi = share_lo(blockIdx.x + 1, T, G);
   if (lo >= hi) return;
