@@ -191,6 +191,42 @@ int pkv_prefill_chunk_attn(const void* q, const void* k_pages, const void* v_pag
                            float scale, pkv_stream_t stream, const pkv_cache_desc* desc, int32_t max_pages_per_seq,
                            int32_t max_q_len, void* workspace, size_t workspace_bytes);
 
+/*
+ * pkv_decode_attn_noalloc -- pkv_decode_attn without a caller-provided workspace.
+ *
+ * The source pages have no counterpart to this call: it exists for callers
+ * that may not allocate device memory where they run decode attention (for
+ * example a plug-in inside a host runtime that owns all device memory through
+ * its own pool, or a serving loop that reserves memory once at start-up and
+ * must not allocate, or implicitly synchronise, afterwards). The caller still
+ * passes q, the pools, the block table, the lengths and out, with the same
+ * meaning and layout as for pkv_decode_attn; the split-KV scratch comes from a
+ * fixed array inside the library instead of a workspace.
+ *
+ *  - The scratch is one device array of PKV_NOALLOC_SCRATCH_BYTES (1 MiB).
+ *    Every GPU that loads the library holds it until the process exits. The
+ *    call itself allocates and frees nothing.
+ *  - Limit: batch <= PKV_NOALLOC_MAX_BATCH (256), and the scratch must cover
+ *    the device's split partials (it does for up to ~240 SMs; a GB300 has 152).
+ *    Larger requests return PKV_ERR_WORKSPACE_TOO_SMALL without launching.
+ *  - The first call on a device looks up the array's device address (a
+ *    one-time set-up); make that first call before any CUDA-graph capture.
+ *  - Every call uses the same array and it keeps the previous call's
+ *    contents; each call zeroes the status word and the split counters on
+ *    `stream` before its kernel. Calls whose kernels overlap on the GPU (on
+ *    different streams, or in parallel graph branches) race on the array:
+ *    issue them in order on one stream.
+ *  - Device-side errors (a page id outside the pool, a length beyond the block
+ *    table) are skipped as in pkv_decode_attn but not reported: the status
+ *    word lives in the library's array and no call reads it back.
+ */
+#define PKV_NOALLOC_SCRATCH_BYTES (1u << 20)
+#define PKV_NOALLOC_MAX_BATCH 256
+
+int pkv_decode_attn_noalloc(const void* q, const void* k_pages, const void* v_pages, const int32_t* block_table,
+                            const int32_t* seq_lens, void* out, float scale, pkv_stream_t stream,
+                            const pkv_cache_desc* desc, int32_t batch, int32_t max_pages_per_seq);
+
 #ifdef __cplusplus
 }
 #endif

@@ -32,6 +32,7 @@ ERRORS = {
 __all__ = [
     "PkvError", "desc", "Workspace", "append", "decode_attn", "prefill_chunk_attn",
     "decode_workspace_bytes", "prefill_workspace_bytes", "workspace_init", "read_status", "status_string",
+    "decode_attn_noalloc",
 ]
 
 
@@ -196,3 +197,29 @@ def prefill_chunk_attn(q, k_pages, v_pages, block_table, prefix_lens, cu_q_lens,
                                             _stream(stream), ctypes.byref(d), block_table.shape[1], int(max_q_len),
                                             _ptr(ws), ws.numel())
     _check(rc, "pkv_prefill_chunk_attn")
+
+
+def decode_attn_noalloc(q, k_pages, v_pages, block_table, seq_lens, out, scale: float, stream=None):
+    """decode_attn without a workspace, for callers that may not allocate device memory.
+
+    The split-KV scratch is a fixed 1 MiB array inside the library (batch <= 256).
+    Calls share that array: run them in order on one stream, never overlapping on
+    the GPU. Make the first call on a device before any CUDA-graph capture.
+    """
+    import torch
+
+    _need(k_pages, torch.bfloat16, "k_pages")
+    dev = k_pages.device
+    _need(v_pages, torch.bfloat16, "v_pages", dev)
+    _need(q, torch.bfloat16, "q", dev)
+    _need(out, torch.bfloat16, "out", dev)
+    _need(block_table, torch.int32, "block_table", dev)
+    _need(seq_lens, torch.int32, "seq_lens", dev)
+    B = q.shape[0]
+    if out.shape != q.shape or block_table.dim() != 2 or block_table.shape[0] != B or seq_lens.numel() != B:
+        raise ValueError("shape mismatch")
+    d = _desc_of(k_pages)
+    rc = _lib.load().pkv_decode_attn_noalloc(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
+                                             _ptr(seq_lens), _ptr(out), float(scale), _stream(stream),
+                                             ctypes.byref(d), B, block_table.shape[1])
+    _check(rc, "pkv_decode_attn_noalloc")
