@@ -19,6 +19,8 @@ __global__ void __launch_bounds__(256) append_kernel(const uint4* __restrict__ k
                                                      const int* __restrict__ slot_mapping, int n_tokens,
                                                      uint4* __restrict__ k_pages, uint4* __restrict__ v_pages,
                                                      int num_pages, int* status) {
+  grid_dependency_wait();
+  allow_dependents();
   const long long total = static_cast<long long>(n_tokens) * kChunksPerToken;
   for (long long u = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; u < total;
        u += static_cast<long long>(gridDim.x) * blockDim.x) {
@@ -50,10 +52,11 @@ int launch_append(const void* k_new, const void* v_new, const int32_t* slot_mapp
   long long blocks = (units + 255) / 256;
   const long long cap = static_cast<long long>(num_sms) * 8;
   if (blocks > cap) blocks = cap;
-  append_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-      static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slot_mapping, n_tokens,
-      static_cast<uint4*>(k_pages), static_cast<uint4*>(v_pages), num_pages, status);
-  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  const cudaError_t e = launch_pdl(append_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream,
+                                   static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slot_mapping,
+                                   n_tokens, static_cast<uint4*>(k_pages), static_cast<uint4*>(v_pages), num_pages,
+                                   status);
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 }  // namespace pkv

@@ -36,23 +36,40 @@
 
 namespace pkv {
 
-constexpr int kDecWarps = 4;
-constexpr int kDecThreads = kDecWarps * 32;
-constexpr int kDecRing = 3;
-constexpr int kDecCtasPerSm = 2;
+// Launch shape (compile-time; the defaults are the tuned configuration).
+#ifndef PKV_DEC_CONSUMERS
+#define PKV_DEC_CONSUMERS 4
+#endif
+#ifndef PKV_DEC_RING
+#define PKV_DEC_RING 3
+#endif
+#ifndef PKV_DEC_CTAS_PER_SM
+#define PKV_DEC_CTAS_PER_SM 2
+#endif
+constexpr int kCons = PKV_DEC_CONSUMERS;         // consumer warps; one more warp produces
+constexpr int kConsThreads = kCons * 32;
+constexpr int kDecThreads = kConsThreads + 32;
+constexpr int kDecRing = PKV_DEC_RING;           // stages per consumer warp
+constexpr int kDecCtasPerSm = PKV_DEC_CTAS_PER_SM;
+constexpr int kStages = kCons * kDecRing;
+static_assert(kHeadDim % kConsThreads == 0 || kConsThreads % kHeadDim == 0, "merge maps threads to head dims");
+constexpr int kDimsPerThread = kConsThreads >= kHeadDim ? 1 : kHeadDim / kConsThreads;  // in the merges
+constexpr int kMergeGroups = kConsThreads >= kHeadDim ? kConsThreads / kHeadDim : 1;  // record groups in the split merge
 constexpr int kStageBytes = 2 * kTileBytes;  // K tile + V tile of one (page, KV head)
 constexpr int kRec = kHeadDim + 4;           // floats per query-head record: m, l, pad, pad, o[128]
 constexpr int kPieceFloats = kGroup * kRec;  // a partial record of one piece (both query heads)
-constexpr int kMaxDecodeBatch = 2048;
+constexpr int kMaxDecodeBatch = 1024;
+constexpr int kMaxGrid = 2048;               // partial-record slots are sized for this many CTAs
 constexpr unsigned kFull = 0xffffffffu;
 
-constexpr int kSmemRing = kDecWarps * kDecRing * kStageBytes;
-constexpr int kSmemBars = kDecWarps * kDecRing * 8;
-constexpr int kMergeFloats = kDecWarps * kGroup * kRec;  // one buffer of warp records
-constexpr int kSmemMerge = 2 * kMergeFloats * 4;         // double-buffered by piece parity
-constexpr int kSmemPbuf = kDecWarps * kPageSize * 4 * 4; // per warp: [16 tokens][p0, p0, p1, p1]
-constexpr int kSmemFlag = 16;
-constexpr int kSmemFixed = kSmemRing + kSmemBars + kSmemMerge + kSmemPbuf + kSmemFlag;
+constexpr int kSmemRing = kStages * kStageBytes;
+constexpr int kSmemBars = 2 * kStages * 8;                 // full + empty barrier per stage
+constexpr int kMergeFloats = kCons * kPieceFloats;         // one record per consumer warp
+constexpr int kSmemMerge = kMergeFloats * 4;
+constexpr int kSmemPbuf = kCons * kPageSize * 4 * 4;       // per warp: [16 tokens][p0, p0, p1, p1]
+constexpr int kSmemSplit = kCons * 2 * 4;                  // per consumer warp: running max of both heads
+constexpr int kSmemMisc = 16 + ((kCons * 4 + 15) / 16) * 16;  // flag words + producer's per-consumer counts
+constexpr int kSmemFixed = kSmemRing + kSmemBars + kSmemMerge + kSmemPbuf + kSmemSplit + kSmemMisc;
 
 static size_t decode_smem_bytes(int batch) { return kSmemFixed + static_cast<size_t>(2 * batch + 1) * 4; }
 
@@ -129,14 +146,35 @@ __device__ __forceinline__ void pv_tokens(uint32_t vrow0, uint32_t prow0, int t0
   }
 }
 
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsThreads) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Request b holding flattened index f: the largest b with pref[b] <= f.
+__device__ __forceinline__ int request_of(long long f, const int* pref, int batch) {
+  int lo_b = 0, hi_b = batch - 1;
+  while (lo_b < hi_b) {
+    const int mid = (lo_b + hi_b + 1) >> 1;
+    if (pref[mid] <= f) lo_b = mid; else hi_b = mid - 1;
+  }
+  return lo_b;
+}
+
 __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(const DecodeArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* ring = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kSmemRing);
-  float* merge = reinterpret_cast<float*>(smem + kSmemRing + kSmemBars);
-  float* pbuf = merge + 2 * kMergeFloats;
-  int* flag = reinterpret_cast<int*>(pbuf + kDecWarps * kPageSize * 4);
-  int* pref = flag + kSmemFlag / 4;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kSmemRing);
+  uint64_t* empty = full + kStages;
+  float* merge = reinterpret_cast<float*>(empty + kStages);
+  float* pbuf = merge + kMergeFloats;
+  float* split = pbuf + kCons * kPageSize * 4;
+  int* flag = reinterpret_cast<int*>(split + kCons * 2);
+  int* sbase = flag + 4;
+  int* pref = reinterpret_cast<int*>(reinterpret_cast<unsigned char*>(flag) + kSmemMisc);
   int* sl = pref + a.batch + 1;
 
   const int tid = threadIdx.x;
@@ -144,9 +182,15 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
   const int lane = tid & 31;
   const int batch = a.batch;
 
-  if (tid < kDecWarps * kDecRing) mbar_init(&bars[tid], 1);
+  if (tid < kStages) {
+    mbar_init(&full[tid], 1);
+    mbar_init(&empty[tid], 1);
+  }
+  if (tid < kCons) sbase[tid] = 0;
+  grid_dependency_wait();  // every argument buffer may come from the previous kernel in the stream
+  allow_dependents();
 
-  // seq lens (clamped) and the exclusive prefix of page-head triples
+  // seq lens (clamped) and the exclusive prefix of (KV head, page) pairs per request
   if (warp == 0) {
     int carry = 0;
     const int cap = a.max_pages * kPageSize;
@@ -192,67 +236,69 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
   if (static_cast<int>(blockIdx.x) >= G) return;
   const long long lo = share_lo(blockIdx.x, T, G);
   const long long hi = share_lo(blockIdx.x + 1, T, G);
-  if (lo >= hi) return;
 
-  unsigned char* my_ring = ring + warp * kDecRing * kStageBytes;
-  uint64_t* my_bars = bars + warp * kDecRing;
-
-  // ---------------------------------------------------------------- producer (lane 0)
-  // Walks this warp's page sequence (pages p0 + warp, p0 + warp + 4, ... of each
-  // piece, pieces in order) kDecRing elements ahead of the consumer.
-  Piece pp{};
-  int pp_page = 0;
-  bool pp_valid = false;
-  int pp_id = 0;  // block-table entry of the element the producer points at
-  int issued = 0;
-  uint64_t policy = 0;
-
-  auto pp_normalize = [&]() {
-    while (pp_valid && pp_page >= pp.p1) {
-      pp_valid = find_piece(pp.fend, hi, pref, batch, pp);
-      pp_page = pp.p0 + warp;
-    }
-  };
-  auto pp_load_id = [&]() {
-    if (pp_valid) pp_id = __ldg(a.block_table + static_cast<size_t>(pp.b) * a.max_pages + pp_page);
-  };
-  auto pp_issue = [&](int slot, int id, int h) {
-    if (id < 0 || id >= a.num_pages) {
-      set_status(a.status, PKV_ERR_OUT_OF_BOUNDS);
-      id = 0;
-    }
-    const size_t off = (static_cast<size_t>(id) * kKVHeads + h) * (kTileBytes / 2);
-    unsigned char* dst = my_ring + slot * kStageBytes;
-    mbar_arrive_expect_tx(&my_bars[slot], kStageBytes);
-    bulk_g2s_hint(dst, a.k_pages + off, kTileBytes, &my_bars[slot], policy);
-    bulk_g2s_hint(dst + kTileBytes, a.v_pages + off, kTileBytes, &my_bars[slot], policy);
-    ++issued;
-  };
-
-  if (lane == 0) {
-    policy = policy_evict_first();
-    pp_valid = find_piece(lo, hi, pref, batch, pp);
-    pp_page = pp.p0 + warp;
-    pp_normalize();
-    int ids[kDecRing], hs[kDecRing];
-    int n0 = 0;
-#pragma unroll
-    for (int r = 0; r < kDecRing; ++r) {
-      if (pp_valid) {
-        ids[r] = __ldg(a.block_table + static_cast<size_t>(pp.b) * a.max_pages + pp_page);
-        hs[r] = pp.h;
-        ++n0;
-        pp_page += kDecWarps;
-        pp_normalize();
+  // ============================================================== producer warp
+  // Walks the share in order, 32 flattened indices at a time (one per lane:
+  // request, KV head, page and block-table entry decoded in parallel), and
+  // fills each page into the next stage of the consumer that will read it:
+  // within a piece, page p0 + i goes to consumer i % kCons.
+  if (warp == kCons) {
+    const uint64_t policy = policy_evict_first();
+    long long piece_start = lo;
+    int piece_len = 0;
+    bool pfail = false;
+    for (long long f0 = lo; f0 < hi && !pfail; f0 += 32) {
+      const long long f = f0 + lane;
+      int hh = 0, id = 0, seg = 0;
+      if (f < hi) {
+        const int b = request_of(f, pref, batch);
+        const int np = (pref[b + 1] - pref[b]) / kKVHeads;
+        const int off = static_cast<int>(f - pref[b]);
+        hh = off / np;
+        const int p = off % np;
+        seg = pref[b] + hh * np;
+        id = __ldg(a.block_table + static_cast<size_t>(b) * a.max_pages + p);
       }
+      const int n = static_cast<int>(hi - f0 < 32 ? hi - f0 : 32);
+      for (int i = 0; i < n; ++i) {
+        const int h_i = __shfl_sync(kFull, hh, i);
+        int id_i = __shfl_sync(kFull, id, i);
+        const int seg_i = __shfl_sync(kFull, seg, i);
+        if (lane == 0 && !pfail) {
+          const long long pstart = seg_i > lo ? seg_i : lo;
+          if (pstart != piece_start) {
+            for (int c = 0; c < kCons; ++c) sbase[c] += piece_len > c ? (piece_len - c + kCons - 1) / kCons : 0;
+            piece_start = pstart;
+            piece_len = 0;
+          }
+          const int prel = static_cast<int>(f0 + i - piece_start);
+          piece_len = prel + 1;
+          const int c = prel % kCons;
+          const int k = sbase[c] + prel / kCons;
+          const int slot = c * kDecRing + k % kDecRing;
+          const int use = k / kDecRing;
+          if (use > 0 && !mbar_wait_bounded(&empty[slot], static_cast<uint32_t>(use - 1) & 1u)) {
+            set_status(a.status, PKV_ERR_DEVICE_TIMEOUT);
+            pfail = true;
+          } else {
+            if (id_i < 0 || id_i >= a.num_pages) {
+              set_status(a.status, PKV_ERR_OUT_OF_BOUNDS);
+              id_i = 0;
+            }
+            const size_t off = (static_cast<size_t>(id_i) * kKVHeads + h_i) * (kTileBytes / 2);
+            unsigned char* dst = ring + slot * kStageBytes;
+            mbar_arrive_expect_tx(&full[slot], kStageBytes);
+            bulk_g2s_hint(dst, a.k_pages + off, kTileBytes, &full[slot], policy);
+            bulk_g2s_hint(dst + kTileBytes, a.v_pages + off, kTileBytes, &full[slot], policy);
+          }
+        }
+      }
+      pfail = __shfl_sync(kFull, pfail ? 1 : 0, 0) != 0;
     }
-    pp_load_id();
-#pragma unroll
-    for (int r = 0; r < kDecRing; ++r)
-      if (r < n0) pp_issue(r, ids[r], hs[r]);
+    return;
   }
 
-  // ---------------------------------------------------------------- consumer
+  // ============================================================== consumer warps
   const int qq = lane & 3;         // quarter of the row for the score pass
   const int tp = (lane >> 2) & 1;  // token parity: rotates the chunk order to avoid bank conflicts
   const int head_mine = qq & 1;    // query head whose score this lane ends up holding
@@ -261,10 +307,8 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
   const int dl = lane & 15;        // dims dl*8 .. dl*8+7 for the V pass
   const uint32_t pb = smem_u32(pbuf + warp * kPageSize * 4);
 
-  int k = 0;         // elements of this warp's sequence visited so far
-  int consumed = 0;  // elements whose copy completed
+  int k = 0;  // pages of this warp's sequence visited so far
   bool failed = false;
-  int piece_idx = 0;
   long long f = lo;
   Piece pc;
   while (find_piece(f, hi, pref, batch, pc)) {
@@ -275,7 +319,8 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
     float2 q2[4][4][2];
 #pragma unroll
     for (int i = 0; i < kGroup; ++i) {
-      const uint4* qrow = reinterpret_cast<const uint4*>(a.q + (static_cast<size_t>(b) * kQHeads + h * kGroup + i) * kHeadDim);
+      const uint4* qrow =
+          reinterpret_cast<const uint4*>(a.q + (static_cast<size_t>(b) * kQHeads + h * kGroup + i) * kHeadDim);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const uint4 u = __ldg(qrow + qq + 4 * (j ^ tp));
@@ -295,19 +340,18 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
 #pragma unroll
       for (int e = 0; e < 4; ++e) o[i][e] = make_float2(0.f, 0.f);
 
-    for (int p = pc.p0 + warp; p < pc.p1; p += kDecWarps) {
-      const int slot = k % kDecRing;
+    for (int p = pc.p0 + warp; p < pc.p1; p += kCons) {
+      const int slot = warp * kDecRing + k % kDecRing;
       const uint32_t parity = static_cast<uint32_t>(k / kDecRing) & 1u;
       if (!failed) {
-        const bool ok = mbar_wait_bounded(&my_bars[slot], parity);
+        const bool ok = mbar_wait_bounded(&full[slot], parity);
         failed = __any_sync(kFull, !ok);
         if (failed && lane == 0) set_status(a.status, PKV_ERR_DEVICE_TIMEOUT);
-        if (!failed) ++consumed;
       }
       if (!failed) {
         const int rem = sl[b] - p * kPageSize;
         const int n_valid = rem < kPageSize ? rem : kPageSize;
-        const uint32_t kt = smem_u32(my_ring + slot * kStageBytes);
+        const uint32_t kt = smem_u32(ring + slot * kStageBytes);
         const uint32_t vt = kt + kTileBytes;
 
         // ---- scores: lanes (token group of 4) x (quarter of the row), two passes of 8 tokens
@@ -378,12 +422,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
         else pv_tokens<true>(vrow0, prow0, hf * 8, n_valid, o);
       }
       __syncwarp();  // the stage and the p buffer are free again
-      if (lane == 0 && !failed && pp_valid) {
-        pp_issue(slot, pp_id, pp.h);
-        pp_page += kDecWarps;
-        pp_normalize();
-        pp_load_id();
-      }
+      if (lane == 0 && !failed) mbar_arrive(&empty[slot]);
       ++k;
     }
 
@@ -404,8 +443,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
     const float l0 = head_mine ? lother : lh;
     const float l1 = head_mine ? lh : lother;
 
-    float* mbuf = merge + (piece_idx & 1) * kMergeFloats;
-    float* mw = mbuf + warp * kPieceFloats;
+    float* mw = merge + warp * kPieceFloats;
     if (lane < 16) {
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
@@ -420,91 +458,179 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
       mw[kRec] = mrun.y;
       mw[kRec + 1] = l1;
     }
-    __syncthreads();
+    consumer_sync();
 
-    // ---- CTA merge of the 4 warp records: thread tid owns dim tid of both heads
-    float M[2], L[2], O[2];
+    // ---- CTA merge of the warp records: thread tid owns dims tid, tid + kConsThreads, ... of both heads
+    float M[2], L[2], O[2][kDimsPerThread];
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       float m = -CUDART_INF_F;
 #pragma unroll
-      for (int w = 0; w < kDecWarps; ++w) m = fmaxf(m, mbuf[w * kPieceFloats + i * kRec]);
-      float l = 0.f, acc = 0.f;
+      for (int w = 0; w < kCons; ++w) m = fmaxf(m, merge[w * kPieceFloats + i * kRec]);
+      float l = 0.f;
 #pragma unroll
-      for (int w = 0; w < kDecWarps; ++w) {
-        const float* r = mbuf + w * kPieceFloats + i * kRec;
+      for (int e = 0; e < kDimsPerThread; ++e) O[i][e] = 0.f;
+#pragma unroll
+      for (int w = 0; w < kCons; ++w) {
+        const float* r = merge + w * kPieceFloats + i * kRec;
         const float sc = ex2(r[0] - m);
         l += r[1] * sc;
-        acc += r[4 + tid] * sc;
+#pragma unroll
+        for (int e = 0; e < kDimsPerThread; ++e) {
+          const int d = (tid + e * kConsThreads) & (kHeadDim - 1);
+          O[i][e] += r[4 + d] * sc;
+        }
       }
       M[i] = m;
       L[i] = l;
-      O[i] = acc;
     }
+    const bool owns_dims = tid < kHeadDim;  // threads past the first 128 only help in the split merge
     const bool complete = (pc.p0 == 0 && pc.p1 == pc.np);
+    __nv_bfloat16* orow = a.out + (static_cast<size_t>(b) * kQHeads + h * kGroup) * kHeadDim;
     if (complete) {
+      if (owns_dims) {
 #pragma unroll
-      for (int i = 0; i < 2; ++i)
-        a.out[(static_cast<size_t>(b) * kQHeads + h * kGroup + i) * kHeadDim + tid] = __float2bfloat16_rn(O[i] / L[i]);
+        for (int e = 0; e < kDimsPerThread; ++e) {
+          const int d = tid + e * kConsThreads;
+          orow[d] = __float2bfloat16_rn(O[0][e] / L[0]);
+          orow[kHeadDim + d] = __float2bfloat16_rn(O[1][e] / L[1]);
+        }
+      }
     } else {
       const long long fseg = pref[b] + static_cast<long long>(h) * pc.np;
       const int cfirst = cta_of(fseg, T, G);
       const int clast = cta_of(fseg + pc.np - 1, T, G);
+      const bool first_has_two = share_lo(cfirst, T, G) < fseg;  // cfirst's piece is its second record
       const int my_slot = 2 * blockIdx.x + (pc.fstart == lo ? 0 : 1);
       float* rec = a.partials + static_cast<size_t>(my_slot) * kPieceFloats;
+      if (owns_dims) {
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        rec[i * kRec + 4 + tid] = O[i];
-        if (tid == 0) {
-          rec[i * kRec] = M[i];
-          rec[i * kRec + 1] = L[i];
+        for (int e = 0; e < kDimsPerThread; ++e) {
+          const int d = tid + e * kConsThreads;
+          rec[4 + d] = O[0][e];
+          rec[kRec + 4 + d] = O[1][e];
         }
       }
-      __syncthreads();
+      if (tid == 0) {
+        rec[0] = M[0];
+        rec[1] = L[0];
+        rec[kRec] = M[1];
+        rec[kRec + 1] = L[1];
+      }
+      consumer_sync();
       if (tid == 0) {
         __threadfence();
         const int old = atomicAdd(a.counters + b * kKVHeads + h, 1);
         flag[0] = (old == clast - cfirst) ? 1 : 0;
       }
-      __syncthreads();
+      consumer_sync();
       if (flag[0]) {
+        // This CTA holds the last piece: merge all partial records of (b, h).
         __threadfence();
+        const int n = clast - cfirst + 1;
+        auto rec_of = [&](int t) {
+          const int c = cfirst + t;
+          return a.partials + static_cast<size_t>(2 * c + ((t == 0 && first_has_two) ? 1 : 0)) * kPieceFloats;
+        };
+        // global max of each head: strided over threads, then over warps
+        float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F;
+        for (int t = tid; t < n; t += kConsThreads) {
+          const float* r = rec_of(t);
+          m0 = fmaxf(m0, __ldcg(r));
+          m1 = fmaxf(m1, __ldcg(r + kRec));
+        }
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          float m = -CUDART_INF_F;
-          for (int c = cfirst; c <= clast; ++c) {
-            const int sidx = 2 * c + ((c == cfirst && share_lo(c, T, G) < fseg) ? 1 : 0);
-            m = fmaxf(m, __ldcg(a.partials + static_cast<size_t>(sidx) * kPieceFloats + i * kRec));
+        for (int o2 = 16; o2 > 0; o2 >>= 1) {
+          m0 = fmaxf(m0, __shfl_xor_sync(kFull, m0, o2));
+          m1 = fmaxf(m1, __shfl_xor_sync(kFull, m1, o2));
+        }
+        if (lane == 0) {
+          split[warp * 2] = m0;
+          split[warp * 2 + 1] = m1;
+        }
+        consumer_sync();
+#pragma unroll
+        for (int w = 0; w < kCons; ++w) {
+          m0 = fmaxf(m0, split[w * 2]);
+          m1 = fmaxf(m1, split[w * 2 + 1]);
+        }
+        // weighted sums: kMergeGroups groups take alternate records, 4 records in flight each
+        const int grp = kConsThreads >= kHeadDim ? tid / kHeadDim : 0;
+        const int dbase = kConsThreads >= kHeadDim ? tid % kHeadDim : tid;
+        float acc0[kDimsPerThread], acc1[kDimsPerThread];
+#pragma unroll
+        for (int e = 0; e < kDimsPerThread; ++e) acc0[e] = acc1[e] = 0.f;
+        float lsum0 = 0.f, lsum1 = 0.f;
+        for (int t0 = grp; t0 < n; t0 += 4 * kMergeGroups) {
+          float mm0[4], mm1[4], ll0[4], ll1[4], v0[4][kDimsPerThread], v1[4][kDimsPerThread];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int t = t0 + u * kMergeGroups;
+            const float* r = rec_of(t < n ? t : 0);
+            mm0[u] = t < n ? __ldcg(r) : -CUDART_INF_F;
+            ll0[u] = __ldcg(r + 1);
+            mm1[u] = t < n ? __ldcg(r + kRec) : -CUDART_INF_F;
+            ll1[u] = __ldcg(r + kRec + 1);
+#pragma unroll
+            for (int e = 0; e < kDimsPerThread; ++e) {
+              v0[u][e] = __ldcg(r + 4 + dbase + e * kConsThreads);
+              v1[u][e] = __ldcg(r + kRec + 4 + dbase + e * kConsThreads);
+            }
           }
-          float l = 0.f, acc = 0.f;
-          for (int c = cfirst; c <= clast; ++c) {
-            const int sidx = 2 * c + ((c == cfirst && share_lo(c, T, G) < fseg) ? 1 : 0);
-            const float* r = a.partials + static_cast<size_t>(sidx) * kPieceFloats + i * kRec;
-            const float sc = ex2(__ldcg(r) - m);
-            l += __ldcg(r + 1) * sc;
-            acc += __ldcg(r + 4 + tid) * sc;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float w0 = ex2(mm0[u] - m0), w1 = ex2(mm1[u] - m1);  // 0 for t >= n
+            lsum0 += ll0[u] * w0;
+            lsum1 += ll1[u] * w1;
+#pragma unroll
+            for (int e = 0; e < kDimsPerThread; ++e) {
+              acc0[e] += v0[u][e] * w0;
+              acc1[e] += v1[u][e] * w1;
+            }
           }
-          a.out[(static_cast<size_t>(b) * kQHeads + h * kGroup + i) * kHeadDim + tid] = __float2bfloat16_rn(acc / l);
+        }
+        if (kMergeGroups > 1) {  // fold the groups (o and l sums) through the (free) merge buffer
+          float* fold = merge;
+          float* lfold = merge + (kMergeGroups - 1) * 2 * kHeadDim;
+          if (grp > 0) {
+            fold[(grp - 1) * 2 * kHeadDim + dbase] = acc0[0];
+            fold[(grp - 1) * 2 * kHeadDim + kHeadDim + dbase] = acc1[0];
+            if (dbase == 0) {
+              lfold[(grp - 1) * 2] = lsum0;
+              lfold[(grp - 1) * 2 + 1] = lsum1;
+            }
+          }
+          consumer_sync();
+          if (grp == 0) {
+            for (int g = 1; g < kMergeGroups; ++g) {
+              acc0[0] += fold[(g - 1) * 2 * kHeadDim + dbase];
+              acc1[0] += fold[(g - 1) * 2 * kHeadDim + kHeadDim + dbase];
+              lsum0 += lfold[(g - 1) * 2];
+              lsum1 += lfold[(g - 1) * 2 + 1];
+            }
+          }
+        }
+        if (grp == 0) {
+#pragma unroll
+          for (int e = 0; e < kDimsPerThread; ++e) {
+            const int d = dbase + e * kConsThreads;
+            orow[d] = __float2bfloat16_rn(acc0[e] / lsum0);
+            orow[kHeadDim + d] = __float2bfloat16_rn(acc1[e] / lsum1);
+          }
         }
         if (tid == 0) a.counters[b * kKVHeads + h] = 0;
       }
     }
+    consumer_sync();  // merge buffer, flag and split staging are free for the next piece
     f = pc.fend;
-    ++piece_idx;
-  }
-
-  // copies still in flight after a timeout: wait for them (bounded) before the CTA exits
-  if (failed && lane == 0) {
-    for (int e = consumed; e < issued; ++e) {
-      if (!mbar_wait_bounded(&my_bars[e % kDecRing], static_cast<uint32_t>(e / kDecRing) & 1u)) break;
-    }
   }
 }
 
 size_t decode_workspace_bytes(int32_t batch, int num_sms) {
   size_t off = PKV_STATUS_BYTES;
   off += (static_cast<size_t>(batch) * kKVHeads * 4 + 255) / 256 * 256;
-  off += static_cast<size_t>(2) * kDecCtasPerSm * num_sms * kPieceFloats * 4;
+  const int grid = kDecCtasPerSm * num_sms < kMaxGrid ? kDecCtasPerSm * num_sms : kMaxGrid;
+  off += static_cast<size_t>(2) * grid * kPieceFloats * 4;
   return off;
 }
 
@@ -544,8 +670,9 @@ int launch_decode(const void* q, const void* k_pages, const void* v_pages, const
   a.counters = reinterpret_cast<int*>(ws + PKV_STATUS_BYTES);
   a.partials = reinterpret_cast<float*>(ws + PKV_STATUS_BYTES +
                                         (static_cast<size_t>(batch) * kKVHeads * 4 + 255) / 256 * 256);
-  decode_kernel<<<num_sms * occ, kDecThreads, smem, stream>>>(a);
-  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  const int grid = num_sms * occ < kMaxGrid ? num_sms * occ : kMaxGrid;
+  return launch_pdl(decode_kernel, dim3(grid), dim3(kDecThreads), smem, stream, a) == cudaSuccess ? PKV_OK
+                                                                                                 : PKV_ERR_CUDA;
 }
 
 }  // namespace pkv

@@ -37,6 +37,33 @@ __device__ __forceinline__ void set_status(int* status, int code) {
 }
 
 // ----------------------------------------------------------------------------
+// programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start while its predecessor in the stream is finishing.
+// grid_dependency_wait() blocks until the predecessor grid has completed and
+// its memory is visible; every kernel here calls it before touching any
+// argument buffer. allow_dependents() lets the successor start launching.
+// Both are no-ops for a normal launch.
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
+// Launch with programmatic stream serialisation allowed.
+template <typename Kernel, typename... Args>
+inline cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// ----------------------------------------------------------------------------
 // shared-memory addresses and mbarriers
 // ----------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
