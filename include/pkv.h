@@ -162,7 +162,7 @@ int pkv_decode_attn(const void* q, const void* k_pages, const void* v_pages, con
                     size_t workspace_bytes);
 
 /*
- * Workspace bytes pkv_prefill_chunk_attn needs (status header only at present).
+ * Workspace bytes pkv_prefill_chunk_attn needs (the status header).
  */
 size_t pkv_prefill_workspace_bytes(const pkv_cache_desc* desc, int32_t num_seqs, int32_t max_q_len);
 
@@ -177,19 +177,25 @@ size_t pkv_prefill_workspace_bytes(const pkv_cache_desc* desc, int32_t num_seqs,
  * follows prefix_lens[n] cached tokens, and row i of the chunk (absolute
  * position prefix_lens[n] + i) attends keys 0 .. prefix_lens[n] + i of the
  * request (bottom-right causal alignment). The chunk's own K/V rows must
- * already be in the pool (pkv_append first).
+ * already be in the pool (pkv_append first). bf16 inputs, fp32 accumulation on
+ * the tensor cores, the softmax weights rounded to bf16 before they multiply
+ * V, bf16 output.
  *
- *  q, out:       bf16 [total_q][num_q_heads][head_dim], total_q = cu_q_lens[num_seqs]
+ *  q, out:       bf16 [total_q][num_q_heads][head_dim]
  *  block_table:  int32 [num_seqs][max_pages_per_seq]
  *  prefix_lens:  int32 [num_seqs]
- *  cu_q_lens:    int32 [num_seqs + 1], cu_q_lens[0] = 0, non-decreasing
- *  max_q_len:    host-side upper bound on any chunk length (sizes the grid)
- *  workspace:    >= pkv_prefill_workspace_bytes(...)
+ *  cu_q_lens:    int32 [num_seqs + 1], cu_q_lens[0] = 0, non-decreasing,
+ *                cu_q_lens[num_seqs] <= total_q
+ *  total_q:      rows of q and out (host value; bounds every access)
+ *  max_q_len:    host-side upper bound on any chunk length (sizes the grid;
+ *                rows of longer chunks are not computed)
+ *  workspace:    >= pkv_prefill_workspace_bytes(...) (status word)
+ * Limits: num_pages * num_kv_heads * page_size < 2^31 rows per pool.
  */
 int pkv_prefill_chunk_attn(const void* q, const void* k_pages, const void* v_pages, const int32_t* block_table,
-                           const int32_t* prefix_lens, const int32_t* cu_q_lens, int32_t num_seqs, void* out,
-                           float scale, pkv_stream_t stream, const pkv_cache_desc* desc, int32_t max_pages_per_seq,
-                           int32_t max_q_len, void* workspace, size_t workspace_bytes);
+                           const int32_t* prefix_lens, const int32_t* cu_q_lens, int32_t num_seqs, int32_t total_q,
+                           void* out, float scale, pkv_stream_t stream, const pkv_cache_desc* desc,
+                           int32_t max_pages_per_seq, int32_t max_q_len, void* workspace, size_t workspace_bytes);
 
 /*
  * pkv_decode_attn_noalloc -- pkv_decode_attn without a caller-provided workspace.

@@ -193,9 +193,9 @@ def prefill_chunk_attn(q, k_pages, v_pages, block_table, prefix_lens, cu_q_lens,
     d = _desc_of(k_pages)
     ws = workspace.tensor
     rc = _lib.load().pkv_prefill_chunk_attn(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
-                                            _ptr(prefix_lens), _ptr(cu_q_lens), S, _ptr(out), float(scale),
-                                            _stream(stream), ctypes.byref(d), block_table.shape[1], int(max_q_len),
-                                            _ptr(ws), ws.numel())
+                                            _ptr(prefix_lens), _ptr(cu_q_lens), S, q.shape[0], _ptr(out),
+                                            float(scale), _stream(stream), ctypes.byref(d), block_table.shape[1],
+                                            int(max_q_len), _ptr(ws), ws.numel())
     _check(rc, "pkv_prefill_chunk_attn")
 
 

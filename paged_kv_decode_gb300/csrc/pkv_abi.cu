@@ -153,15 +153,18 @@ size_t pkv_prefill_workspace_bytes(const pkv_cache_desc* desc, int32_t num_seqs,
 }
 
 int pkv_prefill_chunk_attn(const void* q, const void* k_pages, const void* v_pages, const int32_t* block_table,
-                           const int32_t* prefix_lens, const int32_t* cu_q_lens, int32_t num_seqs, void* out,
-                           float scale, pkv_stream_t stream, const pkv_cache_desc* desc, int32_t max_pages_per_seq,
-                           int32_t max_q_len, void* workspace, size_t workspace_bytes) {
+                           const int32_t* prefix_lens, const int32_t* cu_q_lens, int32_t num_seqs, int32_t total_q,
+                           void* out, float scale, pkv_stream_t stream, const pkv_cache_desc* desc,
+                           int32_t max_pages_per_seq, int32_t max_q_len, void* workspace, size_t workspace_bytes) {
   int rc = check_desc(desc);
   if (rc != PKV_OK) return rc;
-  if (num_seqs < 0 || max_q_len < 0 || max_pages_per_seq < 1) return PKV_ERR_BAD_SHAPE;
+  if (num_seqs < 0 || total_q < 0 || max_q_len < 0 || max_pages_per_seq < 1) return PKV_ERR_BAD_SHAPE;
   if (!table_fits(num_seqs, max_pages_per_seq)) return PKV_ERR_BAD_SHAPE;
+  if (static_cast<long long>(desc->num_pages) * desc->num_kv_heads * desc->page_size >= (1LL << 31))
+    return PKV_ERR_UNSUPPORTED;
   if (workspace == nullptr) return PKV_ERR_NULL_ARG;
-  if (num_seqs == 0 || max_q_len == 0) return PKV_OK;
+  if (workspace_bytes < PKV_STATUS_BYTES) return PKV_ERR_WORKSPACE_TOO_SMALL;
+  if (num_seqs == 0 || max_q_len == 0 || total_q == 0) return PKV_OK;
   if (!q || !k_pages || !v_pages || !block_table || !prefix_lens || !cu_q_lens || !out) return PKV_ERR_NULL_ARG;
   if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(out) || !aligned16(workspace))
     return PKV_ERR_MISALIGNED;
@@ -169,8 +172,8 @@ int pkv_prefill_chunk_attn(const void* q, const void* k_pages, const void* v_pag
   rc = current_device(&sms);
   if (rc != PKV_OK) return rc;
   if (workspace_bytes < pkv::prefill_workspace_bytes(num_seqs, max_q_len, sms)) return PKV_ERR_WORKSPACE_TOO_SMALL;
-  return pkv::launch_prefill(q, k_pages, v_pages, block_table, prefix_lens, cu_q_lens, num_seqs, out, scale,
-                             max_pages_per_seq, max_q_len, desc->num_pages, workspace, sms,
+  return pkv::launch_prefill(q, k_pages, v_pages, block_table, prefix_lens, cu_q_lens, num_seqs, total_q, out, scale,
+                             max_pages_per_seq, max_q_len, desc->num_pages, workspace,
                              reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -1,0 +1,98 @@
+"""Chunked-prefill attention on the GPU (tcgen05 kernel) against the fp64 oracle.
+
+Small cases compare every output row; full-size chunks (4096 rows after 0,
+8192 or 32768 cached tokens) compare sampled rows (every 64th row, the last
+64 rows, all heads), which the oracle computes one by one. Bar as elsewhere:
+max |diff| <= 1e-2, mean |diff| <= 1e-3, relative L2 <= 1e-2.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_decode_gb300 as pkv
+from gpu_util import bits, ensure_built, i32
+from parity import assert_close, bf16_to_f64
+from paged_kv_decode_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+class PrefillOnDevice:
+    def __init__(self, case, dev, layer=0):
+        ensure_built()
+        self.case = case
+        self.q = case.q[layer].to(dev)
+        self.k_pages = case.k_pages[layer].to(dev)
+        self.v_pages = case.v_pages[layer].to(dev)
+        self.k_new = case.k_new[layer].to(dev)
+        self.v_new = case.v_new[layer].to(dev)
+        self.slots = i32(case.slot_mapping, dev)
+        self.block_table = i32(case.block_table, dev)
+        self.prefix = i32(case.prefix_lens, dev)
+        self.cu = i32(case.cu_q_lens, dev)
+        self.out = torch.full_like(self.q, float("nan"))
+        self.ws = pkv.Workspace(pkv.prefill_workspace_bytes(len(case.prefix_lens), int(case.q_lens.max())), dev)
+        self.max_q_len = int(case.q_lens.max())
+
+    def run(self):
+        pkv.append(self.k_new, self.v_new, self.slots, self.k_pages, self.v_pages, self.ws)
+        pkv.prefill_chunk_attn(self.q, self.k_pages, self.v_pages, self.block_table, self.prefix, self.cu, self.out,
+                               self.case.geom.scale, self.max_q_len, self.ws)
+        torch.cuda.synchronize()
+        return self.out
+
+    def oracle_pools(self):
+        c = self.case
+        return oracle.append(c.k_new[0], c.v_new[0], c.slot_mapping, c.k_pages[0], c.v_pages[0])
+
+
+def _check(case, dev, rows=None, what=""):
+    run = PrefillOnDevice(case, dev)
+    out = run.run()
+    kp, vp = run.oracle_pools()
+    assert np.array_equal(bits(run.k_pages), kp) and np.array_equal(bits(run.v_pages), vp)
+    want = oracle.prefill(case.q[0], kp, vp, case.block_table, case.prefix_lens, case.cu_q_lens, case.geom.scale,
+                          rows=rows)
+    got = bf16_to_f64(out)
+    got = got if rows is None else got[np.asarray(rows)]
+    assert_close(got, want, what)
+    assert run.ws.status() == 0
+    return run
+
+
+@pytest.mark.parametrize("prefix,qlen", [(0, 128), (0, 300), (5, 77), (130, 1), (16, 200), (1000, 257)])
+def test_small_chunks_all_rows(cuda_device, prefix, qlen):
+    case = W.prefill_case(40 + qlen, [prefix], [qlen], poison=True)
+    _check(case, cuda_device, what=f"P={prefix} L={qlen}")
+
+
+def test_several_requests_in_one_call(cuda_device):
+    case = W.prefill_case(41, [0, 33, 500], [129, 64, 250], poison=True)
+    _check(case, cuda_device, what="3 requests")
+
+
+def _sample_rows(total):
+    rows = list(range(0, total, 64)) + list(range(max(0, total - 64), total))
+    return sorted(set(rows))
+
+
+@pytest.mark.parametrize("prefix", [0, 8192, 32768])
+def test_full_chunk_sampled_rows(cuda_device, prefix):
+    case = W.prefill_case(42, [prefix], [W.PREFILL_CHUNK], poison=True)
+    _check(case, cuda_device, rows=_sample_rows(W.PREFILL_CHUNK), what=f"chunk 4096 after {prefix}")
+
+
+def test_causality_on_gpu(cuda_device):
+    # perturbing keys/values at positions after row i's limit leaves row i bit-identical
+    case = W.prefill_case(43, [40], [200], poison=False)
+    base = PrefillOnDevice(case, cuda_device).run().clone()
+    lim_row = 100  # rows <= 100 see keys <= 140
+    kn = case.k_new.clone()
+    vn = case.v_new.clone()
+    kn[0, lim_row + 1:] = -kn[0, lim_row + 1:]
+    vn[0, lim_row + 1:] = vn[0, lim_row + 1:] * 2
+    case.k_new, case.v_new = kn, vn
+    pert = PrefillOnDevice(case, cuda_device).run()
+    assert torch.equal(base[: lim_row + 1].view(torch.int16), pert[: lim_row + 1].view(torch.int16))
+    assert not torch.equal(base[lim_row + 1:].view(torch.int16), pert[lim_row + 1:].view(torch.int16))
