@@ -230,6 +230,82 @@ def time_decode_launches(step, reps):
     return float(np.mean(durs)), len(durs)
 
 
+class PrefillStep:
+    """Workload 4: one 4096-token chunk after `prefix` cached tokens plus 15 concurrent decode requests."""
+
+    def __init__(self, device, prefix, seed=4):
+        import torch
+
+        import paged_kv_decode_gb300 as pkv
+        from paged_kv_decode_gb300 import workloads as W
+
+        self.torch, self.pkv = torch, pkv
+        c = W.prefill_case(seed, [prefix], [W.PREFILL_CHUNK], dec_seq_lens=W.mixed_decode_lens(seed), device=device,
+                           poison=True)
+        self.case = c
+        i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)
+        self.q, self.k_new, self.v_new = c.q[0], c.k_new[0], c.v_new[0]
+        self.k_pages, self.v_pages = c.k_pages[0], c.v_pages[0]
+        self.slots, self.bt = i32(c.slot_mapping), i32(c.block_table)
+        self.prefix, self.cu = i32(c.prefix_lens), i32(c.cu_q_lens)
+        self.out = torch.empty_like(self.q)
+        self.dq, self.dk, self.dv = c.dec_q[0], c.dec_k_new[0], c.dec_v_new[0]
+        self.dslots, self.dbt, self.dlens = i32(c.dec_slot_mapping), i32(c.dec_block_table), i32(c.dec_seq_lens)
+        self.dout = torch.empty_like(self.dq)
+        nb = max(pkv.decode_workspace_bytes(len(c.dec_seq_lens), c.dec_block_table.shape[1], c.num_pages),
+                 pkv.prefill_workspace_bytes(1, W.PREFILL_CHUNK, c.num_pages))
+        self.ws = pkv.Workspace(nb, device)
+        self.scale = c.geom.scale
+        P, L = int(prefix), W.PREFILL_CHUNK
+        self.pairs = L * P + L * (L + 1) // 2
+        self.flops = 4 * c.geom.head_dim * c.geom.n_q_heads * self.pairs
+
+    def prefill(self):
+        self.pkv.prefill_chunk_attn(self.q, self.k_pages, self.v_pages, self.bt, self.prefix, self.cu, self.out,
+                                    self.scale, self.case.q_lens.max(), self.ws)
+
+    def mixed(self):
+        pkv = self.pkv
+        pkv.append(self.k_new, self.v_new, self.slots, self.k_pages, self.v_pages, self.ws)
+        pkv.append(self.dk, self.dv, self.dslots, self.k_pages, self.v_pages, self.ws)
+        self.prefill()
+        pkv.decode_attn(self.dq, self.k_pages, self.v_pages, self.dbt, self.dlens, self.dout, self.scale, self.ws)
+
+
+def time_launches(torch, fn, reps):
+    """Mean duration (ms) of fn's GPU work, bracketed by events with the stream kept busy."""
+    st = torch.cuda.current_stream()
+    durs = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(int(2e7))
+        e0.record(st)
+        fn()
+        e1.record(st)
+        torch.cuda.synchronize()
+        durs.append(e0.elapsed_time(e1))
+    return float(np.mean(durs))
+
+
+def measure_prefill(device, bf16_peak, reps=10):
+    import torch
+
+    res = {}
+    for prefix in (0, 8192, 32768):
+        ps = PrefillStep(device, prefix)
+        ps.mixed()
+        torch.cuda.synchronize()
+        ms = time_launches(torch, ps.prefill, reps)
+        mixed_ms = time_launches(torch, ps.mixed, reps)
+        tf = ps.flops / (ms * 1e-3) / 1e12
+        res[f"prefix_{prefix}"] = {"chunk": 4096, "prefill_us": ms * 1e3, "tflops": tf,
+                                   "frac_of_measured_bf16": tf / bf16_peak, "gflop": ps.flops / 1e9,
+                                   "mixed_step_us": mixed_ms * 1e3}
+        del ps
+        torch.cuda.empty_cache()
+    return res
+
+
 def time_e2e(step, steps, warmup, dist_on):
     """Steps/s through the Python API with host buffers: H2D of q, k_new, v_new, slots, lengths and
     block table from pinned memory, the graph-captured step, D2H of the attention output, sync."""
@@ -309,7 +385,7 @@ def cpu_baseline(seed, budget_s=10.0):
                       n_threads=cores)
         t += time.perf_counter() - t0
         layers += 1
-        if layers >= 200:
+        if layers >= 5000:
             break
     steps_per_s = layers / t / 28.0
     return {"value": steps_per_s, "unit": UNIT, "cores": cores, "kind": "oracle",
@@ -426,6 +502,10 @@ def main():
         }
         del long_step
         torch.cuda.empty_cache()
+        extra["chunked_prefill"] = {
+            "workload": "4096-token chunk (1 request) after 0/8192/32768 cached tokens; mixed step adds the chunk "
+                        "append, 15 decode appends and decode attention over U{500..5000}",
+            **measure_prefill(device, bf16)}
 
     if rank != 0:
         if dist_on:

@@ -19,7 +19,8 @@
 //    (M = N = 128, K = 128 in 8 steps of 16) into TMEM, then, once the softmax
 //    warps have written P_h back into TMEM, O_h += P_h V with P_h as the
 //    tensor-memory A operand and V as an MN-major shared-memory B operand.
-//  * Warps 0-3 and 4-7 (one warpgroup per query head, one thread per row) read
+//  * Warps 0-3 and 4-7 (one warpgroup per query head, one thread per row; 224
+//    registers each after a setmaxnreg rebalance, warps 10-11 only donate theirs) read
 //    S_h from TMEM, apply the scale and the causal mask, keep the running max
 //    and sum, and store P_h = exp2(s - m) as bf16 over S_h's first 64 columns.
 //    The O accumulator is rescaled in TMEM only when a row's max grows by more
@@ -40,7 +41,14 @@ constexpr int kPfKeys = 128;                 // keys per K/V tile
 constexpr int kPfPagesPerTile = kPfKeys / kPageSize;
 constexpr int kPfMmaWarp = 8;
 constexpr int kPfTmaWarp = 9;
-constexpr int kPfThreads = 10 * 32;
+constexpr int kPfThreads = 12 * 32;        // 3 warpgroups: softmax head 0, softmax head 1, MMA + TMA (+2 idle)
+// Register split: the launch gives every thread 168 registers (12 warps, 3 per
+// SM sub-partition); the MMA/TMA warpgroup drops to 56 and the two softmax
+// warpgroups rise to 224 ((224 + 224 + 56) * 32 <= 16384 per sub-partition,
+// and the CTA total stays 384 * 168).
+constexpr int kPfRegsSoftmax = 224;
+constexpr int kPfRegsOther = 56;
+static_assert(2 * 128 * kPfRegsSoftmax + 128 * kPfRegsOther <= kPfThreads * 168, "register split");
 constexpr int kPfHalfBytes = kPfRows * 128;  // one 64-column half of a 128 x 128 bf16 tile: 16 KiB
 constexpr int kPfTileBytes = 2 * kPfHalfBytes;
 constexpr int kPfStages = 2;
@@ -83,6 +91,38 @@ struct PfBars {
   uint64_t o_done[2];
 };
 static_assert(sizeof(PfBars) == kNumBars * 8, "barrier block");
+
+// Share of the softmax exponentials (pairs out of every 4) evaluated on the FMA
+// pipe instead of the MUFU unit. With the raw-score max and packed FMAs the
+// softmax is bound by FMA-pipe issue rather than by MUFU, and any share > 0
+// measured slower on a GB300 (0: 670/986/1090, 1: 629/919/1005 TFLOP/s for a
+// 4096-row chunk after 0/8192/32768 cached tokens), so the default is 0.
+#ifndef PKV_PF_POLY_PAIRS
+#define PKV_PF_POLY_PAIRS 0
+#endif
+constexpr int kPfPolyPairsOf4 = PKV_PF_POLY_PAIRS;
+
+// 2^t for a pair of t <= 8 (t = -inf gives about 2^-125) without the MUFU unit:
+// Cody-Waite range reduction 2^t = 2^n * 2^f with n = round(t) (the 1.5 * 2^23
+// addition rounds t to an integer in the low mantissa bits) and f in [-1/2, 1/2],
+// 2^f from a degree-3 polynomial fitted by the Remez exchange for relative
+// error (max 7.5e-5; exp2_poly_fit.py reproduces the constants), and 2^n
+// applied by adding n to the exponent field.
+__device__ __forceinline__ float2 exp2_poly2(float2 t) {
+  constexpr float kRound = 12582912.f;  // 1.5 * 2^23
+  constexpr float c0 = 0.9999280571937561f, c1 = 0.6932609677314758f, c2 = 0.2426111251115799f,
+                  c3 = 0.0551716685295105f;
+  t.x = fmaxf(t.x, -125.f);
+  t.y = fmaxf(t.y, -125.f);
+  const float2 j = __fadd2_rn(t, make_float2(kRound, kRound));
+  const float2 n = __fadd2_rn(j, make_float2(-kRound, -kRound));
+  const float2 f = __ffma2_rn(n, make_float2(-1.f, -1.f), t);
+  float2 p = __ffma2_rn(make_float2(c3, c3), f, make_float2(c2, c2));
+  p = __ffma2_rn(p, f, make_float2(c1, c1));
+  p = __ffma2_rn(p, f, make_float2(c0, c0));
+  return make_float2(__int_as_float(__float_as_int(p.x) + (__float_as_int(j.x) << 23)),
+                     __int_as_float(__float_as_int(p.y) + (__float_as_int(j.y) << 23)));
+}
 
 // Bounded wait that gives up at once after any wait of the CTA has timed out.
 __device__ __forceinline__ bool pf_wait(uint64_t* bar, uint32_t parity, volatile int* fail, int* status) {
@@ -163,8 +203,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   unsigned char* sV = smem + kOffV;
   unsigned char* sK = smem + kOffK;
 
+
   if (warp == kPfTmaWarp) {
     // ------------------------------------------------------------------ TMA producer
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kPfRegsOther));
     if (lane == 0) {
       mbar_arrive_expect_tx(&bars->q_full, 2 * kPfTileBytes);
       for (int h = 0; h < 2; ++h)
@@ -205,6 +247,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
   } else if (warp == kPfMmaWarp) {
     // ------------------------------------------------------------------ MMA issuer
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kPfRegsOther));
     if (pf_wait_warp(&bars->q_full, 0, fail, a.status)) {
       for (int j = 0; j < n_tiles; ++j) {
         const int st = j & 1;
@@ -258,8 +301,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         __syncwarp();
       }
     }
-  } else {
+  } else if (warp < 8) {
     // ------------------------------------------------------------------ softmax warpgroups
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kPfRegsSoftmax));
     const int h = warp >> 2;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;  // row of the tile = TMEM lane
@@ -280,20 +324,27 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       for (int c = 0; c < 4; ++c) tmem_ld32(t_row + kColS + 128 * h + 32 * c, sr[c]);
       tmem_ld_wait();
       const bool diag = j * kPfKeys + kPfKeys - 1 > P + i0;
+      // row max over the raw scores (the scale is positive, so it keeps the order)
       float mx = -CUDART_INF_F;
+      if (diag) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          float x = __uint_as_float(sr[c][e]) * a.scale_log2;
-          if (diag && j * kPfKeys + 32 * c + e > lim) x = -CUDART_INF_F;
-          sr[c][e] = __float_as_uint(x);
-          mx = fmaxf(mx, x);
-        }
+          for (int e = 0; e < 32; ++e) {
+            if (j * kPfKeys + 32 * c + e > lim) sr[c][e] = __float_as_uint(-CUDART_INF_F);
+            mx = fmaxf(mx, __uint_as_float(sr[c][e]));
+          }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(sr[c][e]));
+      }
       const float m_new = fmaxf(m_used, mx);
-      const bool grow = m_new > m_used + 8.f;
+      const bool first = m_used == -CUDART_INF_F;
+      const bool grow = first || (m_new - m_used) * a.scale_log2 > 8.f;
       if (__any_sync(0xffffffffu, grow)) {
-        const float alpha = grow ? ex2(m_used - m_new) : 1.f;
+        const float alpha = first ? 0.f : (grow ? ex2((m_used - m_new) * a.scale_log2) : 1.f);
         if (j > 0) {
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
@@ -311,7 +362,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           m_used = m_new;
         }
       }
-      // P as bf16 pairs over S's first 64 columns (all 128 scores are already in registers)
+      // P = 2^(s * scale * log2 e - m * scale * log2 e) as bf16 pairs over S's first 64 columns
+      const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
+      const float2 nm2 = make_float2(-m_used * a.scale_log2, -m_used * a.scale_log2);
+      float2 l2 = make_float2(0.f, 0.f);
 #pragma unroll
       for (int hc = 0; hc < 2; ++hc) {
         uint32_t pk[32];
@@ -319,13 +373,21 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         for (int c2 = 0; c2 < 2; ++c2)
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
-            const float p0 = ex2(__uint_as_float(sr[2 * hc + c2][e]) - m_used);
-            const float p1 = ex2(__uint_as_float(sr[2 * hc + c2][e + 1]) - m_used);
-            l += p0 + p1;
-            pk[c2 * 16 + (e >> 1)] = pack_bf16x2(p0, p1);
+            const float2 t = __ffma2_rn(make_float2(__uint_as_float(sr[2 * hc + c2][e]),
+                                                    __uint_as_float(sr[2 * hc + c2][e + 1])),
+                                        sc2, nm2);
+            float2 pp;
+            if (((e >> 1) & 3) < kPfPolyPairsOf4) {
+              pp = exp2_poly2(t);
+            } else {
+              pp = make_float2(ex2(t.x), ex2(t.y));
+            }
+            l2 = __fadd2_rn(l2, pp);
+            pk[c2 * 16 + (e >> 1)] = pack_bf16x2(pp.x, pp.y);
           }
         tmem_st32(t_row + kColS + 128 * h + 32 * hc, pk);
       }
+      l += l2.x + l2.y;
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive_cta(&bars->p_full[h]);
@@ -354,6 +416,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
       }
     }
+  } else {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kPfRegsOther));  // idle warps 10-11
   }
 
   tc_fence_before();
