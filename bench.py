@@ -42,6 +42,20 @@ UNIT = "steps/s"
 WORKLOAD = "qwen3-0.6b decode step: 28 layers x bs16, 16q/8kv heads, d128, page 16, seq U{300..3000}"
 
 
+# DRAM traffic of one decode launch on this workload's per-layer pool, from one ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the decode kernel source it was
+# measured on (sha256 prefix of csrc/decode.cu); any other source reports null.
+NCU_DECODE_TRAFFIC = {"4311005b0f2bebf6": 107_391_744 + 3_180_800}
+
+
+def _decode_traffic():
+    import hashlib
+
+    src = os.path.join(ROOT, "paged_kv_decode_gb300", "csrc", "decode.cu")
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    return NCU_DECODE_TRAFFIC.get(h)
+
+
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -180,14 +194,25 @@ def _barrier(dist_on):
 
 
 def _max_over_ranks(x: float, dist_on: bool) -> float:
+    """Slowest rank's value (the tensor lives where the process group's backend wants it)."""
     if not dist_on:
         return x
     import torch
     import torch.distributed as dist
 
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def replica_rate(local_total: float, units_per_rank: int, world: int, dist_on: bool):
+    """Whole-job rate of N independent replicas: all ranks' units over the slowest rank's time.
+
+    local_total is this rank's time for its units (any time unit); returns (slowest time, units / time unit).
+    """
+    slowest = _max_over_ranks(local_total, dist_on)
+    return slowest, world * units_per_rank / slowest
 
 
 def time_graph(step, steps, warmup, dist_on):
@@ -469,14 +494,13 @@ def main():
     dec_ms, dec_n = time_decode_launches(step, reps=max(3, min(20, args.steps // 50)))
     clk = clocks.stop()
 
-    ms_total = _max_over_ranks(ms_total, dist_on)
+    ms_total, steps_per_ms = replica_rate(ms_total, args.steps, world, dist_on)
     ms_per_step = ms_total / args.steps
-    steps_per_s = world * 1e3 / ms_per_step
+    steps_per_s = steps_per_ms * 1e3
 
-    e2e_dt, h2d, d2h = time_e2e(step, max(10, args.steps // 10), args.warmup, dist_on)
-    e2e_dt = _max_over_ranks(e2e_dt, dist_on)
     e2e_steps = max(10, args.steps // 10)
-    e2e_value = world * e2e_steps / e2e_dt
+    e2e_dt, h2d, d2h = time_e2e(step, e2e_steps, args.warmup, dist_on)
+    e2e_dt, e2e_value = replica_rate(e2e_dt, e2e_steps, world, dist_on)
 
     hbm, bf16, peak_kind = _peaks()
     dec_bytes = step.decode_bytes()
@@ -524,7 +548,7 @@ def main():
                        args.layers, pool_bytes / 1e9)},
         "kv_gbps_step": step_bytes / (ms_per_step * 1e-3) / 1e9 * world,
         "roofline": {"bound": "hbm", "kernel": "pkv::decode_kernel", "achieved": achieved, "peak": hbm,
-                     "unit": "GB/s", "frac": achieved / hbm, "traffic": None, "peak_kind": peak_kind,
+                     "unit": "GB/s", "frac": achieved / hbm, "traffic": _decode_traffic(), "peak_kind": peak_kind,
                      "algorithmic_bytes_per_launch": dec_bytes, "launch_us": dec_ms * 1e3,
                      "launches_timed": dec_n, "frac_of_nominal_8tbs": achieved / 8000.0},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
