@@ -1,12 +1,13 @@
 """Benchmark of the paged-KV decode step on one GB300 (or N independent replicas).
 
 A step is one Qwen3-0.6B-shaped decode step at batch 16: for each of 28
-layers, append the new token's K/V rows (pkv_append) and run decode
-attention over the paged cache (pkv_decode_attn). Request lengths are
+layers, append the new token's K/V rows and run decode attention over the
+paged cache, as one pkv_decode_append_attn launch (--unfused: pkv_append
+then pkv_decode_attn; the other variant is timed as an extra). Request lengths are
 U{300..3000} (short clips plus prompt), pages randomly placed, every layer has
 its own KV pool (about 3 GB in total, far larger than the 129 MB L2, so no L2
-flush is needed between steps). The 56 launches of a step are captured once in
-a CUDA graph and replayed.
+flush is needed between steps). The step's launches are captured once in a
+CUDA graph and replayed.
 
 Printed: one JSON line (rank 0). `value` is decode steps/s over all ranks.
 `roofline` is for the decode kernel: algorithmic bytes per launch (every
@@ -39,7 +40,8 @@ if ROOT not in sys.path:
 
 METRIC = "decode-attn KV GB/s & % HBM peak; decode steps/s at bs16 (1×GB300)"
 UNIT = "steps/s"
-WORKLOAD = "qwen3-0.6b decode step: 28 layers x bs16, 16q/8kv heads, d128, page 16, seq U{300..3000}"
+WORKLOAD = ("qwen3-0.6b decode step: 28 layers x bs16, 16q/8kv heads, d128, page 16, seq U{300..3000}; "
+            "per layer one fused KV-append + decode-attention launch")
 
 
 # DRAM traffic of one decode launch on this workload's per-layer pool, from one ncu capture
@@ -125,7 +127,7 @@ class ClockSampler:
 class DecodeStep:
     """Device-resident 28-layer decode step (all layers share one block table)."""
 
-    def __init__(self, device, seq_lens, layers: int, seed: int):
+    def __init__(self, device, seq_lens, layers: int, seed: int, fused: bool = True):
         import torch
 
         import paged_kv_decode_gb300 as pkv
@@ -147,6 +149,7 @@ class DecodeStep:
         nbytes = pkv.decode_workspace_bytes(self.B, case.max_pages, case.num_pages)
         self.ws = pkv.Workspace(nbytes, device)
         self.graph = None
+        self.fused = fused
 
     # algorithmic bytes of one decode launch (one layer)
     def decode_bytes(self) -> int:
@@ -154,7 +157,8 @@ class DecodeStep:
         kv = int(c.seq_lens.astype(np.int64).sum()) * c.geom.n_kv_heads * c.geom.head_dim * 2 * 2
         qo = 2 * self.B * c.geom.n_q_heads * c.geom.head_dim * 2
         meta = self.block_table.numel() * 4 + self.B * 4
-        return kv + qo + meta
+        new_rows = self.append_bytes() if self.fused else 0  # k_new / v_new read and written into the pool
+        return kv + qo + meta + new_rows
 
     def append_bytes(self) -> int:
         c = self.case
@@ -162,9 +166,21 @@ class DecodeStep:
 
     def layer(self, l):
         pkv = self.pkv
+        if self.fused:
+            pkv.decode_append_attn(self.q[l], self.k_new[l], self.v_new[l], self.k_pages[l], self.v_pages[l],
+                                   self.block_table, self.seq_lens, self.out[l], self.scale, self.ws)
+            return
         pkv.append(self.k_new[l], self.v_new[l], self.slot_mapping, self.k_pages[l], self.v_pages[l], self.ws)
         pkv.decode_attn(self.q[l], self.k_pages[l], self.v_pages[l], self.block_table, self.seq_lens, self.out[l],
                         self.scale, self.ws)
+
+    def decode_launch(self, l):
+        """The launch the roofline times: the step's decode kernel for layer l."""
+        if self.fused:
+            self.layer(l)
+        else:
+            self.pkv.decode_attn(self.q[l], self.k_pages[l], self.v_pages[l], self.block_table, self.seq_lens,
+                                 self.out[l], self.scale, self.ws)
 
     def step_eager(self):
         for l in range(self.layers):
@@ -247,8 +263,7 @@ def time_decode_launches(step, reps):
         torch.cuda._sleep(int(2e7))  # ~10 ms of GPU work queued ahead of the launches
         for l in range(n):
             evs[l][0].record(st)
-            pkv.decode_attn(step.q[l], step.k_pages[l], step.v_pages[l], step.block_table, step.seq_lens,
-                            step.out[l], step.scale, step.ws)
+            step.decode_launch(l)
             evs[l][1].record(st)
         torch.cuda.synchronize()
         durs += [a.elapsed_time(b) for a, b in evs]
@@ -452,7 +467,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--layers", type=int, default=28)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-extra", action="store_true", help="skip the 40k-context decode measurement")
+    ap.add_argument("--no-extra", action="store_true", help="skip the 40k-context and prefill measurements")
+    ap.add_argument("--unfused", action="store_true",
+                    help="time the step as separate pkv_append + pkv_decode_attn launches")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -484,9 +501,9 @@ def main():
     torch.cuda.set_device(device)
 
     # each replica runs its own copy of the workload (replicas only: requests are independent)
-    step = DecodeStep(device, W.config_seq_lens(2), args.layers, seed=2 + rank)
+    step = DecodeStep(device, W.config_seq_lens(2), args.layers, seed=2 + rank, fused=not args.unfused)
     step.capture()
-    launches_per_step = 2 * args.layers
+    launches_per_step = args.layers if step.fused else 2 * args.layers
 
     clocks = ClockSampler(device.index)
     clocks.start()
@@ -510,10 +527,18 @@ def main():
 
     extra = {}
     if not args.no_extra:
+        other = DecodeStep(device, W.config_seq_lens(2), args.layers, seed=2 + rank, fused=args.unfused)
+        other.capture()
+        ot = time_graph(other, max(50, args.steps // 4), args.warmup, dist_on) / max(50, args.steps // 4)
+        extra["step_" + ("fused" if other.fused else "separate_append_and_decode")] = {
+            "ms_per_step": ot, "steps_per_s": 1e3 / ot, "launches_per_step": args.layers * (1 if other.fused else 2)}
+        del other
+        torch.cuda.empty_cache()
         long_step = None
         del step
         torch.cuda.empty_cache()
-        long_step = DecodeStep(device, W.config_seq_lens(3, context=40000), args.layers, seed=3 + rank)
+        long_step = DecodeStep(device, W.config_seq_lens(3, context=40000), args.layers, seed=3 + rank,
+                               fused=not args.unfused)
         long_step.capture()
         lt = time_graph(long_step, max(20, args.steps // 4), args.warmup, dist_on) / max(20, args.steps // 4)
         ld_ms, _ = time_decode_launches(long_step, reps=5)

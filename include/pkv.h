@@ -162,6 +162,32 @@ int pkv_decode_attn(const void* q, const void* k_pages, const void* v_pages, con
                     size_t workspace_bytes);
 
 /*
+ * pkv_decode_append_attn -- one decode step of one layer: KV append fused into
+ * decode attention (one launch instead of pkv_append + pkv_decode_attn).
+ *
+ * Source: each generated token adds one K/V row per layer to the paged cache
+ * and then attends over the whole cache ("FunASR vLLM Inference Engine Guide",
+ * section 2; "Optimizing ASR for 90-minute multi-speaker audio", section
+ * "Autoregressive decoding").
+ *
+ * For every request b with seq_lens[b] > 0, the rows k_new[b][g][:] and
+ * v_new[b][g][:] of every KV head g are written at logical position
+ * seq_lens[b] - 1 (page block_table[b][(seq_lens[b]-1) / page_size], slot
+ * (seq_lens[b]-1) % page_size), bit-exactly; then out is computed exactly as
+ * by pkv_decode_attn over seq_lens[b] positions, the new one included. The
+ * result equals pkv_append with slot_mapping[b] = that slot followed by
+ * pkv_decode_attn.
+ *
+ *  k_new, v_new: bf16 [batch][num_kv_heads][head_dim], 16-byte aligned
+ *  k_pages, v_pages: the pools, updated in place at the new slots only
+ *  other arguments and the workspace: as for pkv_decode_attn
+ */
+int pkv_decode_append_attn(const void* q, const void* k_new, const void* v_new, void* k_pages, void* v_pages,
+                           const int32_t* block_table, const int32_t* seq_lens, void* out, float scale,
+                           pkv_stream_t stream, const pkv_cache_desc* desc, int32_t batch, int32_t max_pages_per_seq,
+                           void* workspace, size_t workspace_bytes);
+
+/*
  * Workspace bytes pkv_prefill_chunk_attn needs (the status header).
  */
 size_t pkv_prefill_workspace_bytes(const pkv_cache_desc* desc, int32_t num_seqs, int32_t max_q_len);

@@ -32,7 +32,7 @@ ERRORS = {
 __all__ = [
     "PkvError", "desc", "Workspace", "append", "decode_attn", "prefill_chunk_attn",
     "decode_workspace_bytes", "prefill_workspace_bytes", "workspace_init", "read_status", "status_string",
-    "decode_attn_noalloc",
+    "decode_attn_noalloc", "decode_append_attn",
 ]
 
 
@@ -172,6 +172,34 @@ def decode_attn(q, k_pages, v_pages, block_table, seq_lens, out, scale: float, w
                                      _ptr(out), float(scale), _stream(stream), ctypes.byref(d), B,
                                      block_table.shape[1], _ptr(ws), ws.numel())
     _check(rc, "pkv_decode_attn")
+
+
+def decode_append_attn(q, k_new, v_new, k_pages, v_pages, block_table, seq_lens, out, scale: float,
+                       workspace: Workspace, stream=None):
+    """One decode step of one layer in one launch: write k_new / v_new [B, 8, 128] at position
+    seq_lens[b] - 1 of each request, then decode attention over seq_lens[b] positions."""
+    import torch
+
+    _need(k_pages, torch.bfloat16, "k_pages")
+    dev = k_pages.device
+    _need(v_pages, torch.bfloat16, "v_pages", dev)
+    _need(q, torch.bfloat16, "q", dev)
+    _need(k_new, torch.bfloat16, "k_new", dev)
+    _need(v_new, torch.bfloat16, "v_new", dev)
+    _need(out, torch.bfloat16, "out", dev)
+    _need(block_table, torch.int32, "block_table", dev)
+    _need(seq_lens, torch.int32, "seq_lens", dev)
+    B = q.shape[0]
+    if (out.shape != q.shape or block_table.dim() != 2 or block_table.shape[0] != B or seq_lens.numel() != B
+            or k_new.shape[0] != B or v_new.shape != k_new.shape):
+        raise ValueError("shape mismatch")
+    d = _desc_of(k_pages)
+    ws = workspace.tensor
+    rc = _lib.load().pkv_decode_append_attn(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_pages), _ptr(v_pages),
+                                            _ptr(block_table), _ptr(seq_lens), _ptr(out), float(scale),
+                                            _stream(stream), ctypes.byref(d), B, block_table.shape[1], _ptr(ws),
+                                            ws.numel())
+    _check(rc, "pkv_decode_append_attn")
 
 
 def prefill_chunk_attn(q, k_pages, v_pages, block_table, prefix_lens, cu_q_lens, out, scale: float, max_q_len: int,

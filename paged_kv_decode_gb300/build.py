@@ -69,7 +69,7 @@ def build_library(force: bool = False, verbose: bool = False, extra=()) -> str:
         objs = list(ex.map(lambda s: _compile(s, extra), srcs))
     if force or _stale(LIB, objs):
         tmp = LIB + f".tmp{os.getpid()}"
-        cmd = [nvcc()] + ARCH + ["-shared", "-o", tmp] + objs
+        cmd = [nvcc()] + ARCH + ["-shared", "-Xlinker", "--no-undefined", "-o", tmp] + objs
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

@@ -15,15 +15,19 @@
 //    only on host-known sizes (CUDA-graph friendly) and every CTA streams the
 //    same number of pages whatever the length mix.
 //  * A CTA's share is cut into pieces, one per (request, KV head) it touches.
-//    Inside a piece its 4 warps take pages round-robin. Each warp owns a ring
-//    of 3 shared-memory stages and fills them itself with 1-D bulk copies
+//    Inside a piece its consumer warps take pages round-robin. A producer warp
+//    fills each consumer's ring of shared-memory stages with 1-D bulk copies
 //    (cp.async.bulk, one 4 KiB K tile and one 4 KiB V tile per page) that
-//    complete on an mbarrier, so up to 24 KiB per warp is in flight.
+//    complete on the stage's full barrier; consumers release stages through
+//    empty barriers.
 //  * Both query heads of the GQA group are computed from one K/V read. Scores
 //    use packed fp32 FMAs (two dims per instruction); the softmax is online in
 //    the log2 domain (q pre-scaled by scale * log2 e); tokens past seq_len in
 //    the last page are masked before they can touch the max or the sum, so
 //    unused slots may hold anything, NaN included.
+//  * Optional fused append: the producer lane that copies a request's last
+//    page first writes the request's new K/V row for that head into it
+//    (generic stores, then a proxy fence so its own bulk copy sees them).
 //  * At the end of a piece the warps merge through shared memory. A piece that
 //    covers its whole (request, KV head) writes the bf16 output. Otherwise it
 //    writes an fp32 partial (m, l, o) and bumps a per-(request, KV head)
@@ -54,7 +58,6 @@ constexpr int kDecCtasPerSm = PKV_DEC_CTAS_PER_SM;
 constexpr int kStages = kCons * kDecRing;
 static_assert(kHeadDim % kConsThreads == 0 || kConsThreads % kHeadDim == 0, "merge maps threads to head dims");
 constexpr int kDimsPerThread = kConsThreads >= kHeadDim ? 1 : kHeadDim / kConsThreads;  // in the merges
-constexpr int kMergeGroups = kConsThreads >= kHeadDim ? kConsThreads / kHeadDim : 1;  // record groups in the split merge
 constexpr int kStageBytes = 2 * kTileBytes;  // K tile + V tile of one (page, KV head)
 constexpr int kRec = kHeadDim + 4;           // floats per query-head record: m, l, pad, pad, o[128]
 constexpr int kPieceFloats = kGroup * kRec;  // a partial record of one piece (both query heads)
@@ -68,7 +71,7 @@ constexpr int kMergeFloats = kCons * kPieceFloats;         // one record per con
 constexpr int kSmemMerge = kMergeFloats * 4;
 constexpr int kSmemPbuf = kCons * kPageSize * 4 * 4;       // per warp: [16 tokens][p0, p0, p1, p1]
 constexpr int kSmemSplit = kCons * 2 * 4;                  // per consumer warp: running max of both heads
-constexpr int kSmemMisc = 16 + ((kCons * 4 + 15) / 16) * 16;  // flag words + producer's per-consumer counts
+constexpr int kSmemMisc = 16;                              // flag words
 constexpr int kSmemFixed = kSmemRing + kSmemBars + kSmemMerge + kSmemPbuf + kSmemSplit + kSmemMisc;
 
 static size_t decode_smem_bytes(int batch) { return kSmemFixed + static_cast<size_t>(2 * batch + 1) * 4; }
@@ -77,6 +80,8 @@ int decode_max_batch() { return kMaxDecodeBatch; }
 
 struct DecodeArgs {
   const __nv_bfloat16* q;
+  const __nv_bfloat16* k_new;  // optional fused append: [batch][kv heads][head_dim], nullptr = none
+  const __nv_bfloat16* v_new;
   const __nv_bfloat16* k_pages;
   const __nv_bfloat16* v_pages;
   const int* block_table;
@@ -173,7 +178,6 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
   float* pbuf = merge + kMergeFloats;
   float* split = pbuf + kCons * kPageSize * 4;
   int* flag = reinterpret_cast<int*>(split + kCons * 2);
-  int* sbase = flag + 4;
   int* pref = reinterpret_cast<int*>(reinterpret_cast<unsigned char*>(flag) + kSmemMisc);
   int* sl = pref + a.batch + 1;
 
@@ -186,7 +190,6 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
     mbar_init(&full[tid], 1);
     mbar_init(&empty[tid], 1);
   }
-  if (tid < kCons) sbase[tid] = 0;
   grid_dependency_wait();  // every argument buffer may come from the previous kernel in the stream
   allow_dependents();
 
@@ -238,62 +241,86 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
   const long long hi = share_lo(blockIdx.x + 1, T, G);
 
   // ============================================================== producer warp
-  // Walks the share in order, 32 flattened indices at a time (one per lane:
-  // request, KV head, page and block-table entry decoded in parallel), and
-  // fills each page into the next stage of the consumer that will read it:
-  // within a piece, page p0 + i goes to consumer i % kCons.
+  // Walks the share 32 flattened indices at a time, one per lane: each lane
+  // decodes its (request, KV head, page), loads the block-table entry, and works
+  // out which consumer reads the page (within a piece, page p0 + i goes to
+  // consumer i % kCons) and which stage of that consumer's ring it fills (its
+  // running page count, from the lanes before it with the same consumer). The
+  // lanes then issue their own bulk copies in rounds in which every stage is
+  // filled at most once, so each stage's empty barrier is at most one phase
+  // behind the wait.
   if (warp == kCons) {
     const uint64_t policy = policy_evict_first();
-    long long piece_start = lo;
-    int piece_len = 0;
+    const unsigned lt_mask = (1u << lane) - 1u;
+    int base[kCons];  // pages handed to each consumer before this chunk
+#pragma unroll
+    for (int c = 0; c < kCons; ++c) base[c] = 0;
     bool pfail = false;
     for (long long f0 = lo; f0 < hi && !pfail; f0 += 32) {
       const long long f = f0 + lane;
-      int hh = 0, id = 0, seg = 0;
-      if (f < hi) {
+      const bool valid = f < hi;
+      int hh = 0, id = 0, c = 0, wslot = -1, bb = 0;
+      if (valid) {
         const int b = request_of(f, pref, batch);
         const int np = (pref[b + 1] - pref[b]) / kKVHeads;
         const int off = static_cast<int>(f - pref[b]);
         hh = off / np;
         const int p = off % np;
-        seg = pref[b] + hh * np;
+        const long long seg = pref[b] + static_cast<long long>(hh) * np;
+        c = static_cast<int>((f - (seg > lo ? seg : lo)) % kCons);
+        bb = b;
         id = __ldg(a.block_table + static_cast<size_t>(b) * a.max_pages + p);
+        if (a.k_new != nullptr && p == np - 1) wslot = (sl[b] - 1) % kPageSize;  // the new token's slot
       }
-      const int n = static_cast<int>(hi - f0 < 32 ? hi - f0 : 32);
-      for (int i = 0; i < n; ++i) {
-        const int h_i = __shfl_sync(kFull, hh, i);
-        int id_i = __shfl_sync(kFull, id, i);
-        const int seg_i = __shfl_sync(kFull, seg, i);
-        if (lane == 0 && !pfail) {
-          const long long pstart = seg_i > lo ? seg_i : lo;
-          if (pstart != piece_start) {
-            for (int c = 0; c < kCons; ++c) sbase[c] += piece_len > c ? (piece_len - c + kCons - 1) / kCons : 0;
-            piece_start = pstart;
-            piece_len = 0;
-          }
-          const int prel = static_cast<int>(f0 + i - piece_start);
-          piece_len = prel + 1;
-          const int c = prel % kCons;
-          const int k = sbase[c] + prel / kCons;
-          const int slot = c * kDecRing + k % kDecRing;
-          const int use = k / kDecRing;
+      const unsigned same = __match_any_sync(kFull, valid ? c : -1);
+      const int idx = __popc(same & lt_mask);  // earlier lanes of this chunk feeding the same consumer
+      int my_base = 0;
+#pragma unroll
+      for (int cc = 0; cc < kCons; ++cc) {
+        if (cc == c) my_base = base[cc];
+        base[cc] += __popc(__ballot_sync(kFull, valid && c == cc));
+      }
+      const int k = my_base + idx;
+      const int slot = c * kDecRing + k % kDecRing;
+      const int use = k / kDecRing;
+      const int my_round = idx / kDecRing;
+      int rounds = valid ? my_round + 1 : 0;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) rounds = max(rounds, __shfl_xor_sync(kFull, rounds, o));
+      for (int r = 0; r < rounds; ++r) {
+        if (valid && my_round == r && !pfail) {
           if (use > 0 && !mbar_wait_bounded(&empty[slot], static_cast<uint32_t>(use - 1) & 1u)) {
             set_status(a.status, PKV_ERR_DEVICE_TIMEOUT);
             pfail = true;
           } else {
-            if (id_i < 0 || id_i >= a.num_pages) {
-              set_status(a.status, PKV_ERR_OUT_OF_BOUNDS);
-              id_i = 0;
+            const bool id_ok = id >= 0 && id < a.num_pages;
+            if (!id_ok) set_status(a.status, PKV_ERR_OUT_OF_BOUNDS);
+            const int pid = id_ok ? id : 0;
+            if (wslot >= 0 && id_ok) {
+              // fused append: this page holds the request's new token; write its K and V rows
+              // for this head, then order the writes before this lane's bulk copy of the page
+              const uint4* ks = reinterpret_cast<const uint4*>(a.k_new + (static_cast<size_t>(bb) * kKVHeads + hh) * kHeadDim);
+              const uint4* vs = reinterpret_cast<const uint4*>(a.v_new + (static_cast<size_t>(bb) * kKVHeads + hh) * kHeadDim);
+              const size_t row = ((static_cast<size_t>(pid) * kKVHeads + hh) * kPageSize + wslot) * kHeadDim;
+              uint4* kd = reinterpret_cast<uint4*>(const_cast<__nv_bfloat16*>(a.k_pages) + row);
+              uint4* vd = reinterpret_cast<uint4*>(const_cast<__nv_bfloat16*>(a.v_pages) + row);
+#pragma unroll
+              for (int q4 = 0; q4 < kRowBytes / 16; ++q4) {
+                kd[q4] = __ldg(ks + q4);
+                vd[q4] = __ldg(vs + q4);
+              }
+              fence_proxy_async_global();
             }
-            const size_t off = (static_cast<size_t>(id_i) * kKVHeads + h_i) * (kTileBytes / 2);
+            const size_t off = (static_cast<size_t>(pid) * kKVHeads + hh) * (kTileBytes / 2);
             unsigned char* dst = ring + slot * kStageBytes;
             mbar_arrive_expect_tx(&full[slot], kStageBytes);
             bulk_g2s_hint(dst, a.k_pages + off, kTileBytes, &full[slot], policy);
             bulk_g2s_hint(dst + kTileBytes, a.v_pages + off, kTileBytes, &full[slot], policy);
           }
         }
+        __syncwarp();
       }
-      pfail = __shfl_sync(kFull, pfail ? 1 : 0, 0) != 0;
+      pfail = __any_sync(kFull, pfail);
     }
     return;
   }
@@ -526,96 +553,81 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
       consumer_sync();
       if (flag[0]) {
         // This CTA holds the last piece: merge all partial records of (b, h).
+        // Warp w folds records w, w + kCons, ... online (running max, rescaled
+        // sums), 8 records in flight, one float4 of both heads' o per lane; the
+        // warps' states are then merged through the (free) merge buffer.
         __threadfence();
         const int n = clast - cfirst + 1;
         auto rec_of = [&](int t) {
           const int c = cfirst + t;
           return a.partials + static_cast<size_t>(2 * c + ((t == 0 && first_has_two) ? 1 : 0)) * kPieceFloats;
         };
-        // global max of each head: strided over threads, then over warps
-        float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F;
-        for (int t = tid; t < n; t += kConsThreads) {
-          const float* r = rec_of(t);
-          m0 = fmaxf(m0, __ldcg(r));
-          m1 = fmaxf(m1, __ldcg(r + kRec));
-        }
+        float wm0 = -CUDART_INF_F, wm1 = -CUDART_INF_F, wl0 = 0.f, wl1 = 0.f;
+        float4 wo0 = make_float4(0.f, 0.f, 0.f, 0.f), wo1 = wo0;
+        for (int t0 = warp; t0 < n; t0 += 8 * kCons) {
+          float mm0[8], mm1[8], ll0[8], ll1[8];
+          float4 oo0[8], oo1[8];
 #pragma unroll
-        for (int o2 = 16; o2 > 0; o2 >>= 1) {
-          m0 = fmaxf(m0, __shfl_xor_sync(kFull, m0, o2));
-          m1 = fmaxf(m1, __shfl_xor_sync(kFull, m1, o2));
+          for (int u = 0; u < 8; ++u) {
+            const int t = t0 + u * kCons;
+            mm0[u] = mm1[u] = -CUDART_INF_F;
+            ll0[u] = ll1[u] = 0.f;
+            oo0[u] = oo1[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (t < n) {
+              const float* r = rec_of(t);
+              mm0[u] = __ldcg(r);
+              ll0[u] = __ldcg(r + 1);
+              mm1[u] = __ldcg(r + kRec);
+              ll1[u] = __ldcg(r + kRec + 1);
+              oo0[u] = __ldcg(reinterpret_cast<const float4*>(r + 4) + lane);
+              oo1[u] = __ldcg(reinterpret_cast<const float4*>(r + kRec + 4) + lane);
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            if (mm0[u] == -CUDART_INF_F) continue;  // past the last record
+            const float n0 = fmaxf(wm0, mm0[u]), n1 = fmaxf(wm1, mm1[u]);
+            const float a0 = ex2(wm0 - n0), b0 = ex2(mm0[u] - n0);
+            const float a1 = ex2(wm1 - n1), b1 = ex2(mm1[u] - n1);
+            wl0 = wl0 * a0 + ll0[u] * b0;
+            wl1 = wl1 * a1 + ll1[u] * b1;
+            wo0 = make_float4(wo0.x * a0 + oo0[u].x * b0, wo0.y * a0 + oo0[u].y * b0, wo0.z * a0 + oo0[u].z * b0,
+                              wo0.w * a0 + oo0[u].w * b0);
+            wo1 = make_float4(wo1.x * a1 + oo1[u].x * b1, wo1.y * a1 + oo1[u].y * b1, wo1.z * a1 + oo1[u].z * b1,
+                              wo1.w * a1 + oo1[u].w * b1);
+            wm0 = n0;
+            wm1 = n1;
+          }
         }
+        float* mw = merge + warp * kPieceFloats;  // same record format as the piece merge
+        reinterpret_cast<float4*>(mw + 4)[lane] = wo0;
+        reinterpret_cast<float4*>(mw + kRec + 4)[lane] = wo1;
         if (lane == 0) {
-          split[warp * 2] = m0;
-          split[warp * 2 + 1] = m1;
+          mw[0] = wm0;
+          mw[1] = wl0;
+          mw[kRec] = wm1;
+          mw[kRec + 1] = wl1;
         }
         consumer_sync();
+        if (owns_dims) {
 #pragma unroll
-        for (int w = 0; w < kCons; ++w) {
-          m0 = fmaxf(m0, split[w * 2]);
-          m1 = fmaxf(m1, split[w * 2 + 1]);
-        }
-        // weighted sums: kMergeGroups groups take alternate records, 4 records in flight each
-        const int grp = kConsThreads >= kHeadDim ? tid / kHeadDim : 0;
-        const int dbase = kConsThreads >= kHeadDim ? tid % kHeadDim : tid;
-        float acc0[kDimsPerThread], acc1[kDimsPerThread];
+          for (int i = 0; i < 2; ++i) {
+            float m = -CUDART_INF_F;
 #pragma unroll
-        for (int e = 0; e < kDimsPerThread; ++e) acc0[e] = acc1[e] = 0.f;
-        float lsum0 = 0.f, lsum1 = 0.f;
-        for (int t0 = grp; t0 < n; t0 += 4 * kMergeGroups) {
-          float mm0[4], mm1[4], ll0[4], ll1[4], v0[4][kDimsPerThread], v1[4][kDimsPerThread];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int t = t0 + u * kMergeGroups;
-            const float* r = rec_of(t < n ? t : 0);
-            mm0[u] = t < n ? __ldcg(r) : -CUDART_INF_F;
-            ll0[u] = __ldcg(r + 1);
-            mm1[u] = t < n ? __ldcg(r + kRec) : -CUDART_INF_F;
-            ll1[u] = __ldcg(r + kRec + 1);
+            for (int w = 0; w < kCons; ++w) m = fmaxf(m, merge[w * kPieceFloats + i * kRec]);
 #pragma unroll
             for (int e = 0; e < kDimsPerThread; ++e) {
-              v0[u][e] = __ldcg(r + 4 + dbase + e * kConsThreads);
-              v1[u][e] = __ldcg(r + kRec + 4 + dbase + e * kConsThreads);
-            }
-          }
+              const int d = tid + e * kConsThreads;
+              float lsum = 0.f, acc = 0.f;
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const float w0 = ex2(mm0[u] - m0), w1 = ex2(mm1[u] - m1);  // 0 for t >= n
-            lsum0 += ll0[u] * w0;
-            lsum1 += ll1[u] * w1;
-#pragma unroll
-            for (int e = 0; e < kDimsPerThread; ++e) {
-              acc0[e] += v0[u][e] * w0;
-              acc1[e] += v1[u][e] * w1;
+              for (int w = 0; w < kCons; ++w) {
+                const float* r = merge + w * kPieceFloats + i * kRec;
+                const float sc = r[0] == -CUDART_INF_F ? 0.f : ex2(r[0] - m);  // warps without records
+                lsum += r[1] * sc;
+                acc += r[4 + d] * sc;
+              }
+              orow[i * kHeadDim + d] = __float2bfloat16_rn(acc / lsum);
             }
-          }
-        }
-        if (kMergeGroups > 1) {  // fold the groups (o and l sums) through the (free) merge buffer
-          float* fold = merge;
-          float* lfold = merge + (kMergeGroups - 1) * 2 * kHeadDim;
-          if (grp > 0) {
-            fold[(grp - 1) * 2 * kHeadDim + dbase] = acc0[0];
-            fold[(grp - 1) * 2 * kHeadDim + kHeadDim + dbase] = acc1[0];
-            if (dbase == 0) {
-              lfold[(grp - 1) * 2] = lsum0;
-              lfold[(grp - 1) * 2 + 1] = lsum1;
-            }
-          }
-          consumer_sync();
-          if (grp == 0) {
-            for (int g = 1; g < kMergeGroups; ++g) {
-              acc0[0] += fold[(g - 1) * 2 * kHeadDim + dbase];
-              acc1[0] += fold[(g - 1) * 2 * kHeadDim + kHeadDim + dbase];
-              lsum0 += lfold[(g - 1) * 2];
-              lsum1 += lfold[(g - 1) * 2 + 1];
-            }
-          }
-        }
-        if (grp == 0) {
-#pragma unroll
-          for (int e = 0; e < kDimsPerThread; ++e) {
-            const int d = dbase + e * kConsThreads;
-            orow[d] = __float2bfloat16_rn(acc0[e] / lsum0);
-            orow[kHeadDim + d] = __float2bfloat16_rn(acc1[e] / lsum1);
           }
         }
         if (tid == 0) a.counters[b * kKVHeads + h] = 0;
@@ -634,9 +646,9 @@ size_t decode_workspace_bytes(int32_t batch, int num_sms) {
   return off;
 }
 
-int launch_decode(const void* q, const void* k_pages, const void* v_pages, const int32_t* block_table,
-                  const int32_t* seq_lens, void* out, float scale, int32_t batch, int32_t max_pages,
-                  int32_t num_pages, void* workspace, int num_sms, cudaStream_t stream) {
+int launch_decode(const void* q, const void* k_new, const void* v_new, const void* k_pages, const void* v_pages,
+                  const int32_t* block_table, const int32_t* seq_lens, void* out, float scale, int32_t batch,
+                  int32_t max_pages, int32_t num_pages, void* workspace, int num_sms, cudaStream_t stream) {
   if (batch == 0) return PKV_OK;
   const size_t smem = decode_smem_bytes(batch);
   static bool attr_set[64] = {false};
@@ -657,6 +669,8 @@ int launch_decode(const void* q, const void* k_pages, const void* v_pages, const
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   DecodeArgs a;
   a.q = static_cast<const __nv_bfloat16*>(q);
+  a.k_new = static_cast<const __nv_bfloat16*>(k_new);
+  a.v_new = static_cast<const __nv_bfloat16*>(v_new);
   a.k_pages = static_cast<const __nv_bfloat16*>(k_pages);
   a.v_pages = static_cast<const __nv_bfloat16*>(v_pages);
   a.block_table = block_table;

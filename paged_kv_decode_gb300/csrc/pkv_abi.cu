@@ -141,8 +141,31 @@ int pkv_decode_attn(const void* q, const void* k_pages, const void* v_pages, con
   rc = current_device(&sms);
   if (rc != PKV_OK) return rc;
   if (workspace_bytes < pkv::decode_workspace_bytes(batch, sms)) return PKV_ERR_WORKSPACE_TOO_SMALL;
-  return pkv::launch_decode(q, k_pages, v_pages, block_table, seq_lens, out, scale, batch, max_pages_per_seq,
-                            desc->num_pages, workspace, sms, reinterpret_cast<cudaStream_t>(stream));
+  return pkv::launch_decode(q, nullptr, nullptr, k_pages, v_pages, block_table, seq_lens, out, scale, batch,
+                            max_pages_per_seq, desc->num_pages, workspace, sms, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int pkv_decode_append_attn(const void* q, const void* k_new, const void* v_new, void* k_pages, void* v_pages,
+                           const int32_t* block_table, const int32_t* seq_lens, void* out, float scale,
+                           pkv_stream_t stream, const pkv_cache_desc* desc, int32_t batch, int32_t max_pages_per_seq,
+                           void* workspace, size_t workspace_bytes) {
+  int rc = check_desc(desc);
+  if (rc != PKV_OK) return rc;
+  if (batch < 0 || max_pages_per_seq < 1) return PKV_ERR_BAD_SHAPE;
+  if (batch > pkv::decode_max_batch()) return PKV_ERR_UNSUPPORTED;
+  if (!table_fits(batch, max_pages_per_seq)) return PKV_ERR_BAD_SHAPE;
+  if (workspace == nullptr) return PKV_ERR_NULL_ARG;
+  if (batch == 0) return PKV_OK;
+  if (!q || !k_new || !v_new || !k_pages || !v_pages || !block_table || !seq_lens || !out) return PKV_ERR_NULL_ARG;
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pages) || !aligned16(v_pages) ||
+      !aligned16(out) || !aligned16(workspace))
+    return PKV_ERR_MISALIGNED;
+  int sms = 0;
+  rc = current_device(&sms);
+  if (rc != PKV_OK) return rc;
+  if (workspace_bytes < pkv::decode_workspace_bytes(batch, sms)) return PKV_ERR_WORKSPACE_TOO_SMALL;
+  return pkv::launch_decode(q, k_new, v_new, k_pages, v_pages, block_table, seq_lens, out, scale, batch,
+                            max_pages_per_seq, desc->num_pages, workspace, sms, reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t pkv_prefill_workspace_bytes(const pkv_cache_desc* desc, int32_t num_seqs, int32_t max_q_len) {

@@ -12,9 +12,10 @@ int launch_append(const void* k_new, const void* v_new, const int32_t* slot_mapp
 
 // Decode: workspace = [status header | counters (batch * kv heads) | partials].
 size_t decode_workspace_bytes(int32_t batch, int num_sms);
-int launch_decode(const void* q, const void* k_pages, const void* v_pages, const int32_t* block_table,
-                  const int32_t* seq_lens, void* out, float scale, int32_t batch, int32_t max_pages,
-                  int32_t num_pages, void* workspace, int num_sms, cudaStream_t stream);
+// k_new / v_new (nullable): fused append of each request's new token at position seq_lens[b] - 1.
+int launch_decode(const void* q, const void* k_new, const void* v_new, const void* k_pages, const void* v_pages,
+                  const int32_t* block_table, const int32_t* seq_lens, void* out, float scale, int32_t batch,
+                  int32_t max_pages, int32_t num_pages, void* workspace, int num_sms, cudaStream_t stream);
 int decode_max_batch();
 
 size_t prefill_workspace_bytes(int32_t num_seqs, int32_t max_q_len, int num_sms);

@@ -205,3 +205,40 @@ def test_workspace_too_small_is_rejected(cuda_device):
     with pytest.raises(pkv.PkvError) as e:
         run.step()
     assert e.value.code == -4
+
+
+# ---------------------------------------------------------------------------- fused append + decode
+
+def _fused(case, layer, dev):
+    run = DecodeOnDevice(case, layer, dev)
+    pkv.decode_append_attn(run.q, run.k_new, run.v_new, run.k_pages, run.v_pages, run.block_table, run.seq_lens,
+                           run.out, case.geom.scale, run.ws)
+    torch.cuda.synchronize()
+    return run
+
+
+@pytest.mark.parametrize("cfg", ["tiny", "bs16", "40k", "cfg", "ragged", "padded"])
+def test_fused_append_decode_matches_oracle(cuda_device, cfg):
+    lens = {"tiny": W.config_seq_lens(1), "bs16": W.config_seq_lens(2), "40k": W.config_seq_lens(3),
+            "cfg": W.config_seq_lens(5), "ragged": [1, 15, 16, 17, 32, 33, 1000],
+            "padded": [700, 0, 33, 0, 1, 2900]}[cfg]
+    case = W.decode_case(17, lens, pending_append=True, poison=True)
+    run = _fused(case, 0, cuda_device)
+    # the pools equal the oracle's slot scatter: new rows written, every other slot untouched
+    want_k, want_v = oracle.append(case.k_new[0], case.v_new[0], case.slot_mapping, case.k_pages[0], case.v_pages[0])
+    assert np.array_equal(bits(run.k_pages), want_k) and np.array_equal(bits(run.v_pages), want_v)
+    want = oracle.decode(case.q[0], want_k, want_v, case.block_table, case.seq_lens, case.geom.scale)
+    assert_close(bf16_to_f64(run.out), want, f"fused {cfg}")
+    for b, n in enumerate(case.seq_lens):
+        if n == 0:
+            assert torch.count_nonzero(run.out[b]).item() == 0
+    assert run.ws.status() == 0
+
+
+def test_fused_equals_separate_calls_bitwise(cuda_device):
+    case = W.decode_case(18, W.config_seq_lens(2), pending_append=True, poison=True)
+    sep = DecodeOnDevice(case, 0, cuda_device)
+    out_sep = sep.step().clone()
+    fused = _fused(case, 0, cuda_device)
+    assert torch.equal(out_sep.view(torch.int16), fused.out.view(torch.int16))
+    assert torch.equal(sep.k_pages.view(torch.int16), fused.k_pages.view(torch.int16))
