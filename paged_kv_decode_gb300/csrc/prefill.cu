@@ -26,7 +26,7 @@
 //    The O accumulator is rescaled in TMEM only when a row's max grows by more
 //    than 2^8 (otherwise the stale max is kept; the final O / l is unchanged).
 //  * TMEM: S_0, S_1, O_0, O_1, 128 columns each (512 allocated, 1 CTA per SM).
-//  * Grid: (query tiles, KV heads, requests), the longest tiles first.
+//  * Grid: (query tile x KV head, request), dispatched longest causal tiles first.
 #include <cuda.h>
 #include <math_constants.h>
 
@@ -152,9 +152,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int tile = gridDim.x - 1 - blockIdx.x;  // longest causal tiles first
-  const int g = blockIdx.y;                     // KV head
-  const int n = blockIdx.z;                     // request
+  // CTAs are dispatched in blockIdx.x order: walk (query tile, KV head) pairs
+  // tile-major from the last tile, so every head's longest causal tiles start first.
+  const int n_qtiles = gridDim.x / kKVHeads;
+  const int tile = n_qtiles - 1 - static_cast<int>(blockIdx.x) / kKVHeads;
+  const int g = static_cast<int>(blockIdx.x) % kKVHeads;  // KV head
+  const int n = blockIdx.y;                                 // request
 
   grid_dependency_wait();
   allow_dependents();
@@ -502,7 +505,7 @@ int launch_prefill(const void* q, const void* k_pages, const void* v_pages, cons
   a.num_pages = num_pages;
   a.scale_log2 = scale * kLog2e;
   a.status = static_cast<int*>(workspace);
-  const dim3 grid((max_q_len + kPfRows - 1) / kPfRows, kKVHeads, num_seqs);
+  const dim3 grid(((max_q_len + kPfRows - 1) / kPfRows) * kKVHeads, num_seqs);
   return launch_pdl(prefill_kernel, grid, dim3(kPfThreads), static_cast<size_t>(kPfSmemBytes), stream, qmap, kmap,
                     vmap, a) == cudaSuccess
              ? PKV_OK
