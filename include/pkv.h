@@ -180,12 +180,28 @@ int pkv_decode_attn(const void* q, const void* k_pages, const void* v_pages, con
  *
  *  k_new, v_new: bf16 [batch][num_kv_heads][head_dim], 16-byte aligned
  *  k_pages, v_pages: the pools, updated in place at the new slots only
+ *  flags:        0 or PKV_DECODE_EARLY_PREFETCH (see below); other bits are
+ *                rejected with PKV_ERR_UNSUPPORTED
  *  other arguments and the workspace: as for pkv_decode_attn
  */
 int pkv_decode_append_attn(const void* q, const void* k_new, const void* v_new, void* k_pages, void* v_pages,
                            const int32_t* block_table, const int32_t* seq_lens, void* out, float scale,
                            pkv_stream_t stream, const pkv_cache_desc* desc, int32_t batch, int32_t max_pages_per_seq,
-                           void* workspace, size_t workspace_bytes);
+                           void* workspace, size_t workspace_bytes, uint32_t flags);
+
+/*
+ * Flag for pkv_decode_append_attn. Every kernel of the library is launched
+ * with programmatic stream serialisation and normally waits for the previous
+ * kernel in the stream before it reads any argument. With this flag the
+ * caller promises that the previous kernel writes neither k_pages / v_pages
+ * nor block_table nor seq_lens (the usual case in a decode step, where the
+ * previous kernel produces q, k_new and v_new): the call then reads those
+ * while that kernel is still finishing and starts copying pages into shared
+ * memory, and waits for it only before it reads q / k_new / v_new or writes
+ * anything. Pass 0 when the promise does not hold (for example right after
+ * pkv_append or a prefill chunk that wrote the same pool).
+ */
+#define PKV_DECODE_EARLY_PREFETCH 1u
 
 /*
  * Workspace bytes pkv_prefill_chunk_attn needs (the status header).

@@ -174,10 +174,16 @@ def decode_attn(q, k_pages, v_pages, block_table, seq_lens, out, scale: float, w
     _check(rc, "pkv_decode_attn")
 
 
+EARLY_PREFETCH = 1  # PKV_DECODE_EARLY_PREFETCH
+
+
 def decode_append_attn(q, k_new, v_new, k_pages, v_pages, block_table, seq_lens, out, scale: float,
-                       workspace: Workspace, stream=None):
+                       workspace: Workspace, stream=None, early_prefetch: bool = False):
     """One decode step of one layer in one launch: write k_new / v_new [B, 8, 128] at position
-    seq_lens[b] - 1 of each request, then decode attention over seq_lens[b] positions."""
+    seq_lens[b] - 1 of each request, then decode attention over seq_lens[b] positions.
+
+    early_prefetch: the previous kernel on the stream writes neither the pools nor the block
+    table nor the lengths, so they may be read while it finishes (PKV_DECODE_EARLY_PREFETCH)."""
     import torch
 
     _need(k_pages, torch.bfloat16, "k_pages")
@@ -198,7 +204,7 @@ def decode_append_attn(q, k_new, v_new, k_pages, v_pages, block_table, seq_lens,
     rc = _lib.load().pkv_decode_append_attn(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_pages), _ptr(v_pages),
                                             _ptr(block_table), _ptr(seq_lens), _ptr(out), float(scale),
                                             _stream(stream), ctypes.byref(d), B, block_table.shape[1], _ptr(ws),
-                                            ws.numel())
+                                            ws.numel(), EARLY_PREFETCH if early_prefetch else 0)
     _check(rc, "pkv_decode_append_attn")
 
 

@@ -88,6 +88,8 @@ struct DecodeArgs {
   const int* seq_lens;
   __nv_bfloat16* out;
   float qscale;  // scale * log2(e)
+  int early;     // prefetch before the grid dependency (caller guarantees the predecessor leaves
+                 // pools, block table and lengths alone)
   int batch;
   int max_pages;
   int num_pages;
@@ -190,8 +192,18 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
     mbar_init(&full[tid], 1);
     mbar_init(&empty[tid], 1);
   }
-  grid_dependency_wait();  // every argument buffer may come from the previous kernel in the stream
-  allow_dependents();
+  // Every argument buffer may come from the previous kernel in the stream, so
+  // the kernel waits for it before touching them -- except in early mode, where
+  // the caller guarantees that the predecessor writes neither the pools nor the
+  // block table nor the lengths: then the length scan, the share decoding and
+  // the first bulk copies overlap the predecessor's tail, and each warp waits
+  // only before it reads q / k_new / v_new or writes anything. Dependents are
+  // released only after this grid's own wait, so the kernel two launches back
+  // has always completed when a successor starts early.
+  if (!a.early) {
+    grid_dependency_wait();
+    allow_dependents();
+  }
 
   // seq lens (clamped) and the exclusive prefix of (KV head, page) pairs per request
   if (warp == 0) {
@@ -223,20 +235,29 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
   fence_barrier_init();
   __syncthreads();
 
-  // zero output rows of empty requests (graph-bucket padding)
-  for (int b = blockIdx.x; b < batch; b += gridDim.x) {
-    if (sl[b] == 0) {
-      uint4* o = reinterpret_cast<uint4*>(a.out + static_cast<size_t>(b) * kQHeads * kHeadDim);
-      for (int i = tid; i < kQHeads * kHeadDim / 8; i += kDecThreads) o[i] = make_uint4(0, 0, 0, 0);
-    }
-  }
-
   // Only min(gridDim.x, T) CTAs take a share, so that every share is non-empty
   // and the CTAs between the first and last holder of a (request, KV head) all
   // hold a piece of it.
   const long long T = pref[batch];
   const int G = static_cast<int>(T < gridDim.x ? T : gridDim.x);
-  if (static_cast<int>(blockIdx.x) >= G) return;
+  // zero output rows of empty requests (graph-bucket padding): CTA c clears rows
+  // c, c + gridDim.x, ...; in early mode only after the grid dependency
+  auto zero_empty_rows = [&](int first_thread, int nthreads) {
+    for (int b = blockIdx.x; b < batch; b += gridDim.x) {
+      if (sl[b] == 0) {
+        uint4* o = reinterpret_cast<uint4*>(a.out + static_cast<size_t>(b) * kQHeads * kHeadDim);
+        for (int i = tid - first_thread; i < kQHeads * kHeadDim / 8; i += nthreads) o[i] = make_uint4(0, 0, 0, 0);
+      }
+    }
+  };
+  if (static_cast<int>(blockIdx.x) >= G) {
+    if (a.early) {
+      grid_dependency_wait();
+      allow_dependents();
+    }
+    zero_empty_rows(0, kDecThreads);
+    return;
+  }
   const long long lo = share_lo(blockIdx.x, T, G);
   const long long hi = share_lo(blockIdx.x + 1, T, G);
 
@@ -256,6 +277,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
 #pragma unroll
     for (int c = 0; c < kCons; ++c) base[c] = 0;
     bool pfail = false;
+    bool waited = !a.early;
     for (long long f0 = lo; f0 < hi && !pfail; f0 += 32) {
       const long long f = f0 + lane;
       const bool valid = f < hi;
@@ -287,6 +309,11 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
       int rounds = valid ? my_round + 1 : 0;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) rounds = max(rounds, __shfl_xor_sync(kFull, rounds, o));
+      if (!waited && __any_sync(kFull, wslot >= 0)) {  // new rows come from the predecessor
+        grid_dependency_wait();
+        allow_dependents();
+        waited = true;
+      }
       for (int r = 0; r < rounds; ++r) {
         if (valid && my_round == r && !pfail) {
           if (use > 0 && !mbar_wait_bounded(&empty[slot], static_cast<uint32_t>(use - 1) & 1u)) {
@@ -322,6 +349,10 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
       }
       pfail = __any_sync(kFull, pfail);
     }
+    if (!waited) {
+      grid_dependency_wait();
+      allow_dependents();
+    }
     return;
   }
 
@@ -333,6 +364,12 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
   const int hf = lane >> 4;        // half-warp: tokens hf*8 .. hf*8+7 for the V pass
   const int dl = lane & 15;        // dims dl*8 .. dl*8+7 for the V pass
   const uint32_t pb = smem_u32(pbuf + warp * kPageSize * 4);
+
+  if (a.early) {
+    grid_dependency_wait();
+    allow_dependents();
+  }
+  zero_empty_rows(0, kConsThreads);
 
   int k = 0;  // pages of this warp's sequence visited so far
   bool failed = false;
@@ -648,7 +685,8 @@ size_t decode_workspace_bytes(int32_t batch, int num_sms) {
 
 int launch_decode(const void* q, const void* k_new, const void* v_new, const void* k_pages, const void* v_pages,
                   const int32_t* block_table, const int32_t* seq_lens, void* out, float scale, int32_t batch,
-                  int32_t max_pages, int32_t num_pages, void* workspace, int num_sms, cudaStream_t stream) {
+                  int32_t max_pages, int32_t num_pages, void* workspace, int num_sms, cudaStream_t stream,
+                  uint32_t flags) {
   if (batch == 0) return PKV_OK;
   const size_t smem = decode_smem_bytes(batch);
   static bool attr_set[64] = {false};
@@ -677,6 +715,7 @@ int launch_decode(const void* q, const void* k_new, const void* v_new, const voi
   a.seq_lens = seq_lens;
   a.out = static_cast<__nv_bfloat16*>(out);
   a.qscale = scale * kLog2e;
+  a.early = (flags & PKV_DECODE_EARLY_PREFETCH) ? 1 : 0;
   a.batch = batch;
   a.max_pages = max_pages;
   a.num_pages = num_pages;

@@ -142,13 +142,14 @@ int pkv_decode_attn(const void* q, const void* k_pages, const void* v_pages, con
   if (rc != PKV_OK) return rc;
   if (workspace_bytes < pkv::decode_workspace_bytes(batch, sms)) return PKV_ERR_WORKSPACE_TOO_SMALL;
   return pkv::launch_decode(q, nullptr, nullptr, k_pages, v_pages, block_table, seq_lens, out, scale, batch,
-                            max_pages_per_seq, desc->num_pages, workspace, sms, reinterpret_cast<cudaStream_t>(stream));
+                            max_pages_per_seq, desc->num_pages, workspace, sms, reinterpret_cast<cudaStream_t>(stream),
+                            0u);
 }
 
 int pkv_decode_append_attn(const void* q, const void* k_new, const void* v_new, void* k_pages, void* v_pages,
                            const int32_t* block_table, const int32_t* seq_lens, void* out, float scale,
                            pkv_stream_t stream, const pkv_cache_desc* desc, int32_t batch, int32_t max_pages_per_seq,
-                           void* workspace, size_t workspace_bytes) {
+                           void* workspace, size_t workspace_bytes, uint32_t flags) {
   int rc = check_desc(desc);
   if (rc != PKV_OK) return rc;
   if (batch < 0 || max_pages_per_seq < 1) return PKV_ERR_BAD_SHAPE;
@@ -164,8 +165,10 @@ int pkv_decode_append_attn(const void* q, const void* k_new, const void* v_new, 
   rc = current_device(&sms);
   if (rc != PKV_OK) return rc;
   if (workspace_bytes < pkv::decode_workspace_bytes(batch, sms)) return PKV_ERR_WORKSPACE_TOO_SMALL;
+  if ((flags & ~static_cast<uint32_t>(PKV_DECODE_EARLY_PREFETCH)) != 0) return PKV_ERR_UNSUPPORTED;
   return pkv::launch_decode(q, k_new, v_new, k_pages, v_pages, block_table, seq_lens, out, scale, batch,
-                            max_pages_per_seq, desc->num_pages, workspace, sms, reinterpret_cast<cudaStream_t>(stream));
+                            max_pages_per_seq, desc->num_pages, workspace, sms, reinterpret_cast<cudaStream_t>(stream),
+                            flags);
 }
 
 size_t pkv_prefill_workspace_bytes(const pkv_cache_desc* desc, int32_t num_seqs, int32_t max_q_len) {

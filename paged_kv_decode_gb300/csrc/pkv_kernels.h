@@ -15,7 +15,8 @@ size_t decode_workspace_bytes(int32_t batch, int num_sms);
 // k_new / v_new (nullable): fused append of each request's new token at position seq_lens[b] - 1.
 int launch_decode(const void* q, const void* k_new, const void* v_new, const void* k_pages, const void* v_pages,
                   const int32_t* block_table, const int32_t* seq_lens, void* out, float scale, int32_t batch,
-                  int32_t max_pages, int32_t num_pages, void* workspace, int num_sms, cudaStream_t stream);
+                  int32_t max_pages, int32_t num_pages, void* workspace, int num_sms, cudaStream_t stream,
+                  uint32_t flags);
 int decode_max_batch();
 
 size_t prefill_workspace_bytes(int32_t num_seqs, int32_t max_q_len, int num_sms);

@@ -242,3 +242,49 @@ def test_fused_equals_separate_calls_bitwise(cuda_device):
     fused = _fused(case, 0, cuda_device)
     assert torch.equal(out_sep.view(torch.int16), fused.out.view(torch.int16))
     assert torch.equal(sep.k_pages.view(torch.int16), fused.k_pages.view(torch.int16))
+
+
+@pytest.mark.parametrize("early", [False, True])
+def test_fused_layer_chain_in_a_graph(cuda_device, early):
+    # two layers, each its own pool, replayed from a CUDA graph; with early prefetch each
+    # layer's kernel may start reading its pool while the previous layer's kernel finishes
+    case = W.decode_case(19, W.config_seq_lens(2), layers=2, pending_append=True, poison=True)
+    runs = [DecodeOnDevice(case, layer, cuda_device) for layer in range(2)]
+
+    def step():
+        for r in runs:
+            pkv.decode_append_attn(r.q, r.k_new, r.v_new, r.k_pages, r.v_pages, r.block_table, r.seq_lens, r.out,
+                                   case.geom.scale, r.ws, early_prefetch=early)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for r in runs:
+        r.out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    for layer, r in enumerate(runs):
+        want_k, want_v = oracle.append(case.k_new[layer], case.v_new[layer], case.slot_mapping,
+                                       case.k_pages[layer], case.v_pages[layer])
+        assert np.array_equal(bits(r.k_pages), want_k) and np.array_equal(bits(r.v_pages), want_v)
+        want = oracle.decode(case.q[layer], want_k, want_v, case.block_table, case.seq_lens, case.geom.scale)
+        assert_close(bf16_to_f64(r.out), want, f"graph layer {layer} early={early}")
+        assert r.ws.status() == 0
+
+
+def test_fused_rejects_unknown_flags(cuda_device):
+    case = W.decode_case(20, [40, 50], pending_append=True)
+    run = DecodeOnDevice(case, 0, cuda_device)
+    from paged_kv_decode_gb300 import _lib
+    import ctypes
+    d = pkv.desc(case.num_pages)
+    rc = _lib.load().pkv_decode_append_attn(run.q.data_ptr(), run.k_new.data_ptr(), run.v_new.data_ptr(),
+                                            run.k_pages.data_ptr(), run.v_pages.data_ptr(), run.block_table.data_ptr(),
+                                            run.seq_lens.data_ptr(), run.out.data_ptr(), 1.0, None, ctypes.byref(d),
+                                            2, case.max_pages, run.ws.tensor.data_ptr(), run.ws.nbytes, 6)
+    assert rc == -3
