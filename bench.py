@@ -523,6 +523,7 @@ def main():
     e2e_dt, e2e_value = replica_rate(e2e_dt, e2e_steps, world, dist_on)
 
     hbm, bf16, peak_kind = _peaks()
+    main_fused = step.fused
     dec_bytes = step.decode_bytes()
     isolated = dec_bytes / (dec_ms * 1e-3) / 1e9
     if step.fused:
@@ -533,7 +534,7 @@ def main():
     else:
         launch_us = dec_ms * 1e3
         achieved = isolated
-    step_bytes = args.layers * (dec_bytes + step.append_bytes())
+    step_bytes = args.layers * (dec_bytes + (0 if step.fused else step.append_bytes()))
     pool_bytes = 2 * step.k_pages.numel() * step.k_pages.element_size()
 
     extra = {}
@@ -592,7 +593,7 @@ def main():
         "roofline": {"bound": "hbm", "kernel": "pkv::decode_kernel", "achieved": achieved, "peak": hbm,
                      "unit": "GB/s", "frac": achieved / hbm, "traffic": _decode_traffic(), "peak_kind": peak_kind,
                      "algorithmic_bytes_per_launch": dec_bytes, "launch_us": launch_us,
-                     "launch_us_basis": "timed region / launches" if step.fused else "per-launch events",
+                     "launch_us_basis": "timed region / launches" if main_fused else "per-launch events",
                      "isolated_launch_us": dec_ms * 1e3, "isolated_achieved": isolated,
                      "isolated_launches_timed": dec_n, "frac_of_nominal_8tbs": achieved / 8000.0},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

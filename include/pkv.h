@@ -275,6 +275,19 @@ int pkv_decode_attn_noalloc(const void* q, const void* k_pages, const void* v_pa
                             const int32_t* seq_lens, void* out, float scale, pkv_stream_t stream,
                             const pkv_cache_desc* desc, int32_t batch, int32_t max_pages_per_seq);
 
+/*
+ * pkv_selftest_wait_timeout -- diagnostic of the bounded device waits.
+ *
+ * Not a step of the attention path (the pages have no counterpart): it runs
+ * one CTA that waits, through the same bounded-wait helper the kernels use,
+ * on a shared-memory barrier that nothing ever completes, for at most
+ * limit_cycles SM clock cycles (<= 2^32), and then writes
+ * PKV_ERR_DEVICE_TIMEOUT into the workspace status word. Shows that a wait
+ * which runs out ends the kernel with an error the host can read
+ * (pkv_read_status) and leaves the context usable.
+ */
+int pkv_selftest_wait_timeout(void* workspace, size_t workspace_bytes, int64_t limit_cycles, pkv_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

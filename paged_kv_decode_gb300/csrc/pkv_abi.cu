@@ -203,4 +203,14 @@ int pkv_prefill_chunk_attn(const void* q, const void* k_pages, const void* v_pag
                              reinterpret_cast<cudaStream_t>(stream));
 }
 
+int pkv_selftest_wait_timeout(void* workspace, size_t workspace_bytes, int64_t limit_cycles, pkv_stream_t stream) {
+  if (workspace == nullptr) return PKV_ERR_NULL_ARG;
+  if (workspace_bytes < PKV_STATUS_BYTES) return PKV_ERR_WORKSPACE_TOO_SMALL;
+  if (limit_cycles < 0 || limit_cycles > (1LL << 32)) return PKV_ERR_BAD_SHAPE;
+  int sms = 0;
+  const int rc = current_device(&sms);
+  if (rc != PKV_OK) return rc;
+  return pkv::launch_wait_timeout_selftest(workspace, limit_cycles, reinterpret_cast<cudaStream_t>(stream));
+}
+
 }  // extern "C"

@@ -25,4 +25,6 @@ int launch_prefill(const void* q, const void* k_pages, const void* v_pages, cons
                    void* out, float scale, int32_t max_pages, int32_t max_q_len, int32_t num_pages, void* workspace,
                    cudaStream_t stream);
 
+int launch_wait_timeout_selftest(void* workspace, long long limit_cycles, cudaStream_t stream);
+
 }  // namespace pkv
