@@ -49,7 +49,7 @@ WORKLOAD = ("qwen3-0.6b decode step: 28 layers x bs16, 16q/8kv heads, d128, page
 # DRAM traffic of one decode launch on this workload's per-layer pool, from one ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the decode kernel source it was
 # measured on (sha256 prefix of csrc/decode.cu); any other source reports null.
-NCU_DECODE_TRAFFIC = {"4311005b0f2bebf6": 107_391_744 + 3_180_800}
+NCU_DECODE_TRAFFIC = {"4f0615c7e3b0a402": 107_382_528 + 3_103_232}
 
 
 def _decode_traffic():
