@@ -69,10 +69,15 @@ constexpr int kSmemRing = kStages * kStageBytes;
 constexpr int kSmemBars = 2 * kStages * 8;                 // full + empty barrier per stage
 constexpr int kMergeFloats = kCons * kPieceFloats;         // one record per consumer warp
 constexpr int kSmemMerge = kMergeFloats * 4;
+constexpr int kQBufBytes = kGroup * kRowBytes;             // query rows of one (request, KV head), both heads
+constexpr int kSmemQ = 2 * kQBufBytes;                     // this piece's rows and the next piece's
 constexpr int kSmemPbuf = kCons * kPageSize * 4 * 4;       // per warp: [16 tokens][p0, p0, p1, p1]
-constexpr int kSmemSplit = kCons * 2 * 4;                  // per consumer warp: running max of both heads
 constexpr int kSmemMisc = 16;                              // flag words
-constexpr int kSmemFixed = kSmemRing + kSmemBars + kSmemMerge + kSmemPbuf + kSmemSplit + kSmemMisc;
+constexpr int kSmemFixed = kSmemRing + kSmemBars + kSmemMerge + kSmemQ + kSmemPbuf + kSmemMisc;
+constexpr int kPieceBytes = kPieceFloats * 4;
+constexpr int kMergeCap = kSmemRing / kPieceBytes;         // partial records staged per batch of the final merge
+static_assert((kSmemRing + kSmemBars) % 16 == 0 && kSmemMerge % 16 == 0 && kPieceBytes % 16 == 0, "alignment");
+static_assert(kQBufBytes == 32 * 16, "one 16-byte chunk of a group's query rows per lane");
 
 static size_t decode_smem_bytes(int batch) { return kSmemFixed + static_cast<size_t>(2 * batch + 1) * 4; }
 
@@ -176,11 +181,11 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
   unsigned char* ring = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kSmemRing);
   uint64_t* empty = full + kStages;
-  float* merge = reinterpret_cast<float*>(empty + kStages);
-  float* pbuf = merge + kMergeFloats;
-  float* split = pbuf + kCons * kPageSize * 4;
-  int* flag = reinterpret_cast<int*>(split + kCons * 2);
-  int* pref = reinterpret_cast<int*>(reinterpret_cast<unsigned char*>(flag) + kSmemMisc);
+  float* merge = reinterpret_cast<float*>(smem + kSmemRing + kSmemBars);
+  unsigned char* qbuf = reinterpret_cast<unsigned char*>(merge + kMergeFloats);
+  float* pbuf = reinterpret_cast<float*>(qbuf + kSmemQ);
+  int* flag = reinterpret_cast<int*>(pbuf + kCons * kPageSize * 4);  // [0..1] merge flags, [2] a wait failed
+  int* pref = flag + kSmemMisc / 4;
   int* sl = pref + a.batch + 1;
 
   const int tid = threadIdx.x;
@@ -192,6 +197,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
     mbar_init(&full[tid], 1);
     mbar_init(&empty[tid], 1);
   }
+  if (tid == kStages) flag[2] = 0;
   // Every argument buffer may come from the previous kernel in the stream, so
   // the kernel waits for it before touching them -- except in early mode, where
   // the caller guarantees that the predecessor writes neither the pools nor the
@@ -373,26 +379,64 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
 
   int k = 0;  // pages of this warp's sequence visited so far
   bool failed = false;
-  long long f = lo;
+
+  // Warp 0 stages the query rows of a piece in qbuf[buf], one 16-byte chunk per
+  // lane, so that the next piece's rows are on chip before the current one ends.
+  const uint32_t qb = smem_u32(qbuf);
+  auto stage_q = [&](const Piece& p, int buf) {
+    if (warp == 0) {
+      const unsigned char* src =
+          reinterpret_cast<const unsigned char*>(a.q + (static_cast<size_t>(p.b) * kQHeads + p.h * kGroup) * kHeadDim);
+      cp_async16(qb + buf * kQBufBytes + lane * 16, src + lane * 16);
+    }
+  };
+  // CTAs cfirst .. cfirst + n - 1 hold the pieces of (request b, KV head h); the
+  // record of CTA c is in slot 2c, or 2c + 1 when it is the second split piece
+  // of c's share (first_has_two: the first holder's share starts before (b, h)).
+  auto span_of = [&](int b, int h, int& cfirst, int& n, bool& first_has_two) {
+    const int np = (pref[b + 1] - pref[b]) / kKVHeads;
+    const long long fseg = pref[b] + static_cast<long long>(h) * np;
+    cfirst = cta_of(fseg, T, G);
+    n = cta_of(fseg + np - 1, T, G) - cfirst + 1;
+    first_has_two = share_lo(cfirst, T, G) < fseg;
+  };
+  // Split pieces whose partial records are written but not yet counted: only
+  // the first and the last piece of a share can be split, and both are counted
+  // together after the last piece, so that no piece boundary waits on a fence
+  // or an atomic.
+  int npend = 0;
+  int pb0 = 0, ph0 = 0, pc0 = 0, pn0 = 0, pb1 = 0, ph1 = 0, pc1 = 0, pn1 = 0;
+  bool pt0 = false, pt1 = false;
+
   Piece pc;
-  while (find_piece(f, hi, pref, batch, pc)) {
+  bool have = find_piece(lo, hi, pref, batch, pc);
+  if (have) stage_q(pc, 0);
+  if (warp == 0) cp_async_wait_all();
+  consumer_sync();
+  for (int j = 0; have; ++j) {
+    Piece nx;
+    const bool have_next = find_piece(pc.fend, hi, pref, batch, nx);
+    if (have_next) stage_q(nx, (j + 1) & 1);
     const int b = pc.b;
     const int h = pc.h;
+    const bool complete = (pc.p0 == 0 && pc.p1 == pc.np);
+    int sp_cfirst = 0, sp_n = 0;
+    bool sp_two = false;
+    if (!complete) span_of(b, h, sp_cfirst, sp_n, sp_two);  // before the stream, off the critical path
 
     // query rows of both heads of the group, in this lane's chunk order, pre-scaled
+    const uint32_t qcur = qb + (j & 1) * kQBufBytes;
     float2 q2[4][4][2];
 #pragma unroll
     for (int i = 0; i < kGroup; ++i) {
-      const uint4* qrow =
-          reinterpret_cast<const uint4*>(a.q + (static_cast<size_t>(b) * kQHeads + h * kGroup + i) * kHeadDim);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint4 u = __ldg(qrow + qq + 4 * (j ^ tp));
+      for (int jj = 0; jj < 4; ++jj) {
+        const uint4 u = lds128(qcur + i * kRowBytes + (qq + 4 * (jj ^ tp)) * 16);
         const float2 sc = make_float2(a.qscale, a.qscale);
-        q2[j][0][i] = __fmul2_rn(bf2_to_f2(u.x), sc);
-        q2[j][1][i] = __fmul2_rn(bf2_to_f2(u.y), sc);
-        q2[j][2][i] = __fmul2_rn(bf2_to_f2(u.z), sc);
-        q2[j][3][i] = __fmul2_rn(bf2_to_f2(u.w), sc);
+        q2[jj][0][i] = __fmul2_rn(bf2_to_f2(u.x), sc);
+        q2[jj][1][i] = __fmul2_rn(bf2_to_f2(u.y), sc);
+        q2[jj][2][i] = __fmul2_rn(bf2_to_f2(u.z), sc);
+        q2[jj][3][i] = __fmul2_rn(bf2_to_f2(u.w), sc);
       }
     }
 
@@ -410,7 +454,10 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
       if (!failed) {
         const bool ok = mbar_wait_bounded(&full[slot], parity);
         failed = __any_sync(kFull, !ok);
-        if (failed && lane == 0) set_status(a.status, PKV_ERR_DEVICE_TIMEOUT);
+        if (failed && lane == 0) {
+          set_status(a.status, PKV_ERR_DEVICE_TIMEOUT);
+          flag[2] = 1;
+        }
       }
       if (!failed) {
         const int rem = sl[b] - p * kPageSize;
@@ -548,8 +595,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
       M[i] = m;
       L[i] = l;
     }
-    const bool owns_dims = tid < kHeadDim;  // threads past the first 128 only help in the split merge
-    const bool complete = (pc.p0 == 0 && pc.p1 == pc.np);
+    const bool owns_dims = tid < kHeadDim;
     __nv_bfloat16* orow = a.out + (static_cast<size_t>(b) * kQHeads + h * kGroup) * kHeadDim;
     if (complete) {
       if (owns_dims) {
@@ -561,10 +607,6 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
         }
       }
     } else {
-      const long long fseg = pref[b] + static_cast<long long>(h) * pc.np;
-      const int cfirst = cta_of(fseg, T, G);
-      const int clast = cta_of(fseg + pc.np - 1, T, G);
-      const bool first_has_two = share_lo(cfirst, T, G) < fseg;  // cfirst's piece is its second record
       const int my_slot = 2 * blockIdx.x + (pc.fstart == lo ? 0 : 1);
       float* rec = a.partials + static_cast<size_t>(my_slot) * kPieceFloats;
       if (owns_dims) {
@@ -581,97 +623,156 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
         rec[kRec] = M[1];
         rec[kRec + 1] = L[1];
       }
-      consumer_sync();
-      if (tid == 0) {
-        __threadfence();
-        const int old = atomicAdd(a.counters + b * kKVHeads + h, 1);
-        flag[0] = (old == clast - cfirst) ? 1 : 0;
+      if (npend == 0) {
+        pb0 = b, ph0 = h, pc0 = sp_cfirst, pn0 = sp_n, pt0 = sp_two;
+      } else {
+        pb1 = b, ph1 = h, pc1 = sp_cfirst, pn1 = sp_n, pt1 = sp_two;
       }
-      consumer_sync();
-      if (flag[0]) {
-        // This CTA holds the last piece: merge all partial records of (b, h).
-        // Warp w folds records w, w + kCons, ... online (running max, rescaled
-        // sums), 8 records in flight, one float4 of both heads' o per lane; the
-        // warps' states are then merged through the (free) merge buffer.
-        __threadfence();
-        const int n = clast - cfirst + 1;
-        auto rec_of = [&](int t) {
-          const int c = cfirst + t;
-          return a.partials + static_cast<size_t>(2 * c + ((t == 0 && first_has_two) ? 1 : 0)) * kPieceFloats;
-        };
-        float wm0 = -CUDART_INF_F, wm1 = -CUDART_INF_F, wl0 = 0.f, wl1 = 0.f;
-        float4 wo0 = make_float4(0.f, 0.f, 0.f, 0.f), wo1 = wo0;
-        for (int t0 = warp; t0 < n; t0 += 8 * kCons) {
-          float mm0[8], mm1[8], ll0[8], ll1[8];
-          float4 oo0[8], oo1[8];
+      ++npend;
+    }
+    if (warp == 0) cp_async_wait_all();  // the next piece's query rows have landed
+    consumer_sync();                     // merge buffer and qbuf[j & 1] free, qbuf[(j + 1) & 1] visible
+    pc = nx;
+    have = have_next;
+  }
+  if (npend == 0) return;
+
+  // Count this CTA's records in (release) and learn whether it completed a count
+  // (acquire): the CTA that does merges every record of that (request, KV head).
+  if (tid == 0) {
+    __threadfence();
+    const int old0 = atomicAdd(a.counters + pb0 * kKVHeads + ph0, 1);
+    const int old1 = npend > 1 ? atomicAdd(a.counters + pb1 * kKVHeads + ph1, 1) : -1;
+    __threadfence();
+    flag[0] = old0 == pn0 - 1 ? 1 : 0;
+    flag[1] = old1 == pn1 - 1 ? 1 : 0;
+  }
+  consumer_sync();
+  if (flag[2] != 0) {  // a wait failed: copies may still land in the ring, merge nothing
+    if (tid == 0) {
+      if (flag[0]) a.counters[pb0 * kKVHeads + ph0] = 0;
+      if (flag[1]) a.counters[pb1 * kKVHeads + ph1] = 0;
+    }
+    return;
+  }
+  // Final merges (log-sum-exp over the partial records) of the pairs whose count
+  // this CTA completed. Their records are staged in the drained stage ring by
+  // 16-byte asynchronous copies (one round trip per batch of up to kMergeCap
+  // records); record t of a pair is folded by warp t % kCons, each lane owning
+  // dims 4 lane .. 4 lane + 3 of both heads, and the warps' states are then
+  // combined through the merge buffer. Which warp folds which record, and the
+  // batch boundaries, depend only on the pair, so the result is the same
+  // whichever CTA merges.
+  const int nm0 = flag[0] ? pn0 : 0;
+  const int nm1 = flag[1] ? pn1 : 0;
+  if (nm0 + nm1 == 0) return;
+  const uint32_t ring_s = smem_u32(ring);
+  const float* R = reinterpret_cast<const float*>(ring);
+  constexpr int kChunks = kPieceBytes / 16;
+  static_assert(kChunks > 64 && kChunks <= 96, "a record is copied in three lane-strided passes");
+  static_assert(kConsThreads >= kHeadDim, "the final combine maps one thread to one dim");
+  float fm[2][2], fl[2][2];
+  float4 fo[2][2];
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int t = t0 + u * kCons;
-            mm0[u] = mm1[u] = -CUDART_INF_F;
-            ll0[u] = ll1[u] = 0.f;
-            oo0[u] = oo1[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (t < n) {
-              const float* r = rec_of(t);
-              mm0[u] = __ldcg(r);
-              ll0[u] = __ldcg(r + 1);
-              mm1[u] = __ldcg(r + kRec);
-              ll1[u] = __ldcg(r + kRec + 1);
-              oo0[u] = __ldcg(reinterpret_cast<const float4*>(r + 4) + lane);
-              oo1[u] = __ldcg(reinterpret_cast<const float4*>(r + kRec + 4) + lane);
-            }
-          }
+  for (int i = 0; i < 2; ++i)
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            if (mm0[u] == -CUDART_INF_F) continue;  // past the last record
-            const float n0 = fmaxf(wm0, mm0[u]), n1 = fmaxf(wm1, mm1[u]);
-            const float a0 = ex2(wm0 - n0), b0 = ex2(mm0[u] - n0);
-            const float a1 = ex2(wm1 - n1), b1 = ex2(mm1[u] - n1);
-            wl0 = wl0 * a0 + ll0[u] * b0;
-            wl1 = wl1 * a1 + ll1[u] * b1;
-            wo0 = make_float4(wo0.x * a0 + oo0[u].x * b0, wo0.y * a0 + oo0[u].y * b0, wo0.z * a0 + oo0[u].z * b0,
-                              wo0.w * a0 + oo0[u].w * b0);
-            wo1 = make_float4(wo1.x * a1 + oo1[u].x * b1, wo1.y * a1 + oo1[u].y * b1, wo1.z * a1 + oo1[u].z * b1,
-                              wo1.w * a1 + oo1[u].w * b1);
-            wm0 = n0;
-            wm1 = n1;
-          }
+    for (int hh = 0; hh < 2; ++hh) {
+      fm[i][hh] = -CUDART_INF_F;
+      fl[i][hh] = 0.f;
+      fo[i][hh] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  // One batch: records [t0[i], t1[i]) of pair i, pair 0's first in the ring.
+  auto merge_batch = [&](const int (&t0)[2], const int (&t1)[2]) {
+    const int c0 = t1[0] - t0[0], nb = c0 + t1[1] - t0[1];
+    for (int p = warp; p < nb; p += kCons) {
+      const bool second = p >= c0;
+      const int t = second ? t0[1] + p - c0 : t0[0] + p;
+      const int cf = second ? pc1 : pc0;
+      const bool two = second ? pt1 : pt0;
+      const size_t slot = 2 * static_cast<size_t>(cf + t) + ((t == 0 && two) ? 1 : 0);
+      const unsigned char* src = reinterpret_cast<const unsigned char*>(a.partials + slot * kPieceFloats);
+      const uint32_t dst = ring_s + p * kPieceBytes;
+      cp_async16(dst + lane * 16, src + lane * 16);
+      cp_async16(dst + (lane + 32) * 16, src + (lane + 32) * 16);
+      if (lane < kChunks - 64) cp_async16(dst + (lane + 64) * 16, src + (lane + 64) * 16);
+    }
+    cp_async_wait_all();
+    consumer_sync();
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int ps = i == 0 ? 0 : c0;             // ring position of record t0[i]
+      const int pe = ps + t1[i] - t0[i];
+      const int pfirst = ps + ((warp - t0[i]) % kCons + kCons) % kCons;  // this warp's first record t
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        float m = fm[i][hh];
+        for (int p = pfirst; p < pe; p += kCons) m = fmaxf(m, R[p * kPieceFloats + hh * kRec]);
+        const float keep = fm[i][hh] == -CUDART_INF_F ? 0.f : ex2(fm[i][hh] - m);
+        float l = fl[i][hh] * keep;
+        float4 o = fo[i][hh];
+        o.x *= keep, o.y *= keep, o.z *= keep, o.w *= keep;
+#pragma unroll 4
+        for (int p = pfirst; p < pe; p += kCons) {
+          const float* r = R + p * kPieceFloats + hh * kRec;
+          const float sc = ex2(r[0] - m);
+          l += r[1] * sc;
+          const float4 v = reinterpret_cast<const float4*>(r + 4)[lane];  // plain load: schedulable across records
+          o.x += v.x * sc, o.y += v.y * sc, o.z += v.z * sc, o.w += v.w * sc;
         }
-        float* mw = merge + warp * kPieceFloats;  // same record format as the piece merge
-        reinterpret_cast<float4*>(mw + 4)[lane] = wo0;
-        reinterpret_cast<float4*>(mw + kRec + 4)[lane] = wo1;
-        if (lane == 0) {
-          mw[0] = wm0;
-          mw[1] = wl0;
-          mw[kRec] = wm1;
-          mw[kRec + 1] = wl1;
-        }
-        consumer_sync();
-        if (owns_dims) {
-#pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            float m = -CUDART_INF_F;
-#pragma unroll
-            for (int w = 0; w < kCons; ++w) m = fmaxf(m, merge[w * kPieceFloats + i * kRec]);
-#pragma unroll
-            for (int e = 0; e < kDimsPerThread; ++e) {
-              const int d = tid + e * kConsThreads;
-              float lsum = 0.f, acc = 0.f;
-#pragma unroll
-              for (int w = 0; w < kCons; ++w) {
-                const float* r = merge + w * kPieceFloats + i * kRec;
-                const float sc = r[0] == -CUDART_INF_F ? 0.f : ex2(r[0] - m);  // warps without records
-                lsum += r[1] * sc;
-                acc += r[4 + d] * sc;
-              }
-              orow[i * kHeadDim + d] = __float2bfloat16_rn(acc / lsum);
-            }
-          }
-        }
-        if (tid == 0) a.counters[b * kKVHeads + h] = 0;
+        fm[i][hh] = m;
+        fl[i][hh] = l;
+        fo[i][hh] = o;
       }
     }
-    consumer_sync();  // merge buffer, flag and split staging are free for the next piece
-    f = pc.fend;
+    consumer_sync();  // the ring is free for the next batch
+  };
+  if (nm0 + nm1 <= kMergeCap) {
+    const int t0[2] = {0, 0}, t1[2] = {nm0, nm1};
+    merge_batch(t0, t1);
+  } else {
+    for (int t = 0; t < nm0; t += kMergeCap) {
+      const int t0[2] = {t, 0}, t1[2] = {t + kMergeCap < nm0 ? t + kMergeCap : nm0, 0};
+      merge_batch(t0, t1);
+    }
+    for (int t = 0; t < nm1; t += kMergeCap) {
+      const int t0[2] = {0, t}, t1[2] = {0, t + kMergeCap < nm1 ? t + kMergeCap : nm1};
+      merge_batch(t0, t1);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    if ((i == 0 ? nm0 : nm1) == 0) continue;
+    float* mw = merge + warp * kPieceFloats;
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      reinterpret_cast<float4*>(mw + hh * kRec + 4)[lane] = fo[i][hh];
+      if (lane == 0) {
+        mw[hh * kRec] = fm[i][hh];
+        mw[hh * kRec + 1] = fl[i][hh];
+      }
+    }
+    consumer_sync();
+    const int b = i ? pb1 : pb0, h = i ? ph1 : ph0;
+    if (tid < kHeadDim) {
+      __nv_bfloat16* orow = a.out + (static_cast<size_t>(b) * kQHeads + h * kGroup) * kHeadDim;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        float m = -CUDART_INF_F;
+#pragma unroll
+        for (int w = 0; w < kCons; ++w) m = fmaxf(m, merge[w * kPieceFloats + hh * kRec]);
+        float l = 0.f, acc = 0.f;
+#pragma unroll
+        for (int w = 0; w < kCons; ++w) {
+          const float* r = merge + w * kPieceFloats + hh * kRec;
+          const float sc = r[0] == -CUDART_INF_F ? 0.f : ex2(r[0] - m);  // warps that folded no record
+          l += r[1] * sc;
+          acc += r[4 + tid] * sc;
+        }
+        orow[hh * kHeadDim + tid] = __float2bfloat16_rn(acc / l);
+      }
+    }
+    if (tid == 0) a.counters[b * kKVHeads + h] = 0;
+    consumer_sync();  // merge buffer free for the second pair
   }
 }
 
