@@ -49,7 +49,7 @@ WORKLOAD = ("qwen3-0.6b decode step: 28 layers x bs16, 16q/8kv heads, d128, page
 # DRAM traffic of one decode launch on this workload's per-layer pool, from one ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the decode kernel source it was
 # measured on (sha256 prefix of csrc/decode.cu); any other source reports null.
-NCU_DECODE_TRAFFIC = {"4f0615c7e3b0a402": 107_382_528 + 3_103_232}
+NCU_DECODE_TRAFFIC = {"e6939e0577a1be15": 107_394_560 + 3_320_064}
 
 
 def _decode_traffic():
@@ -564,6 +564,11 @@ def main():
         extra["long_context_40k"] = {
             "workload": "long-audio decode: 28 layers x bs1, context 40000, same geometry",
             "ms_per_step": lt, "steps_per_s": 1e3 / lt,
+            # in the step, like the headline roofline: step time / layers per launch
+            "launch_us_in_step": lt * 1e3 / args.layers,
+            "gbps_in_step": lb / (lt * 1e-3 / args.layers) / 1e9,
+            "frac_of_measured_hbm_in_step": lb / (lt * 1e-3 / args.layers) / 1e9 / hbm,
+            # one launch at a time, events around it
             "decode_kernel_us": ld_ms * 1e3, "decode_gbps": lb / (ld_ms * 1e-3) / 1e9,
             "frac_of_measured_hbm": lb / (ld_ms * 1e-3) / 1e9 / hbm,
         }

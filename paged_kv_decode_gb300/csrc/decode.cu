@@ -28,11 +28,17 @@
 //  * Optional fused append: the producer lane that copies a request's last
 //    page first writes the request's new K/V row for that head into it
 //    (generic stores, then a proxy fence so its own bulk copy sees them).
+//  * The query rows of the next piece are copied into shared memory (cp.async)
+//    while the current piece streams, so a piece boundary costs no round trip.
 //  * At the end of a piece the warps merge through shared memory. A piece that
 //    covers its whole (request, KV head) writes the bf16 output. Otherwise it
-//    writes an fp32 partial (m, l, o) and bumps a per-(request, KV head)
-//    counter; the CTA that brings the counter to the number of pieces merges
-//    all partials (log-sum-exp) and resets the counter to zero.
+//    writes an fp32 partial (m, l, o). Only a share's first and last piece can
+//    be split; after its last piece the CTA bumps the per-(request, KV head)
+//    counters of both at once (one fence, one round trip). The CTA that brings
+//    a counter to the number of holders stages every partial of that pair in
+//    its drained stage ring (cp.async, one round trip), merges them
+//    (log-sum-exp, in an order fixed by the pair alone) and resets the counter
+//    to zero.
 #include <math_constants.h>
 
 #include "pkv_device.cuh"
