@@ -18,7 +18,9 @@
 //  * Warp 8 (MMA) issues, per K/V tile and query head h, S_h = Q_h K^T
 //    (M = N = 128, K = 128 in 8 steps of 16) into TMEM, then, once the softmax
 //    warps have written P_h back into TMEM, O_h += P_h V with P_h as the
-//    tensor-memory A operand and V as an MN-major shared-memory B operand.
+//    tensor-memory A operand and V as an MN-major shared-memory B operand. The
+//    issue order PV_0(j) QK_0(j+1) PV_1(j) QK_1(j+1) keeps the two heads'
+//    softmaxes half a period apart, so one head's MMAs fill the other's softmax.
 //  * Warps 0-3 and 4-7 (one warpgroup per query head, one thread per row; 224
 //    registers each after a setmaxnreg rebalance, warps 10-11 only donate theirs) read
 //    S_h from TMEM, apply the scale and the causal mask, keep the running max
@@ -251,57 +253,77 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   } else if (warp == kPfMmaWarp) {
     // ------------------------------------------------------------------ MMA issuer
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kPfRegsOther));
-    if (pf_wait_warp(&bars->q_full, 0, fail, a.status)) {
-      for (int j = 0; j < n_tiles; ++j) {
-        const int st = j & 1;
-        const uint32_t ph = static_cast<uint32_t>(j >> 1) & 1u;
-        if (!pf_wait_warp(&bars->k_full[st], ph, fail, a.status)) break;
-        bool ok = true;
-        for (int h = 0; h < 2 && ok; ++h) {
-          if (j > 0 && !pf_wait_warp(&bars->o_done[h], static_cast<uint32_t>(j - 1) & 1u, fail, a.status)) ok = false;
-          tc_fence_after();
-          if (ok && lane == 0) {
-            const uint32_t qa = smem_u32(sQ + h * kPfTileBytes);
-            const uint32_t kb = smem_u32(sK + st * kPfTileBytes);
+    // Issue order QK_0(0) QK_1(0) | PV_0(j) QK_0(j+1) PV_1(j) QK_1(j+1) | ...: the
+    // two heads' softmaxes run half a period apart, so while one head's softmax
+    // works the other head's PV and next QK keep the tensor pipe busy. QK_h(j+1)
+    // overwrites S_h, which holds P_h(j), so it waits for PV_h(j) (o_done) --
+    // which also keeps O_h out of the softmax's way while it may rescale it.
+    auto issue_qk = [&](int j, int h) {
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t qa = smem_u32(sQ + h * kPfTileBytes);
+        const uint32_t kb = smem_u32(sK + (j & 1) * kPfTileBytes);
 #pragma unroll
-            for (int s = 0; s < 8; ++s) {
-              const uint32_t off = (s >> 2) * kPfHalfBytes + (s & 3) * 32;
-              mma_ss(tmem + kColS + 128 * h, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
-                     kIdescQK, s > 0 ? 1u : 0u);
-            }
-            mma_commit(&bars->s_full[h]);
-          }
-          __syncwarp();
+        for (int s = 0; s < 8; ++s) {
+          const uint32_t off = (s >> 2) * kPfHalfBytes + (s & 3) * 32;
+          mma_ss(tmem + kColS + 128 * h, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
+                 kIdescQK, s > 0 ? 1u : 0u);
         }
-        if (!ok || !pf_wait_warp(&bars->v_full[st], ph, fail, a.status)) break;
-        if (j == n_tiles - 1 && kv_end < (j + 1) * kPfKeys) {
-          // keys past the end: zero their V rows (unused slots may hold NaN and 0 * NaN = NaN)
-          const int r0 = kv_end - j * kPfKeys;
-          uint4* vbase = reinterpret_cast<uint4*>(sV + st * kPfTileBytes);
-          for (int idx = r0 * 8 + lane; idx < kPfKeys * 8; idx += 32) {
-            vbase[idx] = make_uint4(0, 0, 0, 0);
-            vbase[kPfHalfBytes / 16 + idx] = make_uint4(0, 0, 0, 0);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-        }
-        for (int h = 0; h < 2 && ok; ++h) {
-          if (!pf_wait_warp(&bars->p_full[h], static_cast<uint32_t>(j) & 1u, fail, a.status)) ok = false;
-          tc_fence_after();
-          if (ok && lane == 0) {
-            const uint32_t vb = smem_u32(sV + st * kPfTileBytes);
+        mma_commit(&bars->s_full[h]);
+      }
+      __syncwarp();
+    };
+    auto issue_pv = [&](int j, int h) {
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t vb = smem_u32(sV + (j & 1) * kPfTileBytes);
 #pragma unroll
-            for (int s = 0; s < 8; ++s) {
-              mma_ts(tmem + kColO + 128 * h, tmem + kColS + 128 * h + 8 * s,
-                     sdesc_sw128(vb + s * 2048, kPfHalfBytes, 1024), kIdescPV, (j > 0 || s > 0) ? 1u : 0u);
-            }
-            mma_commit(&bars->o_done[h]);
-          }
-          __syncwarp();
+        for (int s = 0; s < 8; ++s) {
+          mma_ts(tmem + kColO + 128 * h, tmem + kColS + 128 * h + 8 * s,
+                 sdesc_sw128(vb + s * 2048, kPfHalfBytes, 1024), kIdescPV, (j > 0 || s > 0) ? 1u : 0u);
         }
-        if (!ok) break;
-        if (lane == 0) mma_commit(&bars->kv_empty[st]);
+        mma_commit(&bars->o_done[h]);
+      }
+      __syncwarp();
+    };
+    bool ok = pf_wait_warp(&bars->q_full, 0, fail, a.status) && pf_wait_warp(&bars->k_full[0], 0, fail, a.status);
+    if (ok) {
+      issue_qk(0, 0);
+      issue_qk(0, 1);
+    }
+    for (int j = 0; j < n_tiles && ok; ++j) {
+      const int st = j & 1;
+      const uint32_t ph = static_cast<uint32_t>(j >> 1) & 1u;
+      const bool next = j + 1 < n_tiles;
+      const uint32_t ph_next = static_cast<uint32_t>((j + 1) >> 1) & 1u;
+      if (!pf_wait_warp(&bars->v_full[st], ph, fail, a.status)) break;
+      if (j == n_tiles - 1 && kv_end < (j + 1) * kPfKeys) {
+        // keys past the end: zero their V rows (unused slots may hold NaN and 0 * NaN = NaN)
+        const int r0 = kv_end - j * kPfKeys;
+        uint4* vbase = reinterpret_cast<uint4*>(sV + st * kPfTileBytes);
+        for (int idx = r0 * 8 + lane; idx < kPfKeys * 8; idx += 32) {
+          vbase[idx] = make_uint4(0, 0, 0, 0);
+          vbase[kPfHalfBytes / 16 + idx] = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
         __syncwarp();
+      }
+      const uint32_t pj = static_cast<uint32_t>(j) & 1u;
+      if (!pf_wait_warp(&bars->p_full[0], pj, fail, a.status)) break;
+      issue_pv(j, 0);
+      if (next) {
+        if (!pf_wait_warp(&bars->k_full[st ^ 1], ph_next, fail, a.status) ||
+            !pf_wait_warp(&bars->o_done[0], pj, fail, a.status))
+          break;
+        issue_qk(j + 1, 0);
+      }
+      if (!pf_wait_warp(&bars->p_full[1], pj, fail, a.status)) break;
+      issue_pv(j, 1);
+      if (lane == 0) mma_commit(&bars->kv_empty[st]);
+      __syncwarp();
+      if (next) {
+        if (!pf_wait_warp(&bars->o_done[1], pj, fail, a.status)) break;
+        issue_qk(j + 1, 1);
       }
     }
   } else if (warp < 8) {
