@@ -295,9 +295,10 @@ class PrefillStep:
         self.dq, self.dk, self.dv = c.dec_q[0], c.dec_k_new[0], c.dec_v_new[0]
         self.dslots, self.dbt, self.dlens = i32(c.dec_slot_mapping), i32(c.dec_block_table), i32(c.dec_seq_lens)
         self.dout = torch.empty_like(self.dq)
-        nb = max(pkv.decode_workspace_bytes(len(c.dec_seq_lens), c.dec_block_table.shape[1], c.num_pages),
-                 pkv.prefill_workspace_bytes(1, W.PREFILL_CHUNK, c.num_pages))
-        self.ws = pkv.Workspace(nb, device)
+        # one workspace per kind of attention call (decode and prefill keep their counters apart)
+        self.ws = pkv.Workspace(
+            pkv.decode_workspace_bytes(len(c.dec_seq_lens), c.dec_block_table.shape[1], c.num_pages), device)
+        self.pws = pkv.Workspace(pkv.prefill_workspace_bytes(1, W.PREFILL_CHUNK, c.num_pages), device)
         self.scale = c.geom.scale
         P, L = int(prefix), W.PREFILL_CHUNK
         self.pairs = L * P + L * (L + 1) // 2
@@ -305,7 +306,7 @@ class PrefillStep:
 
     def prefill(self):
         self.pkv.prefill_chunk_attn(self.q, self.k_pages, self.v_pages, self.bt, self.prefix, self.cu, self.out,
-                                    self.scale, self.case.q_lens.max(), self.ws)
+                                    self.scale, self.case.q_lens.max(), self.pws)
 
     def mixed(self):
         pkv = self.pkv

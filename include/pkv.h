@@ -51,6 +51,11 @@
  *  - A workspace must be zero-filled once before its first use
  *    (pkv_workspace_init); the kernels leave it ready for the next call. Calls
  *    that may run concurrently (different streams) need separate workspaces.
+ *  - A workspace serves one kind of attention call: decode calls
+ *    (pkv_decode_attn, pkv_decode_append_attn) or prefill calls
+ *    (pkv_prefill_chunk_attn), not both, because each keeps its split counters
+ *    where the other keeps scratch records. pkv_append uses only the status
+ *    word and may share either.
  */
 #ifndef PKV_H_
 #define PKV_H_
@@ -204,7 +209,10 @@ int pkv_decode_append_attn(const void* q, const void* k_new, const void* v_new, 
 #define PKV_DECODE_EARLY_PREFETCH 1u
 
 /*
- * Workspace bytes pkv_prefill_chunk_attn needs (the status header).
+ * Workspace bytes pkv_prefill_chunk_attn needs: the status header, split
+ * counters (num_seqs x 8 KV heads x ceil(max_q_len / 128) x 2 ints) and two
+ * fp32 partial records (2 heads x 130 x 128 floats) per SM of the current
+ * device, for query tiles whose key range is split between CTAs.
  */
 size_t pkv_prefill_workspace_bytes(const pkv_cache_desc* desc, int32_t num_seqs, int32_t max_q_len);
 
@@ -231,8 +239,10 @@ size_t pkv_prefill_workspace_bytes(const pkv_cache_desc* desc, int32_t num_seqs,
  *  total_q:      rows of q and out (host value; bounds every access)
  *  max_q_len:    host-side upper bound on any chunk length (sizes the grid;
  *                rows of longer chunks are not computed)
- *  workspace:    >= pkv_prefill_workspace_bytes(...) (status word)
- * Limits: num_pages * num_kv_heads * page_size < 2^31 rows per pool.
+ *  workspace:    >= pkv_prefill_workspace_bytes(...), zeroed once by
+ *                pkv_workspace_init (the call leaves its counters at zero)
+ * Limits: num_pages * num_kv_heads * page_size < 2^31 rows per pool;
+ * num_seqs <= 1024 (PKV_ERR_UNSUPPORTED beyond).
  */
 int pkv_prefill_chunk_attn(const void* q, const void* k_pages, const void* v_pages, const int32_t* block_table,
                            const int32_t* prefix_lens, const int32_t* cu_q_lens, int32_t num_seqs, int32_t total_q,

@@ -188,6 +188,7 @@ int pkv_prefill_chunk_attn(const void* q, const void* k_pages, const void* v_pag
   if (!table_fits(num_seqs, max_pages_per_seq)) return PKV_ERR_BAD_SHAPE;
   if (static_cast<long long>(desc->num_pages) * desc->num_kv_heads * desc->page_size >= (1LL << 31))
     return PKV_ERR_UNSUPPORTED;
+  if (num_seqs > pkv::prefill_max_seqs()) return PKV_ERR_UNSUPPORTED;
   if (workspace == nullptr) return PKV_ERR_NULL_ARG;
   if (workspace_bytes < PKV_STATUS_BYTES) return PKV_ERR_WORKSPACE_TOO_SMALL;
   if (num_seqs == 0 || max_q_len == 0 || total_q == 0) return PKV_OK;

@@ -20,6 +20,7 @@ int launch_decode(const void* q, const void* k_new, const void* v_new, const voi
 int decode_max_batch();
 
 size_t prefill_workspace_bytes(int32_t num_seqs, int32_t max_q_len, int num_sms);
+int prefill_max_seqs();
 int launch_prefill(const void* q, const void* k_pages, const void* v_pages, const int32_t* block_table,
                    const int32_t* prefix_lens, const int32_t* cu_q_lens, int32_t num_seqs, int32_t total_q,
                    void* out, float scale, int32_t max_pages, int32_t max_q_len, int32_t num_pages, void* workspace,

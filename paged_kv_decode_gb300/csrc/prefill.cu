@@ -28,8 +28,17 @@
 //    The O accumulator is rescaled in TMEM only when a row's max grows by more
 //    than 2^8 (otherwise the stale max is kept; the final O / l is unchanged).
 //  * TMEM: S_0, S_1, O_0, O_1, 128 columns each (512 allocated, 1 CTA per SM).
-//  * Grid: (query tile x KV head, request), dispatched longest causal tiles first.
+//  * Work is a list of items (request, KV head, 128-row query tile), each
+//    needing 1 + (cached + covered rows) / 128 key tiles. Two schedules, chosen
+//    on the device from the lengths: when the largest item is comparable to
+//    a CTA's fair share, one CTA per item, dispatched heaviest first (the
+//    hardware's dispatch is a longest-first list schedule); when there are
+//    many more key tiles than SMs can balance in whole items (long cached
+//    prefixes), one persistent CTA per SM takes an equal share of key tiles,
+//    cutting items, and the CTA that completes an item merges its partial
+//    results (fp16 O / l, fp32 max and sum; log-sum-exp).
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <math_constants.h>
 
 #include "pkv_device.cuh"
@@ -60,8 +69,22 @@ constexpr int kOffQ = 0;                                   // Q_0, Q_1
 constexpr int kOffV = kOffQ + 2 * kPfTileBytes;            // V stages
 constexpr int kOffK = kOffV + kPfStages * kPfTileBytes;    // K stages
 constexpr int kOffBars = kOffK + kPfStages * kPfTileBytes;
-constexpr int kNumBars = 13;
-constexpr int kPfSmemBytes = kOffBars + kNumBars * 8 + 16 + 1024;  // + tmem address, fail flag, alignment slack
+constexpr int kNumBars = 14;
+constexpr int kPfMaxSeqs = 1024;  // request prefix sums live in shared memory
+// + tmem address, fail flag, two merge flags; alignment slack (the request prefix sums follow)
+constexpr int kPfSmemBytes = kOffBars + kNumBars * 8 + 16 + 1024;
+// + the request prefix sums and the CTA's share (lo, hi, U, G) as 64-bit words
+// + the request prefix sums of cost units and of items, the schedule, the CTA's share (lo, hi, U, G) and each
+// softmax group's pending split pieces, as 64-bit words
+static size_t pf_smem_bytes(int num_seqs) {
+  return kPfSmemBytes + static_cast<size_t>(2 * (num_seqs + 1) + 1 + 4 + 4) * 8;
+}
+
+// Item mode (no item is split) when the largest item is at least this share
+// (in percent) of a CTA's average number of key tiles; split mode otherwise.
+#ifndef PKV_PF_ITEM_MODE_PCT
+#define PKV_PF_ITEM_MODE_PCT 75
+#endif
 
 // TMEM columns
 constexpr uint32_t kColS = 0;    // S_h at kColS + 128 h
@@ -71,20 +94,34 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, false);  // B = K tile, K-major
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, true);   // B = V tile, MN-major
 
+// Partial record of a split piece, per query head: the piece's normalised
+// output O / l as fp16, 4 dims per 8-byte word laid out [dim / 4][row] (a warp's
+// 32 rows are one coalesced 256-byte line per word), then the rows' running max
+// (log2 units) and sum as fp32.
+constexpr int kPfRecO = kHeadDim / 4 * kPfRows * 8;
+constexpr int kPfRecHeadBytes = kPfRecO + 2 * kPfRows * 4;
+constexpr int kPfRecBytes = 2 * kPfRecHeadBytes;
+
 struct PrefillArgs {
   const int* block_table;
   const int* prefix_lens;
   const int* cu_q_lens;
   __nv_bfloat16* out;
+  int num_seqs;
   int total_q;
   int max_pages;
   int num_pages;
+  int tmax;     // query tiles computed per request: ceil(max_q_len / 128)
+  int workers;  // split mode: persistent CTAs (one per SM); the grid has max(workers, items) CTAs
   float scale_log2;
   int* status;
+  int* counters;   // [num_seqs][8][tmax][2], zero between calls
+  unsigned char* records;  // [2 * workers][kPfRecBytes]
 };
 
 struct PfBars {
   uint64_t q_full;
+  uint64_t q_empty;
   uint64_t k_full[kPfStages];
   uint64_t v_full[kPfStages];
   uint64_t kv_empty[kPfStages];
@@ -141,6 +178,90 @@ __device__ __forceinline__ bool pf_wait_warp(uint64_t* bar, uint32_t parity, vol
   return __all_sync(0xffffffffu, pf_wait(bar, parity, fail, status));
 }
 
+// Work is a list of items (request n, KV head g, query tile t), ordered by n,
+// then g, then t. Query tile t of a request with P cached tokens and qlen chunk
+// rows needs n_t = ceil((P + min(128 (t + 1), qlen)) / 128) key tiles. Shares
+// are cut in cost units: an item costs kPfItemCost units for its fixed work (the
+// query tile load, the pipeline fill and drain, the epilogue) followed by one
+// unit per key tile, so a CTA whose share holds many small items gets fewer key
+// tiles. A (request, head) costs W = sum over its items; pref[n] = 8 * sum of W
+// before n. A piece is the part of one item inside a CTA's share that holds key
+// tiles: [k0, k1).
+#ifndef PKV_PF_ITEM_COST
+#define PKV_PF_ITEM_COST 2
+#endif
+constexpr int kPfItemCost = PKV_PF_ITEM_COST;
+struct PfPiece {
+  int n, g, t, k0, k1, nt, q0, qlen, P;
+  long long fseg, fend;  // the item's cost units start at fseg; the piece ends at fend
+};
+
+__device__ __forceinline__ int pf_tiles(int P, int qlen, int t) {
+  const int rows = qlen < kPfRows * (t + 1) ? qlen : kPfRows * (t + 1);
+  return (P + rows + kPfKeys - 1) / kPfKeys;
+}
+// Query tiles computed for a request (at most tmax) and the units before tile t
+// (tiles before the last are full: n_s = ceil(P / 128) + s + 1).
+__device__ __forceinline__ int pf_qtiles(int qlen, int tmax) {
+  const int T = (qlen + kPfRows - 1) / kPfRows;
+  return T < tmax ? T : tmax;
+}
+__device__ __forceinline__ long long pf_units_before(int P, int t) {
+  const long long c = (P + kPfKeys - 1) / kPfKeys;
+  return static_cast<long long>(t) * (c + kPfItemCost) + static_cast<long long>(t) * (t + 1) / 2;
+}
+
+// Split mode: a request's items are ordered by KV head, then query tile; the
+// first `workers` CTAs (one per SM) each take an equal contiguous share of the
+// cost units, cutting through items, whose partial results are merged
+// afterwards. (Item mode, CTA b computing item b of each request's items taken
+// heaviest first, needs no pieces.)
+__device__ __forceinline__ bool pf_find_piece(long long f, long long hi, const long long* pref, const PrefillArgs& a,
+                                              PfPiece& pc) {
+  for (; f < hi; f = pc.fend) {
+    int lo_n = 0, hi_n = a.num_seqs - 1;
+    while (lo_n < hi_n) {
+      const int mid = (lo_n + hi_n + 1) >> 1;
+      if (pref[mid] <= f) lo_n = mid; else hi_n = mid - 1;
+    }
+    pc.n = lo_n;
+    pc.q0 = __ldg(a.cu_q_lens + lo_n);
+    pc.qlen = __ldg(a.cu_q_lens + lo_n + 1) - pc.q0;
+    pc.P = __ldg(a.prefix_lens + lo_n);
+    const long long W = (pref[lo_n + 1] - pref[lo_n]) / kKVHeads;
+    const long long off = f - pref[lo_n];
+    pc.g = static_cast<int>(off / W);
+    const long long o2 = off - pc.g * W;
+    int lo_t = 0, hi_t = pf_qtiles(pc.qlen, a.tmax) - 1;
+    while (lo_t < hi_t) {
+      const int mid = (lo_t + hi_t + 1) >> 1;
+      if (pf_units_before(pc.P, mid) <= o2) lo_t = mid; else hi_t = mid - 1;
+    }
+    pc.t = lo_t;
+    pc.nt = pf_tiles(pc.P, pc.qlen, pc.t);
+    const long long ub = pf_units_before(pc.P, pc.t);
+    const long long p0 = o2 - ub;  // position inside the item: fixed-cost units, then key tiles
+    const long long p_end = p0 + (hi - f);
+    const long long p1 = p_end < kPfItemCost + pc.nt ? p_end : kPfItemCost + pc.nt;
+    pc.k0 = static_cast<int>(p0 > kPfItemCost ? p0 - kPfItemCost : 0);
+    pc.k1 = static_cast<int>(p1 - kPfItemCost);
+    pc.fseg = pref[lo_n] + pc.g * W + ub;
+    pc.fend = f + (p1 - p0);
+    if (pc.k1 > pc.k0) return true;
+  }
+  return false;
+}
+
+// CTA whose share [c U / G, (c + 1) U / G) holds unit f.
+__device__ __forceinline__ int pf_cta_of(long long f, long long U, int G) {
+  return static_cast<int>(((f + 1) * G + U - 1) / U - 1);
+}
+__device__ __forceinline__ long long pf_share_lo(int c, long long U, int G) { return static_cast<long long>(c) * U / G; }
+
+__device__ __forceinline__ void pf_group_sync(int h) {  // the 128 softmax threads of query head h
+  asm volatile("bar.sync %0, 128;" ::"r"(2 + h) : "memory");
+}
+
 __global__ void __launch_bounds__(kPfThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
@@ -150,38 +271,19 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   PfBars* bars = reinterpret_cast<PfBars*>(smem + kOffBars);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBars + kNumBars * 8);
   volatile int* fail = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* merge_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);  // [2]
+  long long* pref = reinterpret_cast<long long*>(tmem_slot + 4);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  // CTAs are dispatched in blockIdx.x order: walk (query tile, KV head) pairs
-  // tile-major from the last tile, so every head's longest causal tiles start first.
-  const int n_qtiles = gridDim.x / kKVHeads;
-  const int tile = n_qtiles - 1 - static_cast<int>(blockIdx.x) / kKVHeads;
-  const int g = static_cast<int>(blockIdx.x) % kKVHeads;  // KV head
-  const int n = blockIdx.y;                                 // request
 
   grid_dependency_wait();
   allow_dependents();
 
-  const int q0 = __ldg(a.cu_q_lens + n);
-  const int q1 = __ldg(a.cu_q_lens + n + 1);
-  const int P = __ldg(a.prefix_lens + n);
-  const int qlen = q1 - q0;
-  const int i0 = tile * kPfRows;
-  if (i0 >= qlen) return;
-  const int rows_here = qlen - i0 < kPfRows ? qlen - i0 : kPfRows;
-  const long long kv_end_ll = static_cast<long long>(P) + i0 + rows_here;  // keys 0 .. kv_end-1 are needed
-  if (P < 0 || q0 < 0 || q1 > a.total_q || kv_end_ll > static_cast<long long>(a.max_pages) * kPageSize) {
-    if (tid == 0) set_status(a.status, PKV_ERR_OUT_OF_BOUNDS);
-    return;
-  }
-  const int kv_end = static_cast<int>(kv_end_ll);
-  const int n_tiles = (kv_end + kPfKeys - 1) / kPfKeys;
-  const int n_pages = (kv_end + kPageSize - 1) / kPageSize;
-
   if (tid == 0) {
     mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_empty, 1);
     for (int s = 0; s < kPfStages; ++s) {
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->v_full[s], 1);
@@ -194,6 +296,59 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
     *fail = 0;
     fence_barrier_init();
+  }
+  if (warp == 1) {
+    // units per request (8 W_n; 0 for a request whose shape is out of bounds) and their exclusive prefix
+    long long carry = 0, icarry = 0, tiles_all = 0;
+    int nt_max = 0;
+    long long* ipref = pref + a.num_seqs + 2;
+    const long long cap = static_cast<long long>(a.max_pages) * kPageSize;
+    for (int base = 0; base < a.num_seqs; base += 32) {
+      const int n = base + lane;
+      long long w8 = 0, items = 0;
+      if (n < a.num_seqs) {
+        const int q0 = __ldg(a.cu_q_lens + n), q1 = __ldg(a.cu_q_lens + n + 1);
+        const int P = __ldg(a.prefix_lens + n);
+        const int qlen = q1 - q0;
+        const int T = qlen > 0 ? pf_qtiles(qlen, a.tmax) : 0;
+        const long long rows = qlen < kPfRows * T ? qlen : static_cast<long long>(kPfRows) * T;
+        if (P < 0 || q0 < 0 || qlen < 0 || q1 > a.total_q || static_cast<long long>(P) + rows > cap) {
+          set_status(a.status, PKV_ERR_OUT_OF_BOUNDS);
+        } else if (T > 0) {
+          const int nt_last = pf_tiles(P, qlen, T - 1);
+          w8 = kKVHeads * (pf_units_before(P, T - 1) + kPfItemCost + nt_last);
+          tiles_all += w8 - static_cast<long long>(kKVHeads) * kPfItemCost * T;
+          items = static_cast<long long>(kKVHeads) * T;
+          nt_max = nt_max > nt_last ? nt_max : nt_last;
+        }
+      }
+      long long x = w8, xi = items;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, x, o);
+        const long long yi = __shfl_up_sync(0xffffffffu, xi, o);
+        if (lane >= o) {
+          x += y;
+          xi += yi;
+        }
+      }
+      if (n < a.num_seqs) {
+        pref[n] = carry + x - w8;
+        ipref[n] = icarry + xi - items;
+      }
+      carry += __shfl_sync(0xffffffffu, x, 31);
+      icarry += __shfl_sync(0xffffffffu, xi, 31);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      tiles_all += __shfl_xor_sync(0xffffffffu, tiles_all, o);
+      nt_max = max(nt_max, __shfl_xor_sync(0xffffffffu, nt_max, o));
+    }
+    if (lane == 0) {
+      pref[a.num_seqs] = carry;
+      ipref[a.num_seqs] = icarry;
+      pref[a.num_seqs + 1] = 100LL * nt_max * a.workers >= static_cast<long long>(PKV_PF_ITEM_MODE_PCT) * tiles_all;
+    }
   }
   if (warp == kPfMmaWarp) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -208,61 +363,344 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   unsigned char* sV = smem + kOffV;
   unsigned char* sK = smem + kOffK;
 
+  // Only min(gridDim.x, U) CTAs take a share, so every share is non-empty.
+  const long long U = pref[a.num_seqs];
+  const bool item_mode = pref[a.num_seqs + 1] != 0;
+  const int G = static_cast<int>(U < a.workers ? U : a.workers);
+  const bool active = static_cast<int>(blockIdx.x) < G;
+  const long long lo = active ? pf_share_lo(blockIdx.x, U, G) : 0;
+  const long long hi = active ? pf_share_lo(blockIdx.x + 1, U, G) : 0;
+  // the softmax warps re-read these from shared memory instead of keeping them live
+  volatile long long* share = pref + 2 * a.num_seqs + 3;  // lo, hi, U, G (pref[num_seqs + 1]: item mode)
+  volatile long long* pend_f = share + 4;             // [head][2]: start units of split pieces not yet counted
 
-  if (warp == kPfTmaWarp) {
-    // ------------------------------------------------------------------ TMA producer
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kPfRegsOther));
-    if (lane == 0) {
-      mbar_arrive_expect_tx(&bars->q_full, 2 * kPfTileBytes);
-      for (int h = 0; h < 2; ++h)
-        for (int half = 0; half < 2; ++half)
-          tma_load_3d(sQ + h * kPfTileBytes + half * kPfHalfBytes, &qmap, half * 64, 2 * g + h, q0 + i0,
-                      &bars->q_full);
-    }
-    for (int j = 0; j < n_tiles; ++j) {
-      const int st = j & 1;
-      const int use = j >> 1;
-      if (use > 0 && !pf_wait_warp(&bars->kv_empty[st], static_cast<uint32_t>(use - 1) & 1u, fail, a.status)) break;
-      const int pg = j * kPfPagesPerTile + lane;
-      bool valid = lane < kPfPagesPerTile && pg < n_pages;
-      int id = 0;
-      if (valid) {
-        id = __ldg(a.block_table + static_cast<size_t>(n) * a.max_pages + pg);
-        if (id < 0 || id >= a.num_pages) {
-          set_status(a.status, PKV_ERR_OUT_OF_BOUNDS);
-          valid = false;
+  if (item_mode) {
+    // ================================================================ item mode: CTA b computes item b
+    const long long* ipref = pref + a.num_seqs + 2;
+    const long long b = blockIdx.x;
+    if (b < ipref[a.num_seqs]) {
+      int n = 0, hi_n = a.num_seqs - 1;
+      while (n < hi_n) {
+        const int mid = (n + hi_n + 1) >> 1;
+        if (ipref[mid] <= b) n = mid; else hi_n = mid - 1;
+      }
+      const int q0 = __ldg(a.cu_q_lens + n);
+      const int qlen = __ldg(a.cu_q_lens + n + 1) - q0;
+      const int P = __ldg(a.prefix_lens + n);
+      const int jj = static_cast<int>(b - ipref[n]);
+      const int tile = pf_qtiles(qlen, a.tmax) - 1 - jj / kKVHeads;  // heaviest first
+      const int g = jj % kKVHeads;
+      const int i0 = tile * kPfRows;
+      const int rows_here = qlen - i0 < kPfRows ? qlen - i0 : kPfRows;
+      const int kv_end = P + i0 + rows_here;  // in bounds: the length scan dropped out-of-bounds requests
+      const int n_tiles = (kv_end + kPfKeys - 1) / kPfKeys;
+      const int n_pages = (kv_end + kPageSize - 1) / kPageSize;
+    if (warp == kPfTmaWarp) {
+      // ------------------------------------------------------------------ TMA producer
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kPfRegsOther));
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars->q_full, 2 * kPfTileBytes);
+        for (int h = 0; h < 2; ++h)
+          for (int half = 0; half < 2; ++half)
+            tma_load_3d(sQ + h * kPfTileBytes + half * kPfHalfBytes, &qmap, half * 64, 2 * g + h, q0 + i0,
+                        &bars->q_full);
+      }
+      for (int j = 0; j < n_tiles; ++j) {
+        const int st = j & 1;
+        const int use = j >> 1;
+        if (use > 0 && !pf_wait_warp(&bars->kv_empty[st], static_cast<uint32_t>(use - 1) & 1u, fail, a.status)) break;
+        const int pg = j * kPfPagesPerTile + lane;
+        bool valid = lane < kPfPagesPerTile && pg < n_pages;
+        int id = 0;
+        if (valid) {
+          id = __ldg(a.block_table + static_cast<size_t>(n) * a.max_pages + pg);
+          if (id < 0 || id >= a.num_pages) {
+            set_status(a.status, PKV_ERR_OUT_OF_BOUNDS);
+            valid = false;
+          }
+        }
+        const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+        const uint32_t bytes = static_cast<uint32_t>(__popc(vmask)) * 2u * (kPageSize * 128u);
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bars->k_full[st], bytes);
+          mbar_arrive_expect_tx(&bars->v_full[st], bytes);
+        }
+        __syncwarp();
+        if (valid) {
+          const int row = (id * kKVHeads + g) * kPageSize;
+          unsigned char* kd = sK + st * kPfTileBytes + lane * (kPageSize * 128);
+          unsigned char* vd = sV + st * kPfTileBytes + lane * (kPageSize * 128);
+          tma_load_2d(kd, &kmap, 0, row, &bars->k_full[st]);
+          tma_load_2d(kd + kPfHalfBytes, &kmap, 64, row, &bars->k_full[st]);
+          tma_load_2d(vd, &vmap, 0, row, &bars->v_full[st]);
+          tma_load_2d(vd + kPfHalfBytes, &vmap, 64, row, &bars->v_full[st]);
         }
       }
-      const unsigned vmask = __ballot_sync(0xffffffffu, valid);
-      const uint32_t bytes = static_cast<uint32_t>(__popc(vmask)) * 2u * (kPageSize * 128u);
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&bars->k_full[st], bytes);
-        mbar_arrive_expect_tx(&bars->v_full[st], bytes);
+    } else if (warp == kPfMmaWarp) {
+      // ------------------------------------------------------------------ MMA issuer
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kPfRegsOther));
+      // Issue order QK_0(0) QK_1(0) | PV_0(j) QK_0(j+1) PV_1(j) QK_1(j+1) | ...: the
+      // two heads' softmaxes run half a period apart, so while one head's softmax
+      // works the other head's PV and next QK keep the tensor pipe busy. QK_h(j+1)
+      // overwrites S_h, which holds P_h(j), so it waits for PV_h(j) (o_done) --
+      // which also keeps O_h out of the softmax's way while it may rescale it.
+      auto issue_qk = [&](int j, int h) {
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t qa = smem_u32(sQ + h * kPfTileBytes);
+          const uint32_t kb = smem_u32(sK + (j & 1) * kPfTileBytes);
+  #pragma unroll
+          for (int s = 0; s < 8; ++s) {
+            const uint32_t off = (s >> 2) * kPfHalfBytes + (s & 3) * 32;
+            mma_ss(tmem + kColS + 128 * h, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
+                   kIdescQK, s > 0 ? 1u : 0u);
+          }
+          mma_commit(&bars->s_full[h]);
+        }
+        __syncwarp();
+      };
+      auto issue_pv = [&](int j, int h) {
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t vb = smem_u32(sV + (j & 1) * kPfTileBytes);
+  #pragma unroll
+          for (int s = 0; s < 8; ++s) {
+            mma_ts(tmem + kColO + 128 * h, tmem + kColS + 128 * h + 8 * s,
+                   sdesc_sw128(vb + s * 2048, kPfHalfBytes, 1024), kIdescPV, (j > 0 || s > 0) ? 1u : 0u);
+          }
+          mma_commit(&bars->o_done[h]);
+        }
+        __syncwarp();
+      };
+      bool ok = pf_wait_warp(&bars->q_full, 0, fail, a.status) && pf_wait_warp(&bars->k_full[0], 0, fail, a.status);
+      if (ok) {
+        issue_qk(0, 0);
+        issue_qk(0, 1);
       }
-      __syncwarp();
-      if (valid) {
-        const int row = (id * kKVHeads + g) * kPageSize;
-        unsigned char* kd = sK + st * kPfTileBytes + lane * (kPageSize * 128);
-        unsigned char* vd = sV + st * kPfTileBytes + lane * (kPageSize * 128);
-        tma_load_2d(kd, &kmap, 0, row, &bars->k_full[st]);
-        tma_load_2d(kd + kPfHalfBytes, &kmap, 64, row, &bars->k_full[st]);
-        tma_load_2d(vd, &vmap, 0, row, &bars->v_full[st]);
-        tma_load_2d(vd + kPfHalfBytes, &vmap, 64, row, &bars->v_full[st]);
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        const int st = j & 1;
+        const uint32_t ph = static_cast<uint32_t>(j >> 1) & 1u;
+        const bool next = j + 1 < n_tiles;
+        const uint32_t ph_next = static_cast<uint32_t>((j + 1) >> 1) & 1u;
+        if (!pf_wait_warp(&bars->v_full[st], ph, fail, a.status)) break;
+        if (j == n_tiles - 1 && kv_end < (j + 1) * kPfKeys) {
+          // keys past the end: zero their V rows (unused slots may hold NaN and 0 * NaN = NaN)
+          const int r0 = kv_end - j * kPfKeys;
+          uint4* vbase = reinterpret_cast<uint4*>(sV + st * kPfTileBytes);
+          for (int idx = r0 * 8 + lane; idx < kPfKeys * 8; idx += 32) {
+            vbase[idx] = make_uint4(0, 0, 0, 0);
+            vbase[kPfHalfBytes / 16 + idx] = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+        const uint32_t pj = static_cast<uint32_t>(j) & 1u;
+        if (!pf_wait_warp(&bars->p_full[0], pj, fail, a.status)) break;
+        issue_pv(j, 0);
+        if (next) {
+          if (!pf_wait_warp(&bars->k_full[st ^ 1], ph_next, fail, a.status) ||
+              !pf_wait_warp(&bars->o_done[0], pj, fail, a.status))
+            break;
+          issue_qk(j + 1, 0);
+        }
+        if (!pf_wait_warp(&bars->p_full[1], pj, fail, a.status)) break;
+        issue_pv(j, 1);
+        if (lane == 0) mma_commit(&bars->kv_empty[st]);
+        __syncwarp();
+        if (next) {
+          if (!pf_wait_warp(&bars->o_done[1], pj, fail, a.status)) break;
+          issue_qk(j + 1, 1);
+        }
+      }
+    } else if (warp < 8) {
+      // ------------------------------------------------------------------ softmax warpgroups
+      asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kPfRegsSoftmax));
+      const int h = warp >> 2;
+      const int quarter = warp & 3;
+      const int r = quarter * 32 + lane;  // row of the tile = TMEM lane
+      const int lim_row = P + i0 + r;     // last visible key of this row (causal)
+      const int lim = lim_row < kv_end - 1 ? lim_row : kv_end - 1;
+      const uint32_t t_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+      float m_used = -CUDART_INF_F;
+      float l = 0.f;
+      bool ok = true;
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        if (!pf_wait_warp(&bars->s_full[h], static_cast<uint32_t>(j) & 1u, fail, a.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t sr[4][32];
+  #pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(t_row + kColS + 128 * h + 32 * c, sr[c]);
+        tmem_ld_wait();
+        const bool diag = j * kPfKeys + kPfKeys - 1 > P + i0;
+        // row max over the raw scores (the scale is positive, so it keeps the order)
+        float mx = -CUDART_INF_F;
+        if (diag) {
+  #pragma unroll
+          for (int c = 0; c < 4; ++c)
+  #pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              if (j * kPfKeys + 32 * c + e > lim) sr[c][e] = __float_as_uint(-CUDART_INF_F);
+              mx = fmaxf(mx, __uint_as_float(sr[c][e]));
+            }
+        } else {
+  #pragma unroll
+          for (int c = 0; c < 4; ++c)
+  #pragma unroll
+            for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(sr[c][e]));
+        }
+        const float m_new = fmaxf(m_used, mx);
+        const bool first = m_used == -CUDART_INF_F;
+        const bool grow = first || (m_new - m_used) * a.scale_log2 > 8.f;
+        if (__any_sync(0xffffffffu, grow)) {
+          const float alpha = first ? 0.f : (grow ? ex2((m_used - m_new) * a.scale_log2) : 1.f);
+          if (j > 0) {
+  #pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              uint32_t orr[32];
+              tmem_ld32(t_row + kColO + 128 * h + 32 * c, orr);
+              tmem_ld_wait();
+  #pragma unroll
+              for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+              tmem_st32(t_row + kColO + 128 * h + 32 * c, orr);
+            }
+            tmem_st_wait();
+          }
+          if (grow) {
+            l *= alpha;
+            m_used = m_new;
+          }
+        }
+        // P = 2^(s * scale * log2 e - m * scale * log2 e) as bf16 pairs over S's first 64 columns
+        const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
+        const float2 nm2 = make_float2(-m_used * a.scale_log2, -m_used * a.scale_log2);
+        float2 l2 = make_float2(0.f, 0.f);
+  #pragma unroll
+        for (int hc = 0; hc < 2; ++hc) {
+          uint32_t pk[32];
+  #pragma unroll
+          for (int c2 = 0; c2 < 2; ++c2)
+  #pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              const float2 t = __ffma2_rn(make_float2(__uint_as_float(sr[2 * hc + c2][e]),
+                                                      __uint_as_float(sr[2 * hc + c2][e + 1])),
+                                          sc2, nm2);
+              float2 pp;
+              if (((e >> 1) & 3) < kPfPolyPairsOf4) {
+                pp = exp2_poly2(t);
+              } else {
+                pp = make_float2(ex2(t.x), ex2(t.y));
+              }
+              l2 = __fadd2_rn(l2, pp);
+              pk[c2 * 16 + (e >> 1)] = pack_bf16x2(pp.x, pp.y);
+            }
+          tmem_st32(t_row + kColS + 128 * h + 32 * hc, pk);
+        }
+        l += l2.x + l2.y;
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive_cta(&bars->p_full[h]);
+      }
+      if (ok && pf_wait_warp(&bars->o_done[h], static_cast<uint32_t>(n_tiles - 1) & 1u, fail, a.status)) {
+        tc_fence_after();
+        const float inv = 1.f / l;
+        const bool write = r < rows_here;
+        __nv_bfloat16* orow = a.out + (static_cast<size_t>(q0 + i0 + r) * kQHeads + 2 * g + h) * kHeadDim;
+  #pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t orr[32];
+          tmem_ld32(t_row + kColO + 128 * h + 32 * c, orr);
+          tmem_ld_wait();
+          if (write) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+  #pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint4 v;
+              v.x = pack_bf16x2(__uint_as_float(orr[8 * q + 0]) * inv, __uint_as_float(orr[8 * q + 1]) * inv);
+              v.y = pack_bf16x2(__uint_as_float(orr[8 * q + 2]) * inv, __uint_as_float(orr[8 * q + 3]) * inv);
+              v.z = pack_bf16x2(__uint_as_float(orr[8 * q + 4]) * inv, __uint_as_float(orr[8 * q + 5]) * inv);
+              v.w = pack_bf16x2(__uint_as_float(orr[8 * q + 6]) * inv, __uint_as_float(orr[8 * q + 7]) * inv);
+              dst[q] = v;
+            }
+          }
+        }
+      }
+    } else {
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kPfRegsOther));  // idle warps 10-11
+    }
+
+    }
+  } else if (!active) {
+  } else if (warp == kPfTmaWarp) {
+    // ------------------------------------------------------------------ TMA producer
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kPfRegsOther));
+    int gj = 0;  // key tiles of this CTA so far
+    int pi = 0;
+    PfPiece pc;
+    bool run = true;
+    for (long long f = lo; run && pf_find_piece(f, hi, pref, a, pc); f = pc.fend, ++pi) {
+      // this piece's query tiles, once the previous piece's QK MMAs are done with the buffer
+      if (pi > 0 && !pf_wait_warp(&bars->q_empty, static_cast<uint32_t>(pi - 1) & 1u, fail, a.status)) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars->q_full, 2 * kPfTileBytes);
+        for (int h = 0; h < 2; ++h)
+          for (int half = 0; half < 2; ++half)
+            tma_load_3d(sQ + h * kPfTileBytes + half * kPfHalfBytes, &qmap, half * 64, 2 * pc.g + h,
+                        pc.q0 + pc.t * kPfRows, &bars->q_full);
+      }
+      const int rows = pc.qlen < kPfRows * (pc.t + 1) ? pc.qlen : kPfRows * (pc.t + 1);
+      const int n_pages = (pc.P + rows + kPageSize - 1) / kPageSize;
+      for (int k = pc.k0; k < pc.k1; ++k, ++gj) {
+        const int st = gj & 1;
+        const int use = gj >> 1;
+        if (use > 0 && !pf_wait_warp(&bars->kv_empty[st], static_cast<uint32_t>(use - 1) & 1u, fail, a.status)) {
+          run = false;
+          break;
+        }
+        const int pg = k * kPfPagesPerTile + lane;
+        bool valid = lane < kPfPagesPerTile && pg < n_pages;
+        int id = 0;
+        if (valid) {
+          id = __ldg(a.block_table + static_cast<size_t>(pc.n) * a.max_pages + pg);
+          if (id < 0 || id >= a.num_pages) {
+            set_status(a.status, PKV_ERR_OUT_OF_BOUNDS);
+            valid = false;
+          }
+        }
+        const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+        const uint32_t bytes = static_cast<uint32_t>(__popc(vmask)) * 2u * (kPageSize * 128u);
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bars->k_full[st], bytes);
+          mbar_arrive_expect_tx(&bars->v_full[st], bytes);
+        }
+        __syncwarp();
+        if (valid) {
+          const int row = (id * kKVHeads + pc.g) * kPageSize;
+          unsigned char* kd = sK + st * kPfTileBytes + lane * (kPageSize * 128);
+          unsigned char* vd = sV + st * kPfTileBytes + lane * (kPageSize * 128);
+          tma_load_2d(kd, &kmap, 0, row, &bars->k_full[st]);
+          tma_load_2d(kd + kPfHalfBytes, &kmap, 64, row, &bars->k_full[st]);
+          tma_load_2d(vd, &vmap, 0, row, &bars->v_full[st]);
+          tma_load_2d(vd + kPfHalfBytes, &vmap, 64, row, &bars->v_full[st]);
+        }
       }
     }
   } else if (warp == kPfMmaWarp) {
     // ------------------------------------------------------------------ MMA issuer
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kPfRegsOther));
-    // Issue order QK_0(0) QK_1(0) | PV_0(j) QK_0(j+1) PV_1(j) QK_1(j+1) | ...: the
-    // two heads' softmaxes run half a period apart, so while one head's softmax
-    // works the other head's PV and next QK keep the tensor pipe busy. QK_h(j+1)
-    // overwrites S_h, which holds P_h(j), so it waits for PV_h(j) (o_done) --
-    // which also keeps O_h out of the softmax's way while it may rescale it.
-    auto issue_qk = [&](int j, int h) {
+    // Issue order QK_0(0) QK_1(0) | PV_0(j) QK_0(j+1) PV_1(j) QK_1(j+1) | ... over
+    // the CTA's key tiles (across pieces): the two heads' softmaxes run half a
+    // period apart, so while one head's softmax works the other head's PV and
+    // next QK keep the tensor pipe busy. QK_h(j+1) overwrites S_h, which holds
+    // P_h(j), so it waits for PV_h(j) (o_done) -- which also keeps O_h out of
+    // the softmax's way while it rescales it or reads it at the end of a piece.
+    auto issue_qk = [&](int st, int h) {
       tc_fence_after();
       if (lane == 0) {
         const uint32_t qa = smem_u32(sQ + h * kPfTileBytes);
-        const uint32_t kb = smem_u32(sK + (j & 1) * kPfTileBytes);
+        const uint32_t kb = smem_u32(sK + st * kPfTileBytes);
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
           const uint32_t off = (s >> 2) * kPfHalfBytes + (s & 3) * 32;
@@ -273,33 +711,47 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
       __syncwarp();
     };
-    auto issue_pv = [&](int j, int h) {
+    auto issue_pv = [&](int st, int h, bool acc) {
       tc_fence_after();
       if (lane == 0) {
-        const uint32_t vb = smem_u32(sV + (j & 1) * kPfTileBytes);
+        const uint32_t vb = smem_u32(sV + st * kPfTileBytes);
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
           mma_ts(tmem + kColO + 128 * h, tmem + kColS + 128 * h + 8 * s,
-                 sdesc_sw128(vb + s * 2048, kPfHalfBytes, 1024), kIdescPV, (j > 0 || s > 0) ? 1u : 0u);
+                 sdesc_sw128(vb + s * 2048, kPfHalfBytes, 1024), kIdescPV, (acc || s > 0) ? 1u : 0u);
         }
         mma_commit(&bars->o_done[h]);
       }
       __syncwarp();
     };
-    bool ok = pf_wait_warp(&bars->q_full, 0, fail, a.status) && pf_wait_warp(&bars->k_full[0], 0, fail, a.status);
+    auto commit_q_empty = [&]() {
+      if (lane == 0) mma_commit(&bars->q_empty);
+      __syncwarp();
+    };
+    PfPiece cur, nxt;
+    bool ok = pf_find_piece(lo, hi, pref, a, cur);
+    bool have_nxt = ok && pf_find_piece(cur.fend, hi, pref, a, nxt);
+    ok = ok && pf_wait_warp(&bars->q_full, 0, fail, a.status) && pf_wait_warp(&bars->k_full[0], 0, fail, a.status);
     if (ok) {
       issue_qk(0, 0);
       issue_qk(0, 1);
+      if (cur.k1 - cur.k0 == 1) commit_q_empty();
     }
-    for (int j = 0; j < n_tiles && ok; ++j) {
-      const int st = j & 1;
-      const uint32_t ph = static_cast<uint32_t>(j >> 1) & 1u;
-      const bool next = j + 1 < n_tiles;
-      const uint32_t ph_next = static_cast<uint32_t>((j + 1) >> 1) & 1u;
+    int gj = 0, j = 0, pi = 0;
+    while (ok) {
+      const int st = gj & 1;
+      const uint32_t ph = static_cast<uint32_t>(gj >> 1) & 1u;
+      const uint32_t pj = static_cast<uint32_t>(gj) & 1u;
+      const int ntiles = cur.k1 - cur.k0;
+      const bool next_in = j + 1 < ntiles;
+      const bool next = next_in || have_nxt;
+      const int k = cur.k0 + j;
       if (!pf_wait_warp(&bars->v_full[st], ph, fail, a.status)) break;
-      if (j == n_tiles - 1 && kv_end < (j + 1) * kPfKeys) {
+      const int rows = cur.qlen < kPfRows * (cur.t + 1) ? cur.qlen : kPfRows * (cur.t + 1);
+      const int kv_end = cur.P + rows;
+      if (k == cur.nt - 1 && kv_end < (k + 1) * kPfKeys) {
         // keys past the end: zero their V rows (unused slots may hold NaN and 0 * NaN = NaN)
-        const int r0 = kv_end - j * kPfKeys;
+        const int r0 = kv_end - k * kPfKeys;
         uint4* vbase = reinterpret_cast<uint4*>(sV + st * kPfTileBytes);
         for (int idx = r0 * 8 + lane; idx < kPfKeys * 8; idx += 32) {
           vbase[idx] = make_uint4(0, 0, 0, 0);
@@ -308,22 +760,32 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
       }
-      const uint32_t pj = static_cast<uint32_t>(j) & 1u;
       if (!pf_wait_warp(&bars->p_full[0], pj, fail, a.status)) break;
-      issue_pv(j, 0);
+      issue_pv(st, 0, j > 0);
       if (next) {
-        if (!pf_wait_warp(&bars->k_full[st ^ 1], ph_next, fail, a.status) ||
+        if (!next_in && !pf_wait_warp(&bars->q_full, static_cast<uint32_t>(pi + 1) & 1u, fail, a.status)) break;
+        if (!pf_wait_warp(&bars->k_full[st ^ 1], static_cast<uint32_t>((gj + 1) >> 1) & 1u, fail, a.status) ||
             !pf_wait_warp(&bars->o_done[0], pj, fail, a.status))
           break;
-        issue_qk(j + 1, 0);
+        issue_qk(st ^ 1, 0);
       }
       if (!pf_wait_warp(&bars->p_full[1], pj, fail, a.status)) break;
-      issue_pv(j, 1);
+      issue_pv(st, 1, j > 0);
       if (lane == 0) mma_commit(&bars->kv_empty[st]);
       __syncwarp();
-      if (next) {
-        if (!pf_wait_warp(&bars->o_done[1], pj, fail, a.status)) break;
-        issue_qk(j + 1, 1);
+      if (!next) break;
+      if (!pf_wait_warp(&bars->o_done[1], pj, fail, a.status)) break;
+      issue_qk(st ^ 1, 1);
+      // that was the last QK of its piece: the query buffer may be refilled
+      if (next_in ? j + 2 == ntiles : nxt.k1 - nxt.k0 == 1) commit_q_empty();
+      ++gj;
+      if (next_in) {
+        ++j;
+      } else {
+        cur = nxt;
+        have_nxt = pf_find_piece(cur.fend, hi, pref, a, nxt);
+        j = 0;
+        ++pi;
       }
     }
   } else if (warp < 8) {
@@ -332,75 +794,96 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int h = warp >> 2;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;  // row of the tile = TMEM lane
-    const int lim_row = P + i0 + r;     // last visible key of this row (causal)
-    const int lim = lim_row < kv_end - 1 ? lim_row : kv_end - 1;
     const uint32_t t_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    float m_used = -CUDART_INF_F;
-    float l = 0.f;
+    if (quarter == 0 && lane == 0) {
+      share[0] = lo;
+      share[1] = hi;
+      share[2] = U;
+      share[3] = G;
+      pend_f[2 * h] = -1;
+      pend_f[2 * h + 1] = -1;
+    }
+    pf_group_sync(h);  // both warpgroups write the same values
     bool ok = true;
-    for (int j = 0; j < n_tiles && ok; ++j) {
-      if (!pf_wait_warp(&bars->s_full[h], static_cast<uint32_t>(j) & 1u, fail, a.status)) {
-        ok = false;
-        break;
+    int gj = 0;
+    long long f = share[0];
+    while (true) {
+      // only the scalars the key-tile loop needs stay live across it (the piece is
+      // looked up again for the end-of-piece work)
+      int kb, ke, lim, diag_from;
+      {
+        PfPiece pc;
+        if (!pf_find_piece(f, share[1], pref, a, pc)) break;
+        const int i0 = pc.t * kPfRows;
+        const int rows = pc.qlen < i0 + kPfRows ? pc.qlen : i0 + kPfRows;
+        const int lim_row = pc.P + i0 + r;  // last visible key of this row (causal)
+        lim = lim_row < pc.P + rows - 1 ? lim_row : pc.P + rows - 1;
+        diag_from = pc.P + i0;
+        kb = pc.k0;
+        ke = pc.k1;
       }
-      tc_fence_after();
-      uint32_t sr[4][32];
+      float m_used = -CUDART_INF_F;
+      float l = 0.f;
+      for (int k = kb; k < ke; ++k, ++gj) {
+        if (ok && !pf_wait_warp(&bars->s_full[h], static_cast<uint32_t>(gj) & 1u, fail, a.status)) ok = false;
+        if (!ok) continue;
+        tc_fence_after();
+        uint32_t sr[4][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(t_row + kColS + 128 * h + 32 * c, sr[c]);
-      tmem_ld_wait();
-      const bool diag = j * kPfKeys + kPfKeys - 1 > P + i0;
-      // row max over the raw scores (the scale is positive, so it keeps the order)
-      float mx = -CUDART_INF_F;
-      if (diag) {
+        for (int c = 0; c < 4; ++c) tmem_ld32(t_row + kColS + 128 * h + 32 * c, sr[c]);
+        tmem_ld_wait();
+        const bool diag = k * kPfKeys + kPfKeys - 1 > diag_from;
+        // row max over the raw scores (the scale is positive, so it keeps the order)
+        float mx = -CUDART_INF_F;
+        if (diag) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+          for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            if (j * kPfKeys + 32 * c + e > lim) sr[c][e] = __float_as_uint(-CUDART_INF_F);
-            mx = fmaxf(mx, __uint_as_float(sr[c][e]));
-          }
-      } else {
+            for (int e = 0; e < 32; ++e) {
+              if (k * kPfKeys + 32 * c + e > lim) sr[c][e] = __float_as_uint(-CUDART_INF_F);
+              mx = fmaxf(mx, __uint_as_float(sr[c][e]));
+            }
+        } else {
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+          for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(sr[c][e]));
-      }
-      const float m_new = fmaxf(m_used, mx);
-      const bool first = m_used == -CUDART_INF_F;
-      const bool grow = first || (m_new - m_used) * a.scale_log2 > 8.f;
-      if (__any_sync(0xffffffffu, grow)) {
-        const float alpha = first ? 0.f : (grow ? ex2((m_used - m_new) * a.scale_log2) : 1.f);
-        if (j > 0) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t orr[32];
-            tmem_ld32(t_row + kColO + 128 * h + 32 * c, orr);
-            tmem_ld_wait();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
-            tmem_st32(t_row + kColO + 128 * h + 32 * c, orr);
-          }
-          tmem_st_wait();
+            for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(sr[c][e]));
         }
-        if (grow) {
-          l *= alpha;
-          m_used = m_new;
+        const float m_new = fmaxf(m_used, mx);
+        const bool first = m_used == -CUDART_INF_F;
+        const bool grow = first || (m_new - m_used) * a.scale_log2 > 8.f;
+        if (__any_sync(0xffffffffu, grow)) {
+          const float alpha = first ? 0.f : (grow ? ex2((m_used - m_new) * a.scale_log2) : 1.f);
+          if (k > kb) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              uint32_t orr[32];
+              tmem_ld32(t_row + kColO + 128 * h + 32 * c, orr);
+              tmem_ld_wait();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+              tmem_st32(t_row + kColO + 128 * h + 32 * c, orr);
+            }
+            tmem_st_wait();
+          }
+          if (grow) {
+            l *= alpha;
+            m_used = m_new;
+          }
         }
-      }
-      // P = 2^(s * scale * log2 e - m * scale * log2 e) as bf16 pairs over S's first 64 columns
-      const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
-      const float2 nm2 = make_float2(-m_used * a.scale_log2, -m_used * a.scale_log2);
-      float2 l2 = make_float2(0.f, 0.f);
+        // P = 2^(s * scale * log2 e - m * scale * log2 e) as bf16 pairs over S's first 64 columns;
+        // a row with no visible key yet (a piece that starts past key 0) gets P = 0
+        const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
+        const float mo = m_used == -CUDART_INF_F ? 0.f : -m_used * a.scale_log2;
+        const float2 nm2 = make_float2(mo, mo);
+        float2 l2 = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int hc = 0; hc < 2; ++hc) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2)
+        for (int c = 0; c < 4; ++c) {  // scores 32c .. 32c+31 -> P columns 16c .. 16c+15
+          uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
-            const float2 t = __ffma2_rn(make_float2(__uint_as_float(sr[2 * hc + c2][e]),
-                                                    __uint_as_float(sr[2 * hc + c2][e + 1])),
-                                        sc2, nm2);
+            const float2 t =
+                __ffma2_rn(make_float2(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1])), sc2, nm2);
             float2 pp;
             if (((e >> 1) & 3) < kPfPolyPairsOf4) {
               pp = exp2_poly2(t);
@@ -408,37 +891,167 @@ __global__ void __launch_bounds__(kPfThreads, 1)
               pp = make_float2(ex2(t.x), ex2(t.y));
             }
             l2 = __fadd2_rn(l2, pp);
-            pk[c2 * 16 + (e >> 1)] = pack_bf16x2(pp.x, pp.y);
+            pk[e >> 1] = pack_bf16x2(pp.x, pp.y);
           }
-        tmem_st32(t_row + kColS + 128 * h + 32 * hc, pk);
+          tmem_st16(t_row + kColS + 128 * h + 16 * c, pk);
+        }
+        l += l2.x + l2.y;
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive_cta(&bars->p_full[h]);
       }
-      l += l2.x + l2.y;
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive_cta(&bars->p_full[h]);
-    }
-    if (ok && pf_wait_warp(&bars->o_done[h], static_cast<uint32_t>(n_tiles - 1) & 1u, fail, a.status)) {
-      tc_fence_after();
-      const float inv = 1.f / l;
+      // ---- end of the piece: O_h is complete once PV_h of its last key tile is done
+      if (ok && !pf_wait_warp(&bars->o_done[h], static_cast<uint32_t>(gj - 1) & 1u, fail, a.status)) ok = false;
+      if (ok) tc_fence_after();
+      asm volatile("" : "+l"(f));  // look the piece up again rather than keep it live
+      PfPiece pc;
+      pf_find_piece(f, share[1], pref, a, pc);
+      const int i0 = pc.t * kPfRows;
+      const int rows_here = (pc.qlen < i0 + kPfRows ? pc.qlen : i0 + kPfRows) - i0;
       const bool write = r < rows_here;
-      __nv_bfloat16* orow = a.out + (static_cast<size_t>(q0 + i0 + r) * kQHeads + 2 * g + h) * kHeadDim;
+      __nv_bfloat16* orow = a.out + (static_cast<size_t>(pc.q0 + i0 + r) * kQHeads + 2 * pc.g + h) * kHeadDim;
+      if (pc.k0 == 0 && pc.k1 == pc.nt) {
+        if (ok) {
+          const float inv = 1.f / l;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t orr[32];
-        tmem_ld32(t_row + kColO + 128 * h + 32 * c, orr);
-        tmem_ld_wait();
-        if (write) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+          for (int c = 0; c < 4; ++c) {
+            uint32_t orr[32];
+            tmem_ld32(t_row + kColO + 128 * h + 32 * c, orr);
+            tmem_ld_wait();
+            if (write) {
+              uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(orr[8 * q + 0]) * inv, __uint_as_float(orr[8 * q + 1]) * inv);
-            v.y = pack_bf16x2(__uint_as_float(orr[8 * q + 2]) * inv, __uint_as_float(orr[8 * q + 3]) * inv);
-            v.z = pack_bf16x2(__uint_as_float(orr[8 * q + 4]) * inv, __uint_as_float(orr[8 * q + 5]) * inv);
-            v.w = pack_bf16x2(__uint_as_float(orr[8 * q + 6]) * inv, __uint_as_float(orr[8 * q + 7]) * inv);
-            dst[q] = v;
+              for (int q = 0; q < 4; ++q) {
+                uint4 v;
+                v.x = pack_bf16x2(__uint_as_float(orr[8 * q + 0]) * inv, __uint_as_float(orr[8 * q + 1]) * inv);
+                v.y = pack_bf16x2(__uint_as_float(orr[8 * q + 2]) * inv, __uint_as_float(orr[8 * q + 3]) * inv);
+                v.z = pack_bf16x2(__uint_as_float(orr[8 * q + 4]) * inv, __uint_as_float(orr[8 * q + 5]) * inv);
+                v.w = pack_bf16x2(__uint_as_float(orr[8 * q + 6]) * inv, __uint_as_float(orr[8 * q + 7]) * inv);
+                dst[q] = v;
+              }
+            }
           }
         }
+      } else {
+        // Split piece (only a share's first and last piece can be): write this
+        // CTA's partial record of the row now, count it after the last piece.
+        unsigned char* rec = a.records + static_cast<size_t>(2 * blockIdx.x + (f == share[0] ? 0 : 1)) * kPfRecBytes +
+                             h * kPfRecHeadBytes;
+        uint2* ro = reinterpret_cast<uint2*>(rec);
+        float* rml = reinterpret_cast<float*>(rec + kPfRecO);
+        const float inv = l > 0.f ? 1.f / l : 0.f;  // a row with no visible key in the piece has l = 0
+        if (ok) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t orr[32];
+            tmem_ld32(t_row + kColO + 128 * h + 32 * c, orr);
+            tmem_ld_wait();
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              // O / l is a convex combination of V rows; fp16 holds it (clamped to the fp16 range)
+              auto h16 = [&](int e) { return fminf(fmaxf(__uint_as_float(orr[e]) * inv, -65504.f), 65504.f); };
+              const __half2 lo2 = __floats2half2_rn(h16(4 * q), h16(4 * q + 1));
+              const __half2 hi2 = __floats2half2_rn(h16(4 * q + 2), h16(4 * q + 3));
+              ro[(c * 8 + q) * kPfRows + r] =
+                  make_uint2(*reinterpret_cast<const uint32_t*>(&lo2), *reinterpret_cast<const uint32_t*>(&hi2));
+            }
+          }
+        }
+        rml[r] = m_used == -CUDART_INF_F ? -CUDART_INF_F : m_used * a.scale_log2;
+        rml[kPfRows + r] = l;
+        if (quarter == 0 && lane == 0) pend_f[2 * h + (f == share[0] ? 0 : 1)] = f;
+      }
+      f = pc.fend;
+    }
+    // ---- count the split pieces' records in (one fence, one round trip); the
+    // CTA that completes an item's count merges the records of all its holders
+    // (log-sum-exp) and resets the counter. The barriers run whatever ok is.
+    pf_group_sync(h);  // this head's records and pend_f are written
+    const long long pf0 = pend_f[2 * h], pf1 = pend_f[2 * h + 1];
+    if (pf0 >= 0 || pf1 >= 0) {
+      const long long Us = share[2];
+      const int Gs = static_cast<int>(share[3]);
+      if (quarter == 0 && lane == 0) {
+        int flags = 0;
+        __threadfence();
+        int old[2] = {-1, -1}, want[2] = {0, 0};
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const long long fi = i == 0 ? pf0 : pf1;
+          if (fi < 0) continue;
+          PfPiece pc;
+          pf_find_piece(fi, share[1], pref, a, pc);
+          want[i] = pf_cta_of(pc.fseg + kPfItemCost + pc.nt - 1, Us, Gs) - pf_cta_of(pc.fseg + kPfItemCost, Us, Gs);
+          old[i] = atomicAdd(a.counters + ((static_cast<size_t>(pc.n) * kKVHeads + pc.g) * a.tmax + pc.t) * 2 + h, 1);
+        }
+        __threadfence();
+        if (pf0 >= 0 && old[0] == want[0]) flags |= 1;
+        if (pf1 >= 0 && old[1] == want[1]) flags |= 2;
+        merge_flag[h] = flags;
+      }
+      pf_group_sync(h);
+      const int flags = merge_flag[h];
+#pragma unroll 1
+      for (int i = 0; i < 2; ++i) {
+        if (!((flags >> i) & 1)) continue;
+        PfPiece pc;
+        pf_find_piece(i == 0 ? pf0 : pf1, share[1], pref, a, pc);
+        const int holders0 = pf_cta_of(pc.fseg + kPfItemCost, Us, Gs);
+        const int nhold = pf_cta_of(pc.fseg + kPfItemCost + pc.nt - 1, Us, Gs) - holders0 + 1;
+        const bool first_has_two = pf_share_lo(holders0, Us, Gs) < pc.fseg;
+        auto rec_of = [&](int j) {
+          const int c = holders0 + j;
+          return a.records + static_cast<size_t>(2 * c + ((j == 0 && first_has_two) ? 1 : 0)) * kPfRecBytes +
+                 h * kPfRecHeadBytes;
+        };
+        float M = -CUDART_INF_F;
+        for (int j = 0; j < nhold; ++j) M = fmaxf(M, __ldcg(reinterpret_cast<const float*>(rec_of(j) + kPfRecO) + r));
+        const int i0 = pc.t * kPfRows;
+        const bool write = r < (pc.qlen < i0 + kPfRows ? pc.qlen : i0 + kPfRows) - i0;
+        __nv_bfloat16* orow = a.out + (static_cast<size_t>(pc.q0 + i0 + r) * kQHeads + 2 * pc.g + h) * kHeadDim;
+        float L = 0.f;
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {  // dims 64 half .. 64 half + 63
+          float acc[64];
+#pragma unroll
+          for (int e = 0; e < 64; ++e) acc[e] = 0.f;
+          float lsum = 0.f;
+#pragma unroll 2
+          for (int j = 0; j < nhold; ++j) {
+            const unsigned char* rj = rec_of(j);
+            const float m_j = __ldcg(reinterpret_cast<const float*>(rj + kPfRecO) + r);
+            const float l_j = __ldcg(reinterpret_cast<const float*>(rj + kPfRecO) + kPfRows + r);
+            const float w = m_j == -CUDART_INF_F ? 0.f : ex2(m_j - M) * l_j;  // the record holds O / l
+            lsum += w;
+            const uint2* oj = reinterpret_cast<const uint2*>(rj) + (16 * half) * kPfRows + r;
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+              const uint2 u = __ldcg(oj + q * kPfRows);
+              const float2 a01 = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+              const float2 a23 = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+              acc[4 * q] += w * a01.x;
+              acc[4 * q + 1] += w * a01.y;
+              acc[4 * q + 2] += w * a23.x;
+              acc[4 * q + 3] += w * a23.y;
+            }
+          }
+          if (half == 0) L = lsum;
+          const float inv = 1.f / L;
+          if (write) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + 64 * half);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              uint4 v;
+              v.x = pack_bf16x2(acc[8 * q + 0] * inv, acc[8 * q + 1] * inv);
+              v.y = pack_bf16x2(acc[8 * q + 2] * inv, acc[8 * q + 3] * inv);
+              v.z = pack_bf16x2(acc[8 * q + 4] * inv, acc[8 * q + 5] * inv);
+              v.w = pack_bf16x2(acc[8 * q + 6] * inv, acc[8 * q + 7] * inv);
+              dst[q] = v;
+            }
+          }
+        }
+        if (quarter == 0 && lane == 0)
+          a.counters[((static_cast<size_t>(pc.n) * kKVHeads + pc.g) * a.tmax + pc.t) * 2 + h] = 0;
       }
     }
   } else {
@@ -470,7 +1083,17 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
-size_t prefill_workspace_bytes(int32_t, int32_t, int) { return PKV_STATUS_BYTES; }
+// Workspace: status header, split counters [num_seqs][8][tmax][2], then two
+// partial records per CTA of the persistent grid (one CTA per SM).
+static size_t pf_counter_bytes(int32_t num_seqs, int32_t max_q_len) {
+  const size_t tmax = (static_cast<size_t>(max_q_len) + kPfRows - 1) / kPfRows;
+  return (static_cast<size_t>(num_seqs) * kKVHeads * tmax * 2 * 4 + 255) / 256 * 256;
+}
+size_t prefill_workspace_bytes(int32_t num_seqs, int32_t max_q_len, int num_sms) {
+  return PKV_STATUS_BYTES + pf_counter_bytes(num_seqs, max_q_len) +
+         static_cast<size_t>(2) * num_sms * kPfRecBytes;
+}
+int prefill_max_seqs() { return kPfMaxSeqs; }
 
 int launch_prefill(const void* q, const void* k_pages, const void* v_pages, const int32_t* block_table,
                    const int32_t* prefix_lens, const int32_t* cu_q_lens, int32_t num_seqs, int32_t total_q,
@@ -512,23 +1135,34 @@ int launch_prefill(const void* q, const void* k_pages, const void* v_pages, cons
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
   if (dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmemBytes) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(pf_smem_bytes(kPfMaxSeqs))) != cudaSuccess)
       return PKV_ERR_CUDA;
     attr_set[dev] = true;
   }
+  int num_sms = 0;
+  if (cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return PKV_ERR_CUDA;
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
   PrefillArgs a;
   a.block_table = block_table;
   a.prefix_lens = prefix_lens;
   a.cu_q_lens = cu_q_lens;
   a.out = static_cast<__nv_bfloat16*>(out);
+  a.num_seqs = num_seqs;
   a.total_q = total_q;
   a.max_pages = max_pages;
   a.num_pages = num_pages;
+  a.tmax = (max_q_len + kPfRows - 1) / kPfRows;
+  a.workers = num_sms;
   a.scale_log2 = scale * kLog2e;
-  a.status = static_cast<int*>(workspace);
-  const dim3 grid(((max_q_len + kPfRows - 1) / kPfRows) * kKVHeads, num_seqs);
-  return launch_pdl(prefill_kernel, grid, dim3(kPfThreads), static_cast<size_t>(kPfSmemBytes), stream, qmap, kmap,
+  a.status = reinterpret_cast<int*>(ws);
+  a.counters = reinterpret_cast<int*>(ws + PKV_STATUS_BYTES);
+  a.records = ws + PKV_STATUS_BYTES + pf_counter_bytes(num_seqs, max_q_len);
+  // one CTA per SM fits (TMEM and shared memory); split mode uses the first num_sms CTAs as persistent
+  // workers, item mode one CTA per item
+  const long long items = static_cast<long long>(num_seqs) * kKVHeads * a.tmax;
+  const unsigned grid = static_cast<unsigned>(items > num_sms ? items : num_sms);
+  return launch_pdl(prefill_kernel, dim3(grid), dim3(kPfThreads), pf_smem_bytes(num_seqs), stream, qmap, kmap,
                     vmap, a) == cudaSuccess
              ? PKV_OK
              : PKV_ERR_CUDA;

@@ -83,6 +83,20 @@ def test_full_chunk_sampled_rows(cuda_device, prefix):
     _check(case, cuda_device, rows=_sample_rows(W.PREFILL_CHUNK), what=f"chunk 4096 after {prefix}")
 
 
+def test_split_schedule_several_requests(cuda_device):
+    # three requests of 1536 rows after 3000 cached tokens: the key tiles outnumber what
+    # whole query tiles can balance over the SMs, so CTAs take equal shares that cut
+    # through (request, head, query tile) items, some across request boundaries, and
+    # the split items are merged; sampled rows of every request
+    case = W.prefill_case(44, [3000, 3000, 3000], [1536, 1536, 1536], poison=True)
+    rows = sorted({r for n in range(3) for r in range(n * 1536, (n + 1) * 1536, 48)} |
+                  {n * 1536 + r for n in range(3) for r in range(1536 - 16, 1536)})
+    run = _check(case, cuda_device, rows=rows, what="split schedule, 3 requests")
+    # merges run in an order fixed by the item, whichever CTA completes it: same bits again
+    again = PrefillOnDevice(case, cuda_device).run()
+    assert torch.equal(run.out.view(torch.int16), again.view(torch.int16))
+
+
 def test_causality_on_gpu(cuda_device):
     # perturbing keys/values at positions after row i's limit leaves row i bit-identical
     case = W.prefill_case(43, [40], [200], poison=False)
