@@ -363,16 +363,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   unsigned char* sV = smem + kOffV;
   unsigned char* sK = smem + kOffK;
 
-  // Only min(gridDim.x, U) CTAs take a share, so every share is non-empty.
-  const long long U = pref[a.num_seqs];
   const bool item_mode = pref[a.num_seqs + 1] != 0;
-  const int G = static_cast<int>(U < a.workers ? U : a.workers);
-  const bool active = static_cast<int>(blockIdx.x) < G;
-  const long long lo = active ? pf_share_lo(blockIdx.x, U, G) : 0;
-  const long long hi = active ? pf_share_lo(blockIdx.x + 1, U, G) : 0;
-  // the softmax warps re-read these from shared memory instead of keeping them live
-  volatile long long* share = pref + 2 * a.num_seqs + 3;  // lo, hi, U, G (pref[num_seqs + 1]: item mode)
-  volatile long long* pend_f = share + 4;             // [head][2]: start units of split pieces not yet counted
 
   if (item_mode) {
     // ================================================================ item mode: CTA b computes item b
@@ -632,430 +623,443 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
 
     }
-  } else if (!active) {
-  } else if (warp == kPfTmaWarp) {
-    // ------------------------------------------------------------------ TMA producer
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kPfRegsOther));
-    int gj = 0;  // key tiles of this CTA so far
-    int pi = 0;
-    PfPiece pc;
-    bool run = true;
-    for (long long f = lo; run && pf_find_piece(f, hi, pref, a, pc); f = pc.fend, ++pi) {
-      // this piece's query tiles, once the previous piece's QK MMAs are done with the buffer
-      if (pi > 0 && !pf_wait_warp(&bars->q_empty, static_cast<uint32_t>(pi - 1) & 1u, fail, a.status)) break;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&bars->q_full, 2 * kPfTileBytes);
-        for (int h = 0; h < 2; ++h)
-          for (int half = 0; half < 2; ++half)
-            tma_load_3d(sQ + h * kPfTileBytes + half * kPfHalfBytes, &qmap, half * 64, 2 * pc.g + h,
-                        pc.q0 + pc.t * kPfRows, &bars->q_full);
-      }
-      const int rows = pc.qlen < kPfRows * (pc.t + 1) ? pc.qlen : kPfRows * (pc.t + 1);
-      const int n_pages = (pc.P + rows + kPageSize - 1) / kPageSize;
-      for (int k = pc.k0; k < pc.k1; ++k, ++gj) {
-        const int st = gj & 1;
-        const int use = gj >> 1;
-        if (use > 0 && !pf_wait_warp(&bars->kv_empty[st], static_cast<uint32_t>(use - 1) & 1u, fail, a.status)) {
-          run = false;
-          break;
+  } else {
+    // ================================================================ split mode: shares of key tiles
+    // Only min(workers, U) CTAs take a share, so every share is non-empty.
+    const long long U = pref[a.num_seqs];
+    const int G = static_cast<int>(U < a.workers ? U : a.workers);
+    const bool active = static_cast<int>(blockIdx.x) < G;
+    const long long lo = active ? pf_share_lo(blockIdx.x, U, G) : 0;
+    const long long hi = active ? pf_share_lo(blockIdx.x + 1, U, G) : 0;
+    // the softmax warps re-read these from shared memory instead of keeping them live
+    volatile long long* share = pref + 2 * a.num_seqs + 3;  // lo, hi, U, G
+    volatile long long* pend_f = share + 4;                 // [head][2]: start units of split pieces not yet counted
+  if (!active) {
+    } else if (warp == kPfTmaWarp) {
+      // ------------------------------------------------------------------ TMA producer
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kPfRegsOther));
+      int gj = 0;  // key tiles of this CTA so far
+      int pi = 0;
+      PfPiece pc;
+      bool run = true;
+      for (long long f = lo; run && pf_find_piece(f, hi, pref, a, pc); f = pc.fend, ++pi) {
+        // this piece's query tiles, once the previous piece's QK MMAs are done with the buffer
+        if (pi > 0 && !pf_wait_warp(&bars->q_empty, static_cast<uint32_t>(pi - 1) & 1u, fail, a.status)) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bars->q_full, 2 * kPfTileBytes);
+          for (int h = 0; h < 2; ++h)
+            for (int half = 0; half < 2; ++half)
+              tma_load_3d(sQ + h * kPfTileBytes + half * kPfHalfBytes, &qmap, half * 64, 2 * pc.g + h,
+                          pc.q0 + pc.t * kPfRows, &bars->q_full);
         }
-        const int pg = k * kPfPagesPerTile + lane;
-        bool valid = lane < kPfPagesPerTile && pg < n_pages;
-        int id = 0;
-        if (valid) {
-          id = __ldg(a.block_table + static_cast<size_t>(pc.n) * a.max_pages + pg);
-          if (id < 0 || id >= a.num_pages) {
-            set_status(a.status, PKV_ERR_OUT_OF_BOUNDS);
-            valid = false;
+        const int rows = pc.qlen < kPfRows * (pc.t + 1) ? pc.qlen : kPfRows * (pc.t + 1);
+        const int n_pages = (pc.P + rows + kPageSize - 1) / kPageSize;
+        for (int k = pc.k0; k < pc.k1; ++k, ++gj) {
+          const int st = gj & 1;
+          const int use = gj >> 1;
+          if (use > 0 && !pf_wait_warp(&bars->kv_empty[st], static_cast<uint32_t>(use - 1) & 1u, fail, a.status)) {
+            run = false;
+            break;
+          }
+          const int pg = k * kPfPagesPerTile + lane;
+          bool valid = lane < kPfPagesPerTile && pg < n_pages;
+          int id = 0;
+          if (valid) {
+            id = __ldg(a.block_table + static_cast<size_t>(pc.n) * a.max_pages + pg);
+            if (id < 0 || id >= a.num_pages) {
+              set_status(a.status, PKV_ERR_OUT_OF_BOUNDS);
+              valid = false;
+            }
+          }
+          const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+          const uint32_t bytes = static_cast<uint32_t>(__popc(vmask)) * 2u * (kPageSize * 128u);
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&bars->k_full[st], bytes);
+            mbar_arrive_expect_tx(&bars->v_full[st], bytes);
+          }
+          __syncwarp();
+          if (valid) {
+            const int row = (id * kKVHeads + pc.g) * kPageSize;
+            unsigned char* kd = sK + st * kPfTileBytes + lane * (kPageSize * 128);
+            unsigned char* vd = sV + st * kPfTileBytes + lane * (kPageSize * 128);
+            tma_load_2d(kd, &kmap, 0, row, &bars->k_full[st]);
+            tma_load_2d(kd + kPfHalfBytes, &kmap, 64, row, &bars->k_full[st]);
+            tma_load_2d(vd, &vmap, 0, row, &bars->v_full[st]);
+            tma_load_2d(vd + kPfHalfBytes, &vmap, 64, row, &bars->v_full[st]);
           }
         }
-        const unsigned vmask = __ballot_sync(0xffffffffu, valid);
-        const uint32_t bytes = static_cast<uint32_t>(__popc(vmask)) * 2u * (kPageSize * 128u);
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&bars->k_full[st], bytes);
-          mbar_arrive_expect_tx(&bars->v_full[st], bytes);
-        }
-        __syncwarp();
-        if (valid) {
-          const int row = (id * kKVHeads + pc.g) * kPageSize;
-          unsigned char* kd = sK + st * kPfTileBytes + lane * (kPageSize * 128);
-          unsigned char* vd = sV + st * kPfTileBytes + lane * (kPageSize * 128);
-          tma_load_2d(kd, &kmap, 0, row, &bars->k_full[st]);
-          tma_load_2d(kd + kPfHalfBytes, &kmap, 64, row, &bars->k_full[st]);
-          tma_load_2d(vd, &vmap, 0, row, &bars->v_full[st]);
-          tma_load_2d(vd + kPfHalfBytes, &vmap, 64, row, &bars->v_full[st]);
-        }
       }
-    }
-  } else if (warp == kPfMmaWarp) {
-    // ------------------------------------------------------------------ MMA issuer
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kPfRegsOther));
-    // Issue order QK_0(0) QK_1(0) | PV_0(j) QK_0(j+1) PV_1(j) QK_1(j+1) | ... over
-    // the CTA's key tiles (across pieces): the two heads' softmaxes run half a
-    // period apart, so while one head's softmax works the other head's PV and
-    // next QK keep the tensor pipe busy. QK_h(j+1) overwrites S_h, which holds
-    // P_h(j), so it waits for PV_h(j) (o_done) -- which also keeps O_h out of
-    // the softmax's way while it rescales it or reads it at the end of a piece.
-    auto issue_qk = [&](int st, int h) {
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t qa = smem_u32(sQ + h * kPfTileBytes);
-        const uint32_t kb = smem_u32(sK + st * kPfTileBytes);
-#pragma unroll
-        for (int s = 0; s < 8; ++s) {
-          const uint32_t off = (s >> 2) * kPfHalfBytes + (s & 3) * 32;
-          mma_ss(tmem + kColS + 128 * h, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
-                 kIdescQK, s > 0 ? 1u : 0u);
-        }
-        mma_commit(&bars->s_full[h]);
-      }
-      __syncwarp();
-    };
-    auto issue_pv = [&](int st, int h, bool acc) {
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t vb = smem_u32(sV + st * kPfTileBytes);
-#pragma unroll
-        for (int s = 0; s < 8; ++s) {
-          mma_ts(tmem + kColO + 128 * h, tmem + kColS + 128 * h + 8 * s,
-                 sdesc_sw128(vb + s * 2048, kPfHalfBytes, 1024), kIdescPV, (acc || s > 0) ? 1u : 0u);
-        }
-        mma_commit(&bars->o_done[h]);
-      }
-      __syncwarp();
-    };
-    auto commit_q_empty = [&]() {
-      if (lane == 0) mma_commit(&bars->q_empty);
-      __syncwarp();
-    };
-    PfPiece cur, nxt;
-    bool ok = pf_find_piece(lo, hi, pref, a, cur);
-    bool have_nxt = ok && pf_find_piece(cur.fend, hi, pref, a, nxt);
-    ok = ok && pf_wait_warp(&bars->q_full, 0, fail, a.status) && pf_wait_warp(&bars->k_full[0], 0, fail, a.status);
-    if (ok) {
-      issue_qk(0, 0);
-      issue_qk(0, 1);
-      if (cur.k1 - cur.k0 == 1) commit_q_empty();
-    }
-    int gj = 0, j = 0, pi = 0;
-    while (ok) {
-      const int st = gj & 1;
-      const uint32_t ph = static_cast<uint32_t>(gj >> 1) & 1u;
-      const uint32_t pj = static_cast<uint32_t>(gj) & 1u;
-      const int ntiles = cur.k1 - cur.k0;
-      const bool next_in = j + 1 < ntiles;
-      const bool next = next_in || have_nxt;
-      const int k = cur.k0 + j;
-      if (!pf_wait_warp(&bars->v_full[st], ph, fail, a.status)) break;
-      const int rows = cur.qlen < kPfRows * (cur.t + 1) ? cur.qlen : kPfRows * (cur.t + 1);
-      const int kv_end = cur.P + rows;
-      if (k == cur.nt - 1 && kv_end < (k + 1) * kPfKeys) {
-        // keys past the end: zero their V rows (unused slots may hold NaN and 0 * NaN = NaN)
-        const int r0 = kv_end - k * kPfKeys;
-        uint4* vbase = reinterpret_cast<uint4*>(sV + st * kPfTileBytes);
-        for (int idx = r0 * 8 + lane; idx < kPfKeys * 8; idx += 32) {
-          vbase[idx] = make_uint4(0, 0, 0, 0);
-          vbase[kPfHalfBytes / 16 + idx] = make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-      }
-      if (!pf_wait_warp(&bars->p_full[0], pj, fail, a.status)) break;
-      issue_pv(st, 0, j > 0);
-      if (next) {
-        if (!next_in && !pf_wait_warp(&bars->q_full, static_cast<uint32_t>(pi + 1) & 1u, fail, a.status)) break;
-        if (!pf_wait_warp(&bars->k_full[st ^ 1], static_cast<uint32_t>((gj + 1) >> 1) & 1u, fail, a.status) ||
-            !pf_wait_warp(&bars->o_done[0], pj, fail, a.status))
-          break;
-        issue_qk(st ^ 1, 0);
-      }
-      if (!pf_wait_warp(&bars->p_full[1], pj, fail, a.status)) break;
-      issue_pv(st, 1, j > 0);
-      if (lane == 0) mma_commit(&bars->kv_empty[st]);
-      __syncwarp();
-      if (!next) break;
-      if (!pf_wait_warp(&bars->o_done[1], pj, fail, a.status)) break;
-      issue_qk(st ^ 1, 1);
-      // that was the last QK of its piece: the query buffer may be refilled
-      if (next_in ? j + 2 == ntiles : nxt.k1 - nxt.k0 == 1) commit_q_empty();
-      ++gj;
-      if (next_in) {
-        ++j;
-      } else {
-        cur = nxt;
-        have_nxt = pf_find_piece(cur.fend, hi, pref, a, nxt);
-        j = 0;
-        ++pi;
-      }
-    }
-  } else if (warp < 8) {
-    // ------------------------------------------------------------------ softmax warpgroups
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kPfRegsSoftmax));
-    const int h = warp >> 2;
-    const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;  // row of the tile = TMEM lane
-    const uint32_t t_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    if (quarter == 0 && lane == 0) {
-      share[0] = lo;
-      share[1] = hi;
-      share[2] = U;
-      share[3] = G;
-      pend_f[2 * h] = -1;
-      pend_f[2 * h + 1] = -1;
-    }
-    pf_group_sync(h);  // both warpgroups write the same values
-    bool ok = true;
-    int gj = 0;
-    long long f = share[0];
-    while (true) {
-      // only the scalars the key-tile loop needs stay live across it (the piece is
-      // looked up again for the end-of-piece work)
-      int kb, ke, lim, diag_from;
-      {
-        PfPiece pc;
-        if (!pf_find_piece(f, share[1], pref, a, pc)) break;
-        const int i0 = pc.t * kPfRows;
-        const int rows = pc.qlen < i0 + kPfRows ? pc.qlen : i0 + kPfRows;
-        const int lim_row = pc.P + i0 + r;  // last visible key of this row (causal)
-        lim = lim_row < pc.P + rows - 1 ? lim_row : pc.P + rows - 1;
-        diag_from = pc.P + i0;
-        kb = pc.k0;
-        ke = pc.k1;
-      }
-      float m_used = -CUDART_INF_F;
-      float l = 0.f;
-      for (int k = kb; k < ke; ++k, ++gj) {
-        if (ok && !pf_wait_warp(&bars->s_full[h], static_cast<uint32_t>(gj) & 1u, fail, a.status)) ok = false;
-        if (!ok) continue;
+    } else if (warp == kPfMmaWarp) {
+      // ------------------------------------------------------------------ MMA issuer
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kPfRegsOther));
+      // Issue order QK_0(0) QK_1(0) | PV_0(j) QK_0(j+1) PV_1(j) QK_1(j+1) | ... over
+      // the CTA's key tiles (across pieces): the two heads' softmaxes run half a
+      // period apart, so while one head's softmax works the other head's PV and
+      // next QK keep the tensor pipe busy. QK_h(j+1) overwrites S_h, which holds
+      // P_h(j), so it waits for PV_h(j) (o_done) -- which also keeps O_h out of
+      // the softmax's way while it rescales it or reads it at the end of a piece.
+      auto issue_qk = [&](int st, int h) {
         tc_fence_after();
-        uint32_t sr[4][32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(t_row + kColS + 128 * h + 32 * c, sr[c]);
-        tmem_ld_wait();
-        const bool diag = k * kPfKeys + kPfKeys - 1 > diag_from;
-        // row max over the raw scores (the scale is positive, so it keeps the order)
-        float mx = -CUDART_INF_F;
-        if (diag) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              if (k * kPfKeys + 32 * c + e > lim) sr[c][e] = __float_as_uint(-CUDART_INF_F);
-              mx = fmaxf(mx, __uint_as_float(sr[c][e]));
-            }
-        } else {
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(sr[c][e]));
+        if (lane == 0) {
+          const uint32_t qa = smem_u32(sQ + h * kPfTileBytes);
+          const uint32_t kb = smem_u32(sK + st * kPfTileBytes);
+  #pragma unroll
+          for (int s = 0; s < 8; ++s) {
+            const uint32_t off = (s >> 2) * kPfHalfBytes + (s & 3) * 32;
+            mma_ss(tmem + kColS + 128 * h, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
+                   kIdescQK, s > 0 ? 1u : 0u);
+          }
+          mma_commit(&bars->s_full[h]);
         }
-        const float m_new = fmaxf(m_used, mx);
-        const bool first = m_used == -CUDART_INF_F;
-        const bool grow = first || (m_new - m_used) * a.scale_log2 > 8.f;
-        if (__any_sync(0xffffffffu, grow)) {
-          const float alpha = first ? 0.f : (grow ? ex2((m_used - m_new) * a.scale_log2) : 1.f);
-          if (k > kb) {
-#pragma unroll
+        __syncwarp();
+      };
+      auto issue_pv = [&](int st, int h, bool acc) {
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t vb = smem_u32(sV + st * kPfTileBytes);
+  #pragma unroll
+          for (int s = 0; s < 8; ++s) {
+            mma_ts(tmem + kColO + 128 * h, tmem + kColS + 128 * h + 8 * s,
+                   sdesc_sw128(vb + s * 2048, kPfHalfBytes, 1024), kIdescPV, (acc || s > 0) ? 1u : 0u);
+          }
+          mma_commit(&bars->o_done[h]);
+        }
+        __syncwarp();
+      };
+      auto commit_q_empty = [&]() {
+        if (lane == 0) mma_commit(&bars->q_empty);
+        __syncwarp();
+      };
+      PfPiece cur, nxt;
+      bool ok = pf_find_piece(lo, hi, pref, a, cur);
+      bool have_nxt = ok && pf_find_piece(cur.fend, hi, pref, a, nxt);
+      ok = ok && pf_wait_warp(&bars->q_full, 0, fail, a.status) && pf_wait_warp(&bars->k_full[0], 0, fail, a.status);
+      if (ok) {
+        issue_qk(0, 0);
+        issue_qk(0, 1);
+        if (cur.k1 - cur.k0 == 1) commit_q_empty();
+      }
+      int gj = 0, j = 0, pi = 0;
+      while (ok) {
+        const int st = gj & 1;
+        const uint32_t ph = static_cast<uint32_t>(gj >> 1) & 1u;
+        const uint32_t pj = static_cast<uint32_t>(gj) & 1u;
+        const int ntiles = cur.k1 - cur.k0;
+        const bool next_in = j + 1 < ntiles;
+        const bool next = next_in || have_nxt;
+        const int k = cur.k0 + j;
+        if (!pf_wait_warp(&bars->v_full[st], ph, fail, a.status)) break;
+        const int rows = cur.qlen < kPfRows * (cur.t + 1) ? cur.qlen : kPfRows * (cur.t + 1);
+        const int kv_end = cur.P + rows;
+        if (k == cur.nt - 1 && kv_end < (k + 1) * kPfKeys) {
+          // keys past the end: zero their V rows (unused slots may hold NaN and 0 * NaN = NaN)
+          const int r0 = kv_end - k * kPfKeys;
+          uint4* vbase = reinterpret_cast<uint4*>(sV + st * kPfTileBytes);
+          for (int idx = r0 * 8 + lane; idx < kPfKeys * 8; idx += 32) {
+            vbase[idx] = make_uint4(0, 0, 0, 0);
+            vbase[kPfHalfBytes / 16 + idx] = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+        if (!pf_wait_warp(&bars->p_full[0], pj, fail, a.status)) break;
+        issue_pv(st, 0, j > 0);
+        if (next) {
+          if (!next_in && !pf_wait_warp(&bars->q_full, static_cast<uint32_t>(pi + 1) & 1u, fail, a.status)) break;
+          if (!pf_wait_warp(&bars->k_full[st ^ 1], static_cast<uint32_t>((gj + 1) >> 1) & 1u, fail, a.status) ||
+              !pf_wait_warp(&bars->o_done[0], pj, fail, a.status))
+            break;
+          issue_qk(st ^ 1, 0);
+        }
+        if (!pf_wait_warp(&bars->p_full[1], pj, fail, a.status)) break;
+        issue_pv(st, 1, j > 0);
+        if (lane == 0) mma_commit(&bars->kv_empty[st]);
+        __syncwarp();
+        if (!next) break;
+        if (!pf_wait_warp(&bars->o_done[1], pj, fail, a.status)) break;
+        issue_qk(st ^ 1, 1);
+        // that was the last QK of its piece: the query buffer may be refilled
+        if (next_in ? j + 2 == ntiles : nxt.k1 - nxt.k0 == 1) commit_q_empty();
+        ++gj;
+        if (next_in) {
+          ++j;
+        } else {
+          cur = nxt;
+          have_nxt = pf_find_piece(cur.fend, hi, pref, a, nxt);
+          j = 0;
+          ++pi;
+        }
+      }
+    } else if (warp < 8) {
+      // ------------------------------------------------------------------ softmax warpgroups
+      asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kPfRegsSoftmax));
+      const int h = warp >> 2;
+      const int quarter = warp & 3;
+      const int r = quarter * 32 + lane;  // row of the tile = TMEM lane
+      const uint32_t t_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+      if (quarter == 0 && lane == 0) {
+        share[0] = lo;
+        share[1] = hi;
+        share[2] = U;
+        share[3] = G;
+        pend_f[2 * h] = -1;
+        pend_f[2 * h + 1] = -1;
+      }
+      pf_group_sync(h);  // both warpgroups write the same values
+      bool ok = true;
+      int gj = 0;
+      long long f = share[0];
+      while (true) {
+        // only the scalars the key-tile loop needs stay live across it (the piece is
+        // looked up again for the end-of-piece work)
+        int kb, ke, lim, diag_from;
+        {
+          PfPiece pc;
+          if (!pf_find_piece(f, share[1], pref, a, pc)) break;
+          const int i0 = pc.t * kPfRows;
+          const int rows = pc.qlen < i0 + kPfRows ? pc.qlen : i0 + kPfRows;
+          const int lim_row = pc.P + i0 + r;  // last visible key of this row (causal)
+          lim = lim_row < pc.P + rows - 1 ? lim_row : pc.P + rows - 1;
+          diag_from = pc.P + i0;
+          kb = pc.k0;
+          ke = pc.k1;
+        }
+        float m_used = -CUDART_INF_F;
+        float l = 0.f;
+        for (int k = kb; k < ke; ++k, ++gj) {
+          if (ok && !pf_wait_warp(&bars->s_full[h], static_cast<uint32_t>(gj) & 1u, fail, a.status)) ok = false;
+          if (!ok) continue;
+          tc_fence_after();
+          uint32_t sr[4][32];
+  #pragma unroll
+          for (int c = 0; c < 4; ++c) tmem_ld32(t_row + kColS + 128 * h + 32 * c, sr[c]);
+          tmem_ld_wait();
+          const bool diag = k * kPfKeys + kPfKeys - 1 > diag_from;
+          // row max over the raw scores (the scale is positive, so it keeps the order)
+          float mx = -CUDART_INF_F;
+          if (diag) {
+  #pragma unroll
+            for (int c = 0; c < 4; ++c)
+  #pragma unroll
+              for (int e = 0; e < 32; ++e) {
+                if (k * kPfKeys + 32 * c + e > lim) sr[c][e] = __float_as_uint(-CUDART_INF_F);
+                mx = fmaxf(mx, __uint_as_float(sr[c][e]));
+              }
+          } else {
+  #pragma unroll
+            for (int c = 0; c < 4; ++c)
+  #pragma unroll
+              for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(sr[c][e]));
+          }
+          const float m_new = fmaxf(m_used, mx);
+          const bool first = m_used == -CUDART_INF_F;
+          const bool grow = first || (m_new - m_used) * a.scale_log2 > 8.f;
+          if (__any_sync(0xffffffffu, grow)) {
+            const float alpha = first ? 0.f : (grow ? ex2((m_used - m_new) * a.scale_log2) : 1.f);
+            if (k > kb) {
+  #pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                uint32_t orr[32];
+                tmem_ld32(t_row + kColO + 128 * h + 32 * c, orr);
+                tmem_ld_wait();
+  #pragma unroll
+                for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+                tmem_st32(t_row + kColO + 128 * h + 32 * c, orr);
+              }
+              tmem_st_wait();
+            }
+            if (grow) {
+              l *= alpha;
+              m_used = m_new;
+            }
+          }
+          // P = 2^(s * scale * log2 e - m * scale * log2 e) as bf16 pairs over S's first 64 columns;
+          // a row with no visible key yet (a piece that starts past key 0) gets P = 0
+          const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
+          const float mo = m_used == -CUDART_INF_F ? 0.f : -m_used * a.scale_log2;
+          const float2 nm2 = make_float2(mo, mo);
+          float2 l2 = make_float2(0.f, 0.f);
+  #pragma unroll
+          for (int c = 0; c < 4; ++c) {  // scores 32c .. 32c+31 -> P columns 16c .. 16c+15
+            uint32_t pk[16];
+  #pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              const float2 t =
+                  __ffma2_rn(make_float2(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1])), sc2, nm2);
+              float2 pp;
+              if (((e >> 1) & 3) < kPfPolyPairsOf4) {
+                pp = exp2_poly2(t);
+              } else {
+                pp = make_float2(ex2(t.x), ex2(t.y));
+              }
+              l2 = __fadd2_rn(l2, pp);
+              pk[e >> 1] = pack_bf16x2(pp.x, pp.y);
+            }
+            tmem_st16(t_row + kColS + 128 * h + 16 * c, pk);
+          }
+          l += l2.x + l2.y;
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive_cta(&bars->p_full[h]);
+        }
+        // ---- end of the piece: O_h is complete once PV_h of its last key tile is done
+        if (ok && !pf_wait_warp(&bars->o_done[h], static_cast<uint32_t>(gj - 1) & 1u, fail, a.status)) ok = false;
+        if (ok) tc_fence_after();
+        asm volatile("" : "+l"(f));  // look the piece up again rather than keep it live
+        PfPiece pc;
+        pf_find_piece(f, share[1], pref, a, pc);
+        const int i0 = pc.t * kPfRows;
+        const int rows_here = (pc.qlen < i0 + kPfRows ? pc.qlen : i0 + kPfRows) - i0;
+        const bool write = r < rows_here;
+        __nv_bfloat16* orow = a.out + (static_cast<size_t>(pc.q0 + i0 + r) * kQHeads + 2 * pc.g + h) * kHeadDim;
+        if (pc.k0 == 0 && pc.k1 == pc.nt) {
+          if (ok) {
+            const float inv = 1.f / l;
+  #pragma unroll
             for (int c = 0; c < 4; ++c) {
               uint32_t orr[32];
               tmem_ld32(t_row + kColO + 128 * h + 32 * c, orr);
               tmem_ld_wait();
-#pragma unroll
-              for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
-              tmem_st32(t_row + kColO + 128 * h + 32 * c, orr);
+              if (write) {
+                uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+  #pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                  uint4 v;
+                  v.x = pack_bf16x2(__uint_as_float(orr[8 * q + 0]) * inv, __uint_as_float(orr[8 * q + 1]) * inv);
+                  v.y = pack_bf16x2(__uint_as_float(orr[8 * q + 2]) * inv, __uint_as_float(orr[8 * q + 3]) * inv);
+                  v.z = pack_bf16x2(__uint_as_float(orr[8 * q + 4]) * inv, __uint_as_float(orr[8 * q + 5]) * inv);
+                  v.w = pack_bf16x2(__uint_as_float(orr[8 * q + 6]) * inv, __uint_as_float(orr[8 * q + 7]) * inv);
+                  dst[q] = v;
+                }
+              }
             }
-            tmem_st_wait();
           }
-          if (grow) {
-            l *= alpha;
-            m_used = m_new;
-          }
-        }
-        // P = 2^(s * scale * log2 e - m * scale * log2 e) as bf16 pairs over S's first 64 columns;
-        // a row with no visible key yet (a piece that starts past key 0) gets P = 0
-        const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
-        const float mo = m_used == -CUDART_INF_F ? 0.f : -m_used * a.scale_log2;
-        const float2 nm2 = make_float2(mo, mo);
-        float2 l2 = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {  // scores 32c .. 32c+31 -> P columns 16c .. 16c+15
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const float2 t =
-                __ffma2_rn(make_float2(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1])), sc2, nm2);
-            float2 pp;
-            if (((e >> 1) & 3) < kPfPolyPairsOf4) {
-              pp = exp2_poly2(t);
-            } else {
-              pp = make_float2(ex2(t.x), ex2(t.y));
+        } else {
+          // Split piece (only a share's first and last piece can be): write this
+          // CTA's partial record of the row now, count it after the last piece.
+          unsigned char* rec = a.records + static_cast<size_t>(2 * blockIdx.x + (f == share[0] ? 0 : 1)) * kPfRecBytes +
+                               h * kPfRecHeadBytes;
+          uint2* ro = reinterpret_cast<uint2*>(rec);
+          float* rml = reinterpret_cast<float*>(rec + kPfRecO);
+          const float inv = l > 0.f ? 1.f / l : 0.f;  // a row with no visible key in the piece has l = 0
+          if (ok) {
+  #pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              uint32_t orr[32];
+              tmem_ld32(t_row + kColO + 128 * h + 32 * c, orr);
+              tmem_ld_wait();
+  #pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                // O / l is a convex combination of V rows; fp16 holds it (clamped to the fp16 range)
+                auto h16 = [&](int e) { return fminf(fmaxf(__uint_as_float(orr[e]) * inv, -65504.f), 65504.f); };
+                const __half2 lo2 = __floats2half2_rn(h16(4 * q), h16(4 * q + 1));
+                const __half2 hi2 = __floats2half2_rn(h16(4 * q + 2), h16(4 * q + 3));
+                ro[(c * 8 + q) * kPfRows + r] =
+                    make_uint2(*reinterpret_cast<const uint32_t*>(&lo2), *reinterpret_cast<const uint32_t*>(&hi2));
+              }
             }
-            l2 = __fadd2_rn(l2, pp);
-            pk[e >> 1] = pack_bf16x2(pp.x, pp.y);
           }
-          tmem_st16(t_row + kColS + 128 * h + 16 * c, pk);
+          rml[r] = m_used == -CUDART_INF_F ? -CUDART_INF_F : m_used * a.scale_log2;
+          rml[kPfRows + r] = l;
+          if (quarter == 0 && lane == 0) pend_f[2 * h + (f == share[0] ? 0 : 1)] = f;
         }
-        l += l2.x + l2.y;
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive_cta(&bars->p_full[h]);
+        f = pc.fend;
       }
-      // ---- end of the piece: O_h is complete once PV_h of its last key tile is done
-      if (ok && !pf_wait_warp(&bars->o_done[h], static_cast<uint32_t>(gj - 1) & 1u, fail, a.status)) ok = false;
-      if (ok) tc_fence_after();
-      asm volatile("" : "+l"(f));  // look the piece up again rather than keep it live
-      PfPiece pc;
-      pf_find_piece(f, share[1], pref, a, pc);
-      const int i0 = pc.t * kPfRows;
-      const int rows_here = (pc.qlen < i0 + kPfRows ? pc.qlen : i0 + kPfRows) - i0;
-      const bool write = r < rows_here;
-      __nv_bfloat16* orow = a.out + (static_cast<size_t>(pc.q0 + i0 + r) * kQHeads + 2 * pc.g + h) * kHeadDim;
-      if (pc.k0 == 0 && pc.k1 == pc.nt) {
-        if (ok) {
-          const float inv = 1.f / l;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t orr[32];
-            tmem_ld32(t_row + kColO + 128 * h + 32 * c, orr);
-            tmem_ld_wait();
+      // ---- count the split pieces' records in (one fence, one round trip); the
+      // CTA that completes an item's count merges the records of all its holders
+      // (log-sum-exp) and resets the counter. The barriers run whatever ok is.
+      pf_group_sync(h);  // this head's records and pend_f are written
+      const long long pf0 = pend_f[2 * h], pf1 = pend_f[2 * h + 1];
+      if (pf0 >= 0 || pf1 >= 0) {
+        const long long Us = share[2];
+        const int Gs = static_cast<int>(share[3]);
+        if (quarter == 0 && lane == 0) {
+          int flags = 0;
+          __threadfence();
+          int old[2] = {-1, -1}, want[2] = {0, 0};
+  #pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const long long fi = i == 0 ? pf0 : pf1;
+            if (fi < 0) continue;
+            PfPiece pc;
+            pf_find_piece(fi, share[1], pref, a, pc);
+            want[i] = pf_cta_of(pc.fseg + kPfItemCost + pc.nt - 1, Us, Gs) - pf_cta_of(pc.fseg + kPfItemCost, Us, Gs);
+            old[i] = atomicAdd(a.counters + ((static_cast<size_t>(pc.n) * kKVHeads + pc.g) * a.tmax + pc.t) * 2 + h, 1);
+          }
+          __threadfence();
+          if (pf0 >= 0 && old[0] == want[0]) flags |= 1;
+          if (pf1 >= 0 && old[1] == want[1]) flags |= 2;
+          merge_flag[h] = flags;
+        }
+        pf_group_sync(h);
+        const int flags = merge_flag[h];
+  #pragma unroll 1
+        for (int i = 0; i < 2; ++i) {
+          if (!((flags >> i) & 1)) continue;
+          PfPiece pc;
+          pf_find_piece(i == 0 ? pf0 : pf1, share[1], pref, a, pc);
+          const int holders0 = pf_cta_of(pc.fseg + kPfItemCost, Us, Gs);
+          const int nhold = pf_cta_of(pc.fseg + kPfItemCost + pc.nt - 1, Us, Gs) - holders0 + 1;
+          const bool first_has_two = pf_share_lo(holders0, Us, Gs) < pc.fseg;
+          auto rec_of = [&](int j) {
+            const int c = holders0 + j;
+            return a.records + static_cast<size_t>(2 * c + ((j == 0 && first_has_two) ? 1 : 0)) * kPfRecBytes +
+                   h * kPfRecHeadBytes;
+          };
+          float M = -CUDART_INF_F;
+          for (int j = 0; j < nhold; ++j) M = fmaxf(M, __ldcg(reinterpret_cast<const float*>(rec_of(j) + kPfRecO) + r));
+          const int i0 = pc.t * kPfRows;
+          const bool write = r < (pc.qlen < i0 + kPfRows ? pc.qlen : i0 + kPfRows) - i0;
+          __nv_bfloat16* orow = a.out + (static_cast<size_t>(pc.q0 + i0 + r) * kQHeads + 2 * pc.g + h) * kHeadDim;
+          float L = 0.f;
+  #pragma unroll 1
+          for (int half = 0; half < 2; ++half) {  // dims 64 half .. 64 half + 63
+            float acc[64];
+  #pragma unroll
+            for (int e = 0; e < 64; ++e) acc[e] = 0.f;
+            float lsum = 0.f;
+  #pragma unroll 2
+            for (int j = 0; j < nhold; ++j) {
+              const unsigned char* rj = rec_of(j);
+              const float m_j = __ldcg(reinterpret_cast<const float*>(rj + kPfRecO) + r);
+              const float l_j = __ldcg(reinterpret_cast<const float*>(rj + kPfRecO) + kPfRows + r);
+              const float w = m_j == -CUDART_INF_F ? 0.f : ex2(m_j - M) * l_j;  // the record holds O / l
+              lsum += w;
+              const uint2* oj = reinterpret_cast<const uint2*>(rj) + (16 * half) * kPfRows + r;
+  #pragma unroll
+              for (int q = 0; q < 16; ++q) {
+                const uint2 u = __ldcg(oj + q * kPfRows);
+                const float2 a01 = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+                const float2 a23 = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+                acc[4 * q] += w * a01.x;
+                acc[4 * q + 1] += w * a01.y;
+                acc[4 * q + 2] += w * a23.x;
+                acc[4 * q + 3] += w * a23.y;
+              }
+            }
+            if (half == 0) L = lsum;
+            const float inv = 1.f / L;
             if (write) {
-              uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
+              uint4* dst = reinterpret_cast<uint4*>(orow + 64 * half);
+  #pragma unroll
+              for (int q = 0; q < 8; ++q) {
                 uint4 v;
-                v.x = pack_bf16x2(__uint_as_float(orr[8 * q + 0]) * inv, __uint_as_float(orr[8 * q + 1]) * inv);
-                v.y = pack_bf16x2(__uint_as_float(orr[8 * q + 2]) * inv, __uint_as_float(orr[8 * q + 3]) * inv);
-                v.z = pack_bf16x2(__uint_as_float(orr[8 * q + 4]) * inv, __uint_as_float(orr[8 * q + 5]) * inv);
-                v.w = pack_bf16x2(__uint_as_float(orr[8 * q + 6]) * inv, __uint_as_float(orr[8 * q + 7]) * inv);
+                v.x = pack_bf16x2(acc[8 * q + 0] * inv, acc[8 * q + 1] * inv);
+                v.y = pack_bf16x2(acc[8 * q + 2] * inv, acc[8 * q + 3] * inv);
+                v.z = pack_bf16x2(acc[8 * q + 4] * inv, acc[8 * q + 5] * inv);
+                v.w = pack_bf16x2(acc[8 * q + 6] * inv, acc[8 * q + 7] * inv);
                 dst[q] = v;
               }
             }
           }
+          if (quarter == 0 && lane == 0)
+            a.counters[((static_cast<size_t>(pc.n) * kKVHeads + pc.g) * a.tmax + pc.t) * 2 + h] = 0;
         }
-      } else {
-        // Split piece (only a share's first and last piece can be): write this
-        // CTA's partial record of the row now, count it after the last piece.
-        unsigned char* rec = a.records + static_cast<size_t>(2 * blockIdx.x + (f == share[0] ? 0 : 1)) * kPfRecBytes +
-                             h * kPfRecHeadBytes;
-        uint2* ro = reinterpret_cast<uint2*>(rec);
-        float* rml = reinterpret_cast<float*>(rec + kPfRecO);
-        const float inv = l > 0.f ? 1.f / l : 0.f;  // a row with no visible key in the piece has l = 0
-        if (ok) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t orr[32];
-            tmem_ld32(t_row + kColO + 128 * h + 32 * c, orr);
-            tmem_ld_wait();
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              // O / l is a convex combination of V rows; fp16 holds it (clamped to the fp16 range)
-              auto h16 = [&](int e) { return fminf(fmaxf(__uint_as_float(orr[e]) * inv, -65504.f), 65504.f); };
-              const __half2 lo2 = __floats2half2_rn(h16(4 * q), h16(4 * q + 1));
-              const __half2 hi2 = __floats2half2_rn(h16(4 * q + 2), h16(4 * q + 3));
-              ro[(c * 8 + q) * kPfRows + r] =
-                  make_uint2(*reinterpret_cast<const uint32_t*>(&lo2), *reinterpret_cast<const uint32_t*>(&hi2));
-            }
-          }
-        }
-        rml[r] = m_used == -CUDART_INF_F ? -CUDART_INF_F : m_used * a.scale_log2;
-        rml[kPfRows + r] = l;
-        if (quarter == 0 && lane == 0) pend_f[2 * h + (f == share[0] ? 0 : 1)] = f;
       }
-      f = pc.fend;
+    } else {
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kPfRegsOther));  // idle warps 10-11
     }
-    // ---- count the split pieces' records in (one fence, one round trip); the
-    // CTA that completes an item's count merges the records of all its holders
-    // (log-sum-exp) and resets the counter. The barriers run whatever ok is.
-    pf_group_sync(h);  // this head's records and pend_f are written
-    const long long pf0 = pend_f[2 * h], pf1 = pend_f[2 * h + 1];
-    if (pf0 >= 0 || pf1 >= 0) {
-      const long long Us = share[2];
-      const int Gs = static_cast<int>(share[3]);
-      if (quarter == 0 && lane == 0) {
-        int flags = 0;
-        __threadfence();
-        int old[2] = {-1, -1}, want[2] = {0, 0};
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const long long fi = i == 0 ? pf0 : pf1;
-          if (fi < 0) continue;
-          PfPiece pc;
-          pf_find_piece(fi, share[1], pref, a, pc);
-          want[i] = pf_cta_of(pc.fseg + kPfItemCost + pc.nt - 1, Us, Gs) - pf_cta_of(pc.fseg + kPfItemCost, Us, Gs);
-          old[i] = atomicAdd(a.counters + ((static_cast<size_t>(pc.n) * kKVHeads + pc.g) * a.tmax + pc.t) * 2 + h, 1);
-        }
-        __threadfence();
-        if (pf0 >= 0 && old[0] == want[0]) flags |= 1;
-        if (pf1 >= 0 && old[1] == want[1]) flags |= 2;
-        merge_flag[h] = flags;
-      }
-      pf_group_sync(h);
-      const int flags = merge_flag[h];
-#pragma unroll 1
-      for (int i = 0; i < 2; ++i) {
-        if (!((flags >> i) & 1)) continue;
-        PfPiece pc;
-        pf_find_piece(i == 0 ? pf0 : pf1, share[1], pref, a, pc);
-        const int holders0 = pf_cta_of(pc.fseg + kPfItemCost, Us, Gs);
-        const int nhold = pf_cta_of(pc.fseg + kPfItemCost + pc.nt - 1, Us, Gs) - holders0 + 1;
-        const bool first_has_two = pf_share_lo(holders0, Us, Gs) < pc.fseg;
-        auto rec_of = [&](int j) {
-          const int c = holders0 + j;
-          return a.records + static_cast<size_t>(2 * c + ((j == 0 && first_has_two) ? 1 : 0)) * kPfRecBytes +
-                 h * kPfRecHeadBytes;
-        };
-        float M = -CUDART_INF_F;
-        for (int j = 0; j < nhold; ++j) M = fmaxf(M, __ldcg(reinterpret_cast<const float*>(rec_of(j) + kPfRecO) + r));
-        const int i0 = pc.t * kPfRows;
-        const bool write = r < (pc.qlen < i0 + kPfRows ? pc.qlen : i0 + kPfRows) - i0;
-        __nv_bfloat16* orow = a.out + (static_cast<size_t>(pc.q0 + i0 + r) * kQHeads + 2 * pc.g + h) * kHeadDim;
-        float L = 0.f;
-#pragma unroll 1
-        for (int half = 0; half < 2; ++half) {  // dims 64 half .. 64 half + 63
-          float acc[64];
-#pragma unroll
-          for (int e = 0; e < 64; ++e) acc[e] = 0.f;
-          float lsum = 0.f;
-#pragma unroll 2
-          for (int j = 0; j < nhold; ++j) {
-            const unsigned char* rj = rec_of(j);
-            const float m_j = __ldcg(reinterpret_cast<const float*>(rj + kPfRecO) + r);
-            const float l_j = __ldcg(reinterpret_cast<const float*>(rj + kPfRecO) + kPfRows + r);
-            const float w = m_j == -CUDART_INF_F ? 0.f : ex2(m_j - M) * l_j;  // the record holds O / l
-            lsum += w;
-            const uint2* oj = reinterpret_cast<const uint2*>(rj) + (16 * half) * kPfRows + r;
-#pragma unroll
-            for (int q = 0; q < 16; ++q) {
-              const uint2 u = __ldcg(oj + q * kPfRows);
-              const float2 a01 = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
-              const float2 a23 = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
-              acc[4 * q] += w * a01.x;
-              acc[4 * q + 1] += w * a01.y;
-              acc[4 * q + 2] += w * a23.x;
-              acc[4 * q + 3] += w * a23.y;
-            }
-          }
-          if (half == 0) L = lsum;
-          const float inv = 1.f / L;
-          if (write) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + 64 * half);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              uint4 v;
-              v.x = pack_bf16x2(acc[8 * q + 0] * inv, acc[8 * q + 1] * inv);
-              v.y = pack_bf16x2(acc[8 * q + 2] * inv, acc[8 * q + 3] * inv);
-              v.z = pack_bf16x2(acc[8 * q + 4] * inv, acc[8 * q + 5] * inv);
-              v.w = pack_bf16x2(acc[8 * q + 6] * inv, acc[8 * q + 7] * inv);
-              dst[q] = v;
-            }
-          }
-        }
-        if (quarter == 0 && lane == 0)
-          a.counters[((static_cast<size_t>(pc.n) * kKVHeads + pc.g) * a.tmax + pc.t) * 2 + h] = 0;
-      }
-    }
-  } else {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kPfRegsOther));  // idle warps 10-11
+
   }
 
   tc_fence_before();
