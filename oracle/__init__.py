@@ -10,7 +10,9 @@ shared object is missing, and marshals numpy / torch CPU arrays into it.
 
 Functions:
   append(...)   -- slot scatter of new K/V rows into the page pools
-  decode(...)   -- one query row per request over its paged context
+  decode(...)   -- one query row per request over its paged context (bf16 or float64 queries)
+  rope_cache / rope_f64 / rope_bf16 -- rotary position embedding (rotate-half, theta 1e6 on the
+                   pages), the step before decode attention for the new token's q and k rows
   prefill(...)  -- causal chunk attention, bottom-right aligned (row i of a
                    chunk after P cached tokens sees keys 0 .. P + i)
 
@@ -51,7 +53,7 @@ def build(force: bool = False) -> str:
     if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
         subprocess.check_call(
-            ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-o", tmp, _SRC, "-lm"]
+            ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-pthread", "-o", tmp, _SRC, "-lm"]
         )
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -68,7 +70,12 @@ def _load():
             lib.pkvo_append.argtypes = [gp, vp, vp, vp, i64, vp, vp]
             lib.pkvo_decode.argtypes = [gp, vp, vp, vp, vp, vp, i64, i64, dbl, vp, i32]
             lib.pkvo_prefill.argtypes = [gp, vp, vp, vp, vp, i64, vp, vp, i64, vp, i64, dbl, vp, i32]
-            for f in (lib.pkvo_append, lib.pkvo_decode, lib.pkvo_prefill):
+            lib.pkvo_decode_q64.argtypes = [gp, vp, vp, vp, vp, vp, i64, i64, dbl, vp, i32]
+            lib.pkvo_rope_cache.argtypes = [dbl, i32, i64, vp]
+            lib.pkvo_rope_f64.argtypes = [vp, i64, i32, i32, vp, vp, i64, vp]
+            lib.pkvo_rope_bf16.argtypes = [vp, i64, i32, i32, vp, vp, i64, vp]
+            for f in (lib.pkvo_append, lib.pkvo_decode, lib.pkvo_prefill, lib.pkvo_decode_q64, lib.pkvo_rope_cache,
+                      lib.pkvo_rope_f64, lib.pkvo_rope_bf16):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -90,7 +97,9 @@ def _bits(t) -> np.ndarray:
 
 
 def _i32(a) -> np.ndarray:
-    if not isinstance(a, np.ndarray):
+    if isinstance(a, (list, tuple)):
+        a = np.asarray(a)
+    elif not isinstance(a, np.ndarray):
         a = a.detach().cpu().numpy()
     return np.ascontiguousarray(a, dtype=np.int32)
 
@@ -142,12 +151,14 @@ def append(k_new, v_new, slot_mapping, k_pages, v_pages):
 def decode(q, k_pages, v_pages, block_table, seq_lens, scale, n_threads=None) -> np.ndarray:
     """Decode attention in fp64: out[b, h] = softmax_j(scale * <q[b,h], k_j>) . v_j over j < seq_lens[b].
 
-    q: [batch, n_q_heads, head_dim] bf16; pools [num_pages, n_kv_heads, page_size, head_dim] bf16;
+    q: [batch, n_q_heads, head_dim] bf16, or float64 (e.g. rope_f64's rotated rows);
+    pools [num_pages, n_kv_heads, page_size, head_dim] bf16;
     block_table: [batch, max_pages] int32; seq_lens: [batch] int32. Returns float64 [batch, n_q_heads, head_dim].
     Pinned by tests/test_oracle.py (dense brute force through a different layout, torch SDPA,
     closed forms, head-map and page-map invariants).
     """
-    qb = _bits(q)
+    q64 = isinstance(q, np.ndarray) and q.dtype == np.float64
+    qb = np.ascontiguousarray(q) if q64 else _bits(q)
     kp, vp = _bits(k_pages), _bits(v_pages)
     bt, sl = _i32(block_table), _i32(seq_lens)
     batch, hq, d = qb.shape
@@ -156,7 +167,7 @@ def decode(q, k_pages, v_pages, block_table, seq_lens, scale, n_threads=None) ->
         raise ValueError("shape mismatch")
     out = np.zeros((batch, hq, d), dtype=np.float64)
     g = _geom(hq, n_kv, d, ps, num_pages)
-    rc = _load().pkvo_decode(
+    rc = (_load().pkvo_decode_q64 if q64 else _load().pkvo_decode)(
         ctypes.byref(g), _ptr(qb), _ptr(kp), _ptr(vp), _ptr(bt), _ptr(sl), batch, int(bt.shape[1]),
         float(scale), _ptr(out), _threads(n_threads),
     )
@@ -195,4 +206,50 @@ def prefill(q, k_pages, v_pages, block_table, prefix_lens, cu_q_lens, scale, row
         num_seqs, None if r is None else _ptr(r), n_rows, float(scale), _ptr(out), _threads(n_threads),
     )
     _check(rc, "prefill")
+    return out
+
+
+def rope_cache(theta: float, head_dim: int, max_pos: int) -> np.ndarray:
+    """cos/sin table [max_pos, head_dim] float32 of the rotate-half rotary embedding: row p holds
+    cos(p w_i) for i < head_dim/2, then sin(p w_i), w_i = theta ** (-2 i / head_dim), evaluated in
+    double and rounded to float once. ("Fun-ASR-Nano Native Runtime Design", "Decoder And Prompt":
+    RoPE theta 1e6.) Pinned by tests/test_oracle.py (angle addition, theta from the smallest
+    frequency, row 0)."""
+    out = np.zeros((int(max_pos), int(head_dim)), dtype=np.float32)
+    _check(_load().pkvo_rope_cache(float(theta), int(head_dim), int(max_pos), _ptr(out)), "rope_cache")
+    return out
+
+
+def _rope_args(x, positions, cache):
+    xb = _bits(x)
+    if xb.ndim != 3:
+        raise ValueError("x must be [rows, heads, head_dim]")
+    pos = _i32(positions)
+    cs = np.ascontiguousarray(cache, dtype=np.float32)
+    if pos.shape[0] != xb.shape[0] or cs.ndim != 2 or cs.shape[1] != xb.shape[2]:
+        raise ValueError("shape mismatch")
+    return xb, pos, cs
+
+
+def rope_f64(x, positions, cache) -> np.ndarray:
+    """Rotate rows x [rows, heads, head_dim] (bf16) at positions [rows] (negative: unrotated) in
+    double: y1 = x1 c - x2 s, y2 = x2 c + x1 s over pairs (i, i + head_dim/2). Returns float64.
+    Pinned by tests/test_oracle.py (unit vectors, position 0, pair norms, relative positions)."""
+    xb, pos, cs = _rope_args(x, positions, cache)
+    out = np.zeros(xb.shape, dtype=np.float64)
+    rc = _load().pkvo_rope_f64(_ptr(xb), xb.shape[0], xb.shape[1], xb.shape[2], _ptr(pos), _ptr(cs),
+                               cs.shape[0], _ptr(out))
+    _check(rc, "rope_f64")
+    return out
+
+
+def rope_bf16(x, positions, cache) -> np.ndarray:
+    """The same rotation evaluated in float (products rounded, then one fused multiply-add) and
+    rounded to bf16 ties-to-even -- the form in which a rotated key row is stored. Returns uint16
+    bits. Pinned by tests/test_oracle.py (within one bf16 step of rope_f64; exact at position 0)."""
+    xb, pos, cs = _rope_args(x, positions, cache)
+    out = np.zeros(xb.shape, dtype=np.uint16)
+    rc = _load().pkvo_rope_bf16(_ptr(xb), xb.shape[0], xb.shape[1], xb.shape[2], _ptr(pos), _ptr(cs),
+                                cs.shape[0], _ptr(out))
+    _check(rc, "rope_bf16")
     return out

@@ -324,3 +324,113 @@ def test_huge_scores_do_not_overflow_or_underflow(base, peak):
     want = case.v_pages[0, bt[0, 1], 0, 6 % 4].double().numpy()
     assert np.isfinite(out).all()
     np.testing.assert_allclose(out[0, 0], want, rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------- rotary position embedding
+# RoPE with theta 1e6 ("Fun-ASR-Nano Native Runtime Design", section "Decoder And Prompt"),
+# rotate-half pairs (i, i + 64) of a 128-dim head.
+
+THETA = 1e6
+
+
+def _rope_ref_pair(x1, x2, ang):
+    return x1 * math.cos(ang) - x2 * math.sin(ang), x2 * math.cos(ang) + x1 * math.sin(ang)
+
+
+def test_rope_cache_row0_and_angle_addition():
+    cs = oracle.rope_cache(THETA, 128, 64).astype(np.float64)
+    assert np.array_equal(cs[0, :64], np.ones(64)) and np.array_equal(cs[0, 64:], np.zeros(64))
+    # angles grow linearly with the position: cos((p+1)w) = cos(pw)cos(w) - sin(pw)sin(w), and the
+    # same for sin, for every frequency (float rounding of the table only)
+    c, s = cs[:, :64], cs[:, 64:]
+    c1, s1 = c[1], s[1]
+    assert np.abs(c[1:] - (c[:-1] * c1 - s[:-1] * s1)).max() < 3e-7 * 64
+    assert np.abs(s[1:] - (s[:-1] * c1 + c[:-1] * s1)).max() < 3e-7 * 64
+    assert np.abs(c ** 2 + s ** 2 - 1).max() < 2e-7
+
+
+def test_rope_cache_frequencies_follow_theta():
+    cs = oracle.rope_cache(THETA, 128, 2).astype(np.float64)
+    w = np.arcsin(np.clip(cs[1, 64:], -1, 1))  # sin(w_i) at position 1; w_0 = 1 < pi/2
+    assert abs(w[0] - 1.0) < 1e-7  # w_0 = theta^0
+    # w_i = theta^(-2i/128): log-linear in i with slope -2 ln(theta) / 128
+    slope = np.polyfit(np.arange(1, 64), np.log(w[1:]), 1)[0]
+    assert abs(slope - (-2 * math.log(THETA) / 128)) < 1e-6
+    assert abs(w[63] / THETA ** (-126 / 128) - 1) < 1e-5
+
+
+def test_rope_unit_vectors_pin_pairing_and_direction():
+    cs = oracle.rope_cache(THETA, 128, 8)
+    x = np.zeros((4, 1, 128), dtype=np.float32)
+    x[0, 0, 0] = 1.0   # e_0 at position 5 -> cos(5) e_0 + sin(5) e_64
+    x[1, 0, 64] = 1.0  # e_64 at position 5 -> -sin(5) e_0 + cos(5) e_64
+    x[2, 0, 1] = 1.0   # e_1 pairs with e_65, frequency w_1
+    x[3, 0, 7] = 1.0   # position -1: unrotated
+    xb = torch.from_numpy(x).to(torch.bfloat16)
+    y = oracle.rope_f64(xb, [5, 5, 3, -1], cs)
+    c5, s5 = float(cs[5, 0]), float(cs[5, 64])
+    assert abs(c5 - math.cos(5)) < 1e-7 and abs(s5 - math.sin(5)) < 1e-7
+    want = np.zeros((4, 1, 128))
+    want[0, 0, 0], want[0, 0, 64] = c5, s5
+    want[1, 0, 0], want[1, 0, 64] = -s5, c5
+    want[2, 0, 1], want[2, 0, 65] = float(cs[3, 1]), float(cs[3, 65])
+    want[3, 0, 7] = 1.0
+    assert np.array_equal(y, want)
+    w1 = THETA ** (-2 / 128)
+    assert abs(float(cs[3, 1]) - math.cos(3 * w1)) < 1e-7 and abs(float(cs[3, 65]) - math.sin(3 * w1)) < 1e-7
+
+
+def test_rope_position0_identity_and_pair_norms():
+    cs = oracle.rope_cache(THETA, 128, 50000)
+    g = torch.Generator().manual_seed(7)
+    x = torch.randn(6, 4, 128, generator=g).to(torch.bfloat16)
+    pos = [0, 1, 17, 4095, 40000, 49999]
+    y = oracle.rope_f64(x, pos, cs)
+    xf = x.to(torch.float64).numpy()
+    assert np.array_equal(y[0], xf[0])
+    n_in = xf[..., :64] ** 2 + xf[..., 64:] ** 2
+    n_out = y[..., :64] ** 2 + y[..., 64:] ** 2
+    assert np.abs(n_out - n_in).max() <= 1e-6 * n_in.max()
+    # bf16 form: position 0 returns the input bits
+    assert np.array_equal(oracle.rope_bf16(x, [0] * 6, cs), x.view(torch.int16).numpy().view(np.uint16))
+
+
+def test_rope_scores_depend_on_relative_position_only():
+    # <R(m) q, R(n) k> = <R(m - n) q, k>: with a table built here in double from the definition,
+    # the oracle's rotation reproduces it to float-table rounding
+    d = 128
+    w = THETA ** (-2 * np.arange(64) / d)
+    pos_max = 3000
+    ang = np.arange(pos_max)[:, None] * w[None, :]
+    cs = np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32)
+    g = torch.Generator().manual_seed(8)
+    q = torch.randn(1, 1, d, generator=g).to(torch.bfloat16)
+    k = torch.randn(1, 1, d, generator=g).to(torch.bfloat16)
+    for m, n in [(2900, 2000), (1234, 5), (77, 77)]:
+        lhs = float(np.dot(oracle.rope_f64(q, [m], cs).ravel(), oracle.rope_f64(k, [n], cs).ravel()))
+        rhs = float(np.dot(oracle.rope_f64(q, [m - n], cs).ravel(), k.to(torch.float64).numpy().ravel()))
+        assert abs(lhs - rhs) < 1e-4 * (1 + abs(rhs)), (m, n, lhs, rhs)
+
+
+def test_rope_bf16_is_a_neighbour_of_the_exact_rotation():
+    cs = oracle.rope_cache(THETA, 128, 41000)
+    g = torch.Generator().manual_seed(9)
+    x = (torch.randn(64, 8, 128, generator=g) * 3).to(torch.bfloat16)
+    pos = np.random.default_rng(9).integers(0, 41000, 64).astype(np.int32)
+    exact = oracle.rope_f64(x, pos, cs)
+    got = torch.from_numpy(oracle.rope_bf16(x, pos, cs).view(np.int16)).view(torch.bfloat16).double().numpy()
+    # bf16 keeps 8 significant bits: |got - exact| within one step of the bf16 grid at exact's magnitude
+    step = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(exact), 1e-30))) - 7)
+    assert (np.abs(got - exact) <= step * 1.0001).all()
+    # and mostly the nearest value
+    nearest = torch.from_numpy(exact).to(torch.bfloat16).double().numpy()
+    assert (got == nearest).mean() > 0.99
+
+
+def test_decode_with_float64_queries_matches_bf16_queries():
+    case = W.decode_case(11, [37, 200], pending_append=False, poison=False)
+    q = case.q[0]
+    a = oracle.decode(q, case.k_pages[0], case.v_pages[0], case.block_table, case.seq_lens, case.geom.scale)
+    b = oracle.decode(q.to(torch.float64).numpy(), case.k_pages[0], case.v_pages[0], case.block_table,
+                      case.seq_lens, case.geom.scale)
+    assert np.isfinite(a).all() and np.array_equal(a, b)
