@@ -129,7 +129,8 @@ class ClockSampler:
 class DecodeStep:
     """Device-resident 28-layer decode step (all layers share one block table)."""
 
-    def __init__(self, device, seq_lens, layers: int, seed: int, fused: bool = True, early: bool = True):
+    def __init__(self, device, seq_lens, layers: int, seed: int, fused: bool = True, early: bool = True,
+                 rope: bool = False):
         import torch
 
         import paged_kv_decode_gb300 as pkv
@@ -153,6 +154,8 @@ class DecodeStep:
         self.graph = None
         self.fused = fused
         self.early = early and fused  # each layer's predecessor writes only other layers' pools
+        # rotary embedding of the new token fused in (theta 1e6: "Fun-ASR-Nano Native Runtime Design")
+        self.cos_sin = pkv.rope_cos_sin(1e6, int(np.max(seq_lens)) + 1, device=device) if (rope and fused) else None
     # algorithmic bytes of one decode launch (one layer)
     def decode_bytes(self) -> int:
         c = self.case
@@ -168,6 +171,11 @@ class DecodeStep:
 
     def layer(self, l):
         pkv = self.pkv
+        if self.fused and self.cos_sin is not None:
+            pkv.decode_append_rope_attn(self.q[l], self.k_new[l], self.v_new[l], self.k_pages[l], self.v_pages[l],
+                                        self.block_table, self.seq_lens, self.cos_sin, self.out[l], self.scale,
+                                        self.ws, early_prefetch=self.early)
+            return
         if self.fused:
             pkv.decode_append_attn(self.q[l], self.k_new[l], self.v_new[l], self.k_pages[l], self.v_pages[l],
                                    self.block_table, self.seq_lens, self.out[l], self.scale, self.ws,
@@ -540,12 +548,13 @@ def main():
 
     extra = {}
     if not args.no_extra:
-        variants = [("separate_append_and_decode", False, False), ("fused_no_early_prefetch", True, False),
-                    ("fused_early_prefetch", True, True)]
-        for name, fused, early in variants:
-            if fused == step.fused and early == step.early:
+        variants = [("separate_append_and_decode", False, False, False), ("fused_no_early_prefetch", True, False, False),
+                    ("fused_early_prefetch", True, True, False), ("fused_rope_early_prefetch", True, True, True)]
+        for name, fused, early, rope in variants:
+            if fused == step.fused and early == step.early and not rope:
                 continue
-            other = DecodeStep(device, W.config_seq_lens(2), args.layers, seed=2 + rank, fused=fused, early=early)
+            other = DecodeStep(device, W.config_seq_lens(2), args.layers, seed=2 + rank, fused=fused, early=early,
+                               rope=rope)
             other.capture()
             n_o = max(50, args.steps // 4)
             ot = time_graph(other, n_o, args.warmup, dist_on) / n_o

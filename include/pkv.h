@@ -209,10 +209,47 @@ int pkv_decode_append_attn(const void* q, const void* k_new, const void* v_new, 
 #define PKV_DECODE_EARLY_PREFETCH 1u
 
 /*
+ * pkv_decode_append_rope_attn -- pkv_decode_append_attn with the rotary
+ * position embedding of the new token applied on the way: one launch for the
+ * step that precedes decode attention in a RoPE decoder and the attention.
+ *
+ * Source: the decoder is a Qwen3-style causal LM with RoPE theta 1e6
+ * ("Fun-ASR-Nano Native Runtime Design", section "Decoder And Prompt"). The
+ * pages name RoPE and theta only; the rotate-half form of Qwen3 decoders is
+ * taken: dims i and i + head_dim/2 form a pair rotated by the angle of
+ * (position, i).
+ *
+ * For every request b with seq_lens[b] > 0, at position p = seq_lens[b] - 1,
+ * with c = rope_cos_sin[p][i] and s = rope_cos_sin[p][head_dim/2 + i]:
+ *  - the key row written is k_new[b][g] rotated and rounded to bf16 (ties to
+ *    even), each pair (x1, x2) = (k[i], k[i + head_dim/2]) evaluated in fp32
+ *    as y1 = fmaf(x1, c, -(x2 * s)), y2 = fmaf(x2, c, x1 * s), each product
+ *    rounded to fp32 first (so the written bits are defined exactly);
+ *  - every query row q[b][h] is rotated the same way in fp32 (and kept in
+ *    fp32) before the scores;
+ *  - v_new is written unchanged; everything else is as pkv_decode_append_attn.
+ *
+ *  rope_cos_sin: fp32 [rope_max_pos][head_dim], row p = cos(p w_i) for
+ *                i < head_dim/2, then sin(p w_i) (w_i = theta^(-2i/head_dim));
+ *                caller-owned device memory, 16-byte aligned, read only.
+ *                A position >= rope_max_pos is reported as
+ *                PKV_ERR_OUT_OF_BOUNDS in the status word and clamped to the
+ *                last row.
+ *  rope_max_pos: rows of the table (>= 1)
+ *  other arguments, flags and the workspace: as for pkv_decode_append_attn
+ */
+int pkv_decode_append_rope_attn(const void* q, const void* k_new, const void* v_new, void* k_pages, void* v_pages,
+                                const int32_t* block_table, const int32_t* seq_lens, const float* rope_cos_sin,
+                                int32_t rope_max_pos, void* out, float scale, pkv_stream_t stream,
+                                const pkv_cache_desc* desc, int32_t batch, int32_t max_pages_per_seq, void* workspace,
+                                size_t workspace_bytes, uint32_t flags);
+
+/*
  * Workspace bytes pkv_prefill_chunk_attn needs: the status header, split
  * counters (num_seqs x 8 KV heads x ceil(max_q_len / 128) x 2 ints) and two
- * fp32 partial records (2 heads x 130 x 128 floats) per SM of the current
- * device, for query tiles whose key range is split between CTAs.
+ * partial records per SM of the current device (for each of the 2 query heads
+ * of a KV head: 128 rows x 128 dims of fp16 O / l, then fp32 max and sum per
+ * row: 67,584 bytes), for query tiles whose key range is cut between CTAs.
  */
 size_t pkv_prefill_workspace_bytes(const pkv_cache_desc* desc, int32_t num_seqs, int32_t max_q_len);
 

@@ -177,6 +177,35 @@ def decode_attn(q, k_pages, v_pages, block_table, seq_lens, out, scale: float, w
 EARLY_PREFETCH = 1  # PKV_DECODE_EARLY_PREFETCH
 
 
+def rope_cos_sin(theta: float, max_pos: int, head_dim: int = 128, device=None):
+    """cos/sin table for decode_append_rope_attn: fp32 [max_pos, head_dim], row p = cos(p w_i) for
+    i < head_dim/2, then sin(p w_i), w_i = theta ** (-2 i / head_dim); angles in float64, rounded
+    to float32 once. (RoPE theta 1e6 for the decoder on "Fun-ASR-Nano Native Runtime Design",
+    "Decoder And Prompt".)"""
+    import torch
+
+    half = head_dim // 2
+    w = torch.pow(torch.tensor(float(theta), dtype=torch.float64),
+                  -2.0 * torch.arange(half, dtype=torch.float64) / head_dim)
+    ang = torch.arange(int(max_pos), dtype=torch.float64)[:, None] * w[None, :]
+    table = torch.cat([torch.cos(ang), torch.sin(ang)], dim=1).to(torch.float32)
+    return table.to(device) if device is not None else table
+
+
+def decode_append_rope_attn(q, k_new, v_new, k_pages, v_pages, block_table, seq_lens, cos_sin, out, scale: float,
+                            workspace: Workspace, stream=None, early_prefetch: bool = False):
+    """decode_append_attn with the rotary embedding of the new token: k_new and every q row are
+    rotated at position seq_lens[b] - 1 (pairs i, i + 64; cos_sin from rope_cos_sin) before the
+    append and the scores."""
+    import torch
+
+    _need(cos_sin, torch.float32, "cos_sin", k_pages.device)
+    if cos_sin.dim() != 2 or cos_sin.shape[1] != q.shape[-1]:
+        raise ValueError("cos_sin must be [max_pos, head_dim]")
+    _decode_append(q, k_new, v_new, k_pages, v_pages, block_table, seq_lens, out, scale, workspace, stream,
+                   early_prefetch, cos_sin)
+
+
 def decode_append_attn(q, k_new, v_new, k_pages, v_pages, block_table, seq_lens, out, scale: float,
                        workspace: Workspace, stream=None, early_prefetch: bool = False):
     """One decode step of one layer in one launch: write k_new / v_new [B, 8, 128] at position
@@ -184,6 +213,12 @@ def decode_append_attn(q, k_new, v_new, k_pages, v_pages, block_table, seq_lens,
 
     early_prefetch: the previous kernel on the stream writes neither the pools nor the block
     table nor the lengths, so they may be read while it finishes (PKV_DECODE_EARLY_PREFETCH)."""
+    _decode_append(q, k_new, v_new, k_pages, v_pages, block_table, seq_lens, out, scale, workspace, stream,
+                   early_prefetch, None)
+
+
+def _decode_append(q, k_new, v_new, k_pages, v_pages, block_table, seq_lens, out, scale, workspace, stream,
+                   early_prefetch, cos_sin):
     import torch
 
     _need(k_pages, torch.bfloat16, "k_pages")
@@ -201,11 +236,19 @@ def decode_append_attn(q, k_new, v_new, k_pages, v_pages, block_table, seq_lens,
         raise ValueError("shape mismatch")
     d = _desc_of(k_pages)
     ws = workspace.tensor
-    rc = _lib.load().pkv_decode_append_attn(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_pages), _ptr(v_pages),
-                                            _ptr(block_table), _ptr(seq_lens), _ptr(out), float(scale),
-                                            _stream(stream), ctypes.byref(d), B, block_table.shape[1], _ptr(ws),
-                                            ws.numel(), EARLY_PREFETCH if early_prefetch else 0)
-    _check(rc, "pkv_decode_append_attn")
+    flags = EARLY_PREFETCH if early_prefetch else 0
+    lib = _lib.load()
+    if cos_sin is None:
+        rc = lib.pkv_decode_append_attn(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_pages), _ptr(v_pages),
+                                        _ptr(block_table), _ptr(seq_lens), _ptr(out), float(scale), _stream(stream),
+                                        ctypes.byref(d), B, block_table.shape[1], _ptr(ws), ws.numel(), flags)
+        _check(rc, "pkv_decode_append_attn")
+    else:
+        rc = lib.pkv_decode_append_rope_attn(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_pages), _ptr(v_pages),
+                                             _ptr(block_table), _ptr(seq_lens), _ptr(cos_sin), cos_sin.shape[0],
+                                             _ptr(out), float(scale), _stream(stream), ctypes.byref(d), B,
+                                             block_table.shape[1], _ptr(ws), ws.numel(), flags)
+        _check(rc, "pkv_decode_append_rope_attn")
 
 
 def prefill_chunk_attn(q, k_pages, v_pages, block_table, prefix_lens, cu_q_lens, out, scale: float, max_q_len: int,

@@ -27,7 +27,11 @@
 //    unused slots may hold anything, NaN included.
 //  * Optional fused append: the producer lane that copies a request's last
 //    page first writes the request's new K/V row for that head into it
-//    (generic stores, then a proxy fence so its own bulk copy sees them).
+//    (generic stores, then a proxy fence so its own bulk copy sees them). With
+//    a cos/sin table the whole producer warp writes the row instead, rotating
+//    the key (rotary position embedding at the new token's position, pairs
+//    (i, i + 64), fp32, rounded to bf16), and each piece's query rows are
+//    rotated the same way after they are staged.
 //  * The query rows of the next piece are copied into shared memory (cp.async)
 //    while the current piece streams, so a piece boundary costs no round trip.
 //  * At the end of a piece the warps merge through shared memory. A piece that
@@ -77,13 +81,16 @@ constexpr int kMergeFloats = kCons * kPieceFloats;         // one record per con
 constexpr int kSmemMerge = kMergeFloats * 4;
 constexpr int kQBufBytes = kGroup * kRowBytes;             // query rows of one (request, KV head), both heads
 constexpr int kSmemQ = 2 * kQBufBytes;                     // this piece's rows and the next piece's
+constexpr int kCsBytes = kHeadDim * 4;                     // one cos/sin table row (fp32 cos[64], sin[64])
+constexpr int kSmemCs = 2 * kCsBytes;                      // rows for this piece's and the next piece's position
 constexpr int kSmemPbuf = kCons * kPageSize * 4 * 4;       // per warp: [16 tokens][p0, p0, p1, p1]
 constexpr int kSmemMisc = 16;                              // flag words
-constexpr int kSmemFixed = kSmemRing + kSmemBars + kSmemMerge + kSmemQ + kSmemPbuf + kSmemMisc;
+constexpr int kSmemFixed = kSmemRing + kSmemBars + kSmemMerge + kSmemQ + kSmemCs + kSmemPbuf + kSmemMisc;
 constexpr int kPieceBytes = kPieceFloats * 4;
 constexpr int kMergeCap = kSmemRing / kPieceBytes;         // partial records staged per batch of the final merge
 static_assert((kSmemRing + kSmemBars) % 16 == 0 && kSmemMerge % 16 == 0 && kPieceBytes % 16 == 0, "alignment");
 static_assert(kQBufBytes == 32 * 16, "one 16-byte chunk of a group's query rows per lane");
+static_assert(kCsBytes == 32 * 16, "one 16-byte chunk of a cos/sin row per lane");
 
 static size_t decode_smem_bytes(int batch) { return kSmemFixed + static_cast<size_t>(2 * batch + 1) * 4; }
 
@@ -98,7 +105,9 @@ struct DecodeArgs {
   const int* block_table;
   const int* seq_lens;
   __nv_bfloat16* out;
-  float qscale;  // scale * log2(e)
+  const float* rope;  // optional cos/sin table [rope_max_pos][128] fp32 (rotary embedding), nullptr = none
+  int rope_max_pos;
+  float qscale;       // scale * log2(e)
   int early;     // prefetch before the grid dependency (caller guarantees the predecessor leaves
                  // pools, block table and lengths alone)
   int batch;
@@ -182,6 +191,10 @@ __device__ __forceinline__ int request_of(long long f, const int* pref, int batc
   return lo_b;
 }
 
+// kFused: a.k_new / a.v_new are given (fused append); kRope: a.rope is given too.
+// Each combination is its own instantiation, so a path carries no code (and no
+// registers) for the others.
+template <bool kFused, bool kRope>
 __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(const DecodeArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* ring = smem;
@@ -189,7 +202,8 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
   uint64_t* empty = full + kStages;
   float* merge = reinterpret_cast<float*>(smem + kSmemRing + kSmemBars);
   unsigned char* qbuf = reinterpret_cast<unsigned char*>(merge + kMergeFloats);
-  float* pbuf = reinterpret_cast<float*>(qbuf + kSmemQ);
+  unsigned char* csbuf = qbuf + kSmemQ;
+  float* pbuf = reinterpret_cast<float*>(csbuf + kSmemCs);
   int* flag = reinterpret_cast<int*>(pbuf + kCons * kPageSize * 4);  // [0..1] merge flags, [2] a wait failed
   int* pref = flag + kSmemMisc / 4;
   int* sl = pref + a.batch + 1;
@@ -304,7 +318,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
         c = static_cast<int>((f - (seg > lo ? seg : lo)) % kCons);
         bb = b;
         id = __ldg(a.block_table + static_cast<size_t>(b) * a.max_pages + p);
-        if (a.k_new != nullptr && p == np - 1) wslot = (sl[b] - 1) % kPageSize;  // the new token's slot
+        if (kFused && p == np - 1) wslot = (sl[b] - 1) % kPageSize;  // the new token's slot
       }
       const unsigned same = __match_any_sync(kFull, valid ? c : -1);
       const int idx = __popc(same & lt_mask);  // earlier lanes of this chunk feeding the same consumer
@@ -321,10 +335,49 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
       int rounds = valid ? my_round + 1 : 0;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) rounds = max(rounds, __shfl_xor_sync(kFull, rounds, o));
-      if (!waited && __any_sync(kFull, wslot >= 0)) {  // new rows come from the predecessor
+      if (kFused && !waited && __any_sync(kFull, wslot >= 0)) {  // new rows come from the predecessor
         grid_dependency_wait();
         allow_dependents();
         waited = true;
+      }
+      if (kRope) {
+        // Fused append with the rotary embedding, by the whole warp: every page of this
+        // chunk that holds its request's new token gets the token's rotated K row and its V
+        // row for that head before any lane copies a page. Lanes take key pairs (i, i + 64),
+        // i = lane and lane + 32, rotated in fp32 as y1 = fma(x1, c, -(x2 s)),
+        // y2 = fma(x2, c, x1 s) with each product rounded first, then rounded to bf16.
+        unsigned amask = __ballot_sync(kFull, valid && wslot >= 0 && id >= 0 && id < a.num_pages);
+        if (amask != 0u) {
+          while (amask != 0u) {
+            const int src = __ffs(amask) - 1;
+            amask &= amask - 1u;
+            const int rb = __shfl_sync(kFull, bb, src), rh = __shfl_sync(kFull, hh, src);
+            const int rpid = __shfl_sync(kFull, id, src), rslot = __shfl_sync(kFull, wslot, src);
+            const size_t row = ((static_cast<size_t>(rpid) * kKVHeads + rh) * kPageSize + rslot) * kHeadDim;
+            const size_t srow = (static_cast<size_t>(rb) * kKVHeads + rh) * kHeadDim;
+            __nv_bfloat16* kd = const_cast<__nv_bfloat16*>(a.k_pages) + row;
+            int pos = sl[rb] - 1;
+            if (pos >= a.rope_max_pos) {  // past the table: reported, clamped to its last row
+              if (lane == 0) set_status(a.status, PKV_ERR_OUT_OF_BOUNDS);
+              pos = a.rope_max_pos - 1;
+            }
+            const float* cs = a.rope + static_cast<size_t>(pos) * kHeadDim;
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              const int i = lane + 32 * t;
+              const float x1 = __bfloat162float(a.k_new[srow + i]);
+              const float x2 = __bfloat162float(a.k_new[srow + i + kHeadDim / 2]);
+              const float cc = __ldg(cs + i), sn = __ldg(cs + kHeadDim / 2 + i);
+              kd[i] = __float2bfloat16_rn(__fmaf_rn(x1, cc, -__fmul_rn(x2, sn)));
+              kd[i + kHeadDim / 2] = __float2bfloat16_rn(__fmaf_rn(x2, cc, __fmul_rn(x1, sn)));
+            }
+            if (lane < kRowBytes / 16)
+              reinterpret_cast<uint4*>(const_cast<__nv_bfloat16*>(a.v_pages) + row)[lane] =
+                  __ldg(reinterpret_cast<const uint4*>(a.v_new + srow) + lane);
+          }
+          fence_proxy_async_global();  // this lane's row stores before the warp's bulk copies
+          __syncwarp();
+        }
       }
       for (int r = 0; r < rounds; ++r) {
         if (valid && my_round == r && !pfail) {
@@ -335,7 +388,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
             const bool id_ok = id >= 0 && id < a.num_pages;
             if (!id_ok) set_status(a.status, PKV_ERR_OUT_OF_BOUNDS);
             const int pid = id_ok ? id : 0;
-            if (wslot >= 0 && id_ok) {
+            if (kFused && !kRope && wslot >= 0 && id_ok) {
               // fused append: this page holds the request's new token; write its K and V rows
               // for this head, then order the writes before this lane's bulk copy of the page
               const uint4* ks = reinterpret_cast<const uint4*>(a.k_new + (static_cast<size_t>(bb) * kKVHeads + hh) * kHeadDim);
@@ -387,13 +440,20 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
   bool failed = false;
 
   // Warp 0 stages the query rows of a piece in qbuf[buf], one 16-byte chunk per
-  // lane, so that the next piece's rows are on chip before the current one ends.
+  // lane, so that the next piece's rows are on chip before the current one ends;
+  // with a cos/sin table, also the table row of the request's new position.
   const uint32_t qb = smem_u32(qbuf);
+  const uint32_t csb = smem_u32(csbuf);
   auto stage_q = [&](const Piece& p, int buf) {
     if (warp == 0) {
       const unsigned char* src =
           reinterpret_cast<const unsigned char*>(a.q + (static_cast<size_t>(p.b) * kQHeads + p.h * kGroup) * kHeadDim);
       cp_async16(qb + buf * kQBufBytes + lane * 16, src + lane * 16);
+      if (kRope) {
+        const int pos = min(sl[p.b] - 1, a.rope_max_pos - 1);  // a piece's request has sl >= 1
+        const unsigned char* cs = reinterpret_cast<const unsigned char*>(a.rope + static_cast<size_t>(pos) * kHeadDim);
+        cp_async16(csb + buf * kCsBytes + lane * 16, cs + lane * 16);
+      }
     }
   };
   // CTAs cfirst .. cfirst + n - 1 hold the pieces of (request b, KV head h); the
@@ -430,19 +490,59 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
     bool sp_two = false;
     if (!complete) span_of(b, h, sp_cfirst, sp_n, sp_two);  // before the stream, off the critical path
 
-    // query rows of both heads of the group, in this lane's chunk order, pre-scaled
+    // query rows of both heads of the group, in this lane's chunk order, rotated
+    // (with a cos/sin table) and pre-scaled. The lane's chunks jj and jj + 2
+    // (jj < 2) are chunks c and c + 8 of the row: dims 8c .. 8c+7 pair with dims + 64.
     const uint32_t qcur = qb + (j & 1) * kQBufBytes;
+    const uint32_t ccur = csb + (j & 1) * kCsBytes;
     float2 q2[4][4][2];
+    if constexpr (!kRope) {
 #pragma unroll
-    for (int i = 0; i < kGroup; ++i) {
+      for (int i = 0; i < kGroup; ++i) {
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        const uint4 u = lds128(qcur + i * kRowBytes + (qq + 4 * (jj ^ tp)) * 16);
+        for (int jj = 0; jj < 4; ++jj) {
+          const uint4 u = lds128(qcur + i * kRowBytes + (qq + 4 * (jj ^ tp)) * 16);
+          const float2 sc = make_float2(a.qscale, a.qscale);
+          q2[jj][0][i] = __fmul2_rn(bf2_to_f2(u.x), sc);
+          q2[jj][1][i] = __fmul2_rn(bf2_to_f2(u.y), sc);
+          q2[jj][2][i] = __fmul2_rn(bf2_to_f2(u.z), sc);
+          q2[jj][3][i] = __fmul2_rn(bf2_to_f2(u.w), sc);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < kGroup; ++i) {
+        float2 x[4][4];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const uint4 u = lds128(qcur + i * kRowBytes + (qq + 4 * (jj ^ tp)) * 16);
+          x[jj][0] = bf2_to_f2(u.x);
+          x[jj][1] = bf2_to_f2(u.y);
+          x[jj][2] = bf2_to_f2(u.z);
+          x[jj][3] = bf2_to_f2(u.w);
+        }
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {  // chunk jj (index c < 8) pairs with chunk jj + 2 (index c + 8)
+          const int c = qq + 4 * (jj ^ tp);
+          const float4 c0 = lds128f(ccur + c * 32), c1 = lds128f(ccur + c * 32 + 16);
+          const float4 s0 = lds128f(ccur + kCsBytes / 2 + c * 32), s1 = lds128f(ccur + kCsBytes / 2 + c * 32 + 16);
+          const float2 cs[4] = {make_float2(c0.x, c0.y), make_float2(c0.z, c0.w), make_float2(c1.x, c1.y),
+                                make_float2(c1.z, c1.w)};
+          const float2 sn[4] = {make_float2(s0.x, s0.y), make_float2(s0.z, s0.w), make_float2(s1.x, s1.y),
+                                make_float2(s1.z, s1.w)};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 lo = x[jj][e], hi = x[jj + 2][e];
+            const float2 t1 = __fmul2_rn(hi, sn[e]), t2 = __fmul2_rn(lo, sn[e]);
+            x[jj][e] = __ffma2_rn(lo, cs[e], make_float2(-t1.x, -t1.y));
+            x[jj + 2][e] = __ffma2_rn(hi, cs[e], t2);
+          }
+        }
         const float2 sc = make_float2(a.qscale, a.qscale);
-        q2[jj][0][i] = __fmul2_rn(bf2_to_f2(u.x), sc);
-        q2[jj][1][i] = __fmul2_rn(bf2_to_f2(u.y), sc);
-        q2[jj][2][i] = __fmul2_rn(bf2_to_f2(u.z), sc);
-        q2[jj][3][i] = __fmul2_rn(bf2_to_f2(u.w), sc);
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) q2[jj][e][i] = __fmul2_rn(x[jj][e], sc);
       }
     }
 
@@ -470,7 +570,6 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
         const int n_valid = rem < kPageSize ? rem : kPageSize;
         const uint32_t kt = smem_u32(ring + slot * kStageBytes);
         const uint32_t vt = kt + kTileBytes;
-
         // ---- scores: lanes (token group of 4) x (quarter of the row), two passes of 8 tokens
         float2 acc[2][2];
 #pragma unroll
@@ -791,22 +890,27 @@ size_t decode_workspace_bytes(int32_t batch, int num_sms) {
 }
 
 int launch_decode(const void* q, const void* k_new, const void* v_new, const void* k_pages, const void* v_pages,
-                  const int32_t* block_table, const int32_t* seq_lens, void* out, float scale, int32_t batch,
-                  int32_t max_pages, int32_t num_pages, void* workspace, int num_sms, cudaStream_t stream,
-                  uint32_t flags) {
+                  const int32_t* block_table, const int32_t* seq_lens, const float* rope, int32_t rope_max_pos,
+                  void* out, float scale, int32_t batch, int32_t max_pages, int32_t num_pages, void* workspace,
+                  int num_sms, cudaStream_t stream, uint32_t flags) {
   if (batch == 0) return PKV_OK;
+  if (rope != nullptr && k_new == nullptr) return PKV_ERR_NULL_ARG;
   const size_t smem = decode_smem_bytes(batch);
-  static bool attr_set[64] = {false};
+  void (*kern)(const DecodeArgs) = k_new == nullptr ? decode_kernel<false, false>
+                                   : rope == nullptr ? decode_kernel<true, false>
+                                                     : decode_kernel<true, true>;
+  const int variant = k_new == nullptr ? 0 : rope == nullptr ? 1 : 2;
+  static bool attr_set[64][3] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
-  if (dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (dev < 64 && !attr_set[dev][variant]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(decode_smem_bytes(kMaxDecodeBatch))) != cudaSuccess)
       return PKV_ERR_CUDA;
-    attr_set[dev] = true;
+    attr_set[dev][variant] = true;
   }
   int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_kernel, kDecThreads, smem) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kDecThreads, smem) != cudaSuccess)
     return PKV_ERR_CUDA;
   if (occ < 1) return PKV_ERR_UNSUPPORTED;
   if (occ > kDecCtasPerSm) occ = kDecCtasPerSm;
@@ -821,6 +925,8 @@ int launch_decode(const void* q, const void* k_new, const void* v_new, const voi
   a.block_table = block_table;
   a.seq_lens = seq_lens;
   a.out = static_cast<__nv_bfloat16*>(out);
+  a.rope = rope;
+  a.rope_max_pos = rope_max_pos;
   a.qscale = scale * kLog2e;
   a.early = (flags & PKV_DECODE_EARLY_PREFETCH) ? 1 : 0;
   a.batch = batch;
@@ -831,8 +937,7 @@ int launch_decode(const void* q, const void* k_new, const void* v_new, const voi
   a.partials = reinterpret_cast<float*>(ws + PKV_STATUS_BYTES +
                                         (static_cast<size_t>(batch) * kKVHeads * 4 + 255) / 256 * 256);
   const int grid = num_sms * occ < kMaxGrid ? num_sms * occ : kMaxGrid;
-  return launch_pdl(decode_kernel, dim3(grid), dim3(kDecThreads), smem, stream, a) == cudaSuccess ? PKV_OK
-                                                                                                 : PKV_ERR_CUDA;
+  return launch_pdl(kern, dim3(grid), dim3(kDecThreads), smem, stream, a) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 }  // namespace pkv

@@ -90,6 +90,6 @@ extern "C" int pkv_decode_attn_noalloc(const void* q, const void* k_pages, const
   // stopped early (a timed-out wait) could have left them set.
   const size_t zero_bytes = PKV_STATUS_BYTES + static_cast<size_t>(batch) * desc->num_kv_heads * sizeof(int32_t);
   if (cudaMemsetAsync(scratch, 0, zero_bytes, s) != cudaSuccess) return PKV_ERR_CUDA;
-  return pkv::launch_decode(q, nullptr, nullptr, k_pages, v_pages, block_table, seq_lens, out, scale, batch,
+  return pkv::launch_decode(q, nullptr, nullptr, k_pages, v_pages, block_table, seq_lens, nullptr, 0, out, scale, batch,
                             max_pages_per_seq, desc->num_pages, scratch, sms, s, 0u);
 }

@@ -141,15 +141,16 @@ int pkv_decode_attn(const void* q, const void* k_pages, const void* v_pages, con
   rc = current_device(&sms);
   if (rc != PKV_OK) return rc;
   if (workspace_bytes < pkv::decode_workspace_bytes(batch, sms)) return PKV_ERR_WORKSPACE_TOO_SMALL;
-  return pkv::launch_decode(q, nullptr, nullptr, k_pages, v_pages, block_table, seq_lens, out, scale, batch,
+  return pkv::launch_decode(q, nullptr, nullptr, k_pages, v_pages, block_table, seq_lens, nullptr, 0, out, scale, batch,
                             max_pages_per_seq, desc->num_pages, workspace, sms, reinterpret_cast<cudaStream_t>(stream),
                             0u);
 }
 
-int pkv_decode_append_attn(const void* q, const void* k_new, const void* v_new, void* k_pages, void* v_pages,
-                           const int32_t* block_table, const int32_t* seq_lens, void* out, float scale,
-                           pkv_stream_t stream, const pkv_cache_desc* desc, int32_t batch, int32_t max_pages_per_seq,
-                           void* workspace, size_t workspace_bytes, uint32_t flags) {
+static int decode_append(const void* q, const void* k_new, const void* v_new, void* k_pages, void* v_pages,
+                         const int32_t* block_table, const int32_t* seq_lens, const float* rope_cos_sin,
+                         int32_t rope_max_pos, void* out, float scale, pkv_stream_t stream, const pkv_cache_desc* desc,
+                         int32_t batch, int32_t max_pages_per_seq, void* workspace, size_t workspace_bytes,
+                         uint32_t flags) {
   int rc = check_desc(desc);
   if (rc != PKV_OK) return rc;
   if (batch < 0 || max_pages_per_seq < 1) return PKV_ERR_BAD_SHAPE;
@@ -166,9 +167,29 @@ int pkv_decode_append_attn(const void* q, const void* k_new, const void* v_new, 
   if (rc != PKV_OK) return rc;
   if (workspace_bytes < pkv::decode_workspace_bytes(batch, sms)) return PKV_ERR_WORKSPACE_TOO_SMALL;
   if ((flags & ~static_cast<uint32_t>(PKV_DECODE_EARLY_PREFETCH)) != 0) return PKV_ERR_UNSUPPORTED;
-  return pkv::launch_decode(q, k_new, v_new, k_pages, v_pages, block_table, seq_lens, out, scale, batch,
-                            max_pages_per_seq, desc->num_pages, workspace, sms, reinterpret_cast<cudaStream_t>(stream),
-                            flags);
+  return pkv::launch_decode(q, k_new, v_new, k_pages, v_pages, block_table, seq_lens, rope_cos_sin, rope_max_pos, out,
+                            scale, batch, max_pages_per_seq, desc->num_pages, workspace, sms,
+                            reinterpret_cast<cudaStream_t>(stream), flags);
+}
+
+int pkv_decode_append_attn(const void* q, const void* k_new, const void* v_new, void* k_pages, void* v_pages,
+                           const int32_t* block_table, const int32_t* seq_lens, void* out, float scale,
+                           pkv_stream_t stream, const pkv_cache_desc* desc, int32_t batch, int32_t max_pages_per_seq,
+                           void* workspace, size_t workspace_bytes, uint32_t flags) {
+  return decode_append(q, k_new, v_new, k_pages, v_pages, block_table, seq_lens, nullptr, 0, out, scale, stream, desc,
+                       batch, max_pages_per_seq, workspace, workspace_bytes, flags);
+}
+
+int pkv_decode_append_rope_attn(const void* q, const void* k_new, const void* v_new, void* k_pages, void* v_pages,
+                                const int32_t* block_table, const int32_t* seq_lens, const float* rope_cos_sin,
+                                int32_t rope_max_pos, void* out, float scale, pkv_stream_t stream,
+                                const pkv_cache_desc* desc, int32_t batch, int32_t max_pages_per_seq, void* workspace,
+                                size_t workspace_bytes, uint32_t flags) {
+  if (batch > 0 && rope_cos_sin == nullptr) return PKV_ERR_NULL_ARG;
+  if (rope_max_pos < 1) return PKV_ERR_BAD_SHAPE;
+  if (batch > 0 && !aligned16(rope_cos_sin)) return PKV_ERR_MISALIGNED;
+  return decode_append(q, k_new, v_new, k_pages, v_pages, block_table, seq_lens, rope_cos_sin, rope_max_pos, out,
+                       scale, stream, desc, batch, max_pages_per_seq, workspace, workspace_bytes, flags);
 }
 
 size_t pkv_prefill_workspace_bytes(const pkv_cache_desc* desc, int32_t num_seqs, int32_t max_q_len) {

@@ -13,10 +13,12 @@ int launch_append(const void* k_new, const void* v_new, const int32_t* slot_mapp
 // Decode: workspace = [status header | counters (batch * kv heads) | partials].
 size_t decode_workspace_bytes(int32_t batch, int num_sms);
 // k_new / v_new (nullable): fused append of each request's new token at position seq_lens[b] - 1.
+// rope (nullable, needs k_new): cos/sin table [rope_max_pos][128]; the new key row and the query
+// rows are rotated at that position.
 int launch_decode(const void* q, const void* k_new, const void* v_new, const void* k_pages, const void* v_pages,
-                  const int32_t* block_table, const int32_t* seq_lens, void* out, float scale, int32_t batch,
-                  int32_t max_pages, int32_t num_pages, void* workspace, int num_sms, cudaStream_t stream,
-                  uint32_t flags);
+                  const int32_t* block_table, const int32_t* seq_lens, const float* rope, int32_t rope_max_pos,
+                  void* out, float scale, int32_t batch, int32_t max_pages, int32_t num_pages, void* workspace,
+                  int num_sms, cudaStream_t stream, uint32_t flags);
 int decode_max_batch();
 
 size_t prefill_workspace_bytes(int32_t num_seqs, int32_t max_q_len, int num_sms);

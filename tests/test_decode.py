@@ -288,3 +288,42 @@ def test_fused_rejects_unknown_flags(cuda_device):
                                             run.seq_lens.data_ptr(), run.out.data_ptr(), 1.0, None, ctypes.byref(d),
                                             2, case.max_pages, run.ws.tensor.data_ptr(), run.ws.nbytes, 6)
     assert rc == -3
+
+
+# ---------------------------------------------------------------------------- fused rotary embedding
+
+ROPE_THETA = 1e6  # "Fun-ASR-Nano Native Runtime Design", section "Decoder And Prompt"
+
+
+@pytest.mark.parametrize("cfg", ["tiny", "bs16", "40k", "ragged", "padded"])
+def test_fused_rope_append_decode_matches_oracle(cuda_device, cfg):
+    lens = {"tiny": W.config_seq_lens(1), "bs16": W.config_seq_lens(2), "40k": W.config_seq_lens(3),
+            "ragged": [1, 15, 16, 17, 32, 33, 1000], "padded": [700, 0, 33, 0, 1, 2900]}[cfg]
+    case = W.decode_case(19, lens, pending_append=True, poison=True)
+    cs = oracle.rope_cache(ROPE_THETA, case.geom.head_dim, int(max(lens)) + 3)
+    run = DecodeOnDevice(case, 0, cuda_device)
+    pkv.decode_append_rope_attn(run.q, run.k_new, run.v_new, run.k_pages, run.v_pages, run.block_table,
+                                run.seq_lens, torch.from_numpy(cs).to(cuda_device), run.out, case.geom.scale, run.ws)
+    torch.cuda.synchronize()
+    pos = np.asarray(case.seq_lens, dtype=np.int64) - 1  # -1 for empty requests: nothing appended
+    k_rot = oracle.rope_bf16(case.k_new[0], pos, cs)
+    want_k, want_v = oracle.append(k_rot, case.v_new[0], case.slot_mapping, case.k_pages[0], case.v_pages[0])
+    # the rotated key rows land bit-exactly; every other slot is untouched
+    assert np.array_equal(bits(run.k_pages), want_k) and np.array_equal(bits(run.v_pages), want_v)
+    want = oracle.decode(oracle.rope_f64(case.q[0], pos, cs), want_k, want_v, case.block_table, case.seq_lens,
+                         case.geom.scale)
+    assert_close(bf16_to_f64(run.out), want, f"rope {cfg}")
+    for b, n in enumerate(case.seq_lens):
+        if n == 0:
+            assert torch.count_nonzero(run.out[b]).item() == 0
+    assert run.ws.status() == 0
+
+
+def test_fused_rope_position_beyond_table_is_reported(cuda_device):
+    case = W.decode_case(20, [300, 40], pending_append=True, poison=False)
+    cs = oracle.rope_cache(ROPE_THETA, case.geom.head_dim, 100)  # 300 - 1 is past the last row
+    run = DecodeOnDevice(case, 0, cuda_device)
+    pkv.decode_append_rope_attn(run.q, run.k_new, run.v_new, run.k_pages, run.v_pages, run.block_table,
+                                run.seq_lens, torch.from_numpy(cs).to(cuda_device), run.out, case.geom.scale, run.ws)
+    torch.cuda.synchronize()
+    assert run.ws.status() == -7  # PKV_ERR_OUT_OF_BOUNDS
