@@ -323,6 +323,38 @@ class PrefillStep:
         self.prefill()
         pkv.decode_attn(self.dq, self.k_pages, self.v_pages, self.dbt, self.dlens, self.dout, self.scale, self.ws)
 
+    def mixed_branches(self):
+        """The mixed step as two branches: the chunk (append, prefill) on the current stream and the
+        decode requests (append, attention) on a side stream. They touch disjoint slots and separate
+        workspaces, so a graph of this runs them concurrently where SMs are free."""
+        torch, pkv = self.torch, self.pkv
+        main = torch.cuda.current_stream()
+        if not hasattr(self, "side"):
+            self.side = torch.cuda.Stream()
+        self.side.wait_stream(main)
+        pkv.append(self.k_new, self.v_new, self.slots, self.k_pages, self.v_pages, self.pws)
+        self.prefill()
+        with torch.cuda.stream(self.side):
+            pkv.append(self.dk, self.dv, self.dslots, self.k_pages, self.v_pages, self.ws)
+            pkv.decode_attn(self.dq, self.k_pages, self.v_pages, self.dbt, self.dlens, self.dout, self.scale,
+                            self.ws)
+        main.wait_stream(self.side)
+
+    def capture_mixed(self):
+        """One CUDA graph of the mixed step (two branches)."""
+        torch = self.torch
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            self.mixed_branches()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.mixed_branches()
+        torch.cuda.synchronize()
+        return g
+
 
 def time_launches(torch, fn, reps):
     """Mean duration (ms) of fn's GPU work, bracketed by events with the stream kept busy."""
@@ -349,10 +381,15 @@ def measure_prefill(device, bf16_peak, reps=10):
         torch.cuda.synchronize()
         ms = time_launches(torch, ps.prefill, reps)
         mixed_ms = time_launches(torch, ps.mixed, reps)
+        g = ps.capture_mixed()
+        graph_ms = time_launches(torch, g.replay, reps)
         tf = ps.flops / (ms * 1e-3) / 1e12
         res[f"prefix_{prefix}"] = {"chunk": 4096, "prefill_us": ms * 1e3, "tflops": tf,
                                    "frac_of_measured_bf16": tf / bf16_peak, "gflop": ps.flops / 1e9,
-                                   "mixed_step_us": mixed_ms * 1e3}
+                                   "mixed_step_us": mixed_ms * 1e3,
+                                   # the same step as one CUDA graph, decode requests on a parallel branch
+                                   "mixed_step_graph_us": graph_ms * 1e3}
+        del g
         del ps
         torch.cuda.empty_cache()
     return res

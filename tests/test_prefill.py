@@ -110,3 +110,60 @@ def test_causality_on_gpu(cuda_device):
     pert = PrefillOnDevice(case, cuda_device).run()
     assert torch.equal(base[: lim_row + 1].view(torch.int16), pert[: lim_row + 1].view(torch.int16))
     assert not torch.equal(base[lim_row + 1:].view(torch.int16), pert[lim_row + 1:].view(torch.int16))
+
+
+def test_mixed_step_graph_with_parallel_branches_equals_eager(cuda_device):
+    # the mixed step of workload 4 (a chunk after cached tokens plus concurrent decode requests),
+    # captured as one CUDA graph whose chunk branch (append, prefill) and decode branch (append,
+    # attention) run on different streams: replays give the same bits as sequential eager calls
+    case = W.prefill_case(45, [500], [700], dec_seq_lens=[90, 1000, 17, 2500], poison=True)
+    dev = cuda_device
+
+    def state():
+        c = case
+        return dict(kp=c.k_pages[0].to(dev), vp=c.v_pages[0].to(dev), out=torch.zeros_like(c.q[0], device=dev),
+                    dout=torch.zeros_like(c.dec_q[0], device=dev))
+
+    q, kn, vn = case.q[0].to(dev), case.k_new[0].to(dev), case.v_new[0].to(dev)
+    dq, dk, dv = case.dec_q[0].to(dev), case.dec_k_new[0].to(dev), case.dec_v_new[0].to(dev)
+    slots, bt = i32(case.slot_mapping, dev), i32(case.block_table, dev)
+    prefix, cu = i32(case.prefix_lens, dev), i32(case.cu_q_lens, dev)
+    dslots, dbt, dlens = i32(case.dec_slot_mapping, dev), i32(case.dec_block_table, dev), i32(case.dec_seq_lens, dev)
+    ensure_built()
+    pws = pkv.Workspace(pkv.prefill_workspace_bytes(1, 700), dev)
+    dws = pkv.Workspace(pkv.decode_workspace_bytes(4, case.dec_block_table.shape[1]), dev)
+    scale = case.geom.scale
+
+    def step(s, side=None):
+        pkv.append(kn, vn, slots, s["kp"], s["vp"], pws)
+        pkv.prefill_chunk_attn(q, s["kp"], s["vp"], bt, prefix, cu, s["out"], scale, 700, pws)
+        ctx = torch.cuda.stream(side) if side is not None else None
+        if ctx:
+            side.wait_stream(torch.cuda.current_stream())
+            ctx.__enter__()
+        pkv.append(dk, dv, dslots, s["kp"], s["vp"], dws)
+        pkv.decode_attn(dq, s["kp"], s["vp"], dbt, dlens, s["dout"], scale, dws)
+        if ctx:
+            ctx.__exit__(None, None, None)
+            torch.cuda.current_stream().wait_stream(side)
+
+    eager = state()
+    step(eager)
+    torch.cuda.synchronize()
+    graphed = state()
+    side = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cap):
+        step(state(), side)  # warm-up outside the graph
+    torch.cuda.current_stream().wait_stream(cap)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        step(graphed, side)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    for key in ("out", "dout", "kp", "vp"):
+        assert torch.equal(eager[key].view(torch.int16), graphed[key].view(torch.int16)), key
+    assert pws.status() == 0 and dws.status() == 0
