@@ -49,7 +49,7 @@ WORKLOAD = ("qwen3-0.6b decode step: 28 layers x bs16, 16q/8kv heads, d128, page
 # DRAM traffic of one decode launch on this workload's per-layer pool, from one ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the decode kernel source it was
 # measured on (sha256 prefix of csrc/decode.cu); any other source reports null.
-NCU_DECODE_TRAFFIC = {"e6939e0577a1be15": 107_394_560 + 3_320_064}
+NCU_DECODE_TRAFFIC = {"c47f11f0c5820c2f": 107_395_328 + 3_330_816}
 
 
 def _decode_traffic():
