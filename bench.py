@@ -582,6 +582,7 @@ def main():
         achieved = isolated
     step_bytes = args.layers * (dec_bytes + (0 if step.fused else step.append_bytes()))
     pool_bytes = 2 * step.k_pages.numel() * step.k_pages.element_size()
+    step_tokens = float(np.asarray(step.case.seq_lens, dtype=np.int64).sum())
 
     extra = {}
     if not args.no_extra:
@@ -621,6 +622,30 @@ def main():
         }
         del long_step
         torch.cuda.empty_cache()
+
+        def in_step(lens, seed, name):
+            st = DecodeStep(device, lens, args.layers, seed=seed, fused=not args.unfused)
+            st.capture()
+            n = max(20, args.steps // 4)
+            t = time_graph(st, n, args.warmup, dist_on) / n
+            b = st.decode_bytes()
+            tok = int(np.asarray(lens, dtype=np.int64).sum())
+            res = {"workload": name, "ms_per_step": t, "steps_per_s": 1e3 / t, "launch_us_in_step": t * 1e3 / args.layers,
+                   "gbps_in_step": b / (t * 1e-3 / args.layers) / 1e9,
+                   "frac_of_measured_hbm_in_step": b / (t * 1e-3 / args.layers) / 1e9 / hbm,
+                   "kv_token_layers_per_s": tok * args.layers / (t * 1e-3)}
+            del st
+            torch.cuda.empty_cache()
+            return res
+
+        # the long-audio sweep of workload 3 and the CFG-paired batch of workload 5
+        extra["context_sweep"] = {
+            f"context_{c}": in_step(W.config_seq_lens(3, context=c), 3 + rank,
+                                    f"long-audio decode: 28 layers x bs1, context {c}")
+            for c in (4096, 16384, 65536)}
+        extra["cfg_pairs_bs32"] = in_step(
+            W.config_seq_lens(5), 5 + rank,
+            "CFG-paired decode: 28 layers x bs32 (16 conditional U{1000..8000} + 16 companions U{8..64} + g)")
         extra["chunked_prefill"] = {
             "workload": "4096-token chunk (1 request) after 0/8192/32768 cached tokens; mixed step adds the chunk "
                         "append, 15 decode appends and decode attention over U{500..5000}",
@@ -642,6 +667,9 @@ def main():
                    "l2": "no flush: %d distinct layer pools of %.2f GB in total exceed the 129 MB L2" % (
                        args.layers, pool_bytes / 1e9)},
         "kv_gbps_step": step_bytes / (ms_per_step * 1e-3) / 1e9 * world,
+        # attended (KV token, layer) pairs per second: each cached token of each layer read once
+        "kv_token_layers_per_s": step_tokens * args.layers
+        / (ms_per_step * 1e-3) * world,
         "roofline": {"bound": "hbm", "kernel": "pkv::decode_kernel", "achieved": achieved, "peak": hbm,
                      "unit": "GB/s", "frac": achieved / hbm, "traffic": _decode_traffic(), "peak_kind": peak_kind,
                      "algorithmic_bytes_per_launch": dec_bytes, "launch_us": launch_us,
