@@ -53,9 +53,10 @@
  *    that may run concurrently (different streams) need separate workspaces.
  *  - A workspace serves one kind of attention call: decode calls
  *    (pkv_decode_attn, pkv_decode_append_attn) or prefill calls
- *    (pkv_prefill_chunk_attn), not both, because each keeps its split counters
- *    where the other keeps scratch records. pkv_append uses only the status
- *    word and may share either.
+ *    (pkv_prefill_chunk_attn), not both: each kind relies on its own split
+ *    scratch (counters, and for decode tagged records) having been left
+ *    cleared by the previous call of that kind. pkv_append uses only the
+ *    status word and may share either.
  */
 #ifndef PKV_H_
 #define PKV_H_
@@ -130,8 +131,9 @@ int pkv_append(const void* k_new, const void* v_new, const int32_t* slot_mapping
 
 /*
  * Workspace bytes pkv_decode_attn needs for `batch` requests on the current
- * device (status header, one counter per (request, KV head), and the
- * split-KV partial results). Returns 0 for unsupported arguments.
+ * device: the status header, one counter per (request, KV head), and the
+ * split-KV partial records (two areas of two 1056-byte records per CTA of the
+ * launch grid, one per merge scheme). Returns 0 for unsupported arguments.
  */
 size_t pkv_decode_workspace_bytes(const pkv_cache_desc* desc, int32_t batch, int32_t max_pages_per_seq);
 
@@ -298,7 +300,7 @@ int pkv_prefill_chunk_attn(const void* q, const void* k_pages, const void* v_pag
  * meaning and layout as for pkv_decode_attn; the split-KV scratch comes from a
  * fixed array inside the library instead of a workspace.
  *
- *  - The scratch is one device array of PKV_NOALLOC_SCRATCH_BYTES (1 MiB).
+ *  - The scratch is one device array of PKV_NOALLOC_SCRATCH_BYTES (2 MiB).
  *    Every GPU that loads the library holds it until the process exits. The
  *    call itself allocates and frees nothing.
  *  - Limit: batch <= PKV_NOALLOC_MAX_BATCH (256), and the scratch must cover
@@ -307,7 +309,7 @@ int pkv_prefill_chunk_attn(const void* q, const void* k_pages, const void* v_pag
  *  - The first call on a device looks up the array's device address (a
  *    one-time set-up); make that first call before any CUDA-graph capture.
  *  - Every call uses the same array and it keeps the previous call's
- *    contents; each call zeroes the status word and the split counters on
+ *    contents; each call zeroes the status word, the split counters and records on
  *    `stream` before its kernel. Calls whose kernels overlap on the GPU (on
  *    different streams, or in parallel graph branches) race on the array:
  *    issue them in order on one stream.
@@ -315,7 +317,7 @@ int pkv_prefill_chunk_attn(const void* q, const void* k_pages, const void* v_pag
  *    table) are skipped as in pkv_decode_attn but not reported: the status
  *    word lives in the library's array and no call reads it back.
  */
-#define PKV_NOALLOC_SCRATCH_BYTES (1u << 20)
+#define PKV_NOALLOC_SCRATCH_BYTES (2u << 20)
 #define PKV_NOALLOC_MAX_BATCH 256
 
 int pkv_decode_attn_noalloc(const void* q, const void* k_pages, const void* v_pages, const int32_t* block_table,

@@ -279,7 +279,7 @@ def prefill_chunk_attn(q, k_pages, v_pages, block_table, prefix_lens, cu_q_lens,
 def decode_attn_noalloc(q, k_pages, v_pages, block_table, seq_lens, out, scale: float, stream=None):
     """decode_attn without a workspace, for callers that may not allocate device memory.
 
-    The split-KV scratch is a fixed 1 MiB array inside the library (batch <= 256).
+    The split-KV scratch is a fixed 2 MiB array inside the library (batch <= 256).
     Calls share that array: run them in order on one stream, never overlapping on
     the GPU. Make the first call on a device before any CUDA-graph capture.
     """

@@ -15,7 +15,8 @@
 //    only on host-known sizes (CUDA-graph friendly) and every CTA streams the
 //    same number of pages whatever the length mix.
 //  * A CTA's share is cut into pieces, one per (request, KV head) it touches.
-//    Inside a piece its consumer warps take pages round-robin. A producer warp
+//    Its consumer warps take the share's pages round-robin (page f of the share
+//    goes to consumer (f - lo) mod kCons, across piece boundaries). A producer warp
 //    fills each consumer's ring of shared-memory stages with 1-D bulk copies
 //    (cp.async.bulk, one 4 KiB K tile and one 4 KiB V tile per page) that
 //    complete on the stage's full barrier; consumers release stages through
@@ -36,13 +37,23 @@
 //    while the current piece streams, so a piece boundary costs no round trip.
 //  * At the end of a piece the warps merge through shared memory. A piece that
 //    covers its whole (request, KV head) writes the bf16 output. Otherwise it
-//    writes an fp32 partial (m, l, o). Only a share's first and last piece can
-//    be split; after its last piece the CTA bumps the per-(request, KV head)
-//    counters of both at once (one fence, one round trip). The CTA that brings
-//    a counter to the number of holders stages every partial of that pair in
-//    its drained stage ring (cp.async, one round trip), merges them
-//    (log-sum-exp, in an order fixed by the pair alone) and resets the counter
-//    to zero.
+//    writes a partial record (m, l, o). Only a share's first and last piece
+//    can be split, and a pair's holders are consecutive CTAs. The records are
+//    merged (log-sum-exp, in an order fixed by the pair alone) in one of two
+//    ways, each its own instantiation, chosen by the expected number of
+//    holders per pair (grid size over batch x KV heads):
+//     - Counted, for few pairs over many CTAs (one long request): fp32
+//       records; after its last piece a CTA bumps the pairs' counters (one
+//       fence, one round trip) and the CTA that completes a count stages the
+//       records in its drained stage ring (cp.async, one round trip), merges
+//       them and resets the counter.
+//     - Polled, for many pairs over few CTAs each: records of tagged 32-bit
+//       words -- o rounded to 16 significant bits, m and l exact as the sum of
+//       two such values, a tag in every word's low byte -- written with no
+//       fence or atomic. The CTA holding a pair's last page (necessarily its
+//       first piece, begun by lower-numbered CTAs) reads the holders' records
+//       once its own share is done, again until every word carries the tag,
+//       merges them and clears the records for the next call.
 #include <math_constants.h>
 
 #include "pkv_device.cuh"
@@ -87,7 +98,14 @@ constexpr int kSmemPbuf = kCons * kPageSize * 4 * 4;       // per warp: [16 toke
 constexpr int kSmemMisc = 16;                              // flag words
 constexpr int kSmemFixed = kSmemRing + kSmemBars + kSmemMerge + kSmemQ + kSmemCs + kSmemPbuf + kSmemMisc;
 constexpr int kPieceBytes = kPieceFloats * 4;
-constexpr int kMergeCap = kSmemRing / kPieceBytes;         // partial records staged per batch of the final merge
+constexpr int kMergeCap = kSmemRing / kPieceBytes;         // records staged per batch of a counted merge
+constexpr int kSplitWords = kGroup * kHeadDim + 8;         // tagged words of a polled record: o[2][128], then
+                                                           // m_hi, m_lo, l_hi, l_lo of head 0, then of head 1
+constexpr int kSplitBytes = kSplitWords * 4;
+constexpr uint32_t kTag = 0xa5u;                           // low byte of a word written by this call
+constexpr int kMergeBatch = 8;                             // records a warp has in flight in a polled merge
+constexpr int kPollMax = 8;                                // polled merge up to this many holders per pair
+static_assert(kSplitBytes % 16 == 0, "16-byte loads and clears of a record");
 static_assert((kSmemRing + kSmemBars) % 16 == 0 && kSmemMerge % 16 == 0 && kPieceBytes % 16 == 0, "alignment");
 static_assert(kQBufBytes == 32 * 16, "one 16-byte chunk of a group's query rows per lane");
 static_assert(kCsBytes == 32 * 16, "one 16-byte chunk of a cos/sin row per lane");
@@ -114,8 +132,9 @@ struct DecodeArgs {
   int max_pages;
   int num_pages;
   int* status;
-  int* counters;   // [batch * kKVHeads], zero between calls
-  float* partials; // [2 * gridDim.x][kPieceFloats]
+  int* counters;       // [batch * kKVHeads], zero between calls (counted merge)
+  float* partials;     // [2 * gridDim.x][kPieceFloats] (counted merge)
+  uint32_t* tagged;    // [2 * gridDim.x][kSplitWords], no word tagged between calls (polled merge)
 };
 
 // A piece: pages [p0, p1) of KV head h of request b; flattened indices [fstart, fend).
@@ -173,6 +192,39 @@ __device__ __forceinline__ void pv_tokens(uint32_t vrow0, uint32_t prow0, int t0
   }
 }
 
+// Polled records are 32-bit words: an fp32 value rounded to nearest (even) at
+// 15 mantissa bits, with the tag in the freed low byte. Each word is one
+// single-copy-atomic access, so a reader that sees the tag sees the value,
+// without a fence on the writer's side; a cleared word (zero) carries no tag.
+__device__ __forceinline__ uint32_t tag_word(float v) {
+  const uint32_t u = __float_as_uint(v);
+  if ((u & 0x7fffffffu) > 0x7f800000u) return 0x7fffff00u | kTag;  // NaN stays NaN
+  return ((u + 0x7fu + ((u >> 8) & 1u)) & 0xffffff00u) | kTag;
+}
+__device__ __forceinline__ float untag(uint32_t w) { return __uint_as_float(w & 0xffffff00u); }
+// v = hi + lo with hi and lo both 24-bit floats: exact for every finite fp32 v
+__device__ __forceinline__ void tag_split(float v, uint32_t& hi, uint32_t& lo) {
+  hi = tag_word(v);
+  lo = tag_word(v - untag(hi));
+}
+__device__ __forceinline__ void st_word(uint32_t* p, uint32_t w) {
+  asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(w) : "memory");
+}
+__device__ __forceinline__ uint4 ld_words4(const uint32_t* p) {
+  uint4 r;
+  asm volatile("ld.relaxed.gpu.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p)
+               : "memory");
+  return r;
+}
+__device__ __forceinline__ uint32_t ld_word(const uint32_t* p) {
+  uint32_t r;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(r) : "l"(p) : "memory");
+  return r;
+}
+__device__ __forceinline__ bool tagged(uint32_t w) { return (w & 0xffu) == kTag; }
+
 __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kConsThreads) : "memory");
 }
@@ -191,10 +243,10 @@ __device__ __forceinline__ int request_of(long long f, const int* pref, int batc
   return lo_b;
 }
 
-// kFused: a.k_new / a.v_new are given (fused append); kRope: a.rope is given too.
-// Each combination is its own instantiation, so a path carries no code (and no
+// kFused: a.k_new / a.v_new are given (fused append); kRope: a.rope is given too;
+// kPolled: the polled merge, else the counted one. Each combination is its own instantiation, so a path carries no code (and no
 // registers) for the others.
-template <bool kFused, bool kRope>
+template <bool kFused, bool kRope, bool kPolled>
 __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(const DecodeArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* ring = smem;
@@ -290,12 +342,16 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
   // ============================================================== producer warp
   // Walks the share 32 flattened indices at a time, one per lane: each lane
   // decodes its (request, KV head, page), loads the block-table entry, and works
-  // out which consumer reads the page (within a piece, page p0 + i goes to
-  // consumer i % kCons) and which stage of that consumer's ring it fills (its
-  // running page count, from the lanes before it with the same consumer). The
-  // lanes then issue their own bulk copies in rounds in which every stage is
-  // filled at most once, so each stage's empty barrier is at most one phase
-  // behind the wait.
+  // out which consumer reads the page ((f - lo) mod kCons) and which stage of
+  // that consumer's ring it fills (its running page count, from the lanes
+  // before it with the same consumer). The lanes then issue their own bulk
+  // copies in rounds in which every stage is filled at most once, so each
+  // stage's empty barrier is at most one phase behind the wait. Because the
+  // assignment follows the share and not the piece, round r of a chunk holds
+  // exactly its pages 12r .. 12r + 11 and waits only on pages of earlier
+  // rounds; with a piece-relative assignment a run of one-page pieces piled
+  // onto one consumer, and a round could wait on a consumer held at a piece
+  // boundary by a page of a later round (a deadlock).
   if (warp == kCons) {
     const uint64_t policy = policy_evict_first();
     const unsigned lt_mask = (1u << lane) - 1u;
@@ -314,8 +370,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
         const int off = static_cast<int>(f - pref[b]);
         hh = off / np;
         const int p = off % np;
-        const long long seg = pref[b] + static_cast<long long>(hh) * np;
-        c = static_cast<int>((f - (seg > lo ? seg : lo)) % kCons);
+        c = static_cast<int>((f - lo) % kCons);
         bb = b;
         id = __ldg(a.block_table + static_cast<size_t>(b) * a.max_pages + p);
         if (kFused && p == np - 1) wslot = (sl[b] - 1) % kPageSize;  // the new token's slot
@@ -476,6 +531,10 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
 
   Piece pc;
   bool have = find_piece(lo, hi, pref, batch, pc);
+  // Polled merge: the CTA that holds the last page of a split (request, KV head)
+  // merges it; that pair can only be its first piece, begun by an earlier CTA.
+  const bool merger = kPolled && have && pc.p0 > 0 && pc.p1 == pc.np;
+  const int mb = pc.b, mh = pc.h;
   if (have) stage_q(pc, 0);
   if (warp == 0) cp_async_wait_all();
   consumer_sync();
@@ -488,7 +547,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
     const bool complete = (pc.p0 == 0 && pc.p1 == pc.np);
     int sp_cfirst = 0, sp_n = 0;
     bool sp_two = false;
-    if (!complete) span_of(b, h, sp_cfirst, sp_n, sp_two);  // before the stream, off the critical path
+    if (!kPolled && !complete) span_of(b, h, sp_cfirst, sp_n, sp_two);  // before the stream, off the critical path
 
     // query rows of both heads of the group, in this lane's chunk order, rotated
     // (with a cos/sin table) and pre-scaled. The lane's chunks jj and jj + 2
@@ -554,7 +613,8 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
 #pragma unroll
       for (int e = 0; e < 4; ++e) o[i][e] = make_float2(0.f, 0.f);
 
-    for (int p = pc.p0 + warp; p < pc.p1; p += kCons) {
+    const int w0 = static_cast<int>((pc.fstart - lo) % kCons);  // consumer of the piece's first page
+    for (int p = pc.p0 + (warp - w0 + kCons) % kCons; p < pc.p1; p += kCons) {
       const int slot = warp * kDecRing + k % kDecRing;
       const uint32_t parity = static_cast<uint32_t>(k / kDecRing) & 1u;
       if (!failed) {
@@ -713,153 +773,139 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
       }
     } else {
       const int my_slot = 2 * blockIdx.x + (pc.fstart == lo ? 0 : 1);
-      float* rec = a.partials + static_cast<size_t>(my_slot) * kPieceFloats;
-      if (owns_dims) {
+      if constexpr (kPolled) {
+        uint32_t* rec = a.tagged + static_cast<size_t>(my_slot) * kSplitWords;
+        if (owns_dims) {
 #pragma unroll
-        for (int e = 0; e < kDimsPerThread; ++e) {
-          const int d = tid + e * kConsThreads;
-          rec[4 + d] = O[0][e];
-          rec[kRec + 4 + d] = O[1][e];
+          for (int e = 0; e < kDimsPerThread; ++e) {
+            const int d = tid + e * kConsThreads;
+            st_word(rec + d, tag_word(O[0][e]));
+            st_word(rec + kHeadDim + d, tag_word(O[1][e]));
+          }
         }
-      }
-      if (tid == 0) {
-        rec[0] = M[0];
-        rec[1] = L[0];
-        rec[kRec] = M[1];
-        rec[kRec + 1] = L[1];
-      }
-      if (npend == 0) {
-        pb0 = b, ph0 = h, pc0 = sp_cfirst, pn0 = sp_n, pt0 = sp_two;
+        if (tid < 8) {  // m_hi, m_lo, l_hi, l_lo of head tid / 4
+          const float x = (tid & 2) ? L[tid >> 2] : M[tid >> 2];
+          uint32_t hi, lo;
+          tag_split(x, hi, lo);
+          st_word(rec + 2 * kHeadDim + tid, (tid & 1) ? lo : hi);
+        }
       } else {
-        pb1 = b, ph1 = h, pc1 = sp_cfirst, pn1 = sp_n, pt1 = sp_two;
+        float* rec = a.partials + static_cast<size_t>(my_slot) * kPieceFloats;
+        if (owns_dims) {
+  #pragma unroll
+          for (int e = 0; e < kDimsPerThread; ++e) {
+            const int d = tid + e * kConsThreads;
+            rec[4 + d] = O[0][e];
+            rec[kRec + 4 + d] = O[1][e];
+          }
+        }
+        if (tid == 0) {
+          rec[0] = M[0];
+          rec[1] = L[0];
+          rec[kRec] = M[1];
+          rec[kRec + 1] = L[1];
+        }
+        if (npend == 0) {
+          pb0 = b, ph0 = h, pc0 = sp_cfirst, pn0 = sp_n, pt0 = sp_two;
+        } else {
+          pb1 = b, ph1 = h, pc1 = sp_cfirst, pn1 = sp_n, pt1 = sp_two;
+        }
+        ++npend;
+
       }
-      ++npend;
     }
     if (warp == 0) cp_async_wait_all();  // the next piece's query rows have landed
     consumer_sync();                     // merge buffer and qbuf[j & 1] free, qbuf[(j + 1) & 1] visible
     pc = nx;
     have = have_next;
   }
-  if (npend == 0) return;
+  if constexpr (kPolled) {
+    if (!merger || flag[2] != 0) return;  // (a failed wait: copies may still land, merge nothing)
 
-  // Count this CTA's records in (release) and learn whether it completed a count
-  // (acquire): the CTA that does merges every record of that (request, KV head).
-  if (tid == 0) {
-    __threadfence();
-    const int old0 = atomicAdd(a.counters + pb0 * kKVHeads + ph0, 1);
-    const int old1 = npend > 1 ? atomicAdd(a.counters + pb1 * kKVHeads + ph1, 1) : -1;
-    __threadfence();
-    flag[0] = old0 == pn0 - 1 ? 1 : 0;
-    flag[1] = old1 == pn1 - 1 ? 1 : 0;
-  }
-  consumer_sync();
-  if (flag[2] != 0) {  // a wait failed: copies may still land in the ring, merge nothing
-    if (tid == 0) {
-      if (flag[0]) a.counters[pb0 * kKVHeads + ph0] = 0;
-      if (flag[1]) a.counters[pb1 * kKVHeads + ph1] = 0;
-    }
-    return;
-  }
-  // Final merges (log-sum-exp over the partial records) of the pairs whose count
-  // this CTA completed. Their records are staged in the drained stage ring by
-  // 16-byte asynchronous copies (one round trip per batch of up to kMergeCap
-  // records); record t of a pair is folded by warp t % kCons, each lane owning
-  // dims 4 lane .. 4 lane + 3 of both heads, and the warps' states are then
-  // combined through the merge buffer. Which warp folds which record, and the
-  // batch boundaries, depend only on the pair, so the result is the same
-  // whichever CTA merges.
-  const int nm0 = flag[0] ? pn0 : 0;
-  const int nm1 = flag[1] ? pn1 : 0;
-  if (nm0 + nm1 == 0) return;
-  const uint32_t ring_s = smem_u32(ring);
-  const float* R = reinterpret_cast<const float*>(ring);
-  constexpr int kChunks = kPieceBytes / 16;
-  static_assert(kChunks > 64 && kChunks <= 96, "a record is copied in three lane-strided passes");
-  static_assert(kConsThreads >= kHeadDim, "the final combine maps one thread to one dim");
-  float fm[2][2], fl[2][2];
-  float4 fo[2][2];
-#pragma unroll
-  for (int i = 0; i < 2; ++i)
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      fm[i][hh] = -CUDART_INF_F;
-      fl[i][hh] = 0.f;
-      fo[i][hh] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-  // One batch: records [t0[i], t1[i]) of pair i, pair 0's first in the ring.
-  auto merge_batch = [&](const int (&t0)[2], const int (&t1)[2]) {
-    const int c0 = t1[0] - t0[0], nb = c0 + t1[1] - t0[1];
-    for (int p = warp; p < nb; p += kCons) {
-      const bool second = p >= c0;
-      const int t = second ? t0[1] + p - c0 : t0[0] + p;
-      const int cf = second ? pc1 : pc0;
-      const bool two = second ? pt1 : pt0;
+    // Polled merge (log-sum-exp) of the pair of this CTA's first piece over the
+    // records of its n holders. Warp w folds records t = w, w + kCons, ... in that
+    // order, four at a time, each lane owning dims 4 lane .. 4 lane + 3 of both
+    // heads; a record is read again until every word carries the tag. The order
+    // depends only on the pair, so the result is the same bits on every call.
+    int cf = 0, n = 0;
+    bool two = false;
+    span_of(mb, mh, cf, n, two);
+    auto rec_of = [&](int t) {
       const size_t slot = 2 * static_cast<size_t>(cf + t) + ((t == 0 && two) ? 1 : 0);
-      const unsigned char* src = reinterpret_cast<const unsigned char*>(a.partials + slot * kPieceFloats);
-      const uint32_t dst = ring_s + p * kPieceBytes;
-      cp_async16(dst + lane * 16, src + lane * 16);
-      cp_async16(dst + (lane + 32) * 16, src + (lane + 32) * 16);
-      if (lane < kChunks - 64) cp_async16(dst + (lane + 64) * 16, src + (lane + 64) * 16);
-    }
-    cp_async_wait_all();
-    consumer_sync();
+      return a.tagged + slot * kSplitWords;
+    };
+    float fm[2] = {-CUDART_INF_F, -CUDART_INF_F}, fl[2] = {0.f, 0.f};
+    float4 fo[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+    bool lost = false;  // a record never got its tags (a bounded wait ran out)
+    for (int t0 = warp; t0 < n && !lost; t0 += kMergeBatch * kCons) {
+      uint4 R[kMergeBatch][2];   // o dims 4 lane .. 4 lane + 3 of heads 0 and 1
+      uint32_t W[kMergeBatch];   // lanes 0..7: word lane of the m/l block
+      auto load = [&](int r) {
+        const uint32_t* rec = rec_of(t0 + r * kCons);
+        R[r][0] = ld_words4(rec + 4 * lane);
+        R[r][1] = ld_words4(rec + kHeadDim + 4 * lane);
+        W[r] = lane < 8 ? ld_word(rec + 2 * kHeadDim + lane) : kTag;
+      };
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const int ps = i == 0 ? 0 : c0;             // ring position of record t0[i]
-      const int pe = ps + t1[i] - t0[i];
-      const int pfirst = ps + ((warp - t0[i]) % kCons + kCons) % kCons;  // this warp's first record t
+      for (int r = 0; r < kMergeBatch; ++r)
+        if (t0 + r * kCons < n) load(r);
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        float m = fm[i][hh];
-        for (int p = pfirst; p < pe; p += kCons) m = fmaxf(m, R[p * kPieceFloats + hh * kRec]);
-        const float keep = fm[i][hh] == -CUDART_INF_F ? 0.f : ex2(fm[i][hh] - m);
-        float l = fl[i][hh] * keep;
-        float4 o = fo[i][hh];
-        o.x *= keep, o.y *= keep, o.z *= keep, o.w *= keep;
-#pragma unroll 4
-        for (int p = pfirst; p < pe; p += kCons) {
-          const float* r = R + p * kPieceFloats + hh * kRec;
-          const float sc = ex2(r[0] - m);
-          l += r[1] * sc;
-          const float4 v = reinterpret_cast<const float4*>(r + 4)[lane];  // plain load: schedulable across records
-          o.x += v.x * sc, o.y += v.y * sc, o.z += v.z * sc, o.w += v.w * sc;
+      for (int r = 0; r < kMergeBatch; ++r) {
+        if (t0 + r * kCons >= n) break;
+        auto all_tagged = [&]() {
+          bool ok = tagged(W[r]);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh)
+            ok = ok && tagged(R[r][hh].x) && tagged(R[r][hh].y) && tagged(R[r][hh].z) && tagged(R[r][hh].w);
+          return __all_sync(kFull, ok);
+        };
+        if (!all_tagged()) {
+          const long long tw = clock64();
+          bool ok = false;
+          while (!ok) {
+            if (clock64() - tw > kWaitLimitCycles) break;
+            load(r);
+            ok = all_tagged();
+          }
+          if (!ok) {
+            lost = true;
+            break;
+          }
         }
-        fm[i][hh] = m;
-        fl[i][hh] = l;
-        fo[i][hh] = o;
+        const float ml = untag(W[r]);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const float mr = __shfl_sync(kFull, ml, 4 * hh) + __shfl_sync(kFull, ml, 4 * hh + 1);
+          const float lr = __shfl_sync(kFull, ml, 4 * hh + 2) + __shfl_sync(kFull, ml, 4 * hh + 3);
+          const float mn = fmaxf(fm[hh], mr);
+          const float keep = ex2(fm[hh] - mn), sc = ex2(mr - mn);
+          fl[hh] = fl[hh] * keep + lr * sc;
+          float4& o = fo[hh];
+          o.x = o.x * keep + untag(R[r][hh].x) * sc;
+          o.y = o.y * keep + untag(R[r][hh].y) * sc;
+          o.z = o.z * keep + untag(R[r][hh].z) * sc;
+          o.w = o.w * keep + untag(R[r][hh].w) * sc;
+          fm[hh] = mn;
+        }
       }
     }
-    consumer_sync();  // the ring is free for the next batch
-  };
-  if (nm0 + nm1 <= kMergeCap) {
-    const int t0[2] = {0, 0}, t1[2] = {nm0, nm1};
-    merge_batch(t0, t1);
-  } else {
-    for (int t = 0; t < nm0; t += kMergeCap) {
-      const int t0[2] = {t, 0}, t1[2] = {t + kMergeCap < nm0 ? t + kMergeCap : nm0, 0};
-      merge_batch(t0, t1);
+    if (lost && lane == 0) {
+      set_status(a.status, PKV_ERR_DEVICE_TIMEOUT);
+      flag[2] = 1;
     }
-    for (int t = 0; t < nm1; t += kMergeCap) {
-      const int t0[2] = {0, t}, t1[2] = {0, t + kMergeCap < nm1 ? t + kMergeCap : nm1};
-      merge_batch(t0, t1);
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    if ((i == 0 ? nm0 : nm1) == 0) continue;
     float* mw = merge + warp * kPieceFloats;
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
-      reinterpret_cast<float4*>(mw + hh * kRec + 4)[lane] = fo[i][hh];
+      reinterpret_cast<float4*>(mw + hh * kRec + 4)[lane] = fo[hh];
       if (lane == 0) {
-        mw[hh * kRec] = fm[i][hh];
-        mw[hh * kRec + 1] = fl[i][hh];
+        mw[hh * kRec] = fm[hh];
+        mw[hh * kRec + 1] = fl[hh];
       }
     }
     consumer_sync();
-    const int b = i ? pb1 : pb0, h = i ? ph1 : ph0;
+    if (flag[2] != 0) return;
     if (tid < kHeadDim) {
-      __nv_bfloat16* orow = a.out + (static_cast<size_t>(b) * kQHeads + h * kGroup) * kHeadDim;
+      __nv_bfloat16* orow = a.out + (static_cast<size_t>(mb) * kQHeads + mh * kGroup) * kHeadDim;
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         float m = -CUDART_INF_F;
@@ -876,8 +922,151 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
         orow[hh * kHeadDim + tid] = __float2bfloat16_rn(acc / l);
       }
     }
-    if (tid == 0) a.counters[b * kKVHeads + h] = 0;
-    consumer_sync();  // merge buffer free for the second pair
+    // clear the tags of the merged records for the next call (every read above has completed)
+    for (int i = tid; i < n * (kSplitBytes / 16); i += kConsThreads) {
+      const int t = i / (kSplitBytes / 16), c = i % (kSplitBytes / 16);
+      reinterpret_cast<uint4*>(rec_of(t))[c] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  } else {
+    if (npend == 0) return;
+
+    // Count this CTA's records in (release) and learn whether it completed a count
+    // (acquire): the CTA that does merges every record of that (request, KV head).
+    if (tid == 0) {
+      __threadfence();
+      const int old0 = atomicAdd(a.counters + pb0 * kKVHeads + ph0, 1);
+      const int old1 = npend > 1 ? atomicAdd(a.counters + pb1 * kKVHeads + ph1, 1) : -1;
+      __threadfence();
+      flag[0] = old0 == pn0 - 1 ? 1 : 0;
+      flag[1] = old1 == pn1 - 1 ? 1 : 0;
+    }
+    consumer_sync();
+    if (flag[2] != 0) {  // a wait failed: copies may still land in the ring, merge nothing
+      if (tid == 0) {
+        if (flag[0]) a.counters[pb0 * kKVHeads + ph0] = 0;
+        if (flag[1]) a.counters[pb1 * kKVHeads + ph1] = 0;
+      }
+      return;
+    }
+    // Final merges (log-sum-exp over the partial records) of the pairs whose count
+    // this CTA completed. Their records are staged in the drained stage ring by
+    // 16-byte asynchronous copies (one round trip per batch of up to kMergeCap
+    // records); record t of a pair is folded by warp t % kCons, each lane owning
+    // dims 4 lane .. 4 lane + 3 of both heads, and the warps' states are then
+    // combined through the merge buffer. Which warp folds which record, and the
+    // batch boundaries, depend only on the pair, so the result is the same
+    // whichever CTA merges.
+    const int nm0 = flag[0] ? pn0 : 0;
+    const int nm1 = flag[1] ? pn1 : 0;
+    if (nm0 + nm1 == 0) return;
+    const uint32_t ring_s = smem_u32(ring);
+    const float* R = reinterpret_cast<const float*>(ring);
+    constexpr int kChunks = kPieceBytes / 16;
+    static_assert(kChunks > 64 && kChunks <= 96, "a record is copied in three lane-strided passes");
+    static_assert(kConsThreads >= kHeadDim, "the final combine maps one thread to one dim");
+    float fm[2][2], fl[2][2];
+    float4 fo[2][2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        fm[i][hh] = -CUDART_INF_F;
+        fl[i][hh] = 0.f;
+        fo[i][hh] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    // One batch: records [t0[i], t1[i]) of pair i, pair 0's first in the ring.
+    auto merge_batch = [&](const int (&t0)[2], const int (&t1)[2]) {
+      const int c0 = t1[0] - t0[0], nb = c0 + t1[1] - t0[1];
+      for (int p = warp; p < nb; p += kCons) {
+        const bool second = p >= c0;
+        const int t = second ? t0[1] + p - c0 : t0[0] + p;
+        const int cf = second ? pc1 : pc0;
+        const bool two = second ? pt1 : pt0;
+        const size_t slot = 2 * static_cast<size_t>(cf + t) + ((t == 0 && two) ? 1 : 0);
+        const unsigned char* src = reinterpret_cast<const unsigned char*>(a.partials + slot * kPieceFloats);
+        const uint32_t dst = ring_s + p * kPieceBytes;
+        cp_async16(dst + lane * 16, src + lane * 16);
+        cp_async16(dst + (lane + 32) * 16, src + (lane + 32) * 16);
+        if (lane < kChunks - 64) cp_async16(dst + (lane + 64) * 16, src + (lane + 64) * 16);
+      }
+      cp_async_wait_all();
+      consumer_sync();
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int ps = i == 0 ? 0 : c0;             // ring position of record t0[i]
+        const int pe = ps + t1[i] - t0[i];
+        const int pfirst = ps + ((warp - t0[i]) % kCons + kCons) % kCons;  // this warp's first record t
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          float m = fm[i][hh];
+          for (int p = pfirst; p < pe; p += kCons) m = fmaxf(m, R[p * kPieceFloats + hh * kRec]);
+          const float keep = fm[i][hh] == -CUDART_INF_F ? 0.f : ex2(fm[i][hh] - m);
+          float l = fl[i][hh] * keep;
+          float4 o = fo[i][hh];
+          o.x *= keep, o.y *= keep, o.z *= keep, o.w *= keep;
+#pragma unroll 4
+          for (int p = pfirst; p < pe; p += kCons) {
+            const float* r = R + p * kPieceFloats + hh * kRec;
+            const float sc = ex2(r[0] - m);
+            l += r[1] * sc;
+            const float4 v = reinterpret_cast<const float4*>(r + 4)[lane];  // plain load: schedulable across records
+            o.x += v.x * sc, o.y += v.y * sc, o.z += v.z * sc, o.w += v.w * sc;
+          }
+          fm[i][hh] = m;
+          fl[i][hh] = l;
+          fo[i][hh] = o;
+        }
+      }
+      consumer_sync();  // the ring is free for the next batch
+    };
+    if (nm0 + nm1 <= kMergeCap) {
+      const int t0[2] = {0, 0}, t1[2] = {nm0, nm1};
+      merge_batch(t0, t1);
+    } else {
+      for (int t = 0; t < nm0; t += kMergeCap) {
+        const int t0[2] = {t, 0}, t1[2] = {t + kMergeCap < nm0 ? t + kMergeCap : nm0, 0};
+        merge_batch(t0, t1);
+      }
+      for (int t = 0; t < nm1; t += kMergeCap) {
+        const int t0[2] = {0, t}, t1[2] = {0, t + kMergeCap < nm1 ? t + kMergeCap : nm1};
+        merge_batch(t0, t1);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      if ((i == 0 ? nm0 : nm1) == 0) continue;
+      float* mw = merge + warp * kPieceFloats;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        reinterpret_cast<float4*>(mw + hh * kRec + 4)[lane] = fo[i][hh];
+        if (lane == 0) {
+          mw[hh * kRec] = fm[i][hh];
+          mw[hh * kRec + 1] = fl[i][hh];
+        }
+      }
+      consumer_sync();
+      const int b = i ? pb1 : pb0, h = i ? ph1 : ph0;
+      if (tid < kHeadDim) {
+        __nv_bfloat16* orow = a.out + (static_cast<size_t>(b) * kQHeads + h * kGroup) * kHeadDim;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          float m = -CUDART_INF_F;
+#pragma unroll
+          for (int w = 0; w < kCons; ++w) m = fmaxf(m, merge[w * kPieceFloats + hh * kRec]);
+          float l = 0.f, acc = 0.f;
+#pragma unroll
+          for (int w = 0; w < kCons; ++w) {
+            const float* r = merge + w * kPieceFloats + hh * kRec;
+            const float sc = r[0] == -CUDART_INF_F ? 0.f : ex2(r[0] - m);  // warps that folded no record
+            l += r[1] * sc;
+            acc += r[4 + tid] * sc;
+          }
+          orow[hh * kHeadDim + tid] = __float2bfloat16_rn(acc / l);
+        }
+      }
+      if (tid == 0) a.counters[b * kKVHeads + h] = 0;
+      consumer_sync();  // merge buffer free for the second pair
+    }
   }
 }
 
@@ -886,6 +1075,7 @@ size_t decode_workspace_bytes(int32_t batch, int num_sms) {
   off += (static_cast<size_t>(batch) * kKVHeads * 4 + 255) / 256 * 256;
   const int grid = kDecCtasPerSm * num_sms < kMaxGrid ? kDecCtasPerSm * num_sms : kMaxGrid;
   off += static_cast<size_t>(2) * grid * kPieceFloats * 4;
+  off += static_cast<size_t>(2) * grid * kSplitBytes;
   return off;
 }
 
@@ -896,18 +1086,24 @@ int launch_decode(const void* q, const void* k_new, const void* v_new, const voi
   if (batch == 0) return PKV_OK;
   if (rope != nullptr && k_new == nullptr) return PKV_ERR_NULL_ARG;
   const size_t smem = decode_smem_bytes(batch);
-  void (*kern)(const DecodeArgs) = k_new == nullptr ? decode_kernel<false, false>
-                                   : rope == nullptr ? decode_kernel<true, false>
-                                                     : decode_kernel<true, true>;
+  // Polled merge when a pair is expected to span at most kPollMax CTAs (equal
+  // lengths); the counted merge for few pairs over many CTAs.
+  const int grid = num_sms * kDecCtasPerSm < kMaxGrid ? num_sms * kDecCtasPerSm : kMaxGrid;
+  const bool polled = grid <= kPollMax * batch * kKVHeads;
+  using Kern = void (*)(const DecodeArgs);
+  static const Kern kKerns[2][3] = {
+      {decode_kernel<false, false, false>, decode_kernel<true, false, false>, decode_kernel<true, true, false>},
+      {decode_kernel<false, false, true>, decode_kernel<true, false, true>, decode_kernel<true, true, true>}};
   const int variant = k_new == nullptr ? 0 : rope == nullptr ? 1 : 2;
-  static bool attr_set[64][3] = {};
+  const Kern kern = kKerns[polled ? 1 : 0][variant];
+  static bool attr_set[64][2][3] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
-  if (dev < 64 && !attr_set[dev][variant]) {
+  if (dev < 64 && !attr_set[dev][polled ? 1 : 0][variant]) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(decode_smem_bytes(kMaxDecodeBatch))) != cudaSuccess)
       return PKV_ERR_CUDA;
-    attr_set[dev][variant] = true;
+    attr_set[dev][polled ? 1 : 0][variant] = true;
   }
   int occ = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kDecThreads, smem) != cudaSuccess)
@@ -936,8 +1132,12 @@ int launch_decode(const void* q, const void* k_new, const void* v_new, const voi
   a.counters = reinterpret_cast<int*>(ws + PKV_STATUS_BYTES);
   a.partials = reinterpret_cast<float*>(ws + PKV_STATUS_BYTES +
                                         (static_cast<size_t>(batch) * kKVHeads * 4 + 255) / 256 * 256);
-  const int grid = num_sms * occ < kMaxGrid ? num_sms * occ : kMaxGrid;
-  return launch_pdl(kern, dim3(grid), dim3(kDecThreads), smem, stream, a) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  const int slots = 2 * (num_sms * kDecCtasPerSm < kMaxGrid ? num_sms * kDecCtasPerSm : kMaxGrid);
+  a.tagged = reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(a.partials) +
+                                         static_cast<size_t>(slots) * kPieceFloats * 4);
+  const int launch_grid = num_sms * occ < kMaxGrid ? num_sms * occ : kMaxGrid;
+  return launch_pdl(kern, dim3(launch_grid), dim3(kDecThreads), smem, stream, a) == cudaSuccess ? PKV_OK
+                                                                                                : PKV_ERR_CUDA;
 }
 
 }  // namespace pkv

@@ -86,10 +86,9 @@ extern "C" int pkv_decode_attn_noalloc(const void* q, const void* k_pages, const
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // The array keeps whatever the previous call left. The status word and the
-  // per-(request, KV head) split counters must start at zero; a call that
-  // stopped early (a timed-out wait) could have left them set.
-  const size_t zero_bytes = PKV_STATUS_BYTES + static_cast<size_t>(batch) * desc->num_kv_heads * sizeof(int32_t);
-  if (cudaMemsetAsync(scratch, 0, zero_bytes, s) != cudaSuccess) return PKV_ERR_CUDA;
+  // split records must start at zero; a call that stopped early (a timed-out
+  // wait) could have left tagged words behind.
+  if (cudaMemsetAsync(scratch, 0, pkv::decode_workspace_bytes(batch, sms), s) != cudaSuccess) return PKV_ERR_CUDA;
   return pkv::launch_decode(q, nullptr, nullptr, k_pages, v_pages, block_table, seq_lens, nullptr, 0, out, scale, batch,
                             max_pages_per_seq, desc->num_pages, scratch, sms, s, 0u);
 }

@@ -65,7 +65,8 @@ def test_mixed_step_decode_part(cuda_device):
     _check_case(case, cuda_device, what="mixed decode")
 
 
-@pytest.mark.parametrize("lens", [[1], [17], [15, 16, 17, 31, 32, 33], list(range(1, 65))])
+@pytest.mark.parametrize("lens", [[1], [17], [15, 16, 17, 31, 32, 33], list(range(1, 65)),
+                                  [40000, 16, 16, 16, 16], [3, 30000, 5, 9000]])
 def test_ragged_lengths(cuda_device, lens):
     case = W.decode_case(6, lens, pending_append=True, poison=True)
     _check_case(case, cuda_device, what=f"ragged {lens[:4]}")
@@ -167,16 +168,37 @@ def test_cuda_graph_replay_matches_eager(cuda_device):
         assert r.ws.status() == 0
 
 
-def test_repeated_calls_reuse_the_workspace(cuda_device):
-    # the split-KV counters return to zero, so a second call on the same workspace is identical
-    case = W.decode_case(13, [40000], pending_append=False, poison=True)
+def _split_scratch(ws, batch):
+    """(counters, tagged records) views of a decode workspace. Layout: status
+    header, int32 counters [batch][8] padded to 256 B, fp32 records, tagged
+    records; each record area holds two 1056-byte records per CTA of the grid
+    (two CTAs per SM)."""
+    sms = torch.cuda.get_device_properties(ws.tensor.device).multi_processor_count
+    slots = 2 * min(2 * sms, 2048)
+    cnt_bytes = (batch * 8 * 4 + 255) // 256 * 256
+    off = pkv.PKV_STATUS_BYTES
+    counters = ws.tensor[off:off + cnt_bytes]
+    tagged = ws.tensor[off + cnt_bytes + slots * 1056:off + cnt_bytes + 2 * slots * 1056]
+    assert off + cnt_bytes + 2 * slots * 1056 == ws.nbytes
+    return counters, tagged
+
+
+@pytest.mark.parametrize("lens", [[40000], "bs16", [1, 17, 0, 33, 250, 4095, 16, 15, 3000, 2]])
+def test_repeated_calls_reuse_the_workspace(cuda_device, lens):
+    # the split counters return to zero and the merging CTAs clear every tagged
+    # record they read, so a second call on the same workspace gives the same bits
+    lens = W.config_seq_lens(2) if lens == "bs16" else lens
+    case = W.decode_case(13, lens, pending_append=False, poison=True)
     run = DecodeOnDevice(case, 0, cuda_device)
     a = run.step().clone()
+    torch.cuda.synchronize()
+    counters, tagged = _split_scratch(run.ws, case.batch)
+    assert torch.count_nonzero(counters).item() == 0 and torch.count_nonzero(tagged).item() == 0
     b = run.step().clone()
     torch.cuda.synchronize()
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
-    cnt = run.ws.tensor[256:256 + 4 * 8].view(torch.int32)
-    assert torch.count_nonzero(cnt).item() == 0
+    assert torch.count_nonzero(counters).item() == 0 and torch.count_nonzero(tagged).item() == 0
+    assert run.ws.status() == 0
 
 
 def test_page_id_outside_pool_is_reported_not_read(cuda_device):
