@@ -371,6 +371,63 @@ def time_launches(torch, fn, reps):
     return float(np.mean(durs))
 
 
+class GenericDecodeStep:
+    """Decode attention alone (no append) over `layers` distinct pools of another cache geometry:
+    the generic decode path (any of 1/2/4/8 query heads per KV head, head_dim 64 or 128)."""
+
+    def __init__(self, device, seq_lens, geom, layers: int, seed: int):
+        import torch
+
+        import paged_kv_decode_gb300 as pkv
+        from paged_kv_decode_gb300 import workloads as W
+
+        self.torch, self.pkv, self.layers, self.geom = torch, pkv, layers, geom
+        case = W.decode_case(seed, seq_lens, geom=geom, layers=layers, device=device, pending_append=False,
+                             poison=True)
+        self.case = case
+        i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)
+        self.block_table, self.seq_lens = i32(case.block_table), i32(case.seq_lens)
+        self.out = torch.empty_like(case.q)
+        self.ws = pkv.Workspace(pkv.decode_workspace_bytes(case.batch, case.max_pages, case.num_pages, geom.n_q_heads,
+                                                           geom.n_kv_heads, geom.head_dim), device)
+        self.graph = None
+
+    def decode_bytes(self) -> int:
+        c, g = self.case, self.geom
+        kv = int(c.seq_lens.astype(np.int64).sum()) * g.n_kv_heads * g.head_dim * 2 * 2
+        return kv + 2 * c.batch * g.n_q_heads * g.head_dim * 2 + self.block_table.numel() * 4 + c.batch * 4
+
+    def step_eager(self):
+        c = self.case
+        for l in range(self.layers):
+            self.pkv.decode_attn(c.q[l], c.k_pages[l], c.v_pages[l], self.block_table, self.seq_lens, self.out[l],
+                                 self.geom.scale, self.ws)
+
+    capture = DecodeStep.capture
+
+
+def measure_shapes(device, hbm, layers=8, steps=30, warmup=5):
+    """Other decoder geometries on the generic decode path, bs16 U{300..3000}: per-layer time and
+    bandwidth (the pages name these backbones without head counts; the shapes are examples)."""
+    from paged_kv_decode_gb300 import workloads as W
+
+    res = {}
+    for name, g in (("32q_8kv_d128", W.Geometry(32, 8, 128)), ("32q_32kv_d128", W.Geometry(32, 32, 128)),
+                    ("32q_32kv_d64", W.Geometry(32, 32, 64)), ("64q_8kv_d128", W.Geometry(64, 8, 128))):
+        st = GenericDecodeStep(device, W.config_seq_lens(2), g, layers, seed=31)
+        st.capture()
+        ms = time_graph(st, steps, warmup, False) / steps
+        us = ms * 1e3 / layers
+        gbps = st.decode_bytes() / (us * 1e-6) / 1e9
+        res[name] = {"us_per_layer": us, "gbps": gbps, "frac_of_measured_hbm": gbps / hbm,
+                     "bytes_per_layer": st.decode_bytes(), "layers_in_graph": layers}
+        del st
+        import torch
+
+        torch.cuda.empty_cache()
+    return res
+
+
 def measure_prefill(device, bf16_peak, reps=10):
     import torch
 
@@ -646,6 +703,9 @@ def main():
         extra["cfg_pairs_bs32"] = in_step(
             W.config_seq_lens(5), 5 + rank,
             "CFG-paired decode: 28 layers x bs32 (16 conditional U{1000..8000} + 16 companions U{8..64} + g)")
+        extra["other_geometries_bs16"] = {
+            "workload": "decode attention alone (generic path), bs16 U{300..3000}, 8 layers per graph",
+            **measure_shapes(device, hbm)}
         extra["chunked_prefill"] = {
             "workload": "4096-token chunk (1 request) after 0/8192/32768 cached tokens; mixed step adds the chunk "
                         "append, 15 decode appends and decode attention over U{500..5000}",

@@ -55,11 +55,13 @@ def desc(num_pages: int, num_q_heads: int = 16, num_kv_heads: int = 8, head_dim:
     return _lib.CacheDesc(num_q_heads, num_kv_heads, head_dim, page_size, int(num_pages))
 
 
-def _desc_of(k_pages) -> "_lib.CacheDesc":
+def _desc_of(k_pages, num_q_heads: Optional[int] = None) -> "_lib.CacheDesc":
+    """Descriptor of a pool [num_pages, num_kv_heads, page_size, head_dim]; num_q_heads from the
+    query tensor (default: as many as KV heads, which is all an append needs)."""
     if k_pages.dim() != 4:
         raise ValueError("pools are [num_pages, num_kv_heads, page_size, head_dim]")
     p, hkv, ps, d = k_pages.shape
-    return desc(p, 16, hkv, d, ps)
+    return desc(p, hkv if num_q_heads is None else int(num_q_heads), hkv, d, ps)
 
 
 def _ptr(t) -> Optional[int]:
@@ -99,8 +101,10 @@ def read_status(ws, stream=None) -> int:
     return int(_lib.load().pkv_read_status(ctypes.c_void_p(ws.data_ptr()), _stream(stream)))
 
 
-def decode_workspace_bytes(batch: int, max_pages: int, num_pages: int = 1) -> int:
-    d = desc(num_pages)
+def decode_workspace_bytes(batch: int, max_pages: int, num_pages: int = 1, num_q_heads: int = 16,
+                           num_kv_heads: int = 8, head_dim: int = 128) -> int:
+    """Workspace bytes of a decode call (default geometry: the Qwen3 decoder, 16/8/128)."""
+    d = desc(num_pages, num_q_heads, num_kv_heads, head_dim)
     return int(_lib.load().pkv_decode_workspace_bytes(ctypes.byref(d), int(batch), int(max_pages)))
 
 
@@ -153,7 +157,8 @@ def append(k_new, v_new, slot_mapping, k_pages, v_pages, workspace: Optional[Wor
 
 
 def decode_attn(q, k_pages, v_pages, block_table, seq_lens, out, scale: float, workspace: Workspace, stream=None):
-    """Decode attention: out [B, 16, 128] from q [B, 16, 128] over the paged cache."""
+    """Decode attention: out [B, Hq, D] from q [B, Hq, D] over the paged cache [P, Hkv, 16, D]
+    (Hq / Hkv in 1, 2, 4, 8 and D in 64, 128; 16/8/128 takes the tuned kernel)."""
     import torch
 
     _need(k_pages, torch.bfloat16, "k_pages")
@@ -166,7 +171,7 @@ def decode_attn(q, k_pages, v_pages, block_table, seq_lens, out, scale: float, w
     B = q.shape[0]
     if out.shape != q.shape or block_table.dim() != 2 or block_table.shape[0] != B or seq_lens.numel() != B:
         raise ValueError("shape mismatch")
-    d = _desc_of(k_pages)
+    d = _desc_of(k_pages, q.shape[1])
     ws = workspace.tensor
     rc = _lib.load().pkv_decode_attn(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), _ptr(seq_lens),
                                      _ptr(out), float(scale), _stream(stream), ctypes.byref(d), B,
@@ -234,7 +239,7 @@ def _decode_append(q, k_new, v_new, k_pages, v_pages, block_table, seq_lens, out
     if (out.shape != q.shape or block_table.dim() != 2 or block_table.shape[0] != B or seq_lens.numel() != B
             or k_new.shape[0] != B or v_new.shape != k_new.shape):
         raise ValueError("shape mismatch")
-    d = _desc_of(k_pages)
+    d = _desc_of(k_pages, q.shape[1])
     ws = workspace.tensor
     flags = EARLY_PREFETCH if early_prefetch else 0
     lib = _lib.load()
@@ -267,7 +272,7 @@ def prefill_chunk_attn(q, k_pages, v_pages, block_table, prefix_lens, cu_q_lens,
     S = prefix_lens.numel()
     if cu_q_lens.numel() != S + 1 or block_table.shape[0] != S or out.shape != q.shape:
         raise ValueError("shape mismatch")
-    d = _desc_of(k_pages)
+    d = _desc_of(k_pages, q.shape[1])
     ws = workspace.tensor
     rc = _lib.load().pkv_prefill_chunk_attn(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
                                             _ptr(prefix_lens), _ptr(cu_q_lens), S, q.shape[0], _ptr(out),
@@ -295,7 +300,7 @@ def decode_attn_noalloc(q, k_pages, v_pages, block_table, seq_lens, out, scale: 
     B = q.shape[0]
     if out.shape != q.shape or block_table.dim() != 2 or block_table.shape[0] != B or seq_lens.numel() != B:
         raise ValueError("shape mismatch")
-    d = _desc_of(k_pages)
+    d = _desc_of(k_pages, q.shape[1])
     rc = _lib.load().pkv_decode_attn_noalloc(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
                                              _ptr(seq_lens), _ptr(out), float(scale), _stream(stream),
                                              ctypes.byref(d), B, block_table.shape[1])

@@ -1,6 +1,6 @@
 // pkv_abi.cu -- the extern "C" entry points of libpkv: argument checks on the
 // host, launch-configuration choice, and the status word helpers. All device
-// work is in append.cu, decode.cu and prefill.cu.
+// work is in append.cu, decode.cu, decode_generic.cu and prefill.cu.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -45,12 +45,27 @@ int current_device(int* num_sms) {
   return PKV_OK;
 }
 
+// The geometry every call supports: the Qwen3 decoder's 16 query / 8 KV heads
+// of dimension 128, page size 16 (decode.cu, prefill.cu, the fused calls).
 int check_desc(const pkv_cache_desc* d) {
   if (d == nullptr) return PKV_ERR_NULL_ARG;
   if (d->num_q_heads <= 0 || d->num_kv_heads <= 0 || d->head_dim <= 0 || d->page_size <= 0 || d->num_pages <= 0)
     return PKV_ERR_BAD_SHAPE;
   if (d->num_q_heads != 16 || d->num_kv_heads != 8 || d->head_dim != 128 || d->page_size != 16)
     return PKV_ERR_UNSUPPORTED;
+  return PKV_OK;
+}
+
+// Geometries pkv_append and pkv_decode_attn also serve (decode_generic.cu):
+// page size 16, head_dim 64 or 128, 1, 2, 4 or 8 query heads per KV head.
+// Sets *generic when the call takes the generic decode path.
+int check_desc_decode(const pkv_cache_desc* d, bool* generic) {
+  const int rc = check_desc(d);
+  *generic = false;
+  if (rc != PKV_ERR_UNSUPPORTED) return rc;
+  if (!pkv::decode_generic_supported(d->num_q_heads, d->num_kv_heads, d->head_dim, d->page_size))
+    return PKV_ERR_UNSUPPORTED;
+  *generic = true;
   return PKV_OK;
 }
 
@@ -87,7 +102,9 @@ const char* pkv_status_string(int status) {
     case PKV_OK: return "ok";
     case PKV_ERR_NULL_ARG: return "a required pointer is NULL";
     case PKV_ERR_BAD_SHAPE: return "bad or inconsistent size";
-    case PKV_ERR_UNSUPPORTED: return "unsupported geometry or device (needs 16/8/128/16 on sm_103)";
+    case PKV_ERR_UNSUPPORTED:
+      return "unsupported geometry or device (sm_103; decode and append: page 16, head_dim 64/128, 1/2/4/8 query "
+             "heads per KV head; prefill and fused calls: 16/8/128/16)";
     case PKV_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
     case PKV_ERR_CUDA: return "CUDA runtime or launch error";
     case PKV_ERR_DEVICE_TIMEOUT: return "a device-side wait ran out of time";
@@ -100,7 +117,8 @@ const char* pkv_status_string(int status) {
 int pkv_append(const void* k_new, const void* v_new, const int32_t* slot_mapping, int32_t n_tokens, void* k_pages,
                void* v_pages, const pkv_cache_desc* desc, pkv_stream_t stream, void* workspace,
                size_t workspace_bytes) {
-  int rc = check_desc(desc);
+  bool generic = false;
+  int rc = check_desc_decode(desc, &generic);
   if (rc != PKV_OK) return rc;
   if (n_tokens < 0) return PKV_ERR_BAD_SHAPE;
   if (workspace != nullptr && workspace_bytes < PKV_STATUS_BYTES) return PKV_ERR_WORKSPACE_TOO_SMALL;
@@ -112,22 +130,32 @@ int pkv_append(const void* k_new, const void* v_new, const int32_t* slot_mapping
   rc = current_device(&sms);
   if (rc != PKV_OK) return rc;
   return pkv::launch_append(k_new, v_new, slot_mapping, n_tokens, k_pages, v_pages, desc->num_pages,
-                            static_cast<int*>(workspace), sms, reinterpret_cast<cudaStream_t>(stream));
+                            desc->num_kv_heads, desc->head_dim, static_cast<int*>(workspace), sms,
+                            reinterpret_cast<cudaStream_t>(stream));
+}
+
+// Workspace bytes of a decode call for this geometry (0 if unsupported).
+static size_t decode_ws(const pkv_cache_desc* desc, bool generic, int32_t batch, int32_t max_pages, int sms) {
+  return generic ? pkv::decode_generic_workspace_bytes(desc->num_q_heads, desc->num_kv_heads, desc->head_dim, batch,
+                                                       max_pages, sms)
+                 : pkv::decode_workspace_bytes(batch, sms);
 }
 
 size_t pkv_decode_workspace_bytes(const pkv_cache_desc* desc, int32_t batch, int32_t max_pages_per_seq) {
-  if (check_desc(desc) != PKV_OK || batch < 0 || max_pages_per_seq < 1) return 0;
+  bool generic = false;
+  if (check_desc_decode(desc, &generic) != PKV_OK || batch < 0 || max_pages_per_seq < 1) return 0;
   if (batch > pkv::decode_max_batch() || !table_fits(batch, max_pages_per_seq)) return 0;
   int sms = 0;
   if (current_device(&sms) != PKV_OK) return 0;
-  return pkv::decode_workspace_bytes(batch, sms);
+  return decode_ws(desc, generic, batch, max_pages_per_seq, sms);
 }
 
 int pkv_decode_attn(const void* q, const void* k_pages, const void* v_pages, const int32_t* block_table,
                     const int32_t* seq_lens, void* out, float scale, pkv_stream_t stream,
                     const pkv_cache_desc* desc, int32_t batch, int32_t max_pages_per_seq, void* workspace,
                     size_t workspace_bytes) {
-  int rc = check_desc(desc);
+  bool generic = false;
+  int rc = check_desc_decode(desc, &generic);
   if (rc != PKV_OK) return rc;
   if (batch < 0 || max_pages_per_seq < 1) return PKV_ERR_BAD_SHAPE;
   if (batch > pkv::decode_max_batch()) return PKV_ERR_UNSUPPORTED;
@@ -140,7 +168,11 @@ int pkv_decode_attn(const void* q, const void* k_pages, const void* v_pages, con
   int sms = 0;
   rc = current_device(&sms);
   if (rc != PKV_OK) return rc;
-  if (workspace_bytes < pkv::decode_workspace_bytes(batch, sms)) return PKV_ERR_WORKSPACE_TOO_SMALL;
+  if (workspace_bytes < decode_ws(desc, generic, batch, max_pages_per_seq, sms)) return PKV_ERR_WORKSPACE_TOO_SMALL;
+  if (generic)
+    return pkv::launch_decode_generic(q, k_pages, v_pages, block_table, seq_lens, out, scale, desc->num_q_heads,
+                                      desc->num_kv_heads, desc->head_dim, batch, max_pages_per_seq, desc->num_pages,
+                                      workspace, sms, reinterpret_cast<cudaStream_t>(stream));
   return pkv::launch_decode(q, nullptr, nullptr, k_pages, v_pages, block_table, seq_lens, nullptr, 0, out, scale, batch,
                             max_pages_per_seq, desc->num_pages, workspace, sms, reinterpret_cast<cudaStream_t>(stream),
                             0u);

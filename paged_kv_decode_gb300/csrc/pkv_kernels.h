@@ -7,8 +7,10 @@
 
 namespace pkv {
 
+// Rows of num_kv_heads x head_dim bf16 (head_dim a multiple of 8), page size 16.
 int launch_append(const void* k_new, const void* v_new, const int32_t* slot_mapping, int32_t n_tokens, void* k_pages,
-                  void* v_pages, int32_t num_pages, int* status, int num_sms, cudaStream_t stream);
+                  void* v_pages, int32_t num_pages, int32_t num_kv_heads, int32_t head_dim, int* status, int num_sms,
+                  cudaStream_t stream);
 
 // Decode: workspace = [status header | counters (batch * kv heads) | partials].
 size_t decode_workspace_bytes(int32_t batch, int num_sms);
@@ -20,6 +22,16 @@ int launch_decode(const void* q, const void* k_new, const void* v_new, const voi
                   void* out, float scale, int32_t batch, int32_t max_pages, int32_t num_pages, void* workspace,
                   int num_sms, cudaStream_t stream, uint32_t flags);
 int decode_max_batch();
+
+// Decode for other geometries (decode_generic.cu): page size 16, head_dim 64 or 128,
+// num_q_heads / num_kv_heads in {1, 2, 4, 8}. Workspace = [status | counters | records].
+bool decode_generic_supported(int num_q_heads, int num_kv_heads, int head_dim, int page_size);
+size_t decode_generic_workspace_bytes(int num_q_heads, int num_kv_heads, int head_dim, int32_t batch,
+                                      int32_t max_pages, int num_sms);
+int launch_decode_generic(const void* q, const void* k_pages, const void* v_pages, const int32_t* block_table,
+                          const int32_t* seq_lens, void* out, float scale, int num_q_heads, int num_kv_heads,
+                          int head_dim, int32_t batch, int32_t max_pages, int32_t num_pages, void* workspace,
+                          int num_sms, cudaStream_t stream);
 
 size_t prefill_workspace_bytes(int32_t num_seqs, int32_t max_q_len, int num_sms);
 int prefill_max_seqs();

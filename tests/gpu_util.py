@@ -43,7 +43,9 @@ class DecodeOnDevice:
         self.k_new = None if case.k_new is None else case.k_new[layer].to(device)
         self.v_new = None if case.v_new is None else case.v_new[layer].to(device)
         self.out = torch.empty_like(self.q)
-        nbytes = pkv.decode_workspace_bytes(case.batch, case.max_pages, case.num_pages)
+        g = case.geom
+        nbytes = pkv.decode_workspace_bytes(case.batch, case.max_pages, case.num_pages, g.n_q_heads, g.n_kv_heads,
+                                            g.head_dim)
         assert nbytes > 0
         self.ws = pkv.Workspace(nbytes, device)
 

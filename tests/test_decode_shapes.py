@@ -1,0 +1,129 @@
+"""Decode attention and KV append for cache geometries other than the Qwen3
+decoder's 16/8/128 (the generic decode path), against the fp64 oracle.
+
+The pages name further decoder backbones for the same slot (a Llama-style 2B
+model, Qwen3-8B, OLMo-2-7B, SmolLM2-1.7B) but give no head counts, so the
+geometries here span the supported range instead: 1, 2, 4 and 8 query heads
+per KV head, head_dim 64 and 128, several KV-head counts. Same bar as the
+tuned path (tests/parity.py); exact cases bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_decode_gb300 as pkv
+from gpu_util import DecodeOnDevice, bits, i32
+from parity import assert_close, bf16_to_f64
+from paged_kv_decode_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = {
+    "g4_d128_32q8kv": W.Geometry(32, 8, 128),
+    "g1_d128_32q32kv": W.Geometry(32, 32, 128),
+    "g1_d64_32q32kv": W.Geometry(32, 32, 64),
+    "g2_d64_16q8kv": W.Geometry(16, 8, 64),
+    "g8_d128_64q8kv": W.Geometry(64, 8, 128),
+    "g8_d64_8q1kv": W.Geometry(8, 1, 64),
+    "g2_d128_12q6kv": W.Geometry(12, 6, 128),
+    "g4_d64_16q4kv": W.Geometry(16, 4, 64),
+}
+
+
+def _check(case, dev, what):
+    run = DecodeOnDevice(case, 0, dev)
+    out = run.step()
+    torch.cuda.synchronize()
+    kp, vp = run.pools_cpu()
+    if case.k_new is not None:  # the generic append is bit-exact
+        want_k, want_v = oracle.append(case.k_new[0], case.v_new[0], case.slot_mapping, case.k_pages[0],
+                                       case.v_pages[0])
+        assert np.array_equal(bits(kp), want_k) and np.array_equal(bits(vp), want_v), what
+    want = oracle.decode(case.q[0], bits(kp), bits(vp), case.block_table, case.seq_lens, case.geom.scale)
+    assert_close(bf16_to_f64(out), want, what)
+    assert run.ws.status() == 0
+    return run
+
+
+@pytest.mark.parametrize("shape", sorted(SHAPES))
+def test_batch16_mixed_lengths(cuda_device, shape):
+    geom = SHAPES[shape]
+    case = W.decode_case(21, W.config_seq_lens(2), geom=geom, pending_append=True, poison=True)
+    _check(case, cuda_device, f"{shape} bs16")
+
+
+@pytest.mark.parametrize("shape", ["g4_d128_32q8kv", "g1_d64_32q32kv", "g8_d128_64q8kv"])
+def test_long_context_one_request(cuda_device, shape):
+    case = W.decode_case(22, [40000], geom=SHAPES[shape], pending_append=True, poison=True)
+    _check(case, cuda_device, f"{shape} 40k")
+
+
+@pytest.mark.parametrize("shape", sorted(SHAPES))
+def test_ragged_and_empty_rows(cuda_device, shape):
+    lens = [1, 0, 17, 15, 16, 33, 0, 250, 4095, 3, 30000, 5]
+    case = W.decode_case(23, lens, geom=SHAPES[shape], pending_append=True, poison=True)
+    run = _check(case, cuda_device, f"{shape} ragged")
+    out = run.out.cpu()
+    for b in np.flatnonzero(np.asarray(lens) == 0):
+        assert torch.count_nonzero(out[b].view(torch.int16)).item() == 0
+
+
+@pytest.mark.parametrize("shape", ["g1_d64_32q32kv", "g8_d128_64q8kv"])
+def test_single_cached_token_is_exact(cuda_device, shape):
+    # softmax over one key is 1 and 1 * v rounds back to the same bf16
+    case = W.decode_case(24, [1, 1, 1], geom=SHAPES[shape], pending_append=False, poison=True)
+    run = DecodeOnDevice(case, 0, cuda_device)
+    out = run.step()
+    torch.cuda.synchronize()
+    g = case.geom
+    G = g.n_q_heads // g.n_kv_heads
+    vp = bits(run.v_pages.cpu())
+    for b in range(3):
+        page = int(case.block_table[b, 0])
+        for hq in range(g.n_q_heads):
+            assert np.array_equal(bits(out[b, hq].cpu()), vp[page, hq // G, 0])
+
+
+@pytest.mark.parametrize("shape", ["g4_d128_32q8kv", "g1_d64_32q32kv"])
+def test_graph_replay_and_workspace_reuse(cuda_device, shape):
+    # the split counters return to zero, so replays and repeated calls give the same bits
+    case = W.decode_case(25, [40000, 300, 7000, 1], geom=SHAPES[shape], pending_append=False, poison=True)
+    run = DecodeOnDevice(case, 0, cuda_device)
+    eager = run.step().clone()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        run.step()
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        run.step()
+    for _ in range(3):
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(run.out.view(torch.int16), eager.view(torch.int16))
+    counters = run.ws.tensor[pkv.PKV_STATUS_BYTES:pkv.PKV_STATUS_BYTES + 4 * case.batch * case.geom.n_kv_heads]
+    assert torch.count_nonzero(counters).item() == 0
+    assert run.ws.status() == 0
+
+
+def test_page_id_outside_pool_is_reported(cuda_device):
+    geom = SHAPES["g4_d128_32q8kv"]
+    case = W.decode_case(26, [100, 40], geom=geom, pending_append=False, poison=True)
+    run = DecodeOnDevice(case, 0, cuda_device)
+    bt = case.block_table.copy()
+    bt[1, 0] = case.num_pages + 5
+    run.block_table = i32(bt, cuda_device)
+    run.step()
+    torch.cuda.synchronize()
+    assert run.ws.status() == -7  # PKV_ERR_OUT_OF_BOUNDS
+
+
+def test_fused_and_prefill_calls_reject_other_geometries(cuda_device):
+    geom = SHAPES["g4_d128_32q8kv"]
+    case = W.decode_case(27, [100], geom=geom, pending_append=True, poison=False)
+    run = DecodeOnDevice(case, 0, cuda_device)
+    with pytest.raises(pkv.PkvError, match="UNSUPPORTED"):
+        pkv.decode_append_attn(run.q, run.k_new, run.v_new, run.k_pages, run.v_pages, run.block_table, run.seq_lens,
+                               run.out, geom.scale, run.ws)
