@@ -454,7 +454,8 @@ def measure_prefill(device, bf16_peak, reps=10):
 
 def time_e2e(step, steps, warmup, dist_on):
     """Steps/s through the Python API with host buffers: H2D of q, k_new, v_new, slots, lengths and
-    block table from pinned memory, the graph-captured step, D2H of the attention output, sync."""
+    block table from pinned memory, the step, D2H of the attention output (all in one CUDA graph),
+    then a synchronize, every step."""
     torch = step.torch
     pin = lambda t: t.detach().to("cpu").pin_memory()
     hq, hk, hv = pin(step.q), pin(step.k_new), pin(step.v_new)
@@ -463,15 +464,31 @@ def time_e2e(step, steps, warmup, dist_on):
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hs, hl, hb))
     d2h = hout.numel() * hout.element_size()
 
-    def one():
+    def body():
         step.q.copy_(hq, non_blocking=True)
         step.k_new.copy_(hk, non_blocking=True)
         step.v_new.copy_(hv, non_blocking=True)
         step.slot_mapping.copy_(hs, non_blocking=True)
         step.seq_lens.copy_(hl, non_blocking=True)
         step.block_table.copy_(hb, non_blocking=True)
-        step.graph.replay()
+        step.step_eager()
         hout.copy_(step.out, non_blocking=True)
+
+    # one CUDA graph per step: the host->device copies of the step's inputs from pinned memory,
+    # the layers, and the device->host copy of the output; a replay and a synchronize per step
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        body()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        body()
+    torch.cuda.synchronize()
+
+    def one():
+        g.replay()
         torch.cuda.current_stream().synchronize()
 
     for _ in range(warmup):
