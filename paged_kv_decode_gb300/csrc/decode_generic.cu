@@ -14,17 +14,22 @@
 // Schedule:
 //  * The grid is (splits, KV heads, requests). CTA (s, h, b) takes pages
 //    [s * pps, (s + 1) * pps) of request b, KV head h; pps and the number of
-//    splits come from the host sizes (enough CTAs to fill the GPU twice).
+//    splits come from the host sizes (enough CTAs for two waves).
 //    CTAs past a request's last page exit at once.
-//  * Each of the 4 warps takes every 4th page of the split and keeps a 3-stage
-//    ring of its own: lane 0 issues the page's K and V tiles as 1-D bulk copies
-//    (cp.async.bulk) completing on the stage's mbarrier, three pages ahead.
-//  * Scores: two lanes per token, each over half the row's 16-byte chunks (in
-//    an order rotated by token, so the 32 lanes' reads spread over all shared
-//    memory banks), for all G query heads of the group from one K read; the
-//    query rows sit in shared memory as fp32, pre-scaled by scale * log2(e).
-//    Online softmax in the log2 domain with tokens past seq_len masked.
-//    Values: each lane owns head_dim / 32 dims of every head.
+//  * Each of the 4 warps takes every 4th page of the split and keeps a ring of
+//    its own (2 stages for head_dim 128, 3 for 64: three CTAs fit an SM): lane 0
+//    issues the page's K and V tiles as 1-D bulk copies (cp.async.bulk)
+//    completing on the stage's mbarrier, a ring's depth of pages ahead.
+//  * Scores: kL = G * head_dim / 64 lanes per token (at least 2), so that each
+//    lane keeps its slice of the G query rows (64 floats, pre-scaled by
+//    scale * log2(e)) in registers; packed fp32 FMAs over the lane's 16-byte
+//    chunks of the key row (in an order rotated by token, so the 32 lanes' reads
+//    spread over all shared memory banks), for all G heads from one K read. A
+//    transpose-reduce over the kL lanes (halve the heads each round, then sum
+//    the copies) leaves each lane the full score of one (token, head). Online
+//    softmax in the log2 domain with tokens past seq_len masked; p and the
+//    rescale factors go through shared memory. Values: each lane owns
+//    head_dim / 32 dims of every head.
 //  * The warps' states are merged in shared memory. A request whose pages fit
 //    one split writes the bf16 output; otherwise each split writes an fp32
 //    record (o, m, l per head), counts itself in (fence, atomic), and the CTA
@@ -40,25 +45,33 @@ namespace {
 
 constexpr int kGenWarps = 4;
 constexpr int kGenThreads = kGenWarps * 32;
-constexpr int kGenStages = 3;
 constexpr unsigned kGenFull = 0xffffffffu;
 
 template <int G, int D>
 struct Gen {
   static constexpr int kTile = kPageSize * D * 2;  // one (page, KV head) K or V tile
   static constexpr int kStage = 2 * kTile;
-  static constexpr int kRing = kGenStages * kStage;  // per warp
+  static constexpr int kStages = D == 128 ? 2 : 3;   // per warp: 3 CTAs of 4 warps per SM either way
+  static constexpr int kRing = kStages * kStage;     // per warp
   static constexpr int kChunks = D / 8;              // 16-byte chunks of a row
-  static constexpr int kLaneChunks = kChunks / 2;    // per lane (two lanes per token)
+  // Score pass: kL lanes per token, so that a lane's slice of the G query rows is
+  // 64 floats (kL = G * D / 64, at least 2); kTP tokens per pass, kNP passes per
+  // page, kCH 16-byte chunks of the row per lane. kL >= G always.
+  static constexpr int kL = G * D / 64 < 2 ? 2 : G * D / 64;
+  static constexpr int kTP = 32 / kL;
+  static constexpr int kNP = kPageSize / kTP;
+  static constexpr int kCH = kChunks / kL;
+  static constexpr int kDup = kL / G;                // lanes of a token holding the same head's score
+  static_assert(kCH >= 1 && kNP >= 1 && kDup >= 1, "score pass layout");
   static constexpr int kLaneDims = D / 32;           // value dims per lane
   static constexpr int kRec = D + 2;                 // floats per head in a record: o[D], m, l
   static constexpr int kState = G * kRec;            // a warp's or a split's (o, m, l) of all G heads
   static_assert(kState * 4 <= kRing, "a warp's state fits its drained ring");
   // shared memory: rings | full barriers | q (fp32) | p buffers | flags | page ids
   static constexpr int kOffBars = kGenWarps * kRing;
-  static constexpr int kOffQ = kOffBars + kGenWarps * kGenStages * 8;
+  static constexpr int kOffQ = kOffBars + kGenWarps * kStages * 8;
   static constexpr int kOffP = kOffQ + G * D * 4;
-  static constexpr int kOffFlag = kOffP + kGenWarps * kPageSize * G * 4;
+  static constexpr int kOffFlag = kOffP + kGenWarps * (kPageSize + 1) * G * 8;
   static constexpr int kOffIds = kOffFlag + 16;
   static size_t smem_bytes(int pps) { return kOffIds + static_cast<size_t>(pps) * 4; }
 };
@@ -116,7 +129,7 @@ __global__ void __launch_bounds__(kGenThreads) decode_generic_kernel(const GenAr
   const int p0 = s * a.pps;
   const int p1 = p0 + a.pps < np ? p0 + a.pps : np;
 
-  if (tid < kGenWarps * kGenStages) mbar_init(&full[tid], 1);
+  if (tid < kGenWarps * S::kStages) mbar_init(&full[tid], 1);
   if (tid == 0) flag[0] = 0;
   for (int i = tid; i < G * D; i += kGenThreads)
     qs[i] = __bfloat162float(a.q[(static_cast<size_t>(b) * nq + hq0) * D + i]) * a.qscale;
@@ -134,32 +147,49 @@ __global__ void __launch_bounds__(kGenThreads) decode_generic_kernel(const GenAr
   // ---- this warp's pages: p0 + warp, p0 + warp + 4, ...
   const int nw = p1 - p0 > warp ? (p1 - p0 - warp + kGenWarps - 1) / kGenWarps : 0;
   unsigned char* ring = smem + warp * S::kRing;
-  uint64_t* wfull = full + warp * kGenStages;
-  auto issue = [&](int i) {  // lane 0: page i of this warp into stage i % kGenStages
+  uint64_t* wfull = full + warp * S::kStages;
+  auto issue = [&](int i) {  // lane 0: page i of this warp into stage i % S::kStages
     const int id = ids[warp + i * kGenWarps];
     const size_t off = (static_cast<size_t>(id) * a.hkv + h) * (S::kTile / 2);
-    unsigned char* dst = ring + (i % kGenStages) * S::kStage;
-    mbar_arrive_expect_tx(&wfull[i % kGenStages], S::kStage);
-    bulk_g2s(dst, a.k_pages + off, S::kTile, &wfull[i % kGenStages]);
-    bulk_g2s(dst + S::kTile, a.v_pages + off, S::kTile, &wfull[i % kGenStages]);
+    unsigned char* dst = ring + (i % S::kStages) * S::kStage;
+    mbar_arrive_expect_tx(&wfull[i % S::kStages], S::kStage);
+    bulk_g2s(dst, a.k_pages + off, S::kTile, &wfull[i % S::kStages]);
+    bulk_g2s(dst + S::kTile, a.v_pages + off, S::kTile, &wfull[i % S::kStages]);
   };
   if (lane == 0)
-    for (int i = 0; i < kGenStages && i < nw; ++i) issue(i);
+    for (int i = 0; i < S::kStages && i < nw; ++i) issue(i);
 
-  const int t = lane >> 1, half = lane & 1;
-  float* pb = reinterpret_cast<float*>(smem + S::kOffP) + warp * kPageSize * G;  // [token][head]
-  float mrun[G], lrun[G], o[G][S::kLaneDims];
+  // score-pass position of this lane: token slot i of a pass, part sp of the row
+  const int i = lane / S::kL, sp = lane % S::kL;
+  const int h_own = sp / S::kDup;  // head whose scores this lane holds after the reduce
+  // the lane's query chunks (rotated by token slot, so that the 32 lanes' K reads
+  // spread over all banks): chunk (k) = sp + kL * ((k + i) mod kCH), both as fp32 pairs
+  float2 q2[S::kCH][4][G];
 #pragma unroll
-  for (int g = 0; g < G; ++g) {
-    mrun[g] = -CUDART_INF_F;
-    lrun[g] = 0.f;
+  for (int k = 0; k < S::kCH; ++k) {
+    const int c = sp + S::kL * ((k + i) % S::kCH);
 #pragma unroll
-    for (int k = 0; k < S::kLaneDims; ++k) o[g][k] = 0.f;
+    for (int g = 0; g < G; ++g) {
+      const float4 qa = *reinterpret_cast<const float4*>(qs + g * D + c * 8);
+      const float4 qb = *reinterpret_cast<const float4*>(qs + g * D + c * 8 + 4);
+      q2[k][0][g] = make_float2(qa.x, qa.y);
+      q2[k][1][g] = make_float2(qa.z, qa.w);
+      q2[k][2][g] = make_float2(qb.x, qb.y);
+      q2[k][3][g] = make_float2(qb.z, qb.w);
+    }
   }
+  // p of every (token, head) as the pair (p, p), then every head's rescale factor
+  float2* pb = reinterpret_cast<float2*>(smem + S::kOffP) + warp * (kPageSize + 1) * G;
+  float mrun = -CUDART_INF_F, lrun = 0.f;  // of head h_own
+  float2 o[G][S::kLaneDims / 2];  // dims lane * kLaneDims .., in pairs
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+#pragma unroll
+    for (int k = 0; k < S::kLaneDims / 2; ++k) o[g][k] = make_float2(0.f, 0.f);
   bool failed = false;
-  for (int i = 0; i < nw && !failed; ++i) {
-    const int st = i % kGenStages;
-    const bool ok = mbar_wait_bounded(&wfull[st], static_cast<uint32_t>(i / kGenStages) & 1u);
+  for (int it = 0; it < nw && !failed; ++it) {
+    const int st = it % S::kStages;
+    const bool ok = mbar_wait_bounded(&wfull[st], static_cast<uint32_t>(it / S::kStages) & 1u);
     failed = __any_sync(kGenFull, !ok);
     if (failed) {
       if (lane == 0) {
@@ -168,90 +198,116 @@ __global__ void __launch_bounds__(kGenThreads) decode_generic_kernel(const GenAr
       }
       break;
     }
-    const int page = p0 + warp + i * kGenWarps;
+    const int page = p0 + warp + it * kGenWarps;
     const int rem = sl - page * kPageSize;
     const int n_valid = rem < kPageSize ? rem : kPageSize;
     const unsigned char* kt = ring + st * S::kStage;
     const unsigned char* vt = kt + S::kTile;
-    // scores of token t for the G heads, from half of the row's chunks
-    float acc[G];
+    // ---- scores: pass ps covers tokens ps * kTP .. ; each lane ends with the score
+    // of (token ps * kTP + i, head h_own) after a transpose-reduce over its kL lanes
+    float sc[S::kNP];
 #pragma unroll
-    for (int g = 0; g < G; ++g) acc[g] = 0.f;
+    for (int ps = 0; ps < S::kNP; ++ps) {
+      const int tok = ps * S::kTP + i;
+      float2 acc[G];
 #pragma unroll
-    for (int j = 0; j < S::kLaneChunks; ++j) {
-      const int c = 2 * ((j + t) % S::kLaneChunks) + half;
-      const uint4 u = *reinterpret_cast<const uint4*>(kt + t * (D * 2) + c * 16);
-      const float2 k0 = bf2_to_f2(u.x), k1 = bf2_to_f2(u.y), k2 = bf2_to_f2(u.z), k3 = bf2_to_f2(u.w);
+      for (int g = 0; g < G; ++g) acc[g] = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float4 qa = *reinterpret_cast<const float4*>(qs + g * D + c * 8);
-        const float4 qb = *reinterpret_cast<const float4*>(qs + g * D + c * 8 + 4);
-        acc[g] = fmaf(qa.x, k0.x, acc[g]);
-        acc[g] = fmaf(qa.y, k0.y, acc[g]);
-        acc[g] = fmaf(qa.z, k1.x, acc[g]);
-        acc[g] = fmaf(qa.w, k1.y, acc[g]);
-        acc[g] = fmaf(qb.x, k2.x, acc[g]);
-        acc[g] = fmaf(qb.y, k2.y, acc[g]);
-        acc[g] = fmaf(qb.z, k3.x, acc[g]);
-        acc[g] = fmaf(qb.w, k3.y, acc[g]);
+      for (int k = 0; k < S::kCH; ++k) {
+        const int c = sp + S::kL * ((k + i) % S::kCH);
+        const uint4 u = *reinterpret_cast<const uint4*>(kt + tok * (D * 2) + c * 16);
+        const float2 k0 = bf2_to_f2(u.x), k1 = bf2_to_f2(u.y), k2 = bf2_to_f2(u.z), k3 = bf2_to_f2(u.w);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          acc[g] = __ffma2_rn(q2[k][0][g], k0, acc[g]);
+          acc[g] = __ffma2_rn(q2[k][1][g], k1, acc[g]);
+          acc[g] = __ffma2_rn(q2[k][2][g], k2, acc[g]);
+          acc[g] = __ffma2_rn(q2[k][3][g], k3, acc[g]);
+        }
       }
+      float v[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) v[g] = acc[g].x + acc[g].y;
+      // halving rounds (masks kL/2, kL/4, .. down to kDup): keep one half of the heads,
+      // send the other to the partner; then sum the kDup copies of the last one
+#pragma unroll
+      for (int r = 0; (G >> r) > 1; ++r) {
+        const int m = S::kL >> (r + 1), n = G >> r;
+        const bool up = (sp & m) != 0;
+#pragma unroll
+        for (int j = 0; j < n / 2; ++j) {
+          const float send = up ? v[j] : v[j + n / 2];
+          const float keep = up ? v[j + n / 2] : v[j];
+          v[j] = keep + __shfl_xor_sync(kGenFull, send, m);
+        }
+      }
+#pragma unroll
+      for (int m = S::kDup / 2; m >= 1; m >>= 1) v[0] += __shfl_xor_sync(kGenFull, v[0], m);
+      sc[ps] = tok < n_valid ? v[0] : -CUDART_INF_F;
     }
-    float alpha[G];
+    // ---- online softmax of head h_own over the page's tokens (passes, then token slots)
+    float mx = sc[0];
+#pragma unroll
+    for (int ps = 1; ps < S::kNP; ++ps) mx = fmaxf(mx, sc[ps]);
+#pragma unroll
+    for (int m = S::kL; m < 32; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kGenFull, mx, m));
+    const float mnew = fmaxf(mrun, mx);
+    const float alpha = ex2(mrun - mnew);
+    float psum = 0.f;
+#pragma unroll
+    for (int ps = 0; ps < S::kNP; ++ps) {
+      const float p = ex2(sc[ps] - mnew);
+      psum += p;
+      if (sp % S::kDup == 0) pb[(ps * S::kTP + i) * G + h_own] = make_float2(p, p);
+    }
+#pragma unroll
+    for (int m = S::kL; m < 32; m <<= 1) psum += __shfl_xor_sync(kGenFull, psum, m);
+    lrun = lrun * alpha + psum;
+    mrun = mnew;
+    if (i == 0 && sp % S::kDup == 0) pb[kPageSize * G + h_own] = make_float2(alpha, alpha);
+    __syncwarp();
+    // ---- values: lane owns dims lane * kLaneDims .. of every head (packed pairs)
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-      float sc = acc[g] + __shfl_xor_sync(kGenFull, acc[g], 1);
-      if (t >= n_valid) sc = -CUDART_INF_F;
-      float mx = sc;
+      const float2 al = pb[kPageSize * G + g];
 #pragma unroll
-      for (int x = 2; x < 32; x <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kGenFull, mx, x));
-      const float mnew = fmaxf(mrun[g], mx);
-      alpha[g] = ex2(mrun[g] - mnew);
-      const float p = ex2(sc - mnew);
-      float ps = p;
-#pragma unroll
-      for (int x = 2; x < 32; x <<= 1) ps += __shfl_xor_sync(kGenFull, ps, x);
-      lrun[g] = lrun[g] * alpha[g] + ps;
-      mrun[g] = mnew;
-      if (half == 0) pb[t * G + g] = p;
+      for (int k = 0; k < S::kLaneDims / 2; ++k) o[g][k] = __fmul2_rn(o[g][k], al);
     }
-    __syncwarp();
-    // values: lane owns dims lane * kLaneDims .. of every head
 #pragma unroll
-    for (int g = 0; g < G; ++g)
+    for (int tt = 0; tt < kPageSize; ++tt) {
+      if (tt < n_valid) {
+        float2 vv[S::kLaneDims / 2];
+        if constexpr (S::kLaneDims == 4) {
+          const uint2 u = *reinterpret_cast<const uint2*>(vt + tt * (D * 2) + lane * 8);
+          vv[0] = bf2_to_f2(u.x);
+          vv[1] = bf2_to_f2(u.y);
+        } else {
+          vv[0] = bf2_to_f2(*reinterpret_cast<const uint32_t*>(vt + tt * (D * 2) + lane * 4));
+        }
 #pragma unroll
-      for (int k = 0; k < S::kLaneDims; ++k) o[g][k] *= alpha[g];
-    for (int tt = 0; tt < n_valid; ++tt) {
-      float v[S::kLaneDims];
-      if constexpr (S::kLaneDims == 4) {
-        const uint2 u = *reinterpret_cast<const uint2*>(vt + tt * (D * 2) + lane * 8);
-        const float2 a0 = bf2_to_f2(u.x), a1 = bf2_to_f2(u.y);
-        v[0] = a0.x, v[1] = a0.y, v[2] = a1.x, v[3] = a1.y;
-      } else {
-        const uint32_t u = *reinterpret_cast<const uint32_t*>(vt + tt * (D * 2) + lane * 4);
-        const float2 a0 = bf2_to_f2(u);
-        v[0] = a0.x, v[1] = a0.y;
-      }
+        for (int g = 0; g < G; ++g) {
+          const float2 p = pb[tt * G + g];
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float p = pb[tt * G + g];
-#pragma unroll
-        for (int k = 0; k < S::kLaneDims; ++k) o[g][k] = fmaf(p, v[k], o[g][k]);
+          for (int k = 0; k < S::kLaneDims / 2; ++k) o[g][k] = __ffma2_rn(p, vv[k], o[g][k]);
+        }
       }
     }
     __syncwarp();  // the stage and the p buffer are free again
-    if (lane == 0 && i + kGenStages < nw) issue(i + kGenStages);
+    if (lane == 0 && it + S::kStages < nw) issue(it + S::kStages);
   }
 
   // ---- CTA merge of the warp states (each in its own drained ring)
   float* wst = reinterpret_cast<float*>(ring);
 #pragma unroll
-  for (int g = 0; g < G; ++g) {
+  for (int g = 0; g < G; ++g)
 #pragma unroll
-    for (int k = 0; k < S::kLaneDims; ++k) wst[g * S::kRec + lane * S::kLaneDims + k] = o[g][k];
-    if (lane == 0) {
-      wst[g * S::kRec + D] = mrun[g];
-      wst[g * S::kRec + D + 1] = lrun[g];
+    for (int k = 0; k < S::kLaneDims / 2; ++k) {
+      wst[g * S::kRec + lane * S::kLaneDims + 2 * k] = o[g][k].x;
+      wst[g * S::kRec + lane * S::kLaneDims + 2 * k + 1] = o[g][k].y;
     }
+  if (i == 0 && sp % S::kDup == 0) {  // one lane per head holds its m and l
+    wst[h_own * S::kRec + D] = mrun;
+    wst[h_own * S::kRec + D + 1] = lrun;
   }
   __syncthreads();
   if (flag[0] != 0) return;  // a wait failed: copies may still land, write nothing
@@ -311,15 +367,17 @@ __global__ void __launch_bounds__(kGenThreads) decode_generic_kernel(const GenAr
 }
 
 // Splits per (request, KV head) and pages per split for the host sizes: enough
-// CTAs to fill the GPU twice at the resident CTAs per SM the shape allows.
+// CTAs to fill the GPU twice at the resident CTAs per SM the shape allows, with
+// splits of at least 8 pages.
 template <int G, int D>
 void plan(int batch, int hkv, int max_pages, int num_sms, int& splits, int& pps) {
   const size_t per_sm = 227 * 1024;
   const int resident = static_cast<int>(per_sm / (Gen<G, D>::smem_bytes(1) + 1024));
+  // two waves of CTAs, splits of at least 8 pages (fewer records for short requests)
   const long long want = 2LL * num_sms * (resident > 0 ? resident : 1);
   const long long pairs = static_cast<long long>(batch) * hkv;
   long long sp = (want + pairs - 1) / pairs;
-  if (sp > max_pages) sp = max_pages;
+  if (sp > (max_pages + 7) / 8) sp = (max_pages + 7) / 8;
   if (sp < 1) sp = 1;
   pps = static_cast<int>((max_pages + sp - 1) / sp);
   splits = (max_pages + pps - 1) / pps;
