@@ -30,8 +30,13 @@
  *  - block_table: int32 [rows][max_pages_per_seq]; entries past a request's
  *    last page are never read.
  *
- * Supported geometry: num_q_heads = 16, num_kv_heads = 8, head_dim = 128,
- * page_size = 16 (other values return PKV_ERR_UNSUPPORTED).
+ * Supported geometry:
+ *  - Every call: num_q_heads = 16, num_kv_heads = 8, head_dim = 128,
+ *    page_size = 16 (the Qwen3 decoder; the tuned kernels).
+ *  - pkv_append and pkv_decode_attn also take page_size = 16, head_dim 64 or
+ *    128, any num_kv_heads and num_q_heads = G * num_kv_heads with G in
+ *    {1, 2, 4, 8} (other decoder backbones; a generic split-KV kernel).
+ *  - Anything else returns PKV_ERR_UNSUPPORTED.
  *
  * Conventions for every entry point:
  *  - Every pointer argument except `desc` is DEVICE memory owned by the
@@ -73,9 +78,9 @@ struct CUstream_st;
 typedef struct CUstream_st* pkv_stream_t;
 
 typedef struct pkv_cache_desc {
-  int32_t num_q_heads;  /* query heads (16) */
+  int32_t num_q_heads;  /* query heads (16; see "Supported geometry") */
   int32_t num_kv_heads; /* KV heads (8) */
-  int32_t head_dim;     /* 128 */
+  int32_t head_dim;     /* 128 (or 64) */
   int32_t page_size;    /* tokens per page (16) */
   int32_t num_pages;    /* pages in each of k_pages / v_pages */
 } pkv_cache_desc;
@@ -84,7 +89,7 @@ enum {
   PKV_OK = 0,
   PKV_ERR_NULL_ARG = -1,            /* a required pointer is NULL */
   PKV_ERR_BAD_SHAPE = -2,           /* a size is negative, zero where it may not be, or inconsistent */
-  PKV_ERR_UNSUPPORTED = -3,         /* geometry other than 16/8/128/16, or no sm_103 device */
+  PKV_ERR_UNSUPPORTED = -3,         /* geometry the call does not serve, or no sm_103 device */
   PKV_ERR_WORKSPACE_TOO_SMALL = -4, /* workspace_bytes below the matching *_workspace_bytes() */
   PKV_ERR_CUDA = -5,                /* a CUDA runtime call or the launch failed */
   PKV_ERR_DEVICE_TIMEOUT = -6,      /* device: a bounded wait for a copy ran out (status word only) */
