@@ -824,9 +824,10 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
 
     // Polled merge (log-sum-exp) of the pair of this CTA's first piece over the
     // records of its n holders. Warp w folds records t = w, w + kCons, ... in that
-    // order, four at a time, each lane owning dims 4 lane .. 4 lane + 3 of both
-    // heads; a record is read again until every word carries the tag. The order
-    // depends only on the pair, so the result is the same bits on every call.
+    // order, with up to kMergeBatch of them loaded at a time, each lane owning dims
+    // 4 lane .. 4 lane + 3 of both heads (lanes 0..7 also load the m/l words); a
+    // record is read again until every word carries the tag. The order depends
+    // only on the pair, so the result is the same bits on every call.
     int cf = 0, n = 0;
     bool two = false;
     span_of(mb, mh, cf, n, two);
@@ -938,7 +939,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
       const int old1 = npend > 1 ? atomicAdd(a.counters + pb1 * kKVHeads + ph1, 1) : -1;
       __threadfence();
       flag[0] = old0 == pn0 - 1 ? 1 : 0;
-      flag[1] = old1 == pn1 - 1 ? 1 : 0;
+      flag[1] = npend > 1 && old1 == pn1 - 1 ? 1 : 0;
     }
     consumer_sync();
     if (flag[2] != 0) {  // a wait failed: copies may still land in the ring, merge nothing
