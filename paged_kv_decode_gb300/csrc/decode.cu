@@ -84,6 +84,7 @@ constexpr int kRec = kHeadDim + 4;           // floats per query-head record: m,
 constexpr int kPieceFloats = kGroup * kRec;  // a partial record of one piece (both query heads)
 constexpr int kMaxDecodeBatch = 1024;
 constexpr int kMaxGrid = 2048;               // partial-record slots are sized for this many CTAs
+constexpr int kMinShare = 8;                 // pages a CTA's share holds at least (when the step has that many)
 constexpr unsigned kFull = 0xffffffffu;
 
 constexpr int kSmemRing = kStages * kStageBytes;
@@ -313,11 +314,13 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
   fence_barrier_init();
   __syncthreads();
 
-  // Only min(gridDim.x, T) CTAs take a share, so that every share is non-empty
-  // and the CTAs between the first and last holder of a (request, KV head) all
-  // hold a piece of it.
+  // Only min(gridDim.x, T / 8) CTAs (at least one) take a share, so that every
+  // share holds at least 8 pages (a tiny step is not spread so thin that its
+  // merges dominate) and the CTAs between the first and last holder of a
+  // (request, KV head) all hold a piece of it.
   const long long T = pref[batch];
-  const int G = static_cast<int>(T < gridDim.x ? T : gridDim.x);
+  const long long g_want = T / kMinShare > 0 ? T / kMinShare : 1;
+  const int G = static_cast<int>(g_want < gridDim.x ? g_want : gridDim.x);
   // zero output rows of empty requests (graph-bucket padding): CTA c clears rows
   // c, c + gridDim.x, ...; in early mode only after the grid dependency
   auto zero_empty_rows = [&](int first_thread, int nthreads) {

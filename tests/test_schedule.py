@@ -6,7 +6,7 @@ never waits on a stage more than one barrier phase ahead.
 The model of one CTA of the persistent decode kernel (4 consumer warps, a
 3-stage ring each, 32-lane producer warp):
 - the CTA's share [lo, hi) of the flattened (request, KV head, page) list, with
-  lo(c) = c * T // G over G = min(grid, T) CTAs;
+  lo(c) = c * T // G over G = min(grid, max(1, T // 8)) CTAs;
 - the share is cut into pieces at (request, KV head) boundaries; the consumers
   meet at the end of every piece (a CTA barrier) before any starts the next;
 - page f goes to consumer assign(f); each consumer takes its pages in order,
@@ -28,7 +28,7 @@ def shares(seq_lens, grid):
     pages = [(int(s) + PAGE - 1) // PAGE for s in seq_lens]
     pref = np.concatenate([[0], np.cumsum([p * HKV for p in pages])]).astype(np.int64)
     T = int(pref[-1])
-    G = min(grid, T)
+    G = min(grid, max(1, T // 8))  # shares of at least 8 pages
     seg_starts = sorted({int(pref[b]) + h * pages[b] for b in range(len(pages)) if pages[b] for h in range(HKV)})
     return [(c * T // G, (c + 1) * T // G) for c in range(G)], seg_starts
 
