@@ -105,7 +105,7 @@ constexpr int kSplitWords = kGroup * kHeadDim + 8;         // tagged words of a 
 constexpr int kSplitBytes = kSplitWords * 4;
 constexpr uint32_t kTag = 0xa5u;                           // low byte of a word written by this call
 constexpr int kMergeBatch = 8;                             // records a warp has in flight in a polled merge
-constexpr int kPollMax = 8;                                // polled merge up to this many holders per pair
+constexpr int kPollMax = 24;                               // polled merge up to this many holders per pair
 static_assert(kSplitBytes % 16 == 0, "16-byte loads and clears of a record");
 static_assert((kSmemRing + kSmemBars) % 16 == 0 && kSmemMerge % 16 == 0 && kPieceBytes % 16 == 0, "alignment");
 static_assert(kQBufBytes == 32 * 16, "one 16-byte chunk of a group's query rows per lane");
