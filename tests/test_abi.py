@@ -70,6 +70,10 @@ def test_host_argument_checks(lib):
     # a workspace smaller than the status header
     ws = ctypes.create_string_buffer(64)
     assert lib.pkv_append(None, None, None, 0, None, None, ctypes.byref(d), None, ws, 64) == -4
+    # more requests than one decode launch takes
+    assert lib.pkv_decode_attn(None, None, None, None, None, None, 1.0, None, ctypes.byref(d), 1025, 1, None,
+                               0) == -3
+    assert lib.pkv_decode_workspace_bytes(ctypes.byref(d), 1025, 1) == 0
     # workspace queries refuse bad arguments
     assert lib.pkv_decode_workspace_bytes(None, 1, 1) == 0
     assert lib.pkv_decode_workspace_bytes(ctypes.byref(d), -1, 1) == 0

@@ -72,6 +72,14 @@ def test_ragged_lengths(cuda_device, lens):
     _check_case(case, cuda_device, what=f"ragged {lens[:4]}")
 
 
+def test_maximum_batch(cuda_device):
+    # 1024 requests (the kernel's limit): every CTA holds many whole pieces, and
+    # empty rows, one-token rows and long rows mix
+    lens = np.random.default_rng(17).choice([0, 1, 17, 300, 2000], size=1024)
+    case = W.decode_case(17, lens, pending_append=True, poison=True)
+    _check_case(case, cuda_device, what="batch 1024")
+
+
 def test_graph_bucket_padding_rows_are_zero(cuda_device):
     lens = [700, 0, 33, 0, 0, 1, 2900, 0]
     case = W.decode_case(7, lens, pending_append=True, poison=True)
