@@ -34,8 +34,8 @@
  *  - Every call: num_q_heads = 16, num_kv_heads = 8, head_dim = 128,
  *    page_size = 16 (the Qwen3 decoder; the tuned kernels).
  *  - pkv_append and pkv_decode_attn also take page_size = 16, head_dim 64 or
- *    128, any num_kv_heads and num_q_heads = G * num_kv_heads with G in
- *    {1, 2, 4, 8} (other decoder backbones; a generic split-KV kernel).
+ *    128, any num_kv_heads and num_q_heads = G * num_kv_heads with G from 1
+ *    to 8 (other decoder backbones; a generic split-KV kernel).
  *  - Anything else returns PKV_ERR_UNSUPPORTED.
  *
  * Conventions for every entry point:

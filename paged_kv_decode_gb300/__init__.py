@@ -158,7 +158,7 @@ def append(k_new, v_new, slot_mapping, k_pages, v_pages, workspace: Optional[Wor
 
 def decode_attn(q, k_pages, v_pages, block_table, seq_lens, out, scale: float, workspace: Workspace, stream=None):
     """Decode attention: out [B, Hq, D] from q [B, Hq, D] over the paged cache [P, Hkv, 16, D]
-    (Hq / Hkv in 1, 2, 4, 8 and D in 64, 128; 16/8/128 takes the tuned kernel)."""
+    (Hq / Hkv from 1 to 8 and D in 64, 128; 16/8/128 takes the tuned kernel)."""
     import torch
 
     _need(k_pages, torch.bfloat16, "k_pages")

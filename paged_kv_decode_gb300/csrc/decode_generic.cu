@@ -1,7 +1,9 @@
 // decode_generic.cu -- decode attention for cache geometries other than the
 // Qwen3 decoder's 16 query / 8 KV heads of dimension 128 (decode.cu serves that
-// one): G = num_q_heads / num_kv_heads query heads per KV head with G in
-// {1, 2, 4, 8}, head_dim 64 or 128, any number of KV heads, page size 16.
+// one): G = num_q_heads / num_kv_heads query heads per KV head with G from 1 to
+// 8, head_dim 64 or 128, any number of KV heads, page size 16. A group of 3, 5,
+// 6 or 7 heads runs in the kernel for 4 or 8 with the extra query rows zero and
+// their outputs not written.
 //
 // The operation is the one of decode.cu (PagedAttention decoding, "FunASR vLLM
 // Inference Engine Guide", section 2): for every request and query head, the
@@ -87,6 +89,7 @@ struct GenArgs {
   int max_pages;
   int num_pages;
   int hkv;
+  int gq;      // query heads per KV head (<= G; the rest of the G are padding)
   int pps;     // pages per split
   int splits;  // splits per (request, KV head) in the records
   int* status;
@@ -105,8 +108,8 @@ __global__ void __launch_bounds__(kGenThreads) decode_generic_kernel(const GenAr
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int hq0 = h * G;  // first query head of the group
-  const int nq = a.hkv * G;
+  const int hq0 = h * a.gq;  // first query head of the group
+  const int nq = a.hkv * a.gq;
 
   grid_dependency_wait();
   allow_dependents();
@@ -120,7 +123,7 @@ __global__ void __launch_bounds__(kGenThreads) decode_generic_kernel(const GenAr
   __nv_bfloat16* orow = a.out + (static_cast<size_t>(b) * nq + hq0) * D;
   if (sl == 0) {  // an empty request (graph-bucket padding): zero rows
     if (s == 0)
-      for (int i = tid; i < G * D; i += kGenThreads) orow[i] = __float2bfloat16_rn(0.f);
+      for (int i = tid; i < a.gq * D; i += kGenThreads) orow[i] = __float2bfloat16_rn(0.f);
     return;
   }
   const int np = (sl + kPageSize - 1) / kPageSize;
@@ -131,8 +134,8 @@ __global__ void __launch_bounds__(kGenThreads) decode_generic_kernel(const GenAr
 
   if (tid < kGenWarps * S::kStages) mbar_init(&full[tid], 1);
   if (tid == 0) flag[0] = 0;
-  for (int i = tid; i < G * D; i += kGenThreads)
-    qs[i] = __bfloat162float(a.q[(static_cast<size_t>(b) * nq + hq0) * D + i]) * a.qscale;
+  for (int i = tid; i < G * D; i += kGenThreads)  // padding heads (i / D >= gq) get zero rows
+    qs[i] = i < a.gq * D ? __bfloat162float(a.q[(static_cast<size_t>(b) * nq + hq0) * D + i]) * a.qscale : 0.f;
   for (int p = p0 + tid; p < p1; p += kGenThreads) {
     int id = __ldg(a.block_table + static_cast<size_t>(b) * a.max_pages + p);
     if (id < 0 || id >= a.num_pages) {
@@ -328,7 +331,7 @@ __global__ void __launch_bounds__(kGenThreads) decode_generic_kernel(const GenAr
       if (d < D) acc += r[d] * sc;
     }
     if (whole) {
-      if (d < D) orow[g * D + d] = __float2bfloat16_rn(acc / l);
+      if (d < D && g < a.gq) orow[g * D + d] = __float2bfloat16_rn(acc / l);
     } else if (d < D) {
       rec[g * S::kRec + d] = acc;
     } else {
@@ -350,7 +353,7 @@ __global__ void __launch_bounds__(kGenThreads) decode_generic_kernel(const GenAr
   __syncthreads();
   if (!flag[1]) return;
   const float* recs = a.records + (static_cast<size_t>(b) * a.hkv + h) * a.splits * S::kState;
-  for (int e = tid; e < G * D; e += kGenThreads) {
+  for (int e = tid; e < a.gq * D; e += kGenThreads) {
     const int g = e / D, d = e % D;
     float m = -CUDART_INF_F;
     for (int r = 0; r < nsplit; ++r) m = fmaxf(m, recs[r * S::kState + g * S::kRec + D]);
@@ -395,8 +398,8 @@ size_t gen_workspace(int batch, int hkv, int max_pages, int num_sms) {
 
 template <int G, int D>
 int gen_launch(const void* q, const void* k_pages, const void* v_pages, const int32_t* block_table,
-               const int32_t* seq_lens, void* out, float scale, int batch, int hkv, int max_pages, int num_pages,
-               void* workspace, int num_sms, cudaStream_t stream) {
+               const int32_t* seq_lens, void* out, float scale, int batch, int hkv, int gq, int max_pages,
+               int num_pages, void* workspace, int num_sms, cudaStream_t stream) {
   int splits = 1, pps = 1;
   plan<G, D>(batch, hkv, max_pages, num_sms, splits, pps);
   const size_t smem = Gen<G, D>::smem_bytes(pps);
@@ -422,6 +425,7 @@ int gen_launch(const void* q, const void* k_pages, const void* v_pages, const in
   a.max_pages = max_pages;
   a.num_pages = num_pages;
   a.hkv = hkv;
+  a.gq = gq;
   a.pps = pps;
   a.splits = splits;
   a.status = reinterpret_cast<int*>(ws);
@@ -439,8 +443,11 @@ bool decode_generic_supported(int num_q_heads, int num_kv_heads, int head_dim, i
   if (num_kv_heads < 1 || num_kv_heads > 65535 || page_size != kPageSize) return false;
   if (num_q_heads % num_kv_heads != 0) return false;
   const int g = num_q_heads / num_kv_heads;
-  return (g == 1 || g == 2 || g == 4 || g == 8) && (head_dim == 64 || head_dim == 128);
+  return g >= 1 && g <= 8 && (head_dim == 64 || head_dim == 128);
 }
+
+// The kernel's group size for g query heads per KV head: the next of 1, 2, 4, 8.
+static int padded_group(int g) { return g <= 1 ? 1 : g <= 2 ? 2 : g <= 4 ? 4 : 8; }
 
 #define PKV_GEN_DISPATCH(CALL)                     \
   switch (group * 1000 + head_dim) {               \
@@ -457,7 +464,7 @@ bool decode_generic_supported(int num_q_heads, int num_kv_heads, int head_dim, i
 
 size_t decode_generic_workspace_bytes(int num_q_heads, int num_kv_heads, int head_dim, int32_t batch,
                                       int32_t max_pages, int num_sms) {
-  const int group = num_q_heads / num_kv_heads;
+  const int group = padded_group(num_q_heads / num_kv_heads);
 #define PKV_GEN_WS(G, D) gen_workspace<G, D>(batch, num_kv_heads, max_pages, num_sms)
   PKV_GEN_DISPATCH(PKV_GEN_WS)
 #undef PKV_GEN_WS
@@ -469,10 +476,11 @@ int launch_decode_generic(const void* q, const void* k_pages, const void* v_page
                           int head_dim, int32_t batch, int32_t max_pages, int32_t num_pages, void* workspace,
                           int num_sms, cudaStream_t stream) {
   if (batch == 0) return PKV_OK;
-  const int group = num_q_heads / num_kv_heads;
-#define PKV_GEN_RUN(G, D)                                                                                        \
-  gen_launch<G, D>(q, k_pages, v_pages, block_table, seq_lens, out, scale, batch, num_kv_heads, max_pages, num_pages, \
-                   workspace, num_sms, stream)
+  const int gq = num_q_heads / num_kv_heads;
+  const int group = padded_group(gq);
+#define PKV_GEN_RUN(G, D)                                                                                   \
+  gen_launch<G, D>(q, k_pages, v_pages, block_table, seq_lens, out, scale, batch, num_kv_heads, gq, max_pages, \
+                   num_pages, workspace, num_sms, stream)
   PKV_GEN_DISPATCH(PKV_GEN_RUN)
 #undef PKV_GEN_RUN
   return PKV_ERR_UNSUPPORTED;

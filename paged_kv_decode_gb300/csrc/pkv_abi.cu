@@ -57,7 +57,7 @@ int check_desc(const pkv_cache_desc* d) {
 }
 
 // Geometries pkv_append and pkv_decode_attn also serve (decode_generic.cu):
-// page size 16, head_dim 64 or 128, 1, 2, 4 or 8 query heads per KV head.
+// page size 16, head_dim 64 or 128, 1 to 8 query heads per KV head.
 // Sets *generic when the call takes the generic decode path.
 int check_desc_decode(const pkv_cache_desc* d, bool* generic) {
   const int rc = check_desc(d);
@@ -103,7 +103,7 @@ const char* pkv_status_string(int status) {
     case PKV_ERR_NULL_ARG: return "a required pointer is NULL";
     case PKV_ERR_BAD_SHAPE: return "bad or inconsistent size";
     case PKV_ERR_UNSUPPORTED:
-      return "unsupported geometry or device (sm_103; decode and append: page 16, head_dim 64/128, 1/2/4/8 query "
+      return "unsupported geometry or device (sm_103; decode and append: page 16, head_dim 64/128, 1 to 8 query "
              "heads per KV head; prefill and fused calls: 16/8/128/16)";
     case PKV_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
     case PKV_ERR_CUDA: return "CUDA runtime or launch error";

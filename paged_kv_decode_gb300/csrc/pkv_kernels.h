@@ -24,7 +24,7 @@ int launch_decode(const void* q, const void* k_new, const void* v_new, const voi
 int decode_max_batch();
 
 // Decode for other geometries (decode_generic.cu): page size 16, head_dim 64 or 128,
-// num_q_heads / num_kv_heads in {1, 2, 4, 8}. Workspace = [status | counters | records].
+// num_q_heads / num_kv_heads from 1 to 8. Workspace = [status | counters | records].
 bool decode_generic_supported(int num_q_heads, int num_kv_heads, int head_dim, int page_size);
 size_t decode_generic_workspace_bytes(int num_q_heads, int num_kv_heads, int head_dim, int32_t batch,
                                       int32_t max_pages, int num_sms);

@@ -41,13 +41,14 @@ def test_host_argument_checks(lib):
     # NULL descriptor
     assert lib.pkv_append(None, None, None, 1, None, None, None, None, None, 0) == -1
     # unsupported geometry: decode and append take page size 16, head_dim 64 or 128 and
-    # 1, 2, 4 or 8 query heads per KV head; prefill and the fused calls only 16/8/128/16
-    for bad in (_desc(head_dim=96), _desc(num_q_heads=12, num_kv_heads=4), _desc(num_q_heads=24),
+    # 1 to 8 query heads per KV head; prefill and the fused calls only 16/8/128/16
+    for bad in (_desc(head_dim=96), _desc(num_q_heads=36, num_kv_heads=4), _desc(num_q_heads=20),
                 _desc(page_size=32), _desc(num_q_heads=32, num_kv_heads=2)):
         assert lib.pkv_append(None, None, None, 1, None, None, ctypes.byref(bad), None, None, 0) == -3
         assert lib.pkv_decode_attn(None, None, None, None, None, None, 1.0, None, ctypes.byref(bad), 1, 1, None,
                                    0) == -3
-    for other in (_desc(head_dim=64), _desc(num_q_heads=32, num_kv_heads=8), _desc(num_q_heads=8)):
+    for other in (_desc(head_dim=64), _desc(num_q_heads=32, num_kv_heads=8), _desc(num_q_heads=8),
+                  _desc(num_q_heads=40), _desc(num_q_heads=28, num_kv_heads=4), _desc(num_q_heads=24)):
         # served by the generic decode path: past the geometry check, stopped at the NULL pointers
         assert lib.pkv_decode_attn(None, None, None, None, None, None, 1.0, None, ctypes.byref(other), 1, 1, None,
                                    0) == -1

@@ -3,8 +3,9 @@ decoder's 16/8/128 (the generic decode path), against the fp64 oracle.
 
 The pages name further decoder backbones for the same slot (a Llama-style 2B
 model, Qwen3-8B, OLMo-2-7B, SmolLM2-1.7B) but give no head counts, so the
-geometries here span the supported range instead: 1, 2, 4 and 8 query heads
-per KV head, head_dim 64 and 128, several KV-head counts. Same bar as the
+geometries here span the supported range instead: 1 to 8 query heads per KV
+head (3, 5, 6 and 7 padded inside the kernel), head_dim 64 and 128, several
+KV-head counts. Same bar as the
 tuned path (tests/parity.py); exact cases bit for bit.
 """
 import numpy as np
@@ -28,6 +29,12 @@ SHAPES = {
     "g8_d64_8q1kv": W.Geometry(8, 1, 64),
     "g2_d128_12q6kv": W.Geometry(12, 6, 128),
     "g4_d64_16q4kv": W.Geometry(16, 4, 64),
+    # groups of 3, 5, 6 and 7 run padded to 4 or 8 heads
+    "g3_d128_12q4kv": W.Geometry(12, 4, 128),
+    "g5_d128_40q8kv": W.Geometry(40, 8, 128),
+    "g6_d64_12q2kv": W.Geometry(12, 2, 64),
+    "g7_d128_28q4kv": W.Geometry(28, 4, 128),
+    "g7_d64_14q2kv": W.Geometry(14, 2, 64),
 }
 
 
