@@ -407,14 +407,20 @@ class GenericDecodeStep:
 
 
 def measure_shapes(device, hbm, layers=8, steps=30, warmup=5):
-    """Other decoder geometries on the generic decode path, bs16 U{300..3000}: per-layer time and
-    bandwidth (the pages name these backbones without head counts; the shapes are examples)."""
+    """Other decoder geometries on the generic decode path, bs16 U{300..3000} (one case a single
+    40000-token request): per-layer time and bandwidth (the pages name these backbones without head
+    counts; the shapes are examples)."""
     from paged_kv_decode_gb300 import workloads as W
 
     res = {}
-    for name, g in (("32q_8kv_d128", W.Geometry(32, 8, 128)), ("32q_32kv_d128", W.Geometry(32, 32, 128)),
-                    ("32q_32kv_d64", W.Geometry(32, 32, 64)), ("64q_8kv_d128", W.Geometry(64, 8, 128))):
-        st = GenericDecodeStep(device, W.config_seq_lens(2), g, layers, seed=31)
+    bs16 = W.config_seq_lens(2)
+    for name, g, lens in (("32q_8kv_d128", W.Geometry(32, 8, 128), bs16),
+                          ("32q_32kv_d128", W.Geometry(32, 32, 128), bs16),
+                          ("32q_32kv_d64", W.Geometry(32, 32, 64), bs16),
+                          ("64q_8kv_d128", W.Geometry(64, 8, 128), bs16),
+                          ("16q_8kv_d64", W.Geometry(16, 8, 64), bs16),
+                          ("32q_8kv_d128_40k", W.Geometry(32, 8, 128), [40000])):
+        st = GenericDecodeStep(device, lens, g, layers, seed=31)
         st.capture()
         ms = time_graph(st, steps, warmup, False) / steps
         us = ms * 1e3 / layers
@@ -426,6 +432,23 @@ def measure_shapes(device, hbm, layers=8, steps=30, warmup=5):
 
         torch.cuda.empty_cache()
     return res
+
+
+def run_geometry(args, device):
+    """One generic-path geometry alone (bs16, decode attention only, `layers` pools in a graph)."""
+    from paged_kv_decode_gb300 import workloads as W
+
+    q, kv, d = (int(x) for x in args.geometry.split(","))
+    st = GenericDecodeStep(device, W.config_seq_lens(2), W.Geometry(q, kv, d), args.layers, seed=31)
+    st.capture()
+    ms = time_graph(st, args.steps, args.warmup, False) / args.steps
+    us = ms * 1e3 / args.layers
+    hbm = _peaks()[0]
+    gbps = st.decode_bytes() / (us * 1e-6) / 1e9
+    print(json.dumps({"workload": f"generic decode attention, {q}q/{kv}kv/d{d}, bs16 U{{300..3000}}, "
+                                  f"{args.layers} layers per graph", "us_per_layer": us, "gbps": gbps,
+                      "frac_of_measured_hbm": gbps / hbm, "bytes_per_layer": st.decode_bytes(),
+                      "steps": args.steps, "warmup": args.warmup}), flush=True)
 
 
 def measure_prefill(device, bf16_peak, reps=10):
@@ -591,6 +614,8 @@ def main():
     ap.add_argument("--layers", type=int, default=28)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the 40k-context and prefill measurements")
+    ap.add_argument("--geometry", default=None, metavar="Q,KV,D",
+                    help="time only the generic decode path on that cache geometry (bs16 U{300..3000}) and exit")
     ap.add_argument("--unfused", action="store_true",
                     help="time the step as separate pkv_append + pkv_decode_attn launches")
     args = ap.parse_args()
@@ -622,6 +647,9 @@ def main():
             build_library()
     device = torch.device("cuda", local_rank if dist_on else 0)
     torch.cuda.set_device(device)
+    if args.geometry:
+        run_geometry(args, device)
+        return
 
     # each replica runs its own copy of the workload (replicas only: requests are independent)
     step = DecodeStep(device, W.config_seq_lens(2), args.layers, seed=2 + rank, fused=not args.unfused)
@@ -721,7 +749,8 @@ def main():
             W.config_seq_lens(5), 5 + rank,
             "CFG-paired decode: 28 layers x bs32 (16 conditional U{1000..8000} + 16 companions U{8..64} + g)")
         extra["other_geometries_bs16"] = {
-            "workload": "decode attention alone (generic path), bs16 U{300..3000}, 8 layers per graph",
+            "workload": "decode attention alone (generic path), bs16 U{300..3000} (the _40k case: one 40000-token "
+                        "request), 8 layers per graph",
             **measure_shapes(device, hbm)}
         extra["chunked_prefill"] = {
             "workload": "4096-token chunk (1 request) after 0/8192/32768 cached tokens; mixed step adds the chunk "

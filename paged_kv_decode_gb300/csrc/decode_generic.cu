@@ -1,46 +1,61 @@
-// decode_generic.cu -- decode attention for cache geometries other than the
-// Qwen3 decoder's 16 query / 8 KV heads of dimension 128 (decode.cu serves that
-// one): G = num_q_heads / num_kv_heads query heads per KV head with G from 1 to
-// 8, head_dim 64 or 128, any number of KV heads, page size 16. A group of 3, 5,
-// 6 or 7 heads runs in the kernel for 4 or 8 with the extra query rows zero and
-// their outputs not written.
+// decode_generic.cu -- decode attention for any cache geometry the descriptor
+// may give: G = num_q_heads / num_kv_heads query heads per KV head with G from
+// 1 to 8, head_dim 64 or 128, any number of KV heads, page size 16 (decode.cu
+// keeps its own tuned kernel for the Qwen3 decoder's 16 query / 8 KV heads of
+// dimension 128). A group of 3, 5, 6 or 7 heads runs in the kernel for 4 or 8,
+// the extra query rows zero and their outputs not written.
 //
 // The operation is the one of decode.cu (PagedAttention decoding, "FunASR vLLM
 // Inference Engine Guide", section 2): for every request and query head, the
 // softmax-weighted mean of the value rows over the cached positions, scores
 // scale * <q, k_j>. The pages name other backbones for the same decoder slot
 // (Llama-style and larger Qwen3 / OLMo / SmolLM decoders) without their head
-// counts, so this path exists to serve whatever geometry the cache descriptor
-// gives, at the price of a simpler schedule than decode.cu's.
+// counts, so this path serves whatever geometry the cache descriptor gives.
+//
+// Arithmetic: both products of a page are warp-level bf16 tensor-core MMAs
+// (mma.sync m16n8k16, fp32 accumulation), about 100 warp instructions per page
+// for any group up to 8 heads, where CUDA-core score and value passes need up
+// to 1000 and run out of issue slots long before HBM does:
+//  * scores, transposed: S^T[16 tokens][8 heads] = K[16][D] * Q^T[D][8], one MMA
+//    per 16 dims (the query rows sit in registers as the B operand, rows past
+//    the group zero);
+//  * softmax in registers: a lane holds tokens r and r + 8 of heads 2c, 2c + 1
+//    (r = lane / 4, c = lane % 4), so a head's page max takes three shuffles;
+//    p is rounded to bf16 for the value product, and the running sum adds the
+//    rounded p, so the output is an exact convex combination of value rows;
+//  * values, transposed: O^T[D][8] += V^T[D][16] * P^T[16][8], one MMA per 16
+//    dims; movmatrix turns the score accumulator's (token, head) pairs into
+//    the (head, token) pairs the B operand wants, and the rescale factors of
+//    the online softmax apply to the lane's own accumulator columns.
+// The per-page contraction (16 tokens x at most 8 heads x head_dim) is far below
+// the smallest tcgen05 tile (64 rows), and the softmax sits between the two
+// products of every page, so the warp-level MMA with S and P in registers is
+// the fitting unit here; the prefill kernel, whose tiles are 128 x 128, uses
+// tcgen05 and TMEM.
 //
 // Schedule:
 //  * The grid is (splits, KV heads, requests). CTA (s, h, b) takes pages
 //    [s * pps, (s + 1) * pps) of request b, KV head h; pps and the number of
-//    splits come from the host sizes (enough CTAs for two waves).
-//    CTAs past a request's last page exit at once.
+//    splits come from the host sizes (one wave of CTAs: every SM holds all of
+//    its CTAs from the start), with splits of at least 8 pages. CTAs past a
+//    request's last page exit at once.
 //  * Each of the 4 warps takes every 4th page of the split and keeps a ring of
-//    its own (2 stages for head_dim 128, 3 for 64: three CTAs fit an SM): lane 0
-//    issues the page's K and V tiles as 1-D bulk copies (cp.async.bulk)
-//    completing on the stage's mbarrier, a ring's depth of pages ahead.
-//  * Scores: kL = G * head_dim / 64 lanes per token (at least 2), so that each
-//    lane keeps its slice of the G query rows (64 floats, pre-scaled by
-//    scale * log2(e)) in registers; packed fp32 FMAs over the lane's 16-byte
-//    chunks of the key row (in an order rotated by token, so the 32 lanes' reads
-//    spread over all shared memory banks), for all G heads from one K read. A
-//    transpose-reduce over the kL lanes (halve the heads each round, then sum
-//    the copies) leaves each lane the full score of one (token, head). Online
-//    softmax in the log2 domain with tokens past seq_len masked; p and the
-//    rescale factors go through shared memory. Values: each lane owns
-//    head_dim / 32 dims of every head.
+//    its own (2 stages for head_dim 128, 3 for 64); lane 0 issues the page's K
+//    and V tiles a ring's depth ahead as tiled TMA copies (one 16-row box of
+//    128 bytes per 64 dims) with 128-byte swizzle, so the ldmatrix reads of
+//    eight token rows at the same dims hit eight different bank groups. Tokens
+//    past seq_len are masked in the scores and in the value operand's registers
+//    (unused slots may hold NaN).
 //  * The warps' states are merged in shared memory. A request whose pages fit
 //    one split writes the bf16 output; otherwise each split writes an fp32
 //    record (o, m, l per head), counts itself in (fence, atomic), and the CTA
-//    completing the count merges the request's records (log-sum-exp, in split
-//    order) and resets the counter.
+//    completing the count merges the request's records (log-sum-exp) and
+//    resets the counter.
 #include <math_constants.h>
 
 #include "pkv_device.cuh"
 #include "pkv_kernels.h"
+#include "pkv_tc.cuh"
 
 namespace pkv {
 namespace {
@@ -49,33 +64,22 @@ constexpr int kGenWarps = 4;
 constexpr int kGenThreads = kGenWarps * 32;
 constexpr unsigned kGenFull = 0xffffffffu;
 
+// Shared memory of a CTA: the warps' rings | full barriers | flags | page ids of the split.
 template <int G, int D>
-struct Gen {
-  static constexpr int kTile = kPageSize * D * 2;  // one (page, KV head) K or V tile
+struct Lay {
+  static constexpr int kTile = kPageSize * D * 2;  // one (page, KV head) K or V tile: D / 64 swizzled boxes
   static constexpr int kStage = 2 * kTile;
-  static constexpr int kStages = D == 128 ? 2 : 3;   // per warp: 3 CTAs of 4 warps per SM either way
-  static constexpr int kRing = kStages * kStage;     // per warp
-  static constexpr int kChunks = D / 8;              // 16-byte chunks of a row
-  // Score pass: kL lanes per token, so that a lane's slice of the G query rows is
-  // 64 floats (kL = G * D / 64, at least 2); kTP tokens per pass, kNP passes per
-  // page, kCH 16-byte chunks of the row per lane. kL >= G always.
-  static constexpr int kL = G * D / 64 < 2 ? 2 : G * D / 64;
-  static constexpr int kTP = 32 / kL;
-  static constexpr int kNP = kPageSize / kTP;
-  static constexpr int kCH = kChunks / kL;
-  static constexpr int kDup = kL / G;                // lanes of a token holding the same head's score
-  static_assert(kCH >= 1 && kNP >= 1 && kDup >= 1, "score pass layout");
-  static constexpr int kLaneDims = D / 32;           // value dims per lane
-  static constexpr int kRec = D + 2;                 // floats per head in a record: o[D], m, l
-  static constexpr int kState = G * kRec;            // a warp's or a split's (o, m, l) of all G heads
+  static constexpr int kStages = D == 128 ? 2 : 3;  // per warp: 3 (head_dim 128) or 4 (64) CTAs per SM
+  static constexpr int kRing = kStages * kStage;   // per warp; a multiple of 1024 bytes
+  static constexpr int kKS = D / 16;               // 16-dim steps of both products
+  static constexpr int kRec = D + 4;               // floats per head in a state or record: o[D], m, l, 2 pad
+  static constexpr int kState = G * kRec;
   static_assert(kState * 4 <= kRing, "a warp's state fits its drained ring");
-  // shared memory: rings | full barriers | q (fp32) | p buffers | flags | page ids
+  static_assert(G <= 8, "one 8-column MMA tile of heads");
   static constexpr int kOffBars = kGenWarps * kRing;
-  static constexpr int kOffQ = kOffBars + kGenWarps * kStages * 8;
-  static constexpr int kOffP = kOffQ + G * D * 4;
-  static constexpr int kOffFlag = kOffP + kGenWarps * (kPageSize + 1) * G * 8;
+  static constexpr int kOffFlag = kOffBars + kGenWarps * kStages * 8;
   static constexpr int kOffIds = kOffFlag + 16;
-  static size_t smem_bytes(int pps) { return kOffIds + static_cast<size_t>(pps) * 4; }
+  static size_t smem_bytes(int pps) { return 1024 + kOffIds + static_cast<size_t>(pps) * 4; }
 };
 
 struct GenArgs {
@@ -94,238 +98,91 @@ struct GenArgs {
   int splits;  // splits per (request, KV head) in the records
   int* status;
   int* counters;   // [batch][hkv], zero between calls
-  float* records;  // [batch][hkv][splits][G][D + 2]
+  float* records;  // [batch][hkv][splits][G][D + 4]
 };
 
-template <int G, int D>
-__global__ void __launch_bounds__(kGenThreads) decode_generic_kernel(const GenArgs a) {
-  using S = Gen<G, D>;
-  extern __shared__ __align__(128) unsigned char smem[];
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kOffBars);
-  float* qs = reinterpret_cast<float*>(smem + S::kOffQ);
-  int* flag = reinterpret_cast<int*>(smem + S::kOffFlag);  // [0] a wait failed, [1] this CTA merges
-  int* ids = reinterpret_cast<int*>(smem + S::kOffIds);
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int hq0 = h * a.gq;  // first query head of the group
-  const int nq = a.hkv * a.gq;
-
-  grid_dependency_wait();
-  allow_dependents();
-
-  int sl = __ldg(a.seq_lens + b);
-  const int cap = a.max_pages * kPageSize;
-  if (sl < 0 || sl > cap) {
-    if (tid == 0 && s == 0 && h == 0) set_status(a.status, PKV_ERR_OUT_OF_BOUNDS);
-    sl = sl < 0 ? 0 : cap;
+// Log-sum-exp merge of the nrec records of one (request, KV head) into its bf16
+// output rows, by the whole CTA. rec_at(r): record r, rows [G][D + 4] of o[D],
+// m, l. Every (m, l) is read at once; one warp per head turns the m into
+// weights (kept in `scratch`, 2 * nrec * G + G floats of shared memory); then
+// the o rows are summed as float4 with several records in flight.
+template <int G, int D, class RecAt>
+__device__ __forceinline__ void merge_records(RecAt rec_at, int nrec, int gq, float* scratch, __nv_bfloat16* orow) {
+  constexpr int kRec = D + 4;
+  const int tid = threadIdx.x;
+  float* wgt = scratch;            // [nrec][G]: m, then the weight
+  float* lsp = wgt + nrec * G;     // [nrec][G]: l
+  float* inv = lsp + nrec * G;     // [G]: 1 / merged l
+  for (int e = tid; e < nrec * G; e += kGenThreads) {
+    const float2 ml = __ldcg(reinterpret_cast<const float2*>(rec_at(e / G) + (e % G) * kRec + D));
+    wgt[e] = ml.x;
+    lsp[e] = ml.y;
   }
-  __nv_bfloat16* orow = a.out + (static_cast<size_t>(b) * nq + hq0) * D;
-  if (sl == 0) {  // an empty request (graph-bucket padding): zero rows
-    if (s == 0)
-      for (int i = tid; i < a.gq * D; i += kGenThreads) orow[i] = __float2bfloat16_rn(0.f);
-    return;
-  }
-  const int np = (sl + kPageSize - 1) / kPageSize;
-  const int nsplit = (np + a.pps - 1) / a.pps;
-  if (s >= nsplit) return;
-  const int p0 = s * a.pps;
-  const int p1 = p0 + a.pps < np ? p0 + a.pps : np;
-
-  if (tid < kGenWarps * S::kStages) mbar_init(&full[tid], 1);
-  if (tid == 0) flag[0] = 0;
-  for (int i = tid; i < G * D; i += kGenThreads)  // padding heads (i / D >= gq) get zero rows
-    qs[i] = i < a.gq * D ? __bfloat162float(a.q[(static_cast<size_t>(b) * nq + hq0) * D + i]) * a.qscale : 0.f;
-  for (int p = p0 + tid; p < p1; p += kGenThreads) {
-    int id = __ldg(a.block_table + static_cast<size_t>(b) * a.max_pages + p);
-    if (id < 0 || id >= a.num_pages) {
-      set_status(a.status, PKV_ERR_OUT_OF_BOUNDS);
-      id = 0;  // reported, not read out of bounds
-    }
-    ids[p - p0] = id;
-  }
-  fence_barrier_init();
   __syncthreads();
-
-  // ---- this warp's pages: p0 + warp, p0 + warp + 4, ...
-  const int nw = p1 - p0 > warp ? (p1 - p0 - warp + kGenWarps - 1) / kGenWarps : 0;
-  unsigned char* ring = smem + warp * S::kRing;
-  uint64_t* wfull = full + warp * S::kStages;
-  auto issue = [&](int i) {  // lane 0: page i of this warp into stage i % S::kStages
-    const int id = ids[warp + i * kGenWarps];
-    const size_t off = (static_cast<size_t>(id) * a.hkv + h) * (S::kTile / 2);
-    unsigned char* dst = ring + (i % S::kStages) * S::kStage;
-    mbar_arrive_expect_tx(&wfull[i % S::kStages], S::kStage);
-    bulk_g2s(dst, a.k_pages + off, S::kTile, &wfull[i % S::kStages]);
-    bulk_g2s(dst + S::kTile, a.v_pages + off, S::kTile, &wfull[i % S::kStages]);
-  };
-  if (lane == 0)
-    for (int i = 0; i < S::kStages && i < nw; ++i) issue(i);
-
-  // score-pass position of this lane: token slot i of a pass, part sp of the row
-  const int i = lane / S::kL, sp = lane % S::kL;
-  const int h_own = sp / S::kDup;  // head whose scores this lane holds after the reduce
-  // the lane's query chunks (rotated by token slot, so that the 32 lanes' K reads
-  // spread over all banks): chunk (k) = sp + kL * ((k + i) mod kCH), both as fp32 pairs
-  float2 q2[S::kCH][4][G];
+  {
+    const int warp = tid >> 5, lane = tid & 31;
+    for (int g = warp; g < gq; g += kGenWarps) {
+      float m = -CUDART_INF_F;
+      for (int r = lane; r < nrec; r += 32) m = fmaxf(m, wgt[r * G + g]);
 #pragma unroll
-  for (int k = 0; k < S::kCH; ++k) {
-    const int c = sp + S::kL * ((k + i) % S::kCH);
+      for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      float l = 0.f;
+      for (int r = lane; r < nrec; r += 32) {
+        const float w = ex2(wgt[r * G + g] - m);  // every record holds at least one token
+        wgt[r * G + g] = w;
+        l += lsp[r * G + g] * w;
+      }
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float4 qa = *reinterpret_cast<const float4*>(qs + g * D + c * 8);
-      const float4 qb = *reinterpret_cast<const float4*>(qs + g * D + c * 8 + 4);
-      q2[k][0][g] = make_float2(qa.x, qa.y);
-      q2[k][1][g] = make_float2(qa.z, qa.w);
-      q2[k][2][g] = make_float2(qb.x, qb.y);
-      q2[k][3][g] = make_float2(qb.z, qb.w);
+      for (int o = 16; o >= 1; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+      if (lane == 0) inv[g] = 1.f / l;
     }
   }
-  // p of every (token, head) as the pair (p, p), then every head's rescale factor
-  float2* pb = reinterpret_cast<float2*>(smem + S::kOffP) + warp * (kPageSize + 1) * G;
-  float mrun = -CUDART_INF_F, lrun = 0.f;  // of head h_own
-  float2 o[G][S::kLaneDims / 2];  // dims lane * kLaneDims .., in pairs
-#pragma unroll
-  for (int g = 0; g < G; ++g)
-#pragma unroll
-    for (int k = 0; k < S::kLaneDims / 2; ++k) o[g][k] = make_float2(0.f, 0.f);
-  bool failed = false;
-  for (int it = 0; it < nw && !failed; ++it) {
-    const int st = it % S::kStages;
-    const bool ok = mbar_wait_bounded(&wfull[st], static_cast<uint32_t>(it / S::kStages) & 1u);
-    failed = __any_sync(kGenFull, !ok);
-    if (failed) {
-      if (lane == 0) {
-        set_status(a.status, PKV_ERR_DEVICE_TIMEOUT);
-        flag[0] = 1;
-      }
-      break;
+  __syncthreads();
+  for (int e = tid; e < gq * (D / 4); e += kGenThreads) {
+    const int g = e / (D / 4), d = (e % (D / 4)) * 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+    for (int r = 0; r < nrec; ++r) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(rec_at(r) + g * kRec + d));
+      const float w = wgt[r * G + g];
+      acc.x += v.x * w;
+      acc.y += v.y * w;
+      acc.z += v.z * w;
+      acc.w += v.w * w;
     }
-    const int page = p0 + warp + it * kGenWarps;
-    const int rem = sl - page * kPageSize;
-    const int n_valid = rem < kPageSize ? rem : kPageSize;
-    const unsigned char* kt = ring + st * S::kStage;
-    const unsigned char* vt = kt + S::kTile;
-    // ---- scores: pass ps covers tokens ps * kTP .. ; each lane ends with the score
-    // of (token ps * kTP + i, head h_own) after a transpose-reduce over its kL lanes
-    float sc[S::kNP];
-#pragma unroll
-    for (int ps = 0; ps < S::kNP; ++ps) {
-      const int tok = ps * S::kTP + i;
-      float2 acc[G];
-#pragma unroll
-      for (int g = 0; g < G; ++g) acc[g] = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int k = 0; k < S::kCH; ++k) {
-        const int c = sp + S::kL * ((k + i) % S::kCH);
-        const uint4 u = *reinterpret_cast<const uint4*>(kt + tok * (D * 2) + c * 16);
-        const float2 k0 = bf2_to_f2(u.x), k1 = bf2_to_f2(u.y), k2 = bf2_to_f2(u.z), k3 = bf2_to_f2(u.w);
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          acc[g] = __ffma2_rn(q2[k][0][g], k0, acc[g]);
-          acc[g] = __ffma2_rn(q2[k][1][g], k1, acc[g]);
-          acc[g] = __ffma2_rn(q2[k][2][g], k2, acc[g]);
-          acc[g] = __ffma2_rn(q2[k][3][g], k3, acc[g]);
-        }
-      }
-      float v[G];
-#pragma unroll
-      for (int g = 0; g < G; ++g) v[g] = acc[g].x + acc[g].y;
-      // halving rounds (masks kL/2, kL/4, .. down to kDup): keep one half of the heads,
-      // send the other to the partner; then sum the kDup copies of the last one
-#pragma unroll
-      for (int r = 0; (G >> r) > 1; ++r) {
-        const int m = S::kL >> (r + 1), n = G >> r;
-        const bool up = (sp & m) != 0;
-#pragma unroll
-        for (int j = 0; j < n / 2; ++j) {
-          const float send = up ? v[j] : v[j + n / 2];
-          const float keep = up ? v[j + n / 2] : v[j];
-          v[j] = keep + __shfl_xor_sync(kGenFull, send, m);
-        }
-      }
-#pragma unroll
-      for (int m = S::kDup / 2; m >= 1; m >>= 1) v[0] += __shfl_xor_sync(kGenFull, v[0], m);
-      sc[ps] = tok < n_valid ? v[0] : -CUDART_INF_F;
-    }
-    // ---- online softmax of head h_own over the page's tokens (passes, then token slots)
-    float mx = sc[0];
-#pragma unroll
-    for (int ps = 1; ps < S::kNP; ++ps) mx = fmaxf(mx, sc[ps]);
-#pragma unroll
-    for (int m = S::kL; m < 32; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kGenFull, mx, m));
-    const float mnew = fmaxf(mrun, mx);
-    const float alpha = ex2(mrun - mnew);
-    float psum = 0.f;
-#pragma unroll
-    for (int ps = 0; ps < S::kNP; ++ps) {
-      const float p = ex2(sc[ps] - mnew);
-      psum += p;
-      if (sp % S::kDup == 0) pb[(ps * S::kTP + i) * G + h_own] = make_float2(p, p);
-    }
-#pragma unroll
-    for (int m = S::kL; m < 32; m <<= 1) psum += __shfl_xor_sync(kGenFull, psum, m);
-    lrun = lrun * alpha + psum;
-    mrun = mnew;
-    if (i == 0 && sp % S::kDup == 0) pb[kPageSize * G + h_own] = make_float2(alpha, alpha);
-    __syncwarp();
-    // ---- values: lane owns dims lane * kLaneDims .. of every head (packed pairs)
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float2 al = pb[kPageSize * G + g];
-#pragma unroll
-      for (int k = 0; k < S::kLaneDims / 2; ++k) o[g][k] = __fmul2_rn(o[g][k], al);
-    }
-#pragma unroll
-    for (int tt = 0; tt < kPageSize; ++tt) {
-      if (tt < n_valid) {
-        float2 vv[S::kLaneDims / 2];
-        if constexpr (S::kLaneDims == 4) {
-          const uint2 u = *reinterpret_cast<const uint2*>(vt + tt * (D * 2) + lane * 8);
-          vv[0] = bf2_to_f2(u.x);
-          vv[1] = bf2_to_f2(u.y);
-        } else {
-          vv[0] = bf2_to_f2(*reinterpret_cast<const uint32_t*>(vt + tt * (D * 2) + lane * 4));
-        }
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float2 p = pb[tt * G + g];
-#pragma unroll
-          for (int k = 0; k < S::kLaneDims / 2; ++k) o[g][k] = __ffma2_rn(p, vv[k], o[g][k]);
-        }
-      }
-    }
-    __syncwarp();  // the stage and the p buffer are free again
-    if (lane == 0 && it + S::kStages < nw) issue(it + S::kStages);
+    const float il = inv[g];
+    uint2 packed;
+    packed.x = pack_bf16x2(acc.x * il, acc.y * il);
+    packed.y = pack_bf16x2(acc.z * il, acc.w * il);
+    *reinterpret_cast<uint2*>(orow + g * D + d) = packed;
   }
+}
 
-  // ---- CTA merge of the warp states (each in its own drained ring)
-  float* wst = reinterpret_cast<float*>(ring);
-#pragma unroll
-  for (int g = 0; g < G; ++g)
-#pragma unroll
-    for (int k = 0; k < S::kLaneDims / 2; ++k) {
-      wst[g * S::kRec + lane * S::kLaneDims + 2 * k] = o[g][k].x;
-      wst[g * S::kRec + lane * S::kLaneDims + 2 * k + 1] = o[g][k].y;
-    }
-  if (i == 0 && sp % S::kDup == 0) {  // one lane per head holds its m and l
-    wst[h_own * S::kRec + D] = mrun;
-    wst[h_own * S::kRec + D + 1] = lrun;
-  }
+// The end of a split, once each warp has left its (o, m, l) of the G heads at
+// the start of its drained ring (ring w at rings + w * kRingBytes, layout
+// [G][D + 4]): merge the warps' states; a request whose pages fit one split
+// writes its bf16 output, otherwise the split writes its fp32 record, counts
+// itself in (fence, atomic), and the CTA completing the count merges the
+// request's records (log-sum-exp, in split order) and resets the counter.
+template <int G, int D, int kRingBytes>
+__device__ __forceinline__ void finish_split(const GenArgs& a, const unsigned char* rings, int* flag, int b, int h,
+                                             int s, int nsplit, __nv_bfloat16* orow) {
+  constexpr int kRec = D + 4, kState = G * kRec;  // rows o[D], m, l, 2 pad: 16-byte aligned
+  const int tid = threadIdx.x;
   __syncthreads();
   if (flag[0] != 0) return;  // a wait failed: copies may still land, write nothing
   const bool whole = nsplit == 1;
-  float* rec = a.records + ((static_cast<size_t>(b) * a.hkv + h) * a.splits + s) * S::kState;
+  float* rec = a.records + ((static_cast<size_t>(b) * a.hkv + h) * a.splits + s) * kState;
   for (int e = tid; e < G * (D + 1); e += kGenThreads) {
     const int g = e / (D + 1), d = e % (D + 1);  // d == D: this head's m and l
     float m = -CUDART_INF_F;
 #pragma unroll
     for (int w = 0; w < kGenWarps; ++w)
-      m = fmaxf(m, reinterpret_cast<const float*>(smem + w * S::kRing)[g * S::kRec + D]);
+      m = fmaxf(m, reinterpret_cast<const float*>(rings + w * kRingBytes)[g * kRec + D]);
     float l = 0.f, acc = 0.f;
 #pragma unroll
     for (int w = 0; w < kGenWarps; ++w) {
-      const float* r = reinterpret_cast<const float*>(smem + w * S::kRing) + g * S::kRec;
+      const float* r = reinterpret_cast<const float*>(rings + w * kRingBytes) + g * kRec;
       const float sc = r[D] == -CUDART_INF_F ? 0.f : ex2(r[D] - m);  // warps without pages
       l += r[D + 1] * sc;
       if (d < D) acc += r[d] * sc;
@@ -333,10 +190,10 @@ __global__ void __launch_bounds__(kGenThreads) decode_generic_kernel(const GenAr
     if (whole) {
       if (d < D && g < a.gq) orow[g * D + d] = __float2bfloat16_rn(acc / l);
     } else if (d < D) {
-      rec[g * S::kRec + d] = acc;
+      rec[g * kRec + d] = acc;
     } else {
-      rec[g * S::kRec + D] = m;
-      rec[g * S::kRec + D + 1] = l;
+      rec[g * kRec + D] = m;
+      rec[g * kRec + D + 1] = l;
     }
   }
   if (whole) return;
@@ -352,35 +209,278 @@ __global__ void __launch_bounds__(kGenThreads) decode_generic_kernel(const GenAr
   }
   __syncthreads();
   if (!flag[1]) return;
-  const float* recs = a.records + (static_cast<size_t>(b) * a.hkv + h) * a.splits * S::kState;
-  for (int e = tid; e < a.gq * D; e += kGenThreads) {
-    const int g = e / D, d = e % D;
-    float m = -CUDART_INF_F;
-    for (int r = 0; r < nsplit; ++r) m = fmaxf(m, recs[r * S::kState + g * S::kRec + D]);
-    float l = 0.f, acc = 0.f;
-    for (int r = 0; r < nsplit; ++r) {
-      const float* x = recs + r * S::kState + g * S::kRec;
-      const float sc = ex2(x[D] - m);
-      l += x[D + 1] * sc;
-      acc += x[d] * sc;
-    }
-    orow[g * D + d] = __float2bfloat16_rn(acc / l);
-  }
+  const float* recs = a.records + (static_cast<size_t>(b) * a.hkv + h) * a.splits * kState;
+  merge_records<G, D>([&](int r) { return recs + static_cast<size_t>(r) * kState; }, nsplit, a.gq,
+                      reinterpret_cast<float*>(const_cast<unsigned char*>(rings)), orow);
   if (tid == 0) *counter = 0;
 }
 
+// Byte offset of 16-byte chunk c of token row t in a tile written by the
+// 128-byte swizzled TMA boxes: box c / 8 (2 KiB each, 1024-byte aligned), row t
+// of 128 bytes, chunk (c mod 8) XOR (t mod 8).
+__device__ __forceinline__ uint32_t swz(int t, int c) {
+  return static_cast<uint32_t>((c >> 3) * 2048 + t * 128 + (((c & 7) ^ (t & 7)) << 4));
+}
+__device__ __forceinline__ void ldsm4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+__device__ __forceinline__ void ldsm4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+__device__ __forceinline__ uint32_t movm_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+// c += a * b, m16n8k16, bf16 operands, fp32 accumulators
+__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// One page of the tensor-core path: the scores of its 16 tokens for the 8 head
+// columns, the online-softmax update of this lane's two heads (2c, 2c + 1), and
+// the value product. kt, vt: shared addresses of the page's swizzled K and V
+// tiles; nv: its tokens before seq_len.
+template <int KS>
+__device__ __forceinline__ void mma_page(uint32_t kt, uint32_t vt, const uint32_t (&koff)[KS],
+                                         const uint32_t (&voff)[KS], const uint32_t (&qf)[KS][2], int nv,
+                                         float qscale, float (&o)[KS][4], float& m0, float& m1, float& l0,
+                                         float& l1) {
+  const int lane = threadIdx.x & 31, r = lane >> 2, c = lane & 3;
+    // ---- scores (two accumulators: the k-steps form two dependent chains)
+    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      uint32_t kf[4];
+      ldsm4(kt + koff[ks], kf);
+      if (ks & 1)
+        mma_bf16(sb, kf, qf[ks][0], qf[ks][1]);
+      else
+        mma_bf16(sa, kf, qf[ks][0], qf[ks][1]);
+    }
+    const bool v0 = r < nv, v1 = r + 8 < nv;
+    const float s00 = v0 ? (sa[0] + sb[0]) * qscale : -CUDART_INF_F;  // token r, head 2c
+    const float s01 = v0 ? (sa[1] + sb[1]) * qscale : -CUDART_INF_F;  // token r, head 2c + 1
+    const float s10 = v1 ? (sa[2] + sb[2]) * qscale : -CUDART_INF_F;  // token r + 8
+    const float s11 = v1 ? (sa[3] + sb[3]) * qscale : -CUDART_INF_F;
+
+    // ---- online softmax of heads 2c, 2c + 1 over the page's 16 tokens
+    float x0 = fmaxf(s00, s10), x1 = fmaxf(s01, s11);
+#pragma unroll
+    for (int m = 4; m < 32; m <<= 1) {
+      x0 = fmaxf(x0, __shfl_xor_sync(kGenFull, x0, m));
+      x1 = fmaxf(x1, __shfl_xor_sync(kGenFull, x1, m));
+    }
+    const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
+    const uint32_t pk0 = pack_bf16x2(ex2(s00 - n0), ex2(s01 - n1));  // token r
+    const uint32_t pk1 = pack_bf16x2(ex2(s10 - n0), ex2(s11 - n1));  // token r + 8
+    const float2 q0 = bf2_to_f2(pk0), q1 = bf2_to_f2(pk1);
+    if (__any_sync(kGenFull, n0 != m0 || n1 != m1)) {
+      const float al0 = ex2(m0 - n0), al1 = ex2(m1 - n1);  // 0 on the first page
+      l0 *= al0;
+      l1 *= al1;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        o[ks][0] *= al0;
+        o[ks][1] *= al1;
+        o[ks][2] *= al0;
+        o[ks][3] *= al1;
+      }
+      m0 = n0;
+      m1 = n1;
+    }
+    l0 += q0.x + q1.x;
+    l1 += q0.y + q1.y;
+
+    // ---- values: P^T as the B operand (head r, tokens 2c, 2c + 1 and 8 + 2c, 9 + 2c)
+    const uint32_t pb0 = movm_t(pk0), pb1 = movm_t(pk1);
+    uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;  // value rows past seq_len read as zero
+    if (nv < kPageSize) {
+      mlo = (2 * c < nv ? 0x0000ffffu : 0u) | (2 * c + 1 < nv ? 0xffff0000u : 0u);
+      mhi = (2 * c + 8 < nv ? 0x0000ffffu : 0u) | (2 * c + 9 < nv ? 0xffff0000u : 0u);
+    }
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      uint32_t vf[4];
+      ldsm4_t(vt + voff[ks], vf);
+      vf[0] &= mlo;
+      vf[1] &= mlo;
+      vf[2] &= mhi;
+      vf[3] &= mhi;
+      mma_bf16(o[ks], vf, pb0, pb1);
+    }
+}
+
+template <int G, int D>
+__global__ void __launch_bounds__(kGenThreads) decode_generic_kernel(const __grid_constant__ CUtensorMap kmap,
+                                                                 const __grid_constant__ CUtensorMap vmap,
+                                                                 const GenArgs a) {
+  using S = Lay<G, D>;
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);  // swizzle atoms need 1024
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kOffBars);
+  int* flag = reinterpret_cast<int*>(smem + S::kOffFlag);  // [0] a wait failed, [1] this CTA merges
+  int* ids = reinterpret_cast<int*>(smem + S::kOffIds);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int hq0 = h * a.gq;
+  const int nq = a.hkv * a.gq;
+
+  grid_dependency_wait();
+  allow_dependents();
+
+  int sl = __ldg(a.seq_lens + b);
+  const int cap = a.max_pages * kPageSize;
+  if (sl < 0 || sl > cap) {
+    if (tid == 0 && s == 0 && h == 0) set_status(a.status, PKV_ERR_OUT_OF_BOUNDS);
+    sl = sl < 0 ? 0 : cap;
+  }
+  __nv_bfloat16* orow = a.out + (static_cast<size_t>(b) * nq + hq0) * D;
+  if (sl == 0) {
+    if (s == 0)
+      for (int i = tid; i < a.gq * D; i += kGenThreads) orow[i] = __float2bfloat16_rn(0.f);
+    return;
+  }
+  const int np = (sl + kPageSize - 1) / kPageSize;
+  const int nsplit = (np + a.pps - 1) / a.pps;
+  if (s >= nsplit) return;
+  const int p0 = s * a.pps;
+  const int p1 = p0 + a.pps < np ? p0 + a.pps : np;
+
+  if (tid < kGenWarps * S::kStages) mbar_init(&full[tid], 1);
+  if (tid == 0) flag[0] = 0;
+  for (int p = p0 + tid; p < p1; p += kGenThreads) {
+    int id = __ldg(a.block_table + static_cast<size_t>(b) * a.max_pages + p);
+    if (id < 0 || id >= a.num_pages) {
+      set_status(a.status, PKV_ERR_OUT_OF_BOUNDS);
+      id = 0;
+    }
+    ids[p - p0] = id;
+  }
+  fence_barrier_init();
+  __syncthreads();
+
+  const int nw = p1 - p0 > warp ? (p1 - p0 - warp + kGenWarps - 1) / kGenWarps : 0;
+  unsigned char* ring = smem + warp * S::kRing;
+  uint64_t* wfull = full + warp * S::kStages;
+  auto issue = [&](int i) {  // lane 0: page i of this warp into stage i % kStages
+    const int z = ids[warp + i * kGenWarps] * a.hkv + h;  // tile index in the pool
+    unsigned char* dst = ring + (i % S::kStages) * S::kStage;
+    uint64_t* bar = &wfull[i % S::kStages];
+    mbar_arrive_expect_tx(bar, S::kStage);
+#pragma unroll
+    for (int j = 0; j < D / 64; ++j) {
+      tma_load_3d(dst + j * 2048, &kmap, 64 * j, 0, z, bar);
+      tma_load_3d(dst + S::kTile + j * 2048, &vmap, 64 * j, 0, z, bar);
+    }
+  };
+  if (lane == 0)
+    for (int i = 0; i < S::kStages && i < nw; ++i) issue(i);
+
+  const int r = lane >> 2, c = lane & 3;  // fragment row and column pair
+  const int mi = lane >> 3, mr = lane & 7;  // ldmatrix: matrix and row this lane addresses
+  // Q^T as the B operand: head r, dims 16 ks + 2c (+1) and 16 ks + 8 + 2c (+1)
+  uint32_t qf[S::kKS][2];
+  {
+    const bool live = r < a.gq;
+    const uint32_t* qrow =
+        reinterpret_cast<const uint32_t*>(a.q + (static_cast<size_t>(b) * nq + hq0 + (live ? r : 0)) * D);
+#pragma unroll
+    for (int ks = 0; ks < S::kKS; ++ks) {
+      qf[ks][0] = live ? __ldg(qrow + 8 * ks + c) : 0u;
+      qf[ks][1] = live ? __ldg(qrow + 8 * ks + 4 + c) : 0u;
+    }
+  }
+  // ldmatrix row addresses inside a tile: K as the A operand (matrices: tokens 0-7 /
+  // 8-15 x the two 8-dim halves of a 16-dim step), V transposed (same four blocks in
+  // the order the A operand of the value product wants)
+  uint32_t koff[S::kKS], voff[S::kKS];
+#pragma unroll
+  for (int ks = 0; ks < S::kKS; ++ks) {
+    koff[ks] = swz(mr + ((mi & 1) << 3), 2 * ks + (mi >> 1));
+    voff[ks] = swz(mr + ((mi >> 1) << 3), 2 * ks + (mi & 1));
+  }
+
+  float o[S::kKS][4];  // O^T: dims 16 ks + r (+8) x heads 2c, 2c + 1
+#pragma unroll
+  for (int ks = 0; ks < S::kKS; ++ks) o[ks][0] = o[ks][1] = o[ks][2] = o[ks][3] = 0.f;
+  float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F;  // running max of heads 2c, 2c + 1 (log2 domain)
+  float l0 = 0.f, l1 = 0.f;                      // this lane's part of their running sums
+  bool failed = false;
+  for (int it = 0; it < nw && !failed; ++it) {
+    const int st = it % S::kStages;
+    const bool ok = mbar_wait_bounded(&wfull[st], static_cast<uint32_t>(it / S::kStages) & 1u);
+    failed = __any_sync(kGenFull, !ok);
+    if (failed) {
+      if (lane == 0) {
+        set_status(a.status, PKV_ERR_DEVICE_TIMEOUT);
+        flag[0] = 1;
+      }
+      break;
+    }
+    const int page = p0 + warp + it * kGenWarps;
+    const int rem = sl - page * kPageSize;
+    const int nv = rem < kPageSize ? rem : kPageSize;
+    const uint32_t kt = smem_u32(ring + st * S::kStage), vt = kt + S::kTile;
+
+    mma_page<S::kKS>(kt, vt, koff, voff, qf, nv, a.qscale, o, m0, m1, l0, l1);
+    __syncwarp();  // the stage is free again
+    if (lane == 0 && it + S::kStages < nw) issue(it + S::kStages);
+  }
+
+  // ---- this warp's state into its drained ring: [G][D + 4] as o, m, l
+#pragma unroll
+  for (int m = 4; m < 32; m <<= 1) {
+    l0 += __shfl_xor_sync(kGenFull, l0, m);
+    l1 += __shfl_xor_sync(kGenFull, l1, m);
+  }
+  float* wst = reinterpret_cast<float*>(ring);
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const int n = 2 * c + j;
+    if (n < G) {
+#pragma unroll
+      for (int ks = 0; ks < S::kKS; ++ks) {
+        wst[n * (D + 4) + 16 * ks + r] = o[ks][j];
+        wst[n * (D + 4) + 16 * ks + r + 8] = o[ks][2 + j];
+      }
+      if (r == 0) {
+        wst[n * (D + 4) + D] = j ? m1 : m0;
+        wst[n * (D + 4) + D + 1] = j ? l1 : l0;
+      }
+    }
+  }
+  finish_split<G, D, S::kRing>(a, smem, flag, b, h, s, nsplit, orow);
+}
+
 // Splits per (request, KV head) and pages per split for the host sizes: enough
-// CTAs to fill the GPU twice at the resident CTAs per SM the shape allows, with
-// splits of at least 8 pages.
+// CTAs to fill the GPU once at the resident CTAs per SM the shape allows, with
+// splits of at least 8 pages and at most as many as the merging CTA can weigh
+// in its drained rings.
 template <int G, int D>
 void plan(int batch, int hkv, int max_pages, int num_sms, int& splits, int& pps) {
   const size_t per_sm = 227 * 1024;
-  const int resident = static_cast<int>(per_sm / (Gen<G, D>::smem_bytes(1) + 1024));
-  // two waves of CTAs, splits of at least 8 pages (fewer records for short requests)
-  const long long want = 2LL * num_sms * (resident > 0 ? resident : 1);
+  const int resident = static_cast<int>(per_sm / (Lay<G, D>::smem_bytes(1) + 1024));
+  // one wave of CTAs (each SM holds all of its CTAs from the start), splits of at least 8 pages
+  // (fewer records for short requests)
+  const long long want = 1LL * num_sms * (resident > 0 ? resident : 1);
   const long long pairs = static_cast<long long>(batch) * hkv;
   long long sp = (want + pairs - 1) / pairs;
   if (sp > (max_pages + 7) / 8) sp = (max_pages + 7) / 8;
+  // the merging CTA keeps two floats per (split, head) in its drained rings
+  constexpr int kMaxSplits = (kGenWarps * Lay<G, D>::kRing / 4 - G) / (2 * G);
+  if (sp > kMaxSplits) sp = kMaxSplits;
   if (sp < 1) sp = 1;
   pps = static_cast<int>((max_pages + sp - 1) / sp);
   splits = (max_pages + pps - 1) / pps;
@@ -392,8 +492,49 @@ size_t gen_workspace(int batch, int hkv, int max_pages, int num_sms) {
   plan<G, D>(batch, hkv, max_pages, num_sms, splits, pps);
   size_t off = PKV_STATUS_BYTES;
   off += (static_cast<size_t>(batch) * hkv * 4 + 255) / 256 * 256;
-  off += static_cast<size_t>(batch) * hkv * splits * Gen<G, D>::kState * 4;
+  off += static_cast<size_t>(batch) * hkv * splits * G * (D + 4) * 4;  // records [G][D + 4]
   return off;
+}
+
+// Tensor maps of the two pools for the tensor-core kernel: [tiles][16 rows][D]
+// with tile = page * hkv + KV head, boxes of 64 dims x 16 rows (128-byte rows,
+// 128-byte swizzle).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encoder() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+int page_maps(const void* k_pages, const void* v_pages, int head_dim, int num_pages, int hkv, CUtensorMap* kmap,
+              CUtensorMap* vmap) {
+  const long long tiles = static_cast<long long>(num_pages) * hkv;
+  if (tiles > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;  // tile coordinates are 32-bit
+  EncodeTiledFn enc = encoder();
+  if (enc == nullptr) return PKV_ERR_CUDA;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(kPageSize),
+                              static_cast<cuuint64_t>(tiles)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * 2,
+                                 static_cast<cuuint64_t>(head_dim) * 2 * kPageSize};
+  const cuuint32_t box[3] = {64, kPageSize, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const void* pools[2] = {k_pages, v_pages};
+  CUtensorMap* maps[2] = {kmap, vmap};
+  for (int i = 0; i < 2; ++i)
+    if (enc(maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pools[i]), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return PKV_ERR_CUDA;
+  return PKV_OK;
 }
 
 template <int G, int D>
@@ -402,7 +543,7 @@ int gen_launch(const void* q, const void* k_pages, const void* v_pages, const in
                int num_pages, void* workspace, int num_sms, cudaStream_t stream) {
   int splits = 1, pps = 1;
   plan<G, D>(batch, hkv, max_pages, num_sms, splits, pps);
-  const size_t smem = Gen<G, D>::smem_bytes(pps);
+  const size_t smem = Lay<G, D>::smem_bytes(pps);
   if (smem > 227 * 1024) return PKV_ERR_UNSUPPORTED;
   static bool attr_set[64] = {};
   int dev = 0;
@@ -432,7 +573,11 @@ int gen_launch(const void* q, const void* k_pages, const void* v_pages, const in
   a.counters = reinterpret_cast<int*>(ws + PKV_STATUS_BYTES);
   a.records = reinterpret_cast<float*>(ws + PKV_STATUS_BYTES + (static_cast<size_t>(batch) * hkv * 4 + 255) / 256 * 256);
   const dim3 grid(static_cast<unsigned>(splits), static_cast<unsigned>(hkv), static_cast<unsigned>(batch));
-  return launch_pdl(decode_generic_kernel<G, D>, grid, dim3(kGenThreads), smem, stream, a) == cudaSuccess
+  CUtensorMap kmap, vmap;
+  const int rc = page_maps(k_pages, v_pages, D, num_pages, hkv, &kmap, &vmap);
+  if (rc != PKV_OK) return rc;
+  return launch_pdl(decode_generic_kernel<G, D>, grid, dim3(kGenThreads), smem, stream, kmap, vmap, a) ==
+                 cudaSuccess
              ? PKV_OK
              : PKV_ERR_CUDA;
 }

@@ -152,3 +152,4 @@ def test_piece_relative_schedule_deadlocks_on_one_page_runs():
     # that are held at a piece boundary behind it
     assert not all_ctas_finish(MIXES["short_then_long"], assign_piece)
     assert all_ctas_finish(MIXES["short_then_long"], assign_share)
+
