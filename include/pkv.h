@@ -232,8 +232,8 @@ int pkv_decode_append_attn(const void* q, const void* k_new, const void* v_new, 
  *    even), each pair (x1, x2) = (k[i], k[i + head_dim/2]) evaluated in fp32
  *    as y1 = fmaf(x1, c, -(x2 * s)), y2 = fmaf(x2, c, x1 * s), each product
  *    rounded to fp32 first (so the written bits are defined exactly);
- *  - every query row q[b][h] is rotated the same way in fp32 (and kept in
- *    fp32) before the scores;
+ *  - every query row q[b][h] is rotated the same way in fp32, then rounded to
+ *    bf16 (ties to even), the operand precision of the score product;
  *  - v_new is written unchanged; everything else is as pkv_decode_append_attn.
  *
  *  rope_cos_sin: fp32 [rope_max_pos][head_dim], row p = cos(p w_i) for

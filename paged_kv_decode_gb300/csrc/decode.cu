@@ -17,22 +17,26 @@
 //  * A CTA's share is cut into pieces, one per (request, KV head) it touches.
 //    Its consumer warps take the share's pages round-robin (page f of the share
 //    goes to consumer (f - lo) mod kCons, across piece boundaries). A producer warp
-//    fills each consumer's ring of shared-memory stages with 1-D bulk copies
-//    (cp.async.bulk, one 4 KiB K tile and one 4 KiB V tile per page) that
-//    complete on the stage's full barrier; consumers release stages through
-//    empty barriers.
-//  * Both query heads of the GQA group are computed from one K/V read. Scores
-//    use packed fp32 FMAs (two dims per instruction); the softmax is online in
-//    the log2 domain (q pre-scaled by scale * log2 e); tokens past seq_len in
-//    the last page are masked before they can touch the max or the sum, so
-//    unused slots may hold anything, NaN included.
+//    fills each consumer's ring of shared-memory stages with tiled TMA copies
+//    (cp.async.bulk.tensor, per page two 16-row x 64-dim boxes of the K tile and
+//    two of the V tile, 128-byte swizzle, evict-first) that complete on the
+//    stage's full barrier; consumers release stages through empty barriers.
+//  * Both query heads of the GQA group are computed from one K/V read, the two
+//    products of a page as warp-level bf16 tensor-core MMAs with fp32
+//    accumulation (pkv_mma.cuh): scores S^T = K Q^T with the group's rows as
+//    two of the B operand's 8 columns, softmax online in registers in the log2
+//    domain (scale * log2 e applied to the fp32 scores), p rounded to bf16 for
+//    the value product O^T += V^T P^T. Tokens past seq_len in the last page are
+//    masked in the scores and in the value operand's registers, so unused slots
+//    may hold anything, NaN included.
 //  * Optional fused append: the producer lane that copies a request's last
 //    page first writes the request's new K/V row for that head into it
 //    (generic stores, then a proxy fence so its own bulk copy sees them). With
 //    a cos/sin table the whole producer warp writes the row instead, rotating
 //    the key (rotary position embedding at the new token's position, pairs
 //    (i, i + 64), fp32, rounded to bf16), and each piece's query rows are
-//    rotated the same way after they are staged.
+//    rotated the same way after they are staged (then rounded to bf16 as the
+//    MMA operand).
 //  * The query rows of the next piece are copied into shared memory (cp.async)
 //    while the current piece streams, so a piece boundary costs no round trip.
 //  * At the end of a piece the warps merge through shared memory. A piece that
@@ -58,6 +62,8 @@
 
 #include "pkv_device.cuh"
 #include "pkv_kernels.h"
+#include "pkv_mma.cuh"
+#include "pkv_tc.cuh"
 
 namespace pkv {
 
@@ -95,9 +101,9 @@ constexpr int kQBufBytes = kGroup * kRowBytes;             // query rows of one 
 constexpr int kSmemQ = 2 * kQBufBytes;                     // this piece's rows and the next piece's
 constexpr int kCsBytes = kHeadDim * 4;                     // one cos/sin table row (fp32 cos[64], sin[64])
 constexpr int kSmemCs = 2 * kCsBytes;                      // rows for this piece's and the next piece's position
-constexpr int kSmemPbuf = kCons * kPageSize * 4 * 4;       // per warp: [16 tokens][p0, p0, p1, p1]
 constexpr int kSmemMisc = 16;                              // flag words
-constexpr int kSmemFixed = kSmemRing + kSmemBars + kSmemMerge + kSmemQ + kSmemCs + kSmemPbuf + kSmemMisc;
+constexpr int kSmemAlign = 1024;                           // the ring starts on a 1024-byte boundary (swizzle atoms)
+constexpr int kSmemFixed = kSmemAlign + kSmemRing + kSmemBars + kSmemMerge + kSmemQ + kSmemCs + kSmemMisc;
 constexpr int kPieceBytes = kPieceFloats * 4;
 constexpr int kMergeCap = kSmemRing / kPieceBytes;         // records staged per batch of a counted merge
 constexpr int kSplitWords = kGroup * kHeadDim + 8;         // tagged words of a polled record: o[2][128], then
@@ -171,28 +177,6 @@ __device__ __forceinline__ int cta_of(long long f, long long T, int G) {
 }
 __device__ __forceinline__ long long share_lo(int c, long long T, int G) { return static_cast<long long>(c) * T / G; }
 
-// V accumulation for the tokens of one half-warp; kChecked masks tokens >= n_valid.
-template <bool kChecked>
-__device__ __forceinline__ void pv_tokens(uint32_t vrow0, uint32_t prow0, int t0, int n_valid, float2 (&o)[2][4]) {
-#pragma unroll
-  for (int tt = 0; tt < 8; ++tt) {
-    if (kChecked && t0 + tt >= n_valid) break;
-    const uint4 u = lds128(vrow0 + tt * kRowBytes);
-    const float4 pp = lds128f(prow0 + tt * 16);
-    const float2 ph0 = make_float2(pp.x, pp.y);
-    const float2 ph1 = make_float2(pp.z, pp.w);
-    const float2 v0 = bf2_to_f2(u.x), v1 = bf2_to_f2(u.y), v2 = bf2_to_f2(u.z), v3 = bf2_to_f2(u.w);
-    o[0][0] = __ffma2_rn(ph0, v0, o[0][0]);
-    o[0][1] = __ffma2_rn(ph0, v1, o[0][1]);
-    o[0][2] = __ffma2_rn(ph0, v2, o[0][2]);
-    o[0][3] = __ffma2_rn(ph0, v3, o[0][3]);
-    o[1][0] = __ffma2_rn(ph1, v0, o[1][0]);
-    o[1][1] = __ffma2_rn(ph1, v1, o[1][1]);
-    o[1][2] = __ffma2_rn(ph1, v2, o[1][2]);
-    o[1][3] = __ffma2_rn(ph1, v3, o[1][3]);
-  }
-}
-
 // Polled records are 32-bit words: an fp32 value rounded to nearest (even) at
 // 15 mantissa bits, with the tag in the freed low byte. Each word is one
 // single-copy-atomic access, so a reader that sees the tag sees the value,
@@ -248,16 +232,18 @@ __device__ __forceinline__ int request_of(long long f, const int* pref, int batc
 // kPolled: the polled merge, else the counted one. Each combination is its own instantiation, so a path carries no code (and no
 // registers) for the others.
 template <bool kFused, bool kRope, bool kPolled>
-__global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(const DecodeArgs a) {
-  extern __shared__ __align__(128) unsigned char smem[];
+__global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(const __grid_constant__ CUtensorMap kmap,
+                                                                             const __grid_constant__ CUtensorMap vmap,
+                                                                             const DecodeArgs a) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((kSmemAlign - (smem_u32(smem_raw) & (kSmemAlign - 1))) & (kSmemAlign - 1));
   unsigned char* ring = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kSmemRing);
   uint64_t* empty = full + kStages;
   float* merge = reinterpret_cast<float*>(smem + kSmemRing + kSmemBars);
   unsigned char* qbuf = reinterpret_cast<unsigned char*>(merge + kMergeFloats);
   unsigned char* csbuf = qbuf + kSmemQ;
-  float* pbuf = reinterpret_cast<float*>(csbuf + kSmemCs);
-  int* flag = reinterpret_cast<int*>(pbuf + kCons * kPageSize * 4);  // [0..1] merge flags, [2] a wait failed
+  int* flag = reinterpret_cast<int*>(csbuf + kSmemCs);  // [0..1] merge flags, [2] a wait failed
   int* pref = flag + kSmemMisc / 4;
   int* sl = pref + a.batch + 1;
 
@@ -265,6 +251,10 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int batch = a.batch;
+  if (tid == kConsThreads) {  // the producer's first lane: descriptors before its first copies
+    prefetch_tensormap(&kmap);
+    prefetch_tensormap(&vmap);
+  }
 
   if (tid < kStages) {
     mbar_init(&full[tid], 1);
@@ -461,11 +451,14 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
               }
               fence_proxy_async_global();
             }
-            const size_t off = (static_cast<size_t>(pid) * kKVHeads + hh) * (kTileBytes / 2);
+            const int z = pid * kKVHeads + hh;  // tile of the pool
             unsigned char* dst = ring + slot * kStageBytes;
             mbar_arrive_expect_tx(&full[slot], kStageBytes);
-            bulk_g2s_hint(dst, a.k_pages + off, kTileBytes, &full[slot], policy);
-            bulk_g2s_hint(dst + kTileBytes, a.v_pages + off, kTileBytes, &full[slot], policy);
+#pragma unroll
+            for (int x = 0; x < kHeadDim / 64; ++x) {  // 16 rows x 64 dims per box, 128-byte swizzle
+              tma_load_3d_hint(dst + x * 2048, &kmap, 64 * x, 0, z, &full[slot], policy);
+              tma_load_3d_hint(dst + kTileBytes + x * 2048, &vmap, 64 * x, 0, z, &full[slot], policy);
+            }
           }
         }
         __syncwarp();
@@ -480,13 +473,10 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
   }
 
   // ============================================================== consumer warps
-  const int qq = lane & 3;         // quarter of the row for the score pass
-  const int tp = (lane >> 2) & 1;  // token parity: rotates the chunk order to avoid bank conflicts
-  const int head_mine = qq & 1;    // query head whose score this lane ends up holding
-  const int t_mine = (qq >> 1) * 8 + (lane >> 2);  // token whose score this lane holds
-  const int hf = lane >> 4;        // half-warp: tokens hf*8 .. hf*8+7 for the V pass
-  const int dl = lane & 15;        // dims dl*8 .. dl*8+7 for the V pass
-  const uint32_t pb = smem_u32(pbuf + warp * kPageSize * 4);
+  constexpr int kKS = kHeadDim / 16;        // 16-dim steps of both MMA products
+  const int r = lane >> 2, cq = lane & 3;  // MMA fragment row and column pair of this lane
+  uint32_t koff[kKS], voff[kKS];
+  mma_offsets<kKS>(koff, voff);
 
   if (a.early) {
     grid_dependency_wait();
@@ -552,69 +542,48 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
     bool sp_two = false;
     if (!kPolled && !complete) span_of(b, h, sp_cfirst, sp_n, sp_two);  // before the stream, off the critical path
 
-    // query rows of both heads of the group, in this lane's chunk order, rotated
-    // (with a cos/sin table) and pre-scaled. The lane's chunks jj and jj + 2
-    // (jj < 2) are chunks c and c + 8 of the row: dims 8c .. 8c+7 pair with dims + 64.
+    // Q^T as the B operand of the score MMA: lane (r, cq) holds head r's dims 16 ks + 2 cq (+1) and
+    // 16 ks + 8 + 2 cq (+1); rows r >= kGroup are zero. With a cos/sin table the staged rows are rotated
+    // here (pairs (i, i + 64) sit in steps ks and ks + 4 of the same lane) in fp32, each product rounded
+    // first, then rounded to bf16.
     const uint32_t qcur = qb + (j & 1) * kQBufBytes;
     const uint32_t ccur = csb + (j & 1) * kCsBytes;
-    float2 q2[4][4][2];
+    uint32_t qf[kKS][2];
     if constexpr (!kRope) {
 #pragma unroll
-      for (int i = 0; i < kGroup; ++i) {
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const uint4 u = lds128(qcur + i * kRowBytes + (qq + 4 * (jj ^ tp)) * 16);
-          const float2 sc = make_float2(a.qscale, a.qscale);
-          q2[jj][0][i] = __fmul2_rn(bf2_to_f2(u.x), sc);
-          q2[jj][1][i] = __fmul2_rn(bf2_to_f2(u.y), sc);
-          q2[jj][2][i] = __fmul2_rn(bf2_to_f2(u.z), sc);
-          q2[jj][3][i] = __fmul2_rn(bf2_to_f2(u.w), sc);
-        }
+      for (int ks = 0; ks < kKS; ++ks) {
+        qf[ks][0] = r < kGroup ? lds32(qcur + r * kRowBytes + (16 * ks + 2 * cq) * 2) : 0u;
+        qf[ks][1] = r < kGroup ? lds32(qcur + r * kRowBytes + (16 * ks + 8 + 2 * cq) * 2) : 0u;
       }
     } else {
+      float2 x[kKS][2];
 #pragma unroll
-      for (int i = 0; i < kGroup; ++i) {
-        float2 x[4][4];
+      for (int ks = 0; ks < kKS; ++ks) {
+        x[ks][0] = r < kGroup ? bf2_to_f2(lds32(qcur + r * kRowBytes + (16 * ks + 2 * cq) * 2)) : make_float2(0.f, 0.f);
+        x[ks][1] = r < kGroup ? bf2_to_f2(lds32(qcur + r * kRowBytes + (16 * ks + 8 + 2 * cq) * 2)) : make_float2(0.f, 0.f);
+      }
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const uint4 u = lds128(qcur + i * kRowBytes + (qq + 4 * (jj ^ tp)) * 16);
-          x[jj][0] = bf2_to_f2(u.x);
-          x[jj][1] = bf2_to_f2(u.y);
-          x[jj][2] = bf2_to_f2(u.z);
-          x[jj][3] = bf2_to_f2(u.w);
+      for (int ks = 0; ks < kKS / 2; ++ks)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int d = 16 * ks + 8 * e + 2 * cq;  // dims d, d + 1 pair with d + 64, d + 65
+          const float2 cs = lds64f(ccur + d * 4), sn = lds64f(ccur + kCsBytes / 2 + d * 4);
+          const float2 lo = x[ks][e], hi = x[ks + kKS / 2][e];
+          const float2 t1 = __fmul2_rn(hi, sn), t2 = __fmul2_rn(lo, sn);
+          x[ks][e] = __ffma2_rn(lo, cs, make_float2(-t1.x, -t1.y));
+          x[ks + kKS / 2][e] = __ffma2_rn(hi, cs, t2);
         }
 #pragma unroll
-        for (int jj = 0; jj < 2; ++jj) {  // chunk jj (index c < 8) pairs with chunk jj + 2 (index c + 8)
-          const int c = qq + 4 * (jj ^ tp);
-          const float4 c0 = lds128f(ccur + c * 32), c1 = lds128f(ccur + c * 32 + 16);
-          const float4 s0 = lds128f(ccur + kCsBytes / 2 + c * 32), s1 = lds128f(ccur + kCsBytes / 2 + c * 32 + 16);
-          const float2 cs[4] = {make_float2(c0.x, c0.y), make_float2(c0.z, c0.w), make_float2(c1.x, c1.y),
-                                make_float2(c1.z, c1.w)};
-          const float2 sn[4] = {make_float2(s0.x, s0.y), make_float2(s0.z, s0.w), make_float2(s1.x, s1.y),
-                                make_float2(s1.z, s1.w)};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 lo = x[jj][e], hi = x[jj + 2][e];
-            const float2 t1 = __fmul2_rn(hi, sn[e]), t2 = __fmul2_rn(lo, sn[e]);
-            x[jj][e] = __ffma2_rn(lo, cs[e], make_float2(-t1.x, -t1.y));
-            x[jj + 2][e] = __ffma2_rn(hi, cs[e], t2);
-          }
-        }
-        const float2 sc = make_float2(a.qscale, a.qscale);
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) q2[jj][e][i] = __fmul2_rn(x[jj][e], sc);
+      for (int ks = 0; ks < kKS; ++ks) {
+        qf[ks][0] = pack_bf16x2(x[ks][0].x, x[ks][0].y);
+        qf[ks][1] = pack_bf16x2(x[ks][1].x, x[ks][1].y);
       }
     }
 
-    float2 mrun = make_float2(-CUDART_INF_F, -CUDART_INF_F);
-    float lsum = 0.f;
-    float2 o[2][4];
+    float o[kKS][4];  // O^T: dims 16 ks + r (+8) x heads 2 cq, 2 cq + 1 (cq = 0: the group's two heads)
 #pragma unroll
-    for (int i = 0; i < 2; ++i)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) o[i][e] = make_float2(0.f, 0.f);
+    for (int ks = 0; ks < kKS; ++ks) o[ks][0] = o[ks][1] = o[ks][2] = o[ks][3] = 0.f;
+    float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
 
     const int w0 = static_cast<int>((pc.fstart - lo) % kCons);  // consumer of the piece's first page
     for (int p = pc.p0 + (warp - w0 + kCons) % kCons; p < pc.p1; p += kCons) {
@@ -632,109 +601,33 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
         const int rem = sl[b] - p * kPageSize;
         const int n_valid = rem < kPageSize ? rem : kPageSize;
         const uint32_t kt = smem_u32(ring + slot * kStageBytes);
-        const uint32_t vt = kt + kTileBytes;
-        // ---- scores: lanes (token group of 4) x (quarter of the row), two passes of 8 tokens
-        float2 acc[2][2];
-#pragma unroll
-        for (int ps = 0; ps < 2; ++ps)
-#pragma unroll
-          for (int i = 0; i < 2; ++i) acc[ps][i] = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t coff = (qq + 4 * (j ^ tp)) * 16;
-#pragma unroll
-          for (int ps = 0; ps < 2; ++ps) {
-            const uint4 u = lds128(kt + (ps * 8 + (lane >> 2)) * kRowBytes + coff);
-            const float2 k0 = bf2_to_f2(u.x), k1 = bf2_to_f2(u.y), k2 = bf2_to_f2(u.z), k3 = bf2_to_f2(u.w);
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-              acc[ps][i] = __ffma2_rn(q2[j][0][i], k0, acc[ps][i]);
-              acc[ps][i] = __ffma2_rn(q2[j][1][i], k1, acc[ps][i]);
-              acc[ps][i] = __ffma2_rn(q2[j][2][i], k2, acc[ps][i]);
-              acc[ps][i] = __ffma2_rn(q2[j][3][i], k3, acc[ps][i]);
-            }
-          }
-        }
-        const float a00 = acc[0][0].x + acc[0][0].y, a01 = acc[0][1].x + acc[0][1].y;
-        const float a10 = acc[1][0].x + acc[1][0].y, a11 = acc[1][1].x + acc[1][1].y;
-        // transpose-reduce over the 4 lanes of a token group: lane qq ends with
-        // the full score of (pass qq>>1, head qq&1)
-        const bool hi_pass = (qq & 2) != 0;
-        float keep0 = hi_pass ? a10 : a00, keep1 = hi_pass ? a11 : a01;
-        const float send0 = hi_pass ? a00 : a10, send1 = hi_pass ? a01 : a11;
-        keep0 += __shfl_xor_sync(kFull, send0, 2);
-        keep1 += __shfl_xor_sync(kFull, send1, 2);
-        const float keeph = head_mine ? keep1 : keep0;
-        const float sendh = head_mine ? keep0 : keep1;
-        float s = keeph + __shfl_xor_sync(kFull, sendh, 1);
-        if (t_mine >= n_valid) s = -CUDART_INF_F;
-
-        // ---- online softmax (log2 domain)
-        float mx = s;
-        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
-        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
-        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
-        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
-        const float mo = __shfl_xor_sync(kFull, mx, 1);
-        const float2 mpage = head_mine ? make_float2(mo, mx) : make_float2(mx, mo);
-        const float2 mnew = make_float2(fmaxf(mrun.x, mpage.x), fmaxf(mrun.y, mpage.y));
-        const float2 alpha = make_float2(ex2(mrun.x - mnew.x), ex2(mrun.y - mnew.y));
-        mrun = mnew;
-        const float pj = ex2(s - (head_mine ? mnew.y : mnew.x));
-        lsum = lsum * (head_mine ? alpha.y : alpha.x) + pj;
-        {
-          const uint32_t dst = pb + t_mine * 16 + head_mine * 8;
-          asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(dst), "f"(pj), "f"(pj) : "memory");
-        }
-        const float2 ax = make_float2(alpha.x, alpha.x), ay = make_float2(alpha.y, alpha.y);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          o[0][e] = __fmul2_rn(o[0][e], ax);
-          o[1][e] = __fmul2_rn(o[1][e], ay);
-        }
-        __syncwarp();
-
-        // ---- values
-        const uint32_t vrow0 = vt + (hf * 8) * kRowBytes + dl * 16;
-        const uint32_t prow0 = pb + (hf * 8) * 16;
-        if (n_valid == kPageSize) pv_tokens<false>(vrow0, prow0, hf * 8, n_valid, o);
-        else pv_tokens<true>(vrow0, prow0, hf * 8, n_valid, o);
+        mma_page<kKS>(kt, kt + kTileBytes, koff, voff, qf, n_valid, a.qscale, o, m0, m1, l0, l1);
       }
       __syncwarp();  // the stage and the p buffer are free again
       if (lane == 0 && !failed) mbar_arrive(&empty[slot]);
       ++k;
     }
 
-    // ---- warp totals: combine the two half-warps, sum l over the lanes of each head
+    // ---- warp record: lanes cq = 0 hold the group's two heads (MMA columns 0 and 1); l summed over r
 #pragma unroll
-    for (int i = 0; i < 2; ++i)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        o[i][e].x += __shfl_xor_sync(kFull, o[i][e].x, 16);
-        o[i][e].y += __shfl_xor_sync(kFull, o[i][e].y, 16);
-      }
-    float lh = lsum;
-    lh += __shfl_xor_sync(kFull, lh, 2);
-    lh += __shfl_xor_sync(kFull, lh, 4);
-    lh += __shfl_xor_sync(kFull, lh, 8);
-    lh += __shfl_xor_sync(kFull, lh, 16);
-    const float lother = __shfl_xor_sync(kFull, lh, 1);
-    const float l0 = head_mine ? lother : lh;
-    const float l1 = head_mine ? lh : lother;
-
+    for (int m = 4; m < 32; m <<= 1) {
+      l0 += __shfl_xor_sync(kFull, l0, m);
+      l1 += __shfl_xor_sync(kFull, l1, m);
+    }
     float* mw = merge + warp * kPieceFloats;
-    if (lane < 16) {
+    if (cq == 0) {
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        float4* dst = reinterpret_cast<float4*>(mw + i * kRec + 4 + lane * 8);
-        dst[0] = make_float4(o[i][0].x, o[i][0].y, o[i][1].x, o[i][1].y);
-        dst[1] = make_float4(o[i][2].x, o[i][2].y, o[i][3].x, o[i][3].y);
+      for (int ks = 0; ks < kKS; ++ks) {
+        mw[4 + 16 * ks + r] = o[ks][0];
+        mw[4 + 16 * ks + r + 8] = o[ks][2];
+        mw[kRec + 4 + 16 * ks + r] = o[ks][1];
+        mw[kRec + 4 + 16 * ks + r + 8] = o[ks][3];
       }
     }
     if (lane == 0) {
-      mw[0] = mrun.x;
+      mw[0] = m0;
       mw[1] = l0;
-      mw[kRec] = mrun.y;
+      mw[kRec] = m1;
       mw[kRec + 1] = l1;
     }
     consumer_sync();
@@ -1094,7 +987,7 @@ int launch_decode(const void* q, const void* k_new, const void* v_new, const voi
   // lengths); the counted merge for few pairs over many CTAs.
   const int grid = num_sms * kDecCtasPerSm < kMaxGrid ? num_sms * kDecCtasPerSm : kMaxGrid;
   const bool polled = grid <= kPollMax * batch * kKVHeads;
-  using Kern = void (*)(const DecodeArgs);
+  using Kern = void (*)(const CUtensorMap, const CUtensorMap, const DecodeArgs);
   static const Kern kKerns[2][3] = {
       {decode_kernel<false, false, false>, decode_kernel<true, false, false>, decode_kernel<true, true, false>},
       {decode_kernel<false, false, true>, decode_kernel<true, false, true>, decode_kernel<true, true, true>}};
@@ -1139,9 +1032,13 @@ int launch_decode(const void* q, const void* k_new, const void* v_new, const voi
   const int slots = 2 * (num_sms * kDecCtasPerSm < kMaxGrid ? num_sms * kDecCtasPerSm : kMaxGrid);
   a.tagged = reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(a.partials) +
                                          static_cast<size_t>(slots) * kPieceFloats * 4);
+  CUtensorMap kmap, vmap;
+  const int rc = encode_page_maps(k_pages, v_pages, kHeadDim, num_pages, kKVHeads, &kmap, &vmap);
+  if (rc != PKV_OK) return rc;
   const int launch_grid = num_sms * occ < kMaxGrid ? num_sms * occ : kMaxGrid;
-  return launch_pdl(kern, dim3(launch_grid), dim3(kDecThreads), smem, stream, a) == cudaSuccess ? PKV_OK
-                                                                                                : PKV_ERR_CUDA;
+  return launch_pdl(kern, dim3(launch_grid), dim3(kDecThreads), smem, stream, kmap, vmap, a) == cudaSuccess
+             ? PKV_OK
+             : PKV_ERR_CUDA;
 }
 
 }  // namespace pkv

@@ -55,6 +55,7 @@
 
 #include "pkv_device.cuh"
 #include "pkv_kernels.h"
+#include "pkv_mma.cuh"
 #include "pkv_tc.cuh"
 
 namespace pkv {
@@ -215,112 +216,6 @@ __device__ __forceinline__ void finish_split(const GenArgs& a, const unsigned ch
   if (tid == 0) *counter = 0;
 }
 
-// Byte offset of 16-byte chunk c of token row t in a tile written by the
-// 128-byte swizzled TMA boxes: box c / 8 (2 KiB each, 1024-byte aligned), row t
-// of 128 bytes, chunk (c mod 8) XOR (t mod 8).
-__device__ __forceinline__ uint32_t swz(int t, int c) {
-  return static_cast<uint32_t>((c >> 3) * 2048 + t * 128 + (((c & 7) ^ (t & 7)) << 4));
-}
-__device__ __forceinline__ void ldsm4(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr)
-               : "memory");
-}
-__device__ __forceinline__ void ldsm4_t(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr)
-               : "memory");
-}
-__device__ __forceinline__ uint32_t movm_t(uint32_t x) {
-  uint32_t y;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
-  return y;
-}
-// c += a * b, m16n8k16, bf16 operands, fp32 accumulators
-__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-      "{%0, %1, %2, %3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// One page of the tensor-core path: the scores of its 16 tokens for the 8 head
-// columns, the online-softmax update of this lane's two heads (2c, 2c + 1), and
-// the value product. kt, vt: shared addresses of the page's swizzled K and V
-// tiles; nv: its tokens before seq_len.
-template <int KS>
-__device__ __forceinline__ void mma_page(uint32_t kt, uint32_t vt, const uint32_t (&koff)[KS],
-                                         const uint32_t (&voff)[KS], const uint32_t (&qf)[KS][2], int nv,
-                                         float qscale, float (&o)[KS][4], float& m0, float& m1, float& l0,
-                                         float& l1) {
-  const int lane = threadIdx.x & 31, r = lane >> 2, c = lane & 3;
-    // ---- scores (two accumulators: the k-steps form two dependent chains)
-    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      uint32_t kf[4];
-      ldsm4(kt + koff[ks], kf);
-      if (ks & 1)
-        mma_bf16(sb, kf, qf[ks][0], qf[ks][1]);
-      else
-        mma_bf16(sa, kf, qf[ks][0], qf[ks][1]);
-    }
-    const bool v0 = r < nv, v1 = r + 8 < nv;
-    const float s00 = v0 ? (sa[0] + sb[0]) * qscale : -CUDART_INF_F;  // token r, head 2c
-    const float s01 = v0 ? (sa[1] + sb[1]) * qscale : -CUDART_INF_F;  // token r, head 2c + 1
-    const float s10 = v1 ? (sa[2] + sb[2]) * qscale : -CUDART_INF_F;  // token r + 8
-    const float s11 = v1 ? (sa[3] + sb[3]) * qscale : -CUDART_INF_F;
-
-    // ---- online softmax of heads 2c, 2c + 1 over the page's 16 tokens
-    float x0 = fmaxf(s00, s10), x1 = fmaxf(s01, s11);
-#pragma unroll
-    for (int m = 4; m < 32; m <<= 1) {
-      x0 = fmaxf(x0, __shfl_xor_sync(kGenFull, x0, m));
-      x1 = fmaxf(x1, __shfl_xor_sync(kGenFull, x1, m));
-    }
-    const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
-    const uint32_t pk0 = pack_bf16x2(ex2(s00 - n0), ex2(s01 - n1));  // token r
-    const uint32_t pk1 = pack_bf16x2(ex2(s10 - n0), ex2(s11 - n1));  // token r + 8
-    const float2 q0 = bf2_to_f2(pk0), q1 = bf2_to_f2(pk1);
-    if (__any_sync(kGenFull, n0 != m0 || n1 != m1)) {
-      const float al0 = ex2(m0 - n0), al1 = ex2(m1 - n1);  // 0 on the first page
-      l0 *= al0;
-      l1 *= al1;
-#pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        o[ks][0] *= al0;
-        o[ks][1] *= al1;
-        o[ks][2] *= al0;
-        o[ks][3] *= al1;
-      }
-      m0 = n0;
-      m1 = n1;
-    }
-    l0 += q0.x + q1.x;
-    l1 += q0.y + q1.y;
-
-    // ---- values: P^T as the B operand (head r, tokens 2c, 2c + 1 and 8 + 2c, 9 + 2c)
-    const uint32_t pb0 = movm_t(pk0), pb1 = movm_t(pk1);
-    uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;  // value rows past seq_len read as zero
-    if (nv < kPageSize) {
-      mlo = (2 * c < nv ? 0x0000ffffu : 0u) | (2 * c + 1 < nv ? 0xffff0000u : 0u);
-      mhi = (2 * c + 8 < nv ? 0x0000ffffu : 0u) | (2 * c + 9 < nv ? 0xffff0000u : 0u);
-    }
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      uint32_t vf[4];
-      ldsm4_t(vt + voff[ks], vf);
-      vf[0] &= mlo;
-      vf[1] &= mlo;
-      vf[2] &= mhi;
-      vf[3] &= mhi;
-      mma_bf16(o[ks], vf, pb0, pb1);
-    }
-}
-
 template <int G, int D>
 __global__ void __launch_bounds__(kGenThreads) decode_generic_kernel(const __grid_constant__ CUtensorMap kmap,
                                                                  const __grid_constant__ CUtensorMap vmap,
@@ -336,6 +231,10 @@ __global__ void __launch_bounds__(kGenThreads) decode_generic_kernel(const __gri
   const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int hq0 = h * a.gq;
   const int nq = a.hkv * a.gq;
+  if (tid == 0) {  // descriptors ahead of the first copies
+    prefetch_tensormap(&kmap);
+    prefetch_tensormap(&vmap);
+  }
 
   grid_dependency_wait();
   allow_dependents();
@@ -389,7 +288,6 @@ __global__ void __launch_bounds__(kGenThreads) decode_generic_kernel(const __gri
     for (int i = 0; i < S::kStages && i < nw; ++i) issue(i);
 
   const int r = lane >> 2, c = lane & 3;  // fragment row and column pair
-  const int mi = lane >> 3, mr = lane & 7;  // ldmatrix: matrix and row this lane addresses
   // Q^T as the B operand: head r, dims 16 ks + 2c (+1) and 16 ks + 8 + 2c (+1)
   uint32_t qf[S::kKS][2];
   {
@@ -402,15 +300,8 @@ __global__ void __launch_bounds__(kGenThreads) decode_generic_kernel(const __gri
       qf[ks][1] = live ? __ldg(qrow + 8 * ks + 4 + c) : 0u;
     }
   }
-  // ldmatrix row addresses inside a tile: K as the A operand (matrices: tokens 0-7 /
-  // 8-15 x the two 8-dim halves of a 16-dim step), V transposed (same four blocks in
-  // the order the A operand of the value product wants)
   uint32_t koff[S::kKS], voff[S::kKS];
-#pragma unroll
-  for (int ks = 0; ks < S::kKS; ++ks) {
-    koff[ks] = swz(mr + ((mi & 1) << 3), 2 * ks + (mi >> 1));
-    voff[ks] = swz(mr + ((mi >> 1) << 3), 2 * ks + (mi & 1));
-  }
+  mma_offsets<S::kKS>(koff, voff);
 
   float o[S::kKS][4];  // O^T: dims 16 ks + r (+8) x heads 2c, 2c + 1
 #pragma unroll
@@ -496,47 +387,6 @@ size_t gen_workspace(int batch, int hkv, int max_pages, int num_sms) {
   return off;
 }
 
-// Tensor maps of the two pools for the tensor-core kernel: [tiles][16 rows][D]
-// with tile = page * hkv + KV head, boxes of 64 dims x 16 rows (128-byte rows,
-// 128-byte swizzle).
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encoder() {
-  static EncodeTiledFn fn = nullptr;
-  if (fn == nullptr) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
-  return fn;
-}
-
-int page_maps(const void* k_pages, const void* v_pages, int head_dim, int num_pages, int hkv, CUtensorMap* kmap,
-              CUtensorMap* vmap) {
-  const long long tiles = static_cast<long long>(num_pages) * hkv;
-  if (tiles > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;  // tile coordinates are 32-bit
-  EncodeTiledFn enc = encoder();
-  if (enc == nullptr) return PKV_ERR_CUDA;
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(kPageSize),
-                              static_cast<cuuint64_t>(tiles)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * 2,
-                                 static_cast<cuuint64_t>(head_dim) * 2 * kPageSize};
-  const cuuint32_t box[3] = {64, kPageSize, 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  const void* pools[2] = {k_pages, v_pages};
-  CUtensorMap* maps[2] = {kmap, vmap};
-  for (int i = 0; i < 2; ++i)
-    if (enc(maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pools[i]), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return PKV_ERR_CUDA;
-  return PKV_OK;
-}
-
 template <int G, int D>
 int gen_launch(const void* q, const void* k_pages, const void* v_pages, const int32_t* block_table,
                const int32_t* seq_lens, void* out, float scale, int batch, int hkv, int gq, int max_pages,
@@ -574,7 +424,7 @@ int gen_launch(const void* q, const void* k_pages, const void* v_pages, const in
   a.records = reinterpret_cast<float*>(ws + PKV_STATUS_BYTES + (static_cast<size_t>(batch) * hkv * 4 + 255) / 256 * 256);
   const dim3 grid(static_cast<unsigned>(splits), static_cast<unsigned>(hkv), static_cast<unsigned>(batch));
   CUtensorMap kmap, vmap;
-  const int rc = page_maps(k_pages, v_pages, D, num_pages, hkv, &kmap, &vmap);
+  const int rc = encode_page_maps(k_pages, v_pages, D, num_pages, hkv, &kmap, &vmap);
   if (rc != PKV_OK) return rc;
   return launch_pdl(decode_generic_kernel<G, D>, grid, dim3(kGenThreads), smem, stream, kmap, vmap, a) ==
                  cudaSuccess
@@ -583,6 +433,50 @@ int gen_launch(const void* q, const void* k_pages, const void* v_pages, const in
 }
 
 }  // namespace
+
+// Tensor maps of the two pools for the tensor-core kernel: [tiles][16 rows][D]
+// with tile = page * hkv + KV head, boxes of 64 dims x 16 rows (128-byte rows,
+// 128-byte swizzle).
+namespace {
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encoder() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+}  // namespace
+
+int encode_page_maps(const void* k_pages, const void* v_pages, int head_dim, int num_pages, int hkv, CUtensorMap* kmap,
+              CUtensorMap* vmap) {
+  const long long tiles = static_cast<long long>(num_pages) * hkv;
+  if (tiles > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;  // tile coordinates are 32-bit
+  EncodeTiledFn enc = encoder();
+  if (enc == nullptr) return PKV_ERR_CUDA;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(kPageSize),
+                              static_cast<cuuint64_t>(tiles)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * 2,
+                                 static_cast<cuuint64_t>(head_dim) * 2 * kPageSize};
+  const cuuint32_t box[3] = {64, kPageSize, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const void* pools[2] = {k_pages, v_pages};
+  CUtensorMap* maps[2] = {kmap, vmap};
+  for (int i = 0; i < 2; ++i)
+    if (enc(maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pools[i]), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return PKV_ERR_CUDA;
+  return PKV_OK;
+}
 
 bool decode_generic_supported(int num_q_heads, int num_kv_heads, int head_dim, int page_size) {
   if (num_kv_heads < 1 || num_kv_heads > 65535 || page_size != kPageSize) return false;
