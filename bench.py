@@ -475,29 +475,54 @@ def measure_prefill(device, bf16_peak, reps=10):
     return res
 
 
+def stage_inputs(step, align=256):
+    """One device buffer and one pinned host buffer holding all of a step's inputs: slots, lengths and
+    block table, then q, k_new and v_new of each layer, each 256-byte aligned. The step's tensors become
+    views of the device buffer, so a step's inputs arrive in one host-to-device copy."""
+    torch = step.torch
+    shared = [("slot_mapping", step.slot_mapping), ("seq_lens", step.seq_lens), ("block_table", step.block_table)]
+    per_layer = [("q", step.q), ("k_new", step.k_new), ("v_new", step.v_new)]
+    parts, off = [], 0
+    for name, t in shared:
+        parts.append((name, None, off, t))
+        off += (t.numel() * t.element_size() + align - 1) // align * align
+    for l in range(step.layers):
+        for name, t in per_layer:
+            parts.append((name, l, off, t[l]))
+            off += (t[l].numel() * t[l].element_size() + align - 1) // align * align
+    dev = torch.empty(off, dtype=torch.uint8, device=step.out.device)
+    host = torch.empty(off, dtype=torch.uint8, pin_memory=True)
+    layered = {name: [None] * step.layers for name, _ in per_layer}
+    for name, l, o, t in parts:
+        nb = t.numel() * t.element_size()
+        view = dev[o:o + nb].view(t.dtype).view(t.shape)
+        view.copy_(t)
+        host[o:o + nb].copy_(t.detach().cpu().contiguous().view(-1).view(torch.uint8))
+        if l is None:
+            setattr(step, name, view)
+        else:
+            layered[name][l] = view
+    for name, views in layered.items():
+        setattr(step, name, views)
+    return dev, host
+
+
 def time_e2e(step, steps, warmup, dist_on):
     """Steps/s through the Python API with host buffers: H2D of q, k_new, v_new, slots, lengths and
-    block table from pinned memory, the step, D2H of the attention output (all in one CUDA graph),
-    then a synchronize, every step."""
+    block table from pinned memory (one staging buffer), the step, D2H of the attention output (all in
+    one CUDA graph), then a synchronize, every step."""
     torch = step.torch
-    pin = lambda t: t.detach().to("cpu").pin_memory()
-    hq, hk, hv = pin(step.q), pin(step.k_new), pin(step.v_new)
-    hs, hl, hb = pin(step.slot_mapping), pin(step.seq_lens), pin(step.block_table)
+    dev, host = stage_inputs(step)
     hout = torch.empty(step.out.shape, dtype=step.out.dtype, pin_memory=True)
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hs, hl, hb))
+    h2d = host.numel()
     d2h = hout.numel() * hout.element_size()
 
     def body():
-        step.q.copy_(hq, non_blocking=True)
-        step.k_new.copy_(hk, non_blocking=True)
-        step.v_new.copy_(hv, non_blocking=True)
-        step.slot_mapping.copy_(hs, non_blocking=True)
-        step.seq_lens.copy_(hl, non_blocking=True)
-        step.block_table.copy_(hb, non_blocking=True)
+        dev.copy_(host, non_blocking=True)
         step.step_eager()
         hout.copy_(step.out, non_blocking=True)
 
-    # one CUDA graph per step: the host->device copies of the step's inputs from pinned memory,
+    # one CUDA graph per step: the host->device copy of the step's inputs from pinned memory,
     # the layers, and the device->host copy of the output; a replay and a synchronize per step
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
