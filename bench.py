@@ -372,17 +372,18 @@ def time_launches(torch, fn, reps):
 
 
 class GenericDecodeStep:
-    """Decode attention alone (no append) over `layers` distinct pools of another cache geometry:
-    the generic decode path (any of 1/2/4/8 query heads per KV head, head_dim 64 or 128)."""
+    """Decode attention over `layers` distinct pools of another cache geometry: the generic decode
+    path (1 to 8 query heads per KV head, head_dim 64 or 128). fused: each layer is one fused
+    append + decode launch with early prefetch (the decode step); otherwise decode attention alone."""
 
-    def __init__(self, device, seq_lens, geom, layers: int, seed: int):
+    def __init__(self, device, seq_lens, geom, layers: int, seed: int, fused: bool = False):
         import torch
 
         import paged_kv_decode_gb300 as pkv
         from paged_kv_decode_gb300 import workloads as W
 
-        self.torch, self.pkv, self.layers, self.geom = torch, pkv, layers, geom
-        case = W.decode_case(seed, seq_lens, geom=geom, layers=layers, device=device, pending_append=False,
+        self.torch, self.pkv, self.layers, self.geom, self.fused = torch, pkv, layers, geom, fused
+        case = W.decode_case(seed, seq_lens, geom=geom, layers=layers, device=device, pending_append=fused,
                              poison=True)
         self.case = case
         i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)
@@ -395,13 +396,19 @@ class GenericDecodeStep:
     def decode_bytes(self) -> int:
         c, g = self.case, self.geom
         kv = int(c.seq_lens.astype(np.int64).sum()) * g.n_kv_heads * g.head_dim * 2 * 2
-        return kv + 2 * c.batch * g.n_q_heads * g.head_dim * 2 + self.block_table.numel() * 4 + c.batch * 4
+        new_rows = 2 * 2 * c.batch * g.n_kv_heads * g.head_dim * 2 if self.fused else 0  # read and written
+        return kv + 2 * c.batch * g.n_q_heads * g.head_dim * 2 + self.block_table.numel() * 4 + c.batch * 4 + new_rows
 
     def step_eager(self):
         c = self.case
         for l in range(self.layers):
-            self.pkv.decode_attn(c.q[l], c.k_pages[l], c.v_pages[l], self.block_table, self.seq_lens, self.out[l],
-                                 self.geom.scale, self.ws)
+            if self.fused:  # each layer's predecessor writes only another layer's pool: early prefetch holds
+                self.pkv.decode_append_attn(c.q[l], c.k_new[l], c.v_new[l], c.k_pages[l], c.v_pages[l],
+                                            self.block_table, self.seq_lens, self.out[l], self.geom.scale, self.ws,
+                                            early_prefetch=True)
+            else:
+                self.pkv.decode_attn(c.q[l], c.k_pages[l], c.v_pages[l], self.block_table, self.seq_lens,
+                                     self.out[l], self.geom.scale, self.ws)
 
     capture = DecodeStep.capture
 
@@ -420,17 +427,19 @@ def measure_shapes(device, hbm, layers=8, steps=30, warmup=5):
                           ("64q_8kv_d128", W.Geometry(64, 8, 128), bs16),
                           ("16q_8kv_d64", W.Geometry(16, 8, 64), bs16),
                           ("32q_8kv_d128_40k", W.Geometry(32, 8, 128), [40000])):
-        st = GenericDecodeStep(device, lens, g, layers, seed=31)
-        st.capture()
-        ms = time_graph(st, steps, warmup, False) / steps
-        us = ms * 1e3 / layers
-        gbps = st.decode_bytes() / (us * 1e-6) / 1e9
-        res[name] = {"us_per_layer": us, "gbps": gbps, "frac_of_measured_hbm": gbps / hbm,
-                     "bytes_per_layer": st.decode_bytes(), "layers_in_graph": layers}
-        del st
         import torch
 
-        torch.cuda.empty_cache()
+        res[name] = {"layers_in_graph": layers}
+        for key, fused in (("", False), ("fused_early_", True)):
+            st = GenericDecodeStep(device, lens, g, layers, seed=31, fused=fused)
+            st.capture()
+            ms = time_graph(st, steps, warmup, False) / steps
+            us = ms * 1e3 / layers
+            gbps = st.decode_bytes() / (us * 1e-6) / 1e9
+            res[name].update({f"{key}us_per_layer": us, f"{key}gbps": gbps, f"{key}frac_of_measured_hbm": gbps / hbm,
+                              f"{key}bytes_per_layer": st.decode_bytes()})
+            del st
+            torch.cuda.empty_cache()
     return res
 
 
@@ -439,13 +448,15 @@ def run_geometry(args, device):
     from paged_kv_decode_gb300 import workloads as W
 
     q, kv, d = (int(x) for x in args.geometry.split(","))
-    st = GenericDecodeStep(device, W.config_seq_lens(2), W.Geometry(q, kv, d), args.layers, seed=31)
+    st = GenericDecodeStep(device, W.config_seq_lens(2), W.Geometry(q, kv, d), args.layers, seed=31,
+                           fused=args.geometry_fused)
     st.capture()
     ms = time_graph(st, args.steps, args.warmup, False) / args.steps
     us = ms * 1e3 / args.layers
     hbm = _peaks()[0]
     gbps = st.decode_bytes() / (us * 1e-6) / 1e9
-    print(json.dumps({"workload": f"generic decode attention, {q}q/{kv}kv/d{d}, bs16 U{{300..3000}}, "
+    what = "fused append + decode (early prefetch)" if args.geometry_fused else "decode attention"
+    print(json.dumps({"workload": f"generic {what}, {q}q/{kv}kv/d{d}, bs16 U{{300..3000}}, "
                                   f"{args.layers} layers per graph", "us_per_layer": us, "gbps": gbps,
                       "frac_of_measured_hbm": gbps / hbm, "bytes_per_layer": st.decode_bytes(),
                       "steps": args.steps, "warmup": args.warmup}), flush=True)
@@ -641,6 +652,8 @@ def main():
     ap.add_argument("--no-extra", action="store_true", help="skip the 40k-context and prefill measurements")
     ap.add_argument("--geometry", default=None, metavar="Q,KV,D",
                     help="time only the generic decode path on that cache geometry (bs16 U{300..3000}) and exit")
+    ap.add_argument("--geometry-fused", action="store_true",
+                    help="with --geometry: time the fused append + decode call with early prefetch")
     ap.add_argument("--unfused", action="store_true",
                     help="time the step as separate pkv_append + pkv_decode_attn launches")
     args = ap.parse_args()
@@ -774,8 +787,9 @@ def main():
             W.config_seq_lens(5), 5 + rank,
             "CFG-paired decode: 28 layers x bs32 (16 conditional U{1000..8000} + 16 companions U{8..64} + g)")
         extra["other_geometries_bs16"] = {
-            "workload": "decode attention alone (generic path), bs16 U{300..3000} (the _40k case: one 40000-token "
-                        "request), 8 layers per graph",
+            "workload": "generic path, bs16 U{300..3000} (the _40k case: one 40000-token request), 8 layers per "
+                        "graph: decode attention alone, and (fused_early_*) one fused append + decode launch per "
+                        "layer with early prefetch",
             **measure_shapes(device, hbm)}
         extra["chunked_prefill"] = {
             "workload": "4096-token chunk (1 request) after 0/8192/32768 cached tokens; mixed step adds the chunk "

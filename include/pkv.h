@@ -33,9 +33,10 @@
  * Supported geometry:
  *  - Every call: num_q_heads = 16, num_kv_heads = 8, head_dim = 128,
  *    page_size = 16 (the Qwen3 decoder; the tuned kernels).
- *  - pkv_append and pkv_decode_attn also take page_size = 16, head_dim 64 or
- *    128, any num_kv_heads and num_q_heads = G * num_kv_heads with G from 1
- *    to 8 (other decoder backbones; a generic split-KV kernel).
+ *  - pkv_append, pkv_decode_attn and pkv_decode_append_attn also take
+ *    page_size = 16, head_dim 64 or 128, any num_kv_heads and
+ *    num_q_heads = G * num_kv_heads with G from 1 to 8 (other decoder
+ *    backbones; a generic split-KV kernel, early prefetch included).
  *  - Anything else returns PKV_ERR_UNSUPPORTED.
  *
  * Conventions for every entry point:

@@ -85,6 +85,8 @@ struct Lay {
 
 struct GenArgs {
   const __nv_bfloat16* q;
+  const __nv_bfloat16* k_new;  // fused append: [batch][hkv][D], the new token's rows (kernel kFused only)
+  const __nv_bfloat16* v_new;
   const __nv_bfloat16* k_pages;
   const __nv_bfloat16* v_pages;
   const int* block_table;
@@ -100,6 +102,8 @@ struct GenArgs {
   int* status;
   int* counters;   // [batch][hkv], zero between calls
   float* records;  // [batch][hkv][splits][G][D + 4]
+  int early;       // copy pages before the grid dependency (the caller's promise: the predecessor writes
+                   // neither the pools nor the block table nor the lengths)
 };
 
 // Log-sum-exp merge of the nrec records of one (request, KV head) into its bf16
@@ -216,7 +220,7 @@ __device__ __forceinline__ void finish_split(const GenArgs& a, const unsigned ch
   if (tid == 0) *counter = 0;
 }
 
-template <int G, int D>
+template <int G, int D, bool kFused>
 __global__ void __launch_bounds__(kGenThreads) decode_generic_kernel(const __grid_constant__ CUtensorMap kmap,
                                                                  const __grid_constant__ CUtensorMap vmap,
                                                                  const GenArgs a) {
@@ -236,8 +240,22 @@ __global__ void __launch_bounds__(kGenThreads) decode_generic_kernel(const __gri
     prefetch_tensormap(&vmap);
   }
 
-  grid_dependency_wait();
-  allow_dependents();
+  // Every argument buffer may come from the previous kernel in the stream, so the kernel waits
+  // for it first -- except in early mode, where lengths, block table and pages are read and the
+  // first copies issued while the predecessor finishes; each warp then waits before it reads
+  // q / k_new / v_new or writes anything. Dependents are released only after a wait.
+  bool waited = !a.early;
+  auto wait_once = [&]() {
+    if (!waited) {
+      grid_dependency_wait();
+      allow_dependents();
+      waited = true;
+    }
+  };
+  if (!a.early) {
+    grid_dependency_wait();
+    allow_dependents();
+  }
 
   int sl = __ldg(a.seq_lens + b);
   const int cap = a.max_pages * kPageSize;
@@ -247,6 +265,7 @@ __global__ void __launch_bounds__(kGenThreads) decode_generic_kernel(const __gri
   }
   __nv_bfloat16* orow = a.out + (static_cast<size_t>(b) * nq + hq0) * D;
   if (sl == 0) {
+    wait_once();
     if (s == 0)
       for (int i = tid; i < a.gq * D; i += kGenThreads) orow[i] = __float2bfloat16_rn(0.f);
     return;
@@ -263,7 +282,7 @@ __global__ void __launch_bounds__(kGenThreads) decode_generic_kernel(const __gri
     int id = __ldg(a.block_table + static_cast<size_t>(b) * a.max_pages + p);
     if (id < 0 || id >= a.num_pages) {
       set_status(a.status, PKV_ERR_OUT_OF_BOUNDS);
-      id = 0;
+      id = -1;  // reported; the page is read as page 0 and nothing is appended to it
     }
     ids[p - p0] = id;
   }
@@ -273,19 +292,39 @@ __global__ void __launch_bounds__(kGenThreads) decode_generic_kernel(const __gri
   const int nw = p1 - p0 > warp ? (p1 - p0 - warp + kGenWarps - 1) / kGenWarps : 0;
   unsigned char* ring = smem + warp * S::kRing;
   uint64_t* wfull = full + warp * S::kStages;
-  auto issue = [&](int i) {  // lane 0: page i of this warp into stage i % kStages
-    const int z = ids[warp + i * kGenWarps] * a.hkv + h;  // tile index in the pool
-    unsigned char* dst = ring + (i % S::kStages) * S::kStage;
-    uint64_t* bar = &wfull[i % S::kStages];
-    mbar_arrive_expect_tx(bar, S::kStage);
+  auto issue = [&](int i) {  // whole warp: page i of this warp into stage i % kStages
+    const int page = p0 + warp + i * kGenWarps;
+    const int id = ids[page - p0];
+    if (kFused && page == np - 1 && id >= 0) {
+      // fused append: this page holds the request's new token; its K and V rows for head h are
+      // written first (one 16-byte chunk per lane), then fenced before the warp's tensor copy
+      wait_once();  // the new rows come from the predecessor
+      constexpr int kRowChunks = D / 8;
+      const size_t row = ((static_cast<size_t>(id) * a.hkv + h) * kPageSize + (sl - 1) % kPageSize) * D;
+      const size_t src = (static_cast<size_t>(b) * a.hkv + h) * D;
+      if (lane < 2 * kRowChunks) {
+        const bool is_v = lane >= kRowChunks;
+        const int ch = is_v ? lane - kRowChunks : lane;
+        const uint4 x = __ldg(reinterpret_cast<const uint4*>((is_v ? a.v_new : a.k_new) + src) + ch);
+        reinterpret_cast<uint4*>(const_cast<__nv_bfloat16*>(is_v ? a.v_pages : a.k_pages) + row)[ch] = x;
+        fence_proxy_async_global();
+      }
+      __syncwarp();
+    }
+    if (lane == 0) {
+      const int z = (id < 0 ? 0 : id) * a.hkv + h;  // tile index in the pool
+      unsigned char* dst = ring + (i % S::kStages) * S::kStage;
+      uint64_t* bar = &wfull[i % S::kStages];
+      mbar_arrive_expect_tx(bar, S::kStage);
 #pragma unroll
-    for (int j = 0; j < D / 64; ++j) {
-      tma_load_3d(dst + j * 2048, &kmap, 64 * j, 0, z, bar);
-      tma_load_3d(dst + S::kTile + j * 2048, &vmap, 64 * j, 0, z, bar);
+      for (int j = 0; j < D / 64; ++j) {
+        tma_load_3d(dst + j * 2048, &kmap, 64 * j, 0, z, bar);
+        tma_load_3d(dst + S::kTile + j * 2048, &vmap, 64 * j, 0, z, bar);
+      }
     }
   };
-  if (lane == 0)
-    for (int i = 0; i < S::kStages && i < nw; ++i) issue(i);
+  for (int i = 0; i < S::kStages && i < nw; ++i) issue(i);
+  wait_once();  // q comes from the predecessor
 
   const int r = lane >> 2, c = lane & 3;  // fragment row and column pair
   // Q^T as the B operand: head r, dims 16 ks + 2c (+1) and 16 ks + 8 + 2c (+1)
@@ -327,7 +366,7 @@ __global__ void __launch_bounds__(kGenThreads) decode_generic_kernel(const __gri
 
     mma_page<S::kKS>(kt, vt, koff, voff, qf, nv, a.qscale, o, m0, m1, l0, l1);
     __syncwarp();  // the stage is free again
-    if (lane == 0 && it + S::kStages < nw) issue(it + S::kStages);
+    if (it + S::kStages < nw) issue(it + S::kStages);
   }
 
   // ---- this warp's state into its drained ring: [G][D + 4] as o, m, l
@@ -388,25 +427,31 @@ size_t gen_workspace(int batch, int hkv, int max_pages, int num_sms) {
 }
 
 template <int G, int D>
-int gen_launch(const void* q, const void* k_pages, const void* v_pages, const int32_t* block_table,
-               const int32_t* seq_lens, void* out, float scale, int batch, int hkv, int gq, int max_pages,
-               int num_pages, void* workspace, int num_sms, cudaStream_t stream) {
+int gen_launch(const void* q, const void* k_new, const void* v_new, const void* k_pages, const void* v_pages,
+               const int32_t* block_table, const int32_t* seq_lens, void* out, float scale, int batch, int hkv,
+               int gq, int max_pages, int num_pages, void* workspace, int num_sms, cudaStream_t stream,
+               uint32_t flags) {
   int splits = 1, pps = 1;
   plan<G, D>(batch, hkv, max_pages, num_sms, splits, pps);
   const size_t smem = Lay<G, D>::smem_bytes(pps);
   if (smem > 227 * 1024) return PKV_ERR_UNSUPPORTED;
-  static bool attr_set[64] = {};
+  const bool fused = k_new != nullptr;
+  using Kern = void (*)(const CUtensorMap, const CUtensorMap, const GenArgs);
+  const Kern kern = fused ? decode_generic_kernel<G, D, true> : decode_generic_kernel<G, D, false>;
+  static bool attr_set[64][2] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
-  if (dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(decode_generic_kernel<G, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             227 * 1024) != cudaSuccess)
+  if (dev < 64 && !attr_set[dev][fused ? 1 : 0]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess)
       return PKV_ERR_CUDA;
-    attr_set[dev] = true;
+    attr_set[dev][fused ? 1 : 0] = true;
   }
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   GenArgs a;
   a.q = static_cast<const __nv_bfloat16*>(q);
+  a.k_new = static_cast<const __nv_bfloat16*>(k_new);
+  a.v_new = static_cast<const __nv_bfloat16*>(v_new);
+  a.early = (flags & PKV_DECODE_EARLY_PREFETCH) ? 1 : 0;
   a.k_pages = static_cast<const __nv_bfloat16*>(k_pages);
   a.v_pages = static_cast<const __nv_bfloat16*>(v_pages);
   a.block_table = block_table;
@@ -426,8 +471,7 @@ int gen_launch(const void* q, const void* k_pages, const void* v_pages, const in
   CUtensorMap kmap, vmap;
   const int rc = encode_page_maps(k_pages, v_pages, D, num_pages, hkv, &kmap, &vmap);
   if (rc != PKV_OK) return rc;
-  return launch_pdl(decode_generic_kernel<G, D>, grid, dim3(kGenThreads), smem, stream, kmap, vmap, a) ==
-                 cudaSuccess
+  return launch_pdl(kern, grid, dim3(kGenThreads), smem, stream, kmap, vmap, a) == cudaSuccess
              ? PKV_OK
              : PKV_ERR_CUDA;
 }
@@ -510,16 +554,17 @@ size_t decode_generic_workspace_bytes(int num_q_heads, int num_kv_heads, int hea
   return 0;
 }
 
-int launch_decode_generic(const void* q, const void* k_pages, const void* v_pages, const int32_t* block_table,
-                          const int32_t* seq_lens, void* out, float scale, int num_q_heads, int num_kv_heads,
-                          int head_dim, int32_t batch, int32_t max_pages, int32_t num_pages, void* workspace,
-                          int num_sms, cudaStream_t stream) {
+int launch_decode_generic(const void* q, const void* k_new, const void* v_new, const void* k_pages,
+                          const void* v_pages, const int32_t* block_table, const int32_t* seq_lens, void* out,
+                          float scale, int num_q_heads, int num_kv_heads, int head_dim, int32_t batch,
+                          int32_t max_pages, int32_t num_pages, void* workspace, int num_sms, cudaStream_t stream,
+                          uint32_t flags) {
   if (batch == 0) return PKV_OK;
   const int gq = num_q_heads / num_kv_heads;
   const int group = padded_group(gq);
-#define PKV_GEN_RUN(G, D)                                                                                   \
-  gen_launch<G, D>(q, k_pages, v_pages, block_table, seq_lens, out, scale, batch, num_kv_heads, gq, max_pages, \
-                   num_pages, workspace, num_sms, stream)
+#define PKV_GEN_RUN(G, D)                                                                                    \
+  gen_launch<G, D>(q, k_new, v_new, k_pages, v_pages, block_table, seq_lens, out, scale, batch, num_kv_heads, \
+                   gq, max_pages, num_pages, workspace, num_sms, stream, flags)
   PKV_GEN_DISPATCH(PKV_GEN_RUN)
 #undef PKV_GEN_RUN
   return PKV_ERR_UNSUPPORTED;

@@ -28,10 +28,13 @@ int decode_max_batch();
 bool decode_generic_supported(int num_q_heads, int num_kv_heads, int head_dim, int page_size);
 size_t decode_generic_workspace_bytes(int num_q_heads, int num_kv_heads, int head_dim, int32_t batch,
                                       int32_t max_pages, int num_sms);
-int launch_decode_generic(const void* q, const void* k_pages, const void* v_pages, const int32_t* block_table,
-                          const int32_t* seq_lens, void* out, float scale, int num_q_heads, int num_kv_heads,
-                          int head_dim, int32_t batch, int32_t max_pages, int32_t num_pages, void* workspace,
-                          int num_sms, cudaStream_t stream);
+// k_new / v_new: the fused append's new rows (both nullptr: decode alone); flags: 0 or
+// PKV_DECODE_EARLY_PREFETCH.
+int launch_decode_generic(const void* q, const void* k_new, const void* v_new, const void* k_pages,
+                          const void* v_pages, const int32_t* block_table, const int32_t* seq_lens, void* out,
+                          float scale, int num_q_heads, int num_kv_heads, int head_dim, int32_t batch,
+                          int32_t max_pages, int32_t num_pages, void* workspace, int num_sms, cudaStream_t stream,
+                          uint32_t flags);
 
 size_t prefill_workspace_bytes(int32_t num_seqs, int32_t max_q_len, int num_sms);
 int prefill_max_seqs();

@@ -40,8 +40,8 @@ def test_host_argument_checks(lib):
     d = _desc()
     # NULL descriptor
     assert lib.pkv_append(None, None, None, 1, None, None, None, None, None, 0) == -1
-    # unsupported geometry: decode and append take page size 16, head_dim 64 or 128 and
-    # 1 to 8 query heads per KV head; prefill and the fused calls only 16/8/128/16
+    # unsupported geometry: decode, append and the fused append + decode take page size 16, head_dim
+    # 64 or 128 and 1 to 8 query heads per KV head; prefill and the RoPE call only 16/8/128/16
     for bad in (_desc(head_dim=96), _desc(num_q_heads=36, num_kv_heads=4), _desc(num_q_heads=20),
                 _desc(page_size=32), _desc(num_q_heads=32, num_kv_heads=2)):
         assert lib.pkv_append(None, None, None, 1, None, None, ctypes.byref(bad), None, None, 0) == -3
@@ -54,7 +54,10 @@ def test_host_argument_checks(lib):
                                    0) == -1
         assert lib.pkv_append(None, None, None, 1, None, None, ctypes.byref(other), None, None, 0) == -1
         assert lib.pkv_decode_append_attn(None, None, None, None, None, None, None, None, 1.0, None,
-                                          ctypes.byref(other), 1, 1, None, 0, 0) == -3
+                                          ctypes.byref(other), 1, 1, None, 0, 0) == -1
+        # (a table address the host never reads: the geometry check comes first)
+        assert lib.pkv_decode_append_rope_attn(None, None, None, None, None, None, None, 256, 1, None, 1.0, None,
+                                               ctypes.byref(other), 1, 1, None, 0, 0) == -3
         assert lib.pkv_prefill_chunk_attn(None, None, None, None, None, None, 1, 1, None, 1.0, None,
                                           ctypes.byref(other), 1, 1, None, 0) == -3
     # sizes

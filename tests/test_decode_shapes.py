@@ -1,5 +1,6 @@
-"""Decode attention and KV append for cache geometries other than the Qwen3
-decoder's 16/8/128 (the generic decode path), against the fp64 oracle.
+"""Decode attention, KV append and the fused append + decode call for cache
+geometries other than the Qwen3 decoder's 16/8/128 (the generic decode path),
+against the fp64 oracle.
 
 The pages name further decoder backbones for the same slot (a Llama-style 2B
 model, Qwen3-8B, OLMo-2-7B, SmolLM2-1.7B) but give no head counts, so the
@@ -127,10 +128,82 @@ def test_page_id_outside_pool_is_reported(cuda_device):
     assert run.ws.status() == -7  # PKV_ERR_OUT_OF_BOUNDS
 
 
-def test_fused_and_prefill_calls_reject_other_geometries(cuda_device):
+def _fused(case, layer, dev, early=False):
+    run = DecodeOnDevice(case, layer, dev)
+    pkv.decode_append_attn(run.q, run.k_new, run.v_new, run.k_pages, run.v_pages, run.block_table, run.seq_lens,
+                           run.out, case.geom.scale, run.ws, early_prefetch=early)
+    torch.cuda.synchronize()
+    return run
+
+
+FUSED_LENS = [700, 0, 33, 1, 16, 17, 2900, 5000]  # padding row, page boundaries, one-token and long rows
+
+
+@pytest.mark.parametrize("shape", sorted(SHAPES))
+def test_fused_append_decode_matches_oracle(cuda_device, shape):
+    # one launch appends each request's new K/V rows and attends over the cache with them
+    case = W.decode_case(28, FUSED_LENS, geom=SHAPES[shape], pending_append=True, poison=True)
+    run = _fused(case, 0, cuda_device)
+    want_k, want_v = oracle.append(case.k_new[0], case.v_new[0], case.slot_mapping, case.k_pages[0], case.v_pages[0])
+    assert np.array_equal(bits(run.k_pages.cpu()), want_k) and np.array_equal(bits(run.v_pages.cpu()), want_v)
+    want = oracle.decode(case.q[0], want_k, want_v, case.block_table, case.seq_lens, case.geom.scale)
+    assert_close(bf16_to_f64(run.out), want, f"{shape} fused")
+    for b, n in enumerate(case.seq_lens):
+        if n == 0:
+            assert torch.count_nonzero(run.out[b].view(torch.int16)).item() == 0
+    assert run.ws.status() == 0
+
+
+@pytest.mark.parametrize("shape", ["g4_d128_32q8kv", "g8_d64_8q1kv", "g1_d64_32q32kv", "g6_d64_12q2kv"])
+def test_fused_equals_separate_calls_bitwise(cuda_device, shape):
+    case = W.decode_case(29, FUSED_LENS, geom=SHAPES[shape], pending_append=True, poison=True)
+    sep = DecodeOnDevice(case, 0, cuda_device)
+    out_sep = sep.step().clone()
+    fused = _fused(case, 0, cuda_device)
+    assert torch.equal(out_sep.view(torch.int16), fused.out.view(torch.int16))
+    assert torch.equal(sep.k_pages.view(torch.int16), fused.k_pages.view(torch.int16))
+    assert torch.equal(sep.v_pages.view(torch.int16), fused.v_pages.view(torch.int16))
+
+
+@pytest.mark.parametrize("shape", ["g4_d128_32q8kv", "g2_d64_16q8kv"])
+@pytest.mark.parametrize("early", [False, True])
+def test_fused_layer_chain_in_a_graph(cuda_device, shape, early):
+    # two layers, each its own pool, replayed from a CUDA graph; with early prefetch each layer's
+    # kernel may read its pool while the previous layer's kernel finishes
+    case = W.decode_case(30, W.config_seq_lens(2), geom=SHAPES[shape], layers=2, pending_append=True, poison=True)
+    runs = [DecodeOnDevice(case, layer, cuda_device) for layer in range(2)]
+
+    def step():
+        for r in runs:
+            pkv.decode_append_attn(r.q, r.k_new, r.v_new, r.k_pages, r.v_pages, r.block_table, r.seq_lens, r.out,
+                                   case.geom.scale, r.ws, early_prefetch=early)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for layer, r in enumerate(runs):  # the graph's replay appends again at the same slots: same bits
+        r.out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    for layer, r in enumerate(runs):
+        want_k, want_v = oracle.append(case.k_new[layer], case.v_new[layer], case.slot_mapping,
+                                       case.k_pages[layer], case.v_pages[layer])
+        assert np.array_equal(bits(r.k_pages.cpu()), want_k) and np.array_equal(bits(r.v_pages.cpu()), want_v)
+        want = oracle.decode(case.q[layer], want_k, want_v, case.block_table, case.seq_lens, case.geom.scale)
+        assert_close(bf16_to_f64(r.out), want, f"{shape} graph layer {layer} early={early}")
+        assert r.ws.status() == 0
+
+
+def test_rope_call_rejects_other_geometries(cuda_device):
     geom = SHAPES["g4_d128_32q8kv"]
     case = W.decode_case(27, [100], geom=geom, pending_append=True, poison=False)
     run = DecodeOnDevice(case, 0, cuda_device)
+    cos_sin = pkv.rope_cos_sin(1e6, 128, device=cuda_device)
     with pytest.raises(pkv.PkvError, match="UNSUPPORTED"):
-        pkv.decode_append_attn(run.q, run.k_new, run.v_new, run.k_pages, run.v_pages, run.block_table, run.seq_lens,
-                               run.out, geom.scale, run.ws)
+        pkv.decode_append_rope_attn(run.q, run.k_new, run.v_new, run.k_pages, run.v_pages, run.block_table,
+                                    run.seq_lens, cos_sin, run.out, geom.scale, run.ws)
