@@ -6,8 +6,10 @@ library's CUDA kernels. torch tensors supply device memory and the current
 CUDA stream. There is no CPU fallback: without the compiled library every call
 raises.
 
-Layout (see include/pkv.h): pools bf16 [num_pages, 8, 16, 128]; q / out bf16
-[rows, 16, 128]; block tables int32 [rows, max_pages]; lengths int32.
+Layout (see include/pkv.h): pools bf16 [num_pages, Hkv, 16, D]; q / out bf16
+[rows, Hq, D]; block tables int32 [rows, max_pages]; lengths int32. The Qwen3
+decoder's 16/8/128 runs the tuned kernels; append, decode and the fused append
++ decode call also take head_dim 64 or 128 with 1 to 8 query heads per KV head.
 """
 from __future__ import annotations
 
@@ -213,8 +215,9 @@ def decode_append_rope_attn(q, k_new, v_new, k_pages, v_pages, block_table, seq_
 
 def decode_append_attn(q, k_new, v_new, k_pages, v_pages, block_table, seq_lens, out, scale: float,
                        workspace: Workspace, stream=None, early_prefetch: bool = False):
-    """One decode step of one layer in one launch: write k_new / v_new [B, 8, 128] at position
-    seq_lens[b] - 1 of each request, then decode attention over seq_lens[b] positions.
+    """One decode step of one layer in one launch: write k_new / v_new [B, Hkv, D] at position
+    seq_lens[b] - 1 of each request, then decode attention over seq_lens[b] positions (any geometry
+    decode_attn takes).
 
     early_prefetch: the previous kernel on the stream writes neither the pools nor the block
     table nor the lengths, so they may be read while it finishes (PKV_DECODE_EARLY_PREFETCH)."""
