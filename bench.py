@@ -49,7 +49,7 @@ WORKLOAD = ("qwen3-0.6b decode step: 28 layers x bs16, 16q/8kv heads, d128, page
 # DRAM traffic of one decode launch on this workload's per-layer pool, from one ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the decode kernel source it was
 # measured on (sha256 prefix of csrc/decode.cu); any other source reports null.
-NCU_DECODE_TRAFFIC = {"973e842187866053": 107_392_256 + 3_072_512}
+NCU_DECODE_TRAFFIC = {"856c1d16ad501ffb": 107_398_400 + 2_418_688}
 
 
 def _decode_traffic():

@@ -31,7 +31,7 @@
 //    may hold anything, NaN included.
 //  * Optional fused append: the producer lane that copies a request's last
 //    page first writes the request's new K/V row for that head into it
-//    (generic stores, then a proxy fence so its own bulk copy sees them). With
+//    (generic stores, then a proxy fence so its own tensor copy sees them). With
 //    a cos/sin table the whole producer warp writes the row instead, rotating
 //    the key (rotary position embedding at the new token's position, pairs
 //    (i, i + 64), fp32, rounded to bf16), and each piece's query rows are
@@ -265,7 +265,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
   // the kernel waits for it before touching them -- except in early mode, where
   // the caller guarantees that the predecessor writes neither the pools nor the
   // block table nor the lengths: then the length scan, the share decoding and
-  // the first bulk copies overlap the predecessor's tail, and each warp waits
+  // the first page copies overlap the predecessor's tail, and each warp waits
   // only before it reads q / k_new / v_new or writes anything. Dependents are
   // released only after this grid's own wait, so the kernel two launches back
   // has always completed when a successor starts early.
@@ -337,7 +337,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
   // decodes its (request, KV head, page), loads the block-table entry, and works
   // out which consumer reads the page ((f - lo) mod kCons) and which stage of
   // that consumer's ring it fills (its running page count, from the lanes
-  // before it with the same consumer). The lanes then issue their own bulk
+  // before it with the same consumer). The lanes then issue their own tensor
   // copies in rounds in which every stage is filled at most once, so each
   // stage's empty barrier is at most one phase behind the wait. Because the
   // assignment follows the share and not the piece, round r of a chunk holds
@@ -423,7 +423,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
               reinterpret_cast<uint4*>(const_cast<__nv_bfloat16*>(a.v_pages) + row)[lane] =
                   __ldg(reinterpret_cast<const uint4*>(a.v_new + srow) + lane);
           }
-          fence_proxy_async_global();  // this lane's row stores before the warp's bulk copies
+          fence_proxy_async_global();  // this lane's row stores before the warp's tensor copies
           __syncwarp();
         }
       }
@@ -438,7 +438,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
             const int pid = id_ok ? id : 0;
             if (kFused && !kRope && wslot >= 0 && id_ok) {
               // fused append: this page holds the request's new token; write its K and V rows
-              // for this head, then order the writes before this lane's bulk copy of the page
+              // for this head, then order the writes before this lane's tensor copy of the page
               const uint4* ks = reinterpret_cast<const uint4*>(a.k_new + (static_cast<size_t>(bb) * kKVHeads + hh) * kHeadDim);
               const uint4* vs = reinterpret_cast<const uint4*>(a.v_new + (static_cast<size_t>(bb) * kKVHeads + hh) * kHeadDim);
               const size_t row = ((static_cast<size_t>(pid) * kKVHeads + hh) * kPageSize + wslot) * kHeadDim;

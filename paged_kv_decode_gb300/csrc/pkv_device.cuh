@@ -1,9 +1,9 @@
 // pkv_device.cuh -- device helpers shared by the libpkv kernels (sm_103a).
 //
-// Inline PTX for the pieces the kernels build on: shared-memory mbarriers,
-// 1-D bulk copies (cp.async.bulk) global -> shared with transaction counting,
-// bounded waits that report a timeout instead of hanging, and the
-// first-error-wins status word.
+// Inline PTX for the pieces the kernels build on: shared-memory mbarriers with
+// transaction counting (the tiled TMA copies of pkv_tc.cuh complete on them),
+// 16-byte cp.async copies, bounded waits that report a timeout instead of
+// hanging, and the first-error-wins status word.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -74,13 +74,13 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
 }
 
-// Make barrier initialisation visible to the async proxy (bulk copies).
+// Make barrier initialisation visible to the async proxy (TMA copies).
 __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
 // Order this thread's earlier generic-proxy global writes before its later
-// async-proxy (bulk copy) accesses.
+// async-proxy (TMA copy) accesses.
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
@@ -120,28 +120,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return true;
 }
 
-// ----------------------------------------------------------------------------
-// 1-D bulk copy global -> shared, completing on an mbarrier
-// (both addresses 16-byte aligned, size a multiple of 16)
-// ----------------------------------------------------------------------------
-__device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(smem_dst)),
-      "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
-// Same, with an L2 eviction-priority hint (createpolicy value).
-__device__ __forceinline__ void bulk_g2s_hint(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* bar,
-                                             uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
-      "%4;" ::"r"(smem_u32(smem_dst)),
-      "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
-      : "memory");
-}
-
 // 16-byte asynchronous copy global -> shared (cp.async, generic proxy); the
 // issuing thread waits with cp_async_wait_all (a compiler memory barrier), the
 // other threads after a CTA barrier.
@@ -159,37 +137,14 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
 // ----------------------------------------------------------------------------
 // loads and conversions
 // ----------------------------------------------------------------------------
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-  return v;
-}
-
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
   return v;
 }
-__device__ __forceinline__ uint2 lds64(uint32_t addr) {
-  uint2 v;
-  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
-  return v;
-}
 __device__ __forceinline__ float2 lds64f(uint32_t addr) {
   float2 v;
   asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
-  return v;
-}
-__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
-  asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-__device__ __forceinline__ void sts64(uint32_t addr, uint2 v) {
-  asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(v.x), "r"(v.y) : "memory");
-}
-
-__device__ __forceinline__ float4 lds128f(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
   return v;
 }
 

@@ -1,6 +1,6 @@
 // selftest.cu -- diagnostic for the bounded device-side waits.
 //
-// Every wait of the libpkv kernels on an mbarrier (a bulk copy landing, a
+// Every wait of the libpkv kernels on an mbarrier (a TMA copy landing, a
 // stage being released, an MMA finishing) gives up after a bounded number of
 // SM cycles, records PKV_ERR_DEVICE_TIMEOUT in the workspace status word and
 // lets the kernel wind down, so a lost copy can never hang the GPU. This
