@@ -10,7 +10,9 @@ movmatrix (.trans) and mma.sync m16n8k16 (row.col, bf16 in, fp32 out), with the
 row addresses and fragment registers the kernel computes, and checks that the
 products are exactly S^T = K Q^T and O^T = V^T P^T of the page, that no
 ldmatrix phase has a bank conflict, and that the tail mask keeps NaN in unused
-rows out of the accumulators.
+rows out of the accumulators. Over several pages, the running max, the
+warp-wide rescale vote and the sums of the bf16-rounded weights give the
+softmax mean within the weights' rounding.
 """
 import numpy as np
 import pytest
@@ -148,3 +150,82 @@ def test_ldmatrix_phases_are_conflict_free_and_cover_the_tile(D):
                 assert a % 16 == 0 and 0 <= a and a + 16 <= PAGE * D * 2
                 seen.add(a)
         assert len(seen) == PAGE * D * 2 // 16  # every 16-byte chunk of the tile read once per product
+
+
+def bf16(x):
+    """round float64 values to bf16 (nearest, ties to even) and back"""
+    x = np.asarray(x, np.float64)
+    b = x.astype(np.float32).view(np.uint32).astype(np.uint64)
+    b = (b + 0x7FFF + ((b >> 16) & 1)) & 0xFFFF0000
+    return b.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def run_pages(K, V, q, n_tok):
+    """the kernel's loop over a split's pages with its running state per lane: max (m0, m1 of the lane's two
+    heads), partial sums (l0, l1), O^T fragments, rescaled only when some lane's max moved; p rounded to bf16
+    and the sums taken over the rounded p. Returns O^T / l per head, [D, 8]."""
+    D = K.shape[1]
+    g, c = LANES // 4, LANES % 4
+    m = np.full((32, 2), -np.inf)
+    l = np.zeros((32, 2))
+    o = np.zeros((D // 16, 32, 4))
+    koff, voff = offsets(D)
+    qf = [(np.stack([q[g, 16 * ks + 2 * c], q[g, 16 * ks + 2 * c + 1]], 1),
+           np.stack([q[g, 16 * ks + 8 + 2 * c], q[g, 16 * ks + 9 + 2 * c]], 1)) for ks in range(D // 16)]
+    for p0 in range(0, n_tok, PAGE):
+        nv = min(PAGE, n_tok - p0)
+        kmem, vmem = tma_tile(K[p0:p0 + PAGE], D), tma_tile(V[p0:p0 + PAGE], D)
+        s = np.zeros((32, 4))
+        for ks in range(D // 16):
+            s = mma(s, ldmatrix(kmem, koff[ks]), *qf[ks])
+        valid = np.stack([g < nv, g < nv, g + 8 < nv, g + 8 < nv], 1)
+        s = np.where(valid, s, -np.inf)
+        x = np.maximum(s[:, :2], s[:, 2:])
+        for sh in (4, 8, 16):  # butterfly over the lanes of a column pair
+            x = np.maximum(x, x[LANES ^ sh])
+        n = np.maximum(m, x)
+        p = bf16(np.exp2(s - np.concatenate([n, n], 1)))
+        if (n != m).any():  # the warp-wide vote
+            al = np.exp2(m - n)
+            l *= al
+            o *= np.concatenate([al, al], 1)[None]
+            m = n
+        l += p[:, :2] + p[:, 2:]
+        pb0, pb1 = movmatrix_t(p[:, :2]), movmatrix_t(p[:, 2:])
+        lo = np.stack([2 * c < nv, 2 * c + 1 < nv], 1)
+        hi = np.stack([2 * c + 8 < nv, 2 * c + 9 < nv], 1)
+        for ks in range(D // 16):
+            vf = ldmatrix(vmem, voff[ks], trans=True)
+            vf = np.stack([np.where(lo, vf[0], 0), np.where(lo, vf[1], 0), np.where(hi, vf[2], 0),
+                           np.where(hi, vf[3], 0)])
+            o[ks] = mma(o[ks], vf, pb0, pb1)
+    for sh in (4, 8, 16):
+        l = l + l[LANES ^ sh]
+    ot = np.zeros((D, 8))
+    for ks in range(D // 16):
+        for L in range(32):
+            ot[16 * ks + g[L], 2 * c[L]:2 * c[L] + 2] = o[ks, L, :2] / l[L]
+            ot[16 * ks + g[L] + 8, 2 * c[L]:2 * c[L] + 2] = o[ks, L, 2:] / l[L]
+    return ot
+
+
+@pytest.mark.parametrize("order", ["rising", "falling"])
+def test_split_loop_rescales_to_the_softmax_mean(order):
+    # scores whose page maximum rises page after page (a rescale on every page) or falls (none after the first)
+    rng = np.random.default_rng(7)
+    D, n_tok = 64, 5 * PAGE - 3
+    K = bf16(rng.standard_normal((5 * PAGE, D)))
+    V = bf16(rng.standard_normal((5 * PAGE, D)))
+    q = np.zeros((8, D))
+    q[:4] = bf16(rng.standard_normal((4, D)) * 0.3)
+    ramp = np.repeat(np.arange(5), PAGE)[:, None] * (1.0 if order == "rising" else -1.0)
+    K = bf16(K + ramp * np.sign(q[:4].sum(0))[None] * 0.5)  # shifts every head's scores page by page
+    K[n_tok:] = np.nan
+    V[n_tok:] = np.nan
+    got = run_pages(K, V, q, n_tok)
+    s = q[:4] @ K[:n_tok].T  # [4 heads, tokens], log2 domain as in the kernel (unit scale)
+    w = np.exp2(s - s.max(1, keepdims=True))
+    want = (w @ V[:n_tok] / w.sum(1, keepdims=True)).T  # [D, 4]
+    assert np.isfinite(got).all()
+    # p is rounded to bf16 in the value product and in the sums: relative weight error <= 2^-8
+    assert np.abs(got[:, :4] - want).max() <= 2 ** -8 * np.abs(V[:n_tok]).max()
