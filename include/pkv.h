@@ -33,17 +33,21 @@
  * Supported geometry:
  *  - Every call: num_q_heads = 16, num_kv_heads = 8, head_dim = 128,
  *    page_size = 16 (the Qwen3 decoder; the tuned kernels).
- *  - pkv_append, pkv_decode_attn and pkv_decode_append_attn also take
- *    page_size = 16, head_dim 64 or 128, any num_kv_heads and
- *    num_q_heads = G * num_kv_heads with G from 1 to 8 (other decoder
- *    backbones; a generic split-KV kernel, early prefetch included).
+ *  - pkv_append, pkv_decode_attn, pkv_decode_append_attn and
+ *    pkv_prefill_chunk_attn also take page_size = 16, head_dim 64 or 128,
+ *    any num_kv_heads and num_q_heads = G * num_kv_heads with G from 1 to 8
+ *    (other decoder backbones; decode runs a generic split-KV kernel, early
+ *    prefetch included; prefill runs its tensor-core kernel on pairs of
+ *    query heads).
  *  - Anything else returns PKV_ERR_UNSUPPORTED.
  *
  * Conventions for every entry point:
  *  - Every pointer argument except `desc` is DEVICE memory owned by the
  *    caller; `desc` is a host pointer read during the call only. The library
  *    never allocates, frees or synchronises, and keeps no state between calls
- *    apart from a per-device cache of the SM count.
+ *    apart from a per-device cache of the SM count. The one exception is
+ *    pkv_decode_attn_noalloc, which owns a fixed device array per GPU and has
+ *    no status word the caller can read (see its own block).
  *  - Work is enqueued on `stream` (NULL = the legacy default stream) and is
  *    ordered with the caller's other work on that stream. No call reads
  *    device memory from the host, so the calls can be captured in a CUDA graph.
@@ -57,6 +61,17 @@
  *  - A workspace must be zero-filled once before its first use
  *    (pkv_workspace_init); the kernels leave it ready for the next call. Calls
  *    that may run concurrently (different streams) need separate workspaces.
+ *  - After any call whose status word is not PKV_OK, run pkv_workspace_init on
+ *    the workspace again before its next use. A call that stopped early (a
+ *    bounded wait that ran out, a skipped access) may leave split counters
+ *    above zero or tagged partial records behind, and the next call would
+ *    take them for its own.
+ *  - Split merge of decode batches: the CTA that merges a (request, KV head)
+ *    waits, with a bound, for the partial records of CTAs with lower block
+ *    indices. This relies on the hardware starting a grid's CTAs in
+ *    block-index order, which NVIDIA GPUs do but CUDA does not promise. Were
+ *    it not so, the wait would run out after about one second and report
+ *    PKV_ERR_DEVICE_TIMEOUT; it never hangs.
  *  - A workspace serves one kind of attention call: decode calls
  *    (pkv_decode_attn, pkv_decode_append_attn) or prefill calls
  *    (pkv_prefill_chunk_attn), not both: each kind relies on its own split
@@ -254,10 +269,11 @@ int pkv_decode_append_rope_attn(const void* q, const void* k_new, const void* v_
 
 /*
  * Workspace bytes pkv_prefill_chunk_attn needs: the status header, split
- * counters (num_seqs x 8 KV heads x ceil(max_q_len / 128) x 2 ints) and two
- * partial records per SM of the current device (for each of the 2 query heads
- * of a KV head: 128 rows x 128 dims of fp16 O / l, then fp32 max and sum per
- * row: 67,584 bytes), for query tiles whose key range is cut between CTAs.
+ * counters (num_seqs x head pairs x ceil(max_q_len / 128) x 2 ints, with
+ * num_kv_heads x ceil(G / 2) head pairs) and two partial records per SM of the
+ * current device (for each of the 2 query heads of a pair: 128 rows x
+ * head_dim dims of fp16 O / l, then fp32 max and sum per row: 67,584 bytes at
+ * head_dim 128), for query tiles whose key range is cut between CTAs.
  */
 size_t pkv_prefill_workspace_bytes(const pkv_cache_desc* desc, int32_t num_seqs, int32_t max_q_len);
 
@@ -282,8 +298,11 @@ size_t pkv_prefill_workspace_bytes(const pkv_cache_desc* desc, int32_t num_seqs,
  *  cu_q_lens:    int32 [num_seqs + 1], cu_q_lens[0] = 0, non-decreasing,
  *                cu_q_lens[num_seqs] <= total_q
  *  total_q:      rows of q and out (host value; bounds every access)
- *  max_q_len:    host-side upper bound on any chunk length (sizes the grid;
- *                rows of longer chunks are not computed)
+ *  max_q_len:    host-side upper bound on any chunk length (sizes the grid
+ *                and the workspace). A chunk longer than
+ *                128 * ceil(max_q_len / 128) rows sets PKV_ERR_OUT_OF_BOUNDS
+ *                in the status word; its rows past that bound are not
+ *                computed.
  *  workspace:    >= pkv_prefill_workspace_bytes(...), zeroed once by
  *                pkv_workspace_init (the call leaves its counters at zero)
  * Limits: num_pages * num_kv_heads * page_size < 2^31 rows per pool;
@@ -309,19 +328,29 @@ int pkv_prefill_chunk_attn(const void* q, const void* k_pages, const void* v_pag
  *  - The scratch is one device array of PKV_NOALLOC_SCRATCH_BYTES (2 MiB).
  *    Every GPU that loads the library holds it until the process exits. The
  *    call itself allocates and frees nothing.
+ *  - Geometry: 16 query / 8 KV heads, head_dim 128, page size 16 only (the
+ *    tuned decode kernel); other geometries return PKV_ERR_UNSUPPORTED.
  *  - Limit: batch <= PKV_NOALLOC_MAX_BATCH (256), and the scratch must cover
  *    the device's split partials (it does for up to ~240 SMs; a GB300 has 152).
  *    Larger requests return PKV_ERR_WORKSPACE_TOO_SMALL without launching.
- *  - The first call on a device looks up the array's device address (a
- *    one-time set-up); make that first call before any CUDA-graph capture.
+ *  - The first call on a device, and the first call in each other context
+ *    on it, looks up the array's device address (each context loads its own
+ *    copy of the array): a one-time set-up; make that first call before any
+ *    CUDA-graph capture. The call is not supported after cudaDeviceReset in
+ *    the same process: the device's primary context may come back under the
+ *    same handle while the array has moved.
  *  - Every call uses the same array and it keeps the previous call's
  *    contents; each call zeroes the status word, the split counters and records on
  *    `stream` before its kernel. Calls whose kernels overlap on the GPU (on
  *    different streams, or in parallel graph branches) race on the array:
  *    issue them in order on one stream.
- *  - Device-side errors (a page id outside the pool, a length beyond the block
- *    table) are skipped as in pkv_decode_attn but not reported: the status
- *    word lives in the library's array and no call reads it back.
+ *  - Device-side errors are not reported: the status word lives in the
+ *    library's array and no call reads it back. A page id outside the pool or
+ *    a length beyond the block table is skipped as in pkv_decode_attn. A
+ *    bounded wait of the split merge that runs out (see the convention on the
+ *    split merge above) leaves the output rows of the affected (request, KV
+ *    head) unwritten: `out` keeps whatever it held there, with no signal.
+ *    Callers that need to see such errors use pkv_decode_attn.
  */
 #define PKV_NOALLOC_SCRATCH_BYTES (2u << 20)
 #define PKV_NOALLOC_MAX_BATCH 256

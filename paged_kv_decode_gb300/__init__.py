@@ -8,8 +8,9 @@ raises.
 
 Layout (see include/pkv.h): pools bf16 [num_pages, Hkv, 16, D]; q / out bf16
 [rows, Hq, D]; block tables int32 [rows, max_pages]; lengths int32. The Qwen3
-decoder's 16/8/128 runs the tuned kernels; append, decode and the fused append
-+ decode call also take head_dim 64 or 128 with 1 to 8 query heads per KV head.
+decoder's 16/8/128 runs the tuned kernels; append, decode, the fused append +
+decode call and chunked prefill also take head_dim 64 or 128 with 1 to 8 query
+heads per KV head.
 """
 from __future__ import annotations
 
@@ -30,6 +31,7 @@ ERRORS = {
     -7: "PKV_ERR_OUT_OF_BOUNDS",
     -8: "PKV_ERR_MISALIGNED",
 }
+ERR_CODES = {name: code for code, name in ERRORS.items()}
 
 __all__ = [
     "PkvError", "desc", "Workspace", "append", "decode_attn", "prefill_chunk_attn",
@@ -110,8 +112,10 @@ def decode_workspace_bytes(batch: int, max_pages: int, num_pages: int = 1, num_q
     return int(_lib.load().pkv_decode_workspace_bytes(ctypes.byref(d), int(batch), int(max_pages)))
 
 
-def prefill_workspace_bytes(num_seqs: int, max_q_len: int, num_pages: int = 1) -> int:
-    d = desc(num_pages)
+def prefill_workspace_bytes(num_seqs: int, max_q_len: int, num_pages: int = 1, num_q_heads: int = 16,
+                            num_kv_heads: int = 8, head_dim: int = 128) -> int:
+    """Workspace bytes of a prefill call (default geometry: the Qwen3 decoder, 16/8/128)."""
+    d = desc(num_pages, num_q_heads, num_kv_heads, head_dim)
     return int(_lib.load().pkv_prefill_workspace_bytes(ctypes.byref(d), int(num_seqs), int(max_q_len)))
 
 
@@ -131,6 +135,15 @@ class Workspace:
 
     def status(self) -> int:
         return read_status(self.tensor)
+
+    def check(self, what: str = "device status"):
+        """Read the status word (synchronises); on a device error, zero the workspace again before
+        raising: a call that stopped early may have left split counters or tagged records behind,
+        which the next call would take for its own."""
+        code = self.status()
+        if code != PKV_OK:
+            workspace_init(self.tensor)
+            raise PkvError(code, what)
 
     def ensure(self, nbytes: int):
         if nbytes > self.nbytes:
@@ -261,7 +274,8 @@ def _decode_append(q, k_new, v_new, k_pages, v_pages, block_table, seq_lens, out
 
 def prefill_chunk_attn(q, k_pages, v_pages, block_table, prefix_lens, cu_q_lens, out, scale: float, max_q_len: int,
                        workspace: Workspace, stream=None):
-    """Causal chunk attention: out [total_q, 16, 128] for chunks packed by cu_q_lens."""
+    """Causal chunk attention: out [total_q, Hq, D] for chunks packed by cu_q_lens (Hq / Hkv from 1 to 8,
+    D 64 or 128)."""
     import torch
 
     _need(k_pages, torch.bfloat16, "k_pages")

@@ -13,7 +13,8 @@
 // that loads the library holds it until the process exits. Host code must not
 // pass the array's name to a kernel (on the host it is only a stand-in, not a
 // device address), so the entry point looks the device address up with
-// cudaGetSymbolAddress, once per device, with that device current.
+// cudaGetSymbolAddress, once per device and context, with that device current.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -31,16 +32,40 @@ static __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];
 
 std::mutex g_mu;
 void* g_scratch_addr[kMaxDevices] = {};
+CUcontext g_scratch_ctx[kMaxDevices] = {};
 int g_scratch_sms[kMaxDevices] = {};
 
-// Device address of the scratch array and SM count of the current device;
-// the first call on a device does the lookup.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+// The driver's cuCtxGetCurrent, found through the runtime (the library links
+// only the runtime).
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  }
+  return fn;
+}
+
+// Device address of the scratch array and SM count of the current device.
+// The first call on a device does the lookup, and so does the first call in
+// any other context on it: each context loads its own copy of the module, and
+// with it of the array.
 int scratch_of_current_device(void** addr, int* num_sms) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return PKV_ERR_UNSUPPORTED;
+  CtxGetCurrentFn get_ctx = ctx_get_current();
+  if (get_ctx == nullptr) return PKV_ERR_CUDA;
+  // the context current now (none yet if no runtime call has needed one on this thread)
+  CUcontext ctx = nullptr;
+  if (get_ctx(&ctx) != CUDA_SUCCESS) return PKV_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_scratch_addr[dev] == nullptr) {
+  if (ctx == nullptr || g_scratch_addr[dev] == nullptr || g_scratch_ctx[dev] != ctx) {
     int major = 0, minor = 0, sms = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
@@ -49,7 +74,10 @@ int scratch_of_current_device(void** addr, int* num_sms) {
     if (!(major == 10 && minor == 3)) return PKV_ERR_UNSUPPORTED;
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) return PKV_ERR_CUDA;
+    // the lookup made the device's context current if none was
+    if (get_ctx(&ctx) != CUDA_SUCCESS || ctx == nullptr) return PKV_ERR_CUDA;
     g_scratch_addr[dev] = p;
+    g_scratch_ctx[dev] = ctx;
     g_scratch_sms[dev] = sms;
   }
   *addr = g_scratch_addr[dev];

@@ -103,8 +103,9 @@ const char* pkv_status_string(int status) {
     case PKV_ERR_NULL_ARG: return "a required pointer is NULL";
     case PKV_ERR_BAD_SHAPE: return "bad or inconsistent size";
     case PKV_ERR_UNSUPPORTED:
-      return "unsupported geometry or device (sm_103; decode, fused append + decode and append: page 16, "
-             "head_dim 64/128, 1 to 8 query heads per KV head; prefill and the RoPE call: 16/8/128/16)";
+      return "unsupported geometry or device (sm_103; decode, fused append + decode, append and prefill: "
+             "page 16, head_dim 64/128, 1 to 8 query heads per KV head; the RoPE call and the no-alloc call: "
+             "16/8/128/16)";
     case PKV_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
     case PKV_ERR_CUDA: return "CUDA runtime or launch error";
     case PKV_ERR_DEVICE_TIMEOUT: return "a device-side wait ran out of time";
@@ -230,18 +231,28 @@ int pkv_decode_append_rope_attn(const void* q, const void* k_new, const void* v_
                        scale, stream, desc, batch, max_pages_per_seq, workspace, workspace_bytes, flags);
 }
 
+// Geometries pkv_prefill_chunk_attn serves (prefill.cu): page size 16, head_dim 64 or 128, 1 to 8
+// query heads per KV head; 16/8/128 among them.
+static int check_desc_prefill(const pkv_cache_desc* d) {
+  const int rc = check_desc(d);
+  if (rc != PKV_ERR_UNSUPPORTED) return rc;
+  return pkv::prefill_supported(d->num_q_heads, d->num_kv_heads, d->head_dim, d->page_size) ? PKV_OK
+                                                                                           : PKV_ERR_UNSUPPORTED;
+}
+
 size_t pkv_prefill_workspace_bytes(const pkv_cache_desc* desc, int32_t num_seqs, int32_t max_q_len) {
-  if (check_desc(desc) != PKV_OK || num_seqs < 0 || max_q_len < 0) return 0;
+  if (check_desc_prefill(desc) != PKV_OK || num_seqs < 0 || max_q_len < 0) return 0;
   int sms = 0;
   if (current_device(&sms) != PKV_OK) return 0;
-  return pkv::prefill_workspace_bytes(num_seqs, max_q_len, sms);
+  return pkv::prefill_workspace_bytes(desc->num_q_heads, desc->num_kv_heads, desc->head_dim, num_seqs, max_q_len,
+                                      sms);
 }
 
 int pkv_prefill_chunk_attn(const void* q, const void* k_pages, const void* v_pages, const int32_t* block_table,
                            const int32_t* prefix_lens, const int32_t* cu_q_lens, int32_t num_seqs, int32_t total_q,
                            void* out, float scale, pkv_stream_t stream, const pkv_cache_desc* desc,
                            int32_t max_pages_per_seq, int32_t max_q_len, void* workspace, size_t workspace_bytes) {
-  int rc = check_desc(desc);
+  int rc = check_desc_prefill(desc);
   if (rc != PKV_OK) return rc;
   if (num_seqs < 0 || total_q < 0 || max_q_len < 0 || max_pages_per_seq < 1) return PKV_ERR_BAD_SHAPE;
   if (!table_fits(num_seqs, max_pages_per_seq)) return PKV_ERR_BAD_SHAPE;
@@ -257,10 +268,12 @@ int pkv_prefill_chunk_attn(const void* q, const void* k_pages, const void* v_pag
   int sms = 0;
   rc = current_device(&sms);
   if (rc != PKV_OK) return rc;
-  if (workspace_bytes < pkv::prefill_workspace_bytes(num_seqs, max_q_len, sms)) return PKV_ERR_WORKSPACE_TOO_SMALL;
+  if (workspace_bytes < pkv::prefill_workspace_bytes(desc->num_q_heads, desc->num_kv_heads, desc->head_dim, num_seqs,
+                                                     max_q_len, sms))
+    return PKV_ERR_WORKSPACE_TOO_SMALL;
   return pkv::launch_prefill(q, k_pages, v_pages, block_table, prefix_lens, cu_q_lens, num_seqs, total_q, out, scale,
-                             max_pages_per_seq, max_q_len, desc->num_pages, workspace,
-                             reinterpret_cast<cudaStream_t>(stream));
+                             desc->num_q_heads, desc->num_kv_heads, desc->head_dim, max_pages_per_seq, max_q_len,
+                             desc->num_pages, workspace, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int pkv_selftest_wait_timeout(void* workspace, size_t workspace_bytes, int64_t limit_cycles, pkv_stream_t stream) {

@@ -36,12 +36,15 @@ int launch_decode_generic(const void* q, const void* k_new, const void* v_new, c
                           int32_t max_pages, int32_t num_pages, void* workspace, int num_sms, cudaStream_t stream,
                           uint32_t flags);
 
-size_t prefill_workspace_bytes(int32_t num_seqs, int32_t max_q_len, int num_sms);
+// Chunked prefill (prefill.cu): page size 16, head_dim 64 or 128, 1 to 8 query heads per KV head.
+bool prefill_supported(int num_q_heads, int num_kv_heads, int head_dim, int page_size);
+size_t prefill_workspace_bytes(int num_q_heads, int num_kv_heads, int head_dim, int32_t num_seqs, int32_t max_q_len,
+                               int num_sms);
 int prefill_max_seqs();
 int launch_prefill(const void* q, const void* k_pages, const void* v_pages, const int32_t* block_table,
                    const int32_t* prefix_lens, const int32_t* cu_q_lens, int32_t num_seqs, int32_t total_q,
-                   void* out, float scale, int32_t max_pages, int32_t max_q_len, int32_t num_pages, void* workspace,
-                   cudaStream_t stream);
+                   void* out, float scale, int num_q_heads, int num_kv_heads, int head_dim, int32_t max_pages,
+                   int32_t max_q_len, int32_t num_pages, void* workspace, cudaStream_t stream);
 
 int launch_wait_timeout_selftest(void* workspace, long long limit_cycles, cudaStream_t stream);
 

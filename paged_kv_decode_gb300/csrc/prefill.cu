@@ -60,24 +60,43 @@ constexpr int kPfThreads = 12 * 32;        // 3 warpgroups: softmax head 0, soft
 constexpr int kPfRegsSoftmax = 224;
 constexpr int kPfRegsOther = 56;
 static_assert(2 * 128 * kPfRegsSoftmax + 128 * kPfRegsOther <= kPfThreads * 168, "register split");
-constexpr int kPfHalfBytes = kPfRows * 128;  // one 64-column half of a 128 x 128 bf16 tile: 16 KiB
-constexpr int kPfTileBytes = 2 * kPfHalfBytes;
+constexpr int kPfHalfBytes = kPfRows * 128;  // one 64-column half of a 128-row bf16 tile: 16 KiB
 constexpr int kPfStages = 2;
-
-// shared memory (offsets from a 1024-byte aligned base)
-constexpr int kOffQ = 0;                                   // Q_0, Q_1
-constexpr int kOffV = kOffQ + 2 * kPfTileBytes;            // V stages
-constexpr int kOffK = kOffV + kPfStages * kPfTileBytes;    // K stages
-constexpr int kOffBars = kOffK + kPfStages * kPfTileBytes;
 constexpr int kNumBars = 14;
 constexpr int kPfMaxSeqs = 1024;  // request prefix sums live in shared memory
-// + tmem address, fail flag, two merge flags; alignment slack (the request prefix sums follow)
-constexpr int kPfSmemBytes = kOffBars + kNumBars * 8 + 16 + 1024;
-// + the request prefix sums and the CTA's share (lo, hi, U, G) as 64-bit words
+
+// Sizes that depend on the head dimension HD (64 or 128): a 128-row tile of Q,
+// K or V is HD / 64 halves of 64 columns (128-byte rows, 128-byte swizzle).
+template <int HD>
+struct PfDim {
+  static_assert(HD == 64 || HD == 128, "head_dim 64 or 128");
+  static constexpr int kHalves = HD / 64;
+  static constexpr int kTileBytes = kHalves * kPfHalfBytes;
+  static constexpr int kPageBytes = kPageSize * HD * 2;  // one page of K (or V) of one KV head
+  // shared memory (offsets from a 1024-byte aligned base)
+  static constexpr int kOffQ = 0;                                 // Q_0, Q_1
+  static constexpr int kOffV = kOffQ + 2 * kTileBytes;            // V stages
+  static constexpr int kOffK = kOffV + kPfStages * kTileBytes;    // K stages
+  static constexpr int kOffBars = kOffK + kPfStages * kTileBytes;
+  // + tmem address, fail flag, two merge flags; alignment slack (the request prefix sums follow).
+  // head_dim 64 pads the CTA to more than half the SM's shared memory: one CTA per SM, since each
+  // holds all 512 TMEM columns
+  static constexpr int kSmemBytes =
+      (kOffBars + kNumBars * 8 + 16 + 1024) > 120 * 1024 ? (kOffBars + kNumBars * 8 + 16 + 1024) : 120 * 1024;
+  // Partial record of a split piece, per query head slot: the piece's normalised output O / l as
+  // fp16, 4 dims per 8-byte word laid out [dim / 4][row] (a warp's 32 rows are one coalesced
+  // 256-byte line per word), then the rows' running max (log2 units) and sum as fp32.
+  static constexpr int kRecO = HD / 4 * kPfRows * 8;
+  static constexpr int kRecHeadBytes = kRecO + 2 * kPfRows * 4;
+  static constexpr int kRecBytes = 2 * kRecHeadBytes;
+  static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, HD, true);  // B = V tile, MN-major
+};
+
 // + the request prefix sums of cost units and of items, the schedule, the CTA's share (lo, hi, U, G) and each
 // softmax group's pending split pieces, as 64-bit words
+template <int HD>
 static size_t pf_smem_bytes(int num_seqs) {
-  return kPfSmemBytes + static_cast<size_t>(2 * (num_seqs + 1) + 1 + 4 + 4) * 8;
+  return PfDim<HD>::kSmemBytes + static_cast<size_t>(2 * (num_seqs + 1) + 1 + 4 + 4) * 8;
 }
 
 // Item mode (no item is split) when the largest item is at least this share
@@ -92,16 +111,11 @@ constexpr uint32_t kColO = 256;  // O_h at kColO + 128 h
 constexpr uint32_t kTmemCols = 512;
 
 constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, false);  // B = K tile, K-major
-constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, true);   // B = V tile, MN-major
 
-// Partial record of a split piece, per query head: the piece's normalised
-// output O / l as fp16, 4 dims per 8-byte word laid out [dim / 4][row] (a warp's
-// 32 rows are one coalesced 256-byte line per word), then the rows' running max
-// (log2 units) and sum as fp32.
-constexpr int kPfRecO = kHeadDim / 4 * kPfRows * 8;
-constexpr int kPfRecHeadBytes = kPfRecO + 2 * kPfRows * 4;
-constexpr int kPfRecBytes = 2 * kPfRecHeadBytes;
-
+// A CTA holds two query-head slots of one KV head: head pair p of KV head g is
+// query heads g G + 2p and g G + 2p + 1 (G query heads per KV head). With an
+// odd G the last pair has one head; its second slot repeats the first head and
+// its output is not written.
 struct PrefillArgs {
   const int* block_table;
   const int* prefix_lens;
@@ -113,11 +127,40 @@ struct PrefillArgs {
   int num_pages;
   int tmax;     // query tiles computed per request: ceil(max_q_len / 128)
   int workers;  // split mode: persistent CTAs (one per SM); the grid has max(workers, items) CTAs
+  int hq;       // query heads
+  int hkv;      // KV heads
+  int grp;      // query heads per KV head
+  int npair;    // head pairs per KV head: ceil(grp / 2)
+  int pairs;    // head pairs per request: hkv * npair
   float scale_log2;
   int* status;
-  int* counters;   // [num_seqs][8][tmax][2], zero between calls
-  unsigned char* records;  // [2 * workers][kPfRecBytes]
+  int* counters;   // [num_seqs][pairs][tmax][2], zero between calls
+  unsigned char* records;  // [2 * workers][PfDim::kRecBytes]
 };
+
+// Head counts of a launch: compile-time constants for the Qwen3 decoder's 16 query / 8 KV heads
+// (kFixed; its kernel keeps the register allocation and schedule tuned for it), the launch's
+// arguments for other geometries.
+template <bool kFixed>
+struct PfHeads {
+  __device__ __forceinline__ static int hq(const PrefillArgs& a) { return kFixed ? kQHeads : a.hq; }
+  __device__ __forceinline__ static int hkv(const PrefillArgs& a) { return kFixed ? kKVHeads : a.hkv; }
+  __device__ __forceinline__ static int grp(const PrefillArgs& a) { return kFixed ? kGroup : a.grp; }
+  __device__ __forceinline__ static int npair(const PrefillArgs& a) { return kFixed ? (kGroup + 1) / 2 : a.npair; }
+  __device__ __forceinline__ static int pairs(const PrefillArgs& a) {
+    return kFixed ? kKVHeads * ((kGroup + 1) / 2) : a.pairs;
+  }
+};
+
+// KV head, first query head, and whether the second slot holds a head of its own, of head pair hp.
+template <bool kFixed>
+__device__ __forceinline__ void pf_pair_heads(const PrefillArgs& a, int hp, int& g, int& qh0, bool& two) {
+  using Hd = PfHeads<kFixed>;
+  g = hp / Hd::npair(a);
+  const int p = hp - g * Hd::npair(a);
+  qh0 = g * Hd::grp(a) + 2 * p;
+  two = 2 * p + 1 < Hd::grp(a);
+}
 
 struct PfBars {
   uint64_t q_full;
@@ -130,38 +173,6 @@ struct PfBars {
   uint64_t o_done[2];
 };
 static_assert(sizeof(PfBars) == kNumBars * 8, "barrier block");
-
-// Share of the softmax exponentials (pairs out of every 4) evaluated on the FMA
-// pipe instead of the MUFU unit. With the raw-score max and packed FMAs the
-// softmax is bound by FMA-pipe issue rather than by MUFU, and any share > 0
-// measured slower on a GB300 (0: 670/986/1090, 1: 629/919/1005 TFLOP/s for a
-// 4096-row chunk after 0/8192/32768 cached tokens), so the default is 0.
-#ifndef PKV_PF_POLY_PAIRS
-#define PKV_PF_POLY_PAIRS 0
-#endif
-constexpr int kPfPolyPairsOf4 = PKV_PF_POLY_PAIRS;
-
-// 2^t for a pair of t <= 8 (t = -inf gives about 2^-125) without the MUFU unit:
-// Cody-Waite range reduction 2^t = 2^n * 2^f with n = round(t) (the 1.5 * 2^23
-// addition rounds t to an integer in the low mantissa bits) and f in [-1/2, 1/2],
-// 2^f from a degree-3 polynomial fitted by the Remez exchange for relative
-// error (max 7.5e-5; exp2_poly_fit.py reproduces the constants), and 2^n
-// applied by adding n to the exponent field.
-__device__ __forceinline__ float2 exp2_poly2(float2 t) {
-  constexpr float kRound = 12582912.f;  // 1.5 * 2^23
-  constexpr float c0 = 0.9999280571937561f, c1 = 0.6932609677314758f, c2 = 0.2426111251115799f,
-                  c3 = 0.0551716685295105f;
-  t.x = fmaxf(t.x, -125.f);
-  t.y = fmaxf(t.y, -125.f);
-  const float2 j = __fadd2_rn(t, make_float2(kRound, kRound));
-  const float2 n = __fadd2_rn(j, make_float2(-kRound, -kRound));
-  const float2 f = __ffma2_rn(n, make_float2(-1.f, -1.f), t);
-  float2 p = __ffma2_rn(make_float2(c3, c3), f, make_float2(c2, c2));
-  p = __ffma2_rn(p, f, make_float2(c1, c1));
-  p = __ffma2_rn(p, f, make_float2(c0, c0));
-  return make_float2(__int_as_float(__float_as_int(p.x) + (__float_as_int(j.x) << 23)),
-                     __int_as_float(__float_as_int(p.y) + (__float_as_int(j.y) << 23)));
-}
 
 // Bounded wait that gives up at once after any wait of the CTA has timed out.
 __device__ __forceinline__ bool pf_wait(uint64_t* bar, uint32_t parity, volatile int* fail, int* status) {
@@ -184,15 +195,15 @@ __device__ __forceinline__ bool pf_wait_warp(uint64_t* bar, uint32_t parity, vol
 // are cut in cost units: an item costs kPfItemCost units for its fixed work (the
 // query tile load, the pipeline fill and drain, the epilogue) followed by one
 // unit per key tile, so a CTA whose share holds many small items gets fewer key
-// tiles. A (request, head) costs W = sum over its items; pref[n] = 8 * sum of W
-// before n. A piece is the part of one item inside a CTA's share that holds key
+// tiles. A (request, head pair) costs W = sum over its items; pref[n] = pairs * sum
+// of W before n. A piece is the part of one item inside a CTA's share that holds key
 // tiles: [k0, k1).
 #ifndef PKV_PF_ITEM_COST
 #define PKV_PF_ITEM_COST 2
 #endif
 constexpr int kPfItemCost = PKV_PF_ITEM_COST;
 struct PfPiece {
-  int n, g, t, k0, k1, nt, q0, qlen, P;
+  int n, hp, t, k0, k1, nt, q0, qlen, P;  // hp: head pair of the request
   long long fseg, fend;  // the item's cost units start at fseg; the piece ends at fend
 };
 
@@ -216,6 +227,7 @@ __device__ __forceinline__ long long pf_units_before(int P, int t) {
 // cost units, cutting through items, whose partial results are merged
 // afterwards. (Item mode, CTA b computing item b of each request's items taken
 // heaviest first, needs no pieces.)
+template <bool kFixed>
 __device__ __forceinline__ bool pf_find_piece(long long f, long long hi, const long long* pref, const PrefillArgs& a,
                                               PfPiece& pc) {
   for (; f < hi; f = pc.fend) {
@@ -228,10 +240,10 @@ __device__ __forceinline__ bool pf_find_piece(long long f, long long hi, const l
     pc.q0 = __ldg(a.cu_q_lens + lo_n);
     pc.qlen = __ldg(a.cu_q_lens + lo_n + 1) - pc.q0;
     pc.P = __ldg(a.prefix_lens + lo_n);
-    const long long W = (pref[lo_n + 1] - pref[lo_n]) / kKVHeads;
+    const long long W = (pref[lo_n + 1] - pref[lo_n]) / PfHeads<kFixed>::pairs(a);
     const long long off = f - pref[lo_n];
-    pc.g = static_cast<int>(off / W);
-    const long long o2 = off - pc.g * W;
+    pc.hp = static_cast<int>(off / W);
+    const long long o2 = off - pc.hp * W;
     int lo_t = 0, hi_t = pf_qtiles(pc.qlen, a.tmax) - 1;
     while (lo_t < hi_t) {
       const int mid = (lo_t + hi_t + 1) >> 1;
@@ -245,7 +257,7 @@ __device__ __forceinline__ bool pf_find_piece(long long f, long long hi, const l
     const long long p1 = p_end < kPfItemCost + pc.nt ? p_end : kPfItemCost + pc.nt;
     pc.k0 = static_cast<int>(p0 > kPfItemCost ? p0 - kPfItemCost : 0);
     pc.k1 = static_cast<int>(p1 - kPfItemCost);
-    pc.fseg = pref[lo_n] + pc.g * W + ub;
+    pc.fseg = pref[lo_n] + pc.hp * W + ub;
     pc.fend = f + (p1 - p0);
     if (pc.k1 > pc.k0) return true;
   }
@@ -262,14 +274,17 @@ __device__ __forceinline__ void pf_group_sync(int h) {  // the 128 softmax threa
   asm volatile("bar.sync %0, 128;" ::"r"(2 + h) : "memory");
 }
 
+template <int HD, bool kFixed>
 __global__ void __launch_bounds__(kPfThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem =
       smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);  // 1024-byte aligned for 128-byte swizzle atoms
-  PfBars* bars = reinterpret_cast<PfBars*>(smem + kOffBars);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBars + kNumBars * 8);
+  using Dm = PfDim<HD>;
+  using Hd = PfHeads<kFixed>;
+  PfBars* bars = reinterpret_cast<PfBars*>(smem + Dm::kOffBars);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Dm::kOffBars + kNumBars * 8);
   volatile int* fail = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* merge_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);  // [2]
   long long* pref = reinterpret_cast<long long*>(tmem_slot + 4);
@@ -298,7 +313,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     fence_barrier_init();
   }
   if (warp == 1) {
-    // units per request (8 W_n; 0 for a request whose shape is out of bounds) and their exclusive prefix
+    // units per request (pairs W_n; 0 for a request whose shape is out of bounds) and their exclusive prefix
     long long carry = 0, icarry = 0, tiles_all = 0;
     int nt_max = 0;
     long long* ipref = pref + a.num_seqs + 2;
@@ -315,10 +330,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         if (P < 0 || q0 < 0 || qlen < 0 || q1 > a.total_q || static_cast<long long>(P) + rows > cap) {
           set_status(a.status, PKV_ERR_OUT_OF_BOUNDS);
         } else if (T > 0) {
+          // a chunk longer than the caller's max_q_len bound: its rows past the first tmax query
+          // tiles are not computed, so the call reports it
+          if (qlen > static_cast<long long>(kPfRows) * a.tmax) set_status(a.status, PKV_ERR_OUT_OF_BOUNDS);
           const int nt_last = pf_tiles(P, qlen, T - 1);
-          w8 = kKVHeads * (pf_units_before(P, T - 1) + kPfItemCost + nt_last);
-          tiles_all += w8 - static_cast<long long>(kKVHeads) * kPfItemCost * T;
-          items = static_cast<long long>(kKVHeads) * T;
+          w8 = Hd::pairs(a) * (pf_units_before(P, T - 1) + kPfItemCost + nt_last);
+          tiles_all += w8 - static_cast<long long>(Hd::pairs(a)) * kPfItemCost * T;
+          items = static_cast<long long>(Hd::pairs(a)) * T;
           nt_max = nt_max > nt_last ? nt_max : nt_last;
         }
       }
@@ -359,9 +377,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  unsigned char* sQ = smem + kOffQ;
-  unsigned char* sV = smem + kOffV;
-  unsigned char* sK = smem + kOffK;
+  unsigned char* sQ = smem + Dm::kOffQ;
+  unsigned char* sV = smem + Dm::kOffV;
+  unsigned char* sK = smem + Dm::kOffK;
 
   const bool item_mode = pref[a.num_seqs + 1] != 0;
 
@@ -379,8 +397,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const int qlen = __ldg(a.cu_q_lens + n + 1) - q0;
       const int P = __ldg(a.prefix_lens + n);
       const int jj = static_cast<int>(b - ipref[n]);
-      const int tile = pf_qtiles(qlen, a.tmax) - 1 - jj / kKVHeads;  // heaviest first
-      const int g = jj % kKVHeads;
+      const int tile = pf_qtiles(qlen, a.tmax) - 1 - jj / Hd::pairs(a);  // heaviest first
+      int g, qh0;
+      bool two;
+      pf_pair_heads<kFixed>(a, jj % Hd::pairs(a), g, qh0, two);
       const int i0 = tile * kPfRows;
       const int rows_here = qlen - i0 < kPfRows ? qlen - i0 : kPfRows;
       const int kv_end = P + i0 + rows_here;  // in bounds: the length scan dropped out-of-bounds requests
@@ -390,11 +410,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       // ------------------------------------------------------------------ TMA producer
       asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kPfRegsOther));
       if (lane == 0) {
-        mbar_arrive_expect_tx(&bars->q_full, 2 * kPfTileBytes);
+        mbar_arrive_expect_tx(&bars->q_full, 2 * Dm::kTileBytes);
         for (int h = 0; h < 2; ++h)
-          for (int half = 0; half < 2; ++half)
-            tma_load_3d(sQ + h * kPfTileBytes + half * kPfHalfBytes, &qmap, half * 64, 2 * g + h, q0 + i0,
-                        &bars->q_full);
+          for (int half = 0; half < Dm::kHalves; ++half)
+            tma_load_3d(sQ + h * Dm::kTileBytes + half * kPfHalfBytes, &qmap, half * 64, qh0 + (two ? h : 0),
+                        q0 + i0, &bars->q_full);
       }
       for (int j = 0; j < n_tiles; ++j) {
         const int st = j & 1;
@@ -411,20 +431,22 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           }
         }
         const unsigned vmask = __ballot_sync(0xffffffffu, valid);
-        const uint32_t bytes = static_cast<uint32_t>(__popc(vmask)) * 2u * (kPageSize * 128u);
+        const uint32_t bytes = static_cast<uint32_t>(__popc(vmask)) * static_cast<uint32_t>(Dm::kPageBytes);
         if (lane == 0) {
           mbar_arrive_expect_tx(&bars->k_full[st], bytes);
           mbar_arrive_expect_tx(&bars->v_full[st], bytes);
         }
         __syncwarp();
         if (valid) {
-          const int row = (id * kKVHeads + g) * kPageSize;
-          unsigned char* kd = sK + st * kPfTileBytes + lane * (kPageSize * 128);
-          unsigned char* vd = sV + st * kPfTileBytes + lane * (kPageSize * 128);
-          tma_load_2d(kd, &kmap, 0, row, &bars->k_full[st]);
-          tma_load_2d(kd + kPfHalfBytes, &kmap, 64, row, &bars->k_full[st]);
-          tma_load_2d(vd, &vmap, 0, row, &bars->v_full[st]);
-          tma_load_2d(vd + kPfHalfBytes, &vmap, 64, row, &bars->v_full[st]);
+          const int row = (id * Hd::hkv(a) + g) * kPageSize;
+          unsigned char* kd = sK + st * Dm::kTileBytes + lane * (kPageSize * 128);
+          unsigned char* vd = sV + st * Dm::kTileBytes + lane * (kPageSize * 128);
+  #pragma unroll
+          for (int half = 0; half < Dm::kHalves; ++half)  // K first: the QK MMA waits only for K
+            tma_load_2d(kd + half * kPfHalfBytes, &kmap, 64 * half, row, &bars->k_full[st]);
+  #pragma unroll
+          for (int half = 0; half < Dm::kHalves; ++half)
+            tma_load_2d(vd + half * kPfHalfBytes, &vmap, 64 * half, row, &bars->v_full[st]);
         }
       }
     } else if (warp == kPfMmaWarp) {
@@ -438,10 +460,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       auto issue_qk = [&](int j, int h) {
         tc_fence_after();
         if (lane == 0) {
-          const uint32_t qa = smem_u32(sQ + h * kPfTileBytes);
-          const uint32_t kb = smem_u32(sK + (j & 1) * kPfTileBytes);
+          const uint32_t qa = smem_u32(sQ + h * Dm::kTileBytes);
+          const uint32_t kb = smem_u32(sK + (j & 1) * Dm::kTileBytes);
   #pragma unroll
-          for (int s = 0; s < 8; ++s) {
+          for (int s = 0; s < HD / 16; ++s) {
             const uint32_t off = (s >> 2) * kPfHalfBytes + (s & 3) * 32;
             mma_ss(tmem + kColS + 128 * h, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
                    kIdescQK, s > 0 ? 1u : 0u);
@@ -453,11 +475,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       auto issue_pv = [&](int j, int h) {
         tc_fence_after();
         if (lane == 0) {
-          const uint32_t vb = smem_u32(sV + (j & 1) * kPfTileBytes);
+          const uint32_t vb = smem_u32(sV + (j & 1) * Dm::kTileBytes);
   #pragma unroll
           for (int s = 0; s < 8; ++s) {
             mma_ts(tmem + kColO + 128 * h, tmem + kColS + 128 * h + 8 * s,
-                   sdesc_sw128(vb + s * 2048, kPfHalfBytes, 1024), kIdescPV, (j > 0 || s > 0) ? 1u : 0u);
+                   sdesc_sw128(vb + s * 2048, kPfHalfBytes, 1024), Dm::kIdescPV, (j > 0 || s > 0) ? 1u : 0u);
           }
           mma_commit(&bars->o_done[h]);
         }
@@ -477,10 +499,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         if (j == n_tiles - 1 && kv_end < (j + 1) * kPfKeys) {
           // keys past the end: zero their V rows (unused slots may hold NaN and 0 * NaN = NaN)
           const int r0 = kv_end - j * kPfKeys;
-          uint4* vbase = reinterpret_cast<uint4*>(sV + st * kPfTileBytes);
+          uint4* vbase = reinterpret_cast<uint4*>(sV + st * Dm::kTileBytes);
           for (int idx = r0 * 8 + lane; idx < kPfKeys * 8; idx += 32) {
-            vbase[idx] = make_uint4(0, 0, 0, 0);
-            vbase[kPfHalfBytes / 16 + idx] = make_uint4(0, 0, 0, 0);
+  #pragma unroll
+            for (int half = 0; half < Dm::kHalves; ++half) vbase[half * (kPfHalfBytes / 16) + idx] = make_uint4(0, 0, 0, 0);
           }
           fence_proxy_async_smem();
           __syncwarp();
@@ -549,7 +571,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           const float alpha = first ? 0.f : (grow ? ex2((m_used - m_new) * a.scale_log2) : 1.f);
           if (j > 0) {
   #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < HD / 32; ++c) {
               uint32_t orr[32];
               tmem_ld32(t_row + kColO + 128 * h + 32 * c, orr);
               tmem_ld_wait();
@@ -578,12 +600,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
               const float2 t = __ffma2_rn(make_float2(__uint_as_float(sr[2 * hc + c2][e]),
                                                       __uint_as_float(sr[2 * hc + c2][e + 1])),
                                           sc2, nm2);
-              float2 pp;
-              if (((e >> 1) & 3) < kPfPolyPairsOf4) {
-                pp = exp2_poly2(t);
-              } else {
-                pp = make_float2(ex2(t.x), ex2(t.y));
-              }
+              const float2 pp = make_float2(ex2(t.x), ex2(t.y));
               l2 = __fadd2_rn(l2, pp);
               pk[c2 * 16 + (e >> 1)] = pack_bf16x2(pp.x, pp.y);
             }
@@ -597,10 +614,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       if (ok && pf_wait_warp(&bars->o_done[h], static_cast<uint32_t>(n_tiles - 1) & 1u, fail, a.status)) {
         tc_fence_after();
         const float inv = 1.f / l;
-        const bool write = r < rows_here;
-        __nv_bfloat16* orow = a.out + (static_cast<size_t>(q0 + i0 + r) * kQHeads + 2 * g + h) * kHeadDim;
+        const bool write = r < rows_here && (h == 0 || two);
+        __nv_bfloat16* orow = a.out + (static_cast<size_t>(q0 + i0 + r) * Hd::hq(a) + qh0 + h) * HD;
   #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < HD / 32; ++c) {
           uint32_t orr[32];
           tmem_ld32(t_row + kColO + 128 * h + 32 * c, orr);
           tmem_ld_wait();
@@ -642,14 +659,17 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       int pi = 0;
       PfPiece pc;
       bool run = true;
-      for (long long f = lo; run && pf_find_piece(f, hi, pref, a, pc); f = pc.fend, ++pi) {
+      for (long long f = lo; run && pf_find_piece<kFixed>(f, hi, pref, a, pc); f = pc.fend, ++pi) {
         // this piece's query tiles, once the previous piece's QK MMAs are done with the buffer
         if (pi > 0 && !pf_wait_warp(&bars->q_empty, static_cast<uint32_t>(pi - 1) & 1u, fail, a.status)) break;
         if (lane == 0) {
-          mbar_arrive_expect_tx(&bars->q_full, 2 * kPfTileBytes);
+          int g, qh0;
+          bool two;
+          pf_pair_heads<kFixed>(a, pc.hp, g, qh0, two);
+          mbar_arrive_expect_tx(&bars->q_full, 2 * Dm::kTileBytes);
           for (int h = 0; h < 2; ++h)
-            for (int half = 0; half < 2; ++half)
-              tma_load_3d(sQ + h * kPfTileBytes + half * kPfHalfBytes, &qmap, half * 64, 2 * pc.g + h,
+            for (int half = 0; half < Dm::kHalves; ++half)
+              tma_load_3d(sQ + h * Dm::kTileBytes + half * kPfHalfBytes, &qmap, half * 64, qh0 + (two ? h : 0),
                           pc.q0 + pc.t * kPfRows, &bars->q_full);
         }
         const int rows = pc.qlen < kPfRows * (pc.t + 1) ? pc.qlen : kPfRows * (pc.t + 1);
@@ -672,20 +692,22 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             }
           }
           const unsigned vmask = __ballot_sync(0xffffffffu, valid);
-          const uint32_t bytes = static_cast<uint32_t>(__popc(vmask)) * 2u * (kPageSize * 128u);
+          const uint32_t bytes = static_cast<uint32_t>(__popc(vmask)) * static_cast<uint32_t>(Dm::kPageBytes);
           if (lane == 0) {
             mbar_arrive_expect_tx(&bars->k_full[st], bytes);
             mbar_arrive_expect_tx(&bars->v_full[st], bytes);
           }
           __syncwarp();
           if (valid) {
-            const int row = (id * kKVHeads + pc.g) * kPageSize;
-            unsigned char* kd = sK + st * kPfTileBytes + lane * (kPageSize * 128);
-            unsigned char* vd = sV + st * kPfTileBytes + lane * (kPageSize * 128);
-            tma_load_2d(kd, &kmap, 0, row, &bars->k_full[st]);
-            tma_load_2d(kd + kPfHalfBytes, &kmap, 64, row, &bars->k_full[st]);
-            tma_load_2d(vd, &vmap, 0, row, &bars->v_full[st]);
-            tma_load_2d(vd + kPfHalfBytes, &vmap, 64, row, &bars->v_full[st]);
+            const int row = (id * Hd::hkv(a) + pc.hp / Hd::npair(a)) * kPageSize;
+            unsigned char* kd = sK + st * Dm::kTileBytes + lane * (kPageSize * 128);
+            unsigned char* vd = sV + st * Dm::kTileBytes + lane * (kPageSize * 128);
+  #pragma unroll
+            for (int half = 0; half < Dm::kHalves; ++half)  // K first: the QK MMA waits only for K
+              tma_load_2d(kd + half * kPfHalfBytes, &kmap, 64 * half, row, &bars->k_full[st]);
+  #pragma unroll
+            for (int half = 0; half < Dm::kHalves; ++half)
+              tma_load_2d(vd + half * kPfHalfBytes, &vmap, 64 * half, row, &bars->v_full[st]);
           }
         }
       }
@@ -701,10 +723,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       auto issue_qk = [&](int st, int h) {
         tc_fence_after();
         if (lane == 0) {
-          const uint32_t qa = smem_u32(sQ + h * kPfTileBytes);
-          const uint32_t kb = smem_u32(sK + st * kPfTileBytes);
+          const uint32_t qa = smem_u32(sQ + h * Dm::kTileBytes);
+          const uint32_t kb = smem_u32(sK + st * Dm::kTileBytes);
   #pragma unroll
-          for (int s = 0; s < 8; ++s) {
+          for (int s = 0; s < HD / 16; ++s) {
             const uint32_t off = (s >> 2) * kPfHalfBytes + (s & 3) * 32;
             mma_ss(tmem + kColS + 128 * h, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
                    kIdescQK, s > 0 ? 1u : 0u);
@@ -716,11 +738,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       auto issue_pv = [&](int st, int h, bool acc) {
         tc_fence_after();
         if (lane == 0) {
-          const uint32_t vb = smem_u32(sV + st * kPfTileBytes);
+          const uint32_t vb = smem_u32(sV + st * Dm::kTileBytes);
   #pragma unroll
           for (int s = 0; s < 8; ++s) {
             mma_ts(tmem + kColO + 128 * h, tmem + kColS + 128 * h + 8 * s,
-                   sdesc_sw128(vb + s * 2048, kPfHalfBytes, 1024), kIdescPV, (acc || s > 0) ? 1u : 0u);
+                   sdesc_sw128(vb + s * 2048, kPfHalfBytes, 1024), Dm::kIdescPV, (acc || s > 0) ? 1u : 0u);
           }
           mma_commit(&bars->o_done[h]);
         }
@@ -731,8 +753,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         __syncwarp();
       };
       PfPiece cur, nxt;
-      bool ok = pf_find_piece(lo, hi, pref, a, cur);
-      bool have_nxt = ok && pf_find_piece(cur.fend, hi, pref, a, nxt);
+      bool ok = pf_find_piece<kFixed>(lo, hi, pref, a, cur);
+      bool have_nxt = ok && pf_find_piece<kFixed>(cur.fend, hi, pref, a, nxt);
       ok = ok && pf_wait_warp(&bars->q_full, 0, fail, a.status) && pf_wait_warp(&bars->k_full[0], 0, fail, a.status);
       if (ok) {
         issue_qk(0, 0);
@@ -754,10 +776,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         if (k == cur.nt - 1 && kv_end < (k + 1) * kPfKeys) {
           // keys past the end: zero their V rows (unused slots may hold NaN and 0 * NaN = NaN)
           const int r0 = kv_end - k * kPfKeys;
-          uint4* vbase = reinterpret_cast<uint4*>(sV + st * kPfTileBytes);
+          uint4* vbase = reinterpret_cast<uint4*>(sV + st * Dm::kTileBytes);
           for (int idx = r0 * 8 + lane; idx < kPfKeys * 8; idx += 32) {
-            vbase[idx] = make_uint4(0, 0, 0, 0);
-            vbase[kPfHalfBytes / 16 + idx] = make_uint4(0, 0, 0, 0);
+  #pragma unroll
+            for (int half = 0; half < Dm::kHalves; ++half) vbase[half * (kPfHalfBytes / 16) + idx] = make_uint4(0, 0, 0, 0);
           }
           fence_proxy_async_smem();
           __syncwarp();
@@ -785,7 +807,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           ++j;
         } else {
           cur = nxt;
-          have_nxt = pf_find_piece(cur.fend, hi, pref, a, nxt);
+          have_nxt = pf_find_piece<kFixed>(cur.fend, hi, pref, a, nxt);
           j = 0;
           ++pi;
         }
@@ -815,7 +837,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         int kb, ke, lim, diag_from;
         {
           PfPiece pc;
-          if (!pf_find_piece(f, share[1], pref, a, pc)) break;
+          if (!pf_find_piece<kFixed>(f, share[1], pref, a, pc)) break;
           const int i0 = pc.t * kPfRows;
           const int rows = pc.qlen < i0 + kPfRows ? pc.qlen : i0 + kPfRows;
           const int lim_row = pc.P + i0 + r;  // last visible key of this row (causal)
@@ -858,7 +880,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             const float alpha = first ? 0.f : (grow ? ex2((m_used - m_new) * a.scale_log2) : 1.f);
             if (k > kb) {
   #pragma unroll
-              for (int c = 0; c < 4; ++c) {
+              for (int c = 0; c < HD / 32; ++c) {
                 uint32_t orr[32];
                 tmem_ld32(t_row + kColO + 128 * h + 32 * c, orr);
                 tmem_ld_wait();
@@ -886,12 +908,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             for (int e = 0; e < 32; e += 2) {
               const float2 t =
                   __ffma2_rn(make_float2(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1])), sc2, nm2);
-              float2 pp;
-              if (((e >> 1) & 3) < kPfPolyPairsOf4) {
-                pp = exp2_poly2(t);
-              } else {
-                pp = make_float2(ex2(t.x), ex2(t.y));
-              }
+              const float2 pp = make_float2(ex2(t.x), ex2(t.y));
               l2 = __fadd2_rn(l2, pp);
               pk[e >> 1] = pack_bf16x2(pp.x, pp.y);
             }
@@ -907,16 +924,19 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         if (ok) tc_fence_after();
         asm volatile("" : "+l"(f));  // look the piece up again rather than keep it live
         PfPiece pc;
-        pf_find_piece(f, share[1], pref, a, pc);
+        pf_find_piece<kFixed>(f, share[1], pref, a, pc);
         const int i0 = pc.t * kPfRows;
         const int rows_here = (pc.qlen < i0 + kPfRows ? pc.qlen : i0 + kPfRows) - i0;
-        const bool write = r < rows_here;
-        __nv_bfloat16* orow = a.out + (static_cast<size_t>(pc.q0 + i0 + r) * kQHeads + 2 * pc.g + h) * kHeadDim;
+        int pg_, qh0;
+        bool two;
+        pf_pair_heads<kFixed>(a, pc.hp, pg_, qh0, two);
+        const bool write = r < rows_here && (h == 0 || two);
+        __nv_bfloat16* orow = a.out + (static_cast<size_t>(pc.q0 + i0 + r) * Hd::hq(a) + qh0 + h) * HD;
         if (pc.k0 == 0 && pc.k1 == pc.nt) {
           if (ok) {
             const float inv = 1.f / l;
   #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < HD / 32; ++c) {
               uint32_t orr[32];
               tmem_ld32(t_row + kColO + 128 * h + 32 * c, orr);
               tmem_ld_wait();
@@ -937,14 +957,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         } else {
           // Split piece (only a share's first and last piece can be): write this
           // CTA's partial record of the row now, count it after the last piece.
-          unsigned char* rec = a.records + static_cast<size_t>(2 * blockIdx.x + (f == share[0] ? 0 : 1)) * kPfRecBytes +
-                               h * kPfRecHeadBytes;
+          unsigned char* rec = a.records +
+                               static_cast<size_t>(2 * blockIdx.x + (f == share[0] ? 0 : 1)) * Dm::kRecBytes +
+                               h * Dm::kRecHeadBytes;
           uint2* ro = reinterpret_cast<uint2*>(rec);
-          float* rml = reinterpret_cast<float*>(rec + kPfRecO);
+          float* rml = reinterpret_cast<float*>(rec + Dm::kRecO);
           const float inv = l > 0.f ? 1.f / l : 0.f;  // a row with no visible key in the piece has l = 0
           if (ok) {
   #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < HD / 32; ++c) {
               uint32_t orr[32];
               tmem_ld32(t_row + kColO + 128 * h + 32 * c, orr);
               tmem_ld_wait();
@@ -982,9 +1003,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             const long long fi = i == 0 ? pf0 : pf1;
             if (fi < 0) continue;
             PfPiece pc;
-            pf_find_piece(fi, share[1], pref, a, pc);
+            pf_find_piece<kFixed>(fi, share[1], pref, a, pc);
             want[i] = pf_cta_of(pc.fseg + kPfItemCost + pc.nt - 1, Us, Gs) - pf_cta_of(pc.fseg + kPfItemCost, Us, Gs);
-            old[i] = atomicAdd(a.counters + ((static_cast<size_t>(pc.n) * kKVHeads + pc.g) * a.tmax + pc.t) * 2 + h, 1);
+            old[i] = atomicAdd(a.counters + ((static_cast<size_t>(pc.n) * Hd::pairs(a) + pc.hp) * a.tmax + pc.t) * 2 + h, 1);
           }
           __threadfence();
           if (pf0 >= 0 && old[0] == want[0]) flags |= 1;
@@ -997,23 +1018,27 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         for (int i = 0; i < 2; ++i) {
           if (!((flags >> i) & 1)) continue;
           PfPiece pc;
-          pf_find_piece(i == 0 ? pf0 : pf1, share[1], pref, a, pc);
+          pf_find_piece<kFixed>(i == 0 ? pf0 : pf1, share[1], pref, a, pc);
           const int holders0 = pf_cta_of(pc.fseg + kPfItemCost, Us, Gs);
           const int nhold = pf_cta_of(pc.fseg + kPfItemCost + pc.nt - 1, Us, Gs) - holders0 + 1;
           const bool first_has_two = pf_share_lo(holders0, Us, Gs) < pc.fseg;
           auto rec_of = [&](int j) {
             const int c = holders0 + j;
-            return a.records + static_cast<size_t>(2 * c + ((j == 0 && first_has_two) ? 1 : 0)) * kPfRecBytes +
-                   h * kPfRecHeadBytes;
+            return a.records + static_cast<size_t>(2 * c + ((j == 0 && first_has_two) ? 1 : 0)) * Dm::kRecBytes +
+                   h * Dm::kRecHeadBytes;
           };
           float M = -CUDART_INF_F;
-          for (int j = 0; j < nhold; ++j) M = fmaxf(M, __ldcg(reinterpret_cast<const float*>(rec_of(j) + kPfRecO) + r));
+          for (int j = 0; j < nhold; ++j)
+            M = fmaxf(M, __ldcg(reinterpret_cast<const float*>(rec_of(j) + Dm::kRecO) + r));
           const int i0 = pc.t * kPfRows;
-          const bool write = r < (pc.qlen < i0 + kPfRows ? pc.qlen : i0 + kPfRows) - i0;
-          __nv_bfloat16* orow = a.out + (static_cast<size_t>(pc.q0 + i0 + r) * kQHeads + 2 * pc.g + h) * kHeadDim;
+          int pg_, qh0;
+          bool two;
+          pf_pair_heads<kFixed>(a, pc.hp, pg_, qh0, two);
+          const bool write = r < (pc.qlen < i0 + kPfRows ? pc.qlen : i0 + kPfRows) - i0 && (h == 0 || two);
+          __nv_bfloat16* orow = a.out + (static_cast<size_t>(pc.q0 + i0 + r) * Hd::hq(a) + qh0 + h) * HD;
           float L = 0.f;
   #pragma unroll 1
-          for (int half = 0; half < 2; ++half) {  // dims 64 half .. 64 half + 63
+          for (int half = 0; half < Dm::kHalves; ++half) {  // dims 64 half .. 64 half + 63
             float acc[64];
   #pragma unroll
             for (int e = 0; e < 64; ++e) acc[e] = 0.f;
@@ -1021,8 +1046,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   #pragma unroll 2
             for (int j = 0; j < nhold; ++j) {
               const unsigned char* rj = rec_of(j);
-              const float m_j = __ldcg(reinterpret_cast<const float*>(rj + kPfRecO) + r);
-              const float l_j = __ldcg(reinterpret_cast<const float*>(rj + kPfRecO) + kPfRows + r);
+              const float m_j = __ldcg(reinterpret_cast<const float*>(rj + Dm::kRecO) + r);
+              const float l_j = __ldcg(reinterpret_cast<const float*>(rj + Dm::kRecO) + kPfRows + r);
               const float w = m_j == -CUDART_INF_F ? 0.f : ex2(m_j - M) * l_j;  // the record holds O / l
               lsum += w;
               const uint2* oj = reinterpret_cast<const uint2*>(rj) + (16 * half) * kPfRows + r;
@@ -1053,7 +1078,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             }
           }
           if (quarter == 0 && lane == 0)
-            a.counters[((static_cast<size_t>(pc.n) * kKVHeads + pc.g) * a.tmax + pc.t) * 2 + h] = 0;
+            a.counters[((static_cast<size_t>(pc.n) * Hd::pairs(a) + pc.hp) * a.tmax + pc.t) * 2 + h] = 0;
         }
       }
     } else {
@@ -1087,31 +1112,65 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Workspace: status header, split counters [num_seqs][8][tmax][2], then two
-// partial records per CTA of the persistent grid (one CTA per SM).
-static size_t pf_counter_bytes(int32_t num_seqs, int32_t max_q_len) {
+// Workspace: status header, split counters [num_seqs][head pairs][tmax][2], then
+// two partial records per CTA of the persistent grid (one CTA per SM).
+static int pf_pairs(int hq, int hkv) { return hkv * ((hq / hkv + 1) / 2); }
+static size_t pf_counter_bytes(int32_t num_seqs, int32_t max_q_len, int pairs) {
   const size_t tmax = (static_cast<size_t>(max_q_len) + kPfRows - 1) / kPfRows;
-  return (static_cast<size_t>(num_seqs) * kKVHeads * tmax * 2 * 4 + 255) / 256 * 256;
+  return (static_cast<size_t>(num_seqs) * pairs * tmax * 2 * 4 + 255) / 256 * 256;
 }
-size_t prefill_workspace_bytes(int32_t num_seqs, int32_t max_q_len, int num_sms) {
-  return PKV_STATUS_BYTES + pf_counter_bytes(num_seqs, max_q_len) +
-         static_cast<size_t>(2) * num_sms * kPfRecBytes;
+static size_t pf_rec_bytes(int hd) { return hd == 64 ? PfDim<64>::kRecBytes : PfDim<128>::kRecBytes; }
+
+bool prefill_supported(int num_q_heads, int num_kv_heads, int head_dim, int page_size) {
+  if (num_q_heads <= 0 || num_kv_heads <= 0 || page_size != kPageSize) return false;
+  if (head_dim != 64 && head_dim != 128) return false;
+  if (num_q_heads % num_kv_heads != 0) return false;
+  const int g = num_q_heads / num_kv_heads;
+  return g >= 1 && g <= 8;
+}
+
+size_t prefill_workspace_bytes(int num_q_heads, int num_kv_heads, int head_dim, int32_t num_seqs, int32_t max_q_len,
+                               int num_sms) {
+  return PKV_STATUS_BYTES + pf_counter_bytes(num_seqs, max_q_len, pf_pairs(num_q_heads, num_kv_heads)) +
+         static_cast<size_t>(2) * num_sms * pf_rec_bytes(head_dim);
 }
 int prefill_max_seqs() { return kPfMaxSeqs; }
 
+template <int HD, bool kFixed>
+static int launch_prefill_hd(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                             const PrefillArgs& a, int num_seqs, long long items, int num_sms, cudaStream_t stream) {
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+  if (dev < 64 && !attr_set[dev]) {
+    if (cudaFuncSetAttribute(prefill_kernel<HD, kFixed>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(pf_smem_bytes<HD>(kPfMaxSeqs))) != cudaSuccess)
+      return PKV_ERR_CUDA;
+    attr_set[dev] = true;
+  }
+  // one CTA per SM fits (TMEM and shared memory); split mode uses the first num_sms CTAs as persistent
+  // workers, item mode one CTA per item
+  const unsigned grid = static_cast<unsigned>(items > num_sms ? items : num_sms);
+  return launch_pdl(prefill_kernel<HD, kFixed>, dim3(grid), dim3(kPfThreads), pf_smem_bytes<HD>(num_seqs), stream, qmap,
+                    kmap, vmap, a) == cudaSuccess
+             ? PKV_OK
+             : PKV_ERR_CUDA;
+}
+
 int launch_prefill(const void* q, const void* k_pages, const void* v_pages, const int32_t* block_table,
                    const int32_t* prefix_lens, const int32_t* cu_q_lens, int32_t num_seqs, int32_t total_q,
-                   void* out, float scale, int32_t max_pages, int32_t max_q_len, int32_t num_pages, void* workspace,
-                   cudaStream_t stream) {
+                   void* out, float scale, int num_q_heads, int num_kv_heads, int head_dim, int32_t max_pages,
+                   int32_t max_q_len, int32_t num_pages, void* workspace, cudaStream_t stream) {
   if (num_seqs == 0 || max_q_len == 0 || total_q == 0) return PKV_OK;
+  if (!prefill_supported(num_q_heads, num_kv_heads, head_dim, kPageSize)) return PKV_ERR_UNSUPPORTED;
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return PKV_ERR_CUDA;
+  const cuuint64_t hd = static_cast<cuuint64_t>(head_dim);
 
   CUtensorMap qmap, kmap, vmap;
   {
-    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(kQHeads),
-                                static_cast<cuuint64_t>(total_q)};
-    const cuuint64_t strides[2] = {kHeadDim * 2, static_cast<cuuint64_t>(kQHeads) * kHeadDim * 2};
+    const cuuint64_t dims[3] = {hd, static_cast<cuuint64_t>(num_q_heads), static_cast<cuuint64_t>(total_q)};
+    const cuuint64_t strides[2] = {hd * 2, static_cast<cuuint64_t>(num_q_heads) * hd * 2};
     const cuuint32_t box[3] = {64, 1, kPfRows};
     const cuuint32_t estr[3] = {1, 1, 1};
     if (enc(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, estr,
@@ -1120,9 +1179,8 @@ int launch_prefill(const void* q, const void* k_pages, const void* v_pages, cons
       return PKV_ERR_CUDA;
   }
   {
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim),
-                                static_cast<cuuint64_t>(num_pages) * kKVHeads * kPageSize};
-    const cuuint64_t strides[1] = {kHeadDim * 2};
+    const cuuint64_t dims[2] = {hd, static_cast<cuuint64_t>(num_pages) * num_kv_heads * kPageSize};
+    const cuuint64_t strides[1] = {hd * 2};
     const cuuint32_t box[2] = {64, kPageSize};
     const cuuint32_t estr[2] = {1, 1};
     if (enc(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(k_pages), dims, strides, box, estr,
@@ -1135,16 +1193,8 @@ int launch_prefill(const void* q, const void* k_pages, const void* v_pages, cons
       return PKV_ERR_CUDA;
   }
 
-  static bool attr_set[64] = {false};
-  int dev = 0;
+  int dev = 0, num_sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
-  if (dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(pf_smem_bytes(kPfMaxSeqs))) != cudaSuccess)
-      return PKV_ERR_CUDA;
-    attr_set[dev] = true;
-  }
-  int num_sms = 0;
   if (cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return PKV_ERR_CUDA;
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   PrefillArgs a;
@@ -1158,18 +1208,20 @@ int launch_prefill(const void* q, const void* k_pages, const void* v_pages, cons
   a.num_pages = num_pages;
   a.tmax = (max_q_len + kPfRows - 1) / kPfRows;
   a.workers = num_sms;
+  a.hq = num_q_heads;
+  a.hkv = num_kv_heads;
+  a.grp = num_q_heads / num_kv_heads;
+  a.npair = (a.grp + 1) / 2;
+  a.pairs = num_kv_heads * a.npair;
   a.scale_log2 = scale * kLog2e;
   a.status = reinterpret_cast<int*>(ws);
   a.counters = reinterpret_cast<int*>(ws + PKV_STATUS_BYTES);
-  a.records = ws + PKV_STATUS_BYTES + pf_counter_bytes(num_seqs, max_q_len);
-  // one CTA per SM fits (TMEM and shared memory); split mode uses the first num_sms CTAs as persistent
-  // workers, item mode one CTA per item
-  const long long items = static_cast<long long>(num_seqs) * kKVHeads * a.tmax;
-  const unsigned grid = static_cast<unsigned>(items > num_sms ? items : num_sms);
-  return launch_pdl(prefill_kernel, dim3(grid), dim3(kPfThreads), pf_smem_bytes(num_seqs), stream, qmap, kmap,
-                    vmap, a) == cudaSuccess
-             ? PKV_OK
-             : PKV_ERR_CUDA;
+  a.records = ws + PKV_STATUS_BYTES + pf_counter_bytes(num_seqs, max_q_len, a.pairs);
+  const long long items = static_cast<long long>(num_seqs) * a.pairs * a.tmax;
+  if (head_dim == 64) return launch_prefill_hd<64, false>(qmap, kmap, vmap, a, num_seqs, items, num_sms, stream);
+  if (num_q_heads == kQHeads && num_kv_heads == kKVHeads)  // the Qwen3 decoder: head counts fixed at compile time
+    return launch_prefill_hd<128, true>(qmap, kmap, vmap, a, num_seqs, items, num_sms, stream);
+  return launch_prefill_hd<128, false>(qmap, kmap, vmap, a, num_seqs, items, num_sms, stream);
 }
 
 }  // namespace pkv

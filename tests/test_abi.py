@@ -40,13 +40,15 @@ def test_host_argument_checks(lib):
     d = _desc()
     # NULL descriptor
     assert lib.pkv_append(None, None, None, 1, None, None, None, None, None, 0) == -1
-    # unsupported geometry: decode, append and the fused append + decode take page size 16, head_dim
-    # 64 or 128 and 1 to 8 query heads per KV head; prefill and the RoPE call only 16/8/128/16
+    # unsupported geometry: decode, append, the fused append + decode and prefill take page size 16,
+    # head_dim 64 or 128 and 1 to 8 query heads per KV head; the RoPE call only 16/8/128/16
     for bad in (_desc(head_dim=96), _desc(num_q_heads=36, num_kv_heads=4), _desc(num_q_heads=20),
                 _desc(page_size=32), _desc(num_q_heads=32, num_kv_heads=2)):
         assert lib.pkv_append(None, None, None, 1, None, None, ctypes.byref(bad), None, None, 0) == -3
         assert lib.pkv_decode_attn(None, None, None, None, None, None, 1.0, None, ctypes.byref(bad), 1, 1, None,
                                    0) == -3
+        assert lib.pkv_prefill_chunk_attn(None, None, None, None, None, None, 1, 1, None, 1.0, None,
+                                          ctypes.byref(bad), 1, 1, None, 0) == -3
     for other in (_desc(head_dim=64), _desc(num_q_heads=32, num_kv_heads=8), _desc(num_q_heads=8),
                   _desc(num_q_heads=40), _desc(num_q_heads=28, num_kv_heads=4), _desc(num_q_heads=24)):
         # served by the generic decode path: past the geometry check, stopped at the NULL pointers
@@ -59,7 +61,7 @@ def test_host_argument_checks(lib):
         assert lib.pkv_decode_append_rope_attn(None, None, None, None, None, None, None, 256, 1, None, 1.0, None,
                                                ctypes.byref(other), 1, 1, None, 0, 0) == -3
         assert lib.pkv_prefill_chunk_attn(None, None, None, None, None, None, 1, 1, None, 1.0, None,
-                                          ctypes.byref(other), 1, 1, None, 0) == -3
+                                          ctypes.byref(other), 1, 1, None, 0) == -1
     # sizes
     assert lib.pkv_append(None, None, None, -1, None, None, ctypes.byref(d), None, None, 0) == -2
     assert lib.pkv_decode_attn(None, None, None, None, None, None, 1.0, None, ctypes.byref(d), -1, 1, None, 0) == -2
@@ -82,6 +84,33 @@ def test_host_argument_checks(lib):
     assert lib.pkv_decode_workspace_bytes(None, 1, 1) == 0
     assert lib.pkv_decode_workspace_bytes(ctypes.byref(d), -1, 1) == 0
     assert lib.pkv_decode_workspace_bytes(ctypes.byref(d), 1, 0) == 0
+
+
+def test_noalloc_host_argument_checks(lib):
+    # pkv_decode_attn_noalloc rejects bad arguments before it looks up its device array
+    f = lib.pkv_decode_attn_noalloc
+    d = _desc()
+    dummy = ctypes.create_string_buffer(64)
+    p = (ctypes.addressof(dummy) + 15) // 16 * 16  # 16-byte aligned host address, never dereferenced
+    args = lambda batch=1, max_pages=1, desc=d, ptr=p, q=None: (q or ptr, ptr, ptr, ptr, ptr, ptr, 1.0, None,
+                                                                   None if desc is None else ctypes.byref(desc),
+                                                                   batch, max_pages)
+    assert f(*args(desc=None)) == -1
+    # only the tuned 16/8/128/16 geometry, also where pkv_decode_attn takes the generic kernel
+    for other in (_desc(num_q_heads=32, num_kv_heads=8), _desc(head_dim=64), _desc(num_q_heads=8)):
+        assert f(*args(desc=other)) == -3
+    assert f(*args(desc=_desc(num_pages=0))) == -2
+    assert f(*args(batch=-1)) == -2
+    assert f(*args(max_pages=0)) == -2
+    # more requests than the fixed array holds partial results for
+    assert f(*args(batch=257)) == -4
+    # a block table too large for the kernels' 32-bit indexing
+    assert f(*args(batch=256, max_pages=1 << 20)) == -2
+    # an empty batch is a no-op, without any device
+    assert f(*args(batch=0)) == 0
+    # missing and misaligned pointers
+    assert f(*args(ptr=None)) == -1
+    assert f(*args(q=p + 2)) == -8
 
 
 def test_no_cpu_fallback_without_the_library(monkeypatch, tmp_path):

@@ -45,3 +45,40 @@ def test_wait_that_never_completes_times_out_and_reports(cuda_device):
                          case.geom.scale)
     assert_close(bf16_to_f64(out), want, "after timeout")
     assert run.ws.status() == 0
+
+
+class _FakeLib:
+    """Stands in for libpkv on the CPU: a status word the test sets, and a record of re-inits."""
+
+    def __init__(self, status):
+        self.status = status
+        self.inits = []
+
+    def pkv_read_status(self, ws, stream):
+        return self.status
+
+    def pkv_workspace_init(self, ws, nbytes, stream):
+        self.inits.append((ws.value, nbytes))
+        self.status = 0
+        return 0
+
+    def pkv_status_string(self, code):
+        return b"fake"
+
+
+@pytest.mark.parametrize("code", [-6, -7])
+def test_workspace_is_zeroed_again_after_a_device_error(monkeypatch, code):
+    # the documented rule: after a call whose status word is not PKV_OK, the workspace is
+    # initialised again before its next use (stale counters or tagged records would otherwise
+    # be taken for the next call's own); Workspace.check does that before raising
+    fake = _FakeLib(code)
+    monkeypatch.setattr(_lib, "load", lambda: fake)
+    monkeypatch.setattr(pkv, "_stream", lambda s: ctypes.c_void_p(0))
+    ws = object.__new__(pkv.Workspace)
+    ws.tensor = torch.zeros(1024, dtype=torch.uint8)
+    with pytest.raises(pkv.PkvError) as e:
+        ws.check("decode")
+    assert e.value.code == code
+    assert fake.inits == [(ws.tensor.data_ptr(), 1024)]
+    ws.check("decode")  # clean now: no error, no further init
+    assert len(fake.inits) == 1

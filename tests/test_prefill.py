@@ -1,8 +1,13 @@
 """Chunked-prefill attention on the GPU (tcgen05 kernel) against the fp64 oracle.
 
-Small cases compare every output row; full-size chunks (4096 rows after 0,
-8192 or 32768 cached tokens) compare sampled rows (every 64th row, the last
-64 rows, all heads), which the oracle computes one by one. Bar as elsewhere:
+Small cases compare every output row. Full-size chunks (4096 rows after 0,
+8192 or 32768 cached tokens) compare sampled rows, all heads, which the oracle
+computes one by one: every 13th row (13 is coprime to the 128-row query tile,
+so every row offset of a tile is hit), the last 64 rows, and every row of the
+query tiles whose key range the split schedule divides between CTAs (there
+the partial records and their merge produce the rows). The mixed step of
+workload 4 (the chunk plus 15 decode requests in one pool, as one CUDA graph
+with two branches) is compared with the oracle too. Bar as elsewhere:
 max |diff| <= 1e-2, mean |diff| <= 1e-3, relative L2 <= 1e-2.
 """
 import numpy as np
@@ -72,29 +77,100 @@ def test_several_requests_in_one_call(cuda_device):
     _check(case, cuda_device, what="3 requests")
 
 
+SAMPLE_STRIDE = 13  # coprime to the 128-row query tile: the samples reach every row offset
+
+
 def _sample_rows(total):
-    rows = list(range(0, total, 64)) + list(range(max(0, total - 64), total))
+    rows = list(range(0, total, SAMPLE_STRIDE)) + list(range(max(0, total - 64), total))
     return sorted(set(rows))
+
+
+def split_cut_tiles(prefix_lens, q_lens, workers, item_cost=2, kv_heads=8, tile=128, item_mode_pct=75):
+    """(request, query tile) pairs whose key tiles the prefill kernel's split schedule divides
+    between CTAs; empty when its item schedule runs. A test-side model of the schedule's rule, used
+    only to choose which rows to compare: items are ordered by request, KV head, query tile; an item
+    costs item_cost units plus one per key tile; CTA c of G = min(workers, U) takes units
+    [c U / G, (c + 1) U / G); the item schedule runs when the largest item has at least
+    item_mode_pct % of a CTA's average key tiles."""
+    items = []
+    for n, (P, L) in enumerate(zip(prefix_lens, q_lens)):
+        T = -(-int(L) // tile)
+        for g in range(kv_heads):
+            for t in range(T):
+                items.append((n, t, -(-(int(P) + min(int(L), tile * (t + 1))) // tile)))
+    if not items:
+        return []
+    tiles_all = sum(nt for _, _, nt in items)
+    if 100 * max(nt for _, _, nt in items) * workers >= item_mode_pct * tiles_all:
+        return []
+    U = sum(item_cost + nt for _, _, nt in items)
+    G = min(workers, U)
+    cta_of = lambda f: ((f + 1) * G + U - 1) // U - 1
+    cut, f = set(), 0
+    for n, t, nt in items:
+        if cta_of(f + item_cost) != cta_of(f + item_cost + nt - 1):
+            cut.add((n, t))
+        f += item_cost + nt
+    return sorted(cut)
+
+
+def _workers(dev):
+    return torch.cuda.get_device_properties(dev).multi_processor_count
+
+
+def _cut_rows(case, dev, max_tiles):
+    """All rows of up to max_tiles query tiles (spread over the list) that the split schedule cuts."""
+    cut = split_cut_tiles(case.prefix_lens, case.q_lens, _workers(dev))
+    pick = cut[:: max(1, len(cut) // max_tiles)][:max_tiles] if cut else []
+    rows = set()
+    for n, t in pick:
+        lo = int(case.cu_q_lens[n]) + 128 * t
+        rows |= set(range(lo, min(lo + 128, int(case.cu_q_lens[n + 1]))))
+    return rows, len(cut)
 
 
 @pytest.mark.parametrize("prefix", [0, 8192, 32768])
 def test_full_chunk_sampled_rows(cuda_device, prefix):
     case = W.prefill_case(42, [prefix], [W.PREFILL_CHUNK], poison=True)
-    _check(case, cuda_device, rows=_sample_rows(W.PREFILL_CHUNK), what=f"chunk 4096 after {prefix}")
+    cut_rows, n_cut = _cut_rows(case, cuda_device, max_tiles=2)
+    if prefix > 0:
+        # long cached prefixes run the split schedule (equal shares of key tiles that cut items)
+        assert n_cut > 0 and len(cut_rows) == 256
+    rows = sorted(set(_sample_rows(W.PREFILL_CHUNK)) | cut_rows)
+    assert {r % 128 for r in rows} == set(range(128))
+    _check(case, cuda_device, rows=rows, what=f"chunk 4096 after {prefix}")
 
 
 def test_split_schedule_several_requests(cuda_device):
     # three requests of 1536 rows after 3000 cached tokens: the key tiles outnumber what
     # whole query tiles can balance over the SMs, so CTAs take equal shares that cut
     # through (request, head, query tile) items, some across request boundaries, and
-    # the split items are merged; sampled rows of every request
+    # the split items are merged; sampled rows of every request (every row offset of a
+    # query tile) and every row of three cut query tiles
     case = W.prefill_case(44, [3000, 3000, 3000], [1536, 1536, 1536], poison=True)
-    rows = sorted({r for n in range(3) for r in range(n * 1536, (n + 1) * 1536, 48)} |
-                  {n * 1536 + r for n in range(3) for r in range(1536 - 16, 1536)})
+    cut_rows, n_cut = _cut_rows(case, cuda_device, max_tiles=3)
+    assert n_cut > 0
+    rows = sorted({r for n in range(3) for r in range(n * 1536, (n + 1) * 1536, SAMPLE_STRIDE)} |
+                  {n * 1536 + r for n in range(3) for r in range(1536 - 16, 1536)} | cut_rows)
     run = _check(case, cuda_device, rows=rows, what="split schedule, 3 requests")
     # merges run in an order fixed by the item, whichever CTA completes it: same bits again
     again = PrefillOnDevice(case, cuda_device).run()
     assert torch.equal(run.out.view(torch.int16), again.view(torch.int16))
+
+
+def test_chunk_longer_than_max_q_len_is_reported(cuda_device):
+    # max_q_len = 100 sizes the call for one 128-row query tile; a 300-row chunk then has rows the
+    # call does not compute, and the status word says so (the first tile's rows are still right)
+    case = W.prefill_case(46, [50], [300], poison=True)
+    run = PrefillOnDevice(case, cuda_device)
+    run.max_q_len = 100
+    run.ws = pkv.Workspace(pkv.prefill_workspace_bytes(1, 100), cuda_device)
+    out = run.run()
+    assert run.ws.status() == pkv.ERR_CODES["PKV_ERR_OUT_OF_BOUNDS"]
+    kp, vp = run.oracle_pools()
+    want = oracle.prefill(case.q[0], kp, vp, case.block_table, case.prefix_lens, case.cu_q_lens, case.geom.scale,
+                          rows=range(128))
+    assert_close(bf16_to_f64(out[:128]), want, "first query tile of an over-long chunk")
 
 
 def test_causality_on_gpu(cuda_device):
@@ -167,3 +243,69 @@ def test_mixed_step_graph_with_parallel_branches_equals_eager(cuda_device):
     for key in ("out", "dout", "kp", "vp"):
         assert torch.equal(eager[key].view(torch.int16), graphed[key].view(torch.int16)), key
     assert pws.status() == 0 and dws.status() == 0
+
+
+def _mixed_graph(case, dev):
+    """Workload 4's step as one CUDA graph with two branches: the chunk's append and prefill on
+    the capturing stream, the decode requests' append and attention on a side stream (disjoint
+    slots, separate workspaces). Returns the graph and the device state it writes."""
+    s = dict(kp=case.k_pages[0].to(dev), vp=case.v_pages[0].to(dev),
+             out=torch.full_like(case.q[0], float("nan"), device=dev),
+             dout=torch.full_like(case.dec_q[0], float("nan"), device=dev))
+    q, kn, vn = case.q[0].to(dev), case.k_new[0].to(dev), case.v_new[0].to(dev)
+    dq, dk, dv = case.dec_q[0].to(dev), case.dec_k_new[0].to(dev), case.dec_v_new[0].to(dev)
+    slots, bt = i32(case.slot_mapping, dev), i32(case.block_table, dev)
+    prefix, cu = i32(case.prefix_lens, dev), i32(case.cu_q_lens, dev)
+    dslots, dbt, dlens = i32(case.dec_slot_mapping, dev), i32(case.dec_block_table, dev), i32(case.dec_seq_lens, dev)
+    max_q = int(case.q_lens.max())
+    pws = pkv.Workspace(pkv.prefill_workspace_bytes(len(case.prefix_lens), max_q), dev)
+    dws = pkv.Workspace(pkv.decode_workspace_bytes(len(case.dec_seq_lens), case.dec_block_table.shape[1]), dev)
+    side = torch.cuda.Stream()
+    scale = case.geom.scale
+
+    def step():
+        main = torch.cuda.current_stream()
+        side.wait_stream(main)
+        pkv.append(kn, vn, slots, s["kp"], s["vp"], pws)
+        pkv.prefill_chunk_attn(q, s["kp"], s["vp"], bt, prefix, cu, s["out"], scale, max_q, pws)
+        with torch.cuda.stream(side):
+            pkv.append(dk, dv, dslots, s["kp"], s["vp"], dws)
+            pkv.decode_attn(dq, s["kp"], s["vp"], dbt, dlens, s["dout"], scale, dws)
+        main.wait_stream(side)
+
+    g = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cap):
+        step()  # once outside the graph (the appends rewrite the same rows in every run)
+        cap.synchronize()
+        with torch.cuda.graph(g, stream=cap):
+            step()
+    torch.cuda.synchronize()
+    return g, s, pws, dws
+
+
+@pytest.mark.parametrize("prefix", [0, 32768])
+def test_mixed_step_graph_matches_oracle(cuda_device, prefix):
+    # workload 4 at full size: a 4096-row chunk after `prefix` cached tokens and 15 decode
+    # requests U{500..5000} in one pool, as the two-branch graph; pools bit-exact against the
+    # oracle's appends, sampled chunk rows (every row offset, the split schedule's cut tiles)
+    # and all 15 decode rows against the oracle
+    dev = cuda_device
+    ensure_built()
+    case = W.prefill_case(4, [prefix], [W.PREFILL_CHUNK], dec_seq_lens=W.mixed_decode_lens(4), poison=True)
+    g, s, pws, dws = _mixed_graph(case, dev)
+    for _ in range(2):  # a replay rewrites the same rows: the second sees the first's pools
+        g.replay()
+    torch.cuda.synchronize()
+    assert pws.status() == 0 and dws.status() == 0
+    kp, vp = oracle.append(case.k_new[0], case.v_new[0], case.slot_mapping, case.k_pages[0], case.v_pages[0])
+    kp, vp = oracle.append(case.dec_k_new[0], case.dec_v_new[0], case.dec_slot_mapping, kp, vp)
+    assert np.array_equal(bits(s["kp"]), kp) and np.array_equal(bits(s["vp"]), vp)
+    cut_rows, _ = _cut_rows(case, dev, max_tiles=2)
+    rows = sorted(set(_sample_rows(W.PREFILL_CHUNK)) | cut_rows)
+    want = oracle.prefill(case.q[0], kp, vp, case.block_table, case.prefix_lens, case.cu_q_lens, case.geom.scale,
+                          rows=rows)
+    assert_close(bf16_to_f64(s["out"])[np.asarray(rows)], want, f"mixed step: chunk after {prefix}")
+    want_d = oracle.decode(case.dec_q[0], kp, vp, case.dec_block_table, case.dec_seq_lens, case.geom.scale)
+    assert_close(bf16_to_f64(s["dout"]), want_d, f"mixed step: 15 decode requests (chunk after {prefix})")

@@ -4,10 +4,13 @@ loop that reserves memory once and must not allocate afterwards). Its split-KV
 scratch is a fixed array inside the library instead of a caller workspace.
 
 Checked here through the C ABI: two calls in a row give the same output as
-pkv_decode_attn (the entry point with a workspace) within the parity
-tolerance, on a batch whose contexts are split over many CTAs (so the scratch
-partials and counters are used) and on one long context. This file is named
-to be collected last.
+pkv_decode_attn (the entry point with a workspace). Both run the same kernel
+with the same grid and merge order, so the outputs are compared bit for bit,
+and the result is also checked against the fp64 oracle at the parity
+tolerance. The cases: a batch whose contexts are split over many CTAs (so the
+scratch partials and counters are used), one long context (the counted
+merge) and a ragged batch with padding rows. This file is named to be
+collected last.
 """
 import ctypes
 
@@ -15,6 +18,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import paged_kv_decode_gb300 as pkv
 from gpu_util import DecodeOnDevice
 from parity import assert_close, bf16_to_f64
@@ -30,12 +34,16 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(cuda_device, seq_len
     run = DecodeOnDevice(case, 0, cuda_device)
     ref = run.step().clone()
     torch.cuda.synchronize()
+    assert run.ws.status() == 0
+    want = oracle.decode(case.q[0], case.k_pages[0], case.v_pages[0], case.block_table, case.seq_lens,
+                         case.geom.scale)
     for _ in range(2):
         out = torch.full_like(run.q, float("nan"))
         pkv.decode_attn_noalloc(run.q, run.k_pages, run.v_pages, run.block_table, run.seq_lens, out,
                                 case.geom.scale)
         torch.cuda.synchronize()
-        assert_close(bf16_to_f64(out), bf16_to_f64(ref), "noalloc vs workspace entry point")
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), "noalloc differs from the workspace call"
+        assert_close(bf16_to_f64(out), want, "noalloc vs oracle")
 
 
 def test_noalloc_rejects_batch_beyond_its_scratch(cuda_device):
