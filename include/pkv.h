@@ -33,8 +33,9 @@
  * Supported geometry:
  *  - Every call: num_q_heads = 16, num_kv_heads = 8, head_dim = 128,
  *    page_size = 16 (the Qwen3 decoder; the tuned kernels).
- *  - pkv_append, pkv_decode_attn, pkv_decode_append_attn and
- *    pkv_prefill_chunk_attn also take page_size = 16, head_dim 64 or 128,
+ *  - pkv_append, pkv_decode_attn, pkv_decode_append_attn,
+ *    pkv_decode_append_rope_attn and pkv_prefill_chunk_attn also take
+ *    page_size = 16, head_dim 64 or 128,
  *    any num_kv_heads and num_q_heads = G * num_kv_heads with G from 1 to 8
  *    (other decoder backbones; decode runs a generic split-KV kernel, early
  *    prefetch included; prefill runs its tensor-core kernel on pairs of
@@ -254,7 +255,8 @@ int pkv_decode_append_attn(const void* q, const void* k_new, const void* v_new, 
  *
  *  rope_cos_sin: fp32 [rope_max_pos][head_dim], row p = cos(p w_i) for
  *                i < head_dim/2, then sin(p w_i) (w_i = theta^(-2i/head_dim));
- *                caller-owned device memory, 16-byte aligned, read only.
+ *                caller-owned device memory, 16-byte aligned, read only
+ *                (pkv_rope_table builds it).
  *                A position >= rope_max_pos is reported as
  *                PKV_ERR_OUT_OF_BOUNDS in the status word and clamped to the
  *                last row.
@@ -266,6 +268,27 @@ int pkv_decode_append_rope_attn(const void* q, const void* k_new, const void* v_
                                 int32_t rope_max_pos, void* out, float scale, pkv_stream_t stream,
                                 const pkv_cache_desc* desc, int32_t batch, int32_t max_pages_per_seq, void* workspace,
                                 size_t workspace_bytes, uint32_t flags);
+
+/*
+ * pkv_rope_table -- build the cos/sin table the RoPE decode call reads.
+ *
+ * Source: the decoder's rotary position embedding with theta 1e6
+ * ("Fun-ASR-Nano Native Runtime Design", section "Decoder And Prompt"), in the
+ * rotate-half form of Qwen3 decoders (the pages name RoPE and theta only).
+ *
+ * Writes table[p][i] = cos(p w_i) and table[p][head_dim/2 + i] = sin(p w_i)
+ * for p < max_pos, i < head_dim/2, w_i = theta^(-2i / head_dim); each angle
+ * and its cosine and sine are evaluated in double and rounded to float once.
+ *
+ *  table:     fp32 [max_pos][head_dim], caller-owned device memory, 16-byte
+ *             aligned, written on `stream`
+ *  max_pos:   >= 1 rows (positions 0 .. max_pos - 1)
+ *  head_dim:  even, 2 .. 1024 (the decode calls use 64 or 128)
+ *  theta:     > 0 (1e6 for the Qwen3 decoder)
+ * Returns PKV_ERR_BAD_SHAPE for other sizes, PKV_ERR_MISALIGNED for an
+ * unaligned table; nothing is written then.
+ */
+int pkv_rope_table(float* table, int32_t max_pos, int32_t head_dim, double theta, pkv_stream_t stream);
 
 /*
  * Workspace bytes pkv_prefill_chunk_attn needs: the status header, split

@@ -197,26 +197,28 @@ def decode_attn(q, k_pages, v_pages, block_table, seq_lens, out, scale: float, w
 EARLY_PREFETCH = 1  # PKV_DECODE_EARLY_PREFETCH
 
 
-def rope_cos_sin(theta: float, max_pos: int, head_dim: int = 128, device=None):
-    """cos/sin table for decode_append_rope_attn: fp32 [max_pos, head_dim], row p = cos(p w_i) for
-    i < head_dim/2, then sin(p w_i), w_i = theta ** (-2 i / head_dim); angles in float64, rounded
-    to float32 once. (RoPE theta 1e6 for the decoder on "Fun-ASR-Nano Native Runtime Design",
-    "Decoder And Prompt".)"""
+def rope_cos_sin(theta: float, max_pos: int, head_dim: int = 128, device=None, stream=None):
+    """cos/sin table for decode_append_rope_attn, built on the device by pkv_rope_table: fp32
+    [max_pos, head_dim], row p = cos(p w_i) for i < head_dim/2, then sin(p w_i), w_i = theta ** (-2 i /
+    head_dim), angles in double rounded to float once. (RoPE theta 1e6 for the decoder on "Fun-ASR-Nano
+    Native Runtime Design", "Decoder And Prompt".)"""
     import torch
 
-    half = head_dim // 2
-    w = torch.pow(torch.tensor(float(theta), dtype=torch.float64),
-                  -2.0 * torch.arange(half, dtype=torch.float64) / head_dim)
-    ang = torch.arange(int(max_pos), dtype=torch.float64)[:, None] * w[None, :]
-    table = torch.cat([torch.cos(ang), torch.sin(ang)], dim=1).to(torch.float32)
-    return table.to(device) if device is not None else table
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    if dev.type != "cuda":
+        raise ValueError("the table is built on a CUDA device (the library has no CPU path)")
+    table = torch.empty(int(max_pos), int(head_dim), dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        rc = _lib.load().pkv_rope_table(_ptr(table), int(max_pos), int(head_dim), float(theta), _stream(stream))
+    _check(rc, "pkv_rope_table")
+    return table
 
 
 def decode_append_rope_attn(q, k_new, v_new, k_pages, v_pages, block_table, seq_lens, cos_sin, out, scale: float,
                             workspace: Workspace, stream=None, early_prefetch: bool = False):
     """decode_append_attn with the rotary embedding of the new token: k_new and every q row are
-    rotated at position seq_lens[b] - 1 (pairs i, i + 64; cos_sin from rope_cos_sin) before the
-    append and the scores."""
+    rotated at position seq_lens[b] - 1 (pairs i, i + head_dim/2; cos_sin from rope_cos_sin) before
+    the append and the scores (any geometry decode_append_attn takes)."""
     import torch
 
     _need(cos_sin, torch.float32, "cos_sin", k_pages.device)

@@ -39,6 +39,7 @@ PROTOTYPES = {
                                               _vp, _sz, ctypes.c_uint32]),
     "pkv_decode_append_rope_attn": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _f32, _vp, _dp,
                                                    _i32, _i32, _vp, _sz, ctypes.c_uint32]),
+    "pkv_rope_table": (ctypes.c_int, [_vp, _i32, _i32, ctypes.c_double, _vp]),
     "pkv_prefill_workspace_bytes": (_sz, [_dp, _i32, _i32]),
     "pkv_prefill_chunk_attn": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _vp, _f32, _vp, _dp, _i32,
                                               _i32, _vp, _sz]),

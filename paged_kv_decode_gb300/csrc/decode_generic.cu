@@ -104,7 +104,42 @@ struct GenArgs {
   float* records;  // [batch][hkv][splits][G][D + 4]
   int early;       // copy pages before the grid dependency (the caller's promise: the predecessor writes
                    // neither the pools nor the block table nor the lengths)
+  const float* rope;  // fused append only, optional: cos/sin table [rope_max_pos][D] (rotary embedding)
+  int rope_max_pos;
 };
+
+// Rotary embedding of 8 dims of the new key row (16-byte chunk ch of D / 8): the rotate-half form,
+// dims i and i + D / 2 a pair rotated by the table row's angle for i, in fp32 as
+// y1 = fma(x1, c, -(x2 s)) and y2 = fma(x2, c, x1 s) with each product rounded first, then rounded
+// to bf16 (ties to even), the operation order the tuned kernel and the header state.
+template <int D>
+__device__ __forceinline__ uint4 rope_key_chunk(const __nv_bfloat16* krow, int ch, const float* cs) {
+  constexpr int kHalfChunks = D / 16;
+  const bool first = ch < kHalfChunks;  // this chunk holds x1 of its pairs, else x2
+  const int pch = first ? ch + kHalfChunks : ch - kHalfChunks;
+  const uint4 own = __ldg(reinterpret_cast<const uint4*>(krow) + ch);
+  const uint4 par = __ldg(reinterpret_cast<const uint4*>(krow) + pch);
+  const uint32_t ow[4] = {own.x, own.y, own.z, own.w}, pw[4] = {par.x, par.y, par.z, par.w};
+  const int i0 = 8 * (first ? ch : pch);  // pair index of the chunk's first dim
+  uint32_t res[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 xo = bf2_to_f2(ow[e]), xp = bf2_to_f2(pw[e]);
+    const int i = i0 + 2 * e;
+    const float c0 = __ldg(cs + i), c1 = __ldg(cs + i + 1);
+    const float s0 = __ldg(cs + D / 2 + i), s1 = __ldg(cs + D / 2 + i + 1);
+    float y0, y1;
+    if (first) {
+      y0 = __fmaf_rn(xo.x, c0, -__fmul_rn(xp.x, s0));
+      y1 = __fmaf_rn(xo.y, c1, -__fmul_rn(xp.y, s1));
+    } else {
+      y0 = __fmaf_rn(xo.x, c0, __fmul_rn(xp.x, s0));
+      y1 = __fmaf_rn(xo.y, c1, __fmul_rn(xp.y, s1));
+    }
+    res[e] = pack_bf16x2(y0, y1);
+  }
+  return make_uint4(res[0], res[1], res[2], res[3]);
+}
 
 // Log-sum-exp merge of the nrec records of one (request, KV head) into its bf16
 // output rows, by the whole CTA. rec_at(r): record r, rows [G][D + 4] of o[D],
@@ -273,6 +308,16 @@ __global__ void __launch_bounds__(kGenThreads) decode_generic_kernel(const __gri
   const int np = (sl + kPageSize - 1) / kPageSize;
   const int nsplit = (np + a.pps - 1) / a.pps;
   if (s >= nsplit) return;
+  // the table row of the new token's position (the RoPE call)
+  const float* cs = nullptr;
+  if (kFused && a.rope != nullptr) {
+    int pos = sl - 1;
+    if (pos >= a.rope_max_pos) {  // past the table: reported, clamped to its last row
+      if (tid == 0) set_status(a.status, PKV_ERR_OUT_OF_BOUNDS);
+      pos = a.rope_max_pos - 1;
+    }
+    cs = a.rope + static_cast<size_t>(pos) * D;
+  }
   const int p0 = s * a.pps;
   const int p1 = p0 + a.pps < np ? p0 + a.pps : np;
 
@@ -305,7 +350,9 @@ __global__ void __launch_bounds__(kGenThreads) decode_generic_kernel(const __gri
       if (lane < 2 * kRowChunks) {
         const bool is_v = lane >= kRowChunks;
         const int ch = is_v ? lane - kRowChunks : lane;
-        const uint4 x = __ldg(reinterpret_cast<const uint4*>((is_v ? a.v_new : a.k_new) + src) + ch);
+        const uint4 x = (!is_v && cs != nullptr)
+                            ? rope_key_chunk<D>(a.k_new + src, ch, cs)
+                            : __ldg(reinterpret_cast<const uint4*>((is_v ? a.v_new : a.k_new) + src) + ch);
         reinterpret_cast<uint4*>(const_cast<__nv_bfloat16*>(is_v ? a.v_pages : a.k_pages) + row)[ch] = x;
         fence_proxy_async_global();
       }
@@ -337,6 +384,25 @@ __global__ void __launch_bounds__(kGenThreads) decode_generic_kernel(const __gri
     for (int ks = 0; ks < S::kKS; ++ks) {
       qf[ks][0] = live ? __ldg(qrow + 8 * ks + c) : 0u;
       qf[ks][1] = live ? __ldg(qrow + 8 * ks + 4 + c) : 0u;
+    }
+    if (cs != nullptr) {
+      // the RoPE call: rotate the query rows at the new token's position in fp32 (pairs (d, d + D/2) sit
+      // in steps ks and ks + kKS/2 of the same lane), each product rounded first, then round to bf16 as
+      // the score product's operand
+#pragma unroll
+      for (int ks = 0; ks < S::kKS / 2; ++ks)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int d = 16 * ks + 8 * e + 2 * c;
+          const float2 cc = make_float2(__ldg(cs + d), __ldg(cs + d + 1));
+          const float2 sn = make_float2(__ldg(cs + D / 2 + d), __ldg(cs + D / 2 + d + 1));
+          const float2 lo = bf2_to_f2(qf[ks][e]), hi = bf2_to_f2(qf[ks + S::kKS / 2][e]);
+          const float2 t1 = __fmul2_rn(hi, sn), t2 = __fmul2_rn(lo, sn);
+          const float2 ylo = __ffma2_rn(lo, cc, make_float2(-t1.x, -t1.y));
+          const float2 yhi = __ffma2_rn(hi, cc, t2);
+          qf[ks][e] = pack_bf16x2(ylo.x, ylo.y);
+          qf[ks + S::kKS / 2][e] = pack_bf16x2(yhi.x, yhi.y);
+        }
     }
   }
   uint32_t koff[S::kKS], voff[S::kKS];
@@ -428,9 +494,9 @@ size_t gen_workspace(int batch, int hkv, int max_pages, int num_sms) {
 
 template <int G, int D>
 int gen_launch(const void* q, const void* k_new, const void* v_new, const void* k_pages, const void* v_pages,
-               const int32_t* block_table, const int32_t* seq_lens, void* out, float scale, int batch, int hkv,
-               int gq, int max_pages, int num_pages, void* workspace, int num_sms, cudaStream_t stream,
-               uint32_t flags) {
+               const int32_t* block_table, const int32_t* seq_lens, const float* rope, int rope_max_pos, void* out,
+               float scale, int batch, int hkv, int gq, int max_pages, int num_pages, void* workspace, int num_sms,
+               cudaStream_t stream, uint32_t flags) {
   int splits = 1, pps = 1;
   plan<G, D>(batch, hkv, max_pages, num_sms, splits, pps);
   const size_t smem = Lay<G, D>::smem_bytes(pps);
@@ -452,6 +518,8 @@ int gen_launch(const void* q, const void* k_new, const void* v_new, const void* 
   a.k_new = static_cast<const __nv_bfloat16*>(k_new);
   a.v_new = static_cast<const __nv_bfloat16*>(v_new);
   a.early = (flags & PKV_DECODE_EARLY_PREFETCH) ? 1 : 0;
+  a.rope = fused ? rope : nullptr;
+  a.rope_max_pos = rope_max_pos;
   a.k_pages = static_cast<const __nv_bfloat16*>(k_pages);
   a.v_pages = static_cast<const __nv_bfloat16*>(v_pages);
   a.block_table = block_table;
@@ -555,16 +623,17 @@ size_t decode_generic_workspace_bytes(int num_q_heads, int num_kv_heads, int hea
 }
 
 int launch_decode_generic(const void* q, const void* k_new, const void* v_new, const void* k_pages,
-                          const void* v_pages, const int32_t* block_table, const int32_t* seq_lens, void* out,
-                          float scale, int num_q_heads, int num_kv_heads, int head_dim, int32_t batch,
-                          int32_t max_pages, int32_t num_pages, void* workspace, int num_sms, cudaStream_t stream,
-                          uint32_t flags) {
+                          const void* v_pages, const int32_t* block_table, const int32_t* seq_lens, const float* rope,
+                          int32_t rope_max_pos, void* out, float scale, int num_q_heads, int num_kv_heads,
+                          int head_dim, int32_t batch, int32_t max_pages, int32_t num_pages, void* workspace,
+                          int num_sms, cudaStream_t stream, uint32_t flags) {
   if (batch == 0) return PKV_OK;
+  if (rope != nullptr && k_new == nullptr) return PKV_ERR_NULL_ARG;
   const int gq = num_q_heads / num_kv_heads;
   const int group = padded_group(gq);
 #define PKV_GEN_RUN(G, D)                                                                                    \
-  gen_launch<G, D>(q, k_new, v_new, k_pages, v_pages, block_table, seq_lens, out, scale, batch, num_kv_heads, \
-                   gq, max_pages, num_pages, workspace, num_sms, stream, flags)
+  gen_launch<G, D>(q, k_new, v_new, k_pages, v_pages, block_table, seq_lens, rope, rope_max_pos, out, scale,  \
+                   batch, num_kv_heads, gq, max_pages, num_pages, workspace, num_sms, stream, flags)
   PKV_GEN_DISPATCH(PKV_GEN_RUN)
 #undef PKV_GEN_RUN
   return PKV_ERR_UNSUPPORTED;

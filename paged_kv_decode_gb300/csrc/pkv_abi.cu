@@ -103,9 +103,8 @@ const char* pkv_status_string(int status) {
     case PKV_ERR_NULL_ARG: return "a required pointer is NULL";
     case PKV_ERR_BAD_SHAPE: return "bad or inconsistent size";
     case PKV_ERR_UNSUPPORTED:
-      return "unsupported geometry or device (sm_103; decode, fused append + decode, append and prefill: "
-             "page 16, head_dim 64/128, 1 to 8 query heads per KV head; the RoPE call and the no-alloc call: "
-             "16/8/128/16)";
+      return "unsupported geometry or device (sm_103; decode, the fused calls, append and prefill: page 16, "
+             "head_dim 64/128, 1 to 8 query heads per KV head; the no-alloc call: 16/8/128/16)";
     case PKV_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
     case PKV_ERR_CUDA: return "CUDA runtime or launch error";
     case PKV_ERR_DEVICE_TIMEOUT: return "a device-side wait ran out of time";
@@ -171,9 +170,10 @@ int pkv_decode_attn(const void* q, const void* k_pages, const void* v_pages, con
   if (rc != PKV_OK) return rc;
   if (workspace_bytes < decode_ws(desc, generic, batch, max_pages_per_seq, sms)) return PKV_ERR_WORKSPACE_TOO_SMALL;
   if (generic)
-    return pkv::launch_decode_generic(q, nullptr, nullptr, k_pages, v_pages, block_table, seq_lens, out, scale,
-                                      desc->num_q_heads, desc->num_kv_heads, desc->head_dim, batch, max_pages_per_seq,
-                                      desc->num_pages, workspace, sms, reinterpret_cast<cudaStream_t>(stream), 0u);
+    return pkv::launch_decode_generic(q, nullptr, nullptr, k_pages, v_pages, block_table, seq_lens, nullptr, 0, out,
+                                      scale, desc->num_q_heads, desc->num_kv_heads, desc->head_dim, batch,
+                                      max_pages_per_seq, desc->num_pages, workspace, sms,
+                                      reinterpret_cast<cudaStream_t>(stream), 0u);
   return pkv::launch_decode(q, nullptr, nullptr, k_pages, v_pages, block_table, seq_lens, nullptr, 0, out, scale, batch,
                             max_pages_per_seq, desc->num_pages, workspace, sms, reinterpret_cast<cudaStream_t>(stream),
                             0u);
@@ -187,7 +187,6 @@ static int decode_append(const void* q, const void* k_new, const void* v_new, vo
   bool generic = false;
   int rc = check_desc_decode(desc, &generic);
   if (rc != PKV_OK) return rc;
-  if (generic && rope_cos_sin != nullptr) return PKV_ERR_UNSUPPORTED;  // the RoPE call: 16/8/128 only
   if (batch < 0 || max_pages_per_seq < 1) return PKV_ERR_BAD_SHAPE;
   if (batch > pkv::decode_max_batch()) return PKV_ERR_UNSUPPORTED;
   if (!table_fits(batch, max_pages_per_seq)) return PKV_ERR_BAD_SHAPE;
@@ -203,9 +202,10 @@ static int decode_append(const void* q, const void* k_new, const void* v_new, vo
   if (workspace_bytes < decode_ws(desc, generic, batch, max_pages_per_seq, sms)) return PKV_ERR_WORKSPACE_TOO_SMALL;
   if ((flags & ~static_cast<uint32_t>(PKV_DECODE_EARLY_PREFETCH)) != 0) return PKV_ERR_UNSUPPORTED;
   if (generic)
-    return pkv::launch_decode_generic(q, k_new, v_new, k_pages, v_pages, block_table, seq_lens, out, scale,
-                                      desc->num_q_heads, desc->num_kv_heads, desc->head_dim, batch, max_pages_per_seq,
-                                      desc->num_pages, workspace, sms, reinterpret_cast<cudaStream_t>(stream), flags);
+    return pkv::launch_decode_generic(q, k_new, v_new, k_pages, v_pages, block_table, seq_lens, rope_cos_sin,
+                                      rope_max_pos, out, scale, desc->num_q_heads, desc->num_kv_heads, desc->head_dim,
+                                      batch, max_pages_per_seq, desc->num_pages, workspace, sms,
+                                      reinterpret_cast<cudaStream_t>(stream), flags);
   return pkv::launch_decode(q, k_new, v_new, k_pages, v_pages, block_table, seq_lens, rope_cos_sin, rope_max_pos, out,
                             scale, batch, max_pages_per_seq, desc->num_pages, workspace, sms,
                             reinterpret_cast<cudaStream_t>(stream), flags);
@@ -274,6 +274,17 @@ int pkv_prefill_chunk_attn(const void* q, const void* k_pages, const void* v_pag
   return pkv::launch_prefill(q, k_pages, v_pages, block_table, prefix_lens, cu_q_lens, num_seqs, total_q, out, scale,
                              desc->num_q_heads, desc->num_kv_heads, desc->head_dim, max_pages_per_seq, max_q_len,
                              desc->num_pages, workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int pkv_rope_table(float* table, int32_t max_pos, int32_t head_dim, double theta, pkv_stream_t stream) {
+  if (table == nullptr) return PKV_ERR_NULL_ARG;
+  if (max_pos < 1 || head_dim < 2 || head_dim > 1024 || (head_dim % 2) != 0 || !(theta > 0.0))
+    return PKV_ERR_BAD_SHAPE;
+  if (!aligned16(table)) return PKV_ERR_MISALIGNED;
+  int sms = 0;
+  const int rc = current_device(&sms);
+  if (rc != PKV_OK) return rc;
+  return pkv::launch_rope_table(table, max_pos, head_dim, theta, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int pkv_selftest_wait_timeout(void* workspace, size_t workspace_bytes, int64_t limit_cycles, pkv_stream_t stream) {

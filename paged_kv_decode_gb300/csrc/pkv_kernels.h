@@ -28,13 +28,17 @@ int decode_max_batch();
 bool decode_generic_supported(int num_q_heads, int num_kv_heads, int head_dim, int page_size);
 size_t decode_generic_workspace_bytes(int num_q_heads, int num_kv_heads, int head_dim, int32_t batch,
                                       int32_t max_pages, int num_sms);
-// k_new / v_new: the fused append's new rows (both nullptr: decode alone); flags: 0 or
-// PKV_DECODE_EARLY_PREFETCH.
+// k_new / v_new: the fused append's new rows (both nullptr: decode alone); rope (nullable, needs
+// k_new): cos/sin table [rope_max_pos][head_dim]; flags: 0 or PKV_DECODE_EARLY_PREFETCH.
 int launch_decode_generic(const void* q, const void* k_new, const void* v_new, const void* k_pages,
-                          const void* v_pages, const int32_t* block_table, const int32_t* seq_lens, void* out,
-                          float scale, int num_q_heads, int num_kv_heads, int head_dim, int32_t batch,
-                          int32_t max_pages, int32_t num_pages, void* workspace, int num_sms, cudaStream_t stream,
-                          uint32_t flags);
+                          const void* v_pages, const int32_t* block_table, const int32_t* seq_lens, const float* rope,
+                          int32_t rope_max_pos, void* out, float scale, int num_q_heads, int num_kv_heads,
+                          int head_dim, int32_t batch, int32_t max_pages, int32_t num_pages, void* workspace,
+                          int num_sms, cudaStream_t stream, uint32_t flags);
+
+// Rotary-embedding table (rope.cu): fp32 [max_pos][head_dim], row p = cos(p w_i) for i < head_dim / 2,
+// then sin(p w_i), w_i = theta^(-2 i / head_dim), angles in double rounded to float once.
+int launch_rope_table(float* table, int32_t max_pos, int32_t head_dim, double theta, cudaStream_t stream);
 
 // Chunked prefill (prefill.cu): page size 16, head_dim 64 or 128, 1 to 8 query heads per KV head.
 bool prefill_supported(int num_q_heads, int num_kv_heads, int head_dim, int page_size);

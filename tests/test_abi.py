@@ -57,9 +57,9 @@ def test_host_argument_checks(lib):
         assert lib.pkv_append(None, None, None, 1, None, None, ctypes.byref(other), None, None, 0) == -1
         assert lib.pkv_decode_append_attn(None, None, None, None, None, None, None, None, 1.0, None,
                                           ctypes.byref(other), 1, 1, None, 0, 0) == -1
-        # (a table address the host never reads: the geometry check comes first)
+        # (a table address the host never reads: past the geometry check, stopped at the NULL pointers)
         assert lib.pkv_decode_append_rope_attn(None, None, None, None, None, None, None, 256, 1, None, 1.0, None,
-                                               ctypes.byref(other), 1, 1, None, 0, 0) == -3
+                                               ctypes.byref(other), 1, 1, None, 0, 0) == -1
         assert lib.pkv_prefill_chunk_attn(None, None, None, None, None, None, 1, 1, None, 1.0, None,
                                           ctypes.byref(other), 1, 1, None, 0) == -1
     # sizes
@@ -84,6 +84,20 @@ def test_host_argument_checks(lib):
     assert lib.pkv_decode_workspace_bytes(None, 1, 1) == 0
     assert lib.pkv_decode_workspace_bytes(ctypes.byref(d), -1, 1) == 0
     assert lib.pkv_decode_workspace_bytes(ctypes.byref(d), 1, 0) == 0
+
+
+def test_rope_table_host_argument_checks(lib):
+    # pkv_rope_table checks its arguments before it looks at any device
+    buf = ctypes.create_string_buffer(64)
+    p = (ctypes.addressof(buf) + 15) // 16 * 16  # never written: every call below is rejected
+    f = lib.pkv_rope_table
+    assert f(None, 8, 128, 1e6, None) == -1
+    assert f(p, 0, 128, 1e6, None) == -2
+    assert f(p, 8, 127, 1e6, None) == -2
+    assert f(p, 8, 2048, 1e6, None) == -2
+    assert f(p, 8, 128, 0.0, None) == -2
+    assert f(p, 8, 128, float("nan"), None) == -2
+    assert f(p + 4, 8, 128, 1e6, None) == -8
 
 
 def test_noalloc_host_argument_checks(lib):

@@ -349,6 +349,18 @@ def test_fused_rope_append_decode_matches_oracle(cuda_device, cfg):
     assert run.ws.status() == 0
 
 
+@pytest.mark.parametrize("head_dim", [128, 64])
+def test_library_rope_table_matches_the_oracle_table(cuda_device, head_dim):
+    # pkv_rope_table (the device kernel, double angles rounded to float) and the oracle's C table
+    # follow the same definition independently: within one float ulp, nearly all equal
+    a = pkv.rope_cos_sin(ROPE_THETA, 50000, head_dim, device=cuda_device).cpu().numpy()
+    b = oracle.rope_cache(ROPE_THETA, head_dim, 50000)
+    assert a.shape == b.shape == (50000, head_dim)
+    ulp = np.spacing(np.abs(b).astype(np.float32))
+    assert (np.abs(a.astype(np.float64) - b.astype(np.float64)) <= ulp).all()
+    assert (a == b).mean() > 0.999
+
+
 def test_fused_rope_position_beyond_table_is_reported(cuda_device):
     case = W.decode_case(20, [300, 40], pending_append=True, poison=False)
     cs = oracle.rope_cache(ROPE_THETA, case.geom.head_dim, 100)  # 300 - 1 is past the last row

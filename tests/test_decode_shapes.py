@@ -16,7 +16,7 @@ import torch
 import oracle
 import paged_kv_decode_gb300 as pkv
 from gpu_util import DecodeOnDevice, bits, i32
-from parity import assert_close, bf16_to_f64
+from parity import MEAN_ABS, REL_L2, assert_close, bf16_to_f64, stats
 from paged_kv_decode_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -199,11 +199,43 @@ def test_fused_layer_chain_in_a_graph(cuda_device, shape, early):
         assert r.ws.status() == 0
 
 
-def test_rope_call_rejects_other_geometries(cuda_device):
-    geom = SHAPES["g4_d128_32q8kv"]
-    case = W.decode_case(27, [100], geom=geom, pending_append=True, poison=False)
+@pytest.mark.parametrize("shape", sorted(SHAPES))
+def test_rope_call_matches_oracle(cuda_device, shape):
+    # the fused append + decode with the rotary embedding of the new token (theta 1e6, the table from
+    # the oracle): rotated key rows bit-exact, outputs against decode over the double-rotated queries
+    geom = SHAPES[shape]
+    lens = [1, 0, 17, 300, 33, 2000, 16]
+    case = W.decode_case(27, lens, geom=geom, pending_append=True, poison=True)
+    cs = oracle.rope_cache(1e6, geom.head_dim, int(max(lens)) + 1)
     run = DecodeOnDevice(case, 0, cuda_device)
-    cos_sin = pkv.rope_cos_sin(1e6, 128, device=cuda_device)
-    with pytest.raises(pkv.PkvError, match="UNSUPPORTED"):
-        pkv.decode_append_rope_attn(run.q, run.k_new, run.v_new, run.k_pages, run.v_pages, run.block_table,
-                                    run.seq_lens, cos_sin, run.out, geom.scale, run.ws)
+    pkv.decode_append_rope_attn(run.q, run.k_new, run.v_new, run.k_pages, run.v_pages, run.block_table,
+                                run.seq_lens, torch.from_numpy(cs).to(cuda_device), run.out, geom.scale, run.ws,
+                                early_prefetch=True)
+    torch.cuda.synchronize()
+    assert run.ws.status() == 0
+    pos = np.asarray(case.seq_lens, dtype=np.int64) - 1  # -1 for the empty request: nothing appended
+    k_rot = oracle.rope_bf16(case.k_new[0], pos, cs)
+    want_k, want_v = oracle.append(k_rot, case.v_new[0], case.slot_mapping, case.k_pages[0], case.v_pages[0])
+    assert np.array_equal(bits(run.k_pages), want_k) and np.array_equal(bits(run.v_pages), want_v)
+    # The call rotates each query row in fp32 and rounds it to bf16, the score product's operand (the
+    # header's definition). Element by element the oracle gets the query rotated by its bf16 form
+    # (rope_bf16: the same formula and rounding decision, pinned against the double rotation); against
+    # the double rotation itself the mean and relative-L2 bars hold as well.
+    got = bf16_to_f64(run.out)
+    want = oracle.decode(oracle.rope_bf16(case.q[0], pos, cs), want_k, want_v, case.block_table, case.seq_lens,
+                         geom.scale)
+    assert_close(got, want, f"{shape} rope")
+    exact = stats(got, oracle.decode(oracle.rope_f64(case.q[0], pos, cs), want_k, want_v, case.block_table,
+                                     case.seq_lens, geom.scale))
+    assert exact["mean_abs"] <= MEAN_ABS and exact["rel_l2"] <= REL_L2, exact
+
+
+def test_rope_position_beyond_table_is_reported(cuda_device):
+    geom = SHAPES["g4_d64_16q4kv"]
+    case = W.decode_case(28, [300, 40], geom=geom, pending_append=True, poison=False)
+    cs = oracle.rope_cache(1e6, geom.head_dim, 100)  # 300 - 1 is past the last row
+    run = DecodeOnDevice(case, 0, cuda_device)
+    pkv.decode_append_rope_attn(run.q, run.k_new, run.v_new, run.k_pages, run.v_pages, run.block_table,
+                                run.seq_lens, torch.from_numpy(cs).to(cuda_device), run.out, geom.scale, run.ws)
+    torch.cuda.synchronize()
+    assert run.ws.status() == pkv.ERR_CODES["PKV_ERR_OUT_OF_BOUNDS"]
