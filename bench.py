@@ -337,6 +337,8 @@ class PrefillStep:
         self.ws = pkv.Workspace(
             pkv.decode_workspace_bytes(len(c.dec_seq_lens), c.dec_block_table.shape[1], c.num_pages), device)
         self.pws = pkv.Workspace(pkv.prefill_workspace_bytes(1, W.PREFILL_CHUNK, c.num_pages), device)
+        self.mws = pkv.Workspace(pkv.mixed_workspace_bytes(1, W.PREFILL_CHUNK, len(c.dec_seq_lens),
+                                                           c.dec_block_table.shape[1], c.num_pages), device)
         self.scale = c.geom.scale
         P, L = int(prefix), W.PREFILL_CHUNK
         self.pairs = L * P + L * (L + 1) // 2
@@ -370,18 +372,27 @@ class PrefillStep:
                             self.ws)
         main.wait_stream(self.side)
 
-    def capture_mixed(self):
-        """One CUDA graph of the mixed step (two branches)."""
+    def mixed_one_launch(self):
+        """The mixed step with both attentions in one launch (pkv_mixed_step_attn) after the two appends."""
+        pkv = self.pkv
+        pkv.append(self.k_new, self.v_new, self.slots, self.k_pages, self.v_pages, self.mws)
+        pkv.append(self.dk, self.dv, self.dslots, self.k_pages, self.v_pages, self.mws)
+        pkv.mixed_step_attn(self.q, self.k_pages, self.v_pages, self.bt, self.prefix, self.cu, self.out,
+                            self.case.q_lens.max(), self.dq, self.dbt, self.dlens, self.dout, self.scale, self.mws)
+
+    def capture_mixed(self, body=None):
+        """One CUDA graph of the mixed step (default: two branches)."""
         torch = self.torch
+        body = body or self.mixed_branches
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(s):
-            self.mixed_branches()
+            body()
         torch.cuda.current_stream().wait_stream(s)
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            self.mixed_branches()
+            body()
         torch.cuda.synchronize()
         return g
 
@@ -504,13 +515,17 @@ def measure_prefill(device, bf16_peak, reps=10):
         mixed_ms = time_launches(torch, ps.mixed, reps)
         g = ps.capture_mixed()
         graph_ms = time_launches(torch, g.replay, reps)
+        g1 = ps.capture_mixed(ps.mixed_one_launch)
+        one_ms = time_launches(torch, g1.replay, reps)
         tf = ps.flops / (ms * 1e-3) / 1e12
         res[f"prefix_{prefix}"] = {"chunk": 4096, "prefill_us": ms * 1e3, "tflops": tf,
                                    "frac_of_measured_bf16": tf / bf16_peak, "gflop": ps.flops / 1e9,
                                    "mixed_step_us": mixed_ms * 1e3,
                                    # the same step as one CUDA graph, decode requests on a parallel branch
-                                   "mixed_step_graph_us": graph_ms * 1e3}
-        del g
+                                   "mixed_step_graph_us": graph_ms * 1e3,
+                                   # the appends and one pkv_mixed_step_attn launch, as one CUDA graph
+                                   "mixed_step_one_launch_us": one_ms * 1e3}
+        del g, g1
         del ps
         torch.cuda.empty_cache()
     return res
@@ -907,7 +922,8 @@ def main():
         cp = extra["chunked_prefill"]
         summary["prefill_4096"] = {f"P{P}": {"tflops": cp[f"prefix_{P}"]["tflops"],
                                              "frac_measured": cp[f"prefix_{P}"]["frac_of_measured_bf16"],
-                                             "mixed_graph_us": cp[f"prefix_{P}"]["mixed_step_graph_us"]}
+                                             "mixed_graph_us": cp[f"prefix_{P}"]["mixed_step_graph_us"],
+                                             "mixed_one_launch_us": cp[f"prefix_{P}"]["mixed_step_one_launch_us"]}
                                    for P in (0, 8192, 32768)}
     line["summary"] = _rounded(summary)
     print(json.dumps(line), flush=True)

@@ -337,6 +337,63 @@ int pkv_prefill_chunk_attn(const void* q, const void* k_pages, const void* v_pag
                            int32_t max_pages_per_seq, int32_t max_q_len, void* workspace, size_t workspace_bytes);
 
 /*
+ * Workspace bytes pkv_mixed_step_attn needs: the prefill workspace of the
+ * chunk part (see pkv_prefill_workspace_bytes), then one counter per (decode
+ * request, KV head) and, where a decode context spans more than 64 pages,
+ * partial records of its 64-page chunks (1056 bytes each). Returns 0 for
+ * unsupported arguments.
+ */
+size_t pkv_mixed_workspace_bytes(const pkv_cache_desc* desc, int32_t num_seqs, int32_t max_q_len, int32_t dec_batch,
+                                 int32_t dec_max_pages_per_seq);
+
+/*
+ * pkv_mixed_step_attn -- one scheduler step that interleaves chunked prefill
+ * with decode: the attention of prefill chunks and of decode requests over
+ * the same paged cache, in one launch.
+ *
+ * Source: a long prompt is prefilled in 4096-token chunks, one per scheduler
+ * step, between other requests' decode steps ("Optimizing ASR for 90-minute
+ * multi-speaker audio", section "Chunked prefill for long audio"); running
+ * the chunk and the decode batch as one kernel is the step the same page's
+ * section "后续计划" (future work) leaves open with CUDA-graph capture of
+ * chunked prefill.
+ *
+ * Computes exactly what pkv_prefill_chunk_attn computes for the chunk
+ * arguments (q .. max_q_len) and what pkv_decode_attn computes for the decode
+ * arguments (dec_*), both over k_pages / v_pages; results are within the same
+ * tolerance as those calls but not bit-identical to them (the work is split
+ * differently). All K/V rows, the chunks' and the decode tokens', must already
+ * be in the pools (pkv_append first). The decode requests run in CTAs of their
+ * own, one per chunk of up to 64 pages of a (request, KV head), that the
+ * hardware starts on the SMs the chunk leaves free (the tail of a short chunk;
+ * for a long cached prefix the chunk's persistent schedule keeps a few SMs for
+ * them, in proportion to their pages); chunks of one context are merged by
+ * log-sum-exp.
+ *
+ *  chunk arguments: as for pkv_prefill_chunk_attn; num_seqs = 0 (or total_q =
+ *                   0, max_q_len = 0) means no chunk, and q, out, block_table,
+ *                   prefix_lens and cu_q_lens may then be NULL
+ *  dec_q, dec_out:  bf16 [dec_batch][16][128], 16-byte aligned
+ *  dec_block_table: int32 [dec_batch][dec_max_pages_per_seq]
+ *  dec_seq_lens:    int32 [dec_batch]; 0 gives an all-zero output row; larger
+ *                   than dec_max_pages_per_seq * 16 is clamped and set
+ *                   PKV_ERR_OUT_OF_BOUNDS
+ *  dec_batch:       0 .. 1024 (0: the call is pkv_prefill_chunk_attn)
+ *  workspace:       >= pkv_mixed_workspace_bytes(desc, num_seqs, max_q_len,
+ *                   dec_batch, dec_max_pages_per_seq), zeroed once by
+ *                   pkv_workspace_init (the call leaves its counters at zero);
+ *                   serves mixed-step calls only
+ * Geometry: 16 query / 8 KV heads, head_dim 128, page 16 (PKV_ERR_UNSUPPORTED
+ * otherwise).
+ */
+int pkv_mixed_step_attn(const void* q, const void* k_pages, const void* v_pages, const int32_t* block_table,
+                        const int32_t* prefix_lens, const int32_t* cu_q_lens, int32_t num_seqs, int32_t total_q,
+                        void* out, int32_t max_pages_per_seq, int32_t max_q_len, const void* dec_q,
+                        const int32_t* dec_block_table, const int32_t* dec_seq_lens, void* dec_out, int32_t dec_batch,
+                        int32_t dec_max_pages_per_seq, float scale, pkv_stream_t stream, const pkv_cache_desc* desc,
+                        void* workspace, size_t workspace_bytes);
+
+/*
  * pkv_decode_attn_noalloc -- pkv_decode_attn without a caller-provided workspace.
  *
  * The source pages have no counterpart to this call: it exists for callers

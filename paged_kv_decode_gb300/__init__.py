@@ -36,7 +36,7 @@ ERR_CODES = {name: code for code, name in ERRORS.items()}
 __all__ = [
     "PkvError", "desc", "Workspace", "append", "decode_attn", "prefill_chunk_attn",
     "decode_workspace_bytes", "prefill_workspace_bytes", "workspace_init", "read_status", "status_string",
-    "decode_attn_noalloc", "decode_append_attn",
+    "decode_attn_noalloc", "decode_append_attn", "mixed_step_attn", "mixed_workspace_bytes", "rope_cos_sin",
 ]
 
 
@@ -298,6 +298,53 @@ def prefill_chunk_attn(q, k_pages, v_pages, block_table, prefix_lens, cu_q_lens,
                                             float(scale), _stream(stream), ctypes.byref(d), block_table.shape[1],
                                             int(max_q_len), _ptr(ws), ws.numel())
     _check(rc, "pkv_prefill_chunk_attn")
+
+
+def mixed_workspace_bytes(num_seqs: int, max_q_len: int, dec_batch: int, dec_max_pages: int,
+                          num_pages: int = 1) -> int:
+    """Workspace bytes of a mixed-step call (16/8/128)."""
+    d = desc(num_pages)
+    return int(_lib.load().pkv_mixed_workspace_bytes(ctypes.byref(d), int(num_seqs), int(max_q_len), int(dec_batch),
+                                                     int(dec_max_pages)))
+
+
+def mixed_step_attn(q, k_pages, v_pages, block_table, prefix_lens, cu_q_lens, out, max_q_len: int, dec_q,
+                    dec_block_table, dec_seq_lens, dec_out, scale: float, workspace: Workspace, stream=None):
+    """One scheduler step of chunked prefill interleaved with decode, in one launch (16/8/128): out as
+    prefill_chunk_attn gives it for the chunks (q, block_table, prefix_lens, cu_q_lens; may be empty) and
+    dec_out as decode_attn gives it for the decode requests (dec_q, dec_block_table, dec_seq_lens), over
+    the same pools. The workspace is sized by mixed_workspace_bytes."""
+    import torch
+
+    _need(k_pages, torch.bfloat16, "k_pages")
+    dev = k_pages.device
+    _need(v_pages, torch.bfloat16, "v_pages", dev)
+    _need(dec_q, torch.bfloat16, "dec_q", dev)
+    _need(dec_out, torch.bfloat16, "dec_out", dev)
+    _need(dec_block_table, torch.int32, "dec_block_table", dev)
+    _need(dec_seq_lens, torch.int32, "dec_seq_lens", dev)
+    B = dec_q.shape[0]
+    if dec_out.shape != dec_q.shape or dec_block_table.dim() != 2 or dec_block_table.shape[0] != B \
+            or dec_seq_lens.numel() != B:
+        raise ValueError("shape mismatch (decode part)")
+    S = 0 if prefix_lens is None else prefix_lens.numel()
+    if S:
+        _need(q, torch.bfloat16, "q", dev)
+        _need(out, torch.bfloat16, "out", dev)
+        _need(block_table, torch.int32, "block_table", dev)
+        _need(prefix_lens, torch.int32, "prefix_lens", dev)
+        _need(cu_q_lens, torch.int32, "cu_q_lens", dev)
+        if cu_q_lens.numel() != S + 1 or block_table.shape[0] != S or out.shape != q.shape:
+            raise ValueError("shape mismatch (chunk part)")
+    d = _desc_of(k_pages, dec_q.shape[1])
+    ws = workspace.tensor
+    rc = _lib.load().pkv_mixed_step_attn(
+        _ptr(q) if S else None, _ptr(k_pages), _ptr(v_pages), _ptr(block_table) if S else None,
+        _ptr(prefix_lens) if S else None, _ptr(cu_q_lens) if S else None, S, q.shape[0] if S else 0,
+        _ptr(out) if S else None, block_table.shape[1] if S else 1, int(max_q_len) if S else 0, _ptr(dec_q),
+        _ptr(dec_block_table), _ptr(dec_seq_lens), _ptr(dec_out), B, dec_block_table.shape[1], float(scale),
+        _stream(stream), ctypes.byref(d), _ptr(ws), ws.numel())
+    _check(rc, "pkv_mixed_step_attn")
 
 
 def decode_attn_noalloc(q, k_pages, v_pages, block_table, seq_lens, out, scale: float, stream=None):

@@ -43,6 +43,9 @@ PROTOTYPES = {
     "pkv_prefill_workspace_bytes": (_sz, [_dp, _i32, _i32]),
     "pkv_prefill_chunk_attn": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _vp, _f32, _vp, _dp, _i32,
                                               _i32, _vp, _sz]),
+    "pkv_mixed_workspace_bytes": (_sz, [_dp, _i32, _i32, _i32, _i32]),
+    "pkv_mixed_step_attn": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _vp, _i32, _i32, _vp, _vp, _vp,
+                                           _vp, _i32, _i32, _f32, _vp, _dp, _vp, _sz]),
     "pkv_decode_attn_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _f32, _vp, _dp, _i32, _i32]),
     "pkv_selftest_wait_timeout": (ctypes.c_int, [_vp, _sz, ctypes.c_int64, _vp]),
 }

@@ -276,6 +276,55 @@ int pkv_prefill_chunk_attn(const void* q, const void* k_pages, const void* v_pag
                              desc->num_pages, workspace, reinterpret_cast<cudaStream_t>(stream));
 }
 
+size_t pkv_mixed_workspace_bytes(const pkv_cache_desc* desc, int32_t num_seqs, int32_t max_q_len, int32_t dec_batch,
+                                 int32_t dec_max_pages_per_seq) {
+  if (check_desc(desc) != PKV_OK || num_seqs < 0 || max_q_len < 0 || dec_batch < 0 || dec_max_pages_per_seq < 1)
+    return 0;
+  if (num_seqs > pkv::prefill_max_seqs() || dec_batch > pkv::decode_max_batch()) return 0;
+  int sms = 0;
+  if (current_device(&sms) != PKV_OK) return 0;
+  const bool chunk = num_seqs > 0 && max_q_len > 0;
+  return pkv::mixed_workspace_bytes(chunk ? num_seqs : 0, chunk ? max_q_len : 0, dec_batch, dec_max_pages_per_seq, sms);
+}
+
+int pkv_mixed_step_attn(const void* q, const void* k_pages, const void* v_pages, const int32_t* block_table,
+                        const int32_t* prefix_lens, const int32_t* cu_q_lens, int32_t num_seqs, int32_t total_q,
+                        void* out, int32_t max_pages_per_seq, int32_t max_q_len, const void* dec_q,
+                        const int32_t* dec_block_table, const int32_t* dec_seq_lens, void* dec_out, int32_t dec_batch,
+                        int32_t dec_max_pages_per_seq, float scale, pkv_stream_t stream, const pkv_cache_desc* desc,
+                        void* workspace, size_t workspace_bytes) {
+  int rc = check_desc(desc);  // the tuned 16/8/128 geometry only
+  if (rc != PKV_OK) return rc;
+  if (num_seqs < 0 || total_q < 0 || max_q_len < 0 || max_pages_per_seq < 1) return PKV_ERR_BAD_SHAPE;
+  if (dec_batch < 0 || dec_max_pages_per_seq < 1) return PKV_ERR_BAD_SHAPE;
+  if (!table_fits(num_seqs, max_pages_per_seq) || !table_fits(dec_batch, dec_max_pages_per_seq))
+    return PKV_ERR_BAD_SHAPE;
+  if (static_cast<long long>(desc->num_pages) * desc->num_kv_heads * desc->page_size >= (1LL << 31))
+    return PKV_ERR_UNSUPPORTED;
+  if (num_seqs > pkv::prefill_max_seqs() || dec_batch > pkv::decode_max_batch()) return PKV_ERR_UNSUPPORTED;
+  if (workspace == nullptr) return PKV_ERR_NULL_ARG;
+  if (workspace_bytes < PKV_STATUS_BYTES) return PKV_ERR_WORKSPACE_TOO_SMALL;
+  const bool chunk = num_seqs > 0 && max_q_len > 0 && total_q > 0;
+  if (!chunk && dec_batch == 0) return PKV_OK;
+  if (!k_pages || !v_pages) return PKV_ERR_NULL_ARG;
+  if (chunk && (!q || !block_table || !prefix_lens || !cu_q_lens || !out)) return PKV_ERR_NULL_ARG;
+  if (dec_batch > 0 && (!dec_q || !dec_block_table || !dec_seq_lens || !dec_out)) return PKV_ERR_NULL_ARG;
+  if (!aligned16(k_pages) || !aligned16(v_pages) || !aligned16(workspace)) return PKV_ERR_MISALIGNED;
+  if (chunk && (!aligned16(q) || !aligned16(out))) return PKV_ERR_MISALIGNED;
+  if (dec_batch > 0 && (!aligned16(dec_q) || !aligned16(dec_out))) return PKV_ERR_MISALIGNED;
+  int sms = 0;
+  rc = current_device(&sms);
+  if (rc != PKV_OK) return rc;
+  const int32_t ns = chunk ? num_seqs : 0, mq = chunk ? max_q_len : 0;
+  if (workspace_bytes < pkv::mixed_workspace_bytes(ns, mq, dec_batch, dec_max_pages_per_seq, sms))
+    return PKV_ERR_WORKSPACE_TOO_SMALL;
+  const pkv::MixedDecode dec = {dec_q, dec_block_table, dec_seq_lens, dec_out, dec_batch, dec_max_pages_per_seq};
+  return pkv::launch_prefill(chunk ? q : nullptr, k_pages, v_pages, block_table, prefix_lens, cu_q_lens, ns,
+                             chunk ? total_q : 0, out, scale, desc->num_q_heads, desc->num_kv_heads, desc->head_dim,
+                             max_pages_per_seq, mq, desc->num_pages, workspace, reinterpret_cast<cudaStream_t>(stream),
+                             dec_batch > 0 ? &dec : nullptr);
+}
+
 int pkv_rope_table(float* table, int32_t max_pos, int32_t head_dim, double theta, pkv_stream_t stream) {
   if (table == nullptr) return PKV_ERR_NULL_ARG;
   if (max_pos < 1 || head_dim < 2 || head_dim > 1024 || (head_dim % 2) != 0 || !(theta > 0.0))

@@ -45,10 +45,24 @@ bool prefill_supported(int num_q_heads, int num_kv_heads, int head_dim, int page
 size_t prefill_workspace_bytes(int num_q_heads, int num_kv_heads, int head_dim, int32_t num_seqs, int32_t max_q_len,
                                int num_sms);
 int prefill_max_seqs();
+// The decode half of a mixed step (16/8/128 only): decode requests attended in the prefill launch.
+struct MixedDecode {
+  const void* q;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  void* out;
+  int32_t batch;
+  int32_t max_pages;
+};
+// Workspace of the mixed step: the prefill workspace, then the decode chunks' counters and records.
+size_t mixed_workspace_bytes(int32_t num_seqs, int32_t max_q_len, int32_t dec_batch, int32_t dec_max_pages,
+                             int num_sms);
+// dec: nullptr for prefill alone; otherwise the launch also attends the decode requests (the mixed step).
 int launch_prefill(const void* q, const void* k_pages, const void* v_pages, const int32_t* block_table,
                    const int32_t* prefix_lens, const int32_t* cu_q_lens, int32_t num_seqs, int32_t total_q,
                    void* out, float scale, int num_q_heads, int num_kv_heads, int head_dim, int32_t max_pages,
-                   int32_t max_q_len, int32_t num_pages, void* workspace, cudaStream_t stream);
+                   int32_t max_q_len, int32_t num_pages, void* workspace, cudaStream_t stream,
+                   const MixedDecode* dec = nullptr);
 
 int launch_wait_timeout_selftest(void* workspace, long long limit_cycles, cudaStream_t stream);
 

@@ -25,10 +25,12 @@ int encode_page_maps(const void* k_pages, const void* v_pages, int head_dim, int
                      CUtensorMap* vmap);
 
 // Byte offset of 16-byte chunk c of token row t in a tile written by the
-// 128-byte swizzled TMA boxes: box c / 8 (2 KiB each, 1024-byte aligned), row t
-// of 128 bytes, chunk (c mod 8) XOR (t mod 8).
+// 128-byte swizzled TMA boxes: box c / 8 (kBox bytes apart, each 1024-byte
+// aligned; 2 KiB when a page's boxes are back to back), row t of 128 bytes,
+// chunk (c mod 8) XOR (t mod 8).
+template <int kBox = 2048>
 __device__ __forceinline__ uint32_t swz(int t, int c) {
-  return static_cast<uint32_t>((c >> 3) * 2048 + t * 128 + (((c & 7) ^ (t & 7)) << 4));
+  return static_cast<uint32_t>((c >> 3) * kBox + t * 128 + (((c & 7) ^ (t & 7)) << 4));
 }
 __device__ __forceinline__ void ldsm4(uint32_t addr, uint32_t (&r)[4]) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
@@ -59,14 +61,15 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], 
 // This lane's ldmatrix row addresses inside a page tile, per 16-dim step ks:
 // K as the A operand of the score product (matrices: tokens 0-7 / 8-15 x the
 // two 8-dim halves of the step), V, read transposed, as the A operand of the
-// value product (the same four blocks in the order that operand wants).
-template <int KS>
+// value product (the same four blocks in the order that operand wants). kBox:
+// the distance between a page's 64-dim boxes.
+template <int KS, int kBox = 2048>
 __device__ __forceinline__ void mma_offsets(uint32_t (&koff)[KS], uint32_t (&voff)[KS]) {
   const int lane = threadIdx.x & 31, mi = lane >> 3, mr = lane & 7;
 #pragma unroll
   for (int ks = 0; ks < KS; ++ks) {
-    koff[ks] = swz(mr + ((mi & 1) << 3), 2 * ks + (mi >> 1));
-    voff[ks] = swz(mr + ((mi >> 1) << 3), 2 * ks + (mi & 1));
+    koff[ks] = swz<kBox>(mr + ((mi & 1) << 3), 2 * ks + (mi >> 1));
+    voff[ks] = swz<kBox>(mr + ((mi >> 1) << 3), 2 * ks + (mi & 1));
   }
 }
 

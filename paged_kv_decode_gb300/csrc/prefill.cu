@@ -43,6 +43,7 @@
 
 #include "pkv_device.cuh"
 #include "pkv_kernels.h"
+#include "pkv_mma.cuh"
 #include "pkv_tc.cuh"
 
 namespace pkv {
@@ -60,6 +61,15 @@ constexpr int kPfThreads = 12 * 32;        // 3 warpgroups: softmax head 0, soft
 constexpr int kPfRegsSoftmax = 224;
 constexpr int kPfRegsOther = 56;
 static_assert(2 * 128 * kPfRegsSoftmax + 128 * kPfRegsOther <= kPfThreads * 168, "register split");
+// The mixed-step kernel carries the decode CTAs' code and the decode-page scan as well; there the
+// MMA/TMA warpgroup gets 16 more registers and the softmax ones 8 fewer (at 224 / 56 its split schedule
+// measured 25 % slower than the prefill kernel's; 216 / 72 was the best of the splits tried).
+template <bool kMixed>
+struct PfRegs {
+  static constexpr int kSoftmax = kMixed ? 216 : kPfRegsSoftmax;
+  static constexpr int kOther = kMixed ? 72 : kPfRegsOther;
+  static_assert(2 * 128 * kSoftmax + 128 * kOther <= kPfThreads * 168, "register split");
+};
 constexpr int kPfHalfBytes = kPfRows * 128;  // one 64-column half of a 128-row bf16 tile: 16 KiB
 constexpr int kPfStages = 2;
 constexpr int kNumBars = 14;
@@ -92,11 +102,11 @@ struct PfDim {
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, HD, true);  // B = V tile, MN-major
 };
 
-// + the request prefix sums of cost units and of items, the schedule, the CTA's share (lo, hi, U, G) and each
-// softmax group's pending split pieces, as 64-bit words
+// + the request prefix sums of cost units and of items, the schedule, the CTA's share (lo, hi, U, G), each
+// softmax group's pending split pieces and the split schedule's worker count, as 64-bit words
 template <int HD>
 static size_t pf_smem_bytes(int num_seqs) {
-  return PfDim<HD>::kSmemBytes + static_cast<size_t>(2 * (num_seqs + 1) + 1 + 4 + 4) * 8;
+  return PfDim<HD>::kSmemBytes + static_cast<size_t>(2 * (num_seqs + 1) + 1 + 4 + 4 + 1) * 8;
 }
 
 // Item mode (no item is split) when the largest item is at least this share
@@ -136,6 +146,18 @@ struct PrefillArgs {
   int* status;
   int* counters;   // [num_seqs][pairs][tmax][2], zero between calls
   unsigned char* records;  // [2 * workers][PfDim::kRecBytes]
+  // the mixed step (kMixed): decode requests attended in the same launch, one CTA per (request, KV
+  // head) after the pcta prefill CTAs; the same pools, their own block table and lengths
+  const __nv_bfloat16* dq;  // [dbatch][16][128]
+  const int* dbt;           // [dbatch][dmax_pages]
+  const int* dlens;         // [dbatch]
+  __nv_bfloat16* dout;      // [dbatch][16][128]
+  int dbatch;
+  int dmax_pages;
+  int dmaxc;     // decode chunks per (request, KV head) at most: ceil(dmax_pages / 64)
+  float* drec;   // [dbatch][8][dmaxc][2][132] partial records of chunked pairs
+  int* dcnt;     // [dbatch][8] chunk counters, zero between calls
+  int pcta;  // prefill CTAs of the grid: max(items, workers)
 };
 
 // Head counts of a launch: compile-time constants for the Qwen3 decoder's 16 query / 8 KV heads
@@ -274,7 +296,298 @@ __device__ __forceinline__ void pf_group_sync(int h) {  // the 128 softmax threa
   asm volatile("bar.sync %0, 128;" ::"r"(2 + h) : "memory");
 }
 
-template <int HD, bool kFixed>
+// A decode page of one KV head costs this fraction of a prefill key tile of SM time (the split
+// schedule of the mixed step keeps SMs apart for the decode CTAs in proportion): a key tile of both
+// query heads takes about 2 us of an SM; a decode CTA keeps 24 pages (192 KiB) in flight and streams a
+// page (8 KiB of K and V) in about 0.09 us. (16, 24, 32 and 64 measured within 2 % of each other.)
+#ifndef PKV_MIXED_PAGES_PER_TILE
+#define PKV_MIXED_PAGES_PER_TILE 24
+#endif
+// Pages of one (request, KV head) per decode CTA of the mixed step; longer contexts are cut into
+// chunks whose partial results are merged by the CTA that completes the pair's count.
+// (64 measured faster than 128 and 256: more CTAs stream at once.)
+#ifndef PKV_MIXED_CHUNK_PAGES
+#define PKV_MIXED_CHUNK_PAGES 64
+#endif
+constexpr int kMixChunkPages = PKV_MIXED_CHUNK_PAGES;
+constexpr int kMixStages = 3;  // the two K/V stages of the prefill CTA and the Q area
+constexpr int kMixRec = kHeadDim + 4;  // floats per head of a partial record: o[128], m, l, 2 pad
+static int mixed_chunks_per_pair(int dmax_pages) { return (dmax_pages + kMixChunkPages - 1) / kMixChunkPages; }
+
+// Pages of all (request, KV head) pairs of the mixed step's decode batch (lengths clamped to the
+// block table), summed over the warp. Kept out of line: inlined, its code changed the register
+// allocation of the prefill roles' loops.
+__device__ __noinline__ long long mixed_decode_pages(const int* dlens, int dbatch, int dmax_pages) {
+  const int lane = threadIdx.x & 31;
+  long long pages = 0;
+  for (int base = 0; base < dbatch; base += 32) {
+    const int n = base + lane;
+    if (n < dbatch) {
+      const int len = __ldg(dlens + n);
+      const int cl = len < 0 ? 0 : (len > dmax_pages * kPageSize ? dmax_pages * kPageSize : len);
+      pages += kKVHeads * ((cl + kPageSize - 1) / kPageSize);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) pages += __shfl_xor_sync(0xffffffffu, pages, o);
+  return pages;
+}
+
+// Decode CTA of the mixed step: decode attention of one chunk of <= 64 pages of one (request b, KV
+// head g) pair of the decode batch, in a CTA shaped like the prefill ones. Warp 9 copies the chunk's
+// pages, 8 per 128-key tile, into three stages (the prefill K/V stages and the Q area) through the
+// decode block table, reading a tile's page ids one tile ahead; warps 0-7 take page w of every tile and
+// run the warp-level tensor-core page step of the decode kernels on it (S^T = K Q^T for the group's two
+// query heads, online softmax, O^T += V^T P^T; a page's two 64-dim boxes lie 16 KiB apart in a stage),
+// then merge their (o, m, l) states through shared memory. A pair in one chunk writes its bf16 rows;
+// otherwise the chunk writes a partial record and counts itself in (fence, atomic), and the CTA that
+// completes the count merges the pair's records (log-sum-exp, in chunk order) and resets the counter.
+// Every consumer warp waits for every tile before it frees the stage (8 arrivals per phase), so none
+// runs ahead of the stage ring. Kept out of line, like mixed_decode_pages.
+__device__ __noinline__ void mixed_decode_cta(const PrefillArgs& a, const CUtensorMap* kmap,
+                                                 const CUtensorMap* vmap, PfBars* bars, unsigned char* sQ,
+                                                 unsigned char* sK, unsigned char* sV, volatile int* fail,
+                                                 long long* scratch, int warp, int lane) {
+  using Dm = PfDim<128>;
+  constexpr int kKS = kHeadDim / 16;
+  const int tid = threadIdx.x;
+  if (tid == 32) {  // the stages' barriers: full ones completed by the copies, empty ones by 8 warps
+    for (int st = 0; st < 2; ++st) {
+      mbar_init(&bars->k_full[st], 1);
+      mbar_init(&bars->v_full[st], 1);
+      mbar_init(&bars->kv_empty[st], 8);
+    }
+    mbar_init(&bars->s_full[0], 1);
+    mbar_init(&bars->s_full[1], 1);
+    mbar_init(&bars->p_full[0], 8);
+    *fail = 0;
+    fence_barrier_init();
+  }
+  // ---- which chunk: chunks are ordered by request, KV head, chunk; request b has nc_b chunks per head
+  // (at least one: an empty request writes zeros)
+  const long long e = static_cast<long long>(blockIdx.x) - a.pcta;
+  if (warp == 0) {
+    long long carry = 0;
+    int found = -1;
+    for (int base = 0; base < a.dbatch && found < 0; base += 32) {
+      const int n = base + lane;
+      long long cnt = 0;
+      if (n < a.dbatch) {
+        int len = __ldg(a.dlens + n);
+        len = len < 0 ? 0 : (len > a.dmax_pages * kPageSize ? a.dmax_pages * kPageSize : len);
+        const int np = (len + kPageSize - 1) / kPageSize;
+        cnt = kKVHeads * static_cast<long long>(np > 0 ? (np + kMixChunkPages - 1) / kMixChunkPages : 1);
+      }
+      long long x = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      const bool mine = n < a.dbatch && e >= carry + x - cnt && e < carry + x;
+      const unsigned hit = __ballot_sync(0xffffffffu, mine);
+      if (hit != 0u) {
+        const int src = __ffs(hit) - 1;
+        found = base + src;
+        if (lane == src) {
+          const long long off = e - (carry + x - cnt);  // chunk index within the request: g * nc + c
+          const long long nc = cnt / kKVHeads;
+          scratch[0] = n;
+          scratch[1] = off / nc;  // g
+          scratch[2] = off % nc;  // c
+          scratch[3] = nc;
+        }
+      }
+      carry += __shfl_sync(0xffffffffu, x, 31);
+    }
+    if (found < 0 && lane == 0) scratch[0] = -1;  // past the last chunk
+  }
+  __syncthreads();
+  const int b = static_cast<int>(scratch[0]);
+  if (b < 0) return;
+  const int g = static_cast<int>(scratch[1]), ci = static_cast<int>(scratch[2]), nc = static_cast<int>(scratch[3]);
+  int len = __ldg(a.dlens + b);
+  const int cap = a.dmax_pages * kPageSize;
+  if (len < 0 || len > cap) {
+    if (tid == 0 && g == 0 && ci == 0) set_status(a.status, PKV_ERR_OUT_OF_BOUNDS);
+    len = len < 0 ? 0 : cap;
+  }
+  const int np = (len + kPageSize - 1) / kPageSize;
+  const int pg0 = ci * kMixChunkPages;                                    // the chunk's first page
+  const int pg1 = np < pg0 + kMixChunkPages ? np : pg0 + kMixChunkPages;  // and its end
+  const int ntl = pg1 > pg0 ? (pg1 - pg0 + kPfPagesPerTile - 1) / kPfPagesPerTile : 0;
+  __nv_bfloat16* orow = a.dout + (static_cast<size_t>(b) * kQHeads + kGroup * g) * kHeadDim;
+  // stage s: K and V tiles and their barriers (the third stage is the Q area, on the S/P barriers)
+  auto kst = [&](int st) { return st < 2 ? sK + st * Dm::kTileBytes : sQ; };
+  auto vst = [&](int st) { return st < 2 ? sV + st * Dm::kTileBytes : sQ + Dm::kTileBytes; };
+  auto kfull = [&](int st) { return st < 2 ? &bars->k_full[st] : &bars->s_full[0]; };
+  auto vfull = [&](int st) { return st < 2 ? &bars->v_full[st] : &bars->s_full[1]; };
+  auto empty = [&](int st) { return st < 2 ? &bars->kv_empty[st] : &bars->p_full[0]; };
+
+  if (warp == kPfTmaWarp) {
+    // ------------------------------------------------------------------ page copies
+    auto page_id = [&](int j) {  // this lane's page of tile j (-1: none or outside the pool)
+      const int pg = pg0 + j * kPfPagesPerTile + lane;
+      int id = -1;
+      if (lane < kPfPagesPerTile && pg < pg1) {
+        id = __ldg(a.dbt + static_cast<size_t>(b) * a.dmax_pages + pg);
+        if (id < 0 || id >= a.num_pages) {
+          set_status(a.status, PKV_ERR_OUT_OF_BOUNDS);
+          id = -1;
+        }
+      }
+      return id;
+    };
+    int id_next = ntl > 0 ? page_id(0) : -1;
+    for (int j = 0; j < ntl; ++j) {
+      const int st = j % kMixStages;
+      const int use = j / kMixStages;
+      const int id = id_next;
+      if (j + 1 < ntl) id_next = page_id(j + 1);  // the next tile's ids while this one waits for its stage
+      if (use > 0 && !pf_wait_warp(empty(st), static_cast<uint32_t>(use - 1) & 1u, fail, a.status)) break;
+      const bool valid = id >= 0;
+      const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+      const uint32_t bytes = static_cast<uint32_t>(__popc(vmask)) * static_cast<uint32_t>(Dm::kPageBytes);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(kfull(st), bytes);
+        mbar_arrive_expect_tx(vfull(st), bytes);
+      }
+      __syncwarp();
+      if (valid) {
+        const int row = (id * kKVHeads + g) * kPageSize;
+        unsigned char* kd = kst(st) + lane * (kPageSize * 128);
+        unsigned char* vd = vst(st) + lane * (kPageSize * 128);
+        tma_load_2d(kd, kmap, 0, row, kfull(st));
+        tma_load_2d(kd + kPfHalfBytes, kmap, 64, row, kfull(st));
+        tma_load_2d(vd, vmap, 0, row, vfull(st));
+        tma_load_2d(vd + kPfHalfBytes, vmap, 64, row, vfull(st));
+      }
+    }
+  }
+
+  constexpr int kRec = kMixRec;
+  float* st_all = reinterpret_cast<float*>(sK);  // the warps' states, once every stage is drained
+  if (warp < 8) {
+    // ------------------------------------------------------------------ consumers: page w of every tile
+    const int r = lane >> 2, c = lane & 3;
+    uint32_t qf[kKS][2];  // Q^T as the B operand: head r of the group (rows r >= 2 zero)
+    {
+      const bool live = r < kGroup;
+      const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+          a.dq + (static_cast<size_t>(b) * kQHeads + kGroup * g + (live ? r : 0)) * kHeadDim);
+#pragma unroll
+      for (int ks = 0; ks < kKS; ++ks) {
+        qf[ks][0] = live ? __ldg(qrow + 8 * ks + c) : 0u;
+        qf[ks][1] = live ? __ldg(qrow + 8 * ks + 4 + c) : 0u;
+      }
+    }
+    uint32_t koff[kKS], voff[kKS];
+    mma_offsets<kKS, kPfHalfBytes>(koff, voff);
+    float o[kKS][4];
+#pragma unroll
+    for (int ks = 0; ks < kKS; ++ks) o[ks][0] = o[ks][1] = o[ks][2] = o[ks][3] = 0.f;
+    float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
+    bool ok = true;
+    for (int j = 0; j < ntl; ++j) {
+      const int st = j % kMixStages;
+      const uint32_t ph = static_cast<uint32_t>(j / kMixStages) & 1u;
+      ok = ok && pf_wait_warp(kfull(st), ph, fail, a.status) && pf_wait_warp(vfull(st), ph, fail, a.status);
+      const int p = pg0 + j * kPfPagesPerTile + warp;
+      if (ok && p < pg1) {
+        const int rem = len - p * kPageSize;
+        const uint32_t kt = smem_u32(kst(st) + warp * (kPageSize * 128));
+        const uint32_t vt = smem_u32(vst(st) + warp * (kPageSize * 128));
+        mma_page<kKS>(kt, vt, koff, voff, qf, rem < kPageSize ? rem : kPageSize, a.scale_log2, o, m0, m1, l0, l1);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cta(empty(st));
+    }
+#pragma unroll
+    for (int m = 4; m < 32; m <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, m);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, m);
+    }
+    // every stage is drained (each warp waited for every tile), so stage 0 holds the states:
+    // [warp][head][128 + 4] floats
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    if (c == 0) {  // lanes c == 0 hold heads 0 and 1 of the group
+      float* wst = st_all + warp * kGroup * kRec;
+#pragma unroll
+      for (int n = 0; n < kGroup; ++n) {
+#pragma unroll
+        for (int ks = 0; ks < kKS; ++ks) {
+          wst[n * kRec + 16 * ks + r] = o[ks][n];
+          wst[n * kRec + 16 * ks + r + 8] = o[ks][2 + n];
+        }
+        if (r == 0) {
+          wst[n * kRec + kHeadDim] = n ? m1 : m0;
+          wst[n * kRec + kHeadDim + 1] = n ? l1 : l0;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (*fail) return;
+  // ---- merge the 8 warps' states: one thread per (head, dim); the chunk's result is (O, M, L) with
+  // O = sum_w o_w 2^(m_w - M), L = sum_w l_w 2^(m_w - M), M = max_w m_w (log2 units)
+  float* rec = a.drec + ((static_cast<size_t>(b) * kKVHeads + g) * a.dmaxc + ci) * (kGroup * kRec);
+  if (tid < 256) {
+    const int n = tid >> 7, d = tid & 127;
+    float M = -CUDART_INF_F;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) M = fmaxf(M, st_all[(w * kGroup + n) * kRec + kHeadDim]);
+    float L = 0.f, O = 0.f;
+    if (M != -CUDART_INF_F) {
+#pragma unroll
+      for (int w = 0; w < 8; ++w) {
+        const float* ws = st_all + (w * kGroup + n) * kRec;
+        const float ew = ex2(ws[kHeadDim] - M);  // a warp without pages: m = -inf, weight 0
+        L += ws[kHeadDim + 1] * ew;
+        O += ws[d] * ew;
+      }
+    }
+    if (nc == 1) {
+      orow[n * kHeadDim + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);  // an empty request: zeros
+    } else {
+      rec[n * kRec + d] = O;
+      if (d == 0) {
+        rec[n * kRec + kHeadDim] = M;
+        rec[n * kRec + kHeadDim + 1] = L;
+      }
+    }
+  }
+  if (nc == 1) return;
+  // ---- count the chunk in (release); the CTA completing the pair's count merges (acquire)
+  __syncthreads();
+  volatile int* merge_flag = reinterpret_cast<volatile int*>(scratch + 4);
+  int* counter = a.dcnt + static_cast<size_t>(b) * kKVHeads + g;
+  if (tid == 0) {
+    __threadfence();
+    const int old = atomicAdd(counter, 1);
+    __threadfence();
+    *merge_flag = old == nc - 1 ? 1 : 0;
+  }
+  __syncthreads();
+  if (!*merge_flag) return;
+  if (tid < 256) {
+    const int n = tid >> 7, d = tid & 127;
+    const float* recs = a.drec + (static_cast<size_t>(b) * kKVHeads + g) * a.dmaxc * (kGroup * kRec);
+    float M = -CUDART_INF_F;
+    for (int k = 0; k < nc; ++k) M = fmaxf(M, __ldcg(recs + (k * kGroup + n) * kRec + kHeadDim));
+    float L = 0.f, O = 0.f;
+    for (int k = 0; k < nc; ++k) {  // chunk order: the same bits whichever CTA merges
+      const float* rk = recs + (k * kGroup + n) * kRec;
+      const float mk = __ldcg(rk + kHeadDim);
+      const float ek = mk == -CUDART_INF_F ? 0.f : ex2(mk - M);
+      L += __ldcg(rk + kHeadDim + 1) * ek;
+      O += __ldcg(rk + d) * ek;
+    }
+    orow[n * kHeadDim + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+  }
+  if (tid == 0) *counter = 0;
+}
+
+template <int HD, bool kFixed, bool kMixed>
 __global__ void __launch_bounds__(kPfThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
@@ -283,6 +596,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);  // 1024-byte aligned for 128-byte swizzle atoms
   using Dm = PfDim<HD>;
   using Hd = PfHeads<kFixed>;
+  static_assert(!kMixed || (HD == 128 && kFixed), "the mixed step serves the 16/8/128 geometry");
   PfBars* bars = reinterpret_cast<PfBars*>(smem + Dm::kOffBars);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Dm::kOffBars + kNumBars * 8);
   volatile int* fail = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -295,6 +609,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
   grid_dependency_wait();
   allow_dependents();
+  if constexpr (kMixed) {
+    // the mixed step: CTAs past the prefill ones attend a chunk of a decode (request, KV head) each
+    // (a path of their own, so the prefill roles keep their registers)
+    if (static_cast<int>(blockIdx.x) >= a.pcta) {
+      mixed_decode_cta(a, &kmap, &vmap, bars, smem + Dm::kOffQ, smem + Dm::kOffK, smem + Dm::kOffV, fail, pref, warp,
+                       lane);
+      return;
+    }
+  }
 
   if (tid == 0) {
     mbar_init(&bars->q_full, 1);
@@ -362,10 +685,24 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       tiles_all += __shfl_xor_sync(0xffffffffu, tiles_all, o);
       nt_max = max(nt_max, __shfl_xor_sync(0xffffffffu, nt_max, o));
     }
+    // the mixed step: decode pages of all pairs (their CTAs follow the prefill ones)
+    const long long dec_pages = kMixed ? mixed_decode_pages(a.dlens, a.dbatch, a.dmax_pages) : 0;
     if (lane == 0) {
       pref[a.num_seqs] = carry;
       ipref[a.num_seqs] = icarry;
-      pref[a.num_seqs + 1] = 100LL * nt_max * a.workers >= static_cast<long long>(PKV_PF_ITEM_MODE_PCT) * tiles_all;
+      const bool items_mode =
+          100LL * nt_max * a.workers >= static_cast<long long>(PKV_PF_ITEM_MODE_PCT) * tiles_all;
+      pref[a.num_seqs + 1] = items_mode;
+      // Split schedule of the mixed step: leave k SMs to the decode CTAs, k in proportion to the decode
+      // pages' share of the SM time (item mode needs none: the decode CTAs fill the SMs its tail frees).
+      long long workers = a.workers;
+      if (kMixed && !items_mode && dec_pages > 0) {
+        const long long dec_tiles = (dec_pages + PKV_MIXED_PAGES_PER_TILE - 1) / PKV_MIXED_PAGES_PER_TILE;
+        long long k = (static_cast<long long>(a.workers) * dec_tiles + dec_tiles + tiles_all - 1) / (dec_tiles + tiles_all);
+        k = k < 1 ? 1 : (k > a.workers / 2 ? a.workers / 2 : k);
+        workers = a.workers - k;
+      }
+      pref[2 * a.num_seqs + 11] = workers;
     }
   }
   if (warp == kPfMmaWarp) {
@@ -408,7 +745,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const int n_pages = (kv_end + kPageSize - 1) / kPageSize;
     if (warp == kPfTmaWarp) {
       // ------------------------------------------------------------------ TMA producer
-      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kPfRegsOther));
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(PfRegs<kMixed>::kOther));
       if (lane == 0) {
         mbar_arrive_expect_tx(&bars->q_full, 2 * Dm::kTileBytes);
         for (int h = 0; h < 2; ++h)
@@ -451,7 +788,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
     } else if (warp == kPfMmaWarp) {
       // ------------------------------------------------------------------ MMA issuer
-      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kPfRegsOther));
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(PfRegs<kMixed>::kOther));
       // Issue order QK_0(0) QK_1(0) | PV_0(j) QK_0(j+1) PV_1(j) QK_1(j+1) | ...: the
       // two heads' softmaxes run half a period apart, so while one head's softmax
       // works the other head's PV and next QK keep the tensor pipe busy. QK_h(j+1)
@@ -527,7 +864,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
     } else if (warp < 8) {
       // ------------------------------------------------------------------ softmax warpgroups
-      asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kPfRegsSoftmax));
+      asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(PfRegs<kMixed>::kSoftmax));
       const int h = warp >> 2;
       const int quarter = warp & 3;
       const int r = quarter * 32 + lane;  // row of the tile = TMEM lane
@@ -636,7 +973,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
       }
     } else {
-      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kPfRegsOther));  // idle warps 10-11
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(PfRegs<kMixed>::kOther));  // idle warps 10-11
     }
 
     }
@@ -644,7 +981,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     // ================================================================ split mode: shares of key tiles
     // Only min(workers, U) CTAs take a share, so every share is non-empty.
     const long long U = pref[a.num_seqs];
-    const int G = static_cast<int>(U < a.workers ? U : a.workers);
+    const long long nw = pref[2 * a.num_seqs + 11];  // persistent workers (fewer in a mixed step)
+    const int G = static_cast<int>(U < nw ? U : nw);
     const bool active = static_cast<int>(blockIdx.x) < G;
     const long long lo = active ? pf_share_lo(blockIdx.x, U, G) : 0;
     const long long hi = active ? pf_share_lo(blockIdx.x + 1, U, G) : 0;
@@ -654,7 +992,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   if (!active) {
     } else if (warp == kPfTmaWarp) {
       // ------------------------------------------------------------------ TMA producer
-      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kPfRegsOther));
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(PfRegs<kMixed>::kOther));
       int gj = 0;  // key tiles of this CTA so far
       int pi = 0;
       PfPiece pc;
@@ -713,7 +1051,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
     } else if (warp == kPfMmaWarp) {
       // ------------------------------------------------------------------ MMA issuer
-      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kPfRegsOther));
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(PfRegs<kMixed>::kOther));
       // Issue order QK_0(0) QK_1(0) | PV_0(j) QK_0(j+1) PV_1(j) QK_1(j+1) | ... over
       // the CTA's key tiles (across pieces): the two heads' softmaxes run half a
       // period apart, so while one head's softmax works the other head's PV and
@@ -814,7 +1152,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
     } else if (warp < 8) {
       // ------------------------------------------------------------------ softmax warpgroups
-      asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kPfRegsSoftmax));
+      asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(PfRegs<kMixed>::kSoftmax));
       const int h = warp >> 2;
       const int quarter = warp & 3;
       const int r = quarter * 32 + lane;  // row of the tile = TMEM lane
@@ -1082,7 +1420,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
       }
     } else {
-      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kPfRegsOther));  // idle warps 10-11
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(PfRegs<kMixed>::kOther));  // idle warps 10-11
     }
 
   }
@@ -1134,25 +1472,42 @@ size_t prefill_workspace_bytes(int num_q_heads, int num_kv_heads, int head_dim, 
   return PKV_STATUS_BYTES + pf_counter_bytes(num_seqs, max_q_len, pf_pairs(num_q_heads, num_kv_heads)) +
          static_cast<size_t>(2) * num_sms * pf_rec_bytes(head_dim);
 }
+
+// The mixed step's decode part after the prefill workspace: chunk counters [dec_batch][8] (256-byte
+// padded), then the partial records [dec_batch][8][chunks][2][132] floats.
+static size_t mixed_counter_bytes(int32_t dec_batch) {
+  return (static_cast<size_t>(dec_batch) * kKVHeads * 4 + 255) / 256 * 256;
+}
+size_t mixed_workspace_bytes(int32_t num_seqs, int32_t max_q_len, int32_t dec_batch, int32_t dec_max_pages,
+                             int num_sms) {
+  const int maxc = mixed_chunks_per_pair(dec_max_pages);
+  return prefill_workspace_bytes(kQHeads, kKVHeads, kHeadDim, num_seqs, max_q_len, num_sms) +
+         mixed_counter_bytes(dec_batch) +
+         static_cast<size_t>(dec_batch) * kKVHeads * (maxc > 1 ? maxc : 0) * kGroup * kMixRec * 4;
+}
 int prefill_max_seqs() { return kPfMaxSeqs; }
 
-template <int HD, bool kFixed>
+template <int HD, bool kFixed, bool kMixed>
 static int launch_prefill_hd(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                             const PrefillArgs& a, int num_seqs, long long items, int num_sms, cudaStream_t stream) {
+                             PrefillArgs a, int num_seqs, long long items, int num_sms, cudaStream_t stream) {
   static bool attr_set[64] = {false};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
   if (dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(prefill_kernel<HD, kFixed>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(prefill_kernel<HD, kFixed, kMixed>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(pf_smem_bytes<HD>(kPfMaxSeqs))) != cudaSuccess)
       return PKV_ERR_CUDA;
     attr_set[dev] = true;
   }
-  // one CTA per SM fits (TMEM and shared memory); split mode uses the first num_sms CTAs as persistent
-  // workers, item mode one CTA per item
-  const unsigned grid = static_cast<unsigned>(items > num_sms ? items : num_sms);
-  return launch_pdl(prefill_kernel<HD, kFixed>, dim3(grid), dim3(kPfThreads), pf_smem_bytes<HD>(num_seqs), stream, qmap,
-                    kmap, vmap, a) == cudaSuccess
+  // one CTA per SM fits (TMEM and shared memory); split mode uses the first num_sms CTAs (fewer in a mixed
+  // step) as persistent workers, item mode one CTA per item; the mixed step's decode CTAs follow, one per
+  // chunk of <= 64 pages of a (decode request, KV head), as many as the longest request can need
+  a.pcta = static_cast<int>(items > num_sms ? items : num_sms);
+  const long long grid =
+      static_cast<long long>(a.pcta) + (kMixed ? static_cast<long long>(a.dbatch) * kKVHeads * a.dmaxc : 0);
+  if (grid > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
+  return launch_pdl(prefill_kernel<HD, kFixed, kMixed>, dim3(static_cast<unsigned>(grid)), dim3(kPfThreads),
+                    pf_smem_bytes<HD>(num_seqs), stream, qmap, kmap, vmap, a) == cudaSuccess
              ? PKV_OK
              : PKV_ERR_CUDA;
 }
@@ -1160,8 +1515,12 @@ static int launch_prefill_hd(const CUtensorMap& qmap, const CUtensorMap& kmap, c
 int launch_prefill(const void* q, const void* k_pages, const void* v_pages, const int32_t* block_table,
                    const int32_t* prefix_lens, const int32_t* cu_q_lens, int32_t num_seqs, int32_t total_q,
                    void* out, float scale, int num_q_heads, int num_kv_heads, int head_dim, int32_t max_pages,
-                   int32_t max_q_len, int32_t num_pages, void* workspace, cudaStream_t stream) {
-  if (num_seqs == 0 || max_q_len == 0 || total_q == 0) return PKV_OK;
+                   int32_t max_q_len, int32_t num_pages, void* workspace, cudaStream_t stream,
+                   const MixedDecode* dec) {
+  const bool mixed = dec != nullptr && dec->batch > 0;
+  if (!mixed && (num_seqs == 0 || max_q_len == 0 || total_q == 0)) return PKV_OK;
+  if (mixed && !(num_q_heads == kQHeads && num_kv_heads == kKVHeads && head_dim == kHeadDim))
+    return PKV_ERR_UNSUPPORTED;
   if (!prefill_supported(num_q_heads, num_kv_heads, head_dim, kPageSize)) return PKV_ERR_UNSUPPORTED;
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return PKV_ERR_CUDA;
@@ -1169,11 +1528,15 @@ int launch_prefill(const void* q, const void* k_pages, const void* v_pages, cons
 
   CUtensorMap qmap, kmap, vmap;
   {
-    const cuuint64_t dims[3] = {hd, static_cast<cuuint64_t>(num_q_heads), static_cast<cuuint64_t>(total_q)};
+    // (a mixed step may have no chunk rows: the map then covers one row it never reads)
+    const cuuint64_t rows = total_q > 0 ? static_cast<cuuint64_t>(total_q) : 1;
+    const cuuint64_t dims[3] = {hd, static_cast<cuuint64_t>(num_q_heads), rows};
     const cuuint64_t strides[2] = {hd * 2, static_cast<cuuint64_t>(num_q_heads) * hd * 2};
     const cuuint32_t box[3] = {64, 1, kPfRows};
     const cuuint32_t estr[3] = {1, 1, 1};
-    if (enc(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, estr,
+    // (without chunk rows the map points at the K pool: it needs a valid address and is never read)
+    void* qbase = total_q > 0 && q != nullptr ? const_cast<void*>(q) : const_cast<void*>(k_pages);
+    if (enc(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, qbase, dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return PKV_ERR_CUDA;
@@ -1217,11 +1580,26 @@ int launch_prefill(const void* q, const void* k_pages, const void* v_pages, cons
   a.status = reinterpret_cast<int*>(ws);
   a.counters = reinterpret_cast<int*>(ws + PKV_STATUS_BYTES);
   a.records = ws + PKV_STATUS_BYTES + pf_counter_bytes(num_seqs, max_q_len, a.pairs);
+  a.dq = mixed ? static_cast<const __nv_bfloat16*>(dec->q) : nullptr;
+  a.dbt = mixed ? dec->block_table : nullptr;
+  a.dlens = mixed ? dec->seq_lens : nullptr;
+  a.dout = mixed ? static_cast<__nv_bfloat16*>(dec->out) : nullptr;
+  a.dbatch = mixed ? dec->batch : 0;
+  a.dmax_pages = mixed ? dec->max_pages : 1;
+  a.dmaxc = mixed_chunks_per_pair(a.dmax_pages);
+  {
+    unsigned char* dws = ws + prefill_workspace_bytes(num_q_heads, num_kv_heads, head_dim, num_seqs, max_q_len, num_sms);
+    a.dcnt = mixed ? reinterpret_cast<int*>(dws) : nullptr;
+    a.drec = mixed ? reinterpret_cast<float*>(dws + mixed_counter_bytes(a.dbatch)) : nullptr;
+  }
+  a.pcta = 0;
   const long long items = static_cast<long long>(num_seqs) * a.pairs * a.tmax;
-  if (head_dim == 64) return launch_prefill_hd<64, false>(qmap, kmap, vmap, a, num_seqs, items, num_sms, stream);
+  if (mixed) return launch_prefill_hd<128, true, true>(qmap, kmap, vmap, a, num_seqs, items, num_sms, stream);
+  if (head_dim == 64)
+    return launch_prefill_hd<64, false, false>(qmap, kmap, vmap, a, num_seqs, items, num_sms, stream);
   if (num_q_heads == kQHeads && num_kv_heads == kKVHeads)  // the Qwen3 decoder: head counts fixed at compile time
-    return launch_prefill_hd<128, true>(qmap, kmap, vmap, a, num_seqs, items, num_sms, stream);
-  return launch_prefill_hd<128, false>(qmap, kmap, vmap, a, num_seqs, items, num_sms, stream);
+    return launch_prefill_hd<128, true, false>(qmap, kmap, vmap, a, num_seqs, items, num_sms, stream);
+  return launch_prefill_hd<128, false, false>(qmap, kmap, vmap, a, num_seqs, items, num_sms, stream);
 }
 
 }  // namespace pkv

@@ -100,6 +100,39 @@ def test_rope_table_host_argument_checks(lib):
     assert f(p + 4, 8, 128, 1e6, None) == -8
 
 
+def test_mixed_step_host_argument_checks(lib):
+    # pkv_mixed_step_attn serves 16/8/128 and checks both halves' arguments before any device lookup
+    f = lib.pkv_mixed_step_attn
+    buf = ctypes.create_string_buffer(1024)
+    p = (ctypes.addressof(buf) + 255) // 256 * 256  # aligned host address, never dereferenced
+    d = _desc()
+
+    def call(desc=d, num_seqs=1, total_q=8, max_q=8, dec_batch=2, dec_pages=4, ws=p, ws_bytes=256, q=None, dq=None,
+             kp=None):
+        q = p if q is None else q
+        dq = p if dq is None else dq
+        kp = p if kp is None else kp
+        return f(q, kp, kp, p, p, p, num_seqs, total_q, q, 4, max_q, dq, p, p, dq, dec_batch, dec_pages, 1.0, None,
+                 None if desc is None else ctypes.byref(desc), ws, ws_bytes)
+
+    assert call(desc=None) == -1
+    for other in (_desc(num_q_heads=32), _desc(head_dim=64)):
+        assert call(desc=other) == -3
+    assert call(num_seqs=-1) == -2
+    assert call(dec_batch=-1) == -2
+    assert call(dec_pages=0) == -2
+    assert call(dec_batch=1025) == -3
+    assert call(ws=None) == -1
+    assert call(ws_bytes=64) == -4
+    assert call(num_seqs=0, dec_batch=0) == 0  # nothing to do
+    assert call(kp=0) == -1
+    assert call(q=p + 2) == -8
+    assert call(dq=p + 4) == -8
+    assert lib.pkv_mixed_workspace_bytes(None, 1, 8, 2, 4) == 0
+    assert lib.pkv_mixed_workspace_bytes(ctypes.byref(_desc(num_q_heads=32)), 1, 8, 2, 4) == 0
+    assert lib.pkv_mixed_workspace_bytes(ctypes.byref(d), 1, 8, -1, 4) == 0
+
+
 def test_noalloc_host_argument_checks(lib):
     # pkv_decode_attn_noalloc rejects bad arguments before it looks up its device array
     f = lib.pkv_decode_attn_noalloc

@@ -309,3 +309,93 @@ def test_mixed_step_graph_matches_oracle(cuda_device, prefix):
     assert_close(bf16_to_f64(s["out"])[np.asarray(rows)], want, f"mixed step: chunk after {prefix}")
     want_d = oracle.decode(case.dec_q[0], kp, vp, case.dec_block_table, case.dec_seq_lens, case.geom.scale)
     assert_close(bf16_to_f64(s["dout"]), want_d, f"mixed step: 15 decode requests (chunk after {prefix})")
+
+
+# ---------------------------------------------------------------------------- the mixed-step kernel
+
+def mixed_workers(case, sms, pages_per_tile=24, item_mode_pct=75, kv_heads=8, tile=128):
+    """Persistent prefill workers of the mixed-step kernel's split schedule: the SMs less the ones kept
+    for the decode CTAs, in proportion to the decode pages' share of the SM time (a test-side model of
+    the kernel's rule, used to pick the rows the split schedule cuts)."""
+    tiles = [(-(-(int(P) + min(int(L), tile * (t + 1))) // tile))
+             for P, L in zip(case.prefix_lens, case.q_lens) for t in range(-(-int(L) // tile))]
+    tiles_all = kv_heads * sum(tiles)
+    if not tiles or 100 * max(tiles) * sms >= item_mode_pct * tiles_all:
+        return sms
+    dec_pages = kv_heads * sum(-(-int(n) // 16) for n in case.dec_seq_lens)
+    if dec_pages == 0:
+        return sms
+    dec_tiles = -(-dec_pages // pages_per_tile)
+    k = -(-(sms * dec_tiles) // (dec_tiles + tiles_all))
+    return sms - min(max(k, 1), sms // 2)
+
+
+def _mixed_kernel_run(case, dev):
+    """pkv_append of the chunk and the decode tokens, then one pkv_mixed_step_attn launch."""
+    ensure_built()
+    kp, vp = case.k_pages[0].to(dev), case.v_pages[0].to(dev)
+    S = len(case.prefix_lens)
+    max_q = int(case.q_lens.max()) if S else 0
+    ws = pkv.Workspace(pkv.mixed_workspace_bytes(S, max_q, len(case.dec_seq_lens), case.dec_block_table.shape[1]), dev)
+    q = case.q[0].to(dev)
+    out = torch.full_like(q, float("nan"))
+    dq = case.dec_q[0].to(dev)
+    dout = torch.full_like(dq, float("nan"))
+    if S:
+        pkv.append(case.k_new[0].to(dev), case.v_new[0].to(dev), i32(case.slot_mapping, dev), kp, vp, ws)
+    pkv.append(case.dec_k_new[0].to(dev), case.dec_v_new[0].to(dev), i32(case.dec_slot_mapping, dev), kp, vp, ws)
+    pkv.mixed_step_attn(q if S else None, kp, vp, i32(case.block_table, dev) if S else None,
+                        i32(case.prefix_lens, dev) if S else None, i32(case.cu_q_lens, dev) if S else None,
+                        out if S else None, max_q, dq, i32(case.dec_block_table, dev), i32(case.dec_seq_lens, dev),
+                        dout, case.geom.scale, ws)
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    want_k, want_v = oracle.append(case.k_new[0], case.v_new[0], case.slot_mapping, case.k_pages[0], case.v_pages[0])
+    want_k, want_v = oracle.append(case.dec_k_new[0], case.dec_v_new[0], case.dec_slot_mapping, want_k, want_v)
+    assert np.array_equal(bits(kp), want_k) and np.array_equal(bits(vp), want_v)
+    return out, dout, want_k, want_v
+
+
+@pytest.mark.parametrize("prefix", [0, 8192, 32768])
+def test_mixed_step_kernel_matches_oracle(cuda_device, prefix):
+    # workload 4 at full size through the one-launch mixed step: a 4096-row chunk after `prefix` cached
+    # tokens and 15 decode requests U{500..5000}; sampled chunk rows (every row offset, every row of two
+    # tiles the split schedule cuts) and all decode rows against the oracle
+    case = W.prefill_case(4, [prefix], [W.PREFILL_CHUNK], dec_seq_lens=W.mixed_decode_lens(4), poison=True)
+    out, dout, kp, vp = _mixed_kernel_run(case, cuda_device)
+    workers = mixed_workers(case, _workers(cuda_device))
+    cut = split_cut_tiles(case.prefix_lens, case.q_lens, workers)
+    if prefix > 0:
+        assert cut and workers < _workers(cuda_device)  # split schedule, SMs kept for the decode CTAs
+    rows = set(_sample_rows(W.PREFILL_CHUNK))
+    for n, t in cut[:: max(1, len(cut) // 2)][:2]:
+        rows |= set(range(128 * t, min(128 * t + 128, W.PREFILL_CHUNK)))
+    rows = sorted(rows)
+    want = oracle.prefill(case.q[0], kp, vp, case.block_table, case.prefix_lens, case.cu_q_lens, case.geom.scale,
+                          rows=rows)
+    assert_close(bf16_to_f64(out)[np.asarray(rows)], want, f"mixed kernel: chunk after {prefix}")
+    want_d = oracle.decode(case.dec_q[0], kp, vp, case.dec_block_table, case.dec_seq_lens, case.geom.scale)
+    assert_close(bf16_to_f64(dout), want_d, f"mixed kernel: decode requests (chunk after {prefix})")
+
+
+def test_mixed_step_kernel_small_all_rows(cuda_device):
+    # two chunks and a ragged decode batch (empty, one-token, page-boundary and a 9-page request) in one
+    # pool; every output row against the oracle
+    case = W.prefill_case(47, [130, 0], [300, 77], dec_seq_lens=[0, 1, 16, 17, 129, 2000, 33], poison=True)
+    out, dout, kp, vp = _mixed_kernel_run(case, cuda_device)
+    want = oracle.prefill(case.q[0], kp, vp, case.block_table, case.prefix_lens, case.cu_q_lens, case.geom.scale)
+    assert_close(bf16_to_f64(out), want, "mixed kernel: small chunks")
+    want_d = oracle.decode(case.dec_q[0], kp, vp, case.dec_block_table, case.dec_seq_lens, case.geom.scale)
+    assert_close(bf16_to_f64(dout), want_d, "mixed kernel: ragged decode batch")
+    assert torch.count_nonzero(dout[0].view(torch.int16)).item() == 0  # the empty request: zeros
+    # one-token request: that value row exactly
+    assert torch.equal(dout[1].view(torch.int16).cpu(), torch.from_numpy(
+        np.repeat(vp[case.dec_block_table[1, 0], :, 0, :].view(np.int16), 2, axis=0)))
+
+
+def test_mixed_step_kernel_decode_only(cuda_device):
+    # no chunk: the launch is decode attention alone
+    case = W.prefill_case(48, [], [], dec_seq_lens=[300, 0, 5000, 16], poison=True)
+    _, dout, kp, vp = _mixed_kernel_run(case, cuda_device)
+    want_d = oracle.decode(case.dec_q[0], kp, vp, case.dec_block_table, case.dec_seq_lens, case.geom.scale)
+    assert_close(bf16_to_f64(dout), want_d, "mixed kernel: decode only")
