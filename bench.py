@@ -503,6 +503,40 @@ def run_geometry(args, device):
                       "steps": args.steps, "warmup": args.warmup}), flush=True)
 
 
+def run_prefill_geometry(args, device):
+    """Chunked prefill alone on another cache geometry: a 4096-row chunk after 0 / 8192 / 32768 cached tokens
+    (the prefill kernel on pairs of query heads), TFLOP/s of the causal flops."""
+    import torch
+
+    import paged_kv_decode_gb300 as pkv
+    from paged_kv_decode_gb300 import workloads as W
+
+    q, kv, d = (int(x) for x in args.prefill_geometry.split(","))
+    g = W.Geometry(q, kv, d)
+    bf16 = _peaks()[1]
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)
+    res = {}
+    for P in (0, 8192, 32768):
+        c = W.prefill_case(4, [P], [W.PREFILL_CHUNK], geom=g, device=device, poison=True)
+        kp, vp, qq = c.k_pages[0], c.v_pages[0], c.q[0]
+        out = torch.empty_like(qq)
+        ws = pkv.Workspace(pkv.prefill_workspace_bytes(1, W.PREFILL_CHUNK, c.num_pages, q, kv, d), device)
+        pkv.append(c.k_new[0], c.v_new[0], i32(c.slot_mapping), kp, vp, ws)
+        bt, pl, cu = i32(c.block_table), i32(c.prefix_lens), i32(c.cu_q_lens)
+        fn = lambda: pkv.prefill_chunk_attn(qq, kp, vp, bt, pl, cu, out, g.scale, W.PREFILL_CHUNK, ws)
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        ms = time_launches(torch, fn, max(3, args.steps))
+        flops = 4 * d * q * (W.PREFILL_CHUNK * P + W.PREFILL_CHUNK * (W.PREFILL_CHUNK + 1) // 2)
+        tf = flops / (ms * 1e-3) / 1e12
+        res[f"prefix_{P}"] = {"prefill_us": ms * 1e3, "tflops": tf, "frac_of_measured_bf16": tf / bf16}
+        del c, kp, vp, qq, out, ws
+        torch.cuda.empty_cache()
+    print(json.dumps({"workload": f"chunked prefill, {q}q/{kv}kv/d{d}, 4096-row chunk after 0/8192/32768 cached "
+                                  f"tokens", **res, "steps": args.steps, "warmup": args.warmup}), flush=True)
+
+
 def measure_prefill(device, bf16_peak, reps=10):
     import torch
 
@@ -704,6 +738,8 @@ def main():
     ap.add_argument("--no-extra", action="store_true", help="skip the 40k-context and prefill measurements")
     ap.add_argument("--geometry", default=None, metavar="Q,KV,D",
                     help="time only the generic decode path on that cache geometry (bs16 U{300..3000}) and exit")
+    ap.add_argument("--prefill-geometry", default=None, metavar="Q,KV,D",
+                    help="time only chunked prefill on that cache geometry (4096 rows after 0/8192/32768) and exit")
     ap.add_argument("--geometry-fused", action="store_true",
                     help="with --geometry: time the fused append + decode call with early prefetch")
     ap.add_argument("--unfused", action="store_true",
@@ -739,6 +775,9 @@ def main():
     torch.cuda.set_device(device)
     if args.geometry:
         run_geometry(args, device)
+        return
+    if args.prefill_geometry:
+        run_prefill_geometry(args, device)
         return
 
     # each replica runs its own copy of the workload (replicas only: requests are independent)
