@@ -576,10 +576,13 @@ def stage_inputs(step, align=256):
     for name, t in shared:
         parts.append((name, None, off, t))
         off += (t.numel() * t.element_size() + align - 1) // align * align
+    layer_off = []
     for l in range(step.layers):
+        layer_off.append(off)
         for name, t in per_layer:
             parts.append((name, l, off, t[l]))
             off += (t[l].numel() * t[l].element_size() + align - 1) // align * align
+    step.staging_layer_off = layer_off  # offset of each layer's inputs in the staging buffers
     dev = torch.empty(off, dtype=torch.uint8, device=step.out.device)
     host = torch.empty(off, dtype=torch.uint8, pin_memory=True)
     layered = {name: [None] * step.layers for name, _ in per_layer}
@@ -597,20 +600,44 @@ def stage_inputs(step, align=256):
     return dev, host
 
 
-def time_e2e(step, steps, warmup, dist_on):
+def time_e2e(step, steps, warmup, dist_on, overlap=True):
     """Steps/s through the Python API with host buffers: H2D of q, k_new, v_new, slots, lengths and
     block table from pinned memory (one staging buffer), the step, D2H of the attention output (all in
-    one CUDA graph), then a synchronize, every step."""
+    one CUDA graph), then a synchronize, every step.
+
+    overlap: the lengths, block table and layer 0's inputs are copied first; the other layers' inputs
+    follow on a side stream that only layer 1 waits for, and each layer's output is copied back on a
+    second side stream right after the layer. Kernel-to-kernel edges stay programmatic (no copy feeds a
+    later layer except layer 1's inputs), so the layers keep their overlap."""
     torch = step.torch
     dev, host = stage_inputs(step)
     hout = torch.empty(step.out.shape, dtype=step.out.dtype, pin_memory=True)
     h2d = host.numel()
     d2h = hout.numel() * hout.element_size()
+    split = step.staging_layer_off[1] if step.layers > 1 else host.numel()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
 
     def body():
-        dev.copy_(host, non_blocking=True)
-        step.step_eager()
-        hout.copy_(step.out, non_blocking=True)
+        if not overlap:
+            dev.copy_(host, non_blocking=True)
+            step.step_eager()
+            hout.copy_(step.out, non_blocking=True)
+            return
+        main = torch.cuda.current_stream()
+        s_in.wait_stream(main)
+        s_out.wait_stream(main)
+        dev[:split].copy_(host[:split], non_blocking=True)
+        with torch.cuda.stream(s_in):
+            dev[split:].copy_(host[split:], non_blocking=True)
+        for l in range(step.layers):
+            if l == 1:
+                main.wait_stream(s_in)
+            step.layer(l)
+            s_out.wait_stream(main)
+            with torch.cuda.stream(s_out):
+                hout[l].copy_(step.out[l], non_blocking=True)
+        main.wait_stream(s_in)
+        main.wait_stream(s_out)
 
     # one CUDA graph per step: the host->device copy of the step's inputs from pinned memory,
     # the layers, and the device->host copy of the output; a replay and a synchronize per step
