@@ -239,3 +239,33 @@ def test_rope_position_beyond_table_is_reported(cuda_device):
                                 run.seq_lens, torch.from_numpy(cs).to(cuda_device), run.out, geom.scale, run.ws)
     torch.cuda.synchronize()
     assert run.ws.status() == pkv.ERR_CODES["PKV_ERR_OUT_OF_BOUNDS"]
+
+
+@pytest.mark.parametrize("ranks", [2, 4, 8])
+def test_kv_head_shards_reproduce_the_full_decode(cuda_device, ranks):
+    # KV-head sharding (what a rank would hold when the KV cache is split across GPUs by KV head): shard r
+    # keeps KV heads [r 8/N, (r+1) 8/N) of every page and their query heads, and is a geometry of its own
+    # (16/N query, 8/N KV heads); each shard is an independent decode call here, on one GPU. The shards'
+    # outputs, put side by side along the heads, equal the unsharded call's and the oracle's.
+    case = W.decode_case(29, W.config_seq_lens(2), pending_append=False, poison=True)
+    full = DecodeOnDevice(case, 0, cuda_device)
+    ref = full.step().clone()
+    torch.cuda.synchronize()
+    kv_per, q_per = 8 // ranks, 16 // ranks
+    parts = []
+    for r in range(ranks):
+        kp = full.k_pages[:, r * kv_per:(r + 1) * kv_per].contiguous()
+        vp = full.v_pages[:, r * kv_per:(r + 1) * kv_per].contiguous()
+        q = full.q[:, r * q_per:(r + 1) * q_per].contiguous()
+        out = torch.full_like(q, float("nan"))
+        ws = pkv.Workspace(pkv.decode_workspace_bytes(case.batch, case.max_pages, case.num_pages, q_per, kv_per,
+                                                      128), cuda_device)
+        pkv.decode_attn(q, kp, vp, full.block_table, full.seq_lens, out, case.geom.scale, ws)
+        torch.cuda.synchronize()
+        assert ws.status() == 0
+        parts.append(out)
+    sharded = torch.cat(parts, dim=1)
+    want = oracle.decode(case.q[0], case.k_pages[0], case.v_pages[0], case.block_table, case.seq_lens,
+                         case.geom.scale)
+    assert_close(bf16_to_f64(sharded), want, f"{ranks} KV-head shards")
+    assert_close(bf16_to_f64(sharded), bf16_to_f64(ref), f"{ranks} KV-head shards vs the unsharded call")
