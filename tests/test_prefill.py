@@ -399,3 +399,37 @@ def test_mixed_step_kernel_decode_only(cuda_device):
     _, dout, kp, vp = _mixed_kernel_run(case, cuda_device)
     want_d = oracle.decode(case.dec_q[0], kp, vp, case.dec_block_table, case.dec_seq_lens, case.geom.scale)
     assert_close(bf16_to_f64(dout), want_d, "mixed kernel: decode only")
+
+
+def test_many_requests_in_one_call(cuda_device):
+    # 70 chunks (the length scan runs over three warps' worth of requests) of 1..300 rows after 0..2000
+    # cached tokens, every row against the oracle
+    rng = np.random.default_rng(70)
+    prefix = rng.integers(0, 2000, size=70)
+    qlens = rng.integers(1, 300, size=70)
+    case = W.prefill_case(70, prefix, qlens, poison=True)
+    _check(case, cuda_device, what="70 chunks")
+
+
+def test_many_requests_split_schedule(cuda_device):
+    # 40 chunks of 512 rows after 6000..9000 cached tokens: the split schedule, shares cutting items of many
+    # requests; every 13th row and the last rows of every request
+    rng = np.random.default_rng(71)
+    prefix = rng.integers(6000, 9000, size=40)
+    case = W.prefill_case(71, prefix, [512] * 40, poison=True)
+    assert split_cut_tiles(case.prefix_lens, case.q_lens, _workers(cuda_device))
+    rows = sorted({r for n in range(40) for r in range(512 * n, 512 * (n + 1), SAMPLE_STRIDE)} |
+                  {512 * n + 511 for n in range(40)})
+    _check(case, cuda_device, rows=rows, what="40 chunks, split schedule")
+
+
+def test_mixed_step_kernel_many_requests(cuda_device):
+    # 5 chunks and 64 decode requests of 1..6000 tokens (several 64-page chunks each) in one launch
+    rng = np.random.default_rng(72)
+    case = W.prefill_case(72, rng.integers(0, 3000, size=5), rng.integers(1, 700, size=5),
+                          dec_seq_lens=rng.integers(0, 6000, size=64), poison=True)
+    out, dout, kp, vp = _mixed_kernel_run(case, cuda_device)
+    want = oracle.prefill(case.q[0], kp, vp, case.block_table, case.prefix_lens, case.cu_q_lens, case.geom.scale)
+    assert_close(bf16_to_f64(out), want, "mixed kernel: 5 chunks")
+    want_d = oracle.decode(case.dec_q[0], kp, vp, case.dec_block_table, case.dec_seq_lens, case.geom.scale)
+    assert_close(bf16_to_f64(dout), want_d, "mixed kernel: 64 decode requests")
