@@ -18,9 +18,10 @@
 //    Its consumer warps take the share's pages round-robin (page f of the share
 //    goes to consumer (f - lo) mod kCons, across piece boundaries). A producer warp
 //    fills each consumer's ring of shared-memory stages with tiled TMA copies
-//    (cp.async.bulk.tensor, per page two 16-row x 64-dim boxes of the K tile and
-//    two of the V tile, 128-byte swizzle, evict-first) that complete on the
-//    stage's full barrier; consumers release stages through empty barriers.
+//    (cp.async.bulk.tensor, per page one copy of the K tile and one of the V
+//    tile, each two 16-row x 64-dim swizzled halves, evict-first) that complete
+//    on the stage's full barrier; consumers release stages through empty
+//    barriers.
 //  * Both query heads of the GQA group are computed from one K/V read, the two
 //    products of a page as warp-level bf16 tensor-core MMAs with fp32
 //    accumulation (pkv_mma.cuh): scores S^T = K Q^T with the group's rows as
@@ -77,12 +78,17 @@ namespace pkv {
 #ifndef PKV_DEC_CTAS_PER_SM
 #define PKV_DEC_CTAS_PER_SM 2
 #endif
+#ifndef PKV_DEC_ROUND_PAGES  // pages the producer issues per round
+#define PKV_DEC_ROUND_PAGES 8
+#endif
 constexpr int kCons = PKV_DEC_CONSUMERS;         // consumer warps; one more warp produces
 constexpr int kConsThreads = kCons * 32;
 constexpr int kDecThreads = kConsThreads + 32;
 constexpr int kDecRing = PKV_DEC_RING;           // stages per consumer warp
 constexpr int kDecCtasPerSm = PKV_DEC_CTAS_PER_SM;
 constexpr int kStages = kCons * kDecRing;
+constexpr int kRoundPages = PKV_DEC_ROUND_PAGES;
+static_assert(kRoundPages >= 1 && kRoundPages <= kStages, "a page's previous stage use is in an earlier round");
 static_assert(kHeadDim % kConsThreads == 0 || kConsThreads % kHeadDim == 0, "merge maps threads to head dims");
 constexpr int kDimsPerThread = kConsThreads >= kHeadDim ? 1 : kHeadDim / kConsThreads;  // in the merges
 constexpr int kStageBytes = 2 * kTileBytes;  // K tile + V tile of one (page, KV head)
@@ -338,13 +344,16 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
   // out which consumer reads the page ((f - lo) mod kCons) and which stage of
   // that consumer's ring it fills (its running page count, from the lanes
   // before it with the same consumer). The lanes then issue their own tensor
-  // copies in rounds in which every stage is filled at most once, so each
-  // stage's empty barrier is at most one phase behind the wait. Because the
-  // assignment follows the share and not the piece, round r of a chunk holds
-  // exactly its pages 12r .. 12r + 11 and waits only on pages of earlier
-  // rounds; with a piece-relative assignment a run of one-page pieces piled
-  // onto one consumer, and a round could wait on a consumer held at a piece
-  // boundary by a page of a later round (a deadlock).
+  // copies in rounds of kRoundPages consecutive pages (round r of a chunk holds
+  // its pages R r .. R r + R - 1, R <= kStages), each lane once its stage's
+  // previous use has been consumed. That previous use is the page kStages
+  // earlier in the share, issued in an earlier round, so each stage's empty
+  // barrier is at most one phase behind the wait and a round waits only on
+  // pages of earlier rounds. The assignment follows the share and not the
+  // piece: with a piece-relative one a run of one-page pieces piled onto one
+  // consumer, and a round could wait on a consumer held at a piece boundary by
+  // a page of a later round (a deadlock). Smaller rounds land a CTA's first
+  // pages sooner; one SIMT copy instruction per round amortises the issue.
   if (warp == kCons) {
     const uint64_t policy = policy_evict_first();
     const unsigned lt_mask = (1u << lane) - 1u;
@@ -379,7 +388,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
       const int k = my_base + idx;
       const int slot = c * kDecRing + k % kDecRing;
       const int use = k / kDecRing;
-      const int my_round = idx / kDecRing;
+      const int my_round = lane / kRoundPages;
       int rounds = valid ? my_round + 1 : 0;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) rounds = max(rounds, __shfl_xor_sync(kFull, rounds, o));
@@ -454,11 +463,9 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
             const int z = pid * kKVHeads + hh;  // tile of the pool
             unsigned char* dst = ring + slot * kStageBytes;
             mbar_arrive_expect_tx(&full[slot], kStageBytes);
-#pragma unroll
-            for (int x = 0; x < kHeadDim / 64; ++x) {  // 16 rows x 64 dims per box, 128-byte swizzle
-              tma_load_3d_hint(dst + x * 2048, &kmap, 64 * x, 0, z, &full[slot], policy);
-              tma_load_3d_hint(dst + kTileBytes + x * 2048, &vmap, 64 * x, 0, z, &full[slot], policy);
-            }
+            // one copy per tile: its two 16-row x 64-dim halves, 128-byte swizzled
+            tma_load_4d_hint(dst, &kmap, 0, 0, 0, z, &full[slot], policy);
+            tma_load_4d_hint(dst + kTileBytes, &vmap, 0, 0, 0, z, &full[slot], policy);
           }
         }
         __syncwarp();

@@ -363,11 +363,8 @@ __global__ void __launch_bounds__(kGenThreads) decode_generic_kernel(const __gri
       unsigned char* dst = ring + (i % S::kStages) * S::kStage;
       uint64_t* bar = &wfull[i % S::kStages];
       mbar_arrive_expect_tx(bar, S::kStage);
-#pragma unroll
-      for (int j = 0; j < D / 64; ++j) {
-        tma_load_3d(dst + j * 2048, &kmap, 64 * j, 0, z, bar);
-        tma_load_3d(dst + S::kTile + j * 2048, &vmap, 64 * j, 0, z, bar);
-      }
+      tma_load_4d(dst, &kmap, 0, 0, 0, z, bar);  // the whole K tile (its D / 64 swizzled blocks)
+      tma_load_4d(dst + S::kTile, &vmap, 0, 0, 0, z, bar);
     }
   };
   for (int i = 0; i < S::kStages && i < nw; ++i) issue(i);
@@ -574,16 +571,18 @@ int encode_page_maps(const void* k_pages, const void* v_pages, int head_dim, int
   if (tiles > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;  // tile coordinates are 32-bit
   EncodeTiledFn enc = encoder();
   if (enc == nullptr) return PKV_ERR_CUDA;
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(kPageSize),
-                              static_cast<cuuint64_t>(tiles)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * 2,
+  if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  const cuuint32_t halves = static_cast<cuuint32_t>(head_dim / 64);
+  // (dim within the half, row, half, tile): a tile's halves are 128 bytes apart inside each 2 * head_dim-byte row
+  const cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(kPageSize), halves, static_cast<cuuint64_t>(tiles)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(head_dim) * 2, 128,
                                  static_cast<cuuint64_t>(head_dim) * 2 * kPageSize};
-  const cuuint32_t box[3] = {64, kPageSize, 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
+  const cuuint32_t box[4] = {64, kPageSize, halves, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
   const void* pools[2] = {k_pages, v_pages};
   CUtensorMap* maps[2] = {kmap, vmap};
   for (int i = 0; i < 2; ++i)
-    if (enc(maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pools[i]), dims, strides, box, estr,
+    if (enc(maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(pools[i]), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return PKV_ERR_CUDA;

@@ -19,8 +19,11 @@
 
 namespace pkv {
 
-// Tensor maps of the two pools for the MMA kernels: [page * hkv + KV head][16 rows][head_dim] bf16,
-// boxes of 64 dims x 16 rows with 128-byte swizzle. PKV_ERR_UNSUPPORTED past 2^31 tiles.
+// Tensor maps of the two pools for the MMA kernels, over [page * hkv + KV head][16 rows][head_dim] bf16
+// viewed as 4-D (64 dims, 16 rows, head_dim / 64 halves, tile), the halves' stride (128 bytes) below the
+// rows' (2 * head_dim bytes). One box is a whole tile: coordinates (0, 0, 0, tile) copy it with one
+// instruction into head_dim / 64 consecutive 2 KiB blocks of 16 rows x 64 dims, 128-byte swizzled (the
+// layout swz() reads). PKV_ERR_UNSUPPORTED past 2^31 tiles.
 int encode_page_maps(const void* k_pages, const void* v_pages, int head_dim, int num_pages, int hkv, CUtensorMap* kmap,
                      CUtensorMap* vmap);
 

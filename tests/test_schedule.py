@@ -11,8 +11,10 @@ The model of one CTA of the persistent decode kernel (4 consumer warps, a
   meet at the end of every piece (a CTA barrier) before any starts the next;
 - page f goes to consumer assign(f); each consumer takes its pages in order,
   page k of consumer c in stage k % 3;
-- the producer walks the share 32 pages at a time; a page's round is its index
-  among the chunk's pages of the same consumer, divided by 3. A page is issued
+- the producer walks the share 32 pages at a time; a page's round is its
+  position in the chunk divided by the round size R (8 pages; the earlier
+  rule, a page's index among the chunk's pages of its consumer divided by 3,
+  equals R = 12). A page is issued
   once its stage's previous use has been consumed, and a round ends when all
   its pages have been issued (the warp reconverges before the next round).
 """
@@ -22,6 +24,7 @@ import pytest
 from paged_kv_decode_gb300 import workloads as W
 
 CONS, RING, CHUNK, PAGE, HKV = 4, 3, 32, 16, 8
+ROUND_SIZES = (1, 4, 8, 12)  # the shipped round size (8), the earlier one (12) and others measured
 
 
 def shares(seq_lens, grid):
@@ -61,7 +64,7 @@ def assign_piece(lo, hi, seg_starts):
     return out
 
 
-def simulate(lo, hi, seg_starts, assign):
+def simulate(lo, hi, seg_starts, assign, round_pages=CONS * RING):
     n = hi - lo
     piece = piece_index(lo, hi, seg_starts)
     cons = assign(lo, hi, seg_starts)
@@ -74,7 +77,9 @@ def simulate(lo, hi, seg_starts, assign):
     for m in range(0, n, CHUNK):
         per, rnd = [0] * CONS, {}
         for i in range(m, min(m + CHUNK, n)):
-            rnd.setdefault(per[cons[i]] // RING, []).append(i)
+            # round_pages None: the earlier per-consumer rule (index among the consumer's pages // RING)
+            r = per[cons[i]] // RING if round_pages is None else (i - m) // round_pages
+            rnd.setdefault(r, []).append(i)
             per[cons[i]] += 1
         rounds += [rnd[r] for r in sorted(rnd)]
     round_of = {i: r for r, lst in enumerate(rounds) for i in lst}
@@ -115,9 +120,9 @@ def simulate(lo, hi, seg_starts, assign):
             return all(done)
 
 
-def all_ctas_finish(seq_lens, assign, grid=304):
+def all_ctas_finish(seq_lens, assign, grid=304, round_pages=CONS * RING):
     sh, segs = shares(seq_lens, grid)
-    return all(simulate(lo, hi, segs, assign) for lo, hi in sh)
+    return all(simulate(lo, hi, segs, assign, round_pages) for lo, hi in sh)
 
 
 MIXES = {
@@ -132,24 +137,41 @@ MIXES = {
 }
 
 
+@pytest.mark.parametrize("round_pages", ROUND_SIZES)
 @pytest.mark.parametrize("name", sorted(MIXES))
-def test_share_relative_schedule_never_deadlocks(name):
-    assert all_ctas_finish(MIXES[name], assign_share)
+def test_share_relative_schedule_never_deadlocks(name, round_pages):
+    assert all_ctas_finish(MIXES[name], assign_share, round_pages=round_pages)
 
 
+def test_round_rule_by_position_equals_the_per_consumer_rule():
+    # under the share-relative assignment, position // 12 in a chunk is the page's index among the
+    # chunk's pages of its consumer, divided by 3 (the rule the kernel used before round sizes)
+    for pos in range(CHUNK):
+        assert pos // (CONS * RING) == (pos // CONS) // RING
+
+
+@pytest.mark.parametrize("round_pages", ROUND_SIZES)
 @pytest.mark.parametrize("grid", [2 * 148, 2 * 152, 64, 7])
-def test_share_relative_schedule_random_mixes(grid):
+def test_share_relative_schedule_random_mixes(grid, round_pages):
     rng = np.random.default_rng(grid)
     for _ in range(6):
         b = int(rng.integers(1, 40))
         lens = rng.choice([1, 5, 16, 17, 40, 300, 2000, 12000], size=b)
-        assert all_ctas_finish(lens, assign_share, grid=grid), list(lens)
+        assert all_ctas_finish(lens, assign_share, grid=grid, round_pages=round_pages), list(lens)
+
+
+@pytest.mark.parametrize("round_pages", [13, 16, 32])
+def test_rounds_larger_than_the_ring_break_the_one_phase_rule(round_pages):
+    # a round of more than 12 pages would hold a page and its stage's previous use together;
+    # the kernel's static_assert keeps round sizes at most 12
+    with pytest.raises(AssertionError):
+        all_ctas_finish(MIXES["bs16"], assign_share, round_pages=round_pages)
 
 
 def test_piece_relative_schedule_deadlocks_on_one_page_runs():
     # the rule the share-relative assignment replaced: eight one-page pieces
     # pile onto consumer 0 and the producer's second round waits on consumers
     # that are held at a piece boundary behind it
-    assert not all_ctas_finish(MIXES["short_then_long"], assign_piece)
-    assert all_ctas_finish(MIXES["short_then_long"], assign_share)
+    assert not all_ctas_finish(MIXES["short_then_long"], assign_piece, round_pages=None)
+    assert all_ctas_finish(MIXES["short_then_long"], assign_share, round_pages=None)
 
