@@ -48,16 +48,18 @@ WORKLOAD = ("qwen3-0.6b decode step: 28 layers x bs16, 16q/8kv heads, d128, page
 
 # DRAM traffic of one decode launch on this workload's per-layer pool, from one ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the decode kernel source it was
-# measured on (sha256 prefix of csrc/decode.cu); any other source reports null.
-NCU_DECODE_TRAFFIC = {"856c1d16ad501ffb": 107_398_400 + 2_418_688}
+# measured on (sha256 prefix of csrc/decode_kernel.cuh followed by csrc/pkv_mma.cuh); any other source
+# reports null.
+NCU_DECODE_TRAFFIC = {}
 
 
 def _decode_traffic():
     import hashlib
 
-    src = os.path.join(ROOT, "paged_kv_decode_gb300", "csrc", "decode.cu")
-    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    return NCU_DECODE_TRAFFIC.get(h)
+    h = hashlib.sha256()
+    for f in ("decode_kernel.cuh", "pkv_mma.cuh"):
+        h.update(open(os.path.join(ROOT, "paged_kv_decode_gb300", "csrc", f), "rb").read())
+    return NCU_DECODE_TRAFFIC.get(h.hexdigest()[:16])
 
 
 def _peaks():
@@ -413,8 +415,8 @@ def time_launches(torch, fn, reps):
 
 
 class GenericDecodeStep:
-    """Decode attention over `layers` distinct pools of another cache geometry: the generic decode
-    path (1 to 8 query heads per KV head, head_dim 64 or 128). fused: each layer is one fused
+    """Decode attention over `layers` distinct pools of another cache geometry: the decode kernel with
+    run-time head counts (1 to 8 query heads per KV head, head_dim 64 or 128). fused: each layer is one fused
     append + decode launch with early prefetch (the decode step); otherwise decode attention alone."""
 
     def __init__(self, device, seq_lens, geom, layers: int, seed: int, fused: bool = False):
@@ -455,7 +457,7 @@ class GenericDecodeStep:
 
 
 def measure_shapes(device, hbm, layers=8, steps=30, warmup=5):
-    """Other decoder geometries on the generic decode path, bs16 U{300..3000} (one case a single
+    """Other decoder geometries (run-time head counts), bs16 U{300..3000} (one case a single
     40000-token request): per-layer time and bandwidth (the pages name these backbones without head
     counts; the shapes are examples)."""
     from paged_kv_decode_gb300 import workloads as W
@@ -485,7 +487,7 @@ def measure_shapes(device, hbm, layers=8, steps=30, warmup=5):
 
 
 def run_geometry(args, device):
-    """One generic-path geometry alone (bs16, decode attention only, `layers` pools in a graph)."""
+    """One other geometry alone (bs16, decode attention only, `layers` pools in a graph)."""
     from paged_kv_decode_gb300 import workloads as W
 
     q, kv, d = (int(x) for x in args.geometry.split(","))
@@ -497,7 +499,7 @@ def run_geometry(args, device):
     hbm = _peaks()[0]
     gbps = st.decode_bytes() / (us * 1e-6) / 1e9
     what = "fused append + decode (early prefetch)" if args.geometry_fused else "decode attention"
-    print(json.dumps({"workload": f"generic {what}, {q}q/{kv}kv/d{d}, bs16 U{{300..3000}}, "
+    print(json.dumps({"workload": f"{what}, {q}q/{kv}kv/d{d}, bs16 U{{300..3000}}, "
                                   f"{args.layers} layers per graph", "us_per_layer": us, "gbps": gbps,
                       "frac_of_measured_hbm": gbps / hbm, "bytes_per_layer": st.decode_bytes(),
                       "steps": args.steps, "warmup": args.warmup}), flush=True)
@@ -764,7 +766,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the 40k-context and prefill measurements")
     ap.add_argument("--geometry", default=None, metavar="Q,KV,D",
-                    help="time only the generic decode path on that cache geometry (bs16 U{300..3000}) and exit")
+                    help="time only the decode path on that cache geometry (bs16 U{300..3000}) and exit")
     ap.add_argument("--prefill-geometry", default=None, metavar="Q,KV,D",
                     help="time only chunked prefill on that cache geometry (4096 rows after 0/8192/32768) and exit")
     ap.add_argument("--geometry-fused", action="store_true",
@@ -930,9 +932,9 @@ def main():
             W.config_seq_lens(5), 5 + rank,
             "CFG-paired decode: 28 layers x bs32 (16 conditional U{1000..8000} + 16 companions U{8..64} + g)")
         extra["other_geometries_bs16"] = {
-            "workload": "generic path, bs16 U{300..3000} (the _40k case: one 40000-token request), 8 layers per "
-                        "graph: decode attention alone, and (fused_early_*) one fused append + decode launch per "
-                        "layer with early prefetch",
+            "workload": "other geometries (run-time head counts), bs16 U{300..3000} (the _40k case: one "
+                        "40000-token request), 8 layers per graph: decode attention alone, and (fused_early_*) one "
+                        "fused append + decode launch per layer with early prefetch",
             **measure_shapes(device, hbm)}
         extra["chunked_prefill"] = {
             "workload": "4096-token chunk (1 request) after 0/8192/32768 cached tokens; mixed step adds the chunk "

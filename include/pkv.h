@@ -37,9 +37,9 @@
  *    pkv_decode_append_rope_attn and pkv_prefill_chunk_attn also take
  *    page_size = 16, head_dim 64 or 128,
  *    any num_kv_heads and num_q_heads = G * num_kv_heads with G from 1 to 8
- *    (other decoder backbones; decode runs a generic split-KV kernel, early
- *    prefetch included; prefill runs its tensor-core kernel on pairs of
- *    query heads).
+ *    (other decoder backbones; decode runs the same persistent split-KV
+ *    kernel with the head counts read at run time, early prefetch included;
+ *    prefill runs its tensor-core kernel on pairs of query heads).
  *  - Anything else returns PKV_ERR_UNSUPPORTED.
  *
  * Conventions for every entry point:

@@ -1,1051 +1,111 @@
-// decode.cu -- batched decode attention over the paged KV cache (split-KV).
-//
-// Source of the operation: PagedAttention decoding in the LLM engine
-// ("FunASR vLLM Inference Engine Guide", section 2 "vLLM Engine Architecture");
-// decode is where long-audio serving spends its time ("Optimizing ASR for
-// 90-minute multi-speaker audio", section "Time spent: profiling").
-//
-// The op reads every cached K/V row once and does ~1 FMA per byte, so it is
-// bound by HBM bandwidth. Design:
-//
-//  * Work is the list of (request, KV head, page) triples, ordered by request,
-//    then KV head, then page. The kernel is persistent: gridDim.x CTAs (the SM
-//    count times the CTAs resident per SM) each take an equal contiguous share
-//    of that list, computed on the device from seq_lens, so the grid depends
-//    only on host-known sizes (CUDA-graph friendly) and every CTA streams the
-//    same number of pages whatever the length mix.
-//  * A CTA's share is cut into pieces, one per (request, KV head) it touches.
-//    Its consumer warps take the share's pages round-robin (page f of the share
-//    goes to consumer (f - lo) mod kCons, across piece boundaries). A producer warp
-//    fills each consumer's ring of shared-memory stages with tiled TMA copies
-//    (cp.async.bulk.tensor, per page one copy of the K tile and one of the V
-//    tile, each two 16-row x 64-dim swizzled halves, evict-first) that complete
-//    on the stage's full barrier; consumers release stages through empty
-//    barriers.
-//  * Both query heads of the GQA group are computed from one K/V read, the two
-//    products of a page as warp-level bf16 tensor-core MMAs with fp32
-//    accumulation (pkv_mma.cuh): scores S^T = K Q^T with the group's rows as
-//    two of the B operand's 8 columns, softmax online in registers in the log2
-//    domain (scale * log2 e applied to the fp32 scores), p rounded to bf16 for
-//    the value product O^T += V^T P^T. Tokens past seq_len in the last page are
-//    masked in the scores and in the value operand's registers, so unused slots
-//    may hold anything, NaN included.
-//  * Optional fused append: the producer lane that copies a request's last
-//    page first writes the request's new K/V row for that head into it
-//    (generic stores, then a proxy fence so its own tensor copy sees them). With
-//    a cos/sin table the whole producer warp writes the row instead, rotating
-//    the key (rotary position embedding at the new token's position, pairs
-//    (i, i + 64), fp32, rounded to bf16), and each piece's query rows are
-//    rotated the same way after they are staged (then rounded to bf16 as the
-//    MMA operand).
-//  * The query rows of the next piece are copied into shared memory (cp.async)
-//    while the current piece streams, so a piece boundary costs no round trip.
-//  * At the end of a piece the warps merge through shared memory. A piece that
-//    covers its whole (request, KV head) writes the bf16 output. Otherwise it
-//    writes a partial record (m, l, o). Only a share's first and last piece
-//    can be split, and a pair's holders are consecutive CTAs. The records are
-//    merged (log-sum-exp, in an order fixed by the pair alone) in one of two
-//    ways, each its own instantiation, chosen by the expected number of
-//    holders per pair (grid size over batch x KV heads):
-//     - Counted, for few pairs over many CTAs (one long request): fp32
-//       records; after its last piece a CTA bumps the pairs' counters (one
-//       fence, one round trip) and the CTA that completes a count stages the
-//       records in its drained stage ring (cp.async, one round trip), merges
-//       them and resets the counter.
-//     - Polled, for many pairs over few CTAs each: records of tagged 32-bit
-//       words -- o rounded to 16 significant bits, m and l exact as the sum of
-//       two such values, a tag in every word's low byte -- written with no
-//       fence or atomic. The CTA holding a pair's last page (necessarily its
-//       first piece, begun by lower-numbered CTAs) reads the holders' records
-//       once its own share is done, again until every word carries the tag,
-//       merges them and clears the records for the next call.
-#include <math_constants.h>
-
-#include "pkv_device.cuh"
-#include "pkv_kernels.h"
-#include "pkv_mma.cuh"
-#include "pkv_tc.cuh"
+// decode.cu -- host side of the decode attention kernel (decode_kernel.cuh):
+// the geometry dispatch, the workspace size and the Qwen3 decoder's
+// instantiation (16 query / 8 KV heads of dimension 128, head counts fixed at
+// compile time). The instantiations for run-time head counts are built in
+// decode_d64.cu and decode_d128.cu, so that the three translation units
+// compile in parallel.
+#include "decode_kernel.cuh"
 
 namespace pkv {
 
-// Launch shape (compile-time; the defaults are the tuned configuration).
-#ifndef PKV_DEC_CONSUMERS
-#define PKV_DEC_CONSUMERS 4
-#endif
-#ifndef PKV_DEC_RING
-#define PKV_DEC_RING 3
-#endif
-#ifndef PKV_DEC_CTAS_PER_SM
-#define PKV_DEC_CTAS_PER_SM 2
-#endif
-#ifndef PKV_DEC_ROUND_PAGES  // pages the producer issues per round
-#define PKV_DEC_ROUND_PAGES 8
-#endif
-constexpr int kCons = PKV_DEC_CONSUMERS;         // consumer warps; one more warp produces
-constexpr int kConsThreads = kCons * 32;
-constexpr int kDecThreads = kConsThreads + 32;
-constexpr int kDecRing = PKV_DEC_RING;           // stages per consumer warp
-constexpr int kDecCtasPerSm = PKV_DEC_CTAS_PER_SM;
-constexpr int kStages = kCons * kDecRing;
-constexpr int kRoundPages = PKV_DEC_ROUND_PAGES;
-static_assert(kRoundPages >= 1 && kRoundPages <= kStages, "a page's previous stage use is in an earlier round");
-static_assert(kHeadDim % kConsThreads == 0 || kConsThreads % kHeadDim == 0, "merge maps threads to head dims");
-constexpr int kDimsPerThread = kConsThreads >= kHeadDim ? 1 : kHeadDim / kConsThreads;  // in the merges
-constexpr int kStageBytes = 2 * kTileBytes;  // K tile + V tile of one (page, KV head)
-constexpr int kRec = kHeadDim + 4;           // floats per query-head record: m, l, pad, pad, o[128]
-constexpr int kPieceFloats = kGroup * kRec;  // a partial record of one piece (both query heads)
-constexpr int kMaxDecodeBatch = 1024;
-constexpr int kMaxGrid = 2048;               // partial-record slots are sized for this many CTAs
-constexpr int kMinShare = 8;                 // pages a CTA's share holds at least (when the step has that many)
-constexpr unsigned kFull = 0xffffffffu;
-
-constexpr int kSmemRing = kStages * kStageBytes;
-constexpr int kSmemBars = 2 * kStages * 8;                 // full + empty barrier per stage
-constexpr int kMergeFloats = kCons * kPieceFloats;         // one record per consumer warp
-constexpr int kSmemMerge = kMergeFloats * 4;
-constexpr int kQBufBytes = kGroup * kRowBytes;             // query rows of one (request, KV head), both heads
-constexpr int kSmemQ = 2 * kQBufBytes;                     // this piece's rows and the next piece's
-constexpr int kCsBytes = kHeadDim * 4;                     // one cos/sin table row (fp32 cos[64], sin[64])
-constexpr int kSmemCs = 2 * kCsBytes;                      // rows for this piece's and the next piece's position
-constexpr int kSmemMisc = 16;                              // flag words
-constexpr int kSmemAlign = 1024;                           // the ring starts on a 1024-byte boundary (swizzle atoms)
-constexpr int kSmemFixed = kSmemAlign + kSmemRing + kSmemBars + kSmemMerge + kSmemQ + kSmemCs + kSmemMisc;
-constexpr int kPieceBytes = kPieceFloats * 4;
-constexpr int kMergeCap = kSmemRing / kPieceBytes;         // records staged per batch of a counted merge
-constexpr int kSplitWords = kGroup * kHeadDim + 8;         // tagged words of a polled record: o[2][128], then
-                                                           // m_hi, m_lo, l_hi, l_lo of head 0, then of head 1
-constexpr int kSplitBytes = kSplitWords * 4;
-constexpr uint32_t kTag = 0xa5u;                           // low byte of a word written by this call
-constexpr int kMergeBatch = 8;                             // records a warp has in flight in a polled merge
-constexpr int kPollMax = 24;                               // polled merge up to this many holders per pair
-static_assert(kSplitBytes % 16 == 0, "16-byte loads and clears of a record");
-static_assert((kSmemRing + kSmemBars) % 16 == 0 && kSmemMerge % 16 == 0 && kPieceBytes % 16 == 0, "alignment");
-static_assert(kQBufBytes == 32 * 16, "one 16-byte chunk of a group's query rows per lane");
-static_assert(kCsBytes == 32 * 16, "one 16-byte chunk of a cos/sin row per lane");
-
-static size_t decode_smem_bytes(int batch) { return kSmemFixed + static_cast<size_t>(2 * batch + 1) * 4; }
-
 int decode_max_batch() { return kMaxDecodeBatch; }
 
-struct DecodeArgs {
-  const __nv_bfloat16* q;
-  const __nv_bfloat16* k_new;  // optional fused append: [batch][kv heads][head_dim], nullptr = none
-  const __nv_bfloat16* v_new;
-  const __nv_bfloat16* k_pages;
-  const __nv_bfloat16* v_pages;
-  const int* block_table;
-  const int* seq_lens;
-  __nv_bfloat16* out;
-  const float* rope;  // optional cos/sin table [rope_max_pos][128] fp32 (rotary embedding), nullptr = none
-  int rope_max_pos;
-  float qscale;       // scale * log2(e)
-  int early;     // prefetch before the grid dependency (caller guarantees the predecessor leaves
-                 // pools, block table and lengths alone)
-  int batch;
-  int max_pages;
-  int num_pages;
-  int* status;
-  int* counters;       // [batch * kKVHeads], zero between calls (counted merge)
-  float* partials;     // [2 * gridDim.x][kPieceFloats] (counted merge)
-  uint32_t* tagged;    // [2 * gridDim.x][kSplitWords], no word tagged between calls (polled merge)
-};
+namespace {
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-// A piece: pages [p0, p1) of KV head h of request b; flattened indices [fstart, fend).
-struct Piece {
-  int b, h, np, p0, p1;
-  long long fstart, fend;
-};
-
-// Piece of the CTA share [.., hi) that starts at flattened index f.
-// pref[b] = page-head triples of requests before b (pref[batch] = total).
-__device__ __forceinline__ bool find_piece(long long f, long long hi, const int* pref, int batch, Piece& pc) {
-  if (f >= hi) return false;
-  int lo_b = 0, hi_b = batch - 1;
-  while (lo_b < hi_b) {
-    const int mid = (lo_b + hi_b + 1) >> 1;
-    if (pref[mid] <= f) lo_b = mid; else hi_b = mid - 1;
+EncodeTiledFn encoder() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
   }
-  pc.b = lo_b;
-  pc.np = (pref[lo_b + 1] - pref[lo_b]) / kKVHeads;
-  const long long off = f - pref[lo_b];
-  pc.h = static_cast<int>(off / pc.np);
-  pc.p0 = static_cast<int>(off % pc.np);
-  const long long p1 = pc.p0 + (hi - f);
-  pc.p1 = static_cast<int>(p1 < pc.np ? p1 : pc.np);
-  pc.fstart = f;
-  pc.fend = f + (pc.p1 - pc.p0);
-  return true;
+  return fn;
+}
+}  // namespace
+
+int encode_page_maps(const void* k_pages, const void* v_pages, int head_dim, int num_pages, int hkv, CUtensorMap* kmap,
+                     CUtensorMap* vmap) {
+  const long long tiles = static_cast<long long>(num_pages) * hkv;
+  if (tiles > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;  // tile coordinates are 32-bit
+  if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  EncodeTiledFn enc = encoder();
+  if (enc == nullptr) return PKV_ERR_CUDA;
+  const cuuint32_t halves = static_cast<cuuint32_t>(head_dim / 64);
+  // (dim within the half, row, half, tile): a tile's halves are 128 bytes apart inside each 2 * head_dim-byte row
+  const cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(kPageSize), halves, static_cast<cuuint64_t>(tiles)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(head_dim) * 2, 128,
+                                 static_cast<cuuint64_t>(head_dim) * 2 * kPageSize};
+  const cuuint32_t box[4] = {64, kPageSize, halves, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const void* pools[2] = {k_pages, v_pages};
+  CUtensorMap* maps[2] = {kmap, vmap};
+  for (int i = 0; i < 2; ++i)
+    if (enc(maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(pools[i]), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return PKV_ERR_CUDA;
+  return PKV_OK;
 }
 
-// CTA whose share [lo(c), lo(c+1)) contains flattened index f, with lo(c) = c * T / G.
-__device__ __forceinline__ int cta_of(long long f, long long T, int G) {
-  return static_cast<int>(((f + 1) * G + T - 1) / T - 1);
-}
-__device__ __forceinline__ long long share_lo(int c, long long T, int G) { return static_cast<long long>(c) * T / G; }
+// The kernel's group for g query heads per KV head: the next of 1, 2, 4, 8.
+static int group_pad(int g) { return g <= 1 ? 1 : g <= 2 ? 2 : g <= 4 ? 4 : 8; }
 
-// Polled records are 32-bit words: an fp32 value rounded to nearest (even) at
-// 15 mantissa bits, with the tag in the freed low byte. Each word is one
-// single-copy-atomic access, so a reader that sees the tag sees the value,
-// without a fence on the writer's side; a cleared word (zero) carries no tag.
-__device__ __forceinline__ uint32_t tag_word(float v) {
-  const uint32_t u = __float_as_uint(v);
-  if ((u & 0x7fffffffu) > 0x7f800000u) return 0x7fffff00u | kTag;  // NaN stays NaN
-  return ((u + 0x7fu + ((u >> 8) & 1u)) & 0xffffff00u) | kTag;
-}
-__device__ __forceinline__ float untag(uint32_t w) { return __uint_as_float(w & 0xffffff00u); }
-// v = hi + lo with hi and lo both 24-bit floats: exact for every finite fp32 v
-__device__ __forceinline__ void tag_split(float v, uint32_t& hi, uint32_t& lo) {
-  hi = tag_word(v);
-  lo = tag_word(v - untag(hi));
-}
-__device__ __forceinline__ void st_word(uint32_t* p, uint32_t w) {
-  asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(w) : "memory");
-}
-__device__ __forceinline__ uint4 ld_words4(const uint32_t* p) {
-  uint4 r;
-  asm volatile("ld.relaxed.gpu.global.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p)
-               : "memory");
-  return r;
-}
-__device__ __forceinline__ uint32_t ld_word(const uint32_t* p) {
-  uint32_t r;
-  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(r) : "l"(p) : "memory");
-  return r;
-}
-__device__ __forceinline__ bool tagged(uint32_t w) { return (w & 0xffu) == kTag; }
-
-__device__ __forceinline__ void consumer_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsThreads) : "memory");
+static bool fixed_geometry(int hq, int hkv, int head_dim) {
+  return hq == kQHeads && hkv == kKVHeads && head_dim == kHeadDim;
 }
 
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+bool decode_supported(int num_q_heads, int num_kv_heads, int head_dim, int page_size) {
+  if (num_kv_heads < 1 || num_kv_heads > 65535 || page_size != kPageSize) return false;
+  if (num_q_heads % num_kv_heads != 0) return false;
+  const int g = num_q_heads / num_kv_heads;
+  return g >= 1 && g <= 8 && (head_dim == 64 || head_dim == 128);
 }
 
-// Request b holding flattened index f: the largest b with pref[b] <= f.
-__device__ __forceinline__ int request_of(long long f, const int* pref, int batch) {
-  int lo_b = 0, hi_b = batch - 1;
-  while (lo_b < hi_b) {
-    const int mid = (lo_b + hi_b + 1) >> 1;
-    if (pref[mid] <= f) lo_b = mid; else hi_b = mid - 1;
-  }
-  return lo_b;
-}
-
-// kFused: a.k_new / a.v_new are given (fused append); kRope: a.rope is given too;
-// kPolled: the polled merge, else the counted one. Each combination is its own instantiation, so a path carries no code (and no
-// registers) for the others.
-template <bool kFused, bool kRope, bool kPolled>
-__global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(const __grid_constant__ CUtensorMap kmap,
-                                                                             const __grid_constant__ CUtensorMap vmap,
-                                                                             const DecodeArgs a) {
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  unsigned char* smem = smem_raw + ((kSmemAlign - (smem_u32(smem_raw) & (kSmemAlign - 1))) & (kSmemAlign - 1));
-  unsigned char* ring = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kSmemRing);
-  uint64_t* empty = full + kStages;
-  float* merge = reinterpret_cast<float*>(smem + kSmemRing + kSmemBars);
-  unsigned char* qbuf = reinterpret_cast<unsigned char*>(merge + kMergeFloats);
-  unsigned char* csbuf = qbuf + kSmemQ;
-  int* flag = reinterpret_cast<int*>(csbuf + kSmemCs);  // [0..1] merge flags, [2] a wait failed
-  int* pref = flag + kSmemMisc / 4;
-  int* sl = pref + a.batch + 1;
-
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5;
-  const int lane = tid & 31;
-  const int batch = a.batch;
-  if (tid == kConsThreads) {  // the producer's first lane: descriptors before its first copies
-    prefetch_tensormap(&kmap);
-    prefetch_tensormap(&vmap);
-  }
-
-  if (tid < kStages) {
-    mbar_init(&full[tid], 1);
-    mbar_init(&empty[tid], 1);
-  }
-  if (tid == kStages) flag[2] = 0;
-  // Every argument buffer may come from the previous kernel in the stream, so
-  // the kernel waits for it before touching them -- except in early mode, where
-  // the caller guarantees that the predecessor writes neither the pools nor the
-  // block table nor the lengths: then the length scan, the share decoding and
-  // the first page copies overlap the predecessor's tail, and each warp waits
-  // only before it reads q / k_new / v_new or writes anything. Dependents are
-  // released only after this grid's own wait, so the kernel two launches back
-  // has always completed when a successor starts early.
-  if (!a.early) {
-    grid_dependency_wait();
-    allow_dependents();
-  }
-
-  // seq lens (clamped) and the exclusive prefix of (KV head, page) pairs per request
-  if (warp == 0) {
-    int carry = 0;
-    const int cap = a.max_pages * kPageSize;
-    for (int base = 0; base < batch; base += 32) {
-      const int b = base + lane;
-      int s = 0;
-      if (b < batch) {
-        s = __ldg(a.seq_lens + b);
-        if (s < 0 || s > cap) {
-          set_status(a.status, PKV_ERR_OUT_OF_BOUNDS);
-          s = s < 0 ? 0 : cap;
-        }
-        sl[b] = s;
-      }
-      const int v = ((s + kPageSize - 1) / kPageSize) * kKVHeads;
-      int x = v;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(kFull, x, o);
-        if (lane >= o) x += y;
-      }
-      if (b < batch) pref[b] = carry + x - v;
-      carry += __shfl_sync(kFull, x, 31);
-    }
-    if (lane == 0) pref[batch] = carry;
-  }
-  fence_barrier_init();
-  __syncthreads();
-
-  // Only min(gridDim.x, T / 8) CTAs (at least one) take a share, so that every
-  // share holds at least 8 pages (a tiny step is not spread so thin that its
-  // merges dominate) and the CTAs between the first and last holder of a
-  // (request, KV head) all hold a piece of it.
-  const long long T = pref[batch];
-  const long long g_want = T / kMinShare > 0 ? T / kMinShare : 1;
-  const int G = static_cast<int>(g_want < gridDim.x ? g_want : gridDim.x);
-  // zero output rows of empty requests (graph-bucket padding): CTA c clears rows
-  // c, c + gridDim.x, ...; in early mode only after the grid dependency
-  auto zero_empty_rows = [&](int first_thread, int nthreads) {
-    for (int b = blockIdx.x; b < batch; b += gridDim.x) {
-      if (sl[b] == 0) {
-        uint4* o = reinterpret_cast<uint4*>(a.out + static_cast<size_t>(b) * kQHeads * kHeadDim);
-        for (int i = tid - first_thread; i < kQHeads * kHeadDim / 8; i += nthreads) o[i] = make_uint4(0, 0, 0, 0);
-      }
-    }
-  };
-  if (static_cast<int>(blockIdx.x) >= G) {
-    if (a.early) {
-      grid_dependency_wait();
-      allow_dependents();
-    }
-    zero_empty_rows(0, kDecThreads);
-    return;
-  }
-  const long long lo = share_lo(blockIdx.x, T, G);
-  const long long hi = share_lo(blockIdx.x + 1, T, G);
-
-  // ============================================================== producer warp
-  // Walks the share 32 flattened indices at a time, one per lane: each lane
-  // decodes its (request, KV head, page), loads the block-table entry, and works
-  // out which consumer reads the page ((f - lo) mod kCons) and which stage of
-  // that consumer's ring it fills (its running page count, from the lanes
-  // before it with the same consumer). The lanes then issue their own tensor
-  // copies in rounds of kRoundPages consecutive pages (round r of a chunk holds
-  // its pages R r .. R r + R - 1, R <= kStages), each lane once its stage's
-  // previous use has been consumed. That previous use is the page kStages
-  // earlier in the share, issued in an earlier round, so each stage's empty
-  // barrier is at most one phase behind the wait and a round waits only on
-  // pages of earlier rounds. The assignment follows the share and not the
-  // piece: with a piece-relative one a run of one-page pieces piled onto one
-  // consumer, and a round could wait on a consumer held at a piece boundary by
-  // a page of a later round (a deadlock). Smaller rounds land a CTA's first
-  // pages sooner; one SIMT copy instruction per round amortises the issue.
-  if (warp == kCons) {
-    const uint64_t policy = policy_evict_first();
-    const unsigned lt_mask = (1u << lane) - 1u;
-    int base[kCons];  // pages handed to each consumer before this chunk
-#pragma unroll
-    for (int c = 0; c < kCons; ++c) base[c] = 0;
-    bool pfail = false;
-    bool waited = !a.early;
-    for (long long f0 = lo; f0 < hi && !pfail; f0 += 32) {
-      const long long f = f0 + lane;
-      const bool valid = f < hi;
-      int hh = 0, id = 0, c = 0, wslot = -1, bb = 0;
-      if (valid) {
-        const int b = request_of(f, pref, batch);
-        const int np = (pref[b + 1] - pref[b]) / kKVHeads;
-        const int off = static_cast<int>(f - pref[b]);
-        hh = off / np;
-        const int p = off % np;
-        c = static_cast<int>((f - lo) % kCons);
-        bb = b;
-        id = __ldg(a.block_table + static_cast<size_t>(b) * a.max_pages + p);
-        if (kFused && p == np - 1) wslot = (sl[b] - 1) % kPageSize;  // the new token's slot
-      }
-      const unsigned same = __match_any_sync(kFull, valid ? c : -1);
-      const int idx = __popc(same & lt_mask);  // earlier lanes of this chunk feeding the same consumer
-      int my_base = 0;
-#pragma unroll
-      for (int cc = 0; cc < kCons; ++cc) {
-        if (cc == c) my_base = base[cc];
-        base[cc] += __popc(__ballot_sync(kFull, valid && c == cc));
-      }
-      const int k = my_base + idx;
-      const int slot = c * kDecRing + k % kDecRing;
-      const int use = k / kDecRing;
-      const int my_round = lane / kRoundPages;
-      int rounds = valid ? my_round + 1 : 0;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) rounds = max(rounds, __shfl_xor_sync(kFull, rounds, o));
-      if (kFused && !waited && __any_sync(kFull, wslot >= 0)) {  // new rows come from the predecessor
-        grid_dependency_wait();
-        allow_dependents();
-        waited = true;
-      }
-      if (kRope) {
-        // Fused append with the rotary embedding, by the whole warp: every page of this
-        // chunk that holds its request's new token gets the token's rotated K row and its V
-        // row for that head before any lane copies a page. Lanes take key pairs (i, i + 64),
-        // i = lane and lane + 32, rotated in fp32 as y1 = fma(x1, c, -(x2 s)),
-        // y2 = fma(x2, c, x1 s) with each product rounded first, then rounded to bf16.
-        unsigned amask = __ballot_sync(kFull, valid && wslot >= 0 && id >= 0 && id < a.num_pages);
-        if (amask != 0u) {
-          while (amask != 0u) {
-            const int src = __ffs(amask) - 1;
-            amask &= amask - 1u;
-            const int rb = __shfl_sync(kFull, bb, src), rh = __shfl_sync(kFull, hh, src);
-            const int rpid = __shfl_sync(kFull, id, src), rslot = __shfl_sync(kFull, wslot, src);
-            const size_t row = ((static_cast<size_t>(rpid) * kKVHeads + rh) * kPageSize + rslot) * kHeadDim;
-            const size_t srow = (static_cast<size_t>(rb) * kKVHeads + rh) * kHeadDim;
-            __nv_bfloat16* kd = const_cast<__nv_bfloat16*>(a.k_pages) + row;
-            int pos = sl[rb] - 1;
-            if (pos >= a.rope_max_pos) {  // past the table: reported, clamped to its last row
-              if (lane == 0) set_status(a.status, PKV_ERR_OUT_OF_BOUNDS);
-              pos = a.rope_max_pos - 1;
-            }
-            const float* cs = a.rope + static_cast<size_t>(pos) * kHeadDim;
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
-              const int i = lane + 32 * t;
-              const float x1 = __bfloat162float(a.k_new[srow + i]);
-              const float x2 = __bfloat162float(a.k_new[srow + i + kHeadDim / 2]);
-              const float cc = __ldg(cs + i), sn = __ldg(cs + kHeadDim / 2 + i);
-              kd[i] = __float2bfloat16_rn(__fmaf_rn(x1, cc, -__fmul_rn(x2, sn)));
-              kd[i + kHeadDim / 2] = __float2bfloat16_rn(__fmaf_rn(x2, cc, __fmul_rn(x1, sn)));
-            }
-            if (lane < kRowBytes / 16)
-              reinterpret_cast<uint4*>(const_cast<__nv_bfloat16*>(a.v_pages) + row)[lane] =
-                  __ldg(reinterpret_cast<const uint4*>(a.v_new + srow) + lane);
-          }
-          fence_proxy_async_global();  // this lane's row stores before the warp's tensor copies
-          __syncwarp();
-        }
-      }
-      for (int r = 0; r < rounds; ++r) {
-        if (valid && my_round == r && !pfail) {
-          if (use > 0 && !mbar_wait_bounded(&empty[slot], static_cast<uint32_t>(use - 1) & 1u)) {
-            set_status(a.status, PKV_ERR_DEVICE_TIMEOUT);
-            pfail = true;
-          } else {
-            const bool id_ok = id >= 0 && id < a.num_pages;
-            if (!id_ok) set_status(a.status, PKV_ERR_OUT_OF_BOUNDS);
-            const int pid = id_ok ? id : 0;
-            if (kFused && !kRope && wslot >= 0 && id_ok) {
-              // fused append: this page holds the request's new token; write its K and V rows
-              // for this head, then order the writes before this lane's tensor copy of the page
-              const uint4* ks = reinterpret_cast<const uint4*>(a.k_new + (static_cast<size_t>(bb) * kKVHeads + hh) * kHeadDim);
-              const uint4* vs = reinterpret_cast<const uint4*>(a.v_new + (static_cast<size_t>(bb) * kKVHeads + hh) * kHeadDim);
-              const size_t row = ((static_cast<size_t>(pid) * kKVHeads + hh) * kPageSize + wslot) * kHeadDim;
-              uint4* kd = reinterpret_cast<uint4*>(const_cast<__nv_bfloat16*>(a.k_pages) + row);
-              uint4* vd = reinterpret_cast<uint4*>(const_cast<__nv_bfloat16*>(a.v_pages) + row);
-#pragma unroll
-              for (int q4 = 0; q4 < kRowBytes / 16; ++q4) {
-                kd[q4] = __ldg(ks + q4);
-                vd[q4] = __ldg(vs + q4);
-              }
-              fence_proxy_async_global();
-            }
-            const int z = pid * kKVHeads + hh;  // tile of the pool
-            unsigned char* dst = ring + slot * kStageBytes;
-            mbar_arrive_expect_tx(&full[slot], kStageBytes);
-            // one copy per tile: its two 16-row x 64-dim halves, 128-byte swizzled
-            tma_load_4d_hint(dst, &kmap, 0, 0, 0, z, &full[slot], policy);
-            tma_load_4d_hint(dst + kTileBytes, &vmap, 0, 0, 0, z, &full[slot], policy);
-          }
-        }
-        __syncwarp();
-      }
-      pfail = __any_sync(kFull, pfail);
-    }
-    if (!waited) {
-      grid_dependency_wait();
-      allow_dependents();
-    }
-    return;
-  }
-
-  // ============================================================== consumer warps
-  constexpr int kKS = kHeadDim / 16;        // 16-dim steps of both MMA products
-  const int r = lane >> 2, cq = lane & 3;  // MMA fragment row and column pair of this lane
-  uint32_t koff[kKS], voff[kKS];
-  mma_offsets<kKS>(koff, voff);
-
-  if (a.early) {
-    grid_dependency_wait();
-    allow_dependents();
-  }
-  zero_empty_rows(0, kConsThreads);
-
-  int k = 0;  // pages of this warp's sequence visited so far
-  bool failed = false;
-
-  // Warp 0 stages the query rows of a piece in qbuf[buf], one 16-byte chunk per
-  // lane, so that the next piece's rows are on chip before the current one ends;
-  // with a cos/sin table, also the table row of the request's new position.
-  const uint32_t qb = smem_u32(qbuf);
-  const uint32_t csb = smem_u32(csbuf);
-  auto stage_q = [&](const Piece& p, int buf) {
-    if (warp == 0) {
-      const unsigned char* src =
-          reinterpret_cast<const unsigned char*>(a.q + (static_cast<size_t>(p.b) * kQHeads + p.h * kGroup) * kHeadDim);
-      cp_async16(qb + buf * kQBufBytes + lane * 16, src + lane * 16);
-      if (kRope) {
-        const int pos = min(sl[p.b] - 1, a.rope_max_pos - 1);  // a piece's request has sl >= 1
-        const unsigned char* cs = reinterpret_cast<const unsigned char*>(a.rope + static_cast<size_t>(pos) * kHeadDim);
-        cp_async16(csb + buf * kCsBytes + lane * 16, cs + lane * 16);
-      }
-    }
-  };
-  // CTAs cfirst .. cfirst + n - 1 hold the pieces of (request b, KV head h); the
-  // record of CTA c is in slot 2c, or 2c + 1 when it is the second split piece
-  // of c's share (first_has_two: the first holder's share starts before (b, h)).
-  auto span_of = [&](int b, int h, int& cfirst, int& n, bool& first_has_two) {
-    const int np = (pref[b + 1] - pref[b]) / kKVHeads;
-    const long long fseg = pref[b] + static_cast<long long>(h) * np;
-    cfirst = cta_of(fseg, T, G);
-    n = cta_of(fseg + np - 1, T, G) - cfirst + 1;
-    first_has_two = share_lo(cfirst, T, G) < fseg;
-  };
-  // Split pieces whose partial records are written but not yet counted: only
-  // the first and the last piece of a share can be split, and both are counted
-  // together after the last piece, so that no piece boundary waits on a fence
-  // or an atomic.
-  int npend = 0;
-  int pb0 = 0, ph0 = 0, pc0 = 0, pn0 = 0, pb1 = 0, ph1 = 0, pc1 = 0, pn1 = 0;
-  bool pt0 = false, pt1 = false;
-
-  Piece pc;
-  bool have = find_piece(lo, hi, pref, batch, pc);
-  // Polled merge: the CTA that holds the last page of a split (request, KV head)
-  // merges it; that pair can only be its first piece, begun by an earlier CTA.
-  const bool merger = kPolled && have && pc.p0 > 0 && pc.p1 == pc.np;
-  const int mb = pc.b, mh = pc.h;
-  if (have) stage_q(pc, 0);
-  if (warp == 0) cp_async_wait_all();
-  consumer_sync();
-  for (int j = 0; have; ++j) {
-    Piece nx;
-    const bool have_next = find_piece(pc.fend, hi, pref, batch, nx);
-    if (have_next) stage_q(nx, (j + 1) & 1);
-    const int b = pc.b;
-    const int h = pc.h;
-    const bool complete = (pc.p0 == 0 && pc.p1 == pc.np);
-    int sp_cfirst = 0, sp_n = 0;
-    bool sp_two = false;
-    if (!kPolled && !complete) span_of(b, h, sp_cfirst, sp_n, sp_two);  // before the stream, off the critical path
-
-    // Q^T as the B operand of the score MMA: lane (r, cq) holds head r's dims 16 ks + 2 cq (+1) and
-    // 16 ks + 8 + 2 cq (+1); rows r >= kGroup are zero. With a cos/sin table the staged rows are rotated
-    // here (pairs (i, i + 64) sit in steps ks and ks + 4 of the same lane) in fp32, each product rounded
-    // first, then rounded to bf16.
-    const uint32_t qcur = qb + (j & 1) * kQBufBytes;
-    const uint32_t ccur = csb + (j & 1) * kCsBytes;
-    uint32_t qf[kKS][2];
-    if constexpr (!kRope) {
-#pragma unroll
-      for (int ks = 0; ks < kKS; ++ks) {
-        qf[ks][0] = r < kGroup ? lds32(qcur + r * kRowBytes + (16 * ks + 2 * cq) * 2) : 0u;
-        qf[ks][1] = r < kGroup ? lds32(qcur + r * kRowBytes + (16 * ks + 8 + 2 * cq) * 2) : 0u;
-      }
-    } else {
-      float2 x[kKS][2];
-#pragma unroll
-      for (int ks = 0; ks < kKS; ++ks) {
-        x[ks][0] = r < kGroup ? bf2_to_f2(lds32(qcur + r * kRowBytes + (16 * ks + 2 * cq) * 2)) : make_float2(0.f, 0.f);
-        x[ks][1] = r < kGroup ? bf2_to_f2(lds32(qcur + r * kRowBytes + (16 * ks + 8 + 2 * cq) * 2)) : make_float2(0.f, 0.f);
-      }
-#pragma unroll
-      for (int ks = 0; ks < kKS / 2; ++ks)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int d = 16 * ks + 8 * e + 2 * cq;  // dims d, d + 1 pair with d + 64, d + 65
-          const float2 cs = lds64f(ccur + d * 4), sn = lds64f(ccur + kCsBytes / 2 + d * 4);
-          const float2 lo = x[ks][e], hi = x[ks + kKS / 2][e];
-          const float2 t1 = __fmul2_rn(hi, sn), t2 = __fmul2_rn(lo, sn);
-          x[ks][e] = __ffma2_rn(lo, cs, make_float2(-t1.x, -t1.y));
-          x[ks + kKS / 2][e] = __ffma2_rn(hi, cs, t2);
-        }
-#pragma unroll
-      for (int ks = 0; ks < kKS; ++ks) {
-        qf[ks][0] = pack_bf16x2(x[ks][0].x, x[ks][0].y);
-        qf[ks][1] = pack_bf16x2(x[ks][1].x, x[ks][1].y);
-      }
-    }
-
-    float o[kKS][4];  // O^T: dims 16 ks + r (+8) x heads 2 cq, 2 cq + 1 (cq = 0: the group's two heads)
-#pragma unroll
-    for (int ks = 0; ks < kKS; ++ks) o[ks][0] = o[ks][1] = o[ks][2] = o[ks][3] = 0.f;
-    float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
-
-    const int w0 = static_cast<int>((pc.fstart - lo) % kCons);  // consumer of the piece's first page
-    for (int p = pc.p0 + (warp - w0 + kCons) % kCons; p < pc.p1; p += kCons) {
-      const int slot = warp * kDecRing + k % kDecRing;
-      const uint32_t parity = static_cast<uint32_t>(k / kDecRing) & 1u;
-      if (!failed) {
-        const bool ok = mbar_wait_bounded(&full[slot], parity);
-        failed = __any_sync(kFull, !ok);
-        if (failed && lane == 0) {
-          set_status(a.status, PKV_ERR_DEVICE_TIMEOUT);
-          flag[2] = 1;
-        }
-      }
-      if (!failed) {
-        const int rem = sl[b] - p * kPageSize;
-        const int n_valid = rem < kPageSize ? rem : kPageSize;
-        const uint32_t kt = smem_u32(ring + slot * kStageBytes);
-        mma_page<kKS>(kt, kt + kTileBytes, koff, voff, qf, n_valid, a.qscale, o, m0, m1, l0, l1);
-      }
-      __syncwarp();  // the stage and the p buffer are free again
-      if (lane == 0 && !failed) mbar_arrive(&empty[slot]);
-      ++k;
-    }
-
-    // ---- warp record: lanes cq = 0 hold the group's two heads (MMA columns 0 and 1); l summed over r
-#pragma unroll
-    for (int m = 4; m < 32; m <<= 1) {
-      l0 += __shfl_xor_sync(kFull, l0, m);
-      l1 += __shfl_xor_sync(kFull, l1, m);
-    }
-    float* mw = merge + warp * kPieceFloats;
-    if (cq == 0) {
-#pragma unroll
-      for (int ks = 0; ks < kKS; ++ks) {
-        mw[4 + 16 * ks + r] = o[ks][0];
-        mw[4 + 16 * ks + r + 8] = o[ks][2];
-        mw[kRec + 4 + 16 * ks + r] = o[ks][1];
-        mw[kRec + 4 + 16 * ks + r + 8] = o[ks][3];
-      }
-    }
-    if (lane == 0) {
-      mw[0] = m0;
-      mw[1] = l0;
-      mw[kRec] = m1;
-      mw[kRec + 1] = l1;
-    }
-    consumer_sync();
-
-    // ---- CTA merge of the warp records: thread tid owns dims tid, tid + kConsThreads, ... of both heads
-    float M[2], L[2], O[2][kDimsPerThread];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      float m = -CUDART_INF_F;
-#pragma unroll
-      for (int w = 0; w < kCons; ++w) m = fmaxf(m, merge[w * kPieceFloats + i * kRec]);
-      float l = 0.f;
-#pragma unroll
-      for (int e = 0; e < kDimsPerThread; ++e) O[i][e] = 0.f;
-#pragma unroll
-      for (int w = 0; w < kCons; ++w) {
-        const float* r = merge + w * kPieceFloats + i * kRec;
-        const float sc = ex2(r[0] - m);
-        l += r[1] * sc;
-#pragma unroll
-        for (int e = 0; e < kDimsPerThread; ++e) {
-          const int d = (tid + e * kConsThreads) & (kHeadDim - 1);
-          O[i][e] += r[4 + d] * sc;
-        }
-      }
-      M[i] = m;
-      L[i] = l;
-    }
-    const bool owns_dims = tid < kHeadDim;
-    __nv_bfloat16* orow = a.out + (static_cast<size_t>(b) * kQHeads + h * kGroup) * kHeadDim;
-    if (complete) {
-      if (owns_dims) {
-#pragma unroll
-        for (int e = 0; e < kDimsPerThread; ++e) {
-          const int d = tid + e * kConsThreads;
-          orow[d] = __float2bfloat16_rn(O[0][e] / L[0]);
-          orow[kHeadDim + d] = __float2bfloat16_rn(O[1][e] / L[1]);
-        }
-      }
-    } else {
-      const int my_slot = 2 * blockIdx.x + (pc.fstart == lo ? 0 : 1);
-      if constexpr (kPolled) {
-        uint32_t* rec = a.tagged + static_cast<size_t>(my_slot) * kSplitWords;
-        if (owns_dims) {
-#pragma unroll
-          for (int e = 0; e < kDimsPerThread; ++e) {
-            const int d = tid + e * kConsThreads;
-            st_word(rec + d, tag_word(O[0][e]));
-            st_word(rec + kHeadDim + d, tag_word(O[1][e]));
-          }
-        }
-        if (tid < 8) {  // m_hi, m_lo, l_hi, l_lo of head tid / 4
-          const float x = (tid & 2) ? L[tid >> 2] : M[tid >> 2];
-          uint32_t hi, lo;
-          tag_split(x, hi, lo);
-          st_word(rec + 2 * kHeadDim + tid, (tid & 1) ? lo : hi);
-        }
-      } else {
-        float* rec = a.partials + static_cast<size_t>(my_slot) * kPieceFloats;
-        if (owns_dims) {
-  #pragma unroll
-          for (int e = 0; e < kDimsPerThread; ++e) {
-            const int d = tid + e * kConsThreads;
-            rec[4 + d] = O[0][e];
-            rec[kRec + 4 + d] = O[1][e];
-          }
-        }
-        if (tid == 0) {
-          rec[0] = M[0];
-          rec[1] = L[0];
-          rec[kRec] = M[1];
-          rec[kRec + 1] = L[1];
-        }
-        if (npend == 0) {
-          pb0 = b, ph0 = h, pc0 = sp_cfirst, pn0 = sp_n, pt0 = sp_two;
-        } else {
-          pb1 = b, ph1 = h, pc1 = sp_cfirst, pn1 = sp_n, pt1 = sp_two;
-        }
-        ++npend;
-
-      }
-    }
-    if (warp == 0) cp_async_wait_all();  // the next piece's query rows have landed
-    consumer_sync();                     // merge buffer and qbuf[j & 1] free, qbuf[(j + 1) & 1] visible
-    pc = nx;
-    have = have_next;
-  }
-  if constexpr (kPolled) {
-    if (!merger || flag[2] != 0) return;  // (a failed wait: copies may still land, merge nothing)
-
-    // Polled merge (log-sum-exp) of the pair of this CTA's first piece over the
-    // records of its n holders. Warp w folds records t = w, w + kCons, ... in that
-    // order, with up to kMergeBatch of them loaded at a time, each lane owning dims
-    // 4 lane .. 4 lane + 3 of both heads (lanes 0..7 also load the m/l words); a
-    // record is read again until every word carries the tag. The order depends
-    // only on the pair, so the result is the same bits on every call.
-    int cf = 0, n = 0;
-    bool two = false;
-    span_of(mb, mh, cf, n, two);
-    auto rec_of = [&](int t) {
-      const size_t slot = 2 * static_cast<size_t>(cf + t) + ((t == 0 && two) ? 1 : 0);
-      return a.tagged + slot * kSplitWords;
-    };
-    float fm[2] = {-CUDART_INF_F, -CUDART_INF_F}, fl[2] = {0.f, 0.f};
-    float4 fo[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
-    bool lost = false;  // a record never got its tags (a bounded wait ran out)
-    for (int t0 = warp; t0 < n && !lost; t0 += kMergeBatch * kCons) {
-      uint4 R[kMergeBatch][2];   // o dims 4 lane .. 4 lane + 3 of heads 0 and 1
-      uint32_t W[kMergeBatch];   // lanes 0..7: word lane of the m/l block
-      auto load = [&](int r) {
-        const uint32_t* rec = rec_of(t0 + r * kCons);
-        R[r][0] = ld_words4(rec + 4 * lane);
-        R[r][1] = ld_words4(rec + kHeadDim + 4 * lane);
-        W[r] = lane < 8 ? ld_word(rec + 2 * kHeadDim + lane) : kTag;
-      };
-#pragma unroll
-      for (int r = 0; r < kMergeBatch; ++r)
-        if (t0 + r * kCons < n) load(r);
-#pragma unroll
-      for (int r = 0; r < kMergeBatch; ++r) {
-        if (t0 + r * kCons >= n) break;
-        auto all_tagged = [&]() {
-          bool ok = tagged(W[r]);
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh)
-            ok = ok && tagged(R[r][hh].x) && tagged(R[r][hh].y) && tagged(R[r][hh].z) && tagged(R[r][hh].w);
-          return __all_sync(kFull, ok);
-        };
-        if (!all_tagged()) {
-          const long long tw = clock64();
-          bool ok = false;
-          while (!ok) {
-            if (clock64() - tw > kWaitLimitCycles) break;
-            load(r);
-            ok = all_tagged();
-          }
-          if (!ok) {
-            lost = true;
-            break;
-          }
-        }
-        const float ml = untag(W[r]);
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const float mr = __shfl_sync(kFull, ml, 4 * hh) + __shfl_sync(kFull, ml, 4 * hh + 1);
-          const float lr = __shfl_sync(kFull, ml, 4 * hh + 2) + __shfl_sync(kFull, ml, 4 * hh + 3);
-          const float mn = fmaxf(fm[hh], mr);
-          const float keep = ex2(fm[hh] - mn), sc = ex2(mr - mn);
-          fl[hh] = fl[hh] * keep + lr * sc;
-          float4& o = fo[hh];
-          o.x = o.x * keep + untag(R[r][hh].x) * sc;
-          o.y = o.y * keep + untag(R[r][hh].y) * sc;
-          o.z = o.z * keep + untag(R[r][hh].z) * sc;
-          o.w = o.w * keep + untag(R[r][hh].w) * sc;
-          fm[hh] = mn;
-        }
-      }
-    }
-    if (lost && lane == 0) {
-      set_status(a.status, PKV_ERR_DEVICE_TIMEOUT);
-      flag[2] = 1;
-    }
-    float* mw = merge + warp * kPieceFloats;
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      reinterpret_cast<float4*>(mw + hh * kRec + 4)[lane] = fo[hh];
-      if (lane == 0) {
-        mw[hh * kRec] = fm[hh];
-        mw[hh * kRec + 1] = fl[hh];
-      }
-    }
-    consumer_sync();
-    if (flag[2] != 0) return;
-    if (tid < kHeadDim) {
-      __nv_bfloat16* orow = a.out + (static_cast<size_t>(mb) * kQHeads + mh * kGroup) * kHeadDim;
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        float m = -CUDART_INF_F;
-#pragma unroll
-        for (int w = 0; w < kCons; ++w) m = fmaxf(m, merge[w * kPieceFloats + hh * kRec]);
-        float l = 0.f, acc = 0.f;
-#pragma unroll
-        for (int w = 0; w < kCons; ++w) {
-          const float* r = merge + w * kPieceFloats + hh * kRec;
-          const float sc = r[0] == -CUDART_INF_F ? 0.f : ex2(r[0] - m);  // warps that folded no record
-          l += r[1] * sc;
-          acc += r[4 + tid] * sc;
-        }
-        orow[hh * kHeadDim + tid] = __float2bfloat16_rn(acc / l);
-      }
-    }
-    // clear the tags of the merged records for the next call (every read above has completed)
-    for (int i = tid; i < n * (kSplitBytes / 16); i += kConsThreads) {
-      const int t = i / (kSplitBytes / 16), c = i % (kSplitBytes / 16);
-      reinterpret_cast<uint4*>(rec_of(t))[c] = make_uint4(0u, 0u, 0u, 0u);
-    }
-  } else {
-    if (npend == 0) return;
-
-    // Count this CTA's records in (release) and learn whether it completed a count
-    // (acquire): the CTA that does merges every record of that (request, KV head).
-    if (tid == 0) {
-      __threadfence();
-      const int old0 = atomicAdd(a.counters + pb0 * kKVHeads + ph0, 1);
-      const int old1 = npend > 1 ? atomicAdd(a.counters + pb1 * kKVHeads + ph1, 1) : -1;
-      __threadfence();
-      flag[0] = old0 == pn0 - 1 ? 1 : 0;
-      flag[1] = npend > 1 && old1 == pn1 - 1 ? 1 : 0;
-    }
-    consumer_sync();
-    if (flag[2] != 0) {  // a wait failed: copies may still land in the ring, merge nothing
-      if (tid == 0) {
-        if (flag[0]) a.counters[pb0 * kKVHeads + ph0] = 0;
-        if (flag[1]) a.counters[pb1 * kKVHeads + ph1] = 0;
-      }
-      return;
-    }
-    // Final merges (log-sum-exp over the partial records) of the pairs whose count
-    // this CTA completed. Their records are staged in the drained stage ring by
-    // 16-byte asynchronous copies (one round trip per batch of up to kMergeCap
-    // records); record t of a pair is folded by warp t % kCons, each lane owning
-    // dims 4 lane .. 4 lane + 3 of both heads, and the warps' states are then
-    // combined through the merge buffer. Which warp folds which record, and the
-    // batch boundaries, depend only on the pair, so the result is the same
-    // whichever CTA merges.
-    const int nm0 = flag[0] ? pn0 : 0;
-    const int nm1 = flag[1] ? pn1 : 0;
-    if (nm0 + nm1 == 0) return;
-    const uint32_t ring_s = smem_u32(ring);
-    const float* R = reinterpret_cast<const float*>(ring);
-    constexpr int kChunks = kPieceBytes / 16;
-    static_assert(kChunks > 64 && kChunks <= 96, "a record is copied in three lane-strided passes");
-    static_assert(kConsThreads >= kHeadDim, "the final combine maps one thread to one dim");
-    float fm[2][2], fl[2][2];
-    float4 fo[2][2];
-#pragma unroll
-    for (int i = 0; i < 2; ++i)
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        fm[i][hh] = -CUDART_INF_F;
-        fl[i][hh] = 0.f;
-        fo[i][hh] = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-    // One batch: records [t0[i], t1[i]) of pair i, pair 0's first in the ring.
-    auto merge_batch = [&](const int (&t0)[2], const int (&t1)[2]) {
-      const int c0 = t1[0] - t0[0], nb = c0 + t1[1] - t0[1];
-      for (int p = warp; p < nb; p += kCons) {
-        const bool second = p >= c0;
-        const int t = second ? t0[1] + p - c0 : t0[0] + p;
-        const int cf = second ? pc1 : pc0;
-        const bool two = second ? pt1 : pt0;
-        const size_t slot = 2 * static_cast<size_t>(cf + t) + ((t == 0 && two) ? 1 : 0);
-        const unsigned char* src = reinterpret_cast<const unsigned char*>(a.partials + slot * kPieceFloats);
-        const uint32_t dst = ring_s + p * kPieceBytes;
-        cp_async16(dst + lane * 16, src + lane * 16);
-        cp_async16(dst + (lane + 32) * 16, src + (lane + 32) * 16);
-        if (lane < kChunks - 64) cp_async16(dst + (lane + 64) * 16, src + (lane + 64) * 16);
-      }
-      cp_async_wait_all();
-      consumer_sync();
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const int ps = i == 0 ? 0 : c0;             // ring position of record t0[i]
-        const int pe = ps + t1[i] - t0[i];
-        const int pfirst = ps + ((warp - t0[i]) % kCons + kCons) % kCons;  // this warp's first record t
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          float m = fm[i][hh];
-          for (int p = pfirst; p < pe; p += kCons) m = fmaxf(m, R[p * kPieceFloats + hh * kRec]);
-          const float keep = fm[i][hh] == -CUDART_INF_F ? 0.f : ex2(fm[i][hh] - m);
-          float l = fl[i][hh] * keep;
-          float4 o = fo[i][hh];
-          o.x *= keep, o.y *= keep, o.z *= keep, o.w *= keep;
-#pragma unroll 4
-          for (int p = pfirst; p < pe; p += kCons) {
-            const float* r = R + p * kPieceFloats + hh * kRec;
-            const float sc = ex2(r[0] - m);
-            l += r[1] * sc;
-            const float4 v = reinterpret_cast<const float4*>(r + 4)[lane];  // plain load: schedulable across records
-            o.x += v.x * sc, o.y += v.y * sc, o.z += v.z * sc, o.w += v.w * sc;
-          }
-          fm[i][hh] = m;
-          fl[i][hh] = l;
-          fo[i][hh] = o;
-        }
-      }
-      consumer_sync();  // the ring is free for the next batch
-    };
-    if (nm0 + nm1 <= kMergeCap) {
-      const int t0[2] = {0, 0}, t1[2] = {nm0, nm1};
-      merge_batch(t0, t1);
-    } else {
-      for (int t = 0; t < nm0; t += kMergeCap) {
-        const int t0[2] = {t, 0}, t1[2] = {t + kMergeCap < nm0 ? t + kMergeCap : nm0, 0};
-        merge_batch(t0, t1);
-      }
-      for (int t = 0; t < nm1; t += kMergeCap) {
-        const int t0[2] = {0, t}, t1[2] = {0, t + kMergeCap < nm1 ? t + kMergeCap : nm1};
-        merge_batch(t0, t1);
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      if ((i == 0 ? nm0 : nm1) == 0) continue;
-      float* mw = merge + warp * kPieceFloats;
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        reinterpret_cast<float4*>(mw + hh * kRec + 4)[lane] = fo[i][hh];
-        if (lane == 0) {
-          mw[hh * kRec] = fm[i][hh];
-          mw[hh * kRec + 1] = fl[i][hh];
-        }
-      }
-      consumer_sync();
-      const int b = i ? pb1 : pb0, h = i ? ph1 : ph0;
-      if (tid < kHeadDim) {
-        __nv_bfloat16* orow = a.out + (static_cast<size_t>(b) * kQHeads + h * kGroup) * kHeadDim;
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          float m = -CUDART_INF_F;
-#pragma unroll
-          for (int w = 0; w < kCons; ++w) m = fmaxf(m, merge[w * kPieceFloats + hh * kRec]);
-          float l = 0.f, acc = 0.f;
-#pragma unroll
-          for (int w = 0; w < kCons; ++w) {
-            const float* r = merge + w * kPieceFloats + hh * kRec;
-            const float sc = r[0] == -CUDART_INF_F ? 0.f : ex2(r[0] - m);  // warps that folded no record
-            l += r[1] * sc;
-            acc += r[4 + tid] * sc;
-          }
-          orow[hh * kHeadDim + tid] = __float2bfloat16_rn(acc / l);
-        }
-      }
-      if (tid == 0) a.counters[b * kKVHeads + h] = 0;
-      consumer_sync();  // merge buffer free for the second pair
-    }
-  }
-}
-
-size_t decode_workspace_bytes(int32_t batch, int num_sms) {
-  size_t off = PKV_STATUS_BYTES;
-  off += (static_cast<size_t>(batch) * kKVHeads * 4 + 255) / 256 * 256;
-  const int grid = kDecCtasPerSm * num_sms < kMaxGrid ? kDecCtasPerSm * num_sms : kMaxGrid;
-  off += static_cast<size_t>(2) * grid * kPieceFloats * 4;
-  off += static_cast<size_t>(2) * grid * kSplitBytes;
+size_t decode_workspace_bytes(int num_q_heads, int num_kv_heads, int head_dim, int32_t batch, int num_sms) {
+  const size_t G = static_cast<size_t>(group_pad(num_q_heads / num_kv_heads));
+  const size_t grid = static_cast<size_t>(decode_grid(num_sms));
+  size_t off = PKV_STATUS_BYTES + decode_counter_bytes(batch, num_kv_heads);
+  off += 2 * grid * G * (head_dim + 4) * 4;      // counted records
+  off += 2 * grid * (G * head_dim + 4 * G) * 4;  // polled records
   return off;
 }
 
 int launch_decode(const void* q, const void* k_new, const void* v_new, const void* k_pages, const void* v_pages,
                   const int32_t* block_table, const int32_t* seq_lens, const float* rope, int32_t rope_max_pos,
-                  void* out, float scale, int32_t batch, int32_t max_pages, int32_t num_pages, void* workspace,
-                  int num_sms, cudaStream_t stream, uint32_t flags) {
-  if (batch == 0) return PKV_OK;
-  if (rope != nullptr && k_new == nullptr) return PKV_ERR_NULL_ARG;
-  const size_t smem = decode_smem_bytes(batch);
-  // Polled merge when a pair is expected to span at most kPollMax CTAs (equal
-  // lengths); the counted merge for few pairs over many CTAs.
-  const int grid = num_sms * kDecCtasPerSm < kMaxGrid ? num_sms * kDecCtasPerSm : kMaxGrid;
-  const bool polled = grid <= kPollMax * batch * kKVHeads;
-  using Kern = void (*)(const CUtensorMap, const CUtensorMap, const DecodeArgs);
-  static const Kern kKerns[2][3] = {
-      {decode_kernel<false, false, false>, decode_kernel<true, false, false>, decode_kernel<true, true, false>},
-      {decode_kernel<false, false, true>, decode_kernel<true, false, true>, decode_kernel<true, true, true>}};
-  const int variant = k_new == nullptr ? 0 : rope == nullptr ? 1 : 2;
-  const Kern kern = kKerns[polled ? 1 : 0][variant];
-  static bool attr_set[64][2][3] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
-  if (dev < 64 && !attr_set[dev][polled ? 1 : 0][variant]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(decode_smem_bytes(kMaxDecodeBatch))) != cudaSuccess)
-      return PKV_ERR_CUDA;
-    attr_set[dev][polled ? 1 : 0][variant] = true;
-  }
-  int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kDecThreads, smem) != cudaSuccess)
-    return PKV_ERR_CUDA;
-  if (occ < 1) return PKV_ERR_UNSUPPORTED;
-  if (occ > kDecCtasPerSm) occ = kDecCtasPerSm;
-
-  unsigned char* ws = static_cast<unsigned char*>(workspace);
-  DecodeArgs a;
-  a.q = static_cast<const __nv_bfloat16*>(q);
-  a.k_new = static_cast<const __nv_bfloat16*>(k_new);
-  a.v_new = static_cast<const __nv_bfloat16*>(v_new);
-  a.k_pages = static_cast<const __nv_bfloat16*>(k_pages);
-  a.v_pages = static_cast<const __nv_bfloat16*>(v_pages);
-  a.block_table = block_table;
-  a.seq_lens = seq_lens;
-  a.out = static_cast<__nv_bfloat16*>(out);
-  a.rope = rope;
-  a.rope_max_pos = rope_max_pos;
-  a.qscale = scale * kLog2e;
-  a.early = (flags & PKV_DECODE_EARLY_PREFETCH) ? 1 : 0;
-  a.batch = batch;
-  a.max_pages = max_pages;
-  a.num_pages = num_pages;
-  a.status = reinterpret_cast<int*>(ws);
-  a.counters = reinterpret_cast<int*>(ws + PKV_STATUS_BYTES);
-  a.partials = reinterpret_cast<float*>(ws + PKV_STATUS_BYTES +
-                                        (static_cast<size_t>(batch) * kKVHeads * 4 + 255) / 256 * 256);
-  const int slots = 2 * (num_sms * kDecCtasPerSm < kMaxGrid ? num_sms * kDecCtasPerSm : kMaxGrid);
-  a.tagged = reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(a.partials) +
-                                         static_cast<size_t>(slots) * kPieceFloats * 4);
-  CUtensorMap kmap, vmap;
-  const int rc = encode_page_maps(k_pages, v_pages, kHeadDim, num_pages, kKVHeads, &kmap, &vmap);
-  if (rc != PKV_OK) return rc;
-  const int launch_grid = num_sms * occ < kMaxGrid ? num_sms * occ : kMaxGrid;
-  return launch_pdl(kern, dim3(launch_grid), dim3(kDecThreads), smem, stream, kmap, vmap, a) == cudaSuccess
-             ? PKV_OK
-             : PKV_ERR_CUDA;
+                  void* out, float scale, int num_q_heads, int num_kv_heads, int head_dim, int32_t batch,
+                  int32_t max_pages, int32_t num_pages, void* workspace, int num_sms, cudaStream_t stream,
+                  uint32_t flags) {
+  if (!decode_supported(num_q_heads, num_kv_heads, head_dim, kPageSize)) return PKV_ERR_UNSUPPORTED;
+  DecodeLaunch c;
+  c.q = q;
+  c.k_new = k_new;
+  c.v_new = v_new;
+  c.k_pages = k_pages;
+  c.v_pages = v_pages;
+  c.block_table = block_table;
+  c.seq_lens = seq_lens;
+  c.rope = rope;
+  c.rope_max_pos = rope_max_pos;
+  c.out = out;
+  c.scale = scale;
+  c.hq = num_q_heads;
+  c.hkv = num_kv_heads;
+  c.head_dim = head_dim;
+  c.batch = batch;
+  c.max_pages = max_pages;
+  c.num_pages = num_pages;
+  c.workspace = workspace;
+  c.num_sms = num_sms;
+  c.stream = stream;
+  c.flags = flags;
+  if (fixed_geometry(num_q_heads, num_kv_heads, head_dim)) return launch_decode_geo<DecGeo<128, 2, true>>(c);
+  const int G = group_pad(num_q_heads / num_kv_heads);
+  return head_dim == 64 ? launch_decode_d64(c, G) : launch_decode_d128(c, G);
 }
 
 }  // namespace pkv

@@ -110,13 +110,14 @@ extern "C" int pkv_decode_attn_noalloc(const void* q, const void* k_pages, const
   int sms = 0;
   int rc = scratch_of_current_device(&scratch, &sms);
   if (rc != PKV_OK) return rc;
-  if (pkv::decode_workspace_bytes(batch, sms) > kScratchBytes) return PKV_ERR_WORKSPACE_TOO_SMALL;
+  if (pkv::decode_workspace_bytes(16, 8, 128, batch, sms) > kScratchBytes) return PKV_ERR_WORKSPACE_TOO_SMALL;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // The array keeps whatever the previous call left. The status word and the
   // split records must start at zero; a call that stopped early (a timed-out
   // wait) could have left tagged words behind.
-  if (cudaMemsetAsync(scratch, 0, pkv::decode_workspace_bytes(batch, sms), s) != cudaSuccess) return PKV_ERR_CUDA;
-  return pkv::launch_decode(q, nullptr, nullptr, k_pages, v_pages, block_table, seq_lens, nullptr, 0, out, scale, batch,
-                            max_pages_per_seq, desc->num_pages, scratch, sms, s, 0u);
+  if (cudaMemsetAsync(scratch, 0, pkv::decode_workspace_bytes(16, 8, 128, batch, sms), s) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  return pkv::launch_decode(q, nullptr, nullptr, k_pages, v_pages, block_table, seq_lens, nullptr, 0, out, scale, 16, 8,
+                            128, batch, max_pages_per_seq, desc->num_pages, scratch, sms, s, 0u);
 }

@@ -1,6 +1,6 @@
 // pkv_abi.cu -- the extern "C" entry points of libpkv: argument checks on the
 // host, launch-configuration choice, and the status word helpers. All device
-// work is in append.cu, decode.cu, decode_generic.cu and prefill.cu.
+// work is in append.cu, decode.cu (decode_kernel.cuh) and prefill.cu.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -56,17 +56,14 @@ int check_desc(const pkv_cache_desc* d) {
   return PKV_OK;
 }
 
-// Geometries pkv_append and pkv_decode_attn also serve (decode_generic.cu):
-// page size 16, head_dim 64 or 128, 1 to 8 query heads per KV head.
-// Sets *generic when the call takes the generic decode path.
-int check_desc_decode(const pkv_cache_desc* d, bool* generic) {
+// Geometries pkv_append and the decode calls serve: page size 16, head_dim 64
+// or 128, 1 to 8 query heads per KV head (16 / 8 / 128 on an instantiation
+// with the head counts fixed at compile time).
+int check_desc_decode(const pkv_cache_desc* d) {
   const int rc = check_desc(d);
-  *generic = false;
   if (rc != PKV_ERR_UNSUPPORTED) return rc;
-  if (!pkv::decode_generic_supported(d->num_q_heads, d->num_kv_heads, d->head_dim, d->page_size))
-    return PKV_ERR_UNSUPPORTED;
-  *generic = true;
-  return PKV_OK;
+  return pkv::decode_supported(d->num_q_heads, d->num_kv_heads, d->head_dim, d->page_size) ? PKV_OK
+                                                                                          : PKV_ERR_UNSUPPORTED;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -117,8 +114,7 @@ const char* pkv_status_string(int status) {
 int pkv_append(const void* k_new, const void* v_new, const int32_t* slot_mapping, int32_t n_tokens, void* k_pages,
                void* v_pages, const pkv_cache_desc* desc, pkv_stream_t stream, void* workspace,
                size_t workspace_bytes) {
-  bool generic = false;
-  int rc = check_desc_decode(desc, &generic);
+  int rc = check_desc_decode(desc);
   if (rc != PKV_OK) return rc;
   if (n_tokens < 0) return PKV_ERR_BAD_SHAPE;
   if (workspace != nullptr && workspace_bytes < PKV_STATUS_BYTES) return PKV_ERR_WORKSPACE_TOO_SMALL;
@@ -134,28 +130,24 @@ int pkv_append(const void* k_new, const void* v_new, const int32_t* slot_mapping
                             reinterpret_cast<cudaStream_t>(stream));
 }
 
-// Workspace bytes of a decode call for this geometry (0 if unsupported).
-static size_t decode_ws(const pkv_cache_desc* desc, bool generic, int32_t batch, int32_t max_pages, int sms) {
-  return generic ? pkv::decode_generic_workspace_bytes(desc->num_q_heads, desc->num_kv_heads, desc->head_dim, batch,
-                                                       max_pages, sms)
-                 : pkv::decode_workspace_bytes(batch, sms);
+// Workspace bytes of a decode call for this geometry.
+static size_t decode_ws(const pkv_cache_desc* desc, int32_t batch, int sms) {
+  return pkv::decode_workspace_bytes(desc->num_q_heads, desc->num_kv_heads, desc->head_dim, batch, sms);
 }
 
 size_t pkv_decode_workspace_bytes(const pkv_cache_desc* desc, int32_t batch, int32_t max_pages_per_seq) {
-  bool generic = false;
-  if (check_desc_decode(desc, &generic) != PKV_OK || batch < 0 || max_pages_per_seq < 1) return 0;
+  if (check_desc_decode(desc) != PKV_OK || batch < 0 || max_pages_per_seq < 1) return 0;
   if (batch > pkv::decode_max_batch() || !table_fits(batch, max_pages_per_seq)) return 0;
   int sms = 0;
   if (current_device(&sms) != PKV_OK) return 0;
-  return decode_ws(desc, generic, batch, max_pages_per_seq, sms);
+  return decode_ws(desc, batch, sms);
 }
 
 int pkv_decode_attn(const void* q, const void* k_pages, const void* v_pages, const int32_t* block_table,
                     const int32_t* seq_lens, void* out, float scale, pkv_stream_t stream,
                     const pkv_cache_desc* desc, int32_t batch, int32_t max_pages_per_seq, void* workspace,
                     size_t workspace_bytes) {
-  bool generic = false;
-  int rc = check_desc_decode(desc, &generic);
+  int rc = check_desc_decode(desc);
   if (rc != PKV_OK) return rc;
   if (batch < 0 || max_pages_per_seq < 1) return PKV_ERR_BAD_SHAPE;
   if (batch > pkv::decode_max_batch()) return PKV_ERR_UNSUPPORTED;
@@ -168,15 +160,10 @@ int pkv_decode_attn(const void* q, const void* k_pages, const void* v_pages, con
   int sms = 0;
   rc = current_device(&sms);
   if (rc != PKV_OK) return rc;
-  if (workspace_bytes < decode_ws(desc, generic, batch, max_pages_per_seq, sms)) return PKV_ERR_WORKSPACE_TOO_SMALL;
-  if (generic)
-    return pkv::launch_decode_generic(q, nullptr, nullptr, k_pages, v_pages, block_table, seq_lens, nullptr, 0, out,
-                                      scale, desc->num_q_heads, desc->num_kv_heads, desc->head_dim, batch,
-                                      max_pages_per_seq, desc->num_pages, workspace, sms,
-                                      reinterpret_cast<cudaStream_t>(stream), 0u);
-  return pkv::launch_decode(q, nullptr, nullptr, k_pages, v_pages, block_table, seq_lens, nullptr, 0, out, scale, batch,
-                            max_pages_per_seq, desc->num_pages, workspace, sms, reinterpret_cast<cudaStream_t>(stream),
-                            0u);
+  if (workspace_bytes < decode_ws(desc, batch, sms)) return PKV_ERR_WORKSPACE_TOO_SMALL;
+  return pkv::launch_decode(q, nullptr, nullptr, k_pages, v_pages, block_table, seq_lens, nullptr, 0, out, scale,
+                            desc->num_q_heads, desc->num_kv_heads, desc->head_dim, batch, max_pages_per_seq,
+                            desc->num_pages, workspace, sms, reinterpret_cast<cudaStream_t>(stream), 0u);
 }
 
 static int decode_append(const void* q, const void* k_new, const void* v_new, void* k_pages, void* v_pages,
@@ -184,8 +171,7 @@ static int decode_append(const void* q, const void* k_new, const void* v_new, vo
                          int32_t rope_max_pos, void* out, float scale, pkv_stream_t stream, const pkv_cache_desc* desc,
                          int32_t batch, int32_t max_pages_per_seq, void* workspace, size_t workspace_bytes,
                          uint32_t flags) {
-  bool generic = false;
-  int rc = check_desc_decode(desc, &generic);
+  int rc = check_desc_decode(desc);
   if (rc != PKV_OK) return rc;
   if (batch < 0 || max_pages_per_seq < 1) return PKV_ERR_BAD_SHAPE;
   if (batch > pkv::decode_max_batch()) return PKV_ERR_UNSUPPORTED;
@@ -199,16 +185,11 @@ static int decode_append(const void* q, const void* k_new, const void* v_new, vo
   int sms = 0;
   rc = current_device(&sms);
   if (rc != PKV_OK) return rc;
-  if (workspace_bytes < decode_ws(desc, generic, batch, max_pages_per_seq, sms)) return PKV_ERR_WORKSPACE_TOO_SMALL;
+  if (workspace_bytes < decode_ws(desc, batch, sms)) return PKV_ERR_WORKSPACE_TOO_SMALL;
   if ((flags & ~static_cast<uint32_t>(PKV_DECODE_EARLY_PREFETCH)) != 0) return PKV_ERR_UNSUPPORTED;
-  if (generic)
-    return pkv::launch_decode_generic(q, k_new, v_new, k_pages, v_pages, block_table, seq_lens, rope_cos_sin,
-                                      rope_max_pos, out, scale, desc->num_q_heads, desc->num_kv_heads, desc->head_dim,
-                                      batch, max_pages_per_seq, desc->num_pages, workspace, sms,
-                                      reinterpret_cast<cudaStream_t>(stream), flags);
   return pkv::launch_decode(q, k_new, v_new, k_pages, v_pages, block_table, seq_lens, rope_cos_sin, rope_max_pos, out,
-                            scale, batch, max_pages_per_seq, desc->num_pages, workspace, sms,
-                            reinterpret_cast<cudaStream_t>(stream), flags);
+                            scale, desc->num_q_heads, desc->num_kv_heads, desc->head_dim, batch, max_pages_per_seq,
+                            desc->num_pages, workspace, sms, reinterpret_cast<cudaStream_t>(stream), flags);
 }
 
 int pkv_decode_append_attn(const void* q, const void* k_new, const void* v_new, void* k_pages, void* v_pages,

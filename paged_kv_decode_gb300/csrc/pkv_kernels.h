@@ -12,29 +12,20 @@ int launch_append(const void* k_new, const void* v_new, const int32_t* slot_mapp
                   void* v_pages, int32_t num_pages, int32_t num_kv_heads, int32_t head_dim, int* status, int num_sms,
                   cudaStream_t stream);
 
-// Decode: workspace = [status header | counters (batch * kv heads) | partials].
-size_t decode_workspace_bytes(int32_t batch, int num_sms);
+// Decode (decode.cu, decode_kernel.cuh): page size 16, head_dim 64 or 128, num_q_heads / num_kv_heads
+// from 1 to 8. Workspace = [status header | counters (batch * kv heads) | records].
+bool decode_supported(int num_q_heads, int num_kv_heads, int head_dim, int page_size);
+size_t decode_workspace_bytes(int num_q_heads, int num_kv_heads, int head_dim, int32_t batch, int num_sms);
 // k_new / v_new (nullable): fused append of each request's new token at position seq_lens[b] - 1.
-// rope (nullable, needs k_new): cos/sin table [rope_max_pos][128]; the new key row and the query
-// rows are rotated at that position.
+// rope (nullable, needs k_new): cos/sin table [rope_max_pos][head_dim]; the new key row and the
+// query rows are rotated at that position. flags: 0 or PKV_DECODE_EARLY_PREFETCH.
 int launch_decode(const void* q, const void* k_new, const void* v_new, const void* k_pages, const void* v_pages,
                   const int32_t* block_table, const int32_t* seq_lens, const float* rope, int32_t rope_max_pos,
-                  void* out, float scale, int32_t batch, int32_t max_pages, int32_t num_pages, void* workspace,
-                  int num_sms, cudaStream_t stream, uint32_t flags);
+                  void* out, float scale, int num_q_heads, int num_kv_heads, int head_dim, int32_t batch,
+                  int32_t max_pages, int32_t num_pages, void* workspace, int num_sms, cudaStream_t stream,
+                  uint32_t flags);
 int decode_max_batch();
 
-// Decode for other geometries (decode_generic.cu): page size 16, head_dim 64 or 128,
-// num_q_heads / num_kv_heads from 1 to 8. Workspace = [status | counters | records].
-bool decode_generic_supported(int num_q_heads, int num_kv_heads, int head_dim, int page_size);
-size_t decode_generic_workspace_bytes(int num_q_heads, int num_kv_heads, int head_dim, int32_t batch,
-                                      int32_t max_pages, int num_sms);
-// k_new / v_new: the fused append's new rows (both nullptr: decode alone); rope (nullable, needs
-// k_new): cos/sin table [rope_max_pos][head_dim]; flags: 0 or PKV_DECODE_EARLY_PREFETCH.
-int launch_decode_generic(const void* q, const void* k_new, const void* v_new, const void* k_pages,
-                          const void* v_pages, const int32_t* block_table, const int32_t* seq_lens, const float* rope,
-                          int32_t rope_max_pos, void* out, float scale, int num_q_heads, int num_kv_heads,
-                          int head_dim, int32_t batch, int32_t max_pages, int32_t num_pages, void* workspace,
-                          int num_sms, cudaStream_t stream, uint32_t flags);
 
 // Rotary-embedding table (rope.cu): fp32 [max_pos][head_dim], row p = cos(p w_i) for i < head_dim / 2,
 // then sin(p w_i), w_i = theta^(-2 i / head_dim), angles in double rounded to float once.

@@ -1,5 +1,6 @@
-// pkv_mma.cuh -- warp-level bf16 tensor-core MMA step of a decode page, shared
-// by the tuned decode kernel (decode.cu) and the generic one (decode_generic.cu).
+// pkv_mma.cuh -- warp-level bf16 tensor-core MMA step of a decode page, used by
+// the decode kernel (decode_kernel.cuh) and the mixed step's decode CTAs
+// (prefill.cu).
 //
 // A page of one (request, KV head) is 16 token rows of K and of V, each
 // head_dim bf16 values, in shared memory as written by 128-byte-swizzled tiled

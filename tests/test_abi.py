@@ -51,7 +51,8 @@ def test_host_argument_checks(lib):
                                           ctypes.byref(bad), 1, 1, None, 0) == -3
     for other in (_desc(head_dim=64), _desc(num_q_heads=32, num_kv_heads=8), _desc(num_q_heads=8),
                   _desc(num_q_heads=40), _desc(num_q_heads=28, num_kv_heads=4), _desc(num_q_heads=24)):
-        # served by the generic decode path: past the geometry check, stopped at the NULL pointers
+        # served by the decode path with run-time head counts: past the geometry check, stopped at the NULL
+        # pointers
         assert lib.pkv_decode_attn(None, None, None, None, None, None, 1.0, None, ctypes.byref(other), 1, 1, None,
                                    0) == -1
         assert lib.pkv_append(None, None, None, 1, None, None, ctypes.byref(other), None, None, 0) == -1
@@ -143,7 +144,7 @@ def test_noalloc_host_argument_checks(lib):
                                                                    None if desc is None else ctypes.byref(desc),
                                                                    batch, max_pages)
     assert f(*args(desc=None)) == -1
-    # only the tuned 16/8/128/16 geometry, also where pkv_decode_attn takes the generic kernel
+    # only the 16/8/128/16 geometry, also where pkv_decode_attn serves others
     for other in (_desc(num_q_heads=32, num_kv_heads=8), _desc(head_dim=64), _desc(num_q_heads=8)):
         assert f(*args(desc=other)) == -3
     assert f(*args(desc=_desc(num_pages=0))) == -2

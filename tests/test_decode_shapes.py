@@ -1,6 +1,6 @@
 """Decode attention, KV append and the fused append + decode call for cache
-geometries other than the Qwen3 decoder's 16/8/128 (the generic decode path),
-against the fp64 oracle.
+geometries other than the Qwen3 decoder's 16/8/128 (the decode kernel with
+run-time head counts), against the fp64 oracle.
 
 The pages name further decoder backbones for the same slot (a Llama-style 2B
 model, Qwen3-8B, OLMo-2-7B, SmolLM2-1.7B) but give no head counts, so the
@@ -44,7 +44,7 @@ def _check(case, dev, what):
     out = run.step()
     torch.cuda.synchronize()
     kp, vp = run.pools_cpu()
-    if case.k_new is not None:  # the generic append is bit-exact
+    if case.k_new is not None:  # the append is bit-exact
         want_k, want_v = oracle.append(case.k_new[0], case.v_new[0], case.slot_mapping, case.k_pages[0],
                                        case.v_pages[0])
         assert np.array_equal(bits(kp), want_k) and np.array_equal(bits(vp), want_v), what
