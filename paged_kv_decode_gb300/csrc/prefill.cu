@@ -206,8 +206,12 @@ __device__ __forceinline__ bool pf_wait(uint64_t* bar, uint32_t parity, volatile
 }
 
 // Warp-collective form: every lane waits and the warp agrees on the outcome
-// (the tcgen05.ld/st that follow are warp-wide).
+// (the tcgen05.ld/st that follow are warp-wide). A phase that has already
+// completed costs one try_wait: the CTA's failure flag (a volatile shared load
+// in front of every wait) is read only on the slow path. The MMA issuer's
+// waits sit between its MMA batches, so their cost is idle tensor-pipe time.
 __device__ __forceinline__ bool pf_wait_warp(uint64_t* bar, uint32_t parity, volatile int* fail, int* status) {
+  if (__all_sync(0xffffffffu, mbar_try_wait(smem_u32(bar), parity))) return true;
   return __all_sync(0xffffffffu, pf_wait(bar, parity, fail, status));
 }
 
@@ -753,15 +757,22 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             tma_load_3d(sQ + h * Dm::kTileBytes + half * kPfHalfBytes, &qmap, half * 64, qh0 + (two ? h : 0),
                         q0 + i0, &bars->q_full);
       }
+      // this lane's page id of the first key tile, then of each next tile one tile ahead (the
+      // block-table read is not on the path from a stage's release to its copies)
+      int id_next = lane < kPfPagesPerTile && lane < n_pages
+                        ? __ldg(a.block_table + static_cast<size_t>(n) * a.max_pages + lane) : 0;
       for (int j = 0; j < n_tiles; ++j) {
         const int st = j & 1;
         const int use = j >> 1;
-        if (use > 0 && !pf_wait_warp(&bars->kv_empty[st], static_cast<uint32_t>(use - 1) & 1u, fail, a.status)) break;
         const int pg = j * kPfPagesPerTile + lane;
+        const int id_cur = id_next;
+        if (j + 1 < n_tiles && lane < kPfPagesPerTile && pg + kPfPagesPerTile < n_pages)
+          id_next = __ldg(a.block_table + static_cast<size_t>(n) * a.max_pages + pg + kPfPagesPerTile);
+        if (use > 0 && !pf_wait_warp(&bars->kv_empty[st], static_cast<uint32_t>(use - 1) & 1u, fail, a.status)) break;
         bool valid = lane < kPfPagesPerTile && pg < n_pages;
         int id = 0;
         if (valid) {
-          id = __ldg(a.block_table + static_cast<size_t>(n) * a.max_pages + pg);
+          id = id_cur;
           if (id < 0 || id >= a.num_pages) {
             set_status(a.status, PKV_ERR_OUT_OF_BOUNDS);
             valid = false;
@@ -1012,18 +1023,25 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         const int rows = pc.qlen < kPfRows * (pc.t + 1) ? pc.qlen : kPfRows * (pc.t + 1);
         const int n_pages = (pc.P + rows + kPageSize - 1) / kPageSize;
+        // this lane's page id of the piece's first key tile, then of each next tile one tile ahead
+        int id_next = lane < kPfPagesPerTile && pc.k0 * kPfPagesPerTile + lane < n_pages
+                          ? __ldg(a.block_table + static_cast<size_t>(pc.n) * a.max_pages + pc.k0 * kPfPagesPerTile + lane)
+                          : 0;
         for (int k = pc.k0; k < pc.k1; ++k, ++gj) {
           const int st = gj & 1;
           const int use = gj >> 1;
+          const int pg = k * kPfPagesPerTile + lane;
+          const int id_cur = id_next;
+          if (k + 1 < pc.k1 && lane < kPfPagesPerTile && pg + kPfPagesPerTile < n_pages)
+            id_next = __ldg(a.block_table + static_cast<size_t>(pc.n) * a.max_pages + pg + kPfPagesPerTile);
           if (use > 0 && !pf_wait_warp(&bars->kv_empty[st], static_cast<uint32_t>(use - 1) & 1u, fail, a.status)) {
             run = false;
             break;
           }
-          const int pg = k * kPfPagesPerTile + lane;
           bool valid = lane < kPfPagesPerTile && pg < n_pages;
           int id = 0;
           if (valid) {
-            id = __ldg(a.block_table + static_cast<size_t>(pc.n) * a.max_pages + pg);
+            id = id_cur;
             if (id < 0 || id >= a.num_pages) {
               set_status(a.status, PKV_ERR_OUT_OF_BOUNDS);
               valid = false;
