@@ -214,6 +214,12 @@ __device__ __forceinline__ bool pf_wait_warp(uint64_t* bar, uint32_t parity, vol
   if (__all_sync(0xffffffffu, mbar_try_wait(smem_u32(bar), parity))) return true;
   return __all_sync(0xffffffffu, pf_wait(bar, parity, fail, status));
 }
+// Two waits with one poll when both phases have already completed.
+__device__ __forceinline__ bool pf_wait_warp2(uint64_t* b1, uint32_t p1, uint64_t* b2, uint32_t p2, volatile int* fail,
+                                              int* status) {
+  if (__all_sync(0xffffffffu, mbar_try_wait(smem_u32(b1), p1) && mbar_try_wait(smem_u32(b2), p2))) return true;
+  return pf_wait_warp(b1, p1, fail, status) && pf_wait_warp(b2, p2, fail, status);
+}
 
 // Work is a list of items (request n, KV head g, query tile t), ordered by n,
 // then g, then t. Query tile t of a request with P cached tokens and qlen chunk
@@ -843,7 +849,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const uint32_t ph = static_cast<uint32_t>(j >> 1) & 1u;
         const bool next = j + 1 < n_tiles;
         const uint32_t ph_next = static_cast<uint32_t>((j + 1) >> 1) & 1u;
-        if (!pf_wait_warp(&bars->v_full[st], ph, fail, a.status)) break;
+        if (!pf_wait_warp2(&bars->v_full[st], ph, &bars->p_full[0], static_cast<uint32_t>(j) & 1u, fail, a.status))
+          break;
         if (j == n_tiles - 1 && kv_end < (j + 1) * kPfKeys) {
           // keys past the end: zero their V rows (unused slots may hold NaN and 0 * NaN = NaN)
           const int r0 = kv_end - j * kPfKeys;
@@ -856,11 +863,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           __syncwarp();
         }
         const uint32_t pj = static_cast<uint32_t>(j) & 1u;
-        if (!pf_wait_warp(&bars->p_full[0], pj, fail, a.status)) break;
         issue_pv(j, 0);
         if (next) {
-          if (!pf_wait_warp(&bars->k_full[st ^ 1], ph_next, fail, a.status) ||
-              !pf_wait_warp(&bars->o_done[0], pj, fail, a.status))
+          if (!pf_wait_warp2(&bars->k_full[st ^ 1], ph_next, &bars->o_done[0], pj, fail, a.status))
             break;
           issue_qk(j + 1, 0);
         }
@@ -1126,7 +1131,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const bool next_in = j + 1 < ntiles;
         const bool next = next_in || have_nxt;
         const int k = cur.k0 + j;
-        if (!pf_wait_warp(&bars->v_full[st], ph, fail, a.status)) break;
+        if (!pf_wait_warp2(&bars->v_full[st], ph, &bars->p_full[0], pj, fail, a.status)) break;
         const int rows = cur.qlen < kPfRows * (cur.t + 1) ? cur.qlen : kPfRows * (cur.t + 1);
         const int kv_end = cur.P + rows;
         if (k == cur.nt - 1 && kv_end < (k + 1) * kPfKeys) {
@@ -1140,12 +1145,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           fence_proxy_async_smem();
           __syncwarp();
         }
-        if (!pf_wait_warp(&bars->p_full[0], pj, fail, a.status)) break;
         issue_pv(st, 0, j > 0);
         if (next) {
           if (!next_in && !pf_wait_warp(&bars->q_full, static_cast<uint32_t>(pi + 1) & 1u, fail, a.status)) break;
-          if (!pf_wait_warp(&bars->k_full[st ^ 1], static_cast<uint32_t>((gj + 1) >> 1) & 1u, fail, a.status) ||
-              !pf_wait_warp(&bars->o_done[0], pj, fail, a.status))
+          if (!pf_wait_warp2(&bars->k_full[st ^ 1], static_cast<uint32_t>((gj + 1) >> 1) & 1u, &bars->o_done[0], pj,
+                             fail, a.status))
             break;
           issue_qk(st ^ 1, 0);
         }
