@@ -18,10 +18,13 @@
 //
 //  * Work is the list of (request, KV head, page) triples, ordered by request,
 //    then KV head, then page. The kernel is persistent: gridDim.x CTAs (the SM
-//    count times the CTAs resident per SM) each take an equal contiguous share
-//    of that list, computed on the device from seq_lens, so the grid depends
-//    only on host-known sizes (CUDA-graph friendly) and every CTA streams the
-//    same number of pages whatever the length mix.
+//    count times the CTAs resident per SM) each take a contiguous share of that
+//    list, computed on the device from seq_lens, so the grid depends only on
+//    host-known sizes (CUDA-graph friendly). Shares are equal in cost: a page
+//    costs 1 and, for batches (the polled merge below), each (request, KV head)
+//    that starts inside a share costs kPieceCost more, because a piece boundary
+//    stalls the CTA's stream (a warp merge behind a barrier, the refill of the
+//    stage ring after it) and a split piece's merge waits on its other holders.
 //  * A CTA's share is cut into pieces, one per (request, KV head) it touches.
 //    Its consumer warps take the share's pages round-robin (page f of the share
 //    goes to consumer (f - lo) mod kCons, across piece boundaries). A producer warp
@@ -94,6 +97,9 @@ namespace pkv {
 #ifndef PKV_DEC_ROUND_PAGES  // pages the producer issues per round
 #define PKV_DEC_ROUND_PAGES 8
 #endif
+#ifndef PKV_DEC_PIECE_COST  // pages a (request, KV head) boundary inside a share counts for (polled merge)
+#define PKV_DEC_PIECE_COST 32
+#endif
 constexpr int kCons = PKV_DEC_CONSUMERS;  // consumer warps; one more warp produces
 constexpr int kConsThreads = kCons * 32;
 constexpr int kDecThreads = kConsThreads + 32;
@@ -101,7 +107,7 @@ constexpr int kDecCtasPerSm = PKV_DEC_CTAS_PER_SM;
 constexpr int kRoundPages = PKV_DEC_ROUND_PAGES;
 constexpr int kMaxDecodeBatch = 1024;
 constexpr int kMaxGrid = 2048;  // partial-record slots are sized for this many CTAs
-constexpr int kMinShare = 8;    // pages a CTA's share holds at least (when the step has that many)
+constexpr int kMinShare = 8;    // pages per CTA at least on average (when the step has that many)
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kSmemMisc = 16;                // flag words
 constexpr int kSmemAlign = 1024;             // the ring starts on a 1024-byte boundary (swizzle atoms)
@@ -178,7 +184,7 @@ struct DecGeo {
   static_assert(kMergeCap >= 1, "a record fits the ring");
   __device__ __forceinline__ static int hkv(const DecodeArgs& a) { return kFixed ? kKVHeads : a.hkv; }
   __device__ __forceinline__ static int gq(const DecodeArgs& a) { return kFixed ? kGroup : a.gq; }
-  static size_t smem_bytes(int batch) { return kSmemFixed + static_cast<size_t>(2 * batch + 1) * 4; }
+  static size_t smem_bytes(int batch) { return kSmemFixed + static_cast<size_t>(3 * batch + 2) * 4; }
 };
 
 // A piece: pages [p0, p1) of KV head h of request b; flattened indices [fstart, fend).
@@ -216,11 +222,51 @@ __device__ __forceinline__ bool find_piece(long long f, long long hi, const int*
   return true;
 }
 
-// CTA whose share [lo(c), lo(c+1)) contains flattened index f, with lo(c) = c * T / n.
-__device__ __forceinline__ int cta_of(long long f, long long T, int n) {
-  return static_cast<int>(((f + 1) * n + T - 1) / T - 1);
-}
-__device__ __forceinline__ long long share_lo(int c, long long T, int n) { return static_cast<long long>(c) * T / n; }
+// The shares. Each (request, KV head) boundary inside a share costs kLam pages
+// (the warp merge behind a barrier, the record, the refill of the stage ring
+// after it, the merge's wait for the pair's other holders), so a flattened index
+// f costs C(f) = f + kLam * (pairs starting in (0, f]), and CTA c holds the
+// indices f with floor(c Ctot / n) <= C(f) < floor((c + 1) Ctot / n), Ctot =
+// T + kLam * (pairs - 1): lo(c) is the smallest f with C(f) >= floor(c Ctot / n).
+// A share that falls inside one boundary's jump is empty; the holders of a pair
+// are still consecutive, non-empty shares. With kLam = 0 the shares are equal in
+// pages (lo(c) = c T / n). pcp[b] = non-empty pairs before request b. Measured at
+// bs16: kLam 0 / 8 / 16 / 24 / 32 / 40 / 64 gave 18.67 / 18.82 / 18.55 / 18.02 /
+// 17.91 / 18.02 / 18.95 us per layer; the counted merge (one long request) keeps 0.
+template <int kLam>
+struct Shares {
+  static constexpr int lam = kLam;
+  const int* pref;
+  const int* pcp;
+  const int* sl;
+  int batch, hkv, n;
+  long long T, Ctot;
+  __device__ __forceinline__ long long cost(long long f) const {  // f < T
+    if (kLam == 0) return f;
+    const int b = request_of(f, pref, batch);
+    return f + static_cast<long long>(lam) * (pcp[b] + (f - pref[b]) / pages_of(sl[b]));
+  }
+  // first index of CTA c's share: the smallest f with C(f) >= floor(c Ctot / n)
+  __device__ __forceinline__ long long lo(int c) const {
+    const long long y = static_cast<long long>(c) * Ctot / n;
+    if (kLam == 0) return y;
+    int lb = 0, hb = batch - 1;
+    while (lb < hb) {
+      const int mid = (lb + hb + 1) >> 1;
+      if (pref[mid] + static_cast<long long>(lam) * pcp[mid] <= y) lb = mid; else hb = mid - 1;
+    }
+    const int np = pages_of(sl[lb]);
+    if (np == 0) return pref[lb];
+    const long long key = pref[lb] + static_cast<long long>(lam) * pcp[lb];
+    long long h = (y - key) / (np + lam);
+    if (h > hkv - 1) h = hkv - 1;
+    const long long s_next = pref[lb] + (h + 1) * np;
+    const long long f = y - static_cast<long long>(lam) * (pcp[lb] + h);
+    return f < s_next ? f : s_next;
+  }
+  // the CTA whose share holds index f (< T)
+  __device__ __forceinline__ int cta(long long f) const { return static_cast<int>(((cost(f) + 1) * n + Ctot - 1) / Ctot - 1); }
+};
 
 // Polled records are 32-bit words: an fp32 value rounded to nearest (even) at
 // 15 mantissa bits, with the tag in the freed low byte. Each word is one
@@ -331,6 +377,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
   int* flag = reinterpret_cast<int*>(csbuf + Geo::kSmemCs);  // [0..1] merge flags, [2] a wait failed
   int* pref = flag + kSmemMisc / 4;
   int* sl = pref + a.batch + 1;
+  int* pcp = sl + a.batch;  // [batch + 1] non-empty (request, KV head) pairs before each request
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -364,7 +411,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
 
   // seq lens (clamped) and the exclusive prefix of (KV head, page) pairs per request
   if (warp == 0) {
-    int carry = 0;
+    int carry = 0, pcarry = 0;
     const int cap = a.max_pages * kPageSize;
     for (int base = 0; base < batch; base += 32) {
       const int b = base + lane;
@@ -386,16 +433,28 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
       }
       if (b < batch) pref[b] = carry + x - v;
       carry += __shfl_sync(kFull, x, 31);
+      const int w = kPolled && s > 0 ? hkv : 0;  // (the counted instantiation prices no boundary)
+      int z = w;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(kFull, z, o);
+        if (lane >= o) z += y;
+      }
+      if (b < batch) pcp[b] = pcarry + z - w;
+      pcarry += __shfl_sync(kFull, z, 31);
     }
-    if (lane == 0) pref[batch] = carry;
+    if (lane == 0) {
+      pref[batch] = carry;
+      pcp[batch] = pcarry;
+    }
   }
   fence_barrier_init();
   __syncthreads();
 
-  // Only min(gridDim.x, T / 8) CTAs (at least one) take a share, so that every
-  // share holds at least 8 pages (a tiny step is not spread so thin that its
-  // merges dominate) and the CTAs between the first and last holder of a
-  // (request, KV head) all hold a piece of it.
+  // Only min(gridDim.x, T / 8) CTAs (at least one) take a share, so that a share
+  // holds 8 pages on average (a tiny step is not spread so thin that its merges
+  // dominate); the CTAs between the first and last holder of a (request, KV head)
+  // all hold a piece of it.
   const long long T = pref[batch];
   const long long g_want = T / kMinShare > 0 ? T / kMinShare : 1;
   const int nsh = static_cast<int>(g_want < gridDim.x ? g_want : gridDim.x);
@@ -417,8 +476,19 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
     zero_empty_rows(0, kDecThreads);
     return;
   }
-  const long long lo = share_lo(blockIdx.x, T, nsh);
-  const long long hi = share_lo(blockIdx.x + 1, T, nsh);
+  // the polled instantiation (batches, many short pairs) prices a pair boundary; the counted one
+  // (one long request) does not
+  Shares<kPolled ? PKV_DEC_PIECE_COST : 0> sh;
+  sh.pref = pref;
+  sh.pcp = pcp;
+  sh.sl = sl;
+  sh.batch = batch;
+  sh.hkv = hkv;
+  sh.n = nsh;
+  sh.T = T;
+  sh.Ctot = T + static_cast<long long>(sh.lam) * (pcp[batch] > 0 ? pcp[batch] - 1 : 0);
+  const long long lo = sh.lo(blockIdx.x);
+  const long long hi = sh.lo(blockIdx.x + 1);
 
   // ============================================================== producer warp
   // Walks the share 32 flattened indices at a time, one per lane: each lane
@@ -566,12 +636,6 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
   uint32_t koff[kKS], voff[kKS];
   mma_offsets<kKS>(koff, voff);
 
-  if (a.early) {
-    grid_dependency_wait();
-    allow_dependents();
-  }
-  zero_empty_rows(0, kConsThreads);
-
   int k = 0;  // pages of this warp's sequence visited so far
   bool failed = false;
 
@@ -601,9 +665,9 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
   auto span_of = [&](int b, int h, int& cfirst, int& n, bool& first_has_two) {
     const int np = pages_of(sl[b]);
     const long long fseg = pref[b] + static_cast<long long>(h) * np;
-    cfirst = cta_of(fseg, T, nsh);
-    n = cta_of(fseg + np - 1, T, nsh) - cfirst + 1;
-    first_has_two = share_lo(cfirst, T, nsh) < fseg;
+    cfirst = sh.cta(fseg);
+    n = sh.cta(fseg + np - 1) - cfirst + 1;
+    first_has_two = sh.lo(cfirst) < fseg;
   };
   // Split pieces whose partial records are written but not yet counted: only
   // the first and the last piece of a share can be split, and both are counted
@@ -619,6 +683,17 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
   // merges it; that pair can only be its first piece, begun by an earlier CTA.
   const bool merger = kPolled && have && pc.p0 > 0 && pc.p1 == pc.np;
   const int mb = pc.b, mh = pc.h;
+  // the merger's holders, worked out now rather than after the stream
+  int m_cf = 0, m_n = 0;
+  bool m_two = false;
+  if (merger) span_of(mb, mh, m_cf, m_n, m_two);
+  // in early mode the share, its pieces and the merger's holders above came from the lengths alone;
+  // q, the output and the records wait for the predecessor
+  if (a.early) {
+    grid_dependency_wait();
+    allow_dependents();
+  }
+  zero_empty_rows(0, kConsThreads);
   if (have) stage_q(pc, 0);
   if (warp == 0) cp_async_wait_all();
   consumer_sync();
@@ -822,9 +897,8 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
     // also load the m/l words); a record is read again until every word carries
     // the tag. The order depends only on the pair, so the result is the same bits
     // on every call.
-    int cf = 0, n = 0;
-    bool two = false;
-    span_of(mb, mh, cf, n, two);
+    const int cf = m_cf, n = m_n;
+    const bool two = m_two;
     auto rec_of = [&](int t) {
       const size_t slot = 2 * static_cast<size_t>(cf + t) + ((t == 0 && two) ? 1 : 0);
       return a.tagged + slot * Geo::kSplitWords;

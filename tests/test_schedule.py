@@ -5,8 +5,11 @@ never waits on a stage more than one barrier phase ahead.
 
 The model of one CTA of the persistent decode kernel (4 consumer warps, a
 3-stage ring each, 32-lane producer warp):
-- the CTA's share [lo, hi) of the flattened (request, KV head, page) list, with
-  lo(c) = c * T // G over G = min(grid, max(1, T // 8)) CTAs;
+- the CTA's share [lo, hi) of the flattened (request, KV head, page) list over
+  G = min(grid, max(1, T // 8)) CTAs: shares equal in cost, a page costing 1 and
+  each (request, KV head) that starts inside a share LAM pages more (LAM = 32
+  for batches, the polled merge; 0 for few long requests, the counted merge);
+  with LAM = 0, lo(c) = c * T // G;
 - the share is cut into pieces at (request, KV head) boundaries; the consumers
   meet at the end of every piece (a CTA barrier) before any starts the next;
 - page f goes to consumer assign(f); each consumer takes its pages in order,
@@ -25,15 +28,71 @@ from paged_kv_decode_gb300 import workloads as W
 
 CONS, RING, CHUNK, PAGE, HKV = 4, 3, 32, 16, 8
 ROUND_SIZES = (1, 4, 8, 12)  # the shipped round size (8), the earlier one (12) and others measured
+LAM = 32  # the kernel's piece cost for batches (polled merge)
+POLL_MAX = 24  # the kernel takes the polled merge when grid <= POLL_MAX * batch * KV heads
 
 
-def shares(seq_lens, grid):
-    pages = [(int(s) + PAGE - 1) // PAGE for s in seq_lens]
-    pref = np.concatenate([[0], np.cumsum([p * HKV for p in pages])]).astype(np.int64)
-    T = int(pref[-1])
-    G = min(grid, max(1, T // 8))  # shares of at least 8 pages
+class ShareMap:
+    """The kernel's share map, in the same integer arithmetic: cost C(f) = f + lam * (pairs starting
+    in (0, f]); lo(c) = smallest f with C(f) >= c * Ctot // n; cta(f) = the CTA holding f."""
+
+    def __init__(self, seq_lens, grid, lam, hkv=HKV):
+        self.pages = [(int(s) + PAGE - 1) // PAGE for s in seq_lens]
+        self.hkv, self.lam, self.batch = hkv, lam, len(self.pages)
+        self.pref, self.pcp = [0], [0]
+        for p in self.pages:
+            self.pref.append(self.pref[-1] + p * hkv)
+            self.pcp.append(self.pcp[-1] + (hkv if p > 0 else 0))
+        self.T = self.pref[-1]
+        self.n = min(grid, max(1, self.T // 8))
+        self.Ctot = self.T + lam * max(self.pcp[-1] - 1, 0)
+
+    def request_of(self, f):
+        lo_b, hi_b = 0, self.batch - 1
+        while lo_b < hi_b:
+            mid = (lo_b + hi_b + 1) >> 1
+            if self.pref[mid] <= f:
+                lo_b = mid
+            else:
+                hi_b = mid - 1
+        return lo_b
+
+    def cost(self, f):
+        b = self.request_of(f)
+        return f + self.lam * (self.pcp[b] + (f - self.pref[b]) // self.pages[b])
+
+    def lo(self, c):
+        y = c * self.Ctot // self.n
+        if self.lam == 0:
+            return y
+        lb, hb = 0, self.batch - 1
+        while lb < hb:
+            mid = (lb + hb + 1) >> 1
+            if self.pref[mid] + self.lam * self.pcp[mid] <= y:
+                lb = mid
+            else:
+                hb = mid - 1
+        np_ = self.pages[lb]
+        if np_ == 0:
+            return self.pref[lb]
+        key = self.pref[lb] + self.lam * self.pcp[lb]
+        h = min((y - key) // (np_ + self.lam), self.hkv - 1)
+        return min(y - self.lam * (self.pcp[lb] + h), self.pref[lb] + (h + 1) * np_)
+
+    def cta(self, f):
+        return ((self.cost(f) + 1) * self.n + self.Ctot - 1) // self.Ctot - 1
+
+
+def kernel_lam(seq_lens, grid):
+    """The piece cost the kernel uses for this step (the polled merge prices boundaries)."""
+    return LAM if grid <= POLL_MAX * len(seq_lens) * HKV else 0
+
+
+def shares(seq_lens, grid, lam=None):
+    sm = ShareMap(seq_lens, grid, kernel_lam(seq_lens, grid) if lam is None else lam)
+    pages, pref = sm.pages, sm.pref
     seg_starts = sorted({int(pref[b]) + h * pages[b] for b in range(len(pages)) if pages[b] for h in range(HKV)})
-    return [(c * T // G, (c + 1) * T // G) for c in range(G)], seg_starts
+    return [(sm.lo(c), sm.lo(c + 1)) for c in range(sm.n)], seg_starts
 
 
 def piece_index(lo, hi, seg_starts):
@@ -66,6 +125,8 @@ def assign_piece(lo, hi, seg_starts):
 
 def simulate(lo, hi, seg_starts, assign, round_pages=CONS * RING):
     n = hi - lo
+    if n == 0:  # an empty share (one that falls inside a boundary's cost): nothing to stream
+        return True
     piece = piece_index(lo, hi, seg_starts)
     cons = assign(lo, hi, seg_starts)
     k, seen = [], [0] * CONS
@@ -120,8 +181,8 @@ def simulate(lo, hi, seg_starts, assign, round_pages=CONS * RING):
             return all(done)
 
 
-def all_ctas_finish(seq_lens, assign, grid=304, round_pages=CONS * RING):
-    sh, segs = shares(seq_lens, grid)
+def all_ctas_finish(seq_lens, assign, grid=304, round_pages=CONS * RING, lam=None):
+    sh, segs = shares(seq_lens, grid, lam)
     return all(simulate(lo, hi, segs, assign, round_pages) for lo, hi in sh)
 
 
@@ -172,6 +233,50 @@ def test_piece_relative_schedule_deadlocks_on_one_page_runs():
     # the rule the share-relative assignment replaced: eight one-page pieces
     # pile onto consumer 0 and the producer's second round waits on consumers
     # that are held at a piece boundary behind it
-    assert not all_ctas_finish(MIXES["short_then_long"], assign_piece, round_pages=None)
-    assert all_ctas_finish(MIXES["short_then_long"], assign_share, round_pages=None)
+    # (with the shares of that time: equal page counts)
+    assert not all_ctas_finish(MIXES["short_then_long"], assign_piece, round_pages=None, lam=0)
+    assert all_ctas_finish(MIXES["short_then_long"], assign_share, round_pages=None, lam=0)
 
+
+
+SHARE_MIXES = [[3, 30000, 5, 9000], [0, 700, 0, 33, 1, 2900, 0], list(range(1, 65)), [40000], [1]]
+
+
+@pytest.mark.parametrize("lam", [0, 8, LAM, 64])
+@pytest.mark.parametrize("grid", [7, 64, 304])
+def test_share_map_covers_the_list_and_keeps_holders_consecutive(lam, grid):
+    # every page belongs to exactly the CTA cta() names; shares tile [0, T) in order; the CTAs holding a
+    # (request, KV head) are consecutive and none of them is empty (the merges rely on both); lam 0 gives
+    # equal page counts
+    rng = np.random.default_rng(grid + lam)
+    mixes = SHARE_MIXES + [[int(x) for x in rng.choice([0, 1, 5, 16, 17, 40, 300, 2000, 12000],
+                                                        size=int(rng.integers(1, 40)))] for _ in range(12)]
+    for lens in mixes:
+        if sum(lens) == 0:
+            continue
+        for hkv in (1, 2, 8):
+            sm = ShareMap(lens, grid, lam, hkv)
+            L = [sm.lo(c) for c in range(sm.n + 1)]
+            assert L[0] == 0 and L[-1] == sm.T and all(L[i] <= L[i + 1] for i in range(sm.n))
+            if lam == 0:
+                assert L == [c * sm.T // sm.n for c in range(sm.n + 1)]
+            for f in range(sm.T):
+                c = sm.cta(f)
+                assert L[c] <= f < L[c + 1]
+            for b, p in enumerate(sm.pages):
+                for h in range(hkv if p else 0):
+                    fs = sm.pref[b] + h * p
+                    for c in range(sm.cta(fs), sm.cta(fs + p - 1) + 1):
+                        assert L[c] < L[c + 1] and L[c] < fs + p and L[c + 1] > fs
+
+
+def test_piece_cost_moves_pages_from_ctas_with_boundaries():
+    # at bs16 a share with a (request, KV head) boundary gets fewer pages than one without
+    lens = list(W.config_seq_lens(2))
+    sm = ShareMap(lens, 304, LAM)
+    starts = {sm.pref[b] + h * p for b, p in enumerate(sm.pages) for h in range(HKV)}
+    one, two = [], []
+    for c in range(sm.n):
+        lo, hi = sm.lo(c), sm.lo(c + 1)
+        (two if any(lo < x < hi for x in starts) else one).append(hi - lo)
+    assert one and two and np.mean(two) + LAM // 2 < np.mean(one)
