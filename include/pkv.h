@@ -182,7 +182,9 @@ size_t pkv_decode_workspace_bytes(const pkv_cache_desc* desc, int32_t batch, int
  *                (larger values are clamped and set PKV_ERR_OUT_OF_BOUNDS)
  *  out:          bf16 [batch][num_q_heads][head_dim]
  *  scale:        softmax scale (1/sqrt(head_dim) for the Qwen3 decoder)
- *  batch:        >= 0 (0 launches nothing), max_pages_per_seq >= 1
+ *  batch:        >= 0 (0 launches nothing), max_pages_per_seq >= 1;
+ *                batch * max_pages_per_seq * max(num_kv_heads, 8) < 2^31
+ *                (PKV_ERR_BAD_SHAPE beyond; the same for the fused calls)
  *  workspace:    >= pkv_decode_workspace_bytes(desc, batch, max_pages_per_seq)
  */
 int pkv_decode_attn(const void* q, const void* k_pages, const void* v_pages, const int32_t* block_table,

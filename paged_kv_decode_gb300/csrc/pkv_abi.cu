@@ -68,9 +68,12 @@ int check_desc_decode(const pkv_cache_desc* d) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Largest block table the kernels index with 32-bit triple counts.
-bool table_fits(int32_t rows, int32_t max_pages) {
-  return static_cast<long long>(rows) * max_pages * 8 < (1LL << 31);
+// Largest block table the kernels index with 32-bit counts of (request, KV
+// head, page) triples (the decode kernel's flattened list: at most rows *
+// max_pages * KV heads entries).
+bool table_fits(int32_t rows, int32_t max_pages, int32_t kv_heads = 8) {
+  const long long h = kv_heads > 8 ? kv_heads : 8;
+  return static_cast<long long>(rows) * max_pages * h < (1LL << 31);
 }
 
 }  // namespace
@@ -137,7 +140,7 @@ static size_t decode_ws(const pkv_cache_desc* desc, int32_t batch, int sms) {
 
 size_t pkv_decode_workspace_bytes(const pkv_cache_desc* desc, int32_t batch, int32_t max_pages_per_seq) {
   if (check_desc_decode(desc) != PKV_OK || batch < 0 || max_pages_per_seq < 1) return 0;
-  if (batch > pkv::decode_max_batch() || !table_fits(batch, max_pages_per_seq)) return 0;
+  if (batch > pkv::decode_max_batch() || !table_fits(batch, max_pages_per_seq, desc->num_kv_heads)) return 0;
   int sms = 0;
   if (current_device(&sms) != PKV_OK) return 0;
   return decode_ws(desc, batch, sms);
@@ -151,7 +154,7 @@ int pkv_decode_attn(const void* q, const void* k_pages, const void* v_pages, con
   if (rc != PKV_OK) return rc;
   if (batch < 0 || max_pages_per_seq < 1) return PKV_ERR_BAD_SHAPE;
   if (batch > pkv::decode_max_batch()) return PKV_ERR_UNSUPPORTED;
-  if (!table_fits(batch, max_pages_per_seq)) return PKV_ERR_BAD_SHAPE;
+  if (!table_fits(batch, max_pages_per_seq, desc->num_kv_heads)) return PKV_ERR_BAD_SHAPE;
   if (workspace == nullptr) return PKV_ERR_NULL_ARG;
   if (batch == 0) return PKV_OK;
   if (!q || !k_pages || !v_pages || !block_table || !seq_lens || !out) return PKV_ERR_NULL_ARG;
@@ -175,7 +178,7 @@ static int decode_append(const void* q, const void* k_new, const void* v_new, vo
   if (rc != PKV_OK) return rc;
   if (batch < 0 || max_pages_per_seq < 1) return PKV_ERR_BAD_SHAPE;
   if (batch > pkv::decode_max_batch()) return PKV_ERR_UNSUPPORTED;
-  if (!table_fits(batch, max_pages_per_seq)) return PKV_ERR_BAD_SHAPE;
+  if (!table_fits(batch, max_pages_per_seq, desc->num_kv_heads)) return PKV_ERR_BAD_SHAPE;
   if (workspace == nullptr) return PKV_ERR_NULL_ARG;
   if (batch == 0) return PKV_OK;
   if (!q || !k_new || !v_new || !k_pages || !v_pages || !block_table || !seq_lens || !out) return PKV_ERR_NULL_ARG;

@@ -69,6 +69,15 @@ def test_host_argument_checks(lib):
     assert lib.pkv_decode_attn(None, None, None, None, None, None, 1.0, None, ctypes.byref(d), 1, 0, None, 0) == -2
     zero_pages = _desc(num_pages=0)
     assert lib.pkv_append(None, None, None, 1, None, None, ctypes.byref(zero_pages), None, None, 0) == -2
+    # the decode kernel counts (request, KV head, page) triples in 32 bits: batch * max_pages * max(KV heads, 8)
+    # must stay below 2^31 (1024 * 65536 * 32 = 2^31 is refused for 32 KV heads, the same table for 8 is not)
+    mha = _desc(num_q_heads=32, num_kv_heads=32)
+    assert lib.pkv_decode_attn(None, None, None, None, None, None, 1.0, None, ctypes.byref(mha), 1024, 65536,
+                               None, 0) == -2
+    assert lib.pkv_decode_append_attn(None, None, None, None, None, None, None, None, 1.0, None, ctypes.byref(mha),
+                                      1024, 65536, None, 0, 0) == -2
+    assert lib.pkv_decode_attn(None, None, None, None, None, None, 1.0, None, ctypes.byref(d), 1024, 65536,
+                               None, 0) == -1
     # nothing to do is fine, without any device
     assert lib.pkv_append(None, None, None, 0, None, None, ctypes.byref(d), None, None, 0) == 0
     # missing pointers
