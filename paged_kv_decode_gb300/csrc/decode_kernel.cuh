@@ -109,7 +109,7 @@ constexpr int kMaxDecodeBatch = 1024;
 constexpr int kMaxGrid = 2048;  // partial-record slots are sized for this many CTAs
 constexpr int kMinShare = 8;    // pages per CTA at least on average (when the step has that many)
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kSmemMisc = 16;                // flag words
+constexpr int kSmemMisc = 32;                // flag words, then the CTA's share bounds
 constexpr int kSmemAlign = 1024;             // the ring starts on a 1024-byte boundary (swizzle atoms)
 constexpr uint32_t kTag = 0xa5u;             // low byte of a word written by this call
 constexpr int kPollMax = 24;                 // polled merge up to this many holders per pair
@@ -241,6 +241,25 @@ struct Shares {
   const int* sl;
   int batch, hkv, n;
   long long T, Ctot;
+  long long q;  // Ctot / n
+  int r;        // Ctot mod n
+  __device__ __forceinline__ void init(const int* pref_, const int* pcp_, const int* sl_, int batch_, int hkv_,
+                                       int n_) {
+    pref = pref_;
+    pcp = pcp_;
+    sl = sl_;
+    batch = batch_;
+    hkv = hkv_;
+    n = n_;
+    T = pref[batch];
+    Ctot = T + static_cast<long long>(lam) * (pcp[batch] > 0 ? pcp[batch] - 1 : 0);
+    q = Ctot / n;
+    r = static_cast<int>(Ctot - q * n);
+  }
+  // floor(c Ctot / n) without a 64-bit division (c r < 2^22)
+  __device__ __forceinline__ long long y_of(int c) const {
+    return c * q + static_cast<unsigned>(c * r) / static_cast<unsigned>(n);
+  }
   __device__ __forceinline__ long long cost(long long f) const {  // f < T
     if (kLam == 0) return f;
     const int b = request_of(f, pref, batch);
@@ -248,7 +267,7 @@ struct Shares {
   }
   // first index of CTA c's share: the smallest f with C(f) >= floor(c Ctot / n)
   __device__ __forceinline__ long long lo(int c) const {
-    const long long y = static_cast<long long>(c) * Ctot / n;
+    const long long y = y_of(c);
     if (kLam == 0) return y;
     int lb = 0, hb = batch - 1;
     while (lb < hb) {
@@ -258,7 +277,8 @@ struct Shares {
     const int np = pages_of(sl[lb]);
     if (np == 0) return pref[lb];
     const long long key = pref[lb] + static_cast<long long>(lam) * pcp[lb];
-    long long h = (y - key) / (np + lam);
+    // (y - key < (np + lam) * hkv < 2^32: the table bound keeps max_pages * hkv below 2^31)
+    long long h = static_cast<unsigned>(y - key) / static_cast<unsigned>(np + lam);
     if (h > hkv - 1) h = hkv - 1;
     const long long s_next = pref[lb] + (h + 1) * np;
     const long long f = y - static_cast<long long>(lam) * (pcp[lb] + h);
@@ -374,7 +394,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
   float* merge = reinterpret_cast<float*>(smem + Geo::kSmemRing + Geo::kSmemBars);
   unsigned char* qbuf = reinterpret_cast<unsigned char*>(merge + Geo::kMergeFloats);
   unsigned char* csbuf = qbuf + Geo::kSmemQ;
-  int* flag = reinterpret_cast<int*>(csbuf + Geo::kSmemCs);  // [0..1] merge flags, [2] a wait failed
+  int* flag = reinterpret_cast<int*>(csbuf + Geo::kSmemCs);  // [0..1] merge flags, [2] a wait failed, [4..5] share
   int* pref = flag + kSmemMisc / 4;
   int* sl = pref + a.batch + 1;
   int* pcp = sl + a.batch;  // [batch + 1] non-empty (request, KV head) pairs before each request
@@ -447,6 +467,16 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
       pref[batch] = carry;
       pcp[batch] = pcarry;
     }
+    // this CTA's share bounds, once: lanes 0 and 1 work out lo(c) and lo(c + 1) side by side
+    __syncwarp();
+    const long long Tw = carry;
+    const long long gw = Tw / kMinShare > 0 ? Tw / kMinShare : 1;
+    const int nw = static_cast<int>(gw < gridDim.x ? gw : gridDim.x);
+    if (lane < 2 && static_cast<int>(blockIdx.x) < nw) {
+      Shares<kPolled ? PKV_DEC_PIECE_COST : 0> sw;
+      sw.init(pref, pcp, sl, batch, hkv, nw);
+      flag[4 + lane] = static_cast<int>(sw.lo(blockIdx.x + lane));
+    }
   }
   fence_barrier_init();
   __syncthreads();
@@ -477,18 +507,9 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
     return;
   }
   // the polled instantiation (batches, many short pairs) prices a pair boundary; the counted one
-  // (one long request) does not
-  Shares<kPolled ? PKV_DEC_PIECE_COST : 0> sh;
-  sh.pref = pref;
-  sh.pcp = pcp;
-  sh.sl = sl;
-  sh.batch = batch;
-  sh.hkv = hkv;
-  sh.n = nsh;
-  sh.T = T;
-  sh.Ctot = T + static_cast<long long>(sh.lam) * (pcp[batch] > 0 ? pcp[batch] - 1 : 0);
-  const long long lo = sh.lo(blockIdx.x);
-  const long long hi = sh.lo(blockIdx.x + 1);
+  // (one long request) does not. The share bounds came from warp 0 (T < 2^31: int words)
+  const long long lo = flag[4];
+  const long long hi = flag[5];
 
   // ============================================================== producer warp
   // Walks the share 32 flattened indices at a time, one per lane: each lane
@@ -662,6 +683,8 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
   // CTAs cfirst .. cfirst + n - 1 hold the pieces of (request b, KV head h); the
   // record of CTA c is in slot 2c, or 2c + 1 when it is the second split piece
   // of c's share (first_has_two: the first holder's share starts before (b, h)).
+  Shares<kPolled ? PKV_DEC_PIECE_COST : 0> sh;
+  sh.init(pref, pcp, sl, batch, hkv, nsh);
   auto span_of = [&](int b, int h, int& cfirst, int& n, bool& first_has_two) {
     const int np = pages_of(sl[b]);
     const long long fseg = pref[b] + static_cast<long long>(h) * np;
