@@ -50,7 +50,7 @@ WORKLOAD = ("qwen3-0.6b decode step: 28 layers x bs16, 16q/8kv heads, d128, page
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the decode kernel source it was
 # measured on (sha256 prefix of csrc/decode_kernel.cuh followed by csrc/pkv_mma.cuh); any other source
 # reports null.
-NCU_DECODE_TRAFFIC = {"3a43598de0080b29": 107_483_904 + 3_183_616}
+NCU_DECODE_TRAFFIC = {"5ee96c44b9f36951": 107_485_952 + 3_378_432}
 
 
 def _decode_traffic():
