@@ -43,7 +43,9 @@
 //    value operand's registers, so unused slots may hold anything, NaN included.
 //  * Optional fused append: the producer lane that copies a request's last
 //    page first writes the request's new K/V row for that head into it
-//    (generic stores, then a proxy fence so its own tensor copy sees them). With
+//    (generic stores, then a proxy fence so its own tensor copy sees them); in
+//    early mode that lane alone waits for the predecessor first, so the other
+//    pages of its chunk are copied before the dependency resolves. With
 //    a cos/sin table the whole producer warp writes the row instead, rotating
 //    the key (rotary position embedding at the new token's position, pairs
 //    (i, i + head_dim / 2), fp32, rounded to bf16), and each piece's query rows
@@ -565,7 +567,10 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
       int rounds = valid ? my_round + 1 : 0;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) rounds = max(rounds, __shfl_xor_sync(kFull, rounds, o));
-      if (kFused && !waited && __any_sync(kFull, wslot >= 0)) {  // new rows come from the predecessor
+      // New rows come from the predecessor. With the rotary embedding the whole warp writes them
+      // before the chunk's copies, so it waits first; otherwise only the lane whose page takes a
+      // new row waits, right before it writes the row, and the chunk's other pages go out at once.
+      if (kRope && !waited && __any_sync(kFull, wslot >= 0)) {
         grid_dependency_wait();
         allow_dependents();
         waited = true;
@@ -619,6 +624,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
             if (!id_ok) set_status(a.status, PKV_ERR_OUT_OF_BOUNDS);
             const int pid = id_ok ? id : 0;
             if (kFused && !kRope && wslot >= 0 && id_ok) {
+              grid_dependency_wait();  // (returns at once after the first time)
               // fused append: this page holds the request's new token; write its K and V rows
               // for this head, then order the writes before this lane's tensor copy of the page
               const uint4* ks = reinterpret_cast<const uint4*>(a.k_new + (static_cast<size_t>(bb) * hkv + hh) * D);
@@ -645,7 +651,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(cons
       }
       pfail = __any_sync(kFull, pfail);
     }
-    if (!waited) {
+    if (!kRope || !waited) {
       grid_dependency_wait();
       allow_dependents();
     }
