@@ -79,6 +79,8 @@
 
 #include <math_constants.h>
 
+#include <type_traits>
+
 #include "pkv_device.cuh"
 #include "pkv_kernels.h"
 #include "pkv_mma.cuh"
@@ -115,6 +117,13 @@ constexpr int kSmemMisc = 32;                // flag words, then the CTA's share
 constexpr int kSmemAlign = 1024;             // the ring starts on a 1024-byte boundary (swizzle atoms)
 constexpr uint32_t kTag = 0xa5u;             // low byte of a word written by this call
 constexpr int kPollMax = 24;                 // polled merge up to this many holders per pair
+// A step with few (request, KV head) pairs for the two-CTA grid (the counted
+// merge) runs the wide launch shape when the block table can hold at least this
+// many (request, KV head, page) triples (batch x max_pages x KV heads); with half
+// the CTAs, a pair then has few enough holders for the polled merge. One 40k-token
+// request measured 29.6 -> 28.1 us per layer, 16k 14.6 -> 13.5, but 4k 7.3 -> 7.9
+// (half the CTAs for a small step), hence the bound.
+constexpr long long kWideMinPages = 8192;
 
 struct DecodeArgs {
   const __nv_bfloat16* q;      // [batch][hq][D]
@@ -142,18 +151,23 @@ struct DecodeArgs {
 };
 
 // Geometry of one instantiation: head_dim D, G query heads per KV head computed
-// (1, 2, 4 or 8), and whether the head counts are the Qwen3 decoder's 16 / 8
-// fixed at compile time (otherwise DecodeArgs::hkv / gq).
-template <int D_, int G_, bool kFixed_>
+// (1, 2, 4 or 8), whether the head counts are the Qwen3 decoder's 16 / 8 fixed
+// at compile time (otherwise DecodeArgs::hkv / gq), and the launch shape: two
+// CTAs per SM with kRing stages per consumer, or (kWide, for a few long requests)
+// one CTA per SM with twice the stages, so each (request, KV head) has half as
+// many holders to merge and each CTA twice the bytes in flight.
+template <int D_, int G_, bool kFixed_, bool kWide_ = false>
 struct DecGeo {
   static constexpr int D = D_;
   static constexpr int G = G_;
   static constexpr bool kFixed = kFixed_;
+  static constexpr bool kWide = kWide_;
+  static constexpr int kCtasPerSm = kWide ? 1 : kDecCtasPerSm;
   static_assert(D == 64 || D == 128, "head_dim 64 or 128");
   static_assert(G == 1 || G == 2 || G == 4 || G == 8, "one 8-column MMA tile of heads");
   static_assert(!kFixed || (D == kHeadDim && G == kGroup), "the fixed geometry is 16 / 8 / 128");
   static constexpr int kKS = D / 16;                    // 16-dim steps of both MMA products
-  static constexpr int kRing = D == 128 ? PKV_DEC_RING : 2 * PKV_DEC_RING;  // stages per consumer
+  static constexpr int kRing = (D == 128 ? PKV_DEC_RING : 2 * PKV_DEC_RING) * (kWide ? 2 : 1);  // per consumer
   static constexpr int kStages = kCons * kRing;
   static constexpr int kTile = kPageSize * D * 2;       // one (page, KV head) tile of K or V
   static constexpr int kStage = 2 * kTile;              // K tile + V tile
@@ -383,7 +397,7 @@ __device__ __forceinline__ void store_lane_state(float* mw, int lane, int h0, co
 // kPolled: the polled merge, else the counted one. Each combination is its own
 // instantiation, so a path carries no code (and no registers) for the others.
 template <class Geo, bool kFused, bool kRope, bool kPolled>
-__global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(const __grid_constant__ CUtensorMap kmap,
+__global__ void __launch_bounds__(kDecThreads, Geo::kCtasPerSm) decode_kernel(const __grid_constant__ CUtensorMap kmap,
                                                                              const __grid_constant__ CUtensorMap vmap,
                                                                              const DecodeArgs a) {
   constexpr int D = Geo::D, G = Geo::G, kKS = Geo::kKS, kRing = Geo::kRing, kStages = Geo::kStages;
@@ -1132,35 +1146,54 @@ inline size_t decode_counter_bytes(int32_t batch, int hkv) {
 
 template <class Geo>
 int launch_decode_geo(const DecodeLaunch& c) {
+  using GeoW = DecGeo<Geo::D, Geo::G, Geo::kFixed, true>;
   if (c.batch == 0) return PKV_OK;
   if (c.rope != nullptr && c.k_new == nullptr) return PKV_ERR_NULL_ARG;
-  const size_t smem = Geo::smem_bytes(c.batch);
   // Polled merge when a pair is expected to span at most kPollMax CTAs (equal
-  // lengths); the counted merge for few pairs over many CTAs.
+  // lengths); the counted merge for few pairs over many CTAs. Few pairs and a
+  // table that can hold a long step take the wide shape (half the CTAs), whose
+  // merge is chosen the same way over its own grid. The record slots are laid out
+  // for the two-CTA grid either way.
   const int grid = decode_grid(c.num_sms);
-  const bool polled = grid <= kPollMax * c.batch * c.hkv;
+  const long long pairs = static_cast<long long>(c.batch) * c.hkv;
+  // (head_dim 64 stays narrow: with one CTA per SM its consumers, four per SM, page too slowly -- one
+  // 40k-token request at 16/8/64 measured 19.0 us per layer wide against 17.8 narrow)
+  const bool wide = Geo::D == 128 && grid > kPollMax * pairs && pairs * c.max_pages >= kWideMinPages;
+  const int grid_used = wide ? (c.num_sms < kMaxGrid ? c.num_sms : kMaxGrid) : grid;
+  const bool polled = grid_used <= kPollMax * pairs;
+  const size_t smem = wide ? GeoW::smem_bytes(c.batch) : Geo::smem_bytes(c.batch);
   using Kern = void (*)(const CUtensorMap, const CUtensorMap, const DecodeArgs);
-  static const Kern kKerns[2][3] = {
+  // (the wide rows are never taken at head_dim 64; they name the narrow kernels there so that
+  // no wide head_dim-64 instantiation is built)
+  using GW = typename std::conditional<Geo::D == 128, GeoW, Geo>::type;
+  static const Kern kKerns[4][3] = {
       {decode_kernel<Geo, false, false, false>, decode_kernel<Geo, true, false, false>,
        decode_kernel<Geo, true, true, false>},
       {decode_kernel<Geo, false, false, true>, decode_kernel<Geo, true, false, true>,
-       decode_kernel<Geo, true, true, true>}};
+       decode_kernel<Geo, true, true, true>},
+      {decode_kernel<GW, false, false, false>, decode_kernel<GW, true, false, false>,
+       decode_kernel<GW, true, true, false>},
+      {decode_kernel<GW, false, false, true>, decode_kernel<GW, true, false, true>,
+       decode_kernel<GW, true, true, true>}};
   const int variant = c.k_new == nullptr ? 0 : c.rope == nullptr ? 1 : 2;
-  const Kern kern = kKerns[polled ? 1 : 0][variant];
-  static bool attr_set[64][2][3] = {};
+  const int shape = (wide ? 2 : 0) + (polled ? 1 : 0);
+  const Kern kern = kKerns[shape][variant];
+  static bool attr_set[64][4][3] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
-  if (dev < 64 && !attr_set[dev][polled ? 1 : 0][variant]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(Geo::smem_bytes(kMaxDecodeBatch))) != cudaSuccess)
+  if (dev < 64 && !attr_set[dev][shape][variant]) {
+    const size_t max_smem = wide ? GeoW::smem_bytes(kMaxDecodeBatch) : Geo::smem_bytes(kMaxDecodeBatch);
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(max_smem)) !=
+        cudaSuccess)
       return PKV_ERR_CUDA;
-    attr_set[dev][polled ? 1 : 0][variant] = true;
+    attr_set[dev][shape][variant] = true;
   }
   int occ = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kDecThreads, smem) != cudaSuccess)
     return PKV_ERR_CUDA;
   if (occ < 1) return PKV_ERR_UNSUPPORTED;
-  if (occ > kDecCtasPerSm) occ = kDecCtasPerSm;
+  const int occ_cap = wide ? GeoW::kCtasPerSm : Geo::kCtasPerSm;
+  if (occ > occ_cap) occ = occ_cap;
 
   unsigned char* ws = static_cast<unsigned char*>(c.workspace);
   DecodeArgs a;

@@ -7,9 +7,11 @@ The model of one CTA of the persistent decode kernel (4 consumer warps, a
 3-stage ring each, 32-lane producer warp):
 - the CTA's share [lo, hi) of the flattened (request, KV head, page) list over
   G = min(grid, max(1, T // 8)) CTAs: shares equal in cost, a page costing 1 and
-  each (request, KV head) that starts inside a share LAM pages more (LAM = 32
-  for batches, the polled merge; 0 for few long requests, the counted merge);
-  with LAM = 0, lo(c) = c * T // G;
+  each (request, KV head) that starts inside a share LAM pages more when the
+  kernel takes the polled merge (LAM = 32), none with the counted merge; with
+  few (request, KV head) pairs and a long block table the kernel runs half the
+  grid (one CTA per SM), and the model follows it; with LAM = 0,
+  lo(c) = c * T // G;
 - the share is cut into pieces at (request, KV head) boundaries; the consumers
   meet at the end of every piece (a CTA barrier) before any starts the next;
 - page f goes to consumer assign(f); each consumer takes its pages in order,
@@ -83,13 +85,24 @@ class ShareMap:
         return ((self.cost(f) + 1) * self.n + self.Ctot - 1) // self.Ctot - 1
 
 
-def kernel_lam(seq_lens, grid):
-    """The piece cost the kernel uses for this step (the polled merge prices boundaries)."""
-    return LAM if grid <= POLL_MAX * len(seq_lens) * HKV else 0
+WIDE_MIN_PAGES = 8192  # the kernel's bound for the wide launch shape (one CTA per SM)
+
+
+def kernel_launch(seq_lens, grid):
+    """(grid, piece cost) the kernel uses for this step: few (request, KV head) pairs and a table that can
+    hold a long step take the wide shape (half the grid); the polled merge prices boundaries."""
+    pairs = len(seq_lens) * HKV
+    max_pages = max(1, max((int(s) + PAGE - 1) // PAGE for s in seq_lens))
+    if grid > POLL_MAX * pairs and pairs * max_pages >= WIDE_MIN_PAGES:  # (head_dim 128, as modelled here)
+        grid //= 2
+    return grid, (LAM if grid <= POLL_MAX * pairs else 0)
 
 
 def shares(seq_lens, grid, lam=None):
-    sm = ShareMap(seq_lens, grid, kernel_lam(seq_lens, grid) if lam is None else lam)
+    g, klam = kernel_launch(seq_lens, grid)
+    if lam is not None:  # a fixed share rule (the deadlock regression keeps the one of its time)
+        g, klam = grid, lam
+    sm = ShareMap(seq_lens, g, klam)
     pages, pref = sm.pages, sm.pref
     seg_starts = sorted({int(pref[b]) + h * pages[b] for b in range(len(pages)) if pages[b] for h in range(HKV)})
     return [(sm.lo(c), sm.lo(c + 1)) for c in range(sm.n)], seg_starts
