@@ -259,18 +259,25 @@ struct Shares {
   long long T, Ctot;
   long long q;  // Ctot / n
   int r;        // Ctot mod n
+  // T_ and pairs_: pref[batch] and pcp[batch]
   __device__ __forceinline__ void init(const int* pref_, const int* pcp_, const int* sl_, int batch_, int hkv_,
-                                       int n_) {
+                                       int n_, long long T_, int pairs_) {
     pref = pref_;
     pcp = pcp_;
     sl = sl_;
     batch = batch_;
     hkv = hkv_;
     n = n_;
-    T = pref[batch];
-    Ctot = T + static_cast<long long>(lam) * (pcp[batch] > 0 ? pcp[batch] - 1 : 0);
-    q = Ctot / n;
-    r = static_cast<int>(Ctot - q * n);
+    T = T_;
+    Ctot = T + static_cast<long long>(lam) * (pairs_ > 0 ? pairs_ - 1 : 0);
+    if (Ctot < (1LL << 32)) {  // (the usual case: a 32-bit division)
+      const unsigned c32 = static_cast<unsigned>(Ctot);
+      q = c32 / static_cast<unsigned>(n);
+      r = static_cast<int>(c32 - static_cast<unsigned>(q) * static_cast<unsigned>(n));
+    } else {
+      q = Ctot / n;
+      r = static_cast<int>(Ctot - q * n);
+    }
   }
   // floor(c Ctot / n) without a 64-bit division (c r < 2^22)
   __device__ __forceinline__ long long y_of(int c) const {
@@ -290,6 +297,10 @@ struct Shares {
       const int mid = (lb + hb + 1) >> 1;
       if (pref[mid] + static_cast<long long>(lam) * pcp[mid] <= y) lb = mid; else hb = mid - 1;
     }
+    return lo_in(lb, y);
+  }
+  // the same, given lb: the last request whose first pair costs at most y
+  __device__ __forceinline__ long long lo_in(int lb, long long y) const {
     const int np = pages_of(sl[lb]);
     if (np == 0) return pref[lb];
     const long long key = pref[lb] + static_cast<long long>(lam) * pcp[lb];
@@ -483,15 +494,30 @@ __global__ void __launch_bounds__(kDecThreads, Geo::kCtasPerSm) decode_kernel(co
       pref[batch] = carry;
       pcp[batch] = pcarry;
     }
-    // this CTA's share bounds, once: lanes 0 and 1 work out lo(c) and lo(c + 1) side by side
+    // This CTA's share bounds, once, by this warp: the request holding each bound is the
+    // last one whose first pair costs no more than the bound's cost, counted with ballots
+    // over the requests (their costs are non-decreasing); lanes 0 and 1 then place lo(c)
+    // and lo(c + 1) inside their requests.
     __syncwarp();
     const long long Tw = carry;
     const long long gw = Tw / kMinShare > 0 ? Tw / kMinShare : 1;
     const int nw = static_cast<int>(gw < gridDim.x ? gw : gridDim.x);
-    if (lane < 2 && static_cast<int>(blockIdx.x) < nw) {
+    if (static_cast<int>(blockIdx.x) < nw) {
       Shares<kPolled ? PKV_DEC_PIECE_COST : 0> sw;
-      sw.init(pref, pcp, sl, batch, hkv, nw);
-      flag[4 + lane] = static_cast<int>(sw.lo(blockIdx.x + lane));
+      sw.init(pref, pcp, sl, batch, hkv, nw, Tw, pcarry);
+      const long long y0 = sw.y_of(blockIdx.x), y1 = sw.y_of(blockIdx.x + 1);
+      if (sw.lam == 0) {
+        if (lane < 2) flag[4 + lane] = static_cast<int>(lane ? y1 : y0);
+      } else {
+        int n0 = 0, n1 = 0;
+        for (int base = 0; base < batch; base += 32) {
+          const int b = base + lane;
+          const long long key = b < batch ? pref[b] + static_cast<long long>(sw.lam) * pcp[b] : (1LL << 62);
+          n0 += __popc(__ballot_sync(kFull, key <= y0));
+          n1 += __popc(__ballot_sync(kFull, key <= y1));
+        }
+        if (lane < 2) flag[4 + lane] = static_cast<int>(sw.lo_in((lane ? n1 : n0) - 1, lane ? y1 : y0));
+      }
     }
   }
   fence_barrier_init();
@@ -704,7 +730,7 @@ __global__ void __launch_bounds__(kDecThreads, Geo::kCtasPerSm) decode_kernel(co
   // record of CTA c is in slot 2c, or 2c + 1 when it is the second split piece
   // of c's share (first_has_two: the first holder's share starts before (b, h)).
   Shares<kPolled ? PKV_DEC_PIECE_COST : 0> sh;
-  sh.init(pref, pcp, sl, batch, hkv, nsh);
+  sh.init(pref, pcp, sl, batch, hkv, nsh, T, pcp[batch]);
   auto span_of = [&](int b, int h, int& cfirst, int& n, bool& first_has_two) {
     const int np = pages_of(sl[b]);
     const long long fseg = pref[b] + static_cast<long long>(h) * np;
