@@ -607,20 +607,69 @@ __global__ void __launch_bounds__(kDecThreads, Geo::kCtasPerSm) decode_kernel(co
       int rounds = valid ? my_round + 1 : 0;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) rounds = max(rounds, __shfl_xor_sync(kFull, rounds, o));
-      // New rows come from the predecessor. With the rotary embedding the whole warp writes them
-      // before the chunk's copies, so it waits first; otherwise only the lane whose page takes a
-      // new row waits, right before it writes the row, and the chunk's other pages go out at once.
-      if (kRope && !waited && __any_sync(kFull, wslot >= 0)) {
-        grid_dependency_wait();
-        allow_dependents();
-        waited = true;
-      }
-      if (kRope) {
-        // Fused append with the rotary embedding, by the whole warp: every page of this
-        // chunk that holds its request's new token gets the token's rotated K row and its V
-        // row for that head before any lane copies a page. Lanes take key pairs (i, i + D/2),
-        // i = lane (+ 32 at D = 128), rotated in fp32 as y1 = fma(x1, c, -(x2 s)),
-        // y2 = fma(x2, c, x1 s) with each product rounded first, then rounded to bf16.
+      // The chunk's copies, in rounds; only the lanes in [from, to) take part.
+      auto issue_rounds = [&](int from, int to) {
+        for (int r = 0; r < rounds; ++r) {
+          if (valid && my_round == r && !pfail && lane >= from && lane < to) {
+            if (use > 0 && !mbar_wait_bounded(&empty[slot], static_cast<uint32_t>(use - 1) & 1u)) {
+              set_status(a.status, PKV_ERR_DEVICE_TIMEOUT);
+              pfail = true;
+            } else {
+              const bool id_ok = id >= 0 && id < a.num_pages;
+              if (!id_ok) set_status(a.status, PKV_ERR_OUT_OF_BOUNDS);
+              const int pid = id_ok ? id : 0;
+              if (kFused && !kRope && wslot >= 0 && id_ok) {
+                grid_dependency_wait();  // (returns at once after the first time)
+                // fused append: this page holds the request's new token; write its K and V rows
+                // for this head, then order the writes before this lane's tensor copy of the page
+                const uint4* ks =
+                    reinterpret_cast<const uint4*>(a.k_new + (static_cast<size_t>(bb) * hkv + hh) * D);
+                const uint4* vs =
+                    reinterpret_cast<const uint4*>(a.v_new + (static_cast<size_t>(bb) * hkv + hh) * D);
+                const size_t row = ((static_cast<size_t>(pid) * hkv + hh) * kPageSize + wslot) * D;
+                uint4* kd = reinterpret_cast<uint4*>(const_cast<__nv_bfloat16*>(a.k_pages) + row);
+                uint4* vd = reinterpret_cast<uint4*>(const_cast<__nv_bfloat16*>(a.v_pages) + row);
+#pragma unroll
+                for (int q4 = 0; q4 < Geo::kRowB / 16; ++q4) {
+                  kd[q4] = __ldg(ks + q4);
+                  vd[q4] = __ldg(vs + q4);
+                }
+                fence_proxy_async_global();
+              }
+              const int z = pid * hkv + hh;  // tile of the pool
+              unsigned char* dst = ring + slot * Geo::kStage;
+              mbar_arrive_expect_tx(&full[slot], Geo::kStage);
+              // one copy per tile: its D / 64 16-row x 64-dim halves, 128-byte swizzled
+              tma_load_4d_hint(dst, &kmap, 0, 0, 0, z, &full[slot], policy);
+              tma_load_4d_hint(dst + Geo::kTile, &vmap, 0, 0, 0, z, &full[slot], policy);
+            }
+          }
+          __syncwarp();
+        }
+      };
+      // New rows come from the predecessor. Without the rotary embedding only the lane whose
+      // page takes a new row waits for it, right before it writes the row (above), and the
+      // chunk's other pages go out at once.
+      if (!kRope) {
+        issue_rounds(0, 32);
+      } else {
+        // With it the whole warp writes the rows: every page of this chunk that holds its
+        // request's new token gets the token's rotated K row and its V row for that head
+        // before any lane copies that page. In early mode the pages before the chunk's first
+        // such page are copied first; the rest wait for the predecessor. (Pages go out in
+        // share order either way, so a page's stage was issued before it: no round waits on a
+        // page it holds back.) Lanes take key pairs (i, i + D/2), i = lane (+ 32 at D = 128),
+        // rotated in fp32 as y1 = fma(x1, c, -(x2 s)), y2 = fma(x2, c, x1 s) with each product
+        // rounded first, then rounded to bf16.
+        const unsigned nmask = __ballot_sync(kFull, valid && wslot >= 0);
+        int from = 0;  // lanes already issued
+        if (!waited && nmask != 0u) {
+          from = __ffs(nmask) - 1;
+          issue_rounds(0, from);
+          grid_dependency_wait();
+          allow_dependents();
+          waited = true;
+        }
         unsigned amask = __ballot_sync(kFull, valid && wslot >= 0 && id >= 0 && id < a.num_pages);
         if (amask != 0u) {
           while (amask != 0u) {
@@ -653,41 +702,7 @@ __global__ void __launch_bounds__(kDecThreads, Geo::kCtasPerSm) decode_kernel(co
           fence_proxy_async_global();  // this lane's row stores before the warp's tensor copies
           __syncwarp();
         }
-      }
-      for (int r = 0; r < rounds; ++r) {
-        if (valid && my_round == r && !pfail) {
-          if (use > 0 && !mbar_wait_bounded(&empty[slot], static_cast<uint32_t>(use - 1) & 1u)) {
-            set_status(a.status, PKV_ERR_DEVICE_TIMEOUT);
-            pfail = true;
-          } else {
-            const bool id_ok = id >= 0 && id < a.num_pages;
-            if (!id_ok) set_status(a.status, PKV_ERR_OUT_OF_BOUNDS);
-            const int pid = id_ok ? id : 0;
-            if (kFused && !kRope && wslot >= 0 && id_ok) {
-              grid_dependency_wait();  // (returns at once after the first time)
-              // fused append: this page holds the request's new token; write its K and V rows
-              // for this head, then order the writes before this lane's tensor copy of the page
-              const uint4* ks = reinterpret_cast<const uint4*>(a.k_new + (static_cast<size_t>(bb) * hkv + hh) * D);
-              const uint4* vs = reinterpret_cast<const uint4*>(a.v_new + (static_cast<size_t>(bb) * hkv + hh) * D);
-              const size_t row = ((static_cast<size_t>(pid) * hkv + hh) * kPageSize + wslot) * D;
-              uint4* kd = reinterpret_cast<uint4*>(const_cast<__nv_bfloat16*>(a.k_pages) + row);
-              uint4* vd = reinterpret_cast<uint4*>(const_cast<__nv_bfloat16*>(a.v_pages) + row);
-#pragma unroll
-              for (int q4 = 0; q4 < Geo::kRowB / 16; ++q4) {
-                kd[q4] = __ldg(ks + q4);
-                vd[q4] = __ldg(vs + q4);
-              }
-              fence_proxy_async_global();
-            }
-            const int z = pid * hkv + hh;  // tile of the pool
-            unsigned char* dst = ring + slot * Geo::kStage;
-            mbar_arrive_expect_tx(&full[slot], Geo::kStage);
-            // one copy per tile: its D / 64 16-row x 64-dim halves, 128-byte swizzled
-            tma_load_4d_hint(dst, &kmap, 0, 0, 0, z, &full[slot], policy);
-            tma_load_4d_hint(dst + Geo::kTile, &vmap, 0, 0, 0, z, &full[slot], policy);
-          }
-        }
-        __syncwarp();
+        issue_rounds(from, 32);
       }
       pfail = __any_sync(kFull, pfail);
     }
