@@ -41,16 +41,18 @@
 //    the fp32 scores), p rounded to bf16 for the value product O^T += V^T P^T.
 //    Tokens past seq_len in the last page are masked in the scores and in the
 //    value operand's registers, so unused slots may hold anything, NaN included.
-//  * Optional fused append: the producer lane that copies a request's last
-//    page first writes the request's new K/V row for that head into it
-//    (generic stores, then a proxy fence so its own tensor copy sees them); in
-//    early mode that lane alone waits for the predecessor first, so the other
-//    pages of its chunk are copied before the dependency resolves. With
+//  * Optional fused append: the consumer warp that takes a request's last page
+//    loads the request's new K/V row for that head (with that page's block-table
+//    entry) when its piece starts, and once the page is staged writes the row
+//    over the slot's copied bytes (swizzled, then a proxy fence before the
+//    stage's next tensor copy) and into the pool. The producer copies the page
+//    like any other, so in early mode it never waits for the predecessor. With
 //    a cos/sin table the whole producer warp writes the row instead, rotating
 //    the key (rotary position embedding at the new token's position, pairs
-//    (i, i + head_dim / 2), fp32, rounded to bf16), and each piece's query rows
-//    are rotated the same way after they are staged (then rounded to bf16 as
-//    the MMA operand).
+//    (i, i + head_dim / 2), fp32, rounded to bf16); in early mode the chunk's
+//    pages before its first new-row page are copied before the warp waits.
+//    Each piece's query rows are rotated the same way after they are staged
+//    (then rounded to bf16 as the MMA operand).
 //  * The query rows of the next piece are copied into shared memory (cp.async)
 //    while the current piece streams, so a piece boundary costs no round trip.
 //  * At the end of a piece the warps merge through shared memory (at most four
@@ -121,7 +123,7 @@ constexpr int kPollMax = 24;                 // polled merge up to this many hol
 // merge) runs the wide launch shape when the block table can hold at least this
 // many (request, KV head, page) triples (batch x max_pages x KV heads); with half
 // the CTAs, a pair then has few enough holders for the polled merge. One 40k-token
-// request measured 29.6 -> 28.1 us per layer, 16k 14.6 -> 13.5, but 4k 7.3 -> 7.9
+// request measured 29.25 -> 28.27 us per layer, 16k 14.49 -> 13.57, but 4k 7.30 -> 7.92
 // (half the CTAs for a small step), hence the bound.
 constexpr long long kWideMinPages = 8192;
 
@@ -590,7 +592,7 @@ __global__ void __launch_bounds__(kDecThreads, Geo::kCtasPerSm) decode_kernel(co
         c = static_cast<int>((f - lo) % kCons);
         bb = b;
         id = __ldg(a.block_table + static_cast<size_t>(b) * a.max_pages + p);
-        if (kFused && p == np - 1) wslot = (sl[b] - 1) % kPageSize;  // the new token's slot
+        if (kRope && p == np - 1) wslot = (sl[b] - 1) % kPageSize;  // the new token's slot (rotated append)
       }
       const unsigned same = __match_any_sync(kFull, valid ? c : -1);
       const int idx = __popc(same & lt_mask);  // earlier lanes of this chunk feeding the same consumer
@@ -618,24 +620,6 @@ __global__ void __launch_bounds__(kDecThreads, Geo::kCtasPerSm) decode_kernel(co
               const bool id_ok = id >= 0 && id < a.num_pages;
               if (!id_ok) set_status(a.status, PKV_ERR_OUT_OF_BOUNDS);
               const int pid = id_ok ? id : 0;
-              if (kFused && !kRope && wslot >= 0 && id_ok) {
-                grid_dependency_wait();  // (returns at once after the first time)
-                // fused append: this page holds the request's new token; write its K and V rows
-                // for this head, then order the writes before this lane's tensor copy of the page
-                const uint4* ks =
-                    reinterpret_cast<const uint4*>(a.k_new + (static_cast<size_t>(bb) * hkv + hh) * D);
-                const uint4* vs =
-                    reinterpret_cast<const uint4*>(a.v_new + (static_cast<size_t>(bb) * hkv + hh) * D);
-                const size_t row = ((static_cast<size_t>(pid) * hkv + hh) * kPageSize + wslot) * D;
-                uint4* kd = reinterpret_cast<uint4*>(const_cast<__nv_bfloat16*>(a.k_pages) + row);
-                uint4* vd = reinterpret_cast<uint4*>(const_cast<__nv_bfloat16*>(a.v_pages) + row);
-#pragma unroll
-                for (int q4 = 0; q4 < Geo::kRowB / 16; ++q4) {
-                  kd[q4] = __ldg(ks + q4);
-                  vd[q4] = __ldg(vs + q4);
-                }
-                fence_proxy_async_global();
-              }
               const int z = pid * hkv + hh;  // tile of the pool
               unsigned char* dst = ring + slot * Geo::kStage;
               mbar_arrive_expect_tx(&full[slot], Geo::kStage);
@@ -647,9 +631,9 @@ __global__ void __launch_bounds__(kDecThreads, Geo::kCtasPerSm) decode_kernel(co
           __syncwarp();
         }
       };
-      // New rows come from the predecessor. Without the rotary embedding only the lane whose
-      // page takes a new row waits for it, right before it writes the row (above), and the
-      // chunk's other pages go out at once.
+      // New rows come from the predecessor. Without the rotary embedding the consumer that takes
+      // a request's last page writes the new row into the staged page and into the pool, so
+      // every page goes out at once, whatever the slot of the new row holds now.
       if (!kRope) {
         issue_rounds(0, 32);
       } else {
@@ -837,7 +821,24 @@ __global__ void __launch_bounds__(kDecThreads, Geo::kCtasPerSm) decode_kernel(co
     float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
 
     const int w0 = static_cast<int>((pc.fstart - lo) % kCons);  // consumer of the piece's first page
-    for (int p = pc.p0 + (warp - w0 + kCons) % kCons; p < pc.p1; p += kCons) {
+    const int p_first = pc.p0 + (warp - w0 + kCons) % kCons;    // this warp's first page of the piece
+    // Fused append without the rotary embedding: the warp that takes the request's last page loads
+    // the new token's K and V rows for this head now (lane l: 16-byte chunk l of the K row, or of
+    // the V row from lane D / 8 on) with that page's block-table entry. Once the page is staged it
+    // writes them over the copied slot and into the pool.
+    const bool takes_new =
+        kFused && !kRope && pc.p1 == pc.np && p_first <= pc.np - 1 && (pc.np - 1 - p_first) % kCons == 0;
+    constexpr int kRowChunks = D / 8;
+    uint4 nrow = make_uint4(0u, 0u, 0u, 0u);
+    int nid = -1;
+    if (takes_new) {
+      if (lane < 2 * kRowChunks)
+        nrow = __ldg(reinterpret_cast<const uint4*>((lane < kRowChunks ? a.k_new : a.v_new) +
+                                                    (static_cast<size_t>(b) * hkv + h) * D) +
+                     lane % kRowChunks);
+      nid = __ldg(a.block_table + static_cast<size_t>(b) * a.max_pages + pc.np - 1);
+    }
+    for (int p = p_first; p < pc.p1; p += kCons) {
       const int slot = warp * kRing + k % kRing;
       const uint32_t parity = static_cast<uint32_t>(k / kRing) & 1u;
       if (!failed) {
@@ -852,6 +853,20 @@ __global__ void __launch_bounds__(kDecThreads, Geo::kCtasPerSm) decode_kernel(co
         const int rem = sl[b] - p * kPageSize;
         const int n_valid = rem < kPageSize ? rem : kPageSize;
         const uint32_t kt = smem_u32(ring + slot * Geo::kStage);
+        if (takes_new && p == pc.np - 1) {
+          const int t = (sl[b] - 1) % kPageSize;  // the new token's slot
+          if (lane < 2 * kRowChunks) {
+            const int c = lane % kRowChunks;
+            const int tile = lane < kRowChunks ? 0 : Geo::kTile;
+            *reinterpret_cast<uint4*>(ring + slot * Geo::kStage + tile + swz(t, c)) = nrow;
+            if (nid >= 0 && nid < a.num_pages) {  // (the producer reports a page id out of the pool)
+              __nv_bfloat16* pool = const_cast<__nv_bfloat16*>(lane < kRowChunks ? a.k_pages : a.v_pages);
+              reinterpret_cast<uint4*>(pool + ((static_cast<size_t>(nid) * hkv + h) * kPageSize + t) * D)[c] = nrow;
+            }
+          }
+          fence_proxy_async_smem();  // the row stores before the stage's next tensor copy
+          __syncwarp();
+        }
         mma_page<kKS>(kt, kt + Geo::kTile, koff, voff, qf, n_valid, a.qscale, o, m0, m1, l0, l1);
       }
       __syncwarp();  // the stage and the p buffer are free again

@@ -274,17 +274,26 @@ def test_fused_equals_separate_calls_bitwise(cuda_device):
     assert torch.equal(sep.k_pages.view(torch.int16), fused.k_pages.view(torch.int16))
 
 
-@pytest.mark.parametrize("early", [False, True])
-def test_fused_layer_chain_in_a_graph(cuda_device, early):
+@pytest.mark.parametrize("early,rope,cfg", [(False, False, "bs16"), (True, False, "bs16"), (True, True, "bs16"),
+                                             (True, True, "40k")])
+def test_fused_layer_chain_in_a_graph(cuda_device, early, rope, cfg):
     # two layers, each its own pool, replayed from a CUDA graph; with early prefetch each
-    # layer's kernel may start reading its pool while the previous layer's kernel finishes
-    case = W.decode_case(19, W.config_seq_lens(2), layers=2, pending_append=True, poison=True)
+    # layer's kernel may start reading its pool while the previous layer's kernel finishes (with the
+    # rotary embedding, the pages before a chunk's first new row before the predecessor completes)
+    lens = {"bs16": W.config_seq_lens(2), "40k": W.config_seq_lens(3)}[cfg]
+    case = W.decode_case(19, lens, layers=2, pending_append=True, poison=True)
     runs = [DecodeOnDevice(case, layer, cuda_device) for layer in range(2)]
+    cs = oracle.rope_cache(ROPE_THETA, case.geom.head_dim, int(max(lens)) + 1) if rope else None
+    cs_dev = torch.from_numpy(cs).to(cuda_device) if rope else None
 
     def step():
         for r in runs:
-            pkv.decode_append_attn(r.q, r.k_new, r.v_new, r.k_pages, r.v_pages, r.block_table, r.seq_lens, r.out,
-                                   case.geom.scale, r.ws, early_prefetch=early)
+            if rope:
+                pkv.decode_append_rope_attn(r.q, r.k_new, r.v_new, r.k_pages, r.v_pages, r.block_table, r.seq_lens,
+                                            cs_dev, r.out, case.geom.scale, r.ws, early_prefetch=early)
+            else:
+                pkv.decode_append_attn(r.q, r.k_new, r.v_new, r.k_pages, r.v_pages, r.block_table, r.seq_lens,
+                                       r.out, case.geom.scale, r.ws, early_prefetch=early)
 
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
@@ -298,12 +307,15 @@ def test_fused_layer_chain_in_a_graph(cuda_device, early):
         r.out.zero_()
     g.replay()
     torch.cuda.synchronize()
+    pos = np.asarray(case.seq_lens, dtype=np.int64) - 1
     for layer, r in enumerate(runs):
-        want_k, want_v = oracle.append(case.k_new[layer], case.v_new[layer], case.slot_mapping,
-                                       case.k_pages[layer], case.v_pages[layer])
+        k_new = oracle.rope_bf16(case.k_new[layer], pos, cs) if rope else case.k_new[layer]
+        want_k, want_v = oracle.append(k_new, case.v_new[layer], case.slot_mapping, case.k_pages[layer],
+                                       case.v_pages[layer])
         assert np.array_equal(bits(r.k_pages), want_k) and np.array_equal(bits(r.v_pages), want_v)
-        want = oracle.decode(case.q[layer], want_k, want_v, case.block_table, case.seq_lens, case.geom.scale)
-        assert_close(bf16_to_f64(r.out), want, f"graph layer {layer} early={early}")
+        q = oracle.rope_f64(case.q[layer], pos, cs) if rope else case.q[layer]
+        want = oracle.decode(q, want_k, want_v, case.block_table, case.seq_lens, case.geom.scale)
+        assert_close(bf16_to_f64(r.out), want, f"graph layer {layer} early={early} rope={rope} {cfg}")
         assert r.ws.status() == 0
 
 
