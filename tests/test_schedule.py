@@ -293,3 +293,47 @@ def test_piece_cost_moves_pages_from_ctas_with_boundaries():
         lo, hi = sm.lo(c), sm.lo(c + 1)
         (two if any(lo < x < hi for x in starts) else one).append(hi - lo)
     assert one and two and np.mean(two) + LAM // 2 < np.mean(one)
+
+
+def new_row_takers(seq_lens, grid):
+    """For the fused append: (CTA, consumer warp) pairs that write each (request, KV head)'s new row,
+    by the consumer's rule (the warp whose page walk p_first, p_first + 4, ... of a piece that ends at
+    the pair's last page reaches that page), and the consumer the producer feeds that page to."""
+    bounds, _ = shares(seq_lens, grid)
+    pages = [(int(s) + PAGE - 1) // PAGE for s in seq_lens]
+    pref = np.concatenate([[0], np.cumsum(np.asarray(pages, dtype=np.int64) * HKV)])
+    takers, fed = {}, {}
+    for c, (lo, hi) in enumerate(bounds):
+        f = lo
+        while f < hi:  # the pieces of the share, as the consumers walk them
+            b = int(np.searchsorted(pref, f, side="right") - 1)
+            np_ = pages[b]
+            h = (f - int(pref[b])) // np_
+            seg = int(pref[b]) + h * np_
+            fend = min(hi, seg + np_)
+            p0, p1 = f - seg, fend - seg
+            w0 = (f - lo) % CONS
+            for w in range(CONS):
+                p_first = p0 + (w - w0 + CONS) % CONS
+                if p1 == np_ and p_first <= np_ - 1 and (np_ - 1 - p_first) % CONS == 0:
+                    assert np_ - 1 in range(p_first, p1, CONS)  # the warp's walk visits the page
+                    takers.setdefault((b, h), []).append((c, w))
+            if p1 == np_:
+                fed[(b, h)] = (c, (seg + np_ - 1 - lo) % CONS)
+            f = fend
+    return takers, fed, pages
+
+
+@pytest.mark.parametrize("grid", [304, 152, 8])
+def test_each_new_row_has_one_writer_the_consumer_fed_its_page(grid):
+    # the consumer-side fused append: exactly one warp of one CTA writes each (request, KV head)'s new
+    # row, and it is the consumer the producer hands that page to ((f - lo) mod 4)
+    rng = np.random.default_rng(17 + grid)
+    mixes = [W.config_seq_lens(2), [40000], [4096], [1] * 64, [0, 16, 17, 0, 33, 1]]
+    mixes += [list(rng.integers(0, 3000, size=int(rng.integers(1, 40)))) for _ in range(60)]
+    for lens in mixes:
+        takers, fed, pages = new_row_takers(lens, grid)
+        want = {(b, h) for b, n in enumerate(pages) if n > 0 for h in range(HKV)}
+        assert set(takers) == want and set(fed) == want, lens
+        for key in want:
+            assert takers[key] == [fed[key]], (lens, key, takers[key], fed[key])
