@@ -50,7 +50,7 @@ WORKLOAD = ("qwen3-0.6b decode step: 28 layers x bs16, 16q/8kv heads, d128, page
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the decode kernel source it was
 # measured on (sha256 prefix of csrc/decode_kernel.cuh followed by csrc/pkv_mma.cuh); any other source
 # reports null.
-NCU_DECODE_TRAFFIC = {"d3deb3172c17ca1b": 107_555_840 + 3_419_136}
+NCU_DECODE_TRAFFIC = {"f60bafc4eddad24d": 107_560_448 + 3_036_928}
 
 
 def _decode_traffic():

@@ -101,7 +101,7 @@ namespace pkv {
 #define PKV_DEC_CTAS_PER_SM 2
 #endif
 #ifndef PKV_DEC_ROUND_PAGES  // pages the producer issues per round
-#define PKV_DEC_ROUND_PAGES 8
+#define PKV_DEC_ROUND_PAGES 4
 #endif
 #ifndef PKV_DEC_PIECE_COST  // pages a (request, KV head) boundary inside a share counts for (polled merge)
 #define PKV_DEC_PIECE_COST 32

@@ -17,7 +17,7 @@ The model of one CTA of the persistent decode kernel (4 consumer warps, a
 - page f goes to consumer assign(f); each consumer takes its pages in order,
   page k of consumer c in stage k % 3;
 - the producer walks the share 32 pages at a time; a page's round is its
-  position in the chunk divided by the round size R (8 pages; the earlier
+  position in the chunk divided by the round size R (4 pages; the earlier
   rule, a page's index among the chunk's pages of its consumer divided by 3,
   equals R = 12). A page is issued
   once its stage's previous use has been consumed, and a round ends when all
@@ -29,7 +29,7 @@ import pytest
 from paged_kv_decode_gb300 import workloads as W
 
 CONS, RING, CHUNK, PAGE, HKV = 4, 3, 32, 16, 8
-ROUND_SIZES = (1, 4, 8, 12)  # the shipped round size (8), the earlier one (12) and others measured
+ROUND_SIZES = (1, 4, 8, 12)  # the shipped round size (4), earlier ones (8, 12) and another measured
 LAM = 32  # the kernel's piece cost for batches (polled merge)
 POLL_MAX = 24  # the kernel takes the polled merge when grid <= POLL_MAX * batch * KV heads
 
